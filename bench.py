@@ -1,0 +1,330 @@
+#!/usr/bin/env python3
+"""Benchmark of one routed MoE layer's forward pass on GB300.
+
+Workload (default): the decode layer of a Qwen3-35B-A3B-shaped model --
+d_model 2048, 128 experts, top-8, d_ff 768, MXFP4 weights, 47 cache slots
+(37% of the experts) filled from pinned host memory -- run at 1, 4 and 16
+tokens per step on AR(1) hidden states (rho 0.9).  A step is one moe_forward:
+router, permutation, LRU update, miss fills, expert FFN, combine.
+
+Timing: W warm-up steps, then K timed steps per batch size, each bracketed by
+CUDA events on the launching stream; the L2 is flushed (a 512 MiB write)
+between timed steps, outside the events.  `value` = tokens / summed step time
+over the three batch sizes, inputs resident in HBM.  `e2e` repeats the run
+through the C ABI with pinned host x / y buffers (copies inside the timed
+call, host wall clock).  The roofline entry is the expert FFN phase-1 kernel
+(gate/up GEMV), timed live with the library's per-launch events.
+
+--impl reference times the CPU oracle (FP64, numpy) on a bounded sample of the
+same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (decode, prefill); % of HBM BW / % of dense FP4 tensor peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workload
+
+def decode_tokens(wl, spec, seed, batch, steps):
+    x, _ = wl.ar1_tokens(seed, batch, steps, spec.d_model, 0.9)
+    return x
+
+
+def gateup_bytes(spec, layout, n_experts, n_tokens):
+    """Algorithmic bytes of phase 1 for one step: the gate and up codes and
+    scales of each expert read once, x read, h written (fp32)."""
+    d, f = spec.d_model, spec.d_ff
+    w = 2 * (f * d // 2 + f * d // spec.block)
+    rows = n_tokens * spec.k + (n_tokens if spec.has_shared else 0)
+    return n_experts * w + n_tokens * d * 2 + rows * f * 4
+
+
+def run_decode(args, batch, torch, capi, wl, build_layer, flush, st):
+    spec = wl.DECODE_35B.layer
+    seed = wl.DECODE_35B.seed
+    W, K = args.warmup, args.steps
+    x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
+    xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
+    L = build_layer(spec, seed, batch)
+    y = torch.empty(batch, spec.d_model, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(st):
+        for t in range(W):
+            L.forward(xs[t], y, stream=st)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    capi.moe_profile(L.h, True)
+    launches = misses = distinct = 0
+    fill = 0
+    ffn_bytes = 0
+    with torch.cuda.stream(st):
+        for t in range(K):
+            flush.zero_()
+            ev[t][0].record(st)
+            _, info = L.forward(xs[W + t], y, stream=st)
+            ev[t][1].record(st)
+            launches += info.n_launches
+            misses += info.n_misses
+            distinct += info.n_distinct
+            fill += info.fill_bytes
+            ffn_bytes += gateup_bytes(spec, L.layout, info.n_distinct, batch)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    prof = capi.moe_profile_read(L.h)
+    capi.moe_profile(L.h, False)
+    L.close()
+    return dict(batch=batch, steps=K, ms=ms, tokens=K * batch, launches=launches,
+                misses=misses, distinct=distinct, fill_bytes=fill, prof=prof,
+                gateup_bytes=ffn_bytes)
+
+
+def run_decode_e2e(args, batch, torch, capi, wl, build_layer, flush):
+    spec = wl.DECODE_35B.layer
+    seed = wl.DECODE_35B.seed
+    W, K = args.warmup, args.steps
+    x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
+    xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ys = torch.empty(W + K, batch, spec.d_model, dtype=torch.bfloat16).pin_memory()
+    L = build_layer(spec, seed, batch)
+    for t in range(W):
+        capi.moe_forward(L.h, xs[t], batch, ys[t], None, capi.MOE_REGIME_AUTO)
+    torch.cuda.synchronize()
+    total = 0.0
+    for t in range(K):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        capi.moe_forward(L.h, xs[W + t], batch, ys[W + t], None, capi.MOE_REGIME_AUTO)
+        total += time.perf_counter() - t0
+    L.close()
+    return dict(batch=batch, s=total, tokens=K * batch,
+                h2d=K * batch * spec.d_model * 2, d2h=K * batch * spec.d_model * 2)
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(budget_s: float):
+    """Time the oracle on the decode workload (batch 1, 4, 16 in turn) until
+    the budget is spent; returns (tokens/s, tokens, steps, seconds, cores)."""
+    from oracle import layer as olayer
+    from routed_expert_layer_gemv_gb300 import workloads as wl
+    spec = wl.DECODE_35B.layer
+    seed = wl.DECODE_35B.seed
+    W_r, b = wl.router_weights(spec, seed)
+    O = olayer.Layer(spec, lambda e: wl.expert_weights(spec, seed, e), W_r, b)
+    tokens = steps = 0
+    t0 = time.perf_counter()
+    per_batch = budget_s / 3.0
+    for batch in (1, 4, 16):
+        xb = decode_tokens(wl, spec, seed + batch, batch, 8)
+        tb = time.perf_counter()
+        t = 0
+        while time.perf_counter() - tb < per_batch and t < len(xb):
+            O.forward(wl.bf16_bits_to_f64(xb[t]), "decode")
+            tokens += batch
+            steps += 1
+            t += 1
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return tokens / el, tokens, steps, el, cores
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batches", default="1,4,16")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    ws, rank, local = _dist()
+    batches = [int(b) for b in args.batches.split(",")]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        v, tok, steps, el, cores = cpu_oracle_sample(args.cpu_budget)
+        cfg = {"workload": "decode_35b_a3b_d2048_e128_top8_f768_mxfp4_s47", "batches": batches}
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+                "n_gpus": 0, "steps": steps, "warmup": 0, "ms_per_step": 1000.0 * el / max(1, steps),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": "%d decode steps (%d tokens) of batches 1/4/16, %.1f s" % (steps, tok, el)},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    from routed_expert_layer_gemv_gb300 import capi
+    from routed_expert_layer_gemv_gb300 import workloads as wl
+    from routed_expert_layer_gemv_gb300.layer import build_layer
+    capi.lib()
+
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    runs = [run_decode(args, b, torch, capi, wl, build_layer, flush, st) for b in batches]
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    e2e_runs = [run_decode_e2e(args, b, torch, capi, wl, build_layer, flush) for b in batches]
+
+    ms = sum(r["ms"] for r in runs)
+    tokens = sum(r["tokens"] for r in runs)
+    e2e_s = sum(r["s"] for r in e2e_runs)
+    if ws > 1:
+        t = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_s = float(t[0]), float(t[1])
+    if rank != 0:
+        torch.distributed.barrier() if ws > 1 else None
+        return
+    value = ws * tokens / (ms / 1000.0)
+    e2e_value = ws * tokens / e2e_s
+
+    peak, peak_kind = _peaks()
+    g_ms = sum(r["prof"]["gateup"][0] for r in runs)
+    g_n = sum(r["prof"]["gateup"][1] for r in runs)
+    g_bytes = sum(r["gateup_bytes"] for r in runs)
+    achieved = (g_bytes / max(g_n, 1)) / ((g_ms / max(g_n, 1)) / 1000.0) / 1e9 if g_ms > 0 else None
+    roof = {"bound": "hbm", "kernel": "gemv_gateup (expert FFN phase 1)", "achieved": achieved,
+            "peak": peak, "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+            "traffic": None, "peak_kind": peak_kind,
+            "bytes_per_launch": g_bytes / max(g_n, 1), "ms_per_launch": g_ms / max(g_n, 1)}
+
+    per_batch = {}
+    for r, e in zip(runs, e2e_runs):
+        p = r["prof"]
+        per_batch[str(r["batch"])] = {
+            "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
+            "e2e_tokens_per_s": e["tokens"] / e["s"],
+            "ms_per_step": r["ms"] / r["steps"],
+            "miss_rate": r["misses"] / max(1, r["distinct"]),
+            "fill_GB_per_s": r["fill_bytes"] / max(1e-9, p["fill"][0] / 1000.0) / 1e9 if p["fill"][0] else None,
+            "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
+        }
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, tok, steps, el, cores = cpu_oracle_sample(args.cpu_budget)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": "%d decode steps (%d tokens) of batches 1/4/16, %.1f s" % (steps, tok, el)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps * len(batches), "warmup": args.warmup,
+        "ms_per_step": ms / (args.steps * len(batches)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)xbf16->f32",
+        "data": "synthetic (seeded AR(1) hidden states, random FP4 weights)",
+        "config": {"workload": "decode_35b_a3b_d2048_e128_top8_f768_mxfp4_s47",
+                   "batches": batches, "l2": "flushed (512 MiB write) between timed steps",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "per_batch": per_batch},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": sum(e["h2d"] for e in e2e_runs) / (args.steps * len(batches)),
+                "d2h_bytes_per_step": sum(e["d2h"] for e in e2e_runs) / (args.steps * len(batches))},
+        "gpu_launches": sum(r["launches"] for r in runs),
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,217 @@
+/*
+ * moe.h -- C ABI of one routed mixture-of-experts layer forward pass on a
+ * single NVIDIA GB300 GPU (sm_103a).
+ *
+ * What the layer is.  FreeToken ("FreeToken：把 284B MoE 塞进游戏 PC",
+ * zhichai.net, §二 "Decode: q⋆ = m·B_P/B_H" and "LRU 为什么赢" paragraphs)
+ * serves MoE models whose routed experts live in a GPU-resident LRU expert
+ * cache; experts that miss are loaded into it from host memory.  Its formats
+ * are MXFP4 and NVFP4 (same page §五; juejin.cn overview §五).  The pages give
+ * no formula for the layer; this library computes the standard one:
+ *
+ *   logits = x W_r^T (+ b);  top-k per token (ties -> lower expert id);
+ *   gates  = softmax over the k selected logits (or full-softmax probs);
+ *   y[t]   = sum_j gate[t,j] * FFN_{e_j}(x[t]) (+ FFN_shared(x[t]));
+ *   FFN(x) = W_d (SiLU(W_g x) * (W_u x)),  weights block-scaled FP4.
+ *
+ * Every call returns an int status: MOE_OK (0) or a negative MOE_ERR_*.
+ * Nothing throws across this boundary.  moe_last_error(layer) gives the text
+ * of the last failure on that layer, moe_status_string(code) a fixed text.
+ *
+ * Memory.  The library owns, and allocates with cudaMalloc at create time,
+ * the slot pool (n_slots experts), the shared-expert copy, the router weights,
+ * the slot table and all per-step workspaces.  The caller owns x, y, the
+ * host expert pool and the streams it passes.  Device pointers are CUDA
+ * device addresses on the layer's device (the device current at create).
+ * A layer is not thread-safe; calls on one layer must not overlap.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MOE_OK                 0
+#define MOE_ERR_ARG           -1  /* bad shape, index or pointer            */
+#define MOE_ERR_NOT_INSTALLED -2  /* a miss has no registered host source   */
+#define MOE_ERR_OOM           -3  /* cudaMalloc / pinned allocation failed  */
+#define MOE_ERR_FILL          -4  /* a host->slot copy could not be issued  */
+#define MOE_ERR_TIMEOUT       -5  /* a bounded device wait gave up          */
+#define MOE_ERR_CUDA          -6  /* a CUDA runtime call failed             */
+#define MOE_ERR_STATE         -7  /* call made in the wrong state           */
+#define MOE_ERR_UNSUPPORTED   -8  /* valid request this build cannot serve  */
+
+/* ---- weight formats ---------------------------------------------------- */
+#define MOE_MXFP4 0  /* E2M1 codes, one E8M0 scale per 32 along K            */
+#define MOE_NVFP4 1  /* E2M1 codes, one E4M3 scale per 16 along K, fp32/tensor */
+
+/* ---- regimes ----------------------------------------------------------- */
+#define MOE_REGIME_AUTO    0  /* decode for small N, prefill otherwise       */
+#define MOE_REGIME_DECODE  1  /* FP4 weights x bf16 activations, GEMV        */
+#define MOE_REGIME_PREFILL 2  /* FP4 weights x FP4 activations, grouped GEMM */
+
+typedef struct moe_layer* moe_layer_t;
+
+/* Layer descriptor.  E experts, top-k, d_model, d_ff, n_slots cache slots. */
+typedef struct {
+    int E;            /* routed experts, 1..1024                              */
+    int k;            /* experts per token, 1..min(E, 32)                     */
+    int d_model;      /* multiple of 128                                      */
+    int d_ff;         /* multiple of 128                                      */
+    int n_slots;      /* GPU expert-cache slots, 1..E                         */
+    int fmt;          /* MOE_MXFP4 or MOE_NVFP4                               */
+    int has_shared;   /* 1: one always-on shared expert, weight 1, resident   */
+    int norm_topk;    /* 1: gates renormalised over the k selected            */
+    int has_bias;     /* 1: per-expert router bias added to the logits        */
+    int max_tokens;   /* largest N of one moe_forward (sizes the workspaces)  */
+    float act_scale_x;/* NVFP4 prefill: static fp32 scale of x (power of 2)   */
+    float act_scale_h;/* NVFP4 prefill: static fp32 scale of h (power of 2)   */
+} moe_layer_desc;
+
+/* Byte layout of one expert (identical in the host pool and in a slot).
+ * Matrices are K-contiguous: gate [d_ff, d_model], up [d_ff, d_model],
+ * down [d_model, d_ff].  Codes: two E2M1 per byte, low nibble = even K.
+ * Scales: row-major [rows, K/32] E8M0 (MXFP4) or [rows, K/16] E4M3 (NVFP4).
+ * tensor_scales: three fp32 (gate, up, down; 1.0 for MXFP4).  All offsets
+ * are multiples of 256 bytes; `bytes` is the padded size of one expert. */
+typedef struct {
+    size_t bytes;
+    size_t gate_codes, up_codes, down_codes;
+    size_t gate_scales, up_scales, down_scales;
+    size_t tensor_scales;
+} moe_expert_layout;
+
+/* Filled by moe_forward when `info` is not NULL. */
+typedef struct {
+    int regime;        /* regime actually run                                 */
+    int n_tokens;
+    int n_distinct;    /* |U|: distinct routed experts this step              */
+    int n_hits;
+    int n_misses;
+    int n_waves;       /* ceil(|U| / n_slots)                                 */
+    size_t fill_bytes; /* bytes copied host -> slots this step                */
+    int host_synced;   /* 1 if the call waited for the routing on the host    */
+    int n_launches;    /* kernels this call launched                          */
+} moe_forward_info;
+
+/* Kernel classes of moe_profile_read. */
+#define MOE_PROF_ROUTER      0
+#define MOE_PROF_PERMUTE     1
+#define MOE_PROF_LRU         2
+#define MOE_PROF_GATEUP      3  /* expert FFN phase 1: W_g, W_u, SiLU * mul     */
+#define MOE_PROF_DOWN        4  /* expert FFN phase 2: W_d                      */
+#define MOE_PROF_COMBINE     5
+#define MOE_PROF_FILL        6  /* host -> slot copies on the fill stream       */
+#define MOE_PROF_PREFILL     7  /* prefill grouped GEMM (both phases)           */
+#define MOE_PROF_KINDS       8
+
+/* Layout of one expert for a descriptor (no GPU work). */
+int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out);
+
+/* Create a layer on the current device: validates the descriptor, allocates
+ * the slot pool, table and workspaces, creates the fill stream.  The cache
+ * starts empty (every slot free).  MOE_ERR_ARG on an invalid descriptor,
+ * MOE_ERR_OOM when device memory runs out (nothing is leaked). */
+int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out);
+int moe_layer_destroy(moe_layer_t layer);
+
+/* Router weights W_r fp32 [E, d_model] row-major and, when has_bias, the
+ * fp32 bias [E] (NULL otherwise).  Host or device pointers; copied
+ * synchronously. */
+int moe_set_router(moe_layer_t layer, const float* W_r, const float* bias);
+
+/* Register the caller's host expert pool: E experts back to back, expert e
+ * at byte offset e * layout.bytes.  Must be pinned (page-locked) host memory
+ * of at least E * layout.bytes bytes; it stays owned by the caller and must
+ * outlive the layer's use of it.  It is the source of every cache fill. */
+int moe_register_host_experts(moe_layer_t layer, const void* pool, size_t bytes);
+
+/* Copy the shared expert (layout.bytes, same layout; host or device pointer)
+ * into its resident buffer.  MOE_ERR_STATE if the layer has no shared one. */
+int moe_set_shared_expert(moe_layer_t layer, const void* weights);
+
+/* Install expert `expert` into slot `slot` from the host pool, as most
+ * recently used, ordered on `stream` (NULL = legacy default stream).  An
+ * expert previously in that slot is evicted; if `expert` was resident in
+ * another slot that slot becomes free.  MOE_ERR_NOT_INSTALLED if no host pool
+ * is registered.  (The expert cache of the zhichai.net page, §二.) */
+int moe_cache_install(moe_layer_t layer, int expert, int slot, void* stream);
+
+/* Apply one step's accesses to the device slot table, as moe_forward does:
+ * the distinct experts of experts[0..n) are accessed hits first (ascending
+ * id), then misses (ascending id); a miss takes the lowest free slot, else
+ * evicts the least recently used expert.  Misses are filled from the host
+ * pool when one is registered.  Outputs (host arrays, any may be NULL):
+ * slot_of_out[i] = slot that experts[i] was served from this step;
+ * miss_experts_out / miss_slots_out = the misses in access order (capacity
+ * n); *n_miss_out = their count.  Synchronous: returns after the table and
+ * fills are complete. */
+int moe_lru_touch(moe_layer_t layer, const int* experts, int n, int* slot_of_out,
+                  int* miss_experts_out, int* miss_slots_out, int* n_miss_out,
+                  void* stream);
+
+/* Read / replace the slot table (host arrays of n_slots entries; expert -1 =
+ * free slot; stamps are recency counters, larger = more recent; *clock is
+ * the last stamp issued).  set_state does not move weights: the caller
+ * must make each slot's contents match (e.g. with moe_cache_install). */
+int moe_lru_get_state(moe_layer_t layer, int* expert_of_slot, uint64_t* stamp,
+                      uint64_t* clock);
+int moe_lru_set_state(moe_layer_t layer, const int* expert_of_slot,
+                      const uint64_t* stamp, uint64_t clock);
+
+/* One forward pass: x bf16 [N, d_model] -> y bf16 [N, d_model], ordered on
+ * `stream`.  x and y may be device pointers or host pointers (then staged
+ * through the layer's workspace, and the call returns after y is written).
+ * N == 0 is a no-op; 0 < N <= max_tokens.  With misses (possible unless
+ * every expert is resident) the call waits on the host for the step's routing
+ * (one small device->host copy) and then issues the slot fills on the
+ * layer's fill stream; otherwise it returns without waiting.  regime:
+ * MOE_REGIME_*.  MOE_ERR_NOT_INSTALLED if a miss has no host source. */
+int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
+                int regime, moe_forward_info* info);
+
+/* Kernel timing.  moe_profile(layer, 1) resets the counters and from then
+ * on brackets every launch of the layer with CUDA events on the stream it runs
+ * on (at most 32768 launches are timed); moe_profile(layer, 0) stops.
+ * moe_profile_read synchronizes the device and returns, per MOE_PROF_* class,
+ * the summed device milliseconds and the launch count (arrays of
+ * MOE_PROF_KINDS entries, either may be NULL).  Timing adds one event record
+ * per launch edge and nothing else. */
+int moe_profile(moe_layer_t layer, int enable);
+int moe_profile_read(moe_layer_t layer, double* ms, int* launches);
+
+const char* moe_last_error(moe_layer_t layer);
+const char* moe_status_string(int status);
+
+/* ---- test hooks: each runs one step of moe_forward's path in isolation.
+ * All pointers are device pointers; work is ordered on `stream`. ---------- */
+
+/* Router: idx int32 [N, k] ascending expert id, gates fp32 [N, k], logits fp32
+ * [N, E] (may be NULL). */
+int moe_debug_router(moe_layer_t layer, const void* x, int N, int* idx,
+                     float* gates, float* logits, void* stream);
+
+/* Permutation of idx int32 [N, k]: counts [E], offsets [E+1], row_of [N*k]
+ * (row of (t, j) at t*k + j), tok_of [N*k]. */
+int moe_debug_permute(moe_layer_t layer, const int* idx, int N, int* counts,
+                      int* offsets, int* row_of, int* tok_of, void* stream);
+
+/* Dequantised fp32 weights of matrix m (0 gate, 1 up, 2 down) of the expert
+ * in slot `slot` (slot -1: the shared expert), written row-major to out. */
+int moe_debug_dequant(moe_layer_t layer, int slot, int m, float* out, void* stream);
+
+/* FP4 activation quantiser of the prefill regime on fp32 rows v [rows, K]:
+ * packed codes [rows, K/2], scale bytes [rows, K/block]; `which` 0 uses
+ * act_scale_x, 1 act_scale_h (NVFP4 only). */
+int moe_debug_actquant(moe_layer_t layer, const float* v, int rows, int K,
+                       uint8_t* codes, uint8_t* scales, int which, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,731 @@
+// Host side of the C ABI (include/moe.h): validation, device buffers, the
+// per-step launch sequence, and the host->slot fills of cache misses.
+//
+// One step of moe_forward (decode regime):
+//   caller stream: router -> permute -> LRU step -> [record copy to host]
+//                  -> expert GEMV over the hits (+ shared expert)
+//   host:          wait for the record, then per wave of n_slots accesses:
+//   fill stream:   cudaMemcpyAsync pinned host expert -> evicted slot
+//   caller stream: wait for the wave's fills -> expert GEMV over its misses
+//   caller stream: combine -> y
+// The hits are computed while the host reads the record and the fills are in
+// flight.  When every expert is resident (n_slots >= E, all installed) no
+// miss can happen and the step runs without any host wait.
+//
+// The fill design follows the pages' decode path: misses are loaded into the
+// GPU's LRU expert cache from host memory ("FreeToken：把 284B MoE 塞进游戏
+// PC", zhichai.net, §二 "Decode" paragraph).  The pages' alternative of
+// running some misses on the CPU (their q* split) is not part of this library.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+using namespace moe;
+
+struct moe_layer {
+  moe_layer_desc desc{};
+  Geo g{};
+  moe_expert_layout lay{};
+  int device = 0;
+  int num_sms = 0;
+  std::vector<void*> dev_allocs;
+  void* pinned_rec = nullptr;
+  // device buffers
+  uint8_t* slots = nullptr;
+  uint8_t* shared_w = nullptr;
+  float* Wr = nullptr;
+  float* bias = nullptr;
+  int* slot_of = nullptr;
+  int* expert_of = nullptr;
+  unsigned long long* stamp = nullptr;
+  unsigned long long* clock = nullptr;
+  float* logits = nullptr;
+  int* idx = nullptr;
+  float* gates = nullptr;
+  int* xexp = nullptr;
+  int* counts = nullptr;
+  int* offsets = nullptr;
+  int* row_of = nullptr;
+  int* tok_of = nullptr;
+  void* perm_scratch = nullptr;
+  StepRecord* rec = nullptr;
+  StepRecord* rec_host = nullptr;
+  float* h = nullptr;
+  float* O = nullptr;
+  __nv_bfloat16* x_stage = nullptr;
+  __nv_bfloat16* y_stage = nullptr;
+  int* list_dev = nullptr;
+  int list_cap = 0;
+  // host state
+  const uint8_t* host_pool = nullptr;
+  size_t host_pool_bytes = 0;
+  bool router_set = false;
+  bool shared_set = false;
+  cudaStream_t fill = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_comp = nullptr;
+  std::vector<int> mirror;   // expert per slot as far as the host knows
+  std::string err;
+  // kernel timing (moe_profile)
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_pool;
+  size_t prof_used = 0;
+  std::vector<int> prof_kind;          // one entry per timed launch (pair of events)
+  int launches = 0;                    // kernels launched by the current call
+};
+
+namespace {
+
+int fail(moe_layer* L, int code, const char* fmt, ...) {
+  if (L) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    L->err = buf;
+  }
+  return code;
+}
+
+int cuda_fail(moe_layer* L, cudaError_t e, const char* what) {
+  return fail(L, MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(L, call)                                   \
+  do {                                                      \
+    cudaError_t e_ = (call);                                \
+    if (e_ != cudaSuccess) return cuda_fail((L), e_, #call); \
+  } while (0)
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool is_pow2_float(float v) {
+  if (!(v > 0.f) || !std::isfinite(v)) return false;
+  int ex;
+  return std::frexp(v, &ex) == 0.5f;
+}
+
+int check_desc(const moe_layer_desc* d, std::string* why) {
+  char buf[256];
+  auto bad = [&](const char* m) { *why = m; return MOE_ERR_ARG; };
+  if (!d) return bad("descriptor is NULL");
+  if (d->E < 1 || d->E > kMaxE) return bad("E must be in [1, 1024]");
+  if (d->k < 1 || d->k > d->E || d->k > kMaxK) return bad("k must be in [1, min(E, 32)]");
+  if (d->d_model <= 0 || d->d_model % 128) return bad("d_model must be a positive multiple of 128");
+  if (d->d_ff <= 0 || d->d_ff % 128) return bad("d_ff must be a positive multiple of 128");
+  if (d->n_slots < 1 || d->n_slots > d->E) return bad("n_slots must be in [1, E]");
+  if (d->fmt != MOE_MXFP4 && d->fmt != MOE_NVFP4) return bad("fmt must be MOE_MXFP4 or MOE_NVFP4");
+  if (d->max_tokens < 1) return bad("max_tokens must be >= 1");
+  if ((long long)d->max_tokens * (d->k + 1) > (1LL << 30)) return bad("max_tokens * (k+1) too large");
+  if (d->fmt == MOE_NVFP4 && (!is_pow2_float(d->act_scale_x) || !is_pow2_float(d->act_scale_h))) {
+    snprintf(buf, sizeof buf, "NVFP4 act_scale_x/act_scale_h must be positive powers of two");
+    *why = buf;
+    return MOE_ERR_ARG;
+  }
+  return MOE_OK;
+}
+
+void fill_layout(const moe_layer_desc* d, moe_expert_layout* l) {
+  const size_t D = d->d_model, F = d->d_ff;
+  const size_t blk = d->fmt == MOE_MXFP4 ? 32 : 16;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  l->gate_codes = take(F * D / 2);
+  l->up_codes = take(F * D / 2);
+  l->down_codes = take(D * F / 2);
+  l->gate_scales = take(F * D / blk);
+  l->up_scales = take(F * D / blk);
+  l->down_scales = take(D * F / blk);
+  l->tensor_scales = take(16);
+  l->bytes = off;
+}
+
+Geo make_geo(const moe_layer_desc* d, const moe_expert_layout* l) {
+  Geo g{};
+  g.E = d->E; g.k = d->k; g.d = d->d_model; g.f = d->d_ff; g.S = d->n_slots; g.fmt = d->fmt;
+  g.has_shared = d->has_shared ? 1 : 0; g.norm_topk = d->norm_topk ? 1 : 0;
+  g.has_bias = d->has_bias ? 1 : 0;
+  g.blk = d->fmt == MOE_MXFP4 ? 32 : 16;
+  g.ebytes = l->bytes;
+  g.off_codes[0] = l->gate_codes; g.off_codes[1] = l->up_codes; g.off_codes[2] = l->down_codes;
+  g.off_scales[0] = l->gate_scales; g.off_scales[1] = l->up_scales; g.off_scales[2] = l->down_scales;
+  g.off_tscale = l->tensor_scales;
+  return g;
+}
+
+template <class T>
+int dalloc(moe_layer* L, T** p, size_t bytes) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(L, MOE_ERR_OOM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  L->dev_allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return MOE_OK;
+}
+
+void release(moe_layer* L) {
+  for (cudaEvent_t e : L->prof_pool) cudaEventDestroy(e);
+  L->prof_pool.clear();
+  for (void* p : L->dev_allocs) cudaFree(p);
+  L->dev_allocs.clear();
+  if (L->pinned_rec) cudaFreeHost(L->pinned_rec);
+  L->pinned_rec = nullptr;
+  if (L->ev_route) cudaEventDestroy(L->ev_route);
+  if (L->ev_fill) cudaEventDestroy(L->ev_fill);
+  if (L->ev_comp) cudaEventDestroy(L->ev_comp);
+  if (L->fill) cudaStreamDestroy(L->fill);
+  L->ev_route = L->ev_fill = L->ev_comp = nullptr;
+  L->fill = nullptr;
+}
+
+int pointer_kind(const void* p, bool* on_device, int device) {
+  cudaPointerAttributes a{};
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *on_device = false;
+    return MOE_OK;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    if (a.device != device) return MOE_ERR_ARG;
+    *on_device = true;
+  } else {
+    *on_device = false;
+  }
+  return MOE_OK;
+}
+
+bool all_resident(const moe_layer* L) {
+  if (L->g.S < L->g.E) return false;
+  int n = 0;
+  for (int e : L->mirror) n += e >= 0 ? 1 : 0;
+  return n == L->g.E;
+}
+
+// Apply a step record to the host mirror of the slot table.
+void mirror_apply(moe_layer* L, const StepRecord* r) {
+  const int U = r->U, S = r->S, E = L->g.E;
+  const int* ae = rec_expert(const_cast<StepRecord*>(r));
+  const int* as = rec_slot(const_cast<StepRecord*>(r), E);
+  for (int i = std::max(0, U - S); i < U; ++i) L->mirror[as[i]] = ae[i];
+}
+
+constexpr size_t kProfPairs = 16384;
+
+// Two events bracketing one launch of class `kind` (null when timing is off
+// or the pool is used up); the start event is recorded on `st` here.
+cudaEvent_t* prof_begin(moe_layer* L, int kind, cudaStream_t st) {
+  if (!L->prof_on || L->prof_used + 2 > L->prof_pool.size()) return nullptr;
+  cudaEvent_t* e = &L->prof_pool[L->prof_used];
+  L->prof_used += 2;
+  L->prof_kind.push_back(kind);
+  cudaEventRecord(e[0], st);
+  return e;
+}
+
+void prof_end(cudaEvent_t* e, cudaStream_t st) {
+  if (e) cudaEventRecord(e[1], st);
+}
+
+int n_ent_cap(const moe_layer* L, int N) {
+  long long routed = (long long)N * L->g.k;
+  return (int)std::min<long long>(std::min(L->g.S, L->g.E), routed);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_NOT_INSTALLED: return "expert has no host source";
+    case MOE_ERR_OOM: return "out of memory";
+    case MOE_ERR_FILL: return "cache fill failed";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_STATE: return "invalid state";
+    case MOE_ERR_UNSUPPORTED: return "unsupported by this build";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_last_error(moe_layer_t L) { return L ? L->err.c_str() : "null layer"; }
+
+int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out) {
+  std::string why;
+  if (!out) return MOE_ERR_ARG;
+  int rc = check_desc(desc, &why);
+  if (rc) return rc;
+  fill_layout(desc, out);
+  return MOE_OK;
+}
+
+int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
+  if (!out) return MOE_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  int rc = check_desc(desc, &why);
+  if (rc) return rc;
+  moe_layer* L = new (std::nothrow) moe_layer();
+  if (!L) return MOE_ERR_OOM;
+  L->desc = *desc;
+  fill_layout(desc, &L->lay);
+  L->g = make_geo(desc, &L->lay);
+  if (!gemv_shape_ok(L->g)) {
+    delete L;
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (cudaGetDevice(&L->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device) != cudaSuccess) {
+    cudaGetLastError();
+    delete L;
+    return MOE_ERR_CUDA;
+  }
+  const Geo& g = L->g;
+  const size_t Nm = desc->max_tokens;
+  const size_t rows = Nm * g.k + (g.has_shared ? Nm : 0);
+  rc = MOE_OK;
+#define MOE_ALLOC(ptr, bytes) \
+  if (rc == MOE_OK) rc = dalloc(L, &L->ptr, (bytes))
+  MOE_ALLOC(slots, (size_t)g.S * g.ebytes);
+  if (g.has_shared) MOE_ALLOC(shared_w, g.ebytes);
+  MOE_ALLOC(Wr, (size_t)g.E * g.d * 4);
+  MOE_ALLOC(bias, (size_t)g.E * 4);
+  MOE_ALLOC(slot_of, (size_t)g.E * 4);
+  MOE_ALLOC(expert_of, (size_t)g.S * 4);
+  MOE_ALLOC(stamp, (size_t)g.S * 8);
+  MOE_ALLOC(clock, 8);
+  MOE_ALLOC(logits, Nm * g.E * 4);
+  MOE_ALLOC(idx, Nm * g.k * 4);
+  MOE_ALLOC(gates, Nm * g.k * 4);
+  MOE_ALLOC(xexp, Nm * 4);
+  MOE_ALLOC(counts, (size_t)g.E * 4);
+  MOE_ALLOC(offsets, (size_t)(g.E + 1) * 4);
+  MOE_ALLOC(row_of, Nm * g.k * 4);
+  MOE_ALLOC(tok_of, Nm * g.k * 4);
+  MOE_ALLOC(perm_scratch, permute_scratch_bytes(g, (int)Nm));
+  MOE_ALLOC(rec, rec_bytes(g.E));
+  MOE_ALLOC(h, rows * g.f * 4);
+  MOE_ALLOC(O, rows * g.d * 4);
+  MOE_ALLOC(x_stage, Nm * g.d * 2);
+  MOE_ALLOC(y_stage, Nm * g.d * 2);
+  L->list_cap = (int)std::max<size_t>(Nm * g.k, (size_t)g.E);
+  MOE_ALLOC(list_dev, (size_t)L->list_cap * 4);
+#undef MOE_ALLOC
+  if (rc == MOE_OK && cudaHostAlloc(&L->pinned_rec, rec_bytes(g.E), cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    rc = MOE_ERR_OOM;
+  }
+  if (rc == MOE_OK) {
+    L->rec_host = static_cast<StepRecord*>(L->pinned_rec);
+    if (cudaStreamCreateWithFlags(&L->fill, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&L->ev_route, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&L->ev_comp, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      rc = MOE_ERR_CUDA;
+    }
+  }
+  if (rc == MOE_OK) {
+    // empty cache, zero bias, unit tensor scales for the shared expert slot
+    bool ok = cudaMemset(L->slot_of, 0xff, (size_t)g.E * 4) == cudaSuccess &&
+              cudaMemset(L->expert_of, 0xff, (size_t)g.S * 4) == cudaSuccess &&
+              cudaMemset(L->stamp, 0, (size_t)g.S * 8) == cudaSuccess &&
+              cudaMemset(L->clock, 0, 8) == cudaSuccess &&
+              cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
+              cudaMemset(L->rec, 0, rec_bytes(g.E)) == cudaSuccess &&
+              cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      rc = MOE_ERR_CUDA;
+    }
+  }
+  if (rc != MOE_OK) {
+    release(L);
+    delete L;
+    return rc;
+  }
+  L->mirror.assign(g.S, -1);
+  *out = L;
+  return MOE_OK;
+}
+
+int moe_layer_destroy(moe_layer_t L) {
+  if (!L) return MOE_ERR_ARG;
+  cudaDeviceSynchronize();
+  release(L);
+  delete L;
+  return MOE_OK;
+}
+
+int moe_set_router(moe_layer_t L, const float* W_r, const float* bias) {
+  if (!L) return MOE_ERR_ARG;
+  if (!W_r) return fail(L, MOE_ERR_ARG, "W_r is NULL");
+  if (L->g.has_bias && !bias) return fail(L, MOE_ERR_ARG, "layer has a bias but bias is NULL");
+  MOE_CUDA(L, cudaMemcpy(L->Wr, W_r, (size_t)L->g.E * L->g.d * 4, cudaMemcpyDefault));
+  if (L->g.has_bias) MOE_CUDA(L, cudaMemcpy(L->bias, bias, (size_t)L->g.E * 4, cudaMemcpyDefault));
+  L->router_set = true;
+  return MOE_OK;
+}
+
+int moe_register_host_experts(moe_layer_t L, const void* pool, size_t bytes) {
+  if (!L) return MOE_ERR_ARG;
+  if (!pool) return fail(L, MOE_ERR_ARG, "pool is NULL");
+  if (bytes < (size_t)L->g.E * L->g.ebytes)
+    return fail(L, MOE_ERR_ARG, "pool holds %zu bytes, need E * layout.bytes = %zu", bytes,
+                (size_t)L->g.E * L->g.ebytes);
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, pool) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return fail(L, MOE_ERR_ARG, "pool must be pinned (page-locked) host memory");
+  }
+  L->host_pool = static_cast<const uint8_t*>(pool);
+  L->host_pool_bytes = bytes;
+  return MOE_OK;
+}
+
+int moe_set_shared_expert(moe_layer_t L, const void* weights) {
+  if (!L) return MOE_ERR_ARG;
+  if (!L->g.has_shared) return fail(L, MOE_ERR_STATE, "layer has no shared expert");
+  if (!weights) return fail(L, MOE_ERR_ARG, "weights is NULL");
+  MOE_CUDA(L, cudaMemcpy(L->shared_w, weights, L->g.ebytes, cudaMemcpyDefault));
+  L->shared_set = true;
+  return MOE_OK;
+}
+
+int moe_cache_install(moe_layer_t L, int expert, int slot, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  if (expert < 0 || expert >= L->g.E) return fail(L, MOE_ERR_ARG, "expert %d out of range", expert);
+  if (slot < 0 || slot >= L->g.S) return fail(L, MOE_ERR_ARG, "slot %d out of range", slot);
+  if (!L->host_pool) return fail(L, MOE_ERR_NOT_INSTALLED, "no host expert pool registered");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)slot * L->g.ebytes,
+                              L->host_pool + (size_t)expert * L->g.ebytes, L->g.ebytes,
+                              cudaMemcpyHostToDevice, st));
+  MOE_CUDA(L, launch_lru_install(L->g, expert, slot, L->slot_of, L->expert_of, L->stamp, L->clock, st));
+  for (int s = 0; s < L->g.S; ++s)
+    if (L->mirror[s] == expert) L->mirror[s] = -1;
+  L->mirror[slot] = expert;
+  return MOE_OK;
+}
+
+int moe_lru_get_state(moe_layer_t L, int* expert_of_slot, uint64_t* stamp, uint64_t* clock) {
+  if (!L) return MOE_ERR_ARG;
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  if (expert_of_slot)
+    MOE_CUDA(L, cudaMemcpy(expert_of_slot, L->expert_of, (size_t)L->g.S * 4, cudaMemcpyDeviceToHost));
+  if (stamp) MOE_CUDA(L, cudaMemcpy(stamp, L->stamp, (size_t)L->g.S * 8, cudaMemcpyDeviceToHost));
+  if (clock) MOE_CUDA(L, cudaMemcpy(clock, L->clock, 8, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+int moe_lru_set_state(moe_layer_t L, const int* expert_of_slot, const uint64_t* stamp, uint64_t clock) {
+  if (!L) return MOE_ERR_ARG;
+  if (!expert_of_slot || !stamp) return fail(L, MOE_ERR_ARG, "NULL state array");
+  const int E = L->g.E, S = L->g.S;
+  std::vector<int> slot_of(E, -1);
+  for (int s = 0; s < S; ++s) {
+    const int e = expert_of_slot[s];
+    if (e < -1 || e >= E) return fail(L, MOE_ERR_ARG, "expert %d in slot %d out of range", e, s);
+    if (e >= 0) {
+      if (slot_of[e] >= 0) return fail(L, MOE_ERR_ARG, "expert %d in two slots", e);
+      if (stamp[s] > clock) return fail(L, MOE_ERR_ARG, "stamp of slot %d exceeds clock", s);
+      slot_of[e] = s;
+    }
+  }
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  MOE_CUDA(L, cudaMemcpy(L->expert_of, expert_of_slot, (size_t)S * 4, cudaMemcpyHostToDevice));
+  MOE_CUDA(L, cudaMemcpy(L->slot_of, slot_of.data(), (size_t)E * 4, cudaMemcpyHostToDevice));
+  MOE_CUDA(L, cudaMemcpy(L->stamp, stamp, (size_t)S * 8, cudaMemcpyHostToDevice));
+  MOE_CUDA(L, cudaMemcpy(L->clock, &clock, 8, cudaMemcpyHostToDevice));
+  L->mirror.assign(expert_of_slot, expert_of_slot + S);
+  return MOE_OK;
+}
+
+int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, int* miss_experts_out,
+                  int* miss_slots_out, int* n_miss_out, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  if (n < 0 || n > L->list_cap) return fail(L, MOE_ERR_ARG, "n must be in [0, %d]", L->list_cap);
+  if (n > 0 && !experts) return fail(L, MOE_ERR_ARG, "experts is NULL");
+  for (int i = 0; i < n; ++i)
+    if (experts[i] < 0 || experts[i] >= L->g.E) return fail(L, MOE_ERR_ARG, "expert %d out of range", experts[i]);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Geo& g = L->g;
+  if (n > 0) MOE_CUDA(L, cudaMemcpyAsync(L->list_dev, experts, (size_t)n * 4, cudaMemcpyHostToDevice, st));
+  MOE_CUDA(L, launch_counts_from_list(g, L->list_dev, n, L->counts, st));
+  MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec, st));
+  MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(L, cudaStreamSynchronize(st));
+  const StepRecord* r = L->rec_host;
+  const int* ae = rec_expert(const_cast<StepRecord*>(r));
+  const int* as = rec_slot(const_cast<StepRecord*>(r), g.E);
+  if (r->U < 0 || r->U > g.E || r->n_hit < 0 || r->n_hit > r->U)
+    return fail(L, MOE_ERR_STATE, "step record is inconsistent");
+  for (int i = 0; i < r->U; ++i)
+    if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S)
+      return fail(L, MOE_ERR_STATE, "step record entry %d is out of range", i);
+  if (L->host_pool) {
+    for (int i = r->n_hit; i < r->U; ++i)
+      MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)as[i] * g.ebytes, L->host_pool + (size_t)ae[i] * g.ebytes,
+                                  g.ebytes, cudaMemcpyHostToDevice, st));
+    MOE_CUDA(L, cudaStreamSynchronize(st));
+  }
+  mirror_apply(L, r);
+  if (slot_of_out) {
+    std::vector<int> where(g.E, -1);
+    for (int i = 0; i < r->U; ++i) where[ae[i]] = as[i];
+    for (int i = 0; i < n; ++i) slot_of_out[i] = where[experts[i]];
+  }
+  for (int i = r->n_hit, m = 0; i < r->U; ++i, ++m) {
+    if (miss_experts_out) miss_experts_out[m] = ae[i];
+    if (miss_slots_out) miss_slots_out[m] = as[i];
+  }
+  if (n_miss_out) *n_miss_out = r->n_miss;
+  return MOE_OK;
+}
+
+int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int regime,
+                moe_forward_info* info) {
+  if (!L) return MOE_ERR_ARG;
+  const Geo& g = L->g;
+  if (info) {
+    std::memset(info, 0, sizeof *info);
+    info->n_tokens = N;
+  }
+  if (N < 0 || N > L->desc.max_tokens)
+    return fail(L, MOE_ERR_ARG, "N = %d outside [0, max_tokens = %d]", N, L->desc.max_tokens);
+  if (N == 0) return MOE_OK;
+  if (!x || !y) return fail(L, MOE_ERR_ARG, "x or y is NULL");
+  if (!L->router_set) return fail(L, MOE_ERR_STATE, "router weights not set");
+  if (g.has_shared && !L->shared_set) return fail(L, MOE_ERR_STATE, "shared expert not set");
+  if (regime == MOE_REGIME_PREFILL)
+    return fail(L, MOE_ERR_UNSUPPORTED, "the prefill regime is not built into this library yet");
+  if (regime != MOE_REGIME_AUTO && regime != MOE_REGIME_DECODE)
+    return fail(L, MOE_ERR_ARG, "unknown regime %d", regime);
+  const bool resident = all_resident(L);
+  if (!resident && !L->host_pool)
+    return fail(L, MOE_ERR_NOT_INSTALLED, "not every expert is resident and no host pool is registered");
+  bool x_dev = false, y_dev = false;
+  if (pointer_kind(x, &x_dev, L->device) || pointer_kind(y, &y_dev, L->device))
+    return fail(L, MOE_ERR_ARG, "x or y is device memory of another device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t xbytes = (size_t)N * g.d * 2;
+  const __nv_bfloat16* xd = static_cast<const __nv_bfloat16*>(x);
+  __nv_bfloat16* yd = static_cast<__nv_bfloat16*>(y);
+  if (!x_dev) {
+    MOE_CUDA(L, cudaMemcpyAsync(L->x_stage, x, xbytes, cudaMemcpyHostToDevice, st));
+    xd = L->x_stage;
+  }
+  if (!y_dev) yd = L->y_stage;
+
+  L->launches = 0;
+  cudaEvent_t* pe = prof_begin(L, MOE_PROF_ROUTER, st);
+  MOE_CUDA(L, launch_router(g, xd, N, L->Wr, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
+                            L->gates, L->xexp, st));
+  prof_end(pe, st);
+  L->launches += 2;
+  pe = prof_begin(L, MOE_PROF_PERMUTE, st);
+  MOE_CUDA(L, launch_permute(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
+                             L->perm_scratch, st));
+  prof_end(pe, st);
+  L->launches += N <= 128 ? 1 : 3;
+  pe = prof_begin(L, MOE_PROF_LRU, st);
+  MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec, st));
+  prof_end(pe, st);
+  L->launches += 1;
+  if (!resident) {
+    MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
+    MOE_CUDA(L, cudaEventRecord(L->ev_route, st));
+  }
+  GemvArgs a{};
+  a.slots = L->slots;
+  a.shared_w = L->shared_w;
+  a.rec = L->rec;
+  a.offsets = L->offsets;
+  a.tok_of = L->tok_of;
+  a.N = N;
+  a.mode = kRangeHits;
+  a.wave = 0;
+  a.with_shared = g.has_shared;
+  const int cap = n_ent_cap(L, N);
+  auto gemv = [&](int n_ent) -> int {
+    cudaEvent_t ev[4];
+    const bool room = L->prof_used + 4 <= L->prof_pool.size();
+    cudaEvent_t* p1 = room ? prof_begin(L, MOE_PROF_GATEUP, st) : nullptr;
+    cudaEvent_t* p2 = p1 ? prof_begin(L, MOE_PROF_DOWN, st) : nullptr;
+    const cudaEvent_t* evp = nullptr;
+    if (p1 && p2) {
+      ev[0] = p1[0]; ev[1] = p1[1]; ev[2] = p2[0]; ev[3] = p2[1];
+      evp = ev;
+    }
+    cudaError_t ce = launch_gemv_decode(g, a, xd, L->xexp, L->h, L->O, n_ent, st, evp);
+    if (ce != cudaSuccess) return cuda_fail(L, ce, "launch_gemv_decode");
+    L->launches += 2;
+    return MOE_OK;
+  };
+  int grc = gemv(cap + (g.has_shared ? 1 : 0));
+  if (grc) return grc;
+
+  size_t fill_bytes = 0;
+  int U = -1, n_hit = -1, n_miss = 0, waves = 1;
+  if (!resident) {
+    MOE_CUDA(L, cudaEventSynchronize(L->ev_route));
+    const StepRecord* r = L->rec_host;
+    U = r->U;
+    n_hit = r->n_hit;
+    n_miss = r->n_miss;
+    waves = (U + g.S - 1) / g.S;
+    const int* ae = rec_expert(const_cast<StepRecord*>(r));
+    const int* as = rec_slot(const_cast<StepRecord*>(r), g.E);
+    if (U < 0 || U > g.E || n_hit < 0 || n_hit > U)
+      return fail(L, MOE_ERR_STATE, "step record is inconsistent (U=%d, hits=%d)", U, n_hit);
+    for (int i = 0; i < U; ++i)
+      if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S)
+        return fail(L, MOE_ERR_STATE, "step record entry %d is out of range", i);
+    for (int w = 0; w < waves; ++w) {
+      const int b = std::max(n_hit, w * g.S), e = std::min((w + 1) * g.S, U);
+      if (b >= e) continue;
+      if (w == 0) {
+        // wave 0 fills only free or stale slots: wait for the routing alone
+        MOE_CUDA(L, cudaStreamWaitEvent(L->fill, L->ev_route, 0));
+      } else {
+        // a later wave overwrites slots the previous wave computed from
+        MOE_CUDA(L, cudaEventRecord(L->ev_comp, st));
+        MOE_CUDA(L, cudaStreamWaitEvent(L->fill, L->ev_comp, 0));
+      }
+      cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, L->fill);
+      for (int i = b; i < e; ++i) {
+        cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)as[i] * g.ebytes,
+                                         L->host_pool + (size_t)ae[i] * g.ebytes, g.ebytes,
+                                         cudaMemcpyHostToDevice, L->fill);
+        if (ce != cudaSuccess) return fail(L, MOE_ERR_FILL, "fill of expert %d: %s", ae[i], cudaGetErrorString(ce));
+        fill_bytes += g.ebytes;
+      }
+      prof_end(pf, L->fill);
+      MOE_CUDA(L, cudaEventRecord(L->ev_fill, L->fill));
+      MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
+      a.mode = kRangeWaveMisses;
+      a.wave = w;
+      a.with_shared = 0;
+      grc = gemv(std::min(cap, g.S));
+      if (grc) return grc;
+    }
+    mirror_apply(L, r);
+  }
+  pe = prof_begin(L, MOE_PROF_COMBINE, st);
+  MOE_CUDA(L, launch_combine(g, L->O, L->gates, L->row_of, N, yd, st));
+  prof_end(pe, st);
+  L->launches += 1;
+  if (!y_dev) {
+    MOE_CUDA(L, cudaMemcpyAsync(y, yd, xbytes, cudaMemcpyDeviceToHost, st));
+    MOE_CUDA(L, cudaStreamSynchronize(st));
+  }
+  if (info) {
+    info->regime = MOE_REGIME_DECODE;
+    info->n_distinct = U;
+    info->n_hits = n_hit;
+    info->n_misses = n_miss;
+    info->n_waves = resident ? 1 : waves;
+    info->fill_bytes = fill_bytes;
+    info->host_synced = resident ? 0 : 1;
+    info->n_launches = L->launches;
+  }
+  return MOE_OK;
+}
+
+int moe_profile(moe_layer_t L, int enable) {
+  if (!L) return MOE_ERR_ARG;
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  if (enable && L->prof_pool.empty()) {
+    L->prof_pool.resize(2 * kProfPairs);
+    for (auto& e : L->prof_pool) MOE_CUDA(L, cudaEventCreate(&e));
+  }
+  L->prof_on = enable != 0;
+  L->prof_used = 0;
+  L->prof_kind.clear();
+  return MOE_OK;
+}
+
+int moe_profile_read(moe_layer_t L, double* ms, int* launches) {
+  if (!L) return MOE_ERR_ARG;
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  double acc[MOE_PROF_KINDS] = {0};
+  int cnt[MOE_PROF_KINDS] = {0};
+  for (size_t i = 0; i < L->prof_kind.size(); ++i) {
+    float t = 0.f;
+    MOE_CUDA(L, cudaEventElapsedTime(&t, L->prof_pool[2 * i], L->prof_pool[2 * i + 1]));
+    acc[L->prof_kind[i]] += t;
+    cnt[L->prof_kind[i]] += 1;
+  }
+  for (int k = 0; k < MOE_PROF_KINDS; ++k) {
+    if (ms) ms[k] = acc[k];
+    if (launches) launches[k] = cnt[k];
+  }
+  return MOE_OK;
+}
+
+int moe_debug_router(moe_layer_t L, const void* x, int N, int* idx, float* gates, float* logits,
+                     void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  if (N < 0 || N > L->desc.max_tokens) return fail(L, MOE_ERR_ARG, "N out of range");
+  if (N == 0) return MOE_OK;
+  if (!x || !idx || !gates) return fail(L, MOE_ERR_ARG, "NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(L, launch_router(L->g, static_cast<const __nv_bfloat16*>(x), N, L->Wr,
+                            L->g.has_bias ? L->bias : nullptr, logits ? logits : L->logits, idx,
+                            gates, L->xexp, st));
+  return MOE_OK;
+}
+
+int moe_debug_permute(moe_layer_t L, const int* idx, int N, int* counts, int* offsets, int* row_of,
+                      int* tok_of, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  if (N < 0 || N > L->desc.max_tokens) return fail(L, MOE_ERR_ARG, "N out of range");
+  if (N == 0) return MOE_OK;
+  if (!idx || !counts || !offsets || !row_of || !tok_of) return fail(L, MOE_ERR_ARG, "NULL pointer");
+  MOE_CUDA(L, launch_permute(L->g, idx, N, counts, offsets, row_of, tok_of, L->perm_scratch,
+                             static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_debug_dequant(moe_layer_t L, int slot, int m, float* out, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  if (m < 0 || m > 2 || !out) return fail(L, MOE_ERR_ARG, "bad matrix or NULL out");
+  const uint8_t* base;
+  if (slot == -1) {
+    if (!L->g.has_shared) return fail(L, MOE_ERR_STATE, "no shared expert");
+    base = L->shared_w;
+  } else if (slot >= 0 && slot < L->g.S) {
+    base = L->slots + (size_t)slot * L->g.ebytes;
+  } else {
+    return fail(L, MOE_ERR_ARG, "slot %d out of range", slot);
+  }
+  MOE_CUDA(L, launch_dequant(L->g, base, m, out, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_debug_actquant(moe_layer_t L, const float* v, int rows, int K, uint8_t* codes, uint8_t* scales,
+                       int which, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  if (rows < 0 || K <= 0 || K % 32) return fail(L, MOE_ERR_ARG, "rows >= 0 and K a multiple of 32");
+  if (rows == 0) return MOE_OK;
+  if (!v || !codes || !scales) return fail(L, MOE_ERR_ARG, "NULL pointer");
+  const float gs = which ? L->desc.act_scale_h : L->desc.act_scale_x;
+  MOE_CUDA(L, launch_actquant(L->g, v, rows, K, codes, scales, L->g.fmt == MOE_NVFP4 ? gs : 1.0f,
+                              static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+}  // extern "C"

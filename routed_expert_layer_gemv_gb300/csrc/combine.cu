@@ -1,0 +1,55 @@
+// Combine: y[t] = sum_{j < k} gate[t, j] * O[row_of[t, j]] (+ O[N*k + t] for
+// the shared expert, weight 1), accumulated in fp32 in ascending j (= ascending
+// expert id) and rounded once to bf16.  A fixed summation order with no
+// atomics makes the output reproducible bit for bit.  (The pages do not define
+// the combine; a shared, always-on expert is one of the architecture axes of
+// the ananclaw.com explainer, §核心方法 4.)
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+__global__ void combine_kernel(const float* __restrict__ O, const float* __restrict__ gates,
+                               const int* __restrict__ row_of, int N, int k, int d, int shared,
+                               __nv_bfloat16* __restrict__ y) {
+  const int q = d / 4;
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= N * q) return;
+  const int t = v / q, c4 = v % q;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const float gj = gates[(size_t)t * k + j];
+    const float4 o = reinterpret_cast<const float4*>(O + (size_t)row_of[(size_t)t * k + j] * d)[c4];
+    acc.x = fmaf(gj, o.x, acc.x);
+    acc.y = fmaf(gj, o.y, acc.y);
+    acc.z = fmaf(gj, o.z, acc.z);
+    acc.w = fmaf(gj, o.w, acc.w);
+  }
+  if (shared) {
+    const float4 o = reinterpret_cast<const float4*>(O + ((size_t)N * k + t) * d)[c4];
+    acc.x += o.x;
+    acc.y += o.y;
+    acc.z += o.z;
+    acc.w += o.w;
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 out;
+  out.x = *reinterpret_cast<uint32_t*>(&lo);
+  out.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(y + (size_t)t * d)[c4] = out;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Geo& g, const float* O, const float* gates, const int* row_of,
+                           int N, __nv_bfloat16* y, cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  const int total = N * (g.d / 4);
+  combine_kernel<<<(total + 255) / 256, 256, 0, st>>>(O, gates, row_of, N, g.k, g.d, g.has_shared,
+                                                     y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,111 @@
+// Internal declarations shared by the CUDA translation units of the layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+#define MOE_DEV __device__ __forceinline__
+
+namespace moe {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------- formats
+// E8M0 scale byte -> 2^(x-127) (x = 0 is the fp32 subnormal 2^-127).
+MOE_DEV float e8m0_to_f32(uint32_t x) {
+  return x == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(x << 23);
+}
+
+// E4M3 (fn) byte -> fp32: bias 7 -> fp32 bias 127; exponent 0 is subnormal.
+MOE_DEV float e4m3_to_f32(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float v = e == 0 ? (float)m * (1.0f / 512.0f) : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (b & 0x80u) ? -v : v;
+}
+
+// Two E2M1 codes (one byte, low nibble first) -> f16x2, exact.
+MOE_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(out) : "r"(byte));
+  return out;
+}
+
+// ---------------------------------------------------------------- step record
+// What one step's routing and LRU update decided; written by the LRU kernel,
+// copied to pinned host memory for the fill issue.  Arrays hold |U| entries
+// in access order (hits ascending id, then misses ascending id).
+struct StepRecord {
+  int U;        // distinct routed experts
+  int n_hit;
+  int n_miss;
+  int S;        // slots (wave length)
+  int pad[4];
+  // followed by int acc_expert[E], acc_slot[E], acc_evicted[E]
+};
+__host__ __device__ inline int* rec_expert(StepRecord* r) { return reinterpret_cast<int*>(r + 1); }
+__host__ __device__ inline int* rec_slot(StepRecord* r, int E) { return rec_expert(r) + E; }
+__host__ __device__ inline int* rec_evicted(StepRecord* r, int E) { return rec_expert(r) + 2 * E; }
+inline size_t rec_bytes(int E) { return sizeof(StepRecord) + 3 * sizeof(int) * (size_t)E; }
+
+// ---------------------------------------------------------------- layer geometry
+struct Geo {
+  int E, k, d, f, S, fmt, has_shared, norm_topk, has_bias;
+  int blk;                     // 32 (MXFP4) or 16 (NVFP4)
+  size_t ebytes;               // padded bytes of one expert
+  size_t off_codes[3], off_scales[3], off_tscale;
+};
+
+// Work-range selectors of the expert GEMV launches (resolved on the device
+// from the StepRecord so a launch needs no host round trip).
+enum RangeMode : int { kRangeHits = 0, kRangeWaveMisses = 1, kRangeAll = 2 };
+
+// ---------------------------------------------------------------- launchers
+// router.cu
+cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
+                          const float* bias, float* logits, int* idx, float* gates, int* xexp,
+                          cudaStream_t st);
+// permute.cu
+size_t permute_scratch_bytes(const Geo& g, int max_tokens);
+cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int* offsets,
+                           int* row_of, int* tok_of, void* scratch, cudaStream_t st);
+// lru.cu
+cudaError_t launch_lru_step(const Geo& g, const int* counts, int* slot_of, int* expert_of,
+                            unsigned long long* stamp, unsigned long long* clock,
+                            StepRecord* rec, cudaStream_t st);
+cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
+                               unsigned long long* stamp, unsigned long long* clock,
+                               cudaStream_t st);
+cudaError_t launch_counts_from_list(const Geo& g, const int* experts, int n, int* counts,
+                                    cudaStream_t st);
+// gemv.cu
+struct GemvArgs {
+  const uint8_t* slots;        // slot pool base
+  const uint8_t* shared_w;     // shared expert (or null)
+  const StepRecord* rec;
+  const int* offsets;          // [E+1]
+  const int* tok_of;           // [N*k]
+  int N;
+  int mode, wave;              // RangeMode + wave index
+  int with_shared;             // also run the shared expert (rows N*k .. N*k+N)
+};
+bool gemv_shape_ok(const Geo& g);
+// ev (may be null): 4 events recorded before/after phase 1 and phase 2
+cudaError_t launch_gemv_decode(const Geo& g, const GemvArgs& a, const __nv_bfloat16* x,
+                               const int* xexp, float* h, float* O, int n_ent_max,
+                               cudaStream_t st, const cudaEvent_t* ev);
+// combine.cu
+cudaError_t launch_combine(const Geo& g, const float* O, const float* gates, const int* row_of,
+                           int N, __nv_bfloat16* y, cudaStream_t st);
+// debug.cu
+cudaError_t launch_dequant(const Geo& g, const uint8_t* expert, int m, float* out, cudaStream_t st);
+cudaError_t launch_actquant(const Geo& g, const float* v, int rows, int K, uint8_t* codes,
+                            uint8_t* scales, float gscale, cudaStream_t st);
+
+}  // namespace moe

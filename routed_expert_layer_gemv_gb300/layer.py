@@ -1,0 +1,118 @@
+"""Set-up helpers around the C ABI: build a layer from per-matrix FP4 arrays.
+
+Packing copies each expert's codes, scales and tensor scales into the byte
+layout the library reports (``moe_expert_layout_for``) inside one pinned host
+pool, the source of every cache fill.  No arithmetic of the layer happens
+here; ``forward`` calls ``moe_forward``.
+"""
+from __future__ import annotations
+
+from typing import Callable, Dict, Optional
+
+import numpy as np
+import torch
+
+from . import capi
+from .workloads import LayerSpec, Matrix, MXFP4
+
+
+def make_desc(spec: LayerSpec, max_tokens: int, act_scale_x: float = 1.0,
+              act_scale_h: float = 1.0) -> capi.moe_layer_desc:
+    return capi.moe_layer_desc(
+        E=spec.E, k=spec.k, d_model=spec.d_model, d_ff=spec.d_ff, n_slots=spec.n_slots,
+        fmt=capi.MOE_MXFP4 if spec.fmt == MXFP4 else capi.MOE_NVFP4,
+        has_shared=int(spec.has_shared), norm_topk=int(spec.norm_topk),
+        has_bias=int(spec.has_bias), max_tokens=max_tokens,
+        act_scale_x=act_scale_x, act_scale_h=act_scale_h)
+
+
+def pack_expert(layout: capi.moe_expert_layout, w: Dict[str, Matrix], out: np.ndarray) -> None:
+    """Write one expert (gate, up, down) into ``out`` (uint8, layout.bytes)."""
+    out[:] = 0
+    for name in ("gate", "up", "down"):
+        m = w[name]
+        c0 = getattr(layout, name + "_codes")
+        s0 = getattr(layout, name + "_scales")
+        out[c0:c0 + m.codes.size] = m.codes.reshape(-1)
+        out[s0:s0 + m.scales.size] = m.scales.reshape(-1)
+    ts = np.array([w["gate"].tscale, w["up"].tscale, w["down"].tscale], dtype=np.float32)
+    t0 = layout.tensor_scales
+    out[t0:t0 + 12] = ts.view(np.uint8)
+
+
+class MoELayer:
+    """One layer on the current CUDA device, driven through the C ABI."""
+
+    def __init__(self, spec: LayerSpec, max_tokens: int, act_scale_x: float = 1.0,
+                 act_scale_h: float = 1.0):
+        self.spec = spec
+        self.desc = make_desc(spec, max_tokens, act_scale_x, act_scale_h)
+        self.layout = capi.moe_expert_layout_for(self.desc)
+        self.h = capi.moe_layer_create(self.desc)
+        self.pool: Optional[torch.Tensor] = None
+
+    def close(self) -> None:
+        if self.h:
+            capi.moe_layer_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def expert_bytes(self) -> int:
+        return self.layout.bytes
+
+    def set_router(self, W_r: np.ndarray, bias: Optional[np.ndarray]) -> None:
+        W = np.ascontiguousarray(W_r, dtype=np.float32)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        capi.moe_set_router(self.h, W.ctypes.data, None if b is None else b.ctypes.data)
+
+    def load_host_pool(self, experts_fn: Callable[[int], Dict[str, Matrix]]) -> None:
+        """Pack all E experts into a pinned pool and register it."""
+        nb = self.layout.bytes
+        self.pool = torch.empty(self.spec.E * nb, dtype=torch.uint8, pin_memory=True)
+        view = self.pool.numpy()
+        for e in range(self.spec.E):
+            pack_expert(self.layout, experts_fn(e), view[e * nb:(e + 1) * nb])
+        capi.moe_register_host_experts(self.h, self.pool.data_ptr(), self.pool.numel())
+
+    def set_shared(self, w: Dict[str, Matrix]) -> None:
+        buf = np.zeros(self.layout.bytes, dtype=np.uint8)
+        pack_expert(self.layout, w, buf)
+        capi.moe_set_shared_expert(self.h, buf.ctypes.data)
+
+    def install(self, expert: int, slot: int, stream=None) -> None:
+        capi.moe_cache_install(self.h, expert, slot, stream)
+
+    def install_all(self) -> None:
+        """Expert e into slot e (a cache that holds every expert)."""
+        for e in range(self.spec.E):
+            self.install(e, e)
+        torch.cuda.synchronize()
+
+    def forward(self, x, y=None, stream=None, regime: int = capi.MOE_REGIME_AUTO):
+        N = x.shape[0]
+        if y is None:
+            y = torch.empty((N, self.spec.d_model), dtype=torch.bfloat16, device=x.device)
+        info = capi.moe_forward(self.h, x, N, y, stream, regime)
+        return y, info
+
+
+def build_layer(spec: LayerSpec, seed: int, max_tokens: int, experts_fn=None,
+                install_all: bool = False) -> MoELayer:
+    """A layer with the seeded weights of ``workloads`` (router, pool, shared)."""
+    from . import workloads as wl
+    L = MoELayer(spec, max_tokens)
+    W_r, b = wl.router_weights(spec, seed)
+    L.set_router(W_r, b)
+    fn = experts_fn or (lambda e: wl.expert_weights(spec, seed, e))
+    L.load_host_pool(fn)
+    if spec.has_shared:
+        L.set_shared(wl.expert_weights(spec, seed, 0, shared=True))
+    if install_all:
+        L.install_all()
+    return L

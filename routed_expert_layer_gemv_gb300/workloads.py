@@ -143,7 +143,7 @@ class Matrix:
 
 def _draw_matrix(g: np.random.Generator, rows: int, K: int, fmt: str) -> Matrix:
     # E2M1 codes uniform over all 16 values -> packed bytes uniform over 256
-    codes = g.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+    codes = np.frombuffer(g.bytes(rows * (K // 2)), dtype=np.uint8).reshape(rows, K // 2).copy()
     if fmt == MXFP4:
         # E8M0 exponent uniform over the integers -8..-4 (biased 119..123)
         scales = g.integers(127 - 8, 127 - 4 + 1, size=(rows, K // 32), dtype=np.uint8)

@@ -1,0 +1,177 @@
+"""Whole-layer parity of moe_forward against the FP64 oracle: small shapes
+spanning several row blocks and ragged expert groups, LRU misses with fills
+and overflow waves, the shared expert, NVFP4 with a router bias, determinism,
+token-permutation invariance, host buffers and the error paths."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import (CachedExperts, assert_close_layer, bf16_tensor, need_gpu, oracle_layer,
+                     reject_near_ties, small_spec)
+from oracle.lru import SlotTable
+from routed_expert_layer_gemv_gb300 import capi
+from routed_expert_layer_gemv_gb300 import workloads as wl
+from routed_expert_layer_gemv_gb300.layer import MoELayer, build_layer
+
+pytestmark = pytest.mark.gpu
+DEC = capi.MOE_REGIME_DECODE
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _tokens(spec, seed, N):
+    x, _ = wl.iid_tokens(seed, N, spec.d_model, reject_near_ties(spec, seed))
+    return x
+
+
+@pytest.mark.parametrize("spec,N", [
+    (wl.TINY.layer, 64),
+    (wl.TINY.layer, 1),
+    (small_spec(E=8, k=2, d_model=256, d_ff=512, n_slots=8, has_shared=True), 13),
+    (small_spec(E=32, k=4, d_model=512, d_ff=256, n_slots=32, fmt="nvfp4", has_shared=True,
+                has_bias=True), 21),
+    (small_spec(E=16, k=16, d_model=384, d_ff=384, n_slots=16), 3),   # k = E
+    (small_spec(E=1, k=1, d_model=256, d_ff=128, n_slots=1), 9),      # E = 1: dense SwiGLU
+])
+def test_forward_all_resident(spec, N):
+    seed = 11
+    L = build_layer(spec, seed, N, install_all=True)
+    x = _tokens(spec, seed, N)
+    y, info = L.forward(bf16_tensor(x), regime=DEC)
+    torch.cuda.synchronize()
+    assert info.host_synced == 0 and info.n_misses == 0
+    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "decode")
+    assert_close_layer(y, ref, "%s N=%d" % (spec, N))
+    L.close()
+
+
+def _decode_run(spec, seed, batch, steps, check_every=1):
+    N = batch
+    experts = CachedExperts(spec, seed, cap=96)
+    L = build_layer(spec, seed, N, experts_fn=experts)
+    O = oracle_layer(spec, seed, experts)
+    T = SlotTable(spec.E, spec.n_slots)
+    xs, _ = wl.ar1_tokens(seed, batch, steps, spec.d_model, 0.9, reject_near_ties(spec, seed))
+    tot_miss = tot_u = waves = 0
+    for t in range(steps):
+        xt = bf16_tensor(xs[t])
+        y, info = L.forward(xt, regime=DEC)
+        ref, idx, _ = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
+        acc = T.step(idx.reshape(-1))
+        assert info.host_synced == 1
+        assert info.n_distinct == len(acc)
+        assert info.n_misses == sum(1 for a in acc if not a[2])
+        assert info.fill_bytes == info.n_misses * L.expert_bytes
+        tot_miss += info.n_misses
+        tot_u += info.n_distinct
+        waves = max(waves, info.n_waves)
+        if t % check_every == 0 or t == steps - 1:
+            assert_close_layer(y, ref, "step %d" % t)
+            eo, st, clk = capi.moe_lru_get_state(L.h, spec.n_slots)
+            assert eo == T.expert_of and st == T.stamp and clk == T.clock
+    L.close()
+    return tot_miss, tot_u, waves
+
+
+def test_decode_35b_shape_with_misses():
+    # the decode layer shape, batch 4, cold cache of 47 slots: fills each step
+    spec = wl.DECODE_35B.layer
+    miss, u, waves = _decode_run(spec, 3, 4, 10)
+    assert miss > 0 and miss < u
+
+
+def test_decode_overflow_waves():
+    # batch 16 routes to more distinct experts than the 47 slots hold
+    spec = wl.DECODE_35B.layer
+    miss, u, waves = _decode_run(spec, 4, 16, 3)
+    assert waves >= 2
+
+
+def test_decode_284b_shape_shared_and_waves():
+    spec = wl.DECODE_284B.layer
+    miss, u, waves = _decode_run(spec, 5, 8, 3)
+    assert waves >= 2
+
+
+def test_decode_nvfp4_bias_small_cache():
+    spec = small_spec(E=24, k=3, d_model=512, d_ff=384, n_slots=5, fmt="nvfp4", has_shared=True,
+                      has_bias=True)
+    miss, u, waves = _decode_run(spec, 6, 3, 12)
+    assert miss > 0
+
+
+def test_deterministic_bitwise():
+    spec = wl.DECODE_35B.layer
+    x = _tokens(spec, 8, 16)
+    outs = []
+    for _ in range(2):
+        L = build_layer(spec, 8, 16)
+        for e in range(40):
+            L.install(e, e)
+        y1, _ = L.forward(bf16_tensor(x), regime=DEC)
+        y2, _ = L.forward(bf16_tensor(x), regime=DEC)
+        torch.cuda.synchronize()
+        outs += [y1.cpu(), y2.cpu()]
+        L.close()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_token_permutation_invariance_bitwise():
+    spec = small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True)
+    L = build_layer(spec, 9, 32, install_all=True)
+    x = _tokens(spec, 9, 32)
+    perm = np.random.default_rng(1).permutation(32)
+    y, _ = L.forward(bf16_tensor(x), regime=DEC)
+    yp, _ = L.forward(bf16_tensor(x[perm]), regime=DEC)
+    torch.cuda.synchronize()
+    assert torch.equal(yp.cpu().view(torch.int16), y.cpu()[perm].view(torch.int16))
+    L.close()
+
+
+def test_host_buffers_and_empty_batch():
+    spec = wl.TINY.layer
+    L = build_layer(spec, 12, 64, install_all=True)
+    x = _tokens(spec, 12, 20)
+    y_dev, _ = L.forward(bf16_tensor(x), regime=DEC)
+    xh = bf16_tensor(x, device=None).pin_memory()
+    yh = torch.empty(20, spec.d_model, dtype=torch.bfloat16).pin_memory()
+    capi.moe_forward(L.h, xh, 20, yh, None, DEC)
+    assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
+    yp = torch.empty(20, spec.d_model, dtype=torch.bfloat16)          # pageable
+    capi.moe_forward(L.h, xh, 20, yp, None, DEC)
+    assert torch.equal(yp.view(torch.int16), y_dev.cpu().view(torch.int16))
+    info = capi.moe_forward(L.h, xh, 0, yh, None, DEC)                # N = 0: no-op
+    assert info.n_tokens == 0
+    L.close()
+
+
+def test_error_paths():
+    spec = wl.TINY.layer
+    L = MoELayer(spec, 8)
+    x = torch.zeros(8, spec.d_model, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_forward(L.h, x, 8, y, None, DEC)                      # router not set
+    assert e.value.status == capi.MOE_ERR_STATE
+    W_r, b = wl.router_weights(spec, 0)
+    L.set_router(W_r, b)
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_forward(L.h, x, 8, y, None, DEC)                      # no pool, cache empty
+    assert e.value.status == capi.MOE_ERR_NOT_INSTALLED
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_forward(L.h, x, 9, y, None, DEC)                      # N > max_tokens
+    assert e.value.status == capi.MOE_ERR_ARG
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_forward(L.h, x, -1, y, None, DEC)
+    assert e.value.status == capi.MOE_ERR_ARG
+    with pytest.raises(capi.MoeError) as e:
+        L.install(0, 0)                                                # no host pool
+    assert e.value.status == capi.MOE_ERR_NOT_INSTALLED
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_set_shared_expert(L.h, x.data_ptr())                  # no shared expert
+    assert e.value.status == capi.MOE_ERR_STATE
+    L.close()
