@@ -211,6 +211,30 @@ int moe_debug_dequant(moe_layer_t layer, int slot, int m, float* out, void* stre
 int moe_debug_actquant(moe_layer_t layer, const float* v, int rows, int K,
                        uint8_t* codes, uint8_t* scales, int which, void* stream);
 
+/* ---- allocation-free permutation ----------------------------------------
+ * The FreeToken pages have no counterpart to this entry point.  It is for
+ * callers that cannot allocate GPU memory themselves: code embedded in a host
+ * framework that owns every device allocation, code running under a fixed
+ * memory budget, or code that must not call cudaMalloc because that call can
+ * synchronise the whole device.  It computes what moe_debug_permute computes
+ * (counts [E], offsets [E+1], row_of [N*k], tok_of [N*k] from the sorted top-k
+ * ids idx [N, k]; all device pointers, owned by the caller) without a layer
+ * handle and without allocating anything: its scratch is one fixed 2 MiB array
+ * in the library's device memory, held on every GPU that loads the library
+ * until the process exits.  Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32),
+ * N * k <= 262144 and ceil(N / 128) * E <= 262144; a larger request returns
+ * MOE_ERR_ARG and, when errbuf is not NULL, the reason as text in the caller's
+ * errbuf (errbuf_len bytes, NUL-terminated).  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  Every call shares the one array and finds the
+ * previous call's contents in it (each entry a call reads, that call has
+ * written first, so nothing needs clearing); calls that overlap on the GPU --
+ * on different streams or from different threads -- race, so the caller must
+ * order them.  N == 0 is a no-op.  Work is ordered on `stream`. */
+int moe_permute_noalloc(const int* idx, int N, int k, int E, int* counts, int* offsets,
+                        int* row_of, int* tok_of, void* stream, char* errbuf,
+                        size_t errbuf_len);
+
 #ifdef __cplusplus
 }
 #endif

@@ -78,6 +78,7 @@ _SIGS = {
     "moe_debug_permute": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
     "moe_debug_dequant": ([_P, _I, _I, _P, _P], _I),
     "moe_debug_actquant": ([_P, _P, _I, _I, _P, _P, _I, _P], _I),
+    "moe_permute_noalloc": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, C.c_char_p, C.c_size_t], _I),
 }
 
 _lib: Optional[C.CDLL] = None
@@ -237,3 +238,13 @@ def moe_debug_dequant(h, slot: int, m: int, out, stream=None) -> None:
 def moe_debug_actquant(h, v, rows: int, K: int, codes, scales, which: int = 0, stream=None) -> None:
     check(lib().moe_debug_actquant(h, _ptr(v), rows, K, _ptr(codes), _ptr(scales), which,
                                    _stream(stream)), h)
+
+
+def moe_permute_noalloc(idx, N: int, k: int, E: int, counts, offsets, row_of, tok_of,
+                        stream=None) -> None:
+    """The permutation without a layer handle and without allocating (see moe.h)."""
+    err = C.create_string_buffer(256)
+    rc = lib().moe_permute_noalloc(_ptr(idx), N, k, E, _ptr(counts), _ptr(offsets),
+                                   _ptr(row_of), _ptr(tok_of), _stream(stream), err, len(err))
+    if rc != MOE_OK:
+        raise MoeError(rc, err.value.decode())

@@ -14,6 +14,9 @@
 // lane walks its k experts in step with e).  Popcounts of those ballots give
 // the per-block histogram and each pair's rank inside the block; a scan over
 // blocks and experts gives the final rows.  No atomics anywhere.
+#include <cstdio>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -204,3 +207,74 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------- no-alloc entry
+// Scratch of moe_permute_noalloc (block histograms, then in-block ranks) lives
+// in a file-scope device array, so the call never allocates.  In host code the
+// array's name is only a host-side stand-in; each device's real address is
+// looked up once with cudaGetSymbolAddress and passed to the kernels.
+namespace {
+
+constexpr size_t kNoAllocInts = 2u * 262144u;  // 2 MiB of int
+static __device__ __align__(256) int g_noalloc_scratch[kNoAllocInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_fail(int code, const char* msg, char* errbuf, size_t errbuf_len) {
+  if (errbuf && errbuf_len > 0) snprintf(errbuf, errbuf_len, "%s", msg);
+  return code;
+}
+
+}  // namespace
+
+extern "C" int moe_permute_noalloc(const int* idx, int N, int k, int E, int* counts, int* offsets,
+                                   int* row_of, int* tok_of, void* stream, char* errbuf,
+                                   size_t errbuf_len) {
+  if (errbuf && errbuf_len > 0) errbuf[0] = '\0';
+  if (E < 1 || E > moe::kMaxE)
+    return noalloc_fail(MOE_ERR_ARG, "E must be in [1, 1024]", errbuf, errbuf_len);
+  if (k < 1 || k > E || k > moe::kMaxK)
+    return noalloc_fail(MOE_ERR_ARG, "k must be in [1, min(E, 32)]", errbuf, errbuf_len);
+  if (N < 0) return noalloc_fail(MOE_ERR_ARG, "N must be >= 0", errbuf, errbuf_len);
+  if (N == 0) return MOE_OK;
+  if ((long long)N * k > 262144)
+    return noalloc_fail(MOE_ERR_ARG, "N * k exceeds the 262144 pairs the static scratch holds",
+                        errbuf, errbuf_len);
+  const long long nblk = (N + 127) / 128;
+  if (nblk * E > 262144)
+    return noalloc_fail(MOE_ERR_ARG,
+                        "ceil(N / 128) * E exceeds the 262144 histogram entries of the static scratch",
+                        errbuf, errbuf_len);
+  if (!idx || !counts || !offsets || !row_of || !tok_of)
+    return noalloc_fail(MOE_ERR_ARG, "NULL pointer", errbuf, errbuf_len);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return noalloc_fail(MOE_ERR_CUDA, "cudaGetDevice failed or device index too large", errbuf,
+                        errbuf_len);
+  }
+  int* scratch = nullptr;
+  {
+    // set-up, once per device, with that device current
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return noalloc_fail(MOE_ERR_CUDA, cudaGetErrorString(e), errbuf, errbuf_len);
+      }
+      g_noalloc_ptr[dev] = static_cast<int*>(p);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  moe::Geo g{};
+  g.E = E;
+  g.k = k;
+  cudaError_t e = moe::launch_permute(g, idx, N, counts, offsets, row_of, tok_of, scratch,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return noalloc_fail(MOE_ERR_CUDA, cudaGetErrorString(e), errbuf, errbuf_len);
+  return MOE_OK;
+}
