@@ -1,24 +1,25 @@
-// Decode expert FFN: grouped GEMV over the experts of one work range, read
-// through the slot table, FP4 weights dequantised in registers.
+// Decode expert FFN: split-K grouped GEMV over the experts of one work range,
+// read through the slot table, FP4 weights dequantised in registers.
 //
 // Decode moves each routed expert's weights once per step for a handful of
 // tokens, so the kernel is bound by HBM bandwidth (the pages' decode is bound
 // by the bytes each step must move: "FreeToken：把 284B MoE 塞进游戏 PC",
 // zhichai.net, §二 "Decode" paragraph).  Design:
-//  * work unit = (expert entry, block of output rows); one CTA per unit, grid
-//    sized for the most entries a range can hold, extra CTAs exit at once, so
-//    a launch needs no host knowledge of the routing (the range is resolved
-//    from the step record on the device);
-//  * each lane owns fixed 16-byte chunks (32 E2M1 codes = one MXFP4 block, or
-//    two NVFP4 blocks) of a row and issues all its 128-bit loads before the
-//    activations are staged, so the weight stream is in flight meanwhile;
-//  * codes -> f16x2 with cvt.rn.f16x2.e2m1x2 (exact), products with the
-//    sm_100+ mixed fma.rn.f32.f16 into fp32, block scale applied per chunk;
-//  * activations live in shared memory as f16, scaled per token by a power of
-//    two (amax in [2^14, 2^15)) so no value overflows; the 16-byte pieces are
-//    XOR-swizzled so the 8 lanes of a shared-memory phase hit distinct banks;
-//  * row sums are reduced across the G lanes of a row with shuffles, in a
-//    fixed order (deterministic).
+//  * CTA = (expert entry, 16 output rows); its KS warps split K, each warp
+//    owning kTPW tiles of 128 K, so a CTA has all of its weight loads in flight
+//    before it touches the activations; partial sums are reduced across the
+//    warps in shared memory in a fixed order (deterministic);
+//  * the token dimension goes through tensor-core MMAs (mma.sync m16n8k16,
+//    f16 x f16 -> f32): the 4 lanes of a row each load one 32-bit word of every
+//    16-byte chunk (32 E2M1 codes = one MXFP4 block), convert it with
+//    cvt.rn.f16x2.e2m1x2 (exact) straight into the A fragment, and the
+//    activations are staged in shared memory in the matching permuted K order,
+//    so no lane exchanges are needed and every MMA stays inside one scale
+//    block.  Instructions per byte of weight are flat up to 8 tokens per MMA;
+//  * the block scale is applied to each block's MMA sum in fp32; NVFP4 blocks
+//    (16 codes) split each MMA into two lane-masked halves;
+//  * activations are converted to f16 with a per-token power-of-two scale
+//    (amax in [2^14, 2^15)), undone after the reduction, so nothing overflows.
 // Phase 1: a = W_g x, u = W_u x, h = SiLU(a) * u  (fp32, [rows, d_ff]).
 // Phase 2: O = W_d h                           (fp32, [rows, d_model]).
 #include "common.cuh"
@@ -27,28 +28,30 @@ namespace moe {
 
 namespace {
 
-constexpr int kGemvWarps = 8;
-constexpr int kGemvThreads = kGemvWarps * 32;
+constexpr int kMaxWarps = 16;
 
-MOE_DEV uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+MOE_DEV uint32_t ldg32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
-// two mixed-precision FMAs from packed f16 pairs
-MOE_DEV void fma2(float& acc, uint32_t w2, uint32_t x2) {
-  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
-      "mov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-      "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
-      : "+f"(acc) : "r"(w2), "r"(x2));
+MOE_DEV uint2 ldg64(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
 }
 
-// physical 16-byte slot of logical piece q (0..3) of chunk c in a token row
-MOE_DEV int swz(int c, int q) { return 4 * c + (q ^ ((c >> 1) & 3)); }
-
 MOE_DEV float pow2i(int s) { return __int_as_float((127 + s) << 23); }  // |s| <= 126
+
+MOE_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint2 b, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
+}
 
 struct Entry {
   const uint8_t* w;
@@ -89,147 +92,202 @@ MOE_DEV int row_token(const GemvArgs& a, const Entry& en, int row) {
   return en.shared ? row - en.row0 : a.tok_of[row];
 }
 
-// Dot products of one 16-byte weight chunk with T token pieces in shared
-// memory; adds (scaled) into acc[t].
-template <int T>
-MOE_DEV void chunk_fma(const uint4& w, const uint4* xs, int xstride, int c, int n,
-                       int fmt, uint32_t sc, float* acc) {
-  uint32_t wh[16];
-  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) wh[4 * q + b] = e2m1x2_to_f16x2((ww[q] >> (8 * b)) & 0xffu);
-  float s0, s1;
-  if (fmt == MOE_MXFP4) { s0 = e8m0_to_f32(sc & 0xffu); s1 = s0; }
-  else { s0 = e4m3_to_f32(sc & 0xffu); s1 = e4m3_to_f32((sc >> 8) & 0xffu); }
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    if (t < n) {
-      float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 xv = xs[(size_t)t * xstride + swz(c, q)];
-        float& p = q < 2 ? p0 : p1;
-        fma2(p, wh[4 * q + 0], xv.x);
-        fma2(p, wh[4 * q + 1], xv.y);
-        fma2(p, wh[4 * q + 2], xv.z);
-        fma2(p, wh[4 * q + 3], xv.w);
-      }
-      acc[t] = fmaf(p0, s0, fmaf(p1, s1, acc[t]));
-    }
-  }
-}
+// One warp's slice of a matrix: rows (g, g+8) of a 16-row group, TPW tiles of
+// 128 K.  w[t][h][c] = the lane's word q of 16-byte chunk c (codes 8q..8q+7 of
+// that 32-code block); s[t][h] = the tile's scale bytes of that row.
+template <int FMT, int TPW>
+struct Slice {
+  uint32_t w[TPW][2][4];
+  uint32_t s[TPW][2][FMT == MOE_MXFP4 ? 1 : 2];
+};
 
-MOE_DEV float group_sum(float v, int G) {
-  for (int o = G >> 1; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-MOE_DEV uint32_t load_scale(const uint8_t* sp, int fmt) {
-  if (fmt == MOE_MXFP4) return *sp;
-  return *reinterpret_cast<const uint16_t*>(sp);
-}
-
-// ---------------------------------------------------------------- phase 1
-// Unit = (entry, 8 warps x (32/G) rows of d_ff).  A lane keeps up to kCPLM
-// chunks of its gate row and of its up row in registers; longer rows loop.
-constexpr int kCPLM = 4;
-
-template <int T>
-MOE_DEV void stage_x(const GemvArgs& a, const Entry& en, const __nv_bfloat16* __restrict__ x,
-                     const int* __restrict__ xexp, int K, int t0, int n, uint4* xs, int* sexp_s) {
-  const int xstride = K / 8;
-  for (int v = threadIdx.x; v < n * xstride; v += kGemvThreads) {
-    const int t = v / xstride, L = v % xstride;
-    const int tok = row_token(a, en, en.row0 + t0 + t);
-    const uint4 raw = reinterpret_cast<const uint4*>(x + (size_t)tok * K)[L];
-    const int s = xexp[tok];
-    if (L == 0) sexp_s[t] = s;
-    const float sc = pow2i(-s);
-    const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t o[4];
+template <int FMT, int TPW>
+MOE_DEV void load_slice(Slice<FMT, TPW>& sl, const uint8_t* codes, const uint8_t* scales, int K,
+                        int row, int kt0, int nkt, int q) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = __uint_as_float(rw[i] << 16) * sc;
-      const float hi = __uint_as_float(rw[i] & 0xffff0000u) * sc;
-      const __half2 hh = __floats2half2_rn(lo, hi);
-      o[i] = *reinterpret_cast<const uint32_t*>(&hh);
-    }
-    xs[(size_t)t * xstride + swz(L >> 2, L & 3)] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-template <int T>
-__global__ void __launch_bounds__(kGemvThreads)
-gemv_gateup_kernel(Geo g, GemvArgs a, const __nv_bfloat16* __restrict__ x,
-                   const int* __restrict__ xexp, float* __restrict__ h) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
-  __shared__ int sexp_s[T];
-  const int K = g.d;
-  const int chunks = K / 32;
-  const int G = min(32, chunks & -chunks);      // lanes per row (power of 2)
-  const int cpl = chunks / G;                   // chunks per lane
-  const int rpw = 32 / G;                       // rows per warp
-  const int rpc = kGemvWarps * rpw;             // rows per CTA
-  const int upe = g.f / rpc;                    // units per entry
-  const int ent = blockIdx.x / upe, rb = blockIdx.x % upe;
-  Entry en;
-  if (!get_entry(g, a, ent, en)) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r = rb * rpc + warp * rpw + lane / G;   // row of d_ff
-  const int sbpc = g.fmt == MOE_MXFP4 ? 1 : 2;      // scale bytes per chunk
-  const uint8_t* gc = en.w + g.off_codes[0] + (size_t)r * (K / 2);
-  const uint8_t* uc = en.w + g.off_codes[1] + (size_t)r * (K / 2);
-  const uint8_t* gs = en.w + g.off_scales[0] + (size_t)r * (K / g.blk);
-  const uint8_t* us = en.w + g.off_scales[1] + (size_t)r * (K / g.blk);
-  uint4 wg[kCPLM], wu[kCPLM];
-  uint32_t sg[kCPLM], su[kCPLM];
-  auto load = [&](int j0) {
+  for (int t = 0; t < TPW; ++t) {
+    if (t < nkt) {
+      const int kt = kt0 + t;
 #pragma unroll
-    for (int j = 0; j < kCPLM; ++j) {
-      if (j0 + j < cpl) {
-        const int c = (lane % G) + G * (j0 + j);
-        wg[j] = ldg_stream(gc + (size_t)c * 16);
-        wu[j] = ldg_stream(uc + (size_t)c * 16);
-        sg[j] = load_scale(gs + (size_t)c * sbpc, g.fmt);
-        su[j] = load_scale(us + (size_t)c * sbpc, g.fmt);
-      }
-    }
-  };
-  load(0);   // the weight stream is in flight while x is staged
-  const float* ts = reinterpret_cast<const float*>(en.w + g.off_tscale);
-  const float tg = ts[0], tu = ts[1];
-  const int xstride = K / 8;
-  for (int t0 = 0; t0 < en.nrows; t0 += T) {
-    const int n = min(T, en.nrows - t0);
-    __syncthreads();
-    stage_x<T>(a, en, x, xexp, K, t0, n, xs, sexp_s);
-    __syncthreads();
-    float ag[T], au[T];
+      for (int h = 0; h < 2; ++h) {
+        const uint8_t* cb = codes + (size_t)(row + 8 * h) * (K / 2) + (size_t)kt * 64 + 4 * q;
 #pragma unroll
-    for (int t = 0; t < T; ++t) { ag[t] = 0.f; au[t] = 0.f; }
-    for (int j0 = 0; j0 < cpl; j0 += kCPLM) {
-      if (t0 > 0 || j0 > 0) load(j0);
-#pragma unroll
-      for (int j = 0; j < kCPLM; ++j) {
-        if (j0 + j < cpl) {
-          const int c = (lane % G) + G * (j0 + j);
-          chunk_fma<T>(wg[j], xs, xstride, c, n, g.fmt, sg[j], ag);
-          chunk_fma<T>(wu[j], xs, xstride, c, n, g.fmt, su[j], au);
+        for (int c = 0; c < 4; ++c) sl.w[t][h][c] = ldg32(cb + 16 * c);
+        if (FMT == MOE_MXFP4) {
+          sl.s[t][h][0] = ldg32(scales + (size_t)(row + 8 * h) * (K / 32) + 4 * kt);
+        } else {
+          const uint2 v = ldg64(scales + (size_t)(row + 8 * h) * (K / 16) + 8 * kt);
+          sl.s[t][h][0] = v.x;
+          sl.s[t][h][FMT == MOE_MXFP4 ? 0 : 1] = v.y;
         }
       }
     }
+  }
+}
+
+MOE_DEV float scale_of(int fmt, uint32_t sw, int byte) {
+  const uint32_t b = (sw >> (8 * byte)) & 0xffu;
+  return fmt == MOE_MXFP4 ? e8m0_to_f32(b) : e4m3_to_f32(b);
+}
+
+// A fragments of MMA step st (0, 1) of chunk c: rows g and g+8, codes
+// 8q + 4 st .. + 3 of the chunk's block.
+template <int FMT, int TPW>
+MOE_DEV void afrag(const Slice<FMT, TPW>& sl, int t, int c, int st, uint32_t (&a)[4]) {
+  const uint32_t w0 = sl.w[t][0][c] >> (16 * st), w1 = sl.w[t][1][c] >> (16 * st);
+  a[0] = e2m1x2_to_f16x2(w0 & 0xffu);
+  a[1] = e2m1x2_to_f16x2(w1 & 0xffu);
+  a[2] = e2m1x2_to_f16x2((w0 >> 8) & 0xffu);
+  a[3] = e2m1x2_to_f16x2((w1 >> 8) & 0xffu);
+}
+
+// acc[ng] += W(16 rows, this warp's K) x B(ng) for NG token groups of 8.
+template <int FMT, int TPW, int NG>
+MOE_DEV void slice_mma(const Slice<FMT, TPW>& sl, int kt0, int nkt, const uint2* xs, int ksteps,
+                       int lane, float (&acc)[NG][4]) {
+  const int q = lane & 3;
+  const uint32_t mlo = q < 2 ? 0xffffffffu : 0u, mhi = ~mlo;
+  const float z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-      if (t < n) {
-        const float s = pow2i(sexp_s[t]);
-        const float av = group_sum(ag[t], G) * s * tg;
-        const float uv = group_sum(au[t], G) * s * tu;
-        if ((lane % G) == 0) {
-          const float silu = av / (1.0f + expf(-av));
-          h[(size_t)(en.row0 + t0 + t) * g.f + r] = silu * uv;
+  for (int t = 0; t < TPW; ++t) {
+    if (t < nkt) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int cg = (kt0 + t) * 4 + c;        // global 32-code block
+        uint32_t a0[4], a1[4];
+        afrag(sl, t, c, 0, a0);
+        afrag(sl, t, c, 1, a1);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          const uint2 b0 = xs[((size_t)ng * ksteps + 2 * cg) * 32 + lane];
+          const uint2 b1 = xs[((size_t)ng * ksteps + 2 * cg + 1) * 32 + lane];
+          if (FMT == MOE_MXFP4) {
+            float d[4];
+            mma16816(d, a0, b0, z);
+            mma16816(d, a1, b1, d);
+            const float s0 = scale_of(FMT, sl.s[t][0][0], c), s1 = scale_of(FMT, sl.s[t][1][0], c);
+            acc[ng][0] = fmaf(d[0], s0, acc[ng][0]);
+            acc[ng][1] = fmaf(d[1], s0, acc[ng][1]);
+            acc[ng][2] = fmaf(d[2], s1, acc[ng][2]);
+            acc[ng][3] = fmaf(d[3], s1, acc[ng][3]);
+          } else {
+            // lanes q < 2 hold codes of 16-block 2c, lanes q >= 2 of block 2c+1
+            uint32_t l0[4], l1[4], h0[4], h1[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              l0[i] = a0[i] & mlo; l1[i] = a1[i] & mlo;
+              h0[i] = a0[i] & mhi; h1[i] = a1[i] & mhi;
+            }
+            float dl[4], dh[4];
+            mma16816(dl, l0, b0, z);
+            mma16816(dl, l1, b1, dl);
+            mma16816(dh, h0, b0, z);
+            mma16816(dh, h1, b1, dh);
+            const int wb = c >> 1, by = 2 * (c & 1);   // sub-blocks 2c, 2c+1 of the tile
+            const float sl0 = scale_of(FMT, sl.s[t][0][wb], by), sh0 = scale_of(FMT, sl.s[t][0][wb], by + 1);
+            const float sl1 = scale_of(FMT, sl.s[t][1][wb], by), sh1 = scale_of(FMT, sl.s[t][1][wb], by + 1);
+            acc[ng][0] = fmaf(dl[0], sl0, fmaf(dh[0], sh0, acc[ng][0]));
+            acc[ng][1] = fmaf(dl[1], sl0, fmaf(dh[1], sh0, acc[ng][1]));
+            acc[ng][2] = fmaf(dl[2], sl1, fmaf(dh[2], sh1, acc[ng][2]));
+            acc[ng][3] = fmaf(dl[3], sl1, fmaf(dh[3], sh1, acc[ng][3]));
+          }
+        }
+      }
+    }
+  }
+}
+
+// Shared-memory slot of 4 consecutive activation values (real K k0, token tl)
+// in B-fragment order: [group][k-step][lane] x 8 bytes, k-step = 2 * block +
+// step, lane = 4 * token + q with k0 = 32 block + 8 q + 4 step.
+MOE_DEV int frag_slot(int tl, int k0, int ksteps) {
+  const int c = k0 >> 5, r = k0 & 31;
+  const int q = r >> 3, st = (r >> 2) & 1;
+  return ((tl >> 3) * ksteps + 2 * c + st) * 32 + 4 * (tl & 7) + q;
+}
+
+MOE_DEV uint2 to_f16x4(float a, float b, float c, float d) {
+  const __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
+  uint2 o;
+  o.x = *reinterpret_cast<const uint32_t*>(&lo);
+  o.y = *reinterpret_cast<const uint32_t*>(&hi);
+  return o;
+}
+
+// ---------------------------------------------------------------- phase 1
+template <int FMT, int TPW, int NG>
+__global__ void __launch_bounds__(kMaxWarps * 32)
+gemv_gateup_kernel(Geo g, GemvArgs a, const __nv_bfloat16* __restrict__ x,
+                   const int* __restrict__ xexp, float* __restrict__ h) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int sexp[8 * NG];
+  const int K = g.d, ksteps = K / 16, nkt_all = K / 128;
+  const int KS = blockDim.x >> 5;
+  const int rgs = g.f / 16;
+  const int ent = blockIdx.x / rgs, rg = blockIdx.x % rgs;
+  Entry en;
+  if (!get_entry(g, a, ent, en)) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = lane & 3;
+  const int kt0 = warp * TPW, nkt = min(TPW, nkt_all - kt0);
+  const int row = rg * 16 + (lane >> 2);
+  Slice<FMT, TPW> sg, su;
+  load_slice(sg, en.w + g.off_codes[0], en.w + g.off_scales[0], K, row, kt0, nkt, q);
+  load_slice(su, en.w + g.off_codes[1], en.w + g.off_scales[1], K, row, kt0, nkt, q);
+  const float* ts = reinterpret_cast<const float*>(en.w + g.off_tscale);
+  const float tsg = ts[0], tsu = ts[1];
+  uint2* xs = reinterpret_cast<uint2*>(smem);
+  float* red = reinterpret_cast<float*>(smem + (size_t)NG * ksteps * 256);
+  const int rstride = NG * 8 + 1;
+  for (int t0 = 0; t0 < en.nrows; t0 += 8 * NG) {
+    const int n = min(8 * NG, en.nrows - t0);
+    if (t0 > 0) {
+      __syncthreads();
+      load_slice(sg, en.w + g.off_codes[0], en.w + g.off_scales[0], K, row, kt0, nkt, q);
+      load_slice(su, en.w + g.off_codes[1], en.w + g.off_scales[1], K, row, kt0, nkt, q);
+    }
+    // stage x (bf16 -> f16 scaled by 2^-xexp) in B-fragment order
+    for (int v = threadIdx.x; v < n * (K / 4); v += blockDim.x) {
+      const int tl = v / (K / 4), k0 = (v % (K / 4)) * 4;
+      const int tok = row_token(a, en, en.row0 + t0 + tl);
+      const int s = xexp[tok];
+      if (k0 == 0) sexp[tl] = s;
+      const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)tok * K + k0);
+      const float sc = pow2i(-s);
+      xs[frag_slot(tl, k0, ksteps)] =
+          to_f16x4(__uint_as_float(raw.x << 16) * sc, __uint_as_float(raw.x & 0xffff0000u) * sc,
+                   __uint_as_float(raw.y << 16) * sc, __uint_as_float(raw.y & 0xffff0000u) * sc);
+    }
+    __syncthreads();
+    float ag[NG][4], au[NG][4];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) { ag[ng][j] = 0.f; au[ng][j] = 0.f; }
+    slice_mma<FMT, TPW, NG>(sg, kt0, nkt, xs, ksteps, lane, ag);
+    slice_mma<FMT, TPW, NG>(su, kt0, nkt, xs, ksteps, lane, au);
+    float* my = red + (size_t)(warp * 32 + lane) * rstride;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) { my[ng * 8 + j] = ag[ng][j]; my[ng * 8 + 4 + j] = au[ng][j]; }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tk = 8 * ng + 2 * q + (j & 1);
+          const int r = row + 8 * (j >> 1);
+          float sa = 0.f, su_ = 0.f;
+          for (int w = 0; w < KS; ++w) {
+            sa += red[(size_t)(w * 32 + lane) * rstride + ng * 8 + j];
+            su_ += red[(size_t)(w * 32 + lane) * rstride + ng * 8 + 4 + j];
+          }
+          if (tk < n) {
+            const float sc = pow2i(sexp[tk]);
+            const float av = sa * sc * tsg, uv = su_ * sc * tsu;
+            h[(size_t)(en.row0 + t0 + tk) * g.f + r] = av / (1.0f + expf(-av)) * uv;
+          }
         }
       }
     }
@@ -237,59 +295,35 @@ gemv_gateup_kernel(Geo g, GemvArgs a, const __nv_bfloat16* __restrict__ x,
 }
 
 // ---------------------------------------------------------------- phase 2
-// Unit = (entry, 8 warps x (32/G) x kP2 rows of d_model).  h rows staged as
-// f16 with a per-row power-of-two scale (computed here from the row's amax).
-constexpr int kP2 = 2;
-
-template <int T>
-__global__ void __launch_bounds__(kGemvThreads)
+template <int FMT, int TPW, int NG>
+__global__ void __launch_bounds__(kMaxWarps * 32)
 gemv_down_kernel(Geo g, GemvArgs a, const float* __restrict__ h, float* __restrict__ O) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw);
-  __shared__ int sexp_s[T];
-  const int K = g.f;
-  const int chunks = K / 32;
-  const int G = min(32, chunks & -chunks);
-  const int cpl = chunks / G;
-  const int rpw = 32 / G;
-  const int rpc = kGemvWarps * rpw * kP2;
-  const int upe = g.d / rpc;
-  const int ent = blockIdx.x / upe, rb = blockIdx.x % upe;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int sexp[8 * NG];
+  const int K = g.f, ksteps = K / 16, nkt_all = K / 128;
+  const int KS = blockDim.x >> 5;
+  const int rgs = g.d / 16;
+  const int ent = blockIdx.x / rgs, rg = blockIdx.x % rgs;
   Entry en;
   if (!get_entry(g, a, ent, en)) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sbpc = g.fmt == MOE_MXFP4 ? 1 : 2;
-  const uint8_t* dc[kP2];
-  const uint8_t* ds[kP2];
-  int rows[kP2];
-#pragma unroll
-  for (int p = 0; p < kP2; ++p) {
-    rows[p] = rb * rpc + (p * kGemvWarps + warp) * rpw + lane / G;
-    dc[p] = en.w + g.off_codes[2] + (size_t)rows[p] * (K / 2);
-    ds[p] = en.w + g.off_scales[2] + (size_t)rows[p] * (K / g.blk);
-  }
-  uint4 wd[kP2][kCPLM];
-  uint32_t sd[kP2][kCPLM];
-  auto load = [&](int j0) {
-#pragma unroll
-    for (int p = 0; p < kP2; ++p)
-#pragma unroll
-      for (int j = 0; j < kCPLM; ++j)
-        if (j0 + j < cpl) {
-          const int c = (lane % G) + G * (j0 + j);
-          wd[p][j] = ldg_stream(dc[p] + (size_t)c * 16);
-          sd[p][j] = load_scale(ds[p] + (size_t)c * sbpc, g.fmt);
-        }
-  };
-  load(0);
-  const float td = reinterpret_cast<const float*>(en.w + g.off_tscale)[2];
-  const int xstride = K / 8;
-  for (int t0 = 0; t0 < en.nrows; t0 += T) {
-    const int n = min(T, en.nrows - t0);
-    __syncthreads();
-    // one warp per token: amax, exponent, f16 conversion into shared memory
-    for (int t = warp; t < n; t += kGemvWarps) {
-      const float* hr = h + (size_t)(en.row0 + t0 + t) * K;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = lane & 3;
+  const int kt0 = warp * TPW, nkt = min(TPW, nkt_all - kt0);
+  const int row = rg * 16 + (lane >> 2);
+  Slice<FMT, TPW> sd;
+  load_slice(sd, en.w + g.off_codes[2], en.w + g.off_scales[2], K, row, kt0, nkt, q);
+  const float tsd = reinterpret_cast<const float*>(en.w + g.off_tscale)[2];
+  uint2* xs = reinterpret_cast<uint2*>(smem);
+  float* red = reinterpret_cast<float*>(smem + (size_t)NG * ksteps * 256);
+  const int rstride = NG * 4 + 1;
+  for (int t0 = 0; t0 < en.nrows; t0 += 8 * NG) {
+    const int n = min(8 * NG, en.nrows - t0);
+    if (t0 > 0) {
+      __syncthreads();
+      load_slice(sd, en.w + g.off_codes[2], en.w + g.off_scales[2], K, row, kt0, nkt, q);
+    }
+    // per-row power-of-two exponent of h, then h -> f16 in B-fragment order
+    for (int tl = warp; tl < n; tl += KS) {
+      const float* hr = h + (size_t)(en.row0 + t0 + tl) * K;
       float m = 0.f;
       for (int i = lane; i < K; i += 32) m = fmaxf(m, fabsf(hr[i]));
       for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -299,97 +333,139 @@ gemv_down_kernel(Geo g, GemvArgs a, const float* __restrict__ h, float* __restri
         frexpf(m, &ex);
         s = max(-100, min(100, ex - 15));
       }
-      if (lane == 0) sexp_s[t] = s;
-      const float sc = pow2i(-s);
-      for (int L = lane; L < xstride; L += 32) {
-        const float4 v0 = reinterpret_cast<const float4*>(hr)[2 * L];
-        const float4 v1 = reinterpret_cast<const float4*>(hr)[2 * L + 1];
-        const __half2 a0 = __floats2half2_rn(v0.x * sc, v0.y * sc);
-        const __half2 a1 = __floats2half2_rn(v0.z * sc, v0.w * sc);
-        const __half2 a2 = __floats2half2_rn(v1.x * sc, v1.y * sc);
-        const __half2 a3 = __floats2half2_rn(v1.z * sc, v1.w * sc);
-        xs[(size_t)t * xstride + swz(L >> 2, L & 3)] =
-            make_uint4(*reinterpret_cast<const uint32_t*>(&a0), *reinterpret_cast<const uint32_t*>(&a1),
-                       *reinterpret_cast<const uint32_t*>(&a2), *reinterpret_cast<const uint32_t*>(&a3));
-      }
+      if (lane == 0) sexp[tl] = s;
     }
     __syncthreads();
-    float acc[kP2][T];
-#pragma unroll
-    for (int p = 0; p < kP2; ++p)
-#pragma unroll
-      for (int t = 0; t < T; ++t) acc[p][t] = 0.f;
-    for (int j0 = 0; j0 < cpl; j0 += kCPLM) {
-      if (t0 > 0 || j0 > 0) load(j0);
-#pragma unroll
-      for (int p = 0; p < kP2; ++p)
-#pragma unroll
-        for (int j = 0; j < kCPLM; ++j)
-          if (j0 + j < cpl) {
-            const int c = (lane % G) + G * (j0 + j);
-            chunk_fma<T>(wd[p][j], xs, xstride, c, n, g.fmt, sd[p][j], acc[p]);
-          }
+    for (int v = threadIdx.x; v < n * (K / 4); v += blockDim.x) {
+      const int tl = v / (K / 4), k0 = (v % (K / 4)) * 4;
+      const float4 hv = *reinterpret_cast<const float4*>(h + (size_t)(en.row0 + t0 + tl) * K + k0);
+      const float sc = pow2i(-sexp[tl]);
+      xs[frag_slot(tl, k0, ksteps)] = to_f16x4(hv.x * sc, hv.y * sc, hv.z * sc, hv.w * sc);
     }
+    __syncthreads();
+    float acc[NG][4];
 #pragma unroll
-    for (int p = 0; p < kP2; ++p)
+    for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
-      for (int t = 0; t < T; ++t)
-        if (t < n) {
-          const float v = group_sum(acc[p][t], G) * pow2i(sexp_s[t]) * td;
-          if ((lane % G) == 0) O[(size_t)(en.row0 + t0 + t) * g.d + rows[p]] = v;
+      for (int j = 0; j < 4; ++j) acc[ng][j] = 0.f;
+    slice_mma<FMT, TPW, NG>(sd, kt0, nkt, xs, ksteps, lane, acc);
+    float* my = red + (size_t)(warp * 32 + lane) * rstride;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) my[ng * 4 + j] = acc[ng][j];
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tk = 8 * ng + 2 * q + (j & 1);
+          const int r = row + 8 * (j >> 1);
+          float sum = 0.f;
+          for (int w = 0; w < KS; ++w) sum += red[(size_t)(w * 32 + lane) * rstride + ng * 4 + j];
+          if (tk < n) O[(size_t)(en.row0 + t0 + tk) * g.d + r] = sum * pow2i(sexp[tk]) * tsd;
         }
+      }
+    }
   }
 }
 
-int tok_bucket(int N) { return N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : 8; }
+// Warps per CTA and tiles per warp for a K: the fewest tiles per warp (2 or
+// 4) that keep the CTA at <= kMaxWarps warps.
+void split_k(int K, int* ks, int* tpw) {
+  const int nkt = K / 128;
+  *tpw = (nkt + 1) / 2 <= kMaxWarps ? 2 : 4;
+  *ks = (nkt + *tpw - 1) / *tpw;
+}
 
-template <int T>
-cudaError_t launch_t(const Geo& g, const GemvArgs& a, const __nv_bfloat16* x, const int* xexp,
-                     float* h, float* O, int n_ent_max, cudaStream_t st, const cudaEvent_t* ev) {
+size_t smem_bytes(int K, int ks, int ng, int per_token_vals) {
+  return (size_t)ng * (K / 16) * 256 + (size_t)ks * 32 * (ng * per_token_vals + 1) * 4;
+}
+
+template <int FMT, int TPW, int NG>
+cudaError_t launch_fmt(const Geo& g, const GemvArgs& a, const __nv_bfloat16* x, const int* xexp,
+                       float* h, float* O, int n_ent_max, cudaStream_t st, const cudaEvent_t* ev,
+                       int phase_mask) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(gemv_gateup_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    cudaFuncSetAttribute(gemv_down_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaError_t e1 = cudaFuncSetAttribute(gemv_gateup_kernel<FMT, TPW, NG>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    cudaError_t e2 = cudaFuncSetAttribute(gemv_down_kernel<FMT, TPW, NG>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e1 != cudaSuccess) return e1;
+    if (e2 != cudaSuccess) return e2;
     attr_set = true;
   }
-  const int c1 = g.d / 32, G1 = min(32, c1 & -c1);
-  const int grid1 = n_ent_max * (g.f / (kGemvWarps * (32 / G1)));
-  if (ev) cudaEventRecord(ev[0], st);
-  if (grid1 > 0)
-    gemv_gateup_kernel<T><<<grid1, kGemvThreads, (size_t)T * g.d * 2, st>>>(g, a, x, xexp, h);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = cudaSuccess;
+  if (phase_mask & 1) {
+    int ks, tpw;
+    split_k(g.d, &ks, &tpw);
+    const int grid = n_ent_max * (g.f / 16);
+    if (ev) cudaEventRecord(ev[0], st);
+    if (grid > 0)
+      gemv_gateup_kernel<FMT, TPW, NG><<<grid, ks * 32, smem_bytes(g.d, ks, NG, 8), st>>>(g, a, x, xexp, h);
+    err = cudaGetLastError();
+    if (ev) cudaEventRecord(ev[1], st);
+    if (err != cudaSuccess) return err;
+  }
+  if (phase_mask & 2) {
+    int ks, tpw;
+    split_k(g.f, &ks, &tpw);
+    const int grid = n_ent_max * (g.d / 16);
+    if (ev) cudaEventRecord(ev[2], st);
+    if (grid > 0)
+      gemv_down_kernel<FMT, TPW, NG><<<grid, ks * 32, smem_bytes(g.f, ks, NG, 4), st>>>(g, a, h, O);
+    err = cudaGetLastError();
+    if (ev) cudaEventRecord(ev[3], st);
+  }
+  return err;
+}
+
+template <int FMT, int NG>
+cudaError_t launch_ng(const Geo& g, const GemvArgs& a, const __nv_bfloat16* x, const int* xexp,
+                      float* h, float* O, int n_ent_max, cudaStream_t st, const cudaEvent_t* ev) {
+  // the two phases may need different tiles per warp (K = d_model, then d_ff)
+  int ks1, tpw1, ks2, tpw2;
+  split_k(g.d, &ks1, &tpw1);
+  split_k(g.f, &ks2, &tpw2);
+  cudaError_t err = tpw1 == 2 ? launch_fmt<FMT, 2, NG>(g, a, x, xexp, h, O, n_ent_max, st, ev, 1)
+                              : launch_fmt<FMT, 4, NG>(g, a, x, xexp, h, O, n_ent_max, st, ev, 1);
   if (err != cudaSuccess) return err;
-  if (ev) cudaEventRecord(ev[1], st);
-  const int c2 = g.f / 32, G2 = min(32, c2 & -c2);
-  const int grid2 = n_ent_max * (g.d / (kGemvWarps * (32 / G2) * kP2));
-  if (ev) cudaEventRecord(ev[2], st);
-  if (grid2 > 0) gemv_down_kernel<T><<<grid2, kGemvThreads, (size_t)T * g.f * 2, st>>>(g, a, h, O);
-  if (ev) cudaEventRecord(ev[3], st);
-  return cudaGetLastError();
+  return tpw2 == 2 ? launch_fmt<FMT, 2, NG>(g, a, x, xexp, h, O, n_ent_max, st, ev, 2)
+                   : launch_fmt<FMT, 4, NG>(g, a, x, xexp, h, O, n_ent_max, st, ev, 2);
+}
+
+int pick_ng(const Geo& g, int N) {
+  if (N <= 8) return 1;
+  int ks, tpw;
+  split_k(g.d, &ks, &tpw);
+  return smem_bytes(g.d, ks, 2, 8) <= 200 * 1024 ? 2 : 1;
 }
 
 }  // namespace
 
-// Shapes the decode kernels accept: the CTA row blocks must tile d_ff (phase
-// 1) and d_model (phase 2) exactly, and 8 staged token rows must fit in
-// shared memory.
+// Shapes the decode kernels accept: K = d_model and d_ff up to 8192 (16 warps
+// x 4 tiles of 128) and the staged activations of one token group in shared
+// memory.
 bool gemv_shape_ok(const Geo& g) {
-  const int c1 = g.d / 32, c2 = g.f / 32;
-  const int G1 = min(32, c1 & -c1), G2 = min(32, c2 & -c2);
-  if (g.f % (kGemvWarps * (32 / G1)) != 0) return false;
-  if (g.d % (kGemvWarps * (32 / G2) * kP2) != 0) return false;
-  return (size_t)8 * (size_t)(g.d > g.f ? g.d : g.f) * 2 <= 200 * 1024;
+  if (g.d > 8192 || g.f > 8192) return false;
+  int ks, tpw;
+  split_k(g.d, &ks, &tpw);
+  if (smem_bytes(g.d, ks, 1, 8) > 220 * 1024) return false;
+  split_k(g.f, &ks, &tpw);
+  return smem_bytes(g.f, ks, 1, 4) <= 220 * 1024;
 }
 
 cudaError_t launch_gemv_decode(const Geo& g, const GemvArgs& a, const __nv_bfloat16* x,
                                const int* xexp, float* h, float* O, int n_ent_max,
                                cudaStream_t st, const cudaEvent_t* ev) {
-  switch (tok_bucket(a.N)) {
-    case 1: return launch_t<1>(g, a, x, xexp, h, O, n_ent_max, st, ev);
-    case 2: return launch_t<2>(g, a, x, xexp, h, O, n_ent_max, st, ev);
-    case 4: return launch_t<4>(g, a, x, xexp, h, O, n_ent_max, st, ev);
-    default: return launch_t<8>(g, a, x, xexp, h, O, n_ent_max, st, ev);
-  }
+  const int ng = pick_ng(g, a.N);
+  if (g.fmt == MOE_MXFP4)
+    return ng == 1 ? launch_ng<MOE_MXFP4, 1>(g, a, x, xexp, h, O, n_ent_max, st, ev)
+                   : launch_ng<MOE_MXFP4, 2>(g, a, x, xexp, h, O, n_ent_max, st, ev);
+  return ng == 1 ? launch_ng<MOE_NVFP4, 1>(g, a, x, xexp, h, O, n_ent_max, st, ev)
+                 : launch_ng<MOE_NVFP4, 2>(g, a, x, xexp, h, O, n_ent_max, st, ev);
 }
 
 }  // namespace moe

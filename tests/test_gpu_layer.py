@@ -35,6 +35,9 @@ def _tokens(spec, seed, N):
                 has_bias=True), 21),
     (small_spec(E=16, k=16, d_model=384, d_ff=384, n_slots=16), 3),   # k = E
     (small_spec(E=1, k=1, d_model=256, d_ff=128, n_slots=1), 9),      # E = 1: dense SwiGLU
+    (small_spec(E=4, k=2, d_model=6144, d_ff=256, n_slots=4, fmt="nvfp4", has_shared=True,
+                has_bias=True), 12),                                  # wide K, 2 token groups
+    (small_spec(E=4, k=2, d_model=6144, d_ff=384, n_slots=4), 3),     # wide K, odd tile count
 ])
 def test_forward_all_resident(spec, N):
     seed = 11
