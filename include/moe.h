@@ -51,7 +51,7 @@ extern "C" {
 #define MOE_NVFP4 1  /* E2M1 codes, one E4M3 scale per 16 along K, fp32/tensor */
 
 /* ---- regimes ----------------------------------------------------------- */
-#define MOE_REGIME_AUTO    0  /* decode for small N, prefill otherwise       */
+#define MOE_REGIME_AUTO    0  /* decode for N <= 64, prefill otherwise       */
 #define MOE_REGIME_DECODE  1  /* FP4 weights x bf16 activations, GEMV        */
 #define MOE_REGIME_PREFILL 2  /* FP4 weights x FP4 activations, grouped GEMM */
 
@@ -61,8 +61,8 @@ typedef struct moe_layer* moe_layer_t;
 typedef struct {
     int E;            /* routed experts, 1..1024                              */
     int k;            /* experts per token, 1..min(E, 32)                     */
-    int d_model;      /* multiple of 128                                      */
-    int d_ff;         /* multiple of 128                                      */
+    int d_model;      /* multiple of 128 (of 256 for the prefill regime)      */
+    int d_ff;         /* multiple of 128 (of 256 for the prefill regime)      */
     int n_slots;      /* GPU expert-cache slots, 1..E                         */
     int fmt;          /* MOE_MXFP4 or MOE_NVFP4                               */
     int has_shared;   /* 1: one always-on shared expert, weight 1, resident   */
@@ -103,11 +103,12 @@ typedef struct {
 #define MOE_PROF_ROUTER      0
 #define MOE_PROF_PERMUTE     1
 #define MOE_PROF_LRU         2
-#define MOE_PROF_GATEUP      3  /* expert FFN phase 1: W_g, W_u, SiLU * mul     */
+#define MOE_PROF_GATEUP      3  /* expert FFN phase 1: W_g, W_u, SiLU * mul
+                                   (decode GEMV or prefill grouped GEMM)       */
 #define MOE_PROF_DOWN        4  /* expert FFN phase 2: W_d                      */
 #define MOE_PROF_COMBINE     5
 #define MOE_PROF_FILL        6  /* host -> slot copies on the fill stream       */
-#define MOE_PROF_PREFILL     7  /* prefill grouped GEMM (both phases)           */
+#define MOE_PROF_PREFILL     7  /* prefill: activation gather + FP4 quantiser   */
 #define MOE_PROF_KINDS       8
 
 /* Layout of one expert for a descriptor (no GPU work). */

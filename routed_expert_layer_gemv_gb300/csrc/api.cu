@@ -1,7 +1,9 @@
 // Host side of the C ABI (include/moe.h): validation, device buffers, the
 // per-step launch sequence, and the host->slot fills of cache misses.
 //
-// One step of moe_forward (decode regime):
+// One step of moe_forward (decode regime; the prefill regime quantises the
+// permuted activations to FP4 first and runs the tcgen05 grouped GEMM in place
+// of the GEMV):
 //   caller stream: router -> permute -> LRU step -> [record copy to host]
 //                  -> expert GEMV over the hits (+ shared expert)
 //   host:          wait for the record, then per wave of n_slots accesses:
@@ -63,6 +65,16 @@ struct moe_layer {
   __nv_bfloat16* y_stage = nullptr;
   int* list_dev = nullptr;
   int list_cap = 0;
+  // prefill regime
+  uint8_t* xq_codes = nullptr;   // permuted FP4 activations [(rows + 128), d/2]
+  uint8_t* xq_scales = nullptr;
+  uint8_t* hq_codes = nullptr;   // FP4 h [(rows + 128), f/2]
+  uint8_t* hq_scales = nullptr;
+  void* tiles = nullptr;
+  int* n_tiles = nullptr;
+  PrefillPlan* plan = nullptr;
+  int* err_host = nullptr;       // kernels' timeout flag (mapped pinned memory)
+  int* err_dev = nullptr;
   // host state
   const uint8_t* host_pool = nullptr;
   size_t host_pool_bytes = 0;
@@ -180,6 +192,10 @@ void release(moe_layer* L) {
   L->dev_allocs.clear();
   if (L->pinned_rec) cudaFreeHost(L->pinned_rec);
   L->pinned_rec = nullptr;
+  if (L->err_host) cudaFreeHost(L->err_host);
+  L->err_host = nullptr;
+  if (L->plan) prefill_plan_destroy(L->plan);
+  L->plan = nullptr;
   if (L->ev_route) cudaEventDestroy(L->ev_route);
   if (L->ev_fill) cudaEventDestroy(L->ev_fill);
   if (L->ev_comp) cudaEventDestroy(L->ev_comp);
@@ -299,8 +315,9 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   rc = MOE_OK;
 #define MOE_ALLOC(ptr, bytes) \
   if (rc == MOE_OK) rc = dalloc(L, &L->ptr, (bytes))
-  MOE_ALLOC(slots, (size_t)g.S * g.ebytes);
-  if (g.has_shared) MOE_ALLOC(shared_w, g.ebytes);
+  // n_slots + 1 experts: the last one is the shared expert (resident, not LRU)
+  MOE_ALLOC(slots, (size_t)(g.S + 1) * g.ebytes);
+  if (rc == MOE_OK) L->shared_w = L->slots + (size_t)g.S * g.ebytes;
   MOE_ALLOC(Wr, (size_t)g.E * g.d * 4);
   MOE_ALLOC(bias, (size_t)g.E * 4);
   MOE_ALLOC(slot_of, (size_t)g.E * 4);
@@ -323,7 +340,33 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   MOE_ALLOC(y_stage, Nm * g.d * 2);
   L->list_cap = (int)std::max<size_t>(Nm * g.k, (size_t)g.E);
   MOE_ALLOC(list_dev, (size_t)L->list_cap * 4);
+  const bool prefill_ok = prefill_shape_ok(g);
+  const size_t prows = Nm * g.k + Nm + 128;   // permuted rows (+ shared) + one tile of padding
+  if (prefill_ok) {
+    MOE_ALLOC(xq_codes, prows * g.d / 2);
+    MOE_ALLOC(xq_scales, prows * (g.d / g.blk));
+    MOE_ALLOC(hq_codes, prows * g.f / 2);
+    MOE_ALLOC(hq_scales, prows * (g.f / g.blk));
+    MOE_ALLOC(tiles, prefill_tile_bytes(g, (int)Nm));
+    MOE_ALLOC(n_tiles, 16);
+  }
 #undef MOE_ALLOC
+  if (rc == MOE_OK) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&L->err_host), 16, cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostGetDevicePointer(reinterpret_cast<void**>(&L->err_dev), L->err_host, 0) != cudaSuccess) {
+      cudaGetLastError();
+      rc = MOE_ERR_OOM;
+    } else {
+      *L->err_host = 0;
+    }
+  }
+  if (rc == MOE_OK && prefill_ok) {
+    L->plan = prefill_plan_create(g, L->slots, L->xq_codes, prows, L->hq_codes);
+    if (!prefill_plan_ready(L->plan)) {
+      prefill_plan_destroy(L->plan);
+      L->plan = nullptr;   // prefill regime unavailable (tensor-map encoding failed)
+    }
+  }
   if (rc == MOE_OK && cudaHostAlloc(&L->pinned_rec, rec_bytes(g.E), cudaHostAllocDefault) != cudaSuccess) {
     cudaGetLastError();
     rc = MOE_ERR_OOM;
@@ -510,10 +553,15 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   if (!x || !y) return fail(L, MOE_ERR_ARG, "x or y is NULL");
   if (!L->router_set) return fail(L, MOE_ERR_STATE, "router weights not set");
   if (g.has_shared && !L->shared_set) return fail(L, MOE_ERR_STATE, "shared expert not set");
-  if (regime == MOE_REGIME_PREFILL)
-    return fail(L, MOE_ERR_UNSUPPORTED, "the prefill regime is not built into this library yet");
-  if (regime != MOE_REGIME_AUTO && regime != MOE_REGIME_DECODE)
+  if (regime != MOE_REGIME_AUTO && regime != MOE_REGIME_DECODE && regime != MOE_REGIME_PREFILL)
     return fail(L, MOE_ERR_ARG, "unknown regime %d", regime);
+  if (regime == MOE_REGIME_PREFILL && !L->plan)
+    return fail(L, MOE_ERR_UNSUPPORTED, "the prefill regime needs d_model and d_ff multiples of 256");
+  const bool prefill = regime == MOE_REGIME_PREFILL || (regime == MOE_REGIME_AUTO && N > 64 && L->plan);
+  if (*L->err_host) {
+    *L->err_host = 0;
+    return fail(L, MOE_ERR_TIMEOUT, "a wait inside an earlier step's kernel timed out; its output is invalid");
+  }
   const bool resident = all_resident(L);
   if (!resident && !L->host_pool)
     return fail(L, MOE_ERR_NOT_INSTALLED, "not every expert is resident and no host pool is registered");
@@ -560,6 +608,14 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   a.wave = 0;
   a.with_shared = g.has_shared;
   const int cap = n_ent_cap(L, N);
+  const float gx = g.fmt == MOE_NVFP4 ? L->desc.act_scale_x : 1.0f;
+  const float gh = g.fmt == MOE_NVFP4 ? L->desc.act_scale_h : 1.0f;
+  if (prefill) {
+    pe = prof_begin(L, MOE_PROF_PREFILL, st);
+    MOE_CUDA(L, launch_gather_quant(g, xd, L->tok_of, N, gx, L->xq_codes, L->xq_scales, st));
+    prof_end(pe, st);
+    L->launches += 1;
+  }
   auto gemv = [&](int n_ent) -> int {
     cudaEvent_t ev[4];
     const bool room = L->prof_used + 4 <= L->prof_pool.size();
@@ -570,9 +626,17 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       ev[0] = p1[0]; ev[1] = p1[1]; ev[2] = p2[0]; ev[3] = p2[1];
       evp = ev;
     }
-    cudaError_t ce = launch_gemv_decode(g, a, xd, L->xexp, L->h, L->O, n_ent, st, evp);
-    if (ce != cudaSuccess) return cuda_fail(L, ce, "launch_gemv_decode");
-    L->launches += 2;
+    cudaError_t ce;
+    if (prefill) {
+      ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, N, a.mode, a.wave, a.with_shared,
+                                L->tiles, L->n_tiles, L->slots, L->xq_scales, L->hq_codes,
+                                L->hq_scales, L->O, gx, gh, L->err_dev, st, evp);
+      L->launches += 3;
+    } else {
+      ce = launch_gemv_decode(g, a, xd, L->xexp, L->h, L->O, n_ent, st, evp);
+      L->launches += 2;
+    }
+    if (ce != cudaSuccess) return cuda_fail(L, ce, prefill ? "launch_prefill_gemms" : "launch_gemv_decode");
     return MOE_OK;
   };
   int grc = gemv(cap + (g.has_shared ? 1 : 0));
@@ -633,7 +697,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     MOE_CUDA(L, cudaStreamSynchronize(st));
   }
   if (info) {
-    info->regime = MOE_REGIME_DECODE;
+    info->regime = prefill ? MOE_REGIME_PREFILL : MOE_REGIME_DECODE;
     info->n_distinct = U;
     info->n_hits = n_hit;
     info->n_misses = n_miss;

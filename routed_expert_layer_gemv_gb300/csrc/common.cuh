@@ -100,6 +100,23 @@ bool gemv_shape_ok(const Geo& g);
 cudaError_t launch_gemv_decode(const Geo& g, const GemvArgs& a, const __nv_bfloat16* x,
                                const int* xexp, float* h, float* O, int n_ent_max,
                                cudaStream_t st, const cudaEvent_t* ev);
+// prefill.cu
+struct PrefillPlan;
+bool prefill_shape_ok(const Geo& g);
+PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8_t* xq_codes,
+                                 size_t xq_rows, const uint8_t* hq_codes);
+void prefill_plan_destroy(PrefillPlan* pl);
+bool prefill_plan_ready(const PrefillPlan* pl);
+size_t prefill_tile_bytes(const Geo& g, int N);
+cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* tok_of, int N,
+                                float gx, uint8_t* codes, uint8_t* scales, cudaStream_t st);
+// ev (may be null): 4 events around phase 1 and phase 2
+cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const StepRecord* rec,
+                                 const int* offsets, int N, int mode, int wave, int with_shared,
+                                 void* tiles, int* n_tiles, const uint8_t* slots,
+                                 const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales,
+                                 float* O, float gx, float gh, int* err, cudaStream_t st,
+                                 const cudaEvent_t* ev);
 // combine.cu
 cudaError_t launch_combine(const Geo& g, const float* O, const float* gates, const int* row_of,
                            int N, __nv_bfloat16* y, cudaStream_t st);

@@ -178,3 +178,81 @@ def test_error_paths():
         capi.moe_set_shared_expert(L.h, x.data_ptr())                  # no shared expert
     assert e.value.status == capi.MOE_ERR_STATE
     L.close()
+
+
+# ---------------------------------------------------------------- prefill regime
+
+PRE = capi.MOE_REGIME_PREFILL
+
+
+@pytest.mark.parametrize("spec,N", [
+    (wl.TINY.layer, 64),
+    (small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16), 300),        # several ragged tiles
+    (small_spec(E=32, k=4, d_model=512, d_ff=512, n_slots=32, fmt="nvfp4", has_shared=True,
+                has_bias=True), 200),
+    (small_spec(E=8, k=8, d_model=256, d_ff=256, n_slots=8), 130),           # k = E
+])
+def test_prefill_all_resident(spec, N):
+    seed = 17
+    L = build_layer(spec, seed, N, install_all=True)
+    x = _tokens(spec, seed, N)
+    y, info = L.forward(bf16_tensor(x), regime=PRE)
+    torch.cuda.synchronize()
+    assert info.regime == PRE
+    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "prefill")
+    assert_close_layer(y, ref, "prefill %s N=%d" % (spec, N))
+    L.close()
+
+
+def test_prefill_35b_shape_sampled_tokens():
+    # the prefill layer shape (d 2048, E 128, top-8, d_ff 768) on 512 tokens
+    spec = wl.PREFILL_35B.layer
+    N, seed = 512, 19
+    L = build_layer(spec, seed, N, install_all=True)
+    x = _tokens(spec, seed, N)
+    y, _ = L.forward(bf16_tensor(x), regime=PRE)
+    torch.cuda.synchronize()
+    sample = list(range(0, N, 37)) + [N - 1]
+    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "prefill", tokens=sample)
+    assert_close_layer(y[sample], ref, "prefill 35B shape")
+    L.close()
+
+
+def test_prefill_with_misses_and_waves():
+    spec = small_spec(E=24, k=3, d_model=512, d_ff=256, n_slots=5, fmt="nvfp4", has_shared=True,
+                      has_bias=True)
+    seed, N = 23, 96
+    experts = CachedExperts(spec, seed)
+    L = build_layer(spec, seed, N, experts_fn=experts)
+    O = oracle_layer(spec, seed, experts)
+    for step in range(3):
+        x = _tokens(spec, seed + step, N)
+        y, info = L.forward(bf16_tensor(x), regime=PRE)
+        assert info.n_waves >= 2 and info.n_misses > 0
+        ref, _, _ = O.forward(wl.bf16_bits_to_f64(x), "prefill")
+        assert_close_layer(y, ref, "prefill waves step %d" % step)
+    L.close()
+
+
+def test_prefill_deterministic_bitwise():
+    spec = small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True)
+    x = _tokens(spec, 29, 200)
+    outs = []
+    for _ in range(2):
+        L = build_layer(spec, 29, 200, install_all=True)
+        y, _ = L.forward(bf16_tensor(x), regime=PRE)
+        torch.cuda.synchronize()
+        outs.append(y.cpu())
+        L.close()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_auto_regime_picks_prefill_for_large_batches():
+    spec = wl.TINY.layer
+    L = build_layer(spec, 3, 128, install_all=True)
+    x = _tokens(spec, 3, 128)
+    _, info = L.forward(bf16_tensor(x))
+    assert info.regime == PRE
+    _, info = L.forward(bf16_tensor(x[:16]))
+    assert info.regime == DEC
+    L.close()
