@@ -38,6 +38,10 @@ METRIC = "MoE-layer tokens/s (decode, prefill); % of HBM BW / % of dense FP4 ten
 FALLBACK_HBM_GBS = 6800.0
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_PER_BF16 = 6.0        # nominal dense ratio: 13.5 PF/s FP4 vs 2.25 PF/s bf16
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -46,6 +50,16 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def _fp4_peak():
+    """Dense FP4 TF/s: measured bf16 GEMM burst x the nominal FP4/bf16 ratio."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            return float(json.load(fh)["bf16_tflops"]) * FP4_PER_BF16, "measured bf16 x 6"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS * FP4_PER_BF16, "fallback bf16 x 6"
 
 
 def _dist():
@@ -185,6 +199,56 @@ def run_decode_e2e(args, batch, torch, capi, wl, build_layer, flush):
                 h2d=K * batch * spec.d_model * 2, d2h=K * batch * spec.d_model * 2)
 
 
+def run_prefill(args, work, torch, capi, wl, build_layer, flush, st):
+    """One prefill chunk per step, every expert resident (slot e = expert e)."""
+    spec, N, seed = work.layer, work.n_tokens, work.seed
+    x_host, _ = wl.iid_tokens(seed, N, spec.d_model)
+    x = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
+    L = build_layer(spec, seed, N, install_all=True)
+    y = torch.empty(N, spec.d_model, dtype=torch.bfloat16, device="cuda")
+    W, K = max(3, args.warmup // 4), max(3, args.prefill_steps)
+    with torch.cuda.stream(st):
+        for _ in range(W):
+            L.forward(x, y, stream=st, regime=capi.MOE_REGIME_PREFILL)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    capi.moe_profile(L.h, True)
+    launches = 0
+    with torch.cuda.stream(st):
+        for t in range(K):
+            flush.zero_()
+            ev[t][0].record(st)
+            _, info = L.forward(x, y, stream=st, regime=capi.MOE_REGIME_PREFILL)
+            ev[t][1].record(st)
+            launches += info.n_launches
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    prof = capi.moe_profile_read(L.h)
+    capi.moe_profile(L.h, False)
+    L.close()
+    rows = N * spec.k + (N if spec.has_shared else 0)
+    d, f = spec.d_model, spec.d_ff
+    flops1, flops2 = 2.0 * rows * d * 2 * f, 2.0 * rows * f * d
+    return dict(workload=work.name, steps=K, ms=ms, tokens=K * N, launches=launches, prof=prof,
+                flops1=flops1 * K, flops2=flops2 * K)
+
+
+def prefill_summary(r, fp4_peak):
+    p = r["prof"]
+    g_ms, g_n = p["gateup"]
+    d_ms, d_n = p["down"]
+    t1 = r["flops1"] / (g_ms / 1000.0) / 1e12 if g_ms else None
+    t2 = r["flops2"] / (d_ms / 1000.0) / 1e12 if d_ms else None
+    tboth = (r["flops1"] + r["flops2"]) / ((g_ms + d_ms) / 1000.0) / 1e12 if g_ms + d_ms else None
+    return {
+        "workload": r["workload"], "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
+        "ms_per_step": r["ms"] / r["steps"],
+        "gemm_tflops": {"gateup": t1, "down": t2, "both": tboth},
+        "frac_fp4_peak": (tboth / fp4_peak) if tboth else None,
+        "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
+    }
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def cpu_oracle_sample(budget_s: float):
@@ -224,6 +288,12 @@ def main():
     ap.add_argument("--batches", default="1,4,16")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode35b",
+                    choices=["decode35b", "prefill35b", "prefill753b"],
+                    help="decode35b = the headline decode configuration; the prefill ones "
+                         "print that prefill chunk's line instead")
+    ap.add_argument("--prefill-steps", type=int, default=8)
+    ap.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill result")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = _dist()
@@ -257,6 +327,28 @@ def main():
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     st = torch.cuda.Stream()
     clocks = ClockSampler(local)
+    if args.workload != "decode35b":
+        work = wl.PREFILL_35B if args.workload == "prefill35b" else wl.PREFILL_753B
+        clocks.start()
+        r = run_prefill(args, work, torch, capi, wl, build_layer, flush, st)
+        clk = clocks.stop()
+        fp4, fp4_kind = _fp4_peak()
+        sm = prefill_summary(r, fp4)
+        tboth = sm["gemm_tflops"]["both"]
+        line = {"metric": METRIC, "value": sm["tokens_per_s"] * ws, "unit": "tokens/s", "n_gpus": ws,
+                "steps": r["steps"], "warmup": max(3, args.warmup // 4), "ms_per_step": sm["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "fp4(e2m1)xfp4(e2m1)->f32", "data": "synthetic (seeded i.i.d. hidden states, random FP4 weights)",
+                "config": {"workload": work.name, "l2": "flushed (512 MiB write) between timed steps",
+                           "detail": sm},
+                "roofline": {"bound": "tensor", "kernel": "prefill grouped GEMM (gate/up + down)",
+                             "achieved": tboth, "peak": fp4, "unit": "TFLOP/s",
+                             "frac": (tboth / fp4) if tboth else None, "traffic": None,
+                             "peak_kind": fp4_kind},
+                "gpu_launches": r["launches"], "clocks": clk}
+        if rank == 0:
+            print(json.dumps(line))
+        return
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -300,6 +392,11 @@ def main():
             "fill_GB_per_s": r["fill_bytes"] / max(1e-9, p["fill"][0] / 1000.0) / 1e9 if p["fill"][0] else None,
             "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
         }
+    prefill = None
+    if not args.no_prefill:
+        fp4, _ = _fp4_peak()
+        prefill = prefill_summary(run_prefill(args, wl.PREFILL_35B, torch, capi, wl, build_layer,
+                                              flush, st), fp4)
     cpu = None
     if not args.no_cpu_baseline:
         v, tok, steps, el, cores = cpu_oracle_sample(args.cpu_budget)
@@ -322,6 +419,7 @@ def main():
                 "d2h_bytes_per_step": sum(e["d2h"] for e in e2e_runs) / (args.steps * len(batches))},
         "gpu_launches": sum(r["launches"] for r in runs),
         "clocks": clk,
+        "prefill_35b_a3b_n8192": prefill,
     }
     print(json.dumps(line))
 
