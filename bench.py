@@ -13,7 +13,9 @@ between timed steps, outside the events.  `value` = tokens / summed step time
 over the three batch sizes, inputs resident in HBM.  `e2e` repeats the run
 through the C ABI with pinned host x / y buffers (copies inside the timed
 call, host wall clock).  The roofline entry is the expert FFN phase-1 kernel
-(gate/up GEMV), timed live with the library's per-launch events.
+(gate/up GEMV), timed with the library's per-launch CUDA events in a second
+pass over the same steps (the events cost host time per launch, so the pass
+behind `value` runs without them).
 
 --impl reference times the CPU oracle (FP64, numpy) on a bounded sample of the
 same workload on the host cores.
@@ -138,7 +140,10 @@ def gateup_bytes(spec, layout, n_experts, n_tokens):
     return n_experts * w + n_tokens * d * 2 + rows * f * 4
 
 
-def run_decode(args, batch, torch, capi, wl, build_layer, flush, st):
+def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile):
+    """K timed decode steps after W warm-up steps on a fresh layer (cold cache).
+    profile=False: the clean pass behind `value`; profile=True: the same steps
+    with the library's per-launch events on (kernel times for the roofline)."""
     spec = wl.DECODE_35B.layer
     seed = wl.DECODE_35B.seed
     W, K = args.warmup, args.steps
@@ -151,7 +156,7 @@ def run_decode(args, batch, torch, capi, wl, build_layer, flush, st):
             L.forward(xs[t], y, stream=st)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    capi.moe_profile(L.h, True)
+    capi.moe_profile(L.h, profile)
     launches = misses = distinct = 0
     fill = 0
     ffn_bytes = 0
@@ -200,7 +205,9 @@ def run_decode_e2e(args, batch, torch, capi, wl, build_layer, flush):
 
 
 def run_prefill(args, work, torch, capi, wl, build_layer, flush, st):
-    """One prefill chunk per step, every expert resident (slot e = expert e)."""
+    """One prefill chunk per step, every expert resident (slot e = expert e).
+    Tokens/s from a pass without per-kernel events, kernel times from a second
+    instrumented pass."""
     spec, N, seed = work.layer, work.n_tokens, work.seed
     x_host, _ = wl.iid_tokens(seed, N, spec.d_model)
     x = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
@@ -212,17 +219,19 @@ def run_prefill(args, work, torch, capi, wl, build_layer, flush, st):
             L.forward(x, y, stream=st, regime=capi.MOE_REGIME_PREFILL)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    capi.moe_profile(L.h, True)
-    launches = 0
-    with torch.cuda.stream(st):
-        for t in range(K):
-            flush.zero_()
-            ev[t][0].record(st)
-            _, info = L.forward(x, y, stream=st, regime=capi.MOE_REGIME_PREFILL)
-            ev[t][1].record(st)
-            launches += info.n_launches
-    torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev)
+    for profile in (False, True):
+        capi.moe_profile(L.h, profile)
+        launches = 0
+        with torch.cuda.stream(st):
+            for t in range(K):
+                flush.zero_()
+                ev[t][0].record(st)
+                _, info = L.forward(x, y, stream=st, regime=capi.MOE_REGIME_PREFILL)
+                ev[t][1].record(st)
+                launches += info.n_launches
+        torch.cuda.synchronize()
+        if not profile:
+            ms = sum(a.elapsed_time(b) for a, b in ev)
     prof = capi.moe_profile_read(L.h)
     capi.moe_profile(L.h, False)
     L.close()
@@ -353,9 +362,10 @@ def main():
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    runs = [run_decode(args, b, torch, capi, wl, build_layer, flush, st) for b in batches]
+    runs = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False) for b in batches]
     torch.cuda.synchronize()
     clk = clocks.stop()
+    pruns = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, True) for b in batches]
     e2e_runs = [run_decode_e2e(args, b, torch, capi, wl, build_layer, flush) for b in batches]
 
     ms = sum(r["ms"] for r in runs)
@@ -372,9 +382,9 @@ def main():
     e2e_value = ws * tokens / e2e_s
 
     peak, peak_kind = _peaks()
-    g_ms = sum(r["prof"]["gateup"][0] for r in runs)
-    g_n = sum(r["prof"]["gateup"][1] for r in runs)
-    g_bytes = sum(r["gateup_bytes"] for r in runs)
+    g_ms = sum(r["prof"]["gateup"][0] for r in pruns)
+    g_n = sum(r["prof"]["gateup"][1] for r in pruns)
+    g_bytes = sum(r["gateup_bytes"] for r in pruns)
     achieved = (g_bytes / max(g_n, 1)) / ((g_ms / max(g_n, 1)) / 1000.0) / 1e9 if g_ms > 0 else None
     roof = {"bound": "hbm", "kernel": "gemv_gateup (expert FFN phase 1)", "achieved": achieved,
             "peak": peak, "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
@@ -382,8 +392,8 @@ def main():
             "bytes_per_launch": g_bytes / max(g_n, 1), "ms_per_launch": g_ms / max(g_n, 1)}
 
     per_batch = {}
-    for r, e in zip(runs, e2e_runs):
-        p = r["prof"]
+    for r, e, pr in zip(runs, e2e_runs, pruns):
+        p = pr["prof"]
         per_batch[str(r["batch"])] = {
             "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
             "e2e_tokens_per_s": e["tokens"] / e["s"],
@@ -410,6 +420,8 @@ def main():
         "data": "synthetic (seeded AR(1) hidden states, random FP4 weights)",
         "config": {"workload": "decode_35b_a3b_d2048_e128_top8_f768_mxfp4_s47",
                    "batches": batches, "l2": "flushed (512 MiB write) between timed steps",
+                   "timing": "value from a pass without per-kernel events; kernel times and "
+                             "roofline from a second, instrumented pass of the same steps",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "per_batch": per_batch},
         "roofline": roof,

@@ -101,7 +101,7 @@ typedef struct {
 
 /* Kernel classes of moe_profile_read. */
 #define MOE_PROF_ROUTER      0
-#define MOE_PROF_PERMUTE     1
+#define MOE_PROF_PERMUTE     1  /* permutation (and the LRU step, fused, N<=128) */
 #define MOE_PROF_LRU         2
 #define MOE_PROF_GATEUP      3  /* expert FFN phase 1: W_g, W_u, SiLU * mul
                                    (decode GEMV or prefill grouped GEMM)       */
@@ -175,6 +175,23 @@ int moe_lru_set_state(moe_layer_t layer, const int* expert_of_slot,
  * MOE_REGIME_*.  MOE_ERR_NOT_INSTALLED if a miss has no host source. */
 int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
                 int regime, moe_forward_info* info);
+
+/* How misses reach their slots.  MOE_FILL_MEMCPY (default): the host reads
+ * the step's routing record and issues one cudaMemcpyAsync per miss from the
+ * pinned pool, spread over the layer's side streams, while the hits compute.
+ * MOE_FILL_DEVICE: a copy kernel on a side stream reads the record on the GPU
+ * and pulls the missed experts from the pinned pool itself (unified
+ * addressing over the host link), so moe_forward never waits on the host;
+ * moe_forward_info then reports n_distinct / n_hits = -1 (see moe_stats).
+ * MOE_ERR_STATE if the registered pool is not device-addressable. */
+#define MOE_FILL_MEMCPY 0
+#define MOE_FILL_DEVICE 1
+int moe_set_fill_mode(moe_layer_t layer, int mode);
+
+/* Totals since create, accumulated on the device by the LRU step of every
+ * moe_forward: out4 = {steps, distinct experts, hits, misses}.  Synchronizes
+ * the device. */
+int moe_stats(moe_layer_t layer, uint64_t* out4);
 
 /* Kernel timing.  moe_profile(layer, 1) resets the counters and from then
  * on brackets every launch of the layer with CUDA events on the stream it runs

@@ -31,6 +31,9 @@ MOE_NVFP4 = 1
 
 MOE_PROF_NAMES = ["router", "permute", "lru", "gateup", "down", "combine", "fill", "prefill"]
 
+MOE_FILL_MEMCPY = 0
+MOE_FILL_DEVICE = 1
+
 MOE_REGIME_AUTO = 0
 MOE_REGIME_DECODE = 1
 MOE_REGIME_PREFILL = 2
@@ -70,6 +73,8 @@ _SIGS = {
     "moe_lru_get_state": ([_P, _P, _P, _P], _I),
     "moe_lru_set_state": ([_P, _P, _P, C.c_uint64], _I),
     "moe_forward": ([_P, _P, _I, _P, _P, _I, C.POINTER(moe_forward_info)], _I),
+    "moe_set_fill_mode": ([_P, _I], _I),
+    "moe_stats": ([_P, _P], _I),
     "moe_profile": ([_P, _I], _I),
     "moe_profile_read": ([_P, _P, _P], _I),
     "moe_last_error": ([_P], C.c_char_p),
@@ -206,6 +211,17 @@ def moe_forward(h, x, N: int, y, stream=None, regime: int = MOE_REGIME_AUTO) -> 
     info = moe_forward_info()
     check(lib().moe_forward(h, _ptr(x), N, _ptr(y), _stream(stream), regime, C.byref(info)), h)
     return info
+
+
+def moe_set_fill_mode(h, mode: int) -> None:
+    check(lib().moe_set_fill_mode(h, mode), h)
+
+
+def moe_stats(h):
+    """(steps, distinct experts, hits, misses) accumulated on the device."""
+    out = (C.c_uint64 * 4)()
+    check(lib().moe_stats(h, out), h)
+    return tuple(out)
 
 
 def moe_profile(h, enable: bool) -> None:

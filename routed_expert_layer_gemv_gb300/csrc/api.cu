@@ -31,6 +31,8 @@
 
 using namespace moe;
 
+constexpr int kFillStreams = 4;
+
 struct moe_layer {
   moe_layer_desc desc{};
   Geo g{};
@@ -73,6 +75,7 @@ struct moe_layer {
   void* tiles = nullptr;
   int* n_tiles = nullptr;
   PrefillPlan* plan = nullptr;
+  unsigned int* rcounter = nullptr;  // CTA counter of the one-launch router
   int* err_host = nullptr;       // kernels' timeout flag (mapped pinned memory)
   int* err_dev = nullptr;
   // host state
@@ -80,8 +83,12 @@ struct moe_layer {
   size_t host_pool_bytes = 0;
   bool router_set = false;
   bool shared_set = false;
-  cudaStream_t fill = nullptr;
+  cudaStream_t fill[kFillStreams] = {};       // miss fills, round robin
+  cudaEvent_t ev_fills[kFillStreams] = {};
   cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_comp = nullptr;
+  int fill_mode = MOE_FILL_MEMCPY;
+  const uint8_t* pool_dev = nullptr;          // device address of the host pool
+  unsigned long long* stats = nullptr;        // steps, distinct, hits, misses
   std::vector<int> mirror;   // expert per slot as far as the host knows
   std::string err;
   // kernel timing (moe_profile)
@@ -199,9 +206,13 @@ void release(moe_layer* L) {
   if (L->ev_route) cudaEventDestroy(L->ev_route);
   if (L->ev_fill) cudaEventDestroy(L->ev_fill);
   if (L->ev_comp) cudaEventDestroy(L->ev_comp);
-  if (L->fill) cudaStreamDestroy(L->fill);
+  for (int i = 0; i < kFillStreams; ++i) {
+    if (L->ev_fills[i]) cudaEventDestroy(L->ev_fills[i]);
+    if (L->fill[i]) cudaStreamDestroy(L->fill[i]);
+    L->ev_fills[i] = nullptr;
+    L->fill[i] = nullptr;
+  }
   L->ev_route = L->ev_fill = L->ev_comp = nullptr;
-  L->fill = nullptr;
 }
 
 int pointer_kind(const void* p, bool* on_device, int device) {
@@ -340,6 +351,8 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   MOE_ALLOC(y_stage, Nm * g.d * 2);
   L->list_cap = (int)std::max<size_t>(Nm * g.k, (size_t)g.E);
   MOE_ALLOC(list_dev, (size_t)L->list_cap * 4);
+  MOE_ALLOC(rcounter, 16);
+  MOE_ALLOC(stats, 64);
   const bool prefill_ok = prefill_shape_ok(g);
   const size_t prows = Nm * g.k + Nm + 128;   // permuted rows (+ shared) + one tile of padding
   if (prefill_ok) {
@@ -373,7 +386,11 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   }
   if (rc == MOE_OK) {
     L->rec_host = static_cast<StepRecord*>(L->pinned_rec);
-    if (cudaStreamCreateWithFlags(&L->fill, cudaStreamNonBlocking) != cudaSuccess ||
+    bool sok = true;
+    for (int i = 0; i < kFillStreams; ++i)
+      sok = sok && cudaStreamCreateWithFlags(&L->fill[i], cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&L->ev_fills[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!sok ||
         cudaEventCreateWithFlags(&L->ev_route, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&L->ev_comp, cudaEventDisableTiming) != cudaSuccess) {
@@ -389,6 +406,8 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
               cudaMemset(L->clock, 0, 8) == cudaSuccess &&
               cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
               cudaMemset(L->rec, 0, rec_bytes(g.E)) == cudaSuccess &&
+              cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
+              cudaMemset(L->stats, 0, 64) == cudaSuccess &&
               cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
       cudaGetLastError();
@@ -436,6 +455,13 @@ int moe_register_host_experts(moe_layer_t L, const void* pool, size_t bytes) {
   }
   L->host_pool = static_cast<const uint8_t*>(pool);
   L->host_pool_bytes = bytes;
+  void* dp = nullptr;
+  if (cudaHostGetDevicePointer(&dp, const_cast<void*>(pool), 0) == cudaSuccess) {
+    L->pool_dev = static_cast<const uint8_t*>(dp);
+  } else {
+    cudaGetLastError();
+    L->pool_dev = nullptr;   // device-driven fills unavailable for this pool
+  }
   return MOE_OK;
 }
 
@@ -508,7 +534,8 @@ int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, in
   const Geo& g = L->g;
   if (n > 0) MOE_CUDA(L, cudaMemcpyAsync(L->list_dev, experts, (size_t)n * 4, cudaMemcpyHostToDevice, st));
   MOE_CUDA(L, launch_counts_from_list(g, L->list_dev, n, L->counts, st));
-  MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec, st));
+  MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec,
+                              nullptr, st));
   MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
   MOE_CUDA(L, cudaStreamSynchronize(st));
   const StepRecord* r = L->rec_host;
@@ -581,20 +608,33 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   L->launches = 0;
   cudaEvent_t* pe = prof_begin(L, MOE_PROF_ROUTER, st);
   MOE_CUDA(L, launch_router(g, xd, N, L->Wr, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
-                            L->gates, L->xexp, st));
+                            L->gates, L->xexp, L->rcounter, st));
   prof_end(pe, st);
-  L->launches += 2;
-  pe = prof_begin(L, MOE_PROF_PERMUTE, st);
-  MOE_CUDA(L, launch_permute(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
-                             L->perm_scratch, st));
-  prof_end(pe, st);
-  L->launches += N <= 128 ? 1 : 3;
-  pe = prof_begin(L, MOE_PROF_LRU, st);
-  MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec, st));
-  prof_end(pe, st);
-  L->launches += 1;
+  L->launches += N <= 64 ? 1 : 2;
+  if (N <= 128) {
+    // permutation and LRU step in one CTA
+    pe = prof_begin(L, MOE_PROF_PERMUTE, st);
+    MOE_CUDA(L, launch_route_tail(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
+                                  L->slot_of, L->expert_of, L->stamp, L->clock, L->rec, L->stats,
+                                  st));
+    prof_end(pe, st);
+    L->launches += 1;
+  } else {
+    pe = prof_begin(L, MOE_PROF_PERMUTE, st);
+    MOE_CUDA(L, launch_permute(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
+                               L->perm_scratch, st));
+    prof_end(pe, st);
+    L->launches += 3;
+    pe = prof_begin(L, MOE_PROF_LRU, st);
+    MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec,
+                                L->stats, st));
+    prof_end(pe, st);
+    L->launches += 1;
+  }
+  const bool dev_fill = !resident && L->fill_mode == MOE_FILL_DEVICE;
   if (!resident) {
-    MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
+    if (!dev_fill)
+      MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
     MOE_CUDA(L, cudaEventRecord(L->ev_route, st));
   }
   GemvArgs a{};
@@ -644,7 +684,31 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
 
   size_t fill_bytes = 0;
   int U = -1, n_hit = -1, n_miss = 0, waves = 1;
-  if (!resident) {
+  if (dev_fill) {
+    // no host wait: one copy kernel and one expert-FFN launch per possible wave
+    const int max_waves = (std::min(g.E, N * g.k) + g.S - 1) / g.S;
+    for (int w = 0; w < max_waves; ++w) {
+      cudaStream_t fs = L->fill[0];
+      if (w == 0) {
+        MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
+      } else {
+        MOE_CUDA(L, cudaEventRecord(L->ev_comp, st));
+        MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_comp, 0));
+      }
+      cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
+      MOE_CUDA(L, launch_fill_copy(g, L->rec, w, std::min(cap, g.S), L->pool_dev, L->slots, fs));
+      prof_end(pf, fs);
+      L->launches += 1;
+      MOE_CUDA(L, cudaEventRecord(L->ev_fill, fs));
+      MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
+      a.mode = kRangeWaveMisses;
+      a.wave = w;
+      a.with_shared = 0;
+      grc = gemv(std::min(cap, g.S));
+      if (grc) return grc;
+    }
+    waves = max_waves;
+  } else if (!resident) {
     MOE_CUDA(L, cudaEventSynchronize(L->ev_route));
     const StepRecord* r = L->rec_host;
     U = r->U;
@@ -661,24 +725,30 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     for (int w = 0; w < waves; ++w) {
       const int b = std::max(n_hit, w * g.S), e = std::min((w + 1) * g.S, U);
       if (b >= e) continue;
-      if (w == 0) {
-        // wave 0 fills only free or stale slots: wait for the routing alone
-        MOE_CUDA(L, cudaStreamWaitEvent(L->fill, L->ev_route, 0));
-      } else {
-        // a later wave overwrites slots the previous wave computed from
+      // wave 0 fills only free or stale slots: it waits for the routing alone;
+      // a later wave overwrites slots the previous wave computed from
+      cudaEvent_t trigger = L->ev_route;
+      if (w > 0) {
         MOE_CUDA(L, cudaEventRecord(L->ev_comp, st));
-        MOE_CUDA(L, cudaStreamWaitEvent(L->fill, L->ev_comp, 0));
+        trigger = L->ev_comp;
       }
-      cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, L->fill);
+      const int nfs = std::min(kFillStreams, e - b);
+      for (int j = 0; j < nfs; ++j) MOE_CUDA(L, cudaStreamWaitEvent(L->fill[j], trigger, 0));
+      cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, L->fill[0]);
       for (int i = b; i < e; ++i) {
         cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)as[i] * g.ebytes,
                                          L->host_pool + (size_t)ae[i] * g.ebytes, g.ebytes,
-                                         cudaMemcpyHostToDevice, L->fill);
+                                         cudaMemcpyHostToDevice, L->fill[(i - b) % kFillStreams]);
         if (ce != cudaSuccess) return fail(L, MOE_ERR_FILL, "fill of expert %d: %s", ae[i], cudaGetErrorString(ce));
         fill_bytes += g.ebytes;
       }
-      prof_end(pf, L->fill);
-      MOE_CUDA(L, cudaEventRecord(L->ev_fill, L->fill));
+      // the timing bracket on stream 0 covers the wave: stream 0 waits for the others
+      for (int j = 1; j < nfs; ++j) {
+        MOE_CUDA(L, cudaEventRecord(L->ev_fills[j], L->fill[j]));
+        MOE_CUDA(L, cudaStreamWaitEvent(L->fill[0], L->ev_fills[j], 0));
+      }
+      prof_end(pf, L->fill[0]);
+      MOE_CUDA(L, cudaEventRecord(L->ev_fill, L->fill[0]));
       MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
       a.mode = kRangeWaveMisses;
       a.wave = w;
@@ -703,9 +773,25 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     info->n_misses = n_miss;
     info->n_waves = resident ? 1 : waves;
     info->fill_bytes = fill_bytes;
-    info->host_synced = resident ? 0 : 1;
+    info->host_synced = (resident || dev_fill) ? 0 : 1;
     info->n_launches = L->launches;
   }
+  return MOE_OK;
+}
+
+int moe_set_fill_mode(moe_layer_t L, int mode) {
+  if (!L) return MOE_ERR_ARG;
+  if (mode != MOE_FILL_MEMCPY && mode != MOE_FILL_DEVICE) return fail(L, MOE_ERR_ARG, "unknown fill mode %d", mode);
+  if (mode == MOE_FILL_DEVICE && !L->pool_dev)
+    return fail(L, MOE_ERR_STATE, "device fills need a registered pinned host pool the device can address");
+  L->fill_mode = mode;
+  return MOE_OK;
+}
+
+int moe_stats(moe_layer_t L, uint64_t* out4) {
+  if (!L || !out4) return MOE_ERR_ARG;
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  MOE_CUDA(L, cudaMemcpy(out4, L->stats, 4 * sizeof(uint64_t), cudaMemcpyDeviceToHost));
   return MOE_OK;
 }
 
@@ -749,7 +835,7 @@ int moe_debug_router(moe_layer_t L, const void* x, int N, int* idx, float* gates
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MOE_CUDA(L, launch_router(L->g, static_cast<const __nv_bfloat16*>(x), N, L->Wr,
                             L->g.has_bias ? L->bias : nullptr, logits ? logits : L->logits, idx,
-                            gates, L->xexp, st));
+                            gates, L->xexp, L->rcounter, st));
   return MOE_OK;
 }
 

@@ -68,20 +68,27 @@ enum RangeMode : int { kRangeHits = 0, kRangeWaveMisses = 1, kRangeAll = 2 };
 
 // ---------------------------------------------------------------- launchers
 // router.cu
+// counter: a zeroed device word (enables the one-launch path for N <= 64), or null
 cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
                           const float* bias, float* logits, int* idx, float* gates, int* xexp,
-                          cudaStream_t st);
+                          unsigned int* counter, cudaStream_t st);
 // permute.cu
 size_t permute_scratch_bytes(const Geo& g, int max_tokens);
 cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int* offsets,
                            int* row_of, int* tok_of, void* scratch, cudaStream_t st);
 // lru.cu
+// stats (may be null): steps, distinct experts, hits, misses, accumulated
 cudaError_t launch_lru_step(const Geo& g, const int* counts, int* slot_of, int* expert_of,
                             unsigned long long* stamp, unsigned long long* clock,
-                            StepRecord* rec, cudaStream_t st);
+                            StepRecord* rec, unsigned long long* stats, cudaStream_t st);
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
                                unsigned long long* stamp, unsigned long long* clock,
                                cudaStream_t st);
+// permutation + LRU step in one CTA, for N <= 128 tokens
+cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, int* offsets,
+                              int* row_of, int* tok_of, int* slot_of, int* expert_of,
+                              unsigned long long* stamp, unsigned long long* clock,
+                              StepRecord* rec, unsigned long long* stats, cudaStream_t st);
 cudaError_t launch_counts_from_list(const Geo& g, const int* experts, int n, int* counts,
                                     cudaStream_t st);
 // gemv.cu
@@ -117,6 +124,9 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales,
                                  float* O, float gx, float gh, int* err, cudaStream_t st,
                                  const cudaEvent_t* ev);
+// fill.cu: copy the misses of one wave from the (device-addressable) host pool
+cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int wave, int max_misses,
+                             const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
 // combine.cu
 cudaError_t launch_combine(const Geo& g, const float* O, const float* gates, const int* row_of,
                            int N, __nv_bfloat16* y, cudaStream_t st);

@@ -21,6 +21,7 @@
 // distinct, and a wave's fills must wait for the previous wave's compute.
 // Stamps: access i gets clock + 1 + i; the clock advances by |U|.
 #include "common.cuh"
+#include "permute_dev.cuh"
 
 namespace moe {
 
@@ -54,14 +55,23 @@ MOE_DEV int excl_scan_1024(int v, int* total, int* sh) {
   return r;
 }
 
-__global__ void __launch_bounds__(kLruThreads)
-lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ slot_of,
-                int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
-                unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec) {
-  __shared__ int sh[33];
-  __shared__ int q[kMaxE];        // victim queue (slots)
-  __shared__ int q_old[kMaxE];    // expert that held q[i] before the step (-1 free)
-  __shared__ int acc_e[kMaxE], acc_s[kMaxE];
+// Shared-memory scratch of one LRU step.
+struct LruSmem {
+  int sh[33];
+  int q[kMaxE];        // victim queue (slots)
+  int q_old[kMaxE];    // expert that held q[i] before the step (-1 free)
+  int acc_e[kMaxE], acc_s[kMaxE];
+  int eo[kMaxE];       // expert_of, staged
+  unsigned long long st[kMaxE];   // stamps, staged
+  unsigned char stale[kMaxE];     // occupied by an expert not routed this step
+};
+
+// One step of the table (blockDim.x == 1024).  counts may live in shared or
+// global memory; the table is staged into shared memory before any loop.
+MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of,
+                      int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
+                      unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
+                      unsigned long long* __restrict__ stats, LruSmem& m) {
   const int tid = threadIdx.x;
   const unsigned long long clk = *clock;
 
@@ -71,8 +81,8 @@ lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ 
   const int cur = e < E ? slot_of[e] : -1;
   const bool hit = inU && cur >= 0, miss = inU && cur < 0;
   int n_hit, n_miss;
-  const int hr = excl_scan_1024(hit ? 1 : 0, &n_hit, sh);
-  const int mr = excl_scan_1024(miss ? 1 : 0, &n_miss, sh);
+  const int hr = excl_scan_1024(hit ? 1 : 0, &n_hit, m.sh);
+  const int mr = excl_scan_1024(miss ? 1 : 0, &n_miss, m.sh);
   const int U = n_hit + n_miss;
 
   // victim queue over slots (S <= E <= 1024: one slot per thread)
@@ -85,45 +95,47 @@ lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ 
     fre = old < 0 || old >= E;
     stale = !fre && counts[old] == 0;
     st = stamp[s];
+    m.eo[s] = old;
+    m.st[s] = st;
+    m.stale[s] = stale ? 1 : 0;
   }
   int n_free;
-  const int fr = excl_scan_1024(fre ? 1 : 0, &n_free, sh);
-  if (fre) { q[fr] = s; q_old[fr] = -1; }
+  const int fr = excl_scan_1024(fre ? 1 : 0, &n_free, m.sh);   // (its barriers also publish m.*)
+  if (fre) { m.q[fr] = s; m.q_old[fr] = -1; }
   if (stale) {
     int r = 0;
     for (int s2 = 0; s2 < S; ++s2) {
-      int o2 = expert_of[s2];
-      if (o2 < 0 || o2 >= E || counts[o2] > 0) continue;
-      unsigned long long t2 = stamp[s2];
+      if (!m.stale[s2]) continue;
+      const unsigned long long t2 = m.st[s2];
       r += (t2 < st || (t2 == st && s2 < s)) ? 1 : 0;
     }
     if (n_free + r < S) {
-      q[n_free + r] = s;
-      q_old[n_free + r] = old;
+      m.q[n_free + r] = s;
+      m.q_old[n_free + r] = old;
     }
   }
   __syncthreads();
 
   // accesses 0 .. min(U, S)-1 first, then the later waves reuse slot(i - S)
-  if (hit) { acc_e[hr] = e; acc_s[hr] = cur; }
+  if (hit) { m.acc_e[hr] = e; m.acc_s[hr] = cur; }
   if (miss) {
     const int i = n_hit + mr;
-    acc_e[i] = e;
-    if (i < S) acc_s[i] = q[i - n_hit];   // i - n_hit < S - n_hit = |Q|
+    m.acc_e[i] = e;
+    if (i < S) m.acc_s[i] = m.q[i - n_hit];   // i - n_hit < S - n_hit = |Q|
   }
   __syncthreads();
-  for (int i = S + tid; i < U; i += kLruThreads) acc_s[i] = acc_s[i % S];
+  for (int i = S + tid; i < U; i += kLruThreads) m.acc_s[i] = m.acc_s[i % S];
   __syncthreads();
 
   int* r_e = rec_expert(rec);
   int* r_s = rec_slot(rec, E);
   int* r_v = rec_evicted(rec, E);
   for (int i = tid; i < U; i += kLruThreads) {
-    r_e[i] = acc_e[i];
-    r_s[i] = acc_s[i];
+    r_e[i] = m.acc_e[i];
+    r_s[i] = m.acc_s[i];
     int ev = -1;
-    if (i >= S) ev = acc_e[i - S];
-    else if (i >= n_hit) ev = q_old[i - n_hit];
+    if (i >= S) ev = m.acc_e[i - S];
+    else if (i >= n_hit) ev = m.q_old[i - n_hit];
     r_v[i] = ev;
   }
   if (tid == 0) {
@@ -134,12 +146,12 @@ lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ 
   }
   // table update: experts pushed out of Q lose their slot
   for (int i = n_hit + tid; i < min(U, S); i += kLruThreads) {
-    int ev = q_old[i - n_hit];
+    const int ev = m.q_old[i - n_hit];
     if (ev >= 0 && ev < E) slot_of[ev] = -1;
   }
   __syncthreads();
   for (int i = tid; i < U; i += kLruThreads) {
-    const int ex = acc_e[i], sl = acc_s[i];
+    const int ex = m.acc_e[i], sl = m.acc_s[i];
     if (sl < 0 || sl >= S) continue;   // only a corrupted table gets here
     if (i + S < U) {
       slot_of[ex] = -1;            // evicted later in this same step
@@ -149,7 +161,67 @@ lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ 
       stamp[sl] = clk + 1ull + (unsigned long long)i;
     }
   }
-  if (tid == 0) *clock = clk + (unsigned long long)U;
+  if (tid == 0) {
+    *clock = clk + (unsigned long long)U;
+    if (stats) {
+      stats[0] += 1ull;
+      stats[1] += (unsigned long long)U;
+      stats[2] += (unsigned long long)n_hit;
+      stats[3] += (unsigned long long)n_miss;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kLruThreads)
+lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ slot_of,
+                int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
+                unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
+                unsigned long long* __restrict__ stats) {
+  __shared__ LruSmem m;
+  lru_body(counts, E, S, slot_of, expert_of, stamp, clock, rec, stats, m);
+}
+
+// Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
+// (as perm_single in permute.cu), then the LRU step on the counts it found.
+__global__ void __launch_bounds__(kLruThreads)
+route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int* __restrict__ counts,
+                  int* __restrict__ offsets, int* __restrict__ row_of, int* __restrict__ tok_of,
+                  int* __restrict__ slot_of, int* __restrict__ expert_of,
+                  unsigned long long* __restrict__ stamp, unsigned long long* __restrict__ clock,
+                  StepRecord* __restrict__ rec, unsigned long long* __restrict__ stats) {
+  __shared__ LruSmem m;
+  extern __shared__ uint32_t dsm[];
+  uint32_t* cm = dsm;                                            // [E][4]
+  int* cnt = reinterpret_cast<int*>(cm + E * perm::kPermWarps);  // [E]
+  int* off = cnt + E;                                            // [E]
+  int* rows = off + E;                                           // [128][k]
+  perm::stage_rows(idx, N, k, 0, rows);
+  __syncthreads();
+  if (threadIdx.x < perm::kTokPerBlock) perm::build_ballots(rows, k, E, cm);
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int c = e < E ? perm::block_count(cm, e) : 0;
+  int tot;
+  const int ex = perm::block_excl_scan(c, &tot, m.sh);
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = ex;
+    cnt[e] = c;
+    off[e] = ex;
+  }
+  if (e == 0) offsets[E] = tot;
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t < N) {
+    for (int j = 0; j < k; ++j) {
+      const int ej = rows[t * k + j];
+      const int r = off[ej] + perm::rank_in_block(cm, ej);
+      row_of[(size_t)t * k + j] = r;
+      tok_of[r] = t;
+    }
+  }
+  __syncthreads();
+  lru_body(cnt, E, S, slot_of, expert_of, stamp, clock, rec, stats, m);
 }
 
 __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expert_of,
@@ -178,9 +250,28 @@ __global__ void counts_from_list_kernel(const int* __restrict__ list, int n, int
 
 cudaError_t launch_lru_step(const Geo& g, const int* counts, int* slot_of, int* expert_of,
                             unsigned long long* stamp, unsigned long long* clock,
-                            StepRecord* rec, cudaStream_t st) {
+                            StepRecord* rec, unsigned long long* stats, cudaStream_t st) {
   lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, g.E, g.S, slot_of, expert_of, stamp, clock,
-                                             rec);
+                                             rec, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, int* offsets,
+                              int* row_of, int* tok_of, int* slot_of, int* expert_of,
+                              unsigned long long* stamp, unsigned long long* clock,
+                              StepRecord* rec, unsigned long long* stats, cudaStream_t st) {
+  const size_t smem = (size_t)g.E * perm::kPermWarps * 4 + (size_t)2 * g.E * 4 +
+                      (size_t)perm::kTokPerBlock * g.k * 4;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(route_tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         64 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  route_tail_kernel<<<1, kLruThreads, smem, st>>>(idx, N, g.k, g.E, g.S, counts, offsets, row_of,
+                                                  tok_of, slot_of, expert_of, stamp, clock, rec,
+                                                  stats);
   return cudaGetLastError();
 }
 

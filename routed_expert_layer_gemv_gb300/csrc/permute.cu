@@ -9,93 +9,39 @@
 // weights be read once per step, the point of the expert cache in
 // "FreeToken：把 284B MoE 塞进游戏 PC", zhichai.net, §二.)
 //
-// Block b owns tokens [b*128, b*128+128).  Each warp builds, for every expert
-// e, the 32-bit ballot of its tokens routed to e (idx rows are sorted, so a
-// lane walks its k experts in step with e).  Popcounts of those ballots give
-// the per-block histogram and each pair's rank inside the block; a scan over
-// blocks and experts gives the final rows.  No atomics anywhere.
+// Block b owns tokens [b*128, b*128+128) (ballot scheme: permute_dev.cuh); a
+// scan over blocks and experts turns block histograms and in-block ranks into
+// the final rows.  No atomics anywhere.
 #include <cstdio>
 #include <mutex>
 
 #include "common.cuh"
+#include "permute_dev.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kTokPerBlock = 128;
-constexpr int kPermWarps = kTokPerBlock / 32;
-
-// Ballots of one warp's tokens per expert into cm[e * kPermWarps + warp].
-MOE_DEV void build_ballots(const int* __restrict__ idx, int N, int k, int E, int t_base,
-                           uint32_t* cm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t = t_base + warp * 32 + lane;
-  const int* row = idx + (size_t)t * k;
-  int ptr = 0;
-  int nxt = (t < N && k > 0) ? row[0] : 0x7fffffff;
-  for (int e = 0; e < E; ++e) {
-    bool has = (nxt == e);
-    if (has) {
-      ++ptr;
-      nxt = ptr < k ? row[ptr] : 0x7fffffff;
-    }
-    uint32_t b = __ballot_sync(0xffffffffu, has);
-    if (lane == 0) cm[e * kPermWarps + warp] = b;
-  }
-}
-
-MOE_DEV int rank_in_block(const uint32_t* cm, int e) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int r = 0;
-  for (int w = 0; w < warp; ++w) r += __popc(cm[e * kPermWarps + w]);
-  return r + __popc(cm[e * kPermWarps + warp] & ((1u << lane) - 1u));
-}
+using perm::kTokPerBlock;
+using perm::kPermWarps;
+using perm::block_excl_scan;
 
 // Step 1 (multi-block): block histogram hist[b][e] and in-block ranks.
 __global__ void __launch_bounds__(kTokPerBlock)
 perm_hist_kernel(const int* __restrict__ idx, int N, int k, int E, int* __restrict__ hist,
                  int* __restrict__ rank) {
-  extern __shared__ uint32_t cm[];  // [E][kPermWarps]
+  extern __shared__ uint32_t sm[];
+  uint32_t* cm = sm;                                              // [E][kPermWarps]
+  int* rows = reinterpret_cast<int*>(sm + E * kPermWarps);        // [128][k]
   const int t_base = blockIdx.x * kTokPerBlock;
-  build_ballots(idx, N, k, E, t_base, cm);
+  perm::stage_rows(idx, N, k, t_base, rows);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int c = 0;
-    for (int w = 0; w < kPermWarps; ++w) c += __popc(cm[e * kPermWarps + w]);
-    hist[(size_t)blockIdx.x * E + e] = c;
-  }
+  perm::build_ballots(rows, k, E, cm);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = perm::block_count(cm, e);
   const int t = t_base + threadIdx.x;
   if (t < N)
-    for (int j = 0; j < k; ++j) rank[(size_t)t * k + j] = rank_in_block(cm, idx[(size_t)t * k + j]);
-}
-
-// Block-wide exclusive scan of v over blockDim.x threads (<= 1024); returns
-// the exclusive prefix, *total gets the sum.
-MOE_DEV int block_excl_scan(int v, int* total, int* sh /* >= 33 ints */) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  int inc = v;
-  for (int o = 1; o < 32; o <<= 1) {
-    int u = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += u;
-  }
-  if (lane == 31) sh[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int s = lane < nw ? sh[lane] : 0;
-    int si = s;
-    for (int o = 1; o < 32; o <<= 1) {
-      int u = __shfl_up_sync(0xffffffffu, si, o);
-      if (lane >= o) si += u;
-    }
-    if (lane < nw) sh[lane] = si - s;
-    if (lane == 31) sh[32] = si;
-  }
-  __syncthreads();
-  int res = sh[warp] + inc - v;
-  *total = sh[32];
-  __syncthreads();
-  return res;
+    for (int j = 0; j < k; ++j) rank[(size_t)t * k + j] = perm::rank_in_block(cm, rows[threadIdx.x * k + j]);
 }
 
 // Step 2 (one CTA of 1024 threads): per-expert block prefix, counts, offsets.
@@ -144,17 +90,18 @@ perm_single_kernel(const int* __restrict__ idx, int N, int k, int E, int* __rest
   uint32_t* cm = sm;                                           // [E][kPermWarps]
   int* off = reinterpret_cast<int*>(sm + E * kPermWarps);      // [E]
   int* sh = off + E;                                           // [33]
-  build_ballots(idx, N, k, E, 0, cm);
+  int* rows = sh + 33;                                         // [128][k]
+  perm::stage_rows(idx, N, k, 0, rows);
+  __syncthreads();
+  perm::build_ballots(rows, k, E, cm);
   __syncthreads();
   // exclusive scan of counts over e, kTokPerBlock experts at a time
   int carry = 0;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
-    int c = 0;
-    if (e < E)
-      for (int w = 0; w < kPermWarps; ++w) c += __popc(cm[e * kPermWarps + w]);
+    const int c = e < E ? perm::block_count(cm, e) : 0;
     int tot;
-    int ex = block_excl_scan(c, &tot, sh);
+    const int ex = block_excl_scan(c, &tot, sh);
     if (e < E) {
       counts[e] = c;
       offsets[e] = carry + ex;
@@ -167,8 +114,8 @@ perm_single_kernel(const int* __restrict__ idx, int N, int k, int E, int* __rest
   const int t = threadIdx.x;
   if (t < N) {
     for (int j = 0; j < k; ++j) {
-      const int e = idx[(size_t)t * k + j];
-      const int r = off[e] + rank_in_block(cm, e);
+      const int e = rows[t * k + j];
+      const int r = off[e] + perm::rank_in_block(cm, e);
       row_of[(size_t)t * k + j] = r;
       tok_of[r] = t;
     }
@@ -186,7 +133,7 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
                            int* row_of, int* tok_of, void* scratch, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
   if (N <= kTokPerBlock) {
-    size_t smem = (size_t)g.E * kPermWarps * 4 + (size_t)g.E * 4 + 33 * 4;
+    size_t smem = (size_t)g.E * kPermWarps * 4 + (size_t)g.E * 4 + 33 * 4 + (size_t)kTokPerBlock * g.k * 4;
     perm_single_kernel<<<1, kTokPerBlock, smem, st>>>(idx, N, g.k, g.E, counts, offsets, row_of,
                                                       tok_of);
     return cudaGetLastError();
@@ -194,8 +141,8 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
   const int nblk = (N + kTokPerBlock - 1) / kTokPerBlock;
   int* hist = static_cast<int*>(scratch);
   int* rank = hist + (size_t)nblk * g.E;
-  perm_hist_kernel<<<nblk, kTokPerBlock, (size_t)g.E * kPermWarps * 4, st>>>(idx, N, g.k, g.E,
-                                                                            hist, rank);
+  perm_hist_kernel<<<nblk, kTokPerBlock, (size_t)g.E * kPermWarps * 4 + (size_t)kTokPerBlock * g.k * 4,
+                     st>>>(idx, N, g.k, g.E, hist, rank);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   perm_scan_kernel<<<1, 1024, 0, st>>>(hist, nblk, g.E, counts, offsets);

@@ -1,0 +1,89 @@
+// Device pieces of the atomic-free permutation, shared by the permutation
+// kernels and the fused decode routing tail.
+//
+// Block b owns 128 consecutive tokens.  Each warp builds, for every expert e,
+// the 32-bit ballot of its tokens routed to e (a token's ids are sorted, so a
+// lane walks its k ids in step with e, reading them from shared memory).
+// Popcounts of the ballots give the block histogram and each pair's rank
+// among the block's earlier tokens routed to the same expert.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+namespace perm {
+
+constexpr int kTokPerBlock = 128;
+constexpr int kPermWarps = kTokPerBlock / 32;
+
+// Stage the id rows of tokens [t_base, t_base + 128) into shared memory
+// (threads of the first 128 cover one token each; k <= 32).
+MOE_DEV void stage_rows(const int* __restrict__ idx, int N, int k, int t_base, int* rows) {
+  for (int v = threadIdx.x; v < kTokPerBlock * k; v += blockDim.x) {
+    const int t = t_base + v / k;
+    rows[v] = t < N ? idx[(size_t)t_base * k + v] : 0x7fffffff;
+  }
+}
+
+// Ballots of warp w's tokens per expert into cm[e * kPermWarps + w]; run by
+// the first kPermWarps warps.  rows = the staged id rows.
+MOE_DEV void build_ballots(const int* rows, int k, int E, uint32_t* cm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int* row = rows + (warp * 32 + lane) * k;
+  int ptr = 0;
+  int nxt = row[0];
+  for (int e = 0; e < E; ++e) {
+    const bool has = (nxt == e);
+    if (has) {
+      ++ptr;
+      nxt = ptr < k ? row[ptr] : 0x7fffffff;
+    }
+    const uint32_t b = __ballot_sync(0xffffffffu, has);
+    if (lane == 0) cm[e * kPermWarps + warp] = b;
+  }
+}
+
+// Rank of this thread's token among the block's earlier tokens routed to e
+// (thread t of the first 128 = token t of the block).
+MOE_DEV int rank_in_block(const uint32_t* cm, int e) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int r = 0;
+  for (int w = 0; w < warp; ++w) r += __popc(cm[e * kPermWarps + w]);
+  return r + __popc(cm[e * kPermWarps + warp] & ((1u << lane) - 1u));
+}
+
+MOE_DEV int block_count(const uint32_t* cm, int e) {
+  int c = 0;
+  for (int w = 0; w < kPermWarps; ++w) c += __popc(cm[e * kPermWarps + w]);
+  return c;
+}
+
+// Block-wide exclusive scan over blockDim.x (<= 1024) threads; *total gets
+// the sum.  sh: >= 33 ints of shared memory.
+MOE_DEV int block_excl_scan(int v, int* total, int* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int inc = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = lane < nw ? sh[lane] : 0;
+    int si = s;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += u;
+    }
+    if (lane < nw) sh[lane] = si - s;
+    if (lane == 31) sh[32] = si;
+  }
+  __syncthreads();
+  const int res = sh[warp] + inc - v;
+  *total = sh[32];
+  __syncthreads();
+  return res;
+}
+
+}  // namespace perm
+}  // namespace moe

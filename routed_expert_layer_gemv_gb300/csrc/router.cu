@@ -12,7 +12,9 @@
 // warp reduces TN dot products with shuffles.  CTA (0, tile) also writes each
 // token's power-of-two exponent used by the expert GEMV to convert x to f16
 // without overflow.
-// topk kernel: one warp per token; k rounds of a warp-wide argmax.
+// topk: one warp per token on its logits row staged in shared memory; k rounds
+// of a warp-wide argmax.  For decode-sized batches the last CTA of the logits
+// kernel runs it, so routing is one launch.
 #include "common.cuh"
 
 namespace moe {
@@ -21,13 +23,75 @@ namespace {
 
 constexpr int kRouterWarps = 8;
 
-template <int TN>
+MOE_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+
+// One warp: the k largest of the logits row L (shared memory, E <= 1024
+// entries; ties to the lower expert id), gates, written in ascending id order.
+MOE_DEV void topk_row(const float* L, int E, int k, int norm_topk, int* idx, float* gates) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;  // bit i: entry lane + 32 i already selected
+  int my_e = -1;
+  float my_v = 0.f, top = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int i = 0, e = lane; e < E; ++i, e += 32) {
+      if (taken & (1u << i)) continue;
+      const float v = L[e];
+      if (better(v, e, bv, be)) { bv = v; be = e; }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (j == 0) top = bv;
+    if (lane == j) { my_e = be; my_v = bv; }
+  }
+  // gates (fp32): softmax over the selected logits, or the full softmax
+  const float num = lane < k ? expf(my_v - top) : 0.f;
+  float den = 0.f;
+  if (norm_topk) {
+    den = num;
+  } else {
+    for (int e = lane; e < E; e += 32) den += expf(L[e] - top);
+  }
+  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  // ascending expert order: rank of my_e among the k selected
+  int rank = 0;
+  for (int i = 0; i < k; ++i) {
+    const int oe = __shfl_sync(0xffffffffu, my_e, i);
+    rank += (lane < k && oe < my_e) ? 1 : 0;
+  }
+  if (lane < k) {
+    idx[rank] = my_e;
+    gates[rank] = num / den;
+  }
+}
+
+// Stage row t of the logits into this warp's shared row, bypassing L1 (the
+// row may have been written by other CTAs of the same launch).
+MOE_DEV void stage_logits(const float* logits, int t, int E, float* Ls) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < E; e += 32) Ls[e] = __ldcg(logits + (size_t)t * E + e);
+  __syncwarp();
+}
+
+// logits = x W_r^T (+ b): one warp per expert, TN tokens per CTA held in
+// shared memory.  CTA (0, tile) also writes each token's f16 exponent.  With
+// FUSE, the last CTA to finish (a device counter, reset by that CTA) runs the
+// top-k of every token, so decode-sized batches route in one launch.
+template <int TN, bool FUSE>
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_logits_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
                      const float* __restrict__ Wr, const float* __restrict__ bias,
-                     float* __restrict__ logits, int* __restrict__ xexp) {
+                     float* __restrict__ logits, int* __restrict__ xexp, int k, int norm_topk,
+                     int* __restrict__ idx, float* __restrict__ gates,
+                     unsigned int* __restrict__ counter) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [TN][d]
+  __shared__ bool last;
   const int t0 = blockIdx.y * TN;
   const int nt = min(TN, N - t0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -35,7 +99,7 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
   // stage the token tile (16-byte vectors; d is a multiple of 128)
   const int vec_per_row = d / 8;
   for (int v = threadIdx.x; v < TN * vec_per_row; v += blockDim.x) {
-    int t = v / vec_per_row, c = v % vec_per_row;
+    const int t = v / vec_per_row, c = v % vec_per_row;
     uint4 val = make_uint4(0, 0, 0, 0);
     if (t < nt) val = reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d)[c];
     reinterpret_cast<uint4*>(xs + (size_t)t * d)[c] = val;
@@ -61,115 +125,113 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
   }
 
   const int e = blockIdx.x * kRouterWarps + warp;
-  if (e >= E) return;
-  float acc[TN];
+  if (e < E) {
+    float acc[TN];
 #pragma unroll
-  for (int t = 0; t < TN; ++t) acc[t] = 0.f;
-  const float4* w4 = reinterpret_cast<const float4*>(Wr + (size_t)e * d);
-  for (int i4 = lane; i4 < d / 4; i4 += 32) {
-    float4 w = __ldg(w4 + i4);
+    for (int t = 0; t < TN; ++t) acc[t] = 0.f;
+    const float4* w4 = reinterpret_cast<const float4*>(Wr + (size_t)e * d);
+    for (int i4 = lane; i4 < d / 4; i4 += 32) {
+      const float4 w = __ldg(w4 + i4);
+#pragma unroll
+      for (int t = 0; t < TN; ++t) {
+        const uint2 xv = reinterpret_cast<const uint2*>(xs + (size_t)t * d)[i4];
+        const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xffff0000u);
+        const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xffff0000u);
+        acc[t] = fmaf(w.x, x0, acc[t]);
+        acc[t] = fmaf(w.y, x1, acc[t]);
+        acc[t] = fmaf(w.z, x2, acc[t]);
+        acc[t] = fmaf(w.w, x3, acc[t]);
+      }
+    }
 #pragma unroll
     for (int t = 0; t < TN; ++t) {
-      uint2 xv = reinterpret_cast<const uint2*>(xs + (size_t)t * d)[i4];
-      float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xffff0000u);
-      float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xffff0000u);
-      acc[t] = fmaf(w.x, x0, acc[t]);
-      acc[t] = fmaf(w.y, x1, acc[t]);
-      acc[t] = fmaf(w.z, x2, acc[t]);
-      acc[t] = fmaf(w.w, x3, acc[t]);
+      float v = acc[t];
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc[t] = v;
+    }
+    if (lane == 0) {
+      const float b = bias ? bias[e] : 0.f;
+#pragma unroll
+      for (int t = 0; t < TN; ++t)
+        if (t < nt) logits[(size_t)(t0 + t) * E + e] = acc[t] + b;
     }
   }
-#pragma unroll
-  for (int t = 0; t < TN; ++t) {
-    float v = acc[t];
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    acc[t] = v;
-  }
-  if (lane == 0) {
-    float b = bias ? bias[e] : 0.f;
-#pragma unroll
-    for (int t = 0; t < TN; ++t)
-      if (t < nt) logits[(size_t)(t0 + t) * E + e] = acc[t] + b;
+  if (FUSE) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned int n = atomicAdd(counter, 1u);
+      last = n == gridDim.x * gridDim.y - 1;
+    }
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      float* Ls = reinterpret_cast<float*>(smem_raw + (size_t)TN * d * 2) + (size_t)warp * E;
+      for (int t = warp; t < N; t += kRouterWarps) {
+        stage_logits(logits, t, E, Ls);
+        topk_row(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
+        __syncwarp();
+      }
+      if (threadIdx.x == 0) *counter = 0u;
+    }
   }
 }
-
-MOE_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
 
 __global__ void __launch_bounds__(256)
 router_topk_kernel(const float* __restrict__ logits, int N, int E, int k, int norm_topk,
                    int* __restrict__ idx, float* __restrict__ gates) {
-  const int lane = threadIdx.x & 31;
+  extern __shared__ float Lsm[];
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= N) return;
-  const float* L = logits + (size_t)t * E;
-  uint32_t taken = 0;  // bit i: entry lane + 32 i already selected (E <= 1024)
-  int my_e = -1;
-  float my_v = 0.f, top = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int i = 0, e = lane; e < E; ++i, e += 32) {
-      if (taken & (1u << i)) continue;
-      float v = L[e];
-      if (better(v, e, bv, be)) { bv = v; be = e; }
-    }
-    for (int o = 16; o; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (j == 0) top = bv;
-    if (lane == j) { my_e = be; my_v = bv; }
-  }
-  // gates (fp32): softmax over the selected logits, or the full softmax
-  float num = lane < k ? expf(my_v - top) : 0.f;
-  float den = 0.f;
-  if (norm_topk) {
-    den = num;
-  } else {
-    for (int e = lane; e < E; e += 32) den += expf(L[e] - top);
-  }
-  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  // ascending expert order: rank of my_e among the k selected
-  int rank = 0;
-  for (int i = 0; i < k; ++i) {
-    int oe = __shfl_sync(0xffffffffu, my_e, i);
-    rank += (lane < k && oe < my_e) ? 1 : 0;
-  }
-  if (lane < k) {
-    idx[(size_t)t * k + rank] = my_e;
-    gates[(size_t)t * k + rank] = num / den;
-  }
+  float* Ls = Lsm + (size_t)(threadIdx.x >> 5) * E;
+  stage_logits(logits, t, E, Ls);
+  topk_row(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
 }  // namespace
 
 cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
                           const float* bias, float* logits, int* idx, float* gates,
-                          int* xexp, cudaStream_t st) {
+                          int* xexp, unsigned int* counter, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
   const int TN = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : 8;
+  const bool fuse = N <= 64 && counter != nullptr;
   dim3 grid((g.E + kRouterWarps - 1) / kRouterWarps, (N + TN - 1) / TN);
-  size_t smem = (size_t)TN * g.d * sizeof(__nv_bfloat16);
-  switch (TN) {
-#define MOE_ROUTER_CASE(V)                                                                   \
-  case V:                                                                                    \
-    if (smem > 48 * 1024)                                                                    \
-      cudaFuncSetAttribute(router_logits_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                       \
-    router_logits_kernel<V><<<grid, kRouterWarps * 32, smem, st>>>(x, N, g.d, g.E, Wr, bias,   \
-                                                                  logits, xexp);             \
-    break;
-    MOE_ROUTER_CASE(1)
-    MOE_ROUTER_CASE(2)
-    MOE_ROUTER_CASE(4)
-    MOE_ROUTER_CASE(8)
-#undef MOE_ROUTER_CASE
+  const size_t smem = (size_t)TN * g.d * sizeof(__nv_bfloat16) +
+                      (fuse ? (size_t)kRouterWarps * g.E * sizeof(float) : 0);
+  cudaError_t err = cudaSuccess;
+#define MOE_ROUTER_CASE(V, F)                                                                \
+  {                                                                                          \
+    static bool attr = false;                                                                \
+    if (!attr) {                                                                             \
+      err = cudaFuncSetAttribute(router_logits_kernel<V, F>,                                 \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);   \
+      if (err != cudaSuccess) return err;                                                    \
+      attr = true;                                                                           \
+    }                                                                                        \
+    router_logits_kernel<V, F><<<grid, kRouterWarps * 32, smem, st>>>(                       \
+        x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter);     \
   }
-  cudaError_t err = cudaGetLastError();
+  if (fuse) {
+    switch (TN) {
+      case 1: MOE_ROUTER_CASE(1, true) break;
+      case 2: MOE_ROUTER_CASE(2, true) break;
+      case 4: MOE_ROUTER_CASE(4, true) break;
+      default: MOE_ROUTER_CASE(8, true) break;
+    }
+    return cudaGetLastError();
+  }
+  switch (TN) {
+    case 1: MOE_ROUTER_CASE(1, false) break;
+    case 2: MOE_ROUTER_CASE(2, false) break;
+    case 4: MOE_ROUTER_CASE(4, false) break;
+    default: MOE_ROUTER_CASE(8, false) break;
+  }
+#undef MOE_ROUTER_CASE
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  router_topk_kernel<<<(N + 7) / 8, 256, 0, st>>>(logits, N, g.E, g.k, g.norm_topk, idx, gates);
+  router_topk_kernel<<<(N + 7) / 8, 256, (size_t)8 * g.E * sizeof(float), st>>>(logits, N, g.E, g.k,
+                                                                              g.norm_topk, idx, gates);
   return cudaGetLastError();
 }
 

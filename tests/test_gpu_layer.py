@@ -51,10 +51,11 @@ def test_forward_all_resident(spec, N):
     L.close()
 
 
-def _decode_run(spec, seed, batch, steps, check_every=1):
+def _decode_run(spec, seed, batch, steps, check_every=1, fill=capi.MOE_FILL_MEMCPY):
     N = batch
     experts = CachedExperts(spec, seed, cap=96)
     L = build_layer(spec, seed, N, experts_fn=experts)
+    capi.moe_set_fill_mode(L.h, fill)
     O = oracle_layer(spec, seed, experts)
     T = SlotTable(spec.E, spec.n_slots)
     xs, _ = wl.ar1_tokens(seed, batch, steps, spec.d_model, 0.9, reject_near_ties(spec, seed))
@@ -64,17 +65,24 @@ def _decode_run(spec, seed, batch, steps, check_every=1):
         y, info = L.forward(xt, regime=DEC)
         ref, idx, _ = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
         acc = T.step(idx.reshape(-1))
-        assert info.host_synced == 1
-        assert info.n_distinct == len(acc)
-        assert info.n_misses == sum(1 for a in acc if not a[2])
-        assert info.fill_bytes == info.n_misses * L.expert_bytes
-        tot_miss += info.n_misses
-        tot_u += info.n_distinct
-        waves = max(waves, info.n_waves)
+        n_miss = sum(1 for a in acc if not a[2])
+        if fill == capi.MOE_FILL_MEMCPY:
+            assert info.host_synced == 1
+            assert info.n_distinct == len(acc)
+            assert info.n_misses == n_miss
+            assert info.fill_bytes == info.n_misses * L.expert_bytes
+            waves = max(waves, info.n_waves)
+        else:
+            assert info.host_synced == 0
+            waves = max(waves, (len(acc) + spec.n_slots - 1) // spec.n_slots)
+        tot_miss += n_miss
+        tot_u += len(acc)
         if t % check_every == 0 or t == steps - 1:
             assert_close_layer(y, ref, "step %d" % t)
             eo, st, clk = capi.moe_lru_get_state(L.h, spec.n_slots)
             assert eo == T.expert_of and st == T.stamp and clk == T.clock
+    steps_d, u_d, hits_d, miss_d = capi.moe_stats(L.h)
+    assert (steps_d, u_d, miss_d) == (steps, tot_u, tot_miss) and hits_d == tot_u - tot_miss
     L.close()
     return tot_miss, tot_u, waves
 
@@ -97,6 +105,31 @@ def test_decode_284b_shape_shared_and_waves():
     spec = wl.DECODE_284B.layer
     miss, u, waves = _decode_run(spec, 5, 8, 3)
     assert waves >= 2
+
+
+@pytest.mark.parametrize("batch,steps", [(4, 6), (16, 3)])
+def test_decode_device_fill(batch, steps):
+    # misses pulled from the pinned pool by a copy kernel: no host wait per step
+    spec = wl.DECODE_35B.layer
+    miss, u, waves = _decode_run(spec, 7, batch, steps, fill=capi.MOE_FILL_DEVICE)
+    assert miss > 0
+
+
+def test_prefill_device_fill_waves():
+    spec = small_spec(E=24, k=3, d_model=512, d_ff=256, n_slots=5, fmt="nvfp4", has_shared=True,
+                      has_bias=True)
+    seed, N = 31, 96
+    experts = CachedExperts(spec, seed)
+    L = build_layer(spec, seed, N, experts_fn=experts)
+    capi.moe_set_fill_mode(L.h, capi.MOE_FILL_DEVICE)
+    O = oracle_layer(spec, seed, experts)
+    for step in range(2):
+        x = _tokens(spec, seed + step, N)
+        y, info = L.forward(bf16_tensor(x), regime=capi.MOE_REGIME_PREFILL)
+        assert info.host_synced == 0
+        ref, _, _ = O.forward(wl.bf16_bits_to_f64(x), "prefill")
+        assert_close_layer(y, ref, "prefill device fill step %d" % step)
+    L.close()
 
 
 def test_decode_nvfp4_bias_small_cache():
