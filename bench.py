@@ -140,7 +140,7 @@ def gateup_bytes(spec, layout, n_experts, n_tokens):
     return n_experts * w + n_tokens * d * 2 + rows * f * 4
 
 
-def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile):
+def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile, fill=None):
     """K timed decode steps after W warm-up steps on a fresh layer (cold cache).
     profile=False: the clean pass behind `value`; profile=True: the same steps
     with the library's per-launch events on (kernel times for the roofline)."""
@@ -150,15 +150,18 @@ def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile):
     x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
     xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
     L = build_layer(spec, seed, batch)
+    capi.moe_set_fill_mode(L.h, capi.MOE_FILL_MEMCPY if fill is None else fill)
     y = torch.empty(batch, spec.d_model, dtype=torch.bfloat16, device="cuda")
     with torch.cuda.stream(st):
         for t in range(W):
             L.forward(xs[t], y, stream=st)
     torch.cuda.synchronize()
+    stats0 = capi.moe_stats(L.h)
+    torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     capi.moe_profile(L.h, profile)
-    launches = misses = distinct = 0
-    fill = 0
+    launches = 0
+    fill_b = 0
     ffn_bytes = 0
     with torch.cuda.stream(st):
         for t in range(K):
@@ -167,17 +170,17 @@ def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile):
             _, info = L.forward(xs[W + t], y, stream=st)
             ev[t][1].record(st)
             launches += info.n_launches
-            misses += info.n_misses
-            distinct += info.n_distinct
-            fill += info.fill_bytes
+            fill_b += info.fill_bytes
             ffn_bytes += gateup_bytes(spec, L.layout, info.n_distinct, batch)
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in ev)
     prof = capi.moe_profile_read(L.h)
     capi.moe_profile(L.h, False)
+    stats1 = capi.moe_stats(L.h)
     L.close()
+    d_misses, d_distinct = stats1[3] - stats0[3], stats1[1] - stats0[1]
     return dict(batch=batch, steps=K, ms=ms, tokens=K * batch, launches=launches,
-                misses=misses, distinct=distinct, fill_bytes=fill, prof=prof,
+                misses=d_misses, distinct=d_distinct, fill_bytes=fill_b, prof=prof,
                 gateup_bytes=ffn_bytes)
 
 
@@ -366,6 +369,8 @@ def main():
     torch.cuda.synchronize()
     clk = clocks.stop()
     pruns = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, True) for b in batches]
+    druns = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False, capi.MOE_FILL_DEVICE)
+             for b in batches]
     e2e_runs = [run_decode_e2e(args, b, torch, capi, wl, build_layer, flush) for b in batches]
 
     ms = sum(r["ms"] for r in runs)
@@ -392,7 +397,7 @@ def main():
             "bytes_per_launch": g_bytes / max(g_n, 1), "ms_per_launch": g_ms / max(g_n, 1)}
 
     per_batch = {}
-    for r, e, pr in zip(runs, e2e_runs, pruns):
+    for r, e, pr, dr in zip(runs, e2e_runs, pruns, druns):
         p = pr["prof"]
         per_batch[str(r["batch"])] = {
             "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
@@ -401,6 +406,7 @@ def main():
             "miss_rate": r["misses"] / max(1, r["distinct"]),
             "fill_GB_per_s": r["fill_bytes"] / max(1e-9, p["fill"][0] / 1000.0) / 1e9 if p["fill"][0] else None,
             "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
+            "device_fill_tokens_per_s": dr["tokens"] / (dr["ms"] / 1000.0),
         }
     prefill = None
     if not args.no_prefill:
