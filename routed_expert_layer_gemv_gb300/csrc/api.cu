@@ -62,6 +62,7 @@ struct moe_layer {
   StepRecord* rec = nullptr;
   StepRecord* rec_host = nullptr;
   float* h = nullptr;
+  float* hmax = nullptr;          // decode: per-row maxima of phase 1 per 64 columns
   float* O = nullptr;
   __nv_bfloat16* x_stage = nullptr;
   __nv_bfloat16* y_stage = nullptr;
@@ -75,6 +76,7 @@ struct moe_layer {
   void* tiles = nullptr;
   int* n_tiles = nullptr;
   PrefillPlan* plan = nullptr;
+  GemvPlan* gplan = nullptr;
   unsigned int* rcounter = nullptr;  // CTA counter of the one-launch router
   int* err_host = nullptr;       // kernels' timeout flag (mapped pinned memory)
   int* err_dev = nullptr;
@@ -203,6 +205,8 @@ void release(moe_layer* L) {
   L->err_host = nullptr;
   if (L->plan) prefill_plan_destroy(L->plan);
   L->plan = nullptr;
+  if (L->gplan) gemv_plan_destroy(L->gplan);
+  L->gplan = nullptr;
   if (L->ev_route) cudaEventDestroy(L->ev_route);
   if (L->ev_fill) cudaEventDestroy(L->ev_fill);
   if (L->ev_comp) cudaEventDestroy(L->ev_comp);
@@ -345,7 +349,8 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   MOE_ALLOC(tok_of, Nm * g.k * 4);
   MOE_ALLOC(perm_scratch, permute_scratch_bytes(g, (int)Nm));
   MOE_ALLOC(rec, rec_bytes(g.E));
-  MOE_ALLOC(h, rows * g.f * 4);
+  MOE_ALLOC(h, rows * g.f * 8);   // decode: scaled W_g x and W_u x per row
+  MOE_ALLOC(hmax, rows * (g.f / 64) * 8);
   MOE_ALLOC(O, rows * g.d * 4);
   MOE_ALLOC(x_stage, Nm * g.d * 2);
   MOE_ALLOC(y_stage, Nm * g.d * 2);
@@ -372,6 +377,10 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     } else {
       *L->err_host = 0;
     }
+  }
+  if (rc == MOE_OK) {
+    L->gplan = gemv_plan_create(g, L->slots);
+    if (!gemv_plan_ready(L->gplan)) rc = MOE_ERR_CUDA;   // tensor-map encoding failed
   }
   if (rc == MOE_OK && prefill_ok) {
     L->plan = prefill_plan_create(g, L->slots, L->xq_codes, prows, L->hq_codes);
@@ -602,6 +611,10 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   if (!x_dev) {
     MOE_CUDA(L, cudaMemcpyAsync(L->x_stage, x, xbytes, cudaMemcpyHostToDevice, st));
     xd = L->x_stage;
+  } else if (reinterpret_cast<uintptr_t>(x) % 16) {
+    // the kernels read x in 16-byte vectors
+    MOE_CUDA(L, cudaMemcpyAsync(L->x_stage, x, xbytes, cudaMemcpyDeviceToDevice, st));
+    xd = L->x_stage;
   }
   if (!y_dev) yd = L->y_stage;
 
@@ -647,6 +660,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   a.mode = kRangeHits;
   a.wave = 0;
   a.with_shared = g.has_shared;
+  a.err = L->err_dev;
+  a.hmax = L->hmax;
   const int cap = n_ent_cap(L, N);
   const float gx = g.fmt == MOE_NVFP4 ? L->desc.act_scale_x : 1.0f;
   const float gh = g.fmt == MOE_NVFP4 ? L->desc.act_scale_h : 1.0f;
@@ -673,7 +688,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
                                 L->hq_scales, L->O, gx, gh, L->err_dev, st, evp);
       L->launches += 3;
     } else {
-      ce = launch_gemv_decode(g, a, xd, L->xexp, L->h, L->O, n_ent, st, evp);
+      ce = launch_gemv_decode(g, L->gplan, a, xd, L->xexp, L->h, L->O, n_ent, L->num_sms, st, evp);
       L->launches += 2;
     }
     if (ce != cudaSuccess) return cuda_fail(L, ce, prefill ? "launch_prefill_gemms" : "launch_gemv_decode");

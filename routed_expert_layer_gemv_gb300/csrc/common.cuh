@@ -101,12 +101,20 @@ struct GemvArgs {
   int N;
   int mode, wave;              // RangeMode + wave index
   int with_shared;             // also run the shared expert (rows N*k .. N*k+N)
+  int* err;                    // set to 1 when a bounded wait gives up
+  float* hmax;                 // [rows][2][d_ff / 64]: max |W_g x|, |W_u x| per 64 columns
 };
+struct GemvPlan;               // tensor maps of the slot pool's weight codes
 bool gemv_shape_ok(const Geo& g);
-// ev (may be null): 4 events recorded before/after phase 1 and phase 2
-cudaError_t launch_gemv_decode(const Geo& g, const GemvArgs& a, const __nv_bfloat16* x,
-                               const int* xexp, float* h, float* O, int n_ent_max,
-                               cudaStream_t st, const cudaEvent_t* ev);
+GemvPlan* gemv_plan_create(const Geo& g, const uint8_t* slots);
+void gemv_plan_destroy(GemvPlan* pl);
+bool gemv_plan_ready(const GemvPlan* pl);
+// x must be 16-byte aligned; h holds 2 * d_ff floats per row (phase 1
+// writes W_g x and W_u x, phase 2 forms SiLU(a) * u from them).  ev (may be
+// null): 4 events recorded before/after phase 1 and phase 2
+cudaError_t launch_gemv_decode(const Geo& g, const GemvPlan* pl, const GemvArgs& a,
+                               const __nv_bfloat16* x, const int* xexp, float* h, float* O,
+                               int n_ent_max, int num_sms, cudaStream_t st, const cudaEvent_t* ev);
 // prefill.cu
 struct PrefillPlan;
 bool prefill_shape_ok(const Geo& g);
