@@ -133,11 +133,25 @@ def decode_tokens(wl, spec, seed, batch, steps):
 
 def gateup_bytes(spec, layout, n_experts, n_tokens):
     """Algorithmic bytes of phase 1 for one step: the gate and up codes and
-    scales of each expert read once, x read, h written (fp32)."""
+    scales of each expert read once, x read, W_g x and W_u x written (fp32)."""
     d, f = spec.d_model, spec.d_ff
     w = 2 * (f * d // 2 + f * d // spec.block)
     rows = n_tokens * spec.k + (n_tokens if spec.has_shared else 0)
-    return n_experts * w + n_tokens * d * 2 + rows * f * 4
+    return n_experts * w + n_tokens * d * 2 + rows * 2 * f * 4
+
+
+def traffic_ratio(kernel, workload):
+    """DRAM bytes / algorithmic bytes of a launch, from the ncu capture listed
+    in profiles/traffic.txt (None when the kernel has no current capture)."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.txt")
+    try:
+        for line in open(path):
+            f = line.split()
+            if len(f) >= 5 and not line.startswith("#") and f[0] == kernel and f[1] == workload:
+                return float(f[4])
+    except OSError:
+        pass
+    return None
 
 
 def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile, fill=None):
@@ -391,9 +405,13 @@ def main():
     g_n = sum(r["prof"]["gateup"][1] for r in pruns)
     g_bytes = sum(r["gateup_bytes"] for r in pruns)
     achieved = (g_bytes / max(g_n, 1)) / ((g_ms / max(g_n, 1)) / 1000.0) / 1e9 if g_ms > 0 else None
+    ratio = traffic_ratio("gemv_gateup", "decode35b")
     roof = {"bound": "hbm", "kernel": "gemv_gateup (expert FFN phase 1)", "achieved": achieved,
             "peak": peak, "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
-            "traffic": None, "peak_kind": peak_kind,
+            "traffic": ratio * g_bytes / max(g_n, 1) if ratio else None, "peak_kind": peak_kind,
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one captured launch "
+                              "(profiles/gemv_stream_decode35b_b16.md) scaled to this run's bytes per launch"
+                              if ratio else None,
             "bytes_per_launch": g_bytes / max(g_n, 1), "ms_per_launch": g_ms / max(g_n, 1)}
 
     per_batch = {}

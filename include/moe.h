@@ -115,9 +115,11 @@ typedef struct {
 int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out);
 
 /* Create a layer on the current device: validates the descriptor, allocates
- * the slot pool, table and workspaces, creates the fill stream.  The cache
+ * the slot pool, table and workspaces, creates the fill streams.  The cache
  * starts empty (every slot free).  MOE_ERR_ARG on an invalid descriptor,
- * MOE_ERR_OOM when device memory runs out (nothing is leaked). */
+ * MOE_ERR_UNSUPPORTED when d_model or d_ff exceeds 8192 (the decode kernels
+ * stage one token group's activations in shared memory), MOE_ERR_OOM when
+ * device memory runs out (nothing is leaked). */
 int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out);
 int moe_layer_destroy(moe_layer_t layer);
 
