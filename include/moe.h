@@ -109,7 +109,8 @@ typedef struct {
 #define MOE_PROF_COMBINE     5
 #define MOE_PROF_FILL        6  /* host -> slot copies on the fill stream       */
 #define MOE_PROF_PREFILL     7  /* prefill: activation gather + FP4 quantiser   */
-#define MOE_PROF_KINDS       8
+#define MOE_PROF_COMMIT      8  /* staged misses copied into their LRU slots    */
+#define MOE_PROF_KINDS       9
 
 /* Layout of one expert for a descriptor (no GPU work). */
 int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out);
@@ -173,7 +174,10 @@ int moe_lru_set_state(moe_layer_t layer, const int* expert_of_slot,
  * N == 0 is a no-op; 0 < N <= max_tokens.  With misses (possible unless
  * every expert is resident) the call waits on the host for the step's routing
  * (one small device->host copy) and then issues the slot fills on the
- * layer's fill stream; otherwise it returns without waiting.  regime:
+ * layer's fill streams; otherwise it returns without waiting.  Misses beyond
+ * the first n_slots accesses of a step are filled into staging slots at once
+ * and copied into their LRU slots after the step's expert FFN, so the cache
+ * state after the call is the LRU's either way.  regime:
  * MOE_REGIME_*.  MOE_ERR_NOT_INSTALLED if a miss has no host source. */
 int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
                 int regime, moe_forward_info* info);

@@ -29,7 +29,7 @@ MOE_ERR_UNSUPPORTED = -8
 MOE_MXFP4 = 0
 MOE_NVFP4 = 1
 
-MOE_PROF_NAMES = ["router", "permute", "lru", "gateup", "down", "combine", "fill", "prefill"]
+MOE_PROF_NAMES = ["router", "permute", "lru", "gateup", "down", "combine", "fill", "prefill", "commit"]
 
 MOE_FILL_MEMCPY = 0
 MOE_FILL_DEVICE = 1

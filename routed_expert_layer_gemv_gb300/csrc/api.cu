@@ -6,10 +6,12 @@
 // of the GEMV):
 //   caller stream: router -> permute -> LRU step -> [record copy to host]
 //                  -> expert GEMV over the hits (+ shared expert)
-//   host:          wait for the record, then per wave of n_slots accesses:
-//   fill stream:   cudaMemcpyAsync pinned host expert -> evicted slot
-//   caller stream: wait for the wave's fills -> expert GEMV over its misses
-//   caller stream: combine -> y
+//   host:          wait for the record, then for every miss at once:
+//   fill streams:  cudaMemcpyAsync pinned host expert -> its slot (first wave
+//                  of n_slots accesses) or a staging slot (later accesses,
+//                  whose LRU slots this step still reads)
+//   caller stream: wait for the fills -> expert GEMV over all misses
+//                  -> commit staged experts into their LRU slots -> combine -> y
 // The hits are computed while the host reads the record and the fills are in
 // flight.  When every expert is resident (n_slots >= E, all installed) no
 // miss can happen and the step runs without any host wait.
@@ -87,7 +89,7 @@ struct moe_layer {
   bool shared_set = false;
   cudaStream_t fill[kFillStreams] = {};       // miss fills, round robin
   cudaEvent_t ev_fills[kFillStreams] = {};
-  cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_comp = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_fill = nullptr;
   int fill_mode = MOE_FILL_MEMCPY;
   const uint8_t* pool_dev = nullptr;          // device address of the host pool
   unsigned long long* stats = nullptr;        // steps, distinct, hits, misses
@@ -209,14 +211,13 @@ void release(moe_layer* L) {
   L->gplan = nullptr;
   if (L->ev_route) cudaEventDestroy(L->ev_route);
   if (L->ev_fill) cudaEventDestroy(L->ev_fill);
-  if (L->ev_comp) cudaEventDestroy(L->ev_comp);
   for (int i = 0; i < kFillStreams; ++i) {
     if (L->ev_fills[i]) cudaEventDestroy(L->ev_fills[i]);
     if (L->fill[i]) cudaStreamDestroy(L->fill[i]);
     L->ev_fills[i] = nullptr;
     L->fill[i] = nullptr;
   }
-  L->ev_route = L->ev_fill = L->ev_comp = nullptr;
+  L->ev_route = L->ev_fill = nullptr;
 }
 
 int pointer_kind(const void* p, bool* on_device, int device) {
@@ -324,14 +325,16 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     delete L;
     return MOE_ERR_CUDA;
   }
-  const Geo& g = L->g;
   const size_t Nm = desc->max_tokens;
+  // staging slots: one per miss a step can have beyond the first wave of n_slots
+  L->g.X = (int)std::max<long long>(0, std::min<long long>(L->g.E, (long long)Nm * L->g.k) - L->g.S);
+  const Geo& g = L->g;
   const size_t rows = Nm * g.k + (g.has_shared ? Nm : 0);
   rc = MOE_OK;
 #define MOE_ALLOC(ptr, bytes) \
   if (rc == MOE_OK) rc = dalloc(L, &L->ptr, (bytes))
-  // n_slots + 1 experts: the last one is the shared expert (resident, not LRU)
-  MOE_ALLOC(slots, (size_t)(g.S + 1) * g.ebytes);
+  // n_slots LRU slots, the shared expert (resident, not LRU), then the staging slots
+  MOE_ALLOC(slots, (size_t)(g.S + 1 + g.X) * g.ebytes);
   if (rc == MOE_OK) L->shared_w = L->slots + (size_t)g.S * g.ebytes;
   MOE_ALLOC(Wr, (size_t)g.E * g.d * 4);
   MOE_ALLOC(bias, (size_t)g.E * 4);
@@ -401,8 +404,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
             cudaEventCreateWithFlags(&L->ev_fills[i], cudaEventDisableTiming) == cudaSuccess;
     if (!sok ||
         cudaEventCreateWithFlags(&L->ev_route, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&L->ev_comp, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       rc = MOE_ERR_CUDA;
     }
@@ -658,7 +660,6 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   a.tok_of = L->tok_of;
   a.N = N;
   a.mode = kRangeHits;
-  a.wave = 0;
   a.with_shared = g.has_shared;
   a.err = L->err_dev;
   a.hmax = L->hmax;
@@ -683,7 +684,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     }
     cudaError_t ce;
     if (prefill) {
-      ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, N, a.mode, a.wave, a.with_shared,
+      ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, N, a.mode, a.with_shared,
                                 L->tiles, L->n_tiles, L->slots, L->xq_scales, L->hq_codes,
                                 L->hq_scales, L->O, gx, gh, L->err_dev, st, evp);
       L->launches += 3;
@@ -697,32 +698,26 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   int grc = gemv(cap + (g.has_shared ? 1 : 0));
   if (grc) return grc;
 
+  // Misses.  Every fill starts as soon as the routing is known: first-wave
+  // misses go straight into their (free or stale) LRU slots, later ones into
+  // staging slots, since their LRU slots are still read by this step; one
+  // expert-FFN launch then covers all misses, and the staged experts that
+  // keep their LRU slot are committed into it on the caller stream.
   size_t fill_bytes = 0;
   int U = -1, n_hit = -1, n_miss = 0, waves = 1;
+  const int max_miss = std::min(g.E, N * g.k);
+  const int max_staged = std::max(0, max_miss - g.S);
+  bool any_miss = true, any_staged = max_staged > 0;
   if (dev_fill) {
-    // no host wait: one copy kernel and one expert-FFN launch per possible wave
-    const int max_waves = (std::min(g.E, N * g.k) + g.S - 1) / g.S;
-    for (int w = 0; w < max_waves; ++w) {
-      cudaStream_t fs = L->fill[0];
-      if (w == 0) {
-        MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
-      } else {
-        MOE_CUDA(L, cudaEventRecord(L->ev_comp, st));
-        MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_comp, 0));
-      }
-      cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
-      MOE_CUDA(L, launch_fill_copy(g, L->rec, w, std::min(cap, g.S), L->pool_dev, L->slots, fs));
-      prof_end(pf, fs);
-      L->launches += 1;
-      MOE_CUDA(L, cudaEventRecord(L->ev_fill, fs));
-      MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
-      a.mode = kRangeWaveMisses;
-      a.wave = w;
-      a.with_shared = 0;
-      grc = gemv(std::min(cap, g.S));
-      if (grc) return grc;
-    }
-    waves = max_waves;
+    cudaStream_t fs = L->fill[0];
+    MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
+    cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
+    MOE_CUDA(L, launch_fill_copy(g, L->rec, max_miss, L->pool_dev, L->slots, fs));
+    prof_end(pf, fs);
+    L->launches += 1;
+    MOE_CUDA(L, cudaEventRecord(L->ev_fill, fs));
+    MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
+    waves = (max_miss + g.S - 1) / g.S;
   } else if (!resident) {
     MOE_CUDA(L, cudaEventSynchronize(L->ev_route));
     const StepRecord* r = L->rec_host;
@@ -732,32 +727,25 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     waves = (U + g.S - 1) / g.S;
     const int* ae = rec_expert(const_cast<StepRecord*>(r));
     const int* as = rec_slot(const_cast<StepRecord*>(r), g.E);
-    if (U < 0 || U > g.E || n_hit < 0 || n_hit > U)
+    if (U < 0 || U > g.E || n_hit < 0 || n_hit > U || U - g.S > g.X)
       return fail(L, MOE_ERR_STATE, "step record is inconsistent (U=%d, hits=%d)", U, n_hit);
     for (int i = 0; i < U; ++i)
       if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S)
         return fail(L, MOE_ERR_STATE, "step record entry %d is out of range", i);
-    for (int w = 0; w < waves; ++w) {
-      const int b = std::max(n_hit, w * g.S), e = std::min((w + 1) * g.S, U);
-      if (b >= e) continue;
-      // wave 0 fills only free or stale slots: it waits for the routing alone;
-      // a later wave overwrites slots the previous wave computed from
-      cudaEvent_t trigger = L->ev_route;
-      if (w > 0) {
-        MOE_CUDA(L, cudaEventRecord(L->ev_comp, st));
-        trigger = L->ev_comp;
-      }
-      const int nfs = std::min(kFillStreams, e - b);
-      for (int j = 0; j < nfs; ++j) MOE_CUDA(L, cudaStreamWaitEvent(L->fill[j], trigger, 0));
+    any_miss = n_hit < U;
+    any_staged = U > g.S;
+    if (any_miss) {
+      const int nfs = std::min(kFillStreams, U - n_hit);
+      for (int j = 0; j < nfs; ++j) MOE_CUDA(L, cudaStreamWaitEvent(L->fill[j], L->ev_route, 0));
       cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, L->fill[0]);
-      for (int i = b; i < e; ++i) {
-        cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)as[i] * g.ebytes,
+      for (int i = n_hit; i < U; ++i) {
+        cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)access_slot(as, g.S, i) * g.ebytes,
                                          L->host_pool + (size_t)ae[i] * g.ebytes, g.ebytes,
-                                         cudaMemcpyHostToDevice, L->fill[(i - b) % kFillStreams]);
+                                         cudaMemcpyHostToDevice, L->fill[(i - n_hit) % kFillStreams]);
         if (ce != cudaSuccess) return fail(L, MOE_ERR_FILL, "fill of expert %d: %s", ae[i], cudaGetErrorString(ce));
         fill_bytes += g.ebytes;
       }
-      // the timing bracket on stream 0 covers the wave: stream 0 waits for the others
+      // the timing bracket on stream 0 covers every fill: stream 0 waits for the others
       for (int j = 1; j < nfs; ++j) {
         MOE_CUDA(L, cudaEventRecord(L->ev_fills[j], L->fill[j]));
         MOE_CUDA(L, cudaStreamWaitEvent(L->fill[0], L->ev_fills[j], 0));
@@ -765,13 +753,20 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       prof_end(pf, L->fill[0]);
       MOE_CUDA(L, cudaEventRecord(L->ev_fill, L->fill[0]));
       MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
-      a.mode = kRangeWaveMisses;
-      a.wave = w;
-      a.with_shared = 0;
-      grc = gemv(std::min(cap, g.S));
-      if (grc) return grc;
     }
     mirror_apply(L, r);
+  }
+  if (!resident && any_miss) {
+    a.mode = kRangeMisses;
+    a.with_shared = 0;
+    grc = gemv(max_miss);
+    if (grc) return grc;
+    if (any_staged) {
+      pe = prof_begin(L, MOE_PROF_COMMIT, st);
+      MOE_CUDA(L, launch_stage_commit(g, L->rec, max_staged, L->slots, st));
+      prof_end(pe, st);
+      L->launches += 1;
+    }
   }
   pe = prof_begin(L, MOE_PROF_COMBINE, st);
   MOE_CUDA(L, launch_combine(g, L->O, L->gates, L->row_of, N, yd, st));

@@ -57,14 +57,25 @@ inline size_t rec_bytes(int E) { return sizeof(StepRecord) + 3 * sizeof(int) * (
 // ---------------------------------------------------------------- layer geometry
 struct Geo {
   int E, k, d, f, S, fmt, has_shared, norm_topk, has_bias;
+  int X;                       // staging slots after the shared expert's (S + 1 ...)
   int blk;                     // 32 (MXFP4) or 16 (NVFP4)
   size_t ebytes;               // padded bytes of one expert
   size_t off_codes[3], off_scales[3], off_tscale;
 };
 
-// Work-range selectors of the expert GEMV launches (resolved on the device
-// from the StepRecord so a launch needs no host round trip).
-enum RangeMode : int { kRangeHits = 0, kRangeWaveMisses = 1, kRangeAll = 2 };
+// Work-range selectors of the expert FFN launches (resolved on the device
+// from the StepRecord so a launch needs no host round trip): the step's
+// hits, or all of its misses.
+enum RangeMode : int { kRangeHits = 0, kRangeMisses = 1 };
+
+// Slot whose bytes an access computes from.  Misses of the first wave
+// (access index < S) are filled straight into their LRU slot (a free or
+// stale one); later misses would evict a slot the same step still reads, so
+// they are filled into staging slot S + 1 + (i - S) at once and committed to
+// their LRU slot after the step's expert FFN (launch_stage_commit).
+__host__ __device__ inline int access_slot(const int* acc_slot, int S, int i) {
+  return i < S ? acc_slot[i] : S + 1 + (i - S);
+}
 
 // ---------------------------------------------------------------- launchers
 // router.cu
@@ -99,7 +110,7 @@ struct GemvArgs {
   const int* offsets;          // [E+1]
   const int* tok_of;           // [N*k]
   int N;
-  int mode, wave;              // RangeMode + wave index
+  int mode;                    // RangeMode
   int with_shared;             // also run the shared expert (rows N*k .. N*k+N)
   int* err;                    // set to 1 when a bounded wait gives up
   float* hmax;                 // [rows][2][d_ff / 64]: max |W_g x|, |W_u x| per 64 columns
@@ -127,14 +138,19 @@ cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int*
                                 float gx, uint8_t* codes, uint8_t* scales, cudaStream_t st);
 // ev (may be null): 4 events around phase 1 and phase 2
 cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const StepRecord* rec,
-                                 const int* offsets, int N, int mode, int wave, int with_shared,
+                                 const int* offsets, int N, int mode, int with_shared,
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales,
                                  float* O, float gx, float gh, int* err, cudaStream_t st,
                                  const cudaEvent_t* ev);
-// fill.cu: copy the misses of one wave from the (device-addressable) host pool
-cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int wave, int max_misses,
+// fill.cu: copy every miss of the step from the (device-addressable) host pool
+// into the slot access_slot() names
+cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses,
                              const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
+// copy each staged miss that still owns its LRU slot at the end of the step
+// (access i >= S with i + S >= U) from its staging slot into that slot
+cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int max_staged, uint8_t* slots,
+                                cudaStream_t st);
 // combine.cu
 cudaError_t launch_combine(const Geo& g, const float* O, const float* gates, const int* row_of,
                            int N, __nv_bfloat16* y, cudaStream_t st);

@@ -1,8 +1,9 @@
 // Device-driven miss fill: a copy kernel reads the step record on the GPU and
-// pulls each missed expert of one wave from the pinned host pool (reached over
-// NVLink-C2C through unified addressing) into its slot.  The host never waits
-// for the routing, so a decode step runs without a host round trip.  This is
-// the variant of the default fill (cudaMemcpyAsync from pinned host memory on
+// pulls every missed expert of the step from the pinned host pool (reached
+// over NVLink-C2C through unified addressing) into its slot or staging slot;
+// a second kernel commits staged experts to their LRU slots after the step's
+// expert FFN.  The host never waits for the routing, so a decode step runs
+// without a host round trip.  This is the variant of the default fill (cudaMemcpyAsync from pinned host memory on
 // side streams), which follows the pages' decode path: misses are loaded into
 // the GPU's expert cache from host memory ("FreeToken：把 284B MoE 塞进游戏 PC",
 // zhichai.net, §二 "Decode" paragraph).
@@ -15,43 +16,70 @@ namespace {
 constexpr int kFillThreads = 256;
 constexpr size_t kFillChunk = 64 * 1024;
 
-__global__ void __launch_bounds__(kFillThreads)
-fill_copy_kernel(const StepRecord* __restrict__ rec, int E, int S, int wave,
-                 const uint8_t* __restrict__ pool, uint8_t* __restrict__ slots, size_t ebytes,
-                 int chunks) {
-  const int U = rec->U, nh = rec->n_hit;
-  const int b = max(nh, wave * S), e = min((wave + 1) * S, U);
-  const int m = blockIdx.x / chunks, ch = blockIdx.x % chunks;
-  if (b + m >= e) return;
-  const int i = b + m;
-  const int ex = rec_expert(const_cast<StepRecord*>(rec))[i];
-  const int sl = rec_slot(const_cast<StepRecord*>(rec), E)[i];
-  if (ex < 0 || ex >= E || sl < 0 || sl >= S) return;
+// Copy chunk `ch` of one expert, 4 x 16 bytes in flight per thread.
+__device__ __forceinline__ void copy_chunk(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                           size_t ebytes, int ch) {
   const size_t off = (size_t)ch * kFillChunk;
   if (off >= ebytes) return;
   const size_t n16 = (min(kFillChunk, ebytes - off)) / 16;
-  const uint4* src = reinterpret_cast<const uint4*>(pool + (size_t)ex * ebytes + off);
-  uint4* dst = reinterpret_cast<uint4*>(slots + (size_t)sl * ebytes + off);
+  const uint4* s = reinterpret_cast<const uint4*>(src + off);
+  uint4* d = reinterpret_cast<uint4*>(dst + off);
   for (size_t v = threadIdx.x; v < n16; v += 4 * kFillThreads) {
     uint4 r[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (v + u * kFillThreads < n16) r[u] = src[v + u * kFillThreads];
+      if (v + u * kFillThreads < n16) r[u] = s[v + u * kFillThreads];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (v + u * kFillThreads < n16) dst[v + u * kFillThreads] = r[u];
+      if (v + u * kFillThreads < n16) d[v + u * kFillThreads] = r[u];
   }
+}
+
+// CTA (miss m, chunk ch): access n_hit + m, from the pool to access_slot().
+__global__ void __launch_bounds__(kFillThreads)
+fill_copy_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, const uint8_t* __restrict__ pool,
+                 uint8_t* __restrict__ slots, size_t ebytes, int chunks) {
+  const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
+  const int i = nh + blockIdx.x / chunks, ch = blockIdx.x % chunks;
+  if (i >= U || i - S >= X) return;
+  const int* as = rec_slot(const_cast<StepRecord*>(rec), E);
+  const int ex = rec_expert(const_cast<StepRecord*>(rec))[i];
+  if (ex < 0 || ex >= E || as[i] < 0 || as[i] >= S) return;
+  copy_chunk(pool + (size_t)ex * ebytes, slots + (size_t)access_slot(as, S, i) * ebytes, ebytes, ch);
+}
+
+// CTA (staged miss m, chunk ch): access S + m still owns its LRU slot at the
+// end of the step (no later access of the step maps to that slot) -> copy its
+// staging slot into it.
+__global__ void __launch_bounds__(kFillThreads)
+stage_commit_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, uint8_t* __restrict__ slots,
+                    size_t ebytes, int chunks) {
+  const int U = min(max(rec->U, 0), E);
+  const int i = S + blockIdx.x / chunks, ch = blockIdx.x % chunks;
+  if (i >= U || i - S >= X || i + S < U) return;
+  const int sl = rec_slot(const_cast<StepRecord*>(rec), E)[i];
+  if (sl < 0 || sl >= S) return;
+  copy_chunk(slots + (size_t)(S + 1 + (i - S)) * ebytes, slots + (size_t)sl * ebytes, ebytes, ch);
 }
 
 }  // namespace
 
-cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int wave, int max_misses,
+cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses,
                              const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st) {
   const int chunks = (int)((g.ebytes + kFillChunk - 1) / kFillChunk);
   const long long grid = (long long)chunks * max_misses;
   if (grid <= 0) return cudaSuccess;
-  fill_copy_kernel<<<(unsigned)grid, kFillThreads, 0, st>>>(rec, g.E, g.S, wave, pool_dev, slots,
-                                                            g.ebytes, chunks);
+  fill_copy_kernel<<<(unsigned)grid, kFillThreads, 0, st>>>(rec, g.E, g.S, g.X, pool_dev, slots, g.ebytes,
+                                                            chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int max_staged, uint8_t* slots,
+                                cudaStream_t st) {
+  const int chunks = (int)((g.ebytes + kFillChunk - 1) / kFillChunk);
+  const long long grid = (long long)chunks * max_staged;
+  if (grid <= 0) return cudaSuccess;
+  stage_commit_kernel<<<(unsigned)grid, kFillThreads, 0, st>>>(rec, g.E, g.S, g.X, slots, g.ebytes, chunks);
   return cudaGetLastError();
 }
 

@@ -137,10 +137,8 @@ struct Entry {
 MOE_DEV int count_entries(const Geo& g, const GemvArgs& a, int* base, int* nr) {
   const StepRecord* rec = a.rec;
   const int U = min(max(rec->U, 0), g.E), nh = min(max(rec->n_hit, 0), U), S = g.S;
-  int b = 0, e = 0;
-  if (a.mode == kRangeHits) { b = 0; e = nh; }
-  else if (a.mode == kRangeWaveMisses) { b = max(nh, a.wave * S); e = min((a.wave + 1) * S, U); }
-  else { b = a.wave * S; e = min((a.wave + 1) * S, U); }
+  (void)S;
+  const int b = a.mode == kRangeHits ? 0 : nh, e = a.mode == kRangeHits ? nh : U;
   *base = b;
   *nr = max(0, e - b);
   return *nr + (a.with_shared ? 1 : 0);
@@ -151,8 +149,9 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int en
     StepRecord* rec = const_cast<StepRecord*>(a.rec);
     const int acc = base + ent;
     const int ex = rec_expert(rec)[acc];
-    const int sl = rec_slot(rec, g.E)[acc];
-    if (ex < 0 || ex >= g.E || sl < 0 || sl >= g.S) return false;
+    const int ls = rec_slot(rec, g.E)[acc];
+    if (ex < 0 || ex >= g.E || ls < 0 || ls >= g.S || acc - g.S >= g.X) return false;
+    const int sl = access_slot(rec_slot(rec, g.E), g.S, acc);
     out.slot = sl;
     out.row0 = a.offsets[ex];
     out.nrows = a.offsets[ex + 1] - out.row0;
@@ -734,17 +733,18 @@ bool gemv_shape_ok(const Geo& g) {
 
 GemvPlan* gemv_plan_create(const Geo& g, const uint8_t* slots) {
   GemvPlan* pl = new GemvPlan();
-  pl->ready = make_box_map(&pl->w[0], slots + g.off_codes[0], g.d / 2, g.f, g.S + 1, g.ebytes) &&
-              make_box_map(&pl->w[1], slots + g.off_codes[1], g.d / 2, g.f, g.S + 1, g.ebytes) &&
-              make_box_map(&pl->w[2], slots + g.off_codes[2], g.f / 2, g.d, g.S + 1, g.ebytes);
+  const int ns = g.S + 1 + g.X;   // LRU slots, the shared expert, staging slots
+  pl->ready = make_box_map(&pl->w[0], slots + g.off_codes[0], g.d / 2, g.f, ns, g.ebytes) &&
+              make_box_map(&pl->w[1], slots + g.off_codes[1], g.d / 2, g.f, ns, g.ebytes) &&
+              make_box_map(&pl->w[2], slots + g.off_codes[2], g.f / 2, g.d, ns, g.ebytes);
   // scale maps only where a scale row is a 16-byte multiple (the phase uses them then)
   const SG p1 = make_sg(g, 1), p2 = make_sg(g, 2);
   const uint32_t sb = kBoxes * (g.fmt == MOE_MXFP4 ? 8 : 16);
   if (pl->ready && p1.smode)
-    pl->ready = make_scale_map(&pl->s[0], slots + g.off_scales[0], p1.scale_row, g.f, g.S + 1, g.ebytes, sb) &&
-                make_scale_map(&pl->s[1], slots + g.off_scales[1], p1.scale_row, g.f, g.S + 1, g.ebytes, sb);
+    pl->ready = make_scale_map(&pl->s[0], slots + g.off_scales[0], p1.scale_row, g.f, ns, g.ebytes, sb) &&
+                make_scale_map(&pl->s[1], slots + g.off_scales[1], p1.scale_row, g.f, ns, g.ebytes, sb);
   if (pl->ready && p2.smode)
-    pl->ready = make_scale_map(&pl->s[2], slots + g.off_scales[2], p2.scale_row, g.d, g.S + 1, g.ebytes, sb);
+    pl->ready = make_scale_map(&pl->s[2], slots + g.off_scales[2], p2.scale_row, g.d, ns, g.ebytes, sb);
   return pl;
 }
 

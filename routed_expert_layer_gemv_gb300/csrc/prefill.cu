@@ -8,7 +8,7 @@
 // (actquant.cuh).  Steps:
 //  1. gather_quant: row r of the permuted activations = quant(x[tok_of[r]]);
 //     rows N*k .. N*k+N-1 hold every token for the shared expert.
-//  2. build_tiles: the launch's experts (hits, a wave of misses, + shared) cut
+//  2. build_tiles: the launch's experts (hits, or all misses, + shared) cut
 //     into M tiles of 128 rows; the last tile of an expert is ragged (its extra
 //     rows are computed and dropped).
 //  3. gemm_gateup: CTA = (M tile, 128 rows of d_ff); per K tile of 256 codes
@@ -81,15 +81,12 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
 // ---------------------------------------------------------------- step 2
 __global__ void __launch_bounds__(1024)
 build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ offsets, int E, int S,
-                   int N, int k, int mode, int wave, int with_shared, Tile* __restrict__ tiles,
+                   int X, int N, int k, int mode, int with_shared, Tile* __restrict__ tiles,
                    int* __restrict__ n_tiles) {
   __shared__ int sh[33];
   __shared__ int carry;
-  const int U = rec->U, nh = rec->n_hit;
-  int b = 0, e = 0;
-  if (mode == kRangeHits) { b = 0; e = nh; }
-  else if (mode == kRangeWaveMisses) { b = max(nh, wave * S); e = min((wave + 1) * S, U); }
-  else { b = wave * S; e = min((wave + 1) * S, U); }
+  const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
+  const int b = mode == kRangeHits ? 0 : nh, e = mode == kRangeHits ? nh : U;
   const int nr = max(0, e - b);
   const int n_ent = nr + (with_shared ? 1 : 0);
   if (threadIdx.x == 0) carry = 0;
@@ -100,9 +97,9 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
     const int i = e0 + threadIdx.x;
     int slot = -1, r0 = 0, nrows = 0;
     if (i < nr) {
-      const int ex = ae[b + i], sl = as[b + i];
-      if (ex >= 0 && ex < E && sl >= 0 && sl < S) {
-        slot = sl;
+      const int ex = ae[b + i], ls = as[b + i];
+      if (ex >= 0 && ex < E && ls >= 0 && ls < S && b + i - S < X) {
+        slot = access_slot(as, S, b + i);
         r0 = offsets[ex];
         nrows = offsets[ex + 1] - r0;
       }
@@ -517,9 +514,9 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
   PrefillPlan* pl = new PrefillPlan();
   pl->ready = make_map_2d(&pl->xq, xq_codes, g.d / 2, xq_rows) &&
               make_map_2d(&pl->hq, hq_codes, g.f / 2, xq_rows) &&
-              make_map_3d(&pl->wg, slots + g.off_codes[0], g.d / 2, g.f, g.S + 1, g.ebytes) &&
-              make_map_3d(&pl->wu, slots + g.off_codes[1], g.d / 2, g.f, g.S + 1, g.ebytes) &&
-              make_map_3d(&pl->wd, slots + g.off_codes[2], g.f / 2, g.d, g.S + 1, g.ebytes);
+              make_map_3d(&pl->wg, slots + g.off_codes[0], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes) &&
+              make_map_3d(&pl->wu, slots + g.off_codes[1], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes) &&
+              make_map_3d(&pl->wd, slots + g.off_codes[2], g.f / 2, g.d, g.S + 1 + g.X, g.ebytes);
   return pl;
 }
 
@@ -542,13 +539,13 @@ int prefill_max_tiles(const Geo& g, int N) {
 }
 
 cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const StepRecord* rec,
-                                 const int* offsets, int N, int mode, int wave, int with_shared,
+                                 const int* offsets, int N, int mode, int with_shared,
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales,
                                  float* O, float gx, float gh, int* err, cudaStream_t st,
                                  const cudaEvent_t* ev) {
   Tile* tl = static_cast<Tile*>(tiles);
-  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, g.E, g.S, N, g.k, mode, wave, with_shared, tl,
+  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, g.E, g.S, g.X, N, g.k, mode, with_shared, tl,
                                          n_tiles);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -8,6 +8,7 @@ import torch
 
 from helpers import (CachedExperts, assert_close_layer, bf16_tensor, need_gpu, oracle_layer,
                      reject_near_ties, small_spec)
+from oracle import formats
 from oracle.lru import SlotTable
 from routed_expert_layer_gemv_gb300 import capi
 from routed_expert_layer_gemv_gb300 import workloads as wl
@@ -113,6 +114,43 @@ def test_decode_device_fill(batch, steps):
     spec = wl.DECODE_35B.layer
     miss, u, waves = _decode_run(spec, 7, batch, steps, fill=capi.MOE_FILL_DEVICE)
     assert miss > 0
+
+
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_MEMCPY, capi.MOE_FILL_DEVICE])
+def test_staged_misses_land_in_their_lru_slots(fill):
+    # more distinct experts per step than slots: misses past the first wave are
+    # filled into staging slots and committed afterwards; every LRU slot must
+    # then hold exactly the expert the slot table names
+    spec = small_spec(E=32, k=4, d_model=256, d_ff=256, n_slots=6, has_shared=True)
+    seed, batch = 13, 8
+    experts = CachedExperts(spec, seed)
+    L = build_layer(spec, seed, batch, experts_fn=experts)
+    capi.moe_set_fill_mode(L.h, fill)
+    O = oracle_layer(spec, seed, experts)
+    T = SlotTable(spec.E, spec.n_slots)
+    xs, _ = wl.ar1_tokens(seed, batch, 3, spec.d_model, 0.9, reject_near_ties(spec, seed))
+    overflow = 0
+    for t in range(3):
+        y, info = L.forward(bf16_tensor(xs[t]), regime=DEC)
+        ref, idx, _ = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
+        acc = T.step(idx.reshape(-1))
+        overflow += len(acc) > spec.n_slots
+        assert_close_layer(y, ref, "step %d" % t)
+        eo, _, _ = capi.moe_lru_get_state(L.h, spec.n_slots)
+        assert eo == T.expert_of
+        torch.cuda.synchronize()
+        for slot, e in enumerate(eo):
+            if e < 0:
+                continue
+            w = experts(e)
+            for m, name in enumerate(("gate", "up", "down")):
+                mat = w[name]
+                out = torch.empty(mat.rows, mat.K, dtype=torch.float32, device="cuda")
+                capi.moe_debug_dequant(L.h, slot, m, out)
+                want = formats.dequant(mat.codes, mat.scales, mat.tscale, spec.fmt)
+                assert np.array_equal(out.cpu().numpy().astype(np.float64), want), (t, slot, e, name)
+    assert overflow > 0
+    L.close()
 
 
 def test_prefill_device_fill_waves():
