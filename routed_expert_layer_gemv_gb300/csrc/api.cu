@@ -686,7 +686,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     if (prefill) {
       ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, N, a.mode, a.with_shared,
                                 L->tiles, L->n_tiles, L->slots, L->xq_scales, L->hq_codes,
-                                L->hq_scales, L->O, gx, gh, L->err_dev, st, evp);
+                                L->hq_scales, L->O, gx, gh, L->err_dev, L->num_sms, st, evp);
       L->launches += 3;
     } else {
       ce = launch_gemv_decode(g, L->gplan, a, xd, L->xexp, L->h, L->O, n_ent, L->num_sms, st, evp);

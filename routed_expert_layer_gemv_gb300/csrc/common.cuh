@@ -141,7 +141,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  const int* offsets, int N, int mode, int with_shared,
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales,
-                                 float* O, float gx, float gh, int* err, cudaStream_t st,
+                                 float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
                                  const cudaEvent_t* ev);
 // fill.cu: copy every miss of the step from the (device-addressable) host pool
 // into the slot access_slot() names

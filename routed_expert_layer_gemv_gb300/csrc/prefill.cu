@@ -11,14 +11,16 @@
 //  2. build_tiles: the launch's experts (hits, or all misses, + shared) cut
 //     into M tiles of 128 rows; the last tile of an expert is ragged (its extra
 //     rows are computed and dropped).
-//  3. gemm_gateup: CTA = (M tile, 128 rows of d_ff); per K tile of 256 codes
-//     TMA brings A (128 x 128 B), B_gate and B_up (128 x 128 B each) into
-//     shared memory (128B swizzle), cp.async brings the block scales; four
-//     warps write the scales to TMEM; one thread issues the MMAs into two TMEM
-//     accumulators (gate, up).  Epilogue: h = SiLU(a) * u, re-quantised to FP4.
-//  4. gemm_down: CTA = (M tile, 128 rows of d_model), O = h W_d^T in fp32.
-// Every wait is bounded (~2 s); on a timeout the CTA records an error, waits
-// for its own copies and MMAs (bounded again), frees its TMEM and returns.
+//  3. phase 1 (gemm_ws_kernel<fmt, 1>): tiles of 128 rows x 64 d_ff columns;
+//     B stacks the 64 gate rows over the same 64 up rows, so one N = 128 MMA
+//     yields both halves of SwiGLU; epilogue h = SiLU(a) * u, re-quantised.
+//  4. phase 2 (gemm_ws_kernel<fmt, 2>): tiles of 128 rows x 128 d_model
+//     columns, O = h W_d^T in fp32.
+// Both phases run the persistent warp-specialised kernel below (TMA warp, MMA
+// warp, block-scale warps, epilogue warps).  Every wait is bounded (~2 s); on
+// a timeout the CTA records an error, skips its remaining waits, waits for its
+// own copies and MMAs (bounded again), frees its TMEM and returns.
+#include <algorithm>
 #include <cstdio>
 
 #include "actquant.cuh"
@@ -29,7 +31,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kStages = 3;
 constexpr int kTileRows = 128;          // M and N of one MMA tile
 constexpr int kKTileBytes = 128;        // 256 FP4 codes per K tile
 constexpr int kOpBytes = kTileRows * kKTileBytes;   // 16 KB per operand tile
@@ -169,283 +170,306 @@ struct GemmArgs {
   int O_ld;
 };
 
-// bytes of one row's block scales in a K tile of 256 codes
-__device__ __forceinline__ int scale_bytes(int fmt) { return fmt == MOE_MXFP4 ? 8 : 16; }
+// ---------------------------------------------------------------- persistent warp-specialised GEMM
+// One CTA per SM walks the launch's (M tile, N tile) pairs.  Ten warps, each
+// with one job, meeting only at mbarriers:
+//   warp 0     TMA: A (128 token rows x 256 K) and B (128 weight rows x 256 K,
+//              phase 1: 64 gate rows over the same 64 up rows) per stage;
+//   warp 1     one thread issues the block-scaled MMAs (M = 128, N = 128,
+//              K = 64 each) into one of two TMEM accumulators;
+//   warps 2-5  block scales: each loads the stage's A and B scale bytes from
+//              global memory (each 32-byte sector covers several stages, so
+//              most loads hit L1; the next sectors are prefetched) and writes
+//              them into a TMEM ring slot in the layout the MMA reads (every
+//              lane quarter holds all 128 rows), one warp per lane quarter;
+//   warps 6-9  epilogue, one per lane quarter (32 rows): drain an accumulator
+//              into registers, release it, then SiLU * mul + FP4 quantisation
+//              of h (phase 1) or the fp32 O rows (phase 2), while the MMAs of
+//              the next tile run into the other accumulator.
+constexpr int kWsThreads = 320;
+constexpr int kSfBase = 256;            // TMEM columns 0..255: two 128-column accumulators
 
-// Copy `bytes` (8 or 16) from global to shared asynchronously.
-__device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes) {
-  if (bytes == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(tc::su32(dst)), "l"(src) : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(tc::su32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// Ring stages: phase 1 takes 6; phase 2 takes 5 and keeps room to stage O
+// for its epilogue: per epilogue warp 32 rows x 64 fp32 (half a tile at a
+// time), rows padded by 4 floats so the row writes and reads spread over the
+// banks.
+template <int PH> constexpr int ws_stages() { return PH == 1 ? 6 : 5; }
+constexpr int kOStride = 68;
+constexpr size_t kOStage = 4 * 32 * kOStride * 4;
 
-// Write the scale groups of one operand tile (128 rows, staged in shared
-// memory as [row][sb bytes]) into TMEM at column `col0`: group g goes to
-// columns col0 + 4g .. + 3, lane 32w + i, column 4g + j = row 32j + i.
-__device__ __forceinline__ void scales_to_tmem(const uint8_t* st, int sb, uint32_t tmem_lane_base,
-                                               uint32_t col0) {
-  const int i = threadIdx.x & 31;
-  const int groups = sb / 4;
-  for (int g = 0; g < groups; ++g) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint32_t*>(st + (32 * j + i) * sb + 4 * g);
-    tc::tmem_st4(tmem_lane_base + col0 + 4 * g, w[0], w[1], w[2], w[3]);
-  }
-}
+template <int PH>
+size_t ws_smem() { return 1024 + (size_t)ws_stages<PH>() * 2 * kOpBytes + (PH == 2 ? kOStage : 0); }
 
-// Issue the MMAs of one K tile: nb B operands (1 or 2) into accumulators at
-// columns 0, 128 (each N = 128).
-__device__ __forceinline__ void issue_mmas(int fmt, uint32_t tb, uint32_t a_smem, const uint32_t* b_smem,
-                                           int nb, uint32_t sfa_col, const uint32_t* sfb_col,
-                                           bool acc_first) {
-  for (int kk = 0; kk < 4; ++kk) {
-    const uint64_t ad = tc::sdesc_sw128(a_smem + 32 * kk);
-    for (int bi = 0; bi < nb; ++bi) {
-      const uint64_t bd = tc::sdesc_sw128(b_smem[bi] + 32 * kk);
-      const bool acc = acc_first || kk > 0;
-      if (fmt == MOE_MXFP4) {
-        const uint32_t sf = 2 * (kk & 1), g = kk >> 1;
-        tc::mma_mxf4(tb + 128 * bi, ad, bd, tc::idesc_fp4(128, true, sf, sf), tb + sfa_col + 4 * g,
-                     tb + sfb_col[bi] + 4 * g, acc);
-      } else {
-        tc::mma_nvf4(tb + 128 * bi, ad, bd, tc::idesc_fp4(128, false, 0, 0), tb + sfa_col + 4 * kk,
-                     tb + sfb_col[bi] + 4 * kk, acc);
-      }
-    }
-  }
+__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (*abort_flag) return false;
+  if (tc::mbar_wait(bar, parity)) return true;
+  *abort_flag = 1;
+  atomicExch(err, 1);
+  return false;
 }
 
-// The shared mainloop of both phases: A = activations (tensor map ta, rows
-// row_start..), nb weight operands (tensor maps tw[bi], rows n0.., slot z).
-// On return the accumulators hold the full-K products (or *bad is set).
-template <int NB>
-__device__ bool gemm_mainloop(const GemmArgs& p, const CUtensorMap* ta, const CUtensorMap* const* tw,
-                              const Tile& tile, int n0, uint8_t* smem, uint64_t* full, uint64_t* done,
-                              uint32_t tb, uint32_t scol0, int* n_committed) {
-  const int nkt = p.K / 256;
-  const int sb = scale_bytes(p.fmt);
-  const int stage_bytes = (1 + NB) * kOpBytes;
-  uint8_t* sc_base = smem + kStages * stage_bytes;           // [stage][1+NB][128][sb]
-  const int sc_stage = (1 + NB) * kTileRows * 16;
-  const uint32_t lane_base = (uint32_t)(32 * (threadIdx.x >> 5)) << 16;
-  const uint32_t scols = (uint32_t)(1 + NB) * (uint32_t)(sb);  // TMEM columns per stage (4 per group)
-  const int row = threadIdx.x;                                // one scale row per thread
-  const uint8_t* wbase = p.slots + (size_t)tile.slot * p.ebytes;
-  bool ok = true;
-
-  auto issue_loads = [&](int kt) {
-    const int s = kt % kStages;
-    uint8_t* st = smem + s * stage_bytes;
-    if (threadIdx.x == 0) {
-      tc::mbar_expect_tx(&full[s], (uint32_t)stage_bytes);
-      tc::tma_load_2d(st, ta, &full[s], kt * kKTileBytes, tile.row_start);
-      for (int bi = 0; bi < NB; ++bi)
-        tc::tma_load_3d(st + (1 + bi) * kOpBytes, tw[bi], &full[s], kt * kKTileBytes, n0, tile.slot);
-    }
-    // block scales of this K tile: A rows, then each weight operand's rows
-    uint8_t* sst = sc_base + s * sc_stage;
-    cp_async(sst + row * sb, p.a_scales + (size_t)(tile.row_start + row) * (p.K / (p.fmt == MOE_MXFP4 ? 32 : 16)) +
-                                 (size_t)kt * sb, sb);
-    for (int bi = 0; bi < NB; ++bi) {
-      const uint8_t* ws = wbase + p.w_scales_off[bi] + (size_t)(n0 + row) * (p.K / (p.fmt == MOE_MXFP4 ? 32 : 16)) +
-                          (size_t)kt * sb;
-      cp_async(sst + (1 + bi) * kTileRows * sb + row * sb, ws, sb);
-    }
-    cp_async_commit();
-  };
-
-  for (int kt = 0; kt < kStages - 1 && kt < nkt; ++kt) issue_loads(kt);
-  for (int kt = 0; kt < nkt; ++kt) {
-    const int s = kt % kStages;
-    // keep the pipeline kStages - 1 tiles ahead: refill the stage of tile kt-1
-    if (kt + kStages - 1 < nkt) {
-      if (kt >= 1) {
-        const int ps = (kt - 1) % kStages;
-        bool w = true;
-        if (threadIdx.x == 0) w = tc::mbar_wait(&done[ps], (uint32_t)(((kt - 1) / kStages) & 1));
-        if (!__syncthreads_and(w)) { ok = false; break; }
-      }
-      issue_loads(kt + kStages - 1);
-      cp_async_wait<kStages - 1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    // scales of tile kt -> TMEM (its stage's previous MMAs finished: waited above)
-    const uint8_t* sst = sc_base + s * sc_stage;
-    const uint32_t c0 = scol0 + (uint32_t)s * scols;
-    scales_to_tmem(sst, sb, tb + lane_base, c0);
-    for (int bi = 0; bi < NB; ++bi)
-      scales_to_tmem(sst + (1 + bi) * kTileRows * sb, sb, tb + lane_base, c0 + (uint32_t)(1 + bi) * (uint32_t)(sb));
-    tc::tmem_st_wait();
-    tc::fence_before();
-    __syncthreads();
-    bool w = true;
-    if (threadIdx.x == 0) {
-      tc::fence_after();
-      w = tc::mbar_wait(&full[s], (uint32_t)((kt / kStages) & 1));
-      if (w) {
-        uint8_t* st = smem + s * stage_bytes;
-        uint32_t bs[2], sfb[2];
-        for (int bi = 0; bi < NB; ++bi) {
-          bs[bi] = tc::su32(st + (1 + bi) * kOpBytes);
-          sfb[bi] = c0 + (uint32_t)(1 + bi) * (uint32_t)(sb);
-        }
-        issue_mmas(p.fmt, tb, tc::su32(st), bs, NB, c0, sfb, kt > 0);
-        tc::mma_commit(&done[s]);
-        ++*n_committed;
-      }
-    }
-    if (!__syncthreads_and(w)) { ok = false; break; }
-  }
-  // all MMAs: wait for the last commit (they complete in order)
-  if (ok && nkt > 0) {
-    const int last = nkt - 1;
-    const bool w = tc::mbar_wait(&done[last % kStages], (uint32_t)((last / kStages) & 1));
-    ok = __syncthreads_and(w);
-  }
-  tc::fence_after();
-  return ok;
+__device__ __forceinline__ void ws_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::su32(bar)) : "memory");
 }
 
-// Bounded clean-up after an error: let copies and MMAs in flight finish.
-__device__ void drain(uint64_t* full, uint64_t* done) {
-  cp_async_wait<0>();
-  if (threadIdx.x == 0) {
-    const long long t0 = clock64();
-    while (clock64() - t0 < 200000000LL) {
-    }
-  }
-  __syncthreads();
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" :: "l"(p));
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(128, 1)
-gemm_gateup_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tg,
-                   const __grid_constant__ CUtensorMap tu, GemmArgs p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+template <int FMT, int PH>
+__global__ void __launch_bounds__(kWsThreads, 1)
+gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
+               const __grid_constant__ CUtensorMap tb1, GemmArgs p) {
+  constexpr int G = FMT == MOE_MXFP4 ? 2 : 4;    // 4-byte scale groups per row per 256-K stage
+  constexpr int SB = 4 * G;                       // scale bytes per row per stage
+  constexpr int SFC = 2 * 4 * G;                  // TMEM columns of one scale slot (A, then B)
+  constexpr int NCOL = PH == 1 ? 64 : 128;        // output columns of one tile
+  constexpr int kWsStages = ws_stages<PH>();
+  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kStages], done[kStages];
+  __shared__ __align__(8) uint64_t full[kWsStages], empty[kWsStages], sfull[kWsStages], accf[2], acce[2], fin;
   __shared__ uint32_t tmem_base;
-  if ((int)blockIdx.x >= *p.n_tiles) return;
-  const Tile tile = p.tiles[blockIdx.x];
-  const int n0 = blockIdx.y * kTileRows;
-  const int warp = threadIdx.x >> 5;
+  __shared__ volatile int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&done[s], 1); }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < kWsStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&sfull[s], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 4);
+    }
+    tc::mbar_init(&fin, 1);
+    s_abort = 0;
     tc::mbar_init_fence();
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tb = tmem_base;
-  const CUtensorMap* tw[2] = {&tg, &tu};
-  int n_committed = 0;
-  const bool ok = gemm_mainloop<2>(p, &ta, tw, tile, n0, smem, full, done, tb, 256, &n_committed);
-  if (!ok) {
-    if (threadIdx.x == 0) atomicExch(p.err, 1);
-    drain(full, done);
-  } else {
-    // epilogue: row m of the tile, 128 gate and 128 up columns
-    const int m = threadIdx.x;
-    const int r = tile.row_start + m;
-    const bool live = r < tile.row_end;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    const float* ts = reinterpret_cast<const float*>(p.slots + (size_t)tile.slot * p.ebytes +
-                                                     p.w_scales_off[2]);  // tensor scales
-    const float sg = FMT == MOE_MXFP4 ? 1.0f : ts[0] * p.act_scale;
-    const float su = FMT == MOE_MXFP4 ? 1.0f : ts[1] * p.act_scale;
-    const int f = p.rows_out;
-    for (int c = 0; c < 4; ++c) {
-      uint32_t gv[32], uv[32];
-      tc::tmem_ld32(tb + lane_base + 32 * c, gv);
-      tc::tmem_ld32(tb + lane_base + 128 + 32 * c, uv);
-      tc::tmem_ld_wait();
-      float h[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = __uint_as_float(gv[i]) * sg, u = __uint_as_float(uv[i]) * su;
-        h[i] = a / (1.0f + expf(-a)) * u;
-      }
-      if (live) {
-        const int col = n0 + 32 * c;
-        uint32_t words[4];
-        if (FMT == MOE_MXFP4) {
-          p.h_scales[(size_t)r * (f / 32) + col / 32] = (uint8_t)quant_mx32(h, words);
-        } else {
-          uint32_t w2[2];
-          p.h_scales[(size_t)r * (f / 16) + col / 16] = (uint8_t)quant_nv16(h, p.act_scale_h, words);
-          p.h_scales[(size_t)r * (f / 16) + col / 16 + 1] = (uint8_t)quant_nv16(h + 16, p.act_scale_h, w2);
-          words[2] = w2[0];
-          words[3] = w2[1];
+  const int n_m = *p.n_tiles;
+  const int NT = p.rows_out / NCOL;
+  const long long T = (long long)n_m * NT;
+  const int nkt = p.K / 256;
+  const int srow = p.K / (FMT == MOE_MXFP4 ? 32 : 16);   // scale bytes per row
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool stop = false;
+      for (long long t = blockIdx.x; t < T && !stop; t += gridDim.x) {
+        const Tile tile = p.tiles[t / NT];
+        const int n0 = (int)(t % NT) * NCOL;
+        for (int kt = 0; kt < nkt; ++kt, ++it) {
+          const int s = it % kWsStages;
+          const uint32_t k = it / kWsStages;
+          if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) { stop = true; break; }
+          uint8_t* st = smem + (size_t)s * 2 * kOpBytes;
+          tc::mbar_expect_tx(&full[s], 2 * kOpBytes);
+          tc::tma_load_2d(st, &ta, &full[s], kt * kKTileBytes, tile.row_start);
+          if (PH == 1) {
+            tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
+            tc::tma_load_3d(st + kOpBytes + kOpBytes / 2, &tb1, &full[s], kt * kKTileBytes, n0, tile.slot);
+          } else {
+            tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
+          }
         }
-        *reinterpret_cast<uint4*>(p.h_codes + (size_t)r * (f / 2) + col / 2) =
-            make_uint4(words[0], words[1], words[2], words[3]);
+      }
+      // copies in flight land before the CTA exits (bounded)
+      const uint32_t first = it > (uint32_t)kWsStages ? it - kWsStages : 0;
+      for (uint32_t i = first; i < it; ++i)
+        if (!tc::mbar_wait(&full[i % kWsStages], (i / kWsStages) & 1)) { atomicExch(p.err, 1); break; }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, nt_done = 0;
+      bool stop = false;
+      for (long long t = blockIdx.x; t < T && !stop; t += gridDim.x, ++nt_done) {
+        const int b = nt_done & 1;
+        const uint32_t u = nt_done >> 1;
+        if (u > 0 && !ws_wait(&acce[b], (u - 1) & 1, &s_abort, p.err)) { stop = true; break; }
+        tc::fence_after();
+        for (int kt = 0; kt < nkt; ++kt, ++it) {
+          const int s = it % kWsStages;
+          const uint32_t ph = (it / kWsStages) & 1;
+          if (!ws_wait(&full[s], ph, &s_abort, p.err) || !ws_wait(&sfull[s], ph, &s_abort, p.err)) {
+            stop = true;
+            break;
+          }
+          tc::fence_after();
+          const uint32_t a_s = tc::su32(smem + (size_t)s * 2 * kOpBytes), b_s = a_s + kOpBytes;
+          const uint32_t sfa = tb + kSfBase + (uint32_t)(s * SFC), sfb = sfa + 4 * G;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = tc::sdesc_sw128(a_s + 32 * kk), bd = tc::sdesc_sw128(b_s + 32 * kk);
+            const bool acc = kt > 0 || kk > 0;
+            if (FMT == MOE_MXFP4) {
+              const uint32_t id = 2 * (kk & 1), g = kk >> 1;
+              tc::mma_mxf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, true, id, id), sfa + 4 * g, sfb + 4 * g, acc);
+            } else {
+              tc::mma_nvf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, false, 0, 0), sfa + 4 * kk, sfb + 4 * kk, acc);
+            }
+          }
+          tc::mma_commit(&empty[s]);   // the stage's smem and scale slot are free once these MMAs finish
+        }
+        if (stop) break;
+        tc::mma_commit(&accf[b]);
+      }
+      // every MMA issued (also of a tile cut short) has finished before the CTA
+      // frees TMEM (bounded)
+      tc::mma_commit(&fin);
+      if (!tc::mbar_wait(&fin, 0)) atomicExch(p.err, 1);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ block scales -> TMEM
+    const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's lane quarter
+    uint32_t it = 0;
+    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+      const Tile tile = p.tiles[t / NT];
+      const int n0 = (int)(t % NT) * NCOL;
+      const uint8_t* wb = p.slots + (size_t)tile.slot * p.ebytes;
+      const uint8_t* pa[4];
+      const uint8_t* pb[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pa[j] = p.a_scales + (size_t)(tile.row_start + 32 * j + lane) * srow;
+        if (PH == 1) pb[j] = wb + p.w_scales_off[j < 2 ? 0 : 1] + (size_t)(n0 + 32 * (j & 1) + lane) * srow;
+        else pb[j] = wb + p.w_scales_off[0] + (size_t)(n0 + 32 * j + lane) * srow;
+      }
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        const int s = it % kWsStages;
+        const uint32_t k = it / kWsStages;
+        if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) continue;
+        if (s_abort) continue;
+        if (kt + 4 < nkt) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            prefetch_l1(pa[j] + (kt + 4) * SB);
+            prefetch_l1(pb[j] + (kt + 4) * SB);
+          }
+        }
+        uint32_t wa[4][G], wv[4][G];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (FMT == MOE_MXFP4) {
+            const uint2 va = *reinterpret_cast<const uint2*>(pa[j] + kt * SB);
+            const uint2 vb = *reinterpret_cast<const uint2*>(pb[j] + kt * SB);
+            wa[j][0] = va.x; wa[j][G - 1] = va.y;
+            wv[j][0] = vb.x; wv[j][G - 1] = vb.y;
+          } else {
+            const uint4 va = *reinterpret_cast<const uint4*>(pa[j] + kt * SB);
+            const uint4 vb = *reinterpret_cast<const uint4*>(pb[j] + kt * SB);
+            const uint32_t ta4[4] = {va.x, va.y, va.z, va.w}, tb4[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+            for (int g = 0; g < G; ++g) { wa[j][g] = ta4[g & 3]; wv[j][g] = tb4[g & 3]; }
+          }
+        }
+        const uint32_t col = tb + lq + kSfBase + (uint32_t)(s * SFC);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          tc::tmem_st4(col + 4 * g, wa[0][g], wa[1][g], wa[2][g], wa[3][g]);
+          tc::tmem_st4(col + 4 * G + 4 * g, wv[0][g], wv[1][g], wv[2][g], wv[3][g]);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) ws_arrive(&sfull[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
+    const int rl = 32 * (warp & 3) + lane;   // tile row of this thread
+    uint32_t nt_done = 0;
+    for (long long t = blockIdx.x; t < T; t += gridDim.x, ++nt_done) {
+      const Tile tile = p.tiles[t / NT];
+      const int n0 = (int)(t % NT) * NCOL;
+      const int b = nt_done & 1;
+      if (!ws_wait(&accf[b], (nt_done >> 1) & 1, &s_abort, p.err)) continue;
+      tc::fence_after();
+      const int r = tile.row_start + rl;
+      const bool live = r < tile.row_end;
+      const float* ts = reinterpret_cast<const float*>(p.slots + (size_t)tile.slot * p.ebytes + p.w_scales_off[2]);
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      const uint32_t acc = tb + lq + 128 * b;
+      tc::tmem_ld32(acc, v0);
+      tc::tmem_ld32(acc + 32, v1);
+      tc::tmem_ld32(acc + 64, v2);
+      tc::tmem_ld32(acc + 96, v3);
+      tc::tmem_ld_wait();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) ws_arrive(&acce[b]);   // the accumulator is free for the tile after next
+      if (PH == 1) {
+        // columns 0..63: W_g rows n0.., 64..127: W_u rows n0..
+        const float sg = FMT == MOE_MXFP4 ? 1.0f : ts[0] * p.act_scale;
+        const float su = FMT == MOE_MXFP4 ? 1.0f : ts[1] * p.act_scale;
+        const int f = p.rows_out;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t* gv = c == 0 ? v0 : v1;
+          const uint32_t* uv = c == 0 ? v2 : v3;
+          float hv[32];
+#pragma unroll
+          for (int i2 = 0; i2 < 32; ++i2) {
+            const float a = __uint_as_float(gv[i2]) * sg, u = __uint_as_float(uv[i2]) * su;
+            hv[i2] = a / (1.0f + __expf(-a)) * u;
+          }
+          if (live) {
+            const int col = n0 + 32 * c;
+            uint32_t words[4];
+            if (FMT == MOE_MXFP4) {
+              p.h_scales[(size_t)r * (f / 32) + col / 32] = (uint8_t)quant_mx32(hv, words);
+            } else {
+              uint32_t w2[2];
+              p.h_scales[(size_t)r * (f / 16) + col / 16] = (uint8_t)quant_nv16(hv, p.act_scale_h, words);
+              p.h_scales[(size_t)r * (f / 16) + col / 16 + 1] = (uint8_t)quant_nv16(hv + 16, p.act_scale_h, w2);
+              words[2] = w2[0];
+              words[3] = w2[1];
+            }
+            *reinterpret_cast<uint4*>(p.h_codes + (size_t)r * (f / 2) + col / 2) =
+                make_uint4(words[0], words[1], words[2], words[3]);
+          }
+        }
+      } else {
+        // lane = row in TMEM; go through shared memory, half a tile at a
+        // time, so that each store instruction writes 256 contiguous bytes
+        const float sd = FMT == MOE_MXFP4 ? 1.0f : ts[2] * p.act_scale;
+        float* ost = reinterpret_cast<float*>(smem + (size_t)kWsStages * 2 * kOpBytes) +
+                     (size_t)(warp - 6) * 32 * kOStride;
+        float4* myrow = reinterpret_cast<float4*>(ost + lane * kOStride);
+        const int row0 = tile.row_start + 32 * (warp & 3);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t* vv = hf == 0 ? (c == 0 ? v0 : v1) : (c == 0 ? v2 : v3);
+#pragma unroll
+            for (int i2 = 0; i2 < 8; ++i2)
+              myrow[8 * c + i2] = make_float4(__uint_as_float(vv[4 * i2]) * sd, __uint_as_float(vv[4 * i2 + 1]) * sd,
+                                              __uint_as_float(vv[4 * i2 + 2]) * sd, __uint_as_float(vv[4 * i2 + 3]) * sd);
+          }
+          __syncwarp();
+          // two rows per instruction: lanes 0-15 row rr, lanes 16-31 row rr + 1
+          for (int rr = 0; rr < 32; rr += 2) {
+            const int rw = rr + (lane >> 4), rg = row0 + rw;
+            if (rg < tile.row_end)
+              reinterpret_cast<float4*>(p.O + (size_t)rg * p.O_ld + n0 + 64 * hf)[lane & 15] =
+                  reinterpret_cast<const float4*>(ost + rw * kOStride)[lane & 15];
+          }
+          __syncwarp();
+        }
       }
     }
   }
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
-}
-
-template <int FMT>
-__global__ void __launch_bounds__(128, 1)
-gemm_down_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tdn,
-                 GemmArgs p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kStages], done[kStages];
-  __shared__ uint32_t tmem_base;
-  if ((int)blockIdx.x >= *p.n_tiles) return;
-  const Tile tile = p.tiles[blockIdx.x];
-  const int n0 = blockIdx.y * kTileRows;
-  const int warp = threadIdx.x >> 5;
-  if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { tc::mbar_init(&full[s], 1); tc::mbar_init(&done[s], 1); }
-    tc::mbar_init_fence();
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tb = tmem_base;
-  const CUtensorMap* tw[1] = {&tdn};
-  int n_committed = 0;
-  const bool ok = gemm_mainloop<1>(p, &ta, tw, tile, n0, smem, full, done, tb, 128, &n_committed);
-  if (!ok) {
-    if (threadIdx.x == 0) atomicExch(p.err, 1);
-    drain(full, done);
-  } else {
-    const int m = threadIdx.x;
-    const int r = tile.row_start + m;
-    const bool live = r < tile.row_end;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    const float* ts = reinterpret_cast<const float*>(p.slots + (size_t)tile.slot * p.ebytes +
-                                                     p.w_scales_off[2]);
-    const float sd = FMT == MOE_MXFP4 ? 1.0f : ts[2] * p.act_scale;
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tc::tmem_ld32(tb + lane_base + 32 * c, v);
-      tc::tmem_ld_wait();
-      if (live) {
-        float4* dst = reinterpret_cast<float4*>(p.O + (size_t)r * p.O_ld + n0 + 32 * c);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(__uint_as_float(v[4 * i]) * sd, __uint_as_float(v[4 * i + 1]) * sd,
-                               __uint_as_float(v[4 * i + 2]) * sd, __uint_as_float(v[4 * i + 3]) * sd);
-      }
-    }
-  }
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 256);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -481,27 +505,25 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
 }
 
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
-                 uint64_t slot_stride) {
+                 uint64_t slot_stride, uint32_t box_rows = kTileRows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {row_bytes, rows, slots};
   cuuint64_t strides[2] = {row_bytes, slot_stride};
-  cuuint32_t box[3] = {kKTileBytes, kTileRows, 1};
+  cuuint32_t box[3] = {kKTileBytes, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t gemm_smem(int nb) {
-  return 1024 + (size_t)kStages * (1 + nb) * kOpBytes + (size_t)kStages * (1 + nb) * kTileRows * 16;
-}
 
 }  // namespace
 
 // ---------------------------------------------------------------- host side
 struct PrefillPlan {
   CUtensorMap xq, hq, wg, wu, wd;
+  CUtensorMap wg64, wu64;   // gate / up in 64-row boxes (stacked into one 128-row B tile)
   bool ready;
 };
 
@@ -516,7 +538,9 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
               make_map_2d(&pl->hq, hq_codes, g.f / 2, xq_rows) &&
               make_map_3d(&pl->wg, slots + g.off_codes[0], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes) &&
               make_map_3d(&pl->wu, slots + g.off_codes[1], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes) &&
-              make_map_3d(&pl->wd, slots + g.off_codes[2], g.f / 2, g.d, g.S + 1 + g.X, g.ebytes);
+              make_map_3d(&pl->wd, slots + g.off_codes[2], g.f / 2, g.d, g.S + 1 + g.X, g.ebytes) &&
+              make_map_3d(&pl->wg64, slots + g.off_codes[0], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes, 64) &&
+              make_map_3d(&pl->wu64, slots + g.off_codes[1], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes, 64);
   return pl;
 }
 
@@ -542,7 +566,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  const int* offsets, int N, int mode, int with_shared,
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales,
-                                 float* O, float gx, float gh, int* err, cudaStream_t st,
+                                 float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
                                  const cudaEvent_t* ev) {
   Tile* tl = static_cast<Tile*>(tiles);
   build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, g.E, g.S, g.X, N, g.k, mode, with_shared, tl,
@@ -552,10 +576,11 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   const int max_tiles = prefill_max_tiles(g, N);
   static bool attr = false;
   if (!attr) {
-    e = cudaFuncSetAttribute(gemm_gateup_kernel<MOE_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem(2));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_gateup_kernel<MOE_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem(2));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_down_kernel<MOE_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem(1));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_down_kernel<MOE_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem(1));
+    const int s1 = (int)ws_smem<1>(), s2 = (int)ws_smem<2>();
+    e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_MXFP4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_NVFP4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_MXFP4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_NVFP4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -577,12 +602,12 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.h_codes = hq_codes;
   p.h_scales = hq_scales;
   p.act_scale_h = gh;
-  dim3 grid1(max_tiles, g.f / kTileRows);
+  const int grid1 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.f / 64));
   if (ev) cudaEventRecord(ev[0], st);
   if (g.fmt == MOE_MXFP4)
-    gemm_gateup_kernel<MOE_MXFP4><<<grid1, 128, gemm_smem(2), st>>>(pl->xq, pl->wg, pl->wu, p);
+    gemm_ws_kernel<MOE_MXFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   else
-    gemm_gateup_kernel<MOE_NVFP4><<<grid1, 128, gemm_smem(2), st>>>(pl->xq, pl->wg, pl->wu, p);
+    gemm_ws_kernel<MOE_NVFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[1], st);
   if (e != cudaSuccess) return e;
@@ -595,12 +620,12 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.act_scale = g.fmt == MOE_MXFP4 ? 1.0f : gh;
   p.O = O;
   p.O_ld = g.d;
-  dim3 grid2(max_tiles, g.d / kTileRows);
+  const int grid2 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.d / kTileRows));
   if (ev) cudaEventRecord(ev[2], st);
   if (g.fmt == MOE_MXFP4)
-    gemm_down_kernel<MOE_MXFP4><<<grid2, 128, gemm_smem(1), st>>>(pl->hq, pl->wd, p);
+    gemm_ws_kernel<MOE_MXFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else
-    gemm_down_kernel<MOE_NVFP4><<<grid2, 128, gemm_smem(1), st>>>(pl->hq, pl->wd, p);
+    gemm_ws_kernel<MOE_NVFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[3], st);
   return e;
