@@ -58,6 +58,8 @@ MOE_DEV int excl_scan_1024(int v, int* total, int* sh) {
 // Shared-memory scratch of one LRU step.
 struct LruSmem {
   int sh[33];
+  unsigned long long clk;         // clock, staged
+  int so[kMaxE];       // slot_of, staged
   int q[kMaxE];        // victim queue (slots)
   int q_old[kMaxE];    // expert that held q[i] before the step (-1 free)
   int acc_e[kMaxE], acc_s[kMaxE];
@@ -66,19 +68,45 @@ struct LruSmem {
   unsigned char stale[kMaxE];     // occupied by an expert not routed this step
 };
 
-// One step of the table (blockDim.x == 1024).  counts may live in shared or
-// global memory; the table is staged into shared memory before any loop.
+// The table's state, read once per step: every thread issues its loads
+// together (one memory round trip) and parks them in shared memory; callers
+// put other independent loads between lru_load and lru_park.
+struct LruRegs {
+  int so, eo;
+  unsigned long long st, clk;
+};
+MOE_DEV LruRegs lru_load(int E, int S, const int* __restrict__ slot_of, const int* __restrict__ expert_of,
+                         const unsigned long long* __restrict__ stamp,
+                         const unsigned long long* __restrict__ clock) {
+  const int t = threadIdx.x;
+  LruRegs r;
+  r.so = t < E ? slot_of[t] : -1;
+  r.eo = t < S ? expert_of[t] : -1;
+  r.st = t < S ? stamp[t] : 0ull;
+  r.clk = t == 0 ? *clock : 0ull;
+  return r;
+}
+MOE_DEV void lru_park(const LruRegs& r, int E, int S, LruSmem& m) {
+  const int t = threadIdx.x;
+  if (t < E) m.so[t] = r.so;
+  if (t < S) { m.eo[t] = r.eo; m.st[t] = r.st; }
+  if (t == 0) m.clk = r.clk;
+}
+
+// One step of the table (blockDim.x == 1024) on the state parked in m (the
+// caller synchronises after lru_park).  counts may live in shared or global
+// memory.
 MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of,
                       int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                       unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
                       unsigned long long* __restrict__ stats, LruSmem& m) {
   const int tid = threadIdx.x;
-  const unsigned long long clk = *clock;
+  const unsigned long long clk = m.clk;
 
   // hits / misses over experts (E <= 1024: one expert per thread)
   const int e = tid;
   const bool inU = e < E && counts[e] > 0;
-  const int cur = e < E ? slot_of[e] : -1;
+  const int cur = e < E ? m.so[e] : -1;
   const bool hit = inU && cur >= 0, miss = inU && cur < 0;
   int n_hit, n_miss;
   const int hr = excl_scan_1024(hit ? 1 : 0, &n_hit, m.sh);
@@ -91,12 +119,10 @@ MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of
   bool fre = false, stale = false;
   unsigned long long st = 0;
   if (s < S) {
-    old = expert_of[s];
+    old = m.eo[s];
     fre = old < 0 || old >= E;
     stale = !fre && counts[old] == 0;
-    st = stamp[s];
-    m.eo[s] = old;
-    m.st[s] = st;
+    st = m.st[s];
     m.stale[s] = stale ? 1 : 0;
   }
   int n_free;
@@ -163,11 +189,11 @@ MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of
   }
   if (tid == 0) {
     *clock = clk + (unsigned long long)U;
-    if (stats) {
-      stats[0] += 1ull;
-      stats[1] += (unsigned long long)U;
-      stats[2] += (unsigned long long)n_hit;
-      stats[3] += (unsigned long long)n_miss;
+    if (stats) {   // fire-and-forget adds: no round trip
+      atomicAdd(stats + 0, 1ull);
+      atomicAdd(stats + 1, (unsigned long long)U);
+      atomicAdd(stats + 2, (unsigned long long)n_hit);
+      atomicAdd(stats + 3, (unsigned long long)n_miss);
     }
   }
 }
@@ -178,6 +204,8 @@ lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ 
                 unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
                 unsigned long long* __restrict__ stats) {
   __shared__ LruSmem m;
+  lru_park(lru_load(E, S, slot_of, expert_of, stamp, clock), E, S, m);
+  __syncthreads();
   lru_body(counts, E, S, slot_of, expert_of, stamp, clock, rec, stats, m);
 }
 
@@ -195,7 +223,10 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int* 
   int* cnt = reinterpret_cast<int*>(cm + E * perm::kPermWarps);  // [E]
   int* off = cnt + E;                                            // [E]
   int* rows = off + E;                                           // [128][k]
+  // the table's loads and the token ids' loads go out together
+  const LruRegs lr = lru_load(E, S, slot_of, expert_of, stamp, clock);
   perm::stage_rows(idx, N, k, 0, rows);
+  lru_park(lr, E, S, m);
   __syncthreads();
   if (threadIdx.x < perm::kTokPerBlock) perm::build_ballots(rows, k, E, cm);
   __syncthreads();

@@ -13,8 +13,9 @@
 // token's power-of-two exponent used by the expert GEMV to convert x to f16
 // without overflow.
 // topk: one warp per token on its logits row staged in shared memory; k rounds
-// of a warp-wide argmax.  For decode-sized batches the last CTA of the logits
-// kernel runs it, so routing is one launch.
+// of a warp-wide argmax.  For decode-sized batches (router_dec_kernel: one
+// CTA per expert, K split over its warps) the last CTA runs it, so routing is
+// one launch.
 #include "common.cuh"
 
 namespace moe {
@@ -177,6 +178,114 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
   }
 }
 
+// Decode-sized batches (N <= 64): one CTA per expert and token tile, its 8
+// warps splitting K, so each lane issues all of its W_r loads at once (2
+// float4 per lane for d = 2048) and the expert's dot products finish after
+// about one memory round trip; x comes straight from L2.  The 8 partial sums
+// of each logit are added in a fixed order.  The last CTA to finish runs the
+// top-k of every token (one launch for the whole routing).
+template <int TN>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_dec_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
+                  const float* __restrict__ Wr, const float* __restrict__ bias,
+                  float* __restrict__ logits, int* __restrict__ xexp, int k, int norm_topk,
+                  int* __restrict__ idx, float* __restrict__ gates, unsigned int* __restrict__ counter) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __shared__ float part[kRouterWarps][TN];
+  __shared__ bool last;
+  const int e = blockIdx.x, t0 = blockIdx.y * TN;
+  const int nt = min(TN, N - t0);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ks = d / kRouterWarps;          // this warp's K slice (a multiple of 16)
+  const int k0 = warp * ks;
+  // W_r: 4 floats per load, every load of the slice issued before any use
+  const float4* w4 = reinterpret_cast<const float4*>(Wr + (size_t)e * d + k0);
+  const int nv = ks / 4;                     // float4 per warp slice
+  float acc[TN];
+#pragma unroll
+  for (int t = 0; t < TN; ++t) acc[t] = 0.f;
+  for (int base = 0; base < nv; base += 4 * 32) {
+    float4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * 32 + lane;
+      w[u] = i < nv ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int t = 0; t < TN; ++t) {
+      if (t < nt) {
+        const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * d + k0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = base + u * 32 + lane;
+          if (i < nv) {
+            const uint2 xv = xr[i];
+            acc[t] = fmaf(w[u].x, __uint_as_float(xv.x << 16), acc[t]);
+            acc[t] = fmaf(w[u].y, __uint_as_float(xv.x & 0xffff0000u), acc[t]);
+            acc[t] = fmaf(w[u].z, __uint_as_float(xv.y << 16), acc[t]);
+            acc[t] = fmaf(w[u].w, __uint_as_float(xv.y & 0xffff0000u), acc[t]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TN; ++t) {
+    float v = acc[t];
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) part[warp][t] = v;
+  }
+  if (e == 0 && xexp != nullptr) {
+    // per-token exponent s with amax(|x|) * 2^-s in [2^14, 2^15): warp t takes token t
+    for (int t = warp; t < nt; t += kRouterWarps) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d);
+      float m = 0.f;
+      for (int i = lane; i < d / 8; i += 32) {
+        const uint4 v = xr[i];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xffff0000u))));
+      }
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) {
+        int s = 0;
+        if (m > 0.f) {
+          int ex;
+          frexpf(m, &ex);
+          s = max(-100, min(100, ex - 15));
+        }
+        xexp[t0 + t] = s;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < nt) {
+    float v = bias ? bias[e] : 0.f;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRouterWarps; ++w) sum += part[w][threadIdx.x];
+    logits[(size_t)(t0 + threadIdx.x) * E + e] = sum + v;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int n = atomicAdd(counter, 1u);
+    last = n == gridDim.x * gridDim.y - 1;
+  }
+  __syncthreads();
+  if (last) {
+    __threadfence();
+    float* Ls = reinterpret_cast<float*>(smem_raw) + (size_t)warp * E;
+    for (int t = warp; t < N; t += kRouterWarps) {
+      stage_logits(logits, t, E, Ls);
+      topk_row(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
+      __syncwarp();
+    }
+    if (threadIdx.x == 0) *counter = 0u;
+  }
+}
+
 __global__ void __launch_bounds__(256)
 router_topk_kernel(const float* __restrict__ logits, int N, int E, int k, int norm_topk,
                    int* __restrict__ idx, float* __restrict__ gates) {
@@ -213,11 +322,14 @@ cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const flo
         x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter);     \
   }
   if (fuse) {
+    // decode sizes: one CTA per expert and token tile (router_dec_kernel)
+    const dim3 gd(g.E, (N + TN - 1) / TN);
+    const size_t sm = (size_t)kRouterWarps * g.E * sizeof(float);
     switch (TN) {
-      case 1: MOE_ROUTER_CASE(1, true) break;
-      case 2: MOE_ROUTER_CASE(2, true) break;
-      case 4: MOE_ROUTER_CASE(4, true) break;
-      default: MOE_ROUTER_CASE(8, true) break;
+      case 1: router_dec_kernel<1><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
+      case 2: router_dec_kernel<2><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
+      case 4: router_dec_kernel<4><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
+      default: router_dec_kernel<8><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
     }
     return cudaGetLastError();
   }
