@@ -89,7 +89,7 @@ struct moe_layer {
   bool shared_set = false;
   cudaStream_t fill[kFillStreams] = {};       // miss fills, round robin
   cudaEvent_t ev_fills[kFillStreams] = {};
-  cudaEvent_t ev_route = nullptr, ev_fill = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_rec = nullptr;
   int fill_mode = MOE_FILL_MEMCPY;
   const uint8_t* pool_dev = nullptr;          // device address of the host pool
   unsigned long long* stats = nullptr;        // steps, distinct, hits, misses
@@ -217,7 +217,8 @@ void release(moe_layer* L) {
     L->ev_fills[i] = nullptr;
     L->fill[i] = nullptr;
   }
-  L->ev_route = L->ev_fill = nullptr;
+  if (L->ev_rec) cudaEventDestroy(L->ev_rec);
+  L->ev_route = L->ev_fill = L->ev_rec = nullptr;
 }
 
 int pointer_kind(const void* p, bool* on_device, int device) {
@@ -404,7 +405,8 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
             cudaEventCreateWithFlags(&L->ev_fills[i], cudaEventDisableTiming) == cudaSuccess;
     if (!sok ||
         cudaEventCreateWithFlags(&L->ev_route, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&L->ev_rec, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       rc = MOE_ERR_CUDA;
     }
@@ -648,9 +650,14 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   }
   const bool dev_fill = !resident && L->fill_mode == MOE_FILL_DEVICE;
   if (!resident) {
-    if (!dev_fill)
-      MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
     MOE_CUDA(L, cudaEventRecord(L->ev_route, st));
+    if (!dev_fill) {
+      // the record goes to the host from a side stream, so the caller stream
+      // runs routing -> expert FFN kernel to kernel
+      MOE_CUDA(L, cudaStreamWaitEvent(L->fill[0], L->ev_route, 0));
+      MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, L->fill[0]));
+      MOE_CUDA(L, cudaEventRecord(L->ev_rec, L->fill[0]));
+    }
   }
   GemvArgs a{};
   a.slots = L->slots;
@@ -719,7 +726,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
     waves = (max_miss + g.S - 1) / g.S;
   } else if (!resident) {
-    MOE_CUDA(L, cudaEventSynchronize(L->ev_route));
+    MOE_CUDA(L, cudaEventSynchronize(L->ev_rec));
     const StepRecord* r = L->rec_host;
     U = r->U;
     n_hit = r->n_hit;

@@ -13,6 +13,7 @@ namespace {
 __global__ void combine_kernel(const float* __restrict__ O, const float* __restrict__ gates,
                                const int* __restrict__ row_of, int N, int k, int d, int shared,
                                __nv_bfloat16* __restrict__ y) {
+  pdl_wait();
   const int q = d / 4;
   const int v = blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= N * q) return;
@@ -47,9 +48,8 @@ cudaError_t launch_combine(const Geo& g, const float* O, const float* gates, con
                            int N, __nv_bfloat16* y, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
   const int total = N * (g.d / 4);
-  combine_kernel<<<(total + 255) / 256, 256, 0, st>>>(O, gates, row_of, N, g.k, g.d, g.has_shared,
-                                                     y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((total + 255) / 256), dim3(256), 0, st, O, gates, row_of, N, g.k,
+                    g.d, g.has_shared, y);
 }
 
 }  // namespace moe

@@ -12,6 +12,34 @@
 
 namespace moe {
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel started with launch_pdl may begin while its predecessor on the
+// stream still runs (programmatic dependent launch): it must call pdl_wait()
+// before it reads anything the predecessor (or an earlier kernel) writes, and
+// it may only write what no running kernel reads.  pdl_trigger() lets the
+// successor start early; a kernel whose successor reads anything before its
+// own pdl_wait() triggers only after its own pdl_wait(), so those reads see
+// the finished work of every kernel before it.  Both are no-ops for kernels
+// launched normally.
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 constexpr int kWarp = 32;

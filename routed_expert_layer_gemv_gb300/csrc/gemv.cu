@@ -419,6 +419,13 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     tc::mbar_init_fence();
   }
   __syncthreads();
+  // launched as a dependent of the previous kernel: phase 2's producer only
+  // reads the step record and weights, both final before phase 1 got past its
+  // own wait, so it starts streaming at once; everything else waits for the
+  // predecessor.  The successor is released only after this wait, so what
+  // the successor's producer reads without waiting is final by then.
+  if (PH == 1 || warp != kProd) pdl_wait();
+  pdl_trigger();
   const Range rr = cta_range(g, a, p);
   // the first token group is staged by every warp but the producer (its
   // latency is on the critical path); the epilogue stages later ones ahead
@@ -651,8 +658,8 @@ cudaError_t launch_phase(const Geo& g, const GemvPlan* pl, const GemvArgs& a, co
   const CUtensorMap& m1 = PH == 1 ? pl->w[1] : pl->w[2];
   const CUtensorMap& s0 = PH == 1 ? pl->s[0] : pl->s[2];
   const CUtensorMap& s1 = PH == 1 ? pl->s[1] : pl->s[2];
-  gemv_stream_kernel<FMT, PH><<<grid, kThreads, p.smem, st>>>(m0, m1, s0, s1, g, a, p, x, xexp, h, O);
-  return cudaGetLastError();
+  return launch_pdl(gemv_stream_kernel<FMT, PH>, dim3(grid), dim3(kThreads), (size_t)p.smem, st, m0, m1, s0, s1, g,
+                    a, p, x, xexp, h, O);
 }
 
 template <int FMT>

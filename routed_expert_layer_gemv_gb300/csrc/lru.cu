@@ -223,8 +223,11 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int* 
   int* cnt = reinterpret_cast<int*>(cm + E * perm::kPermWarps);  // [E]
   int* off = cnt + E;                                            // [E]
   int* rows = off + E;                                           // [128][k]
-  // the table's loads and the token ids' loads go out together
+  // the table was last written by the previous step's tail, which finished
+  // before the router began: its loads go out before waiting for the router
+  pdl_trigger();
   const LruRegs lr = lru_load(E, S, slot_of, expert_of, stamp, clock);
+  pdl_wait();
   perm::stage_rows(idx, N, k, 0, rows);
   lru_park(lr, E, S, m);
   __syncthreads();
@@ -300,10 +303,8 @@ cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  route_tail_kernel<<<1, kLruThreads, smem, st>>>(idx, N, g.k, g.E, g.S, counts, offsets, row_of,
-                                                  tok_of, slot_of, expert_of, stamp, clock, rec,
-                                                  stats);
-  return cudaGetLastError();
+  return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, counts,
+                    offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, rec, stats);
 }
 
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,

@@ -193,6 +193,7 @@ router_dec_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ float part[kRouterWarps][TN];
   __shared__ bool last;
+  pdl_trigger();   // the routing tail may start: it waits for these results before reading them
   const int e = blockIdx.x, t0 = blockIdx.y * TN;
   const int nt = min(TN, N - t0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
