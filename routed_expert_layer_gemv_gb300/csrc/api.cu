@@ -47,6 +47,7 @@ struct moe_layer {
   uint8_t* slots = nullptr;
   uint8_t* shared_w = nullptr;
   float* Wr = nullptr;
+  __nv_bfloat16* Wr_hl = nullptr;   // W_r as three bf16 parts summing to it (tensor-core router)
   float* bias = nullptr;
   int* slot_of = nullptr;
   int* expert_of = nullptr;
@@ -338,6 +339,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   MOE_ALLOC(slots, (size_t)(g.S + 1 + g.X) * g.ebytes);
   if (rc == MOE_OK) L->shared_w = L->slots + (size_t)g.S * g.ebytes;
   MOE_ALLOC(Wr, (size_t)g.E * g.d * 4);
+  MOE_ALLOC(Wr_hl, (size_t)g.E * g.d * 6);
   MOE_ALLOC(bias, (size_t)g.E * 4);
   MOE_ALLOC(slot_of, (size_t)g.E * 4);
   MOE_ALLOC(expert_of, (size_t)g.S * 4);
@@ -450,6 +452,8 @@ int moe_set_router(moe_layer_t L, const float* W_r, const float* bias) {
   if (!W_r) return fail(L, MOE_ERR_ARG, "W_r is NULL");
   if (L->g.has_bias && !bias) return fail(L, MOE_ERR_ARG, "layer has a bias but bias is NULL");
   MOE_CUDA(L, cudaMemcpy(L->Wr, W_r, (size_t)L->g.E * L->g.d * 4, cudaMemcpyDefault));
+  MOE_CUDA(L, launch_router_split(L->g, L->Wr, L->Wr_hl, nullptr));
+  MOE_CUDA(L, cudaDeviceSynchronize());
   if (L->g.has_bias) MOE_CUDA(L, cudaMemcpy(L->bias, bias, (size_t)L->g.E * 4, cudaMemcpyDefault));
   L->router_set = true;
   return MOE_OK;
@@ -624,7 +628,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
 
   L->launches = 0;
   cudaEvent_t* pe = prof_begin(L, MOE_PROF_ROUTER, st);
-  MOE_CUDA(L, launch_router(g, xd, N, L->Wr, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
+  MOE_CUDA(L, launch_router(g, xd, N, L->Wr, L->Wr_hl, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
                             L->gates, L->xexp, L->rcounter, st));
   prof_end(pe, st);
   L->launches += N <= 64 ? 1 : 2;
@@ -850,7 +854,7 @@ int moe_debug_router(moe_layer_t L, const void* x, int N, int* idx, float* gates
   if (N == 0) return MOE_OK;
   if (!x || !idx || !gates) return fail(L, MOE_ERR_ARG, "NULL pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(L, launch_router(L->g, static_cast<const __nv_bfloat16*>(x), N, L->Wr,
+  MOE_CUDA(L, launch_router(L->g, static_cast<const __nv_bfloat16*>(x), N, L->Wr, L->Wr_hl,
                             L->g.has_bias ? L->bias : nullptr, logits ? logits : L->logits, idx,
                             gates, L->xexp, L->rcounter, st));
   return MOE_OK;

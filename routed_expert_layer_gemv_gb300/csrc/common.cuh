@@ -108,9 +108,13 @@ __host__ __device__ inline int access_slot(const int* acc_slot, int S, int i) {
 // ---------------------------------------------------------------- launchers
 // router.cu
 // counter: a zeroed device word (enables the one-launch path for N <= 64), or null
+// Whl (may be null): W_r split into three bf16 parts [3][E][d]
+// (launch_router_split); with it, batches over 64 tokens take the tensor-core
+// logits kernel
 cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
-                          const float* bias, float* logits, int* idx, float* gates, int* xexp,
-                          unsigned int* counter, cudaStream_t st);
+                          const __nv_bfloat16* Whl, const float* bias, float* logits, int* idx,
+                          float* gates, int* xexp, unsigned int* counter, cudaStream_t st);
+cudaError_t launch_router_split(const Geo& g, const float* Wr, __nv_bfloat16* Whl, cudaStream_t st);
 // permute.cu
 size_t permute_scratch_bytes(const Geo& g, int max_tokens);
 cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int* offsets,

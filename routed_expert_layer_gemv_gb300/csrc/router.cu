@@ -7,15 +7,14 @@
 // MoE 塞进游戏 PC", zhichai.net, §二 "Decode" paragraph; ananclaw.com
 // explainer, §核心方法 1).  This is the standard softmax top-k router.
 //
-// logits kernel: one warp per expert, a tile of TN tokens per CTA held in
-// shared memory as bf16; W_r rows stream through with 128-bit loads.  The
-// warp reduces TN dot products with shuffles.  CTA (0, tile) also writes each
-// token's power-of-two exponent used by the expert GEMV to convert x to f16
-// without overflow.
-// topk: one warp per token on its logits row staged in shared memory; k rounds
-// of a warp-wide argmax.  For decode-sized batches (router_dec_kernel: one
-// CTA per expert, K split over its warps) the last CTA runs it, so routing is
-// one launch.
+// Decode-sized batches (router_dec_kernel): one CTA per expert and token
+// tile, K split over its warps; its last CTA runs the top-k, so routing is
+// one launch.  Larger batches (router_tc_kernel): logits on tensor cores from
+// a three-part bf16 split of W_r, then router_topk_kernel.  The CTAs that
+// see a token's whole row also write its power-of-two exponent, used by the
+// expert GEMV to convert x to f16 without overflow.
+// topk: one warp per token on its logits row staged in shared memory; k
+// rounds of a warp-wide argmax.
 #include "common.cuh"
 
 namespace moe {
@@ -77,105 +76,6 @@ MOE_DEV void stage_logits(const float* logits, int t, int E, float* Ls) {
   const int lane = threadIdx.x & 31;
   for (int e = lane; e < E; e += 32) Ls[e] = __ldcg(logits + (size_t)t * E + e);
   __syncwarp();
-}
-
-// logits = x W_r^T (+ b): one warp per expert, TN tokens per CTA held in
-// shared memory.  CTA (0, tile) also writes each token's f16 exponent.  With
-// FUSE, the last CTA to finish (a device counter, reset by that CTA) runs the
-// top-k of every token, so decode-sized batches route in one launch.
-template <int TN, bool FUSE>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-router_logits_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
-                     const float* __restrict__ Wr, const float* __restrict__ bias,
-                     float* __restrict__ logits, int* __restrict__ xexp, int k, int norm_topk,
-                     int* __restrict__ idx, float* __restrict__ gates,
-                     unsigned int* __restrict__ counter) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem_raw);  // [TN][d]
-  __shared__ bool last;
-  const int t0 = blockIdx.y * TN;
-  const int nt = min(TN, N - t0);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-  // stage the token tile (16-byte vectors; d is a multiple of 128)
-  const int vec_per_row = d / 8;
-  for (int v = threadIdx.x; v < TN * vec_per_row; v += blockDim.x) {
-    const int t = v / vec_per_row, c = v % vec_per_row;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (t < nt) val = reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d)[c];
-    reinterpret_cast<uint4*>(xs + (size_t)t * d)[c] = val;
-  }
-  __syncthreads();
-
-  if (blockIdx.x == 0 && xexp != nullptr) {
-    // per-token exponent s with amax(|x|) * 2^-s in [2^14, 2^15)
-    for (int t = warp; t < nt; t += kRouterWarps) {
-      float m = 0.f;
-      for (int i = lane; i < d; i += 32) m = fmaxf(m, fabsf(__bfloat162float(xs[(size_t)t * d + i])));
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) {
-        int s = 0;
-        if (m > 0.f) {
-          int ex;
-          frexpf(m, &ex);
-          s = max(-100, min(100, ex - 15));
-        }
-        xexp[t0 + t] = s;
-      }
-    }
-  }
-
-  const int e = blockIdx.x * kRouterWarps + warp;
-  if (e < E) {
-    float acc[TN];
-#pragma unroll
-    for (int t = 0; t < TN; ++t) acc[t] = 0.f;
-    const float4* w4 = reinterpret_cast<const float4*>(Wr + (size_t)e * d);
-    for (int i4 = lane; i4 < d / 4; i4 += 32) {
-      const float4 w = __ldg(w4 + i4);
-#pragma unroll
-      for (int t = 0; t < TN; ++t) {
-        const uint2 xv = reinterpret_cast<const uint2*>(xs + (size_t)t * d)[i4];
-        const float x0 = __uint_as_float(xv.x << 16), x1 = __uint_as_float(xv.x & 0xffff0000u);
-        const float x2 = __uint_as_float(xv.y << 16), x3 = __uint_as_float(xv.y & 0xffff0000u);
-        acc[t] = fmaf(w.x, x0, acc[t]);
-        acc[t] = fmaf(w.y, x1, acc[t]);
-        acc[t] = fmaf(w.z, x2, acc[t]);
-        acc[t] = fmaf(w.w, x3, acc[t]);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < TN; ++t) {
-      float v = acc[t];
-      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      acc[t] = v;
-    }
-    if (lane == 0) {
-      const float b = bias ? bias[e] : 0.f;
-#pragma unroll
-      for (int t = 0; t < TN; ++t)
-        if (t < nt) logits[(size_t)(t0 + t) * E + e] = acc[t] + b;
-    }
-  }
-  if (FUSE) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const unsigned int n = atomicAdd(counter, 1u);
-      last = n == gridDim.x * gridDim.y - 1;
-    }
-    __syncthreads();
-    if (last) {
-      __threadfence();
-      float* Ls = reinterpret_cast<float*>(smem_raw + (size_t)TN * d * 2) + (size_t)warp * E;
-      for (int t = warp; t < N; t += kRouterWarps) {
-        stage_logits(logits, t, E, Ls);
-        topk_row(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
-        __syncwarp();
-      }
-      if (threadIdx.x == 0) *counter = 0u;
-    }
-  }
 }
 
 // Decode-sized batches (N <= 64): one CTA per expert and token tile, its 8
@@ -287,6 +187,179 @@ router_dec_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
   }
 }
 
+// Large batches (prefill): logits on tensor cores.  W_r is split once into
+// three bf16 parts W = W0 + W1 + W2 + r with W0 = bf16(W), W1 = bf16(W - W0),
+// W2 = bf16(W - W0 - W1) (each difference is exact in fp32), so |r| <= 2^-24
+// |W|: the split is as close to W as W's own fp32 rounding.  x is exact in
+// bf16, so x W^T = sum_p x W_p^T with fp32 accumulation (mma.sync m16n8k16
+// bf16) gives fp32-class logits at tensor-core rate.  CTA tile 64 tokens x 64
+// experts, K in chunks of 64 through a cp.async double buffer; 8 warps as 2
+// (tokens) x 4 (experts), each 32 x 16.  CTAs of expert tile 0 also write the
+// per-token f16 exponent of x.
+constexpr int kTcM = 64, kTcN = 64, kTcK = 64, kTcParts = 3;
+constexpr int kTcRow = kTcK + 8;          // padded smem row (bf16): 144 bytes, conflict-free ldmatrix
+constexpr int kTcRows = kTcM + kTcParts * kTcN;
+constexpr int kTcStage = kTcRows * kTcRow;   // bf16 elements per stage
+
+__global__ void router_split_kernel(const float* __restrict__ W, size_t n, __nv_bfloat16* __restrict__ parts) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float r = W[i];
+#pragma unroll
+  for (int p = 0; p < kTcParts; ++p) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(r);
+    parts[(size_t)p * n + i] = h;
+    r -= __bfloat162float(h);
+  }
+}
+
+MOE_DEV void cp16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+
+MOE_DEV void ldsm_x4(const void* p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+
+MOE_DEV void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+               "{%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(256)
+router_tc_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E, const __nv_bfloat16* __restrict__ Wp,
+                 const float* __restrict__ bias, float* __restrict__ logits, int* __restrict__ xexp) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __nv_bfloat16* sm = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  const int t0 = blockIdx.x * kTcM, e0 = blockIdx.y * kTcN;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wm = warp >> 2, wn = warp & 3;      // 2 x 4 warps: 32 tokens x 16 experts each
+  const size_t part = (size_t)E * d;
+  const int nk = d / kTcK;
+  auto load = [&](int kc, int buf) {
+    __nv_bfloat16* st = sm + (size_t)buf * kTcStage;
+    // rows: 64 tokens, then 64 experts of each W part; 8 chunks of 16 bytes per row
+    for (int v = threadIdx.x; v < kTcRows * 8; v += 256) {
+      const int r = v >> 3, c = v & 7;
+      const __nv_bfloat16* src;
+      bool ok;
+      if (r < kTcM) {
+        ok = t0 + r < N;
+        src = x + (size_t)min(t0 + r, N - 1) * d + kc * kTcK + 8 * c;
+      } else {
+        const int rr = (r - kTcM) % kTcN, p = (r - kTcM) / kTcN;
+        ok = e0 + rr < E;
+        src = Wp + p * part + (size_t)min(e0 + rr, E - 1) * d + kc * kTcK + 8 * c;
+      }
+      cp16_zfill(st + (size_t)r * kTcRow + 8 * c, src, ok);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  float acc[2][2][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.f;
+  load(0, 0);
+  for (int kc = 0; kc < nk; ++kc) {
+    if (kc + 1 < nk) {
+      load(kc + 1, (kc + 1) & 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    const __nv_bfloat16* xa = sm + (size_t)(kc & 1) * kTcStage;
+    const __nv_bfloat16* wb = xa + (size_t)kTcM * kTcRow;
+#pragma unroll
+    for (int k16 = 0; k16 < kTcK / 16; ++k16) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int row = wm * 32 + 16 * i + (lane & 7) + 8 * ((lane >> 3) & 1);
+        ldsm_x4(xa + (size_t)row * kTcRow + 16 * k16 + 8 * (lane >> 4), a[i]);
+      }
+      // The tensor core's own accumulation is not round-to-nearest, so a
+      // long chain of MMAs on one accumulator drifts: each 16-wide step sums
+      // its three parts (smallest first) from zero, and the step's result is
+      // added to the running sums with ordinary fp32 adds.
+      float tmp[2][2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tmp[i][j][q] = 0.f;
+#pragma unroll
+      for (int p = kTcParts - 1; p >= 0; --p) {
+        uint32_t b[4];   // b0, b1 of experts n0..n0+7, then of n0+8..n0+15
+        const int n = p * kTcN + wn * 16 + (lane & 7) + 8 * (lane >> 4);
+        ldsm_x4(wb + (size_t)n * kTcRow + 16 * k16 + 8 * ((lane >> 3) & 1), b);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          mma_bf16(tmp[i][0], a[i], b[0], b[1]);
+          mma_bf16(tmp[i][1], a[i], b[2], b[3]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[i][j][q] += tmp[i][j][q];
+    }
+    __syncthreads();
+  }
+  // fragment (i, j): rows wm*32 + 16i + g (+8), columns wn*16 + 8j + 2q (+1)
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int t = t0 + wm * 32 + 16 * i + g + 8 * hh;
+        const int e = e0 + wn * 16 + 8 * j + 2 * q;
+        if (t < N) {
+          if (e < E) logits[(size_t)t * E + e] = acc[i][j][2 * hh] + (bias ? bias[e] : 0.f);
+          if (e + 1 < E) logits[(size_t)t * E + e + 1] = acc[i][j][2 * hh + 1] + (bias ? bias[e + 1] : 0.f);
+        }
+      }
+  if (blockIdx.y == 0 && xexp != nullptr) {
+    // per-token exponent s with amax(|x|) * 2^-s in [2^14, 2^15): warp w takes tokens w, w + 8, ...
+    for (int tl = warp; tl < kTcM; tl += 8) {
+      const int t = t0 + tl;
+      if (t >= N) break;
+      const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+      float m = 0.f;
+      for (int i2 = lane; i2 < d / 8; i2 += 32) {
+        const uint4 v = xr[i2];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[qq] << 16)), fabsf(__uint_as_float(wv[qq] & 0xffff0000u))));
+      }
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) {
+        int s = 0;
+        if (m > 0.f) {
+          int ex;
+          frexpf(m, &ex);
+          s = max(-100, min(100, ex - 15));
+        }
+        xexp[t] = s;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256)
 router_topk_kernel(const float* __restrict__ logits, int N, int E, int k, int norm_topk,
                    int* __restrict__ idx, float* __restrict__ gates) {
@@ -300,51 +373,44 @@ router_topk_kernel(const float* __restrict__ logits, int N, int E, int k, int no
 
 }  // namespace
 
+cudaError_t launch_router_split(const Geo& g, const float* Wr, __nv_bfloat16* Wp, cudaStream_t st) {
+  const size_t n = (size_t)g.E * g.d;
+  router_split_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(Wr, n, Wp);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
-                          const float* bias, float* logits, int* idx, float* gates,
-                          int* xexp, unsigned int* counter, cudaStream_t st) {
+                          const __nv_bfloat16* Whl, const float* bias, float* logits, int* idx,
+                          float* gates, int* xexp, unsigned int* counter, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
-  const int TN = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : 8;
-  const bool fuse = N <= 64 && counter != nullptr;
-  dim3 grid((g.E + kRouterWarps - 1) / kRouterWarps, (N + TN - 1) / TN);
-  const size_t smem = (size_t)TN * g.d * sizeof(__nv_bfloat16) +
-                      (fuse ? (size_t)kRouterWarps * g.E * sizeof(float) : 0);
-  cudaError_t err = cudaSuccess;
-#define MOE_ROUTER_CASE(V, F)                                                                \
-  {                                                                                          \
-    static bool attr = false;                                                                \
-    if (!attr) {                                                                             \
-      err = cudaFuncSetAttribute(router_logits_kernel<V, F>,                                 \
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);   \
-      if (err != cudaSuccess) return err;                                                    \
-      attr = true;                                                                           \
-    }                                                                                        \
-    router_logits_kernel<V, F><<<grid, kRouterWarps * 32, smem, st>>>(                       \
-        x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter);     \
-  }
-  if (fuse) {
-    // decode sizes: one CTA per expert and token tile (router_dec_kernel)
-    const dim3 gd(g.E, (N + TN - 1) / TN);
-    const size_t sm = (size_t)kRouterWarps * g.E * sizeof(float);
-    switch (TN) {
-      case 1: router_dec_kernel<1><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
-      case 2: router_dec_kernel<2><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
-      case 4: router_dec_kernel<4><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
-      default: router_dec_kernel<8><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
+  if (Whl == nullptr || counter == nullptr) return cudaErrorInvalidValue;
+  if (N > 64) {
+    // large batches: tensor-core logits, then the top-k kernel
+    const size_t smem = (size_t)2 * kTcStage * sizeof(__nv_bfloat16);
+    static bool attr = false;
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
     }
+    const dim3 grid((N + kTcM - 1) / kTcM, (g.E + kTcN - 1) / kTcN);
+    router_tc_kernel<<<grid, 256, smem, st>>>(x, N, g.d, g.E, Whl, bias, logits, xexp);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    router_topk_kernel<<<(N + 7) / 8, 256, (size_t)8 * g.E * sizeof(float), st>>>(logits, N, g.E, g.k,
+                                                                                g.norm_topk, idx, gates);
     return cudaGetLastError();
   }
+  // decode sizes: one CTA per expert and token tile, top-k fused (router_dec_kernel)
+  const int TN = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : 8;
+  const dim3 gd(g.E, (N + TN - 1) / TN);
+  const size_t sm = (size_t)kRouterWarps * g.E * sizeof(float);
   switch (TN) {
-    case 1: MOE_ROUTER_CASE(1, false) break;
-    case 2: MOE_ROUTER_CASE(2, false) break;
-    case 4: MOE_ROUTER_CASE(4, false) break;
-    default: MOE_ROUTER_CASE(8, false) break;
+    case 1: router_dec_kernel<1><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
+    case 2: router_dec_kernel<2><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
+    case 4: router_dec_kernel<4><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
+    default: router_dec_kernel<8><<<gd, kRouterWarps * 32, sm, st>>>(x, N, g.d, g.E, Wr, bias, logits, xexp, g.k, g.norm_topk, idx, gates, counter); break;
   }
-#undef MOE_ROUTER_CASE
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  router_topk_kernel<<<(N + 7) / 8, 256, (size_t)8 * g.E * sizeof(float), st>>>(logits, N, g.E, g.k,
-                                                                              g.norm_topk, idx, gates);
   return cudaGetLastError();
 }
 

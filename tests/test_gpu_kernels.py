@@ -82,7 +82,10 @@ def test_activation_quantiser_bit_exact(fmt, g_x):
     dict(spec=wl.PREFILL_753B.layer, N=24),                         # bias, E=256, d=6144
     dict(spec=small_spec(E=32, k=6, d_model=512, norm_topk=False), N=33),
     dict(spec=small_spec(E=16, k=16, n_slots=16), N=5),             # k = E
-    dict(spec=wl.DECODE_284B.layer, N=150),                          # separate top-k launch
+    dict(spec=wl.DECODE_284B.layer, N=150),                          # tensor-core logits
+    dict(spec=wl.PREFILL_753B.layer, N=200),                         # 2 expert tiles, ragged tokens
+    dict(spec=small_spec(E=32, k=6, d_model=512, norm_topk=False), N=130),   # E below one tile
+    dict(spec=wl.DECODE_35B.layer, N=65),                            # one token past the decode router
 ])
 def test_router_indices_bit_exact(case):
     spec, N = case["spec"], case["N"]
