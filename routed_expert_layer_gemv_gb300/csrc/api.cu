@@ -354,7 +354,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   MOE_ALLOC(row_of, Nm * g.k * 4);
   MOE_ALLOC(tok_of, Nm * g.k * 4);
   MOE_ALLOC(perm_scratch, permute_scratch_bytes(g, (int)Nm));
-  MOE_ALLOC(rec, rec_bytes(g.E));
+  MOE_ALLOC(rec, rec_dev_bytes(g.E));
   MOE_ALLOC(h, rows * g.f * 8);   // decode: scaled W_g x and W_u x per row
   MOE_ALLOC(hmax, rows * (g.f / 64) * 8);
   MOE_ALLOC(O, rows * g.d * 4);
@@ -420,7 +420,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
               cudaMemset(L->stamp, 0, (size_t)g.S * 8) == cudaSuccess &&
               cudaMemset(L->clock, 0, 8) == cudaSuccess &&
               cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
-              cudaMemset(L->rec, 0, rec_bytes(g.E)) == cudaSuccess &&
+              cudaMemset(L->rec, 0, rec_dev_bytes(g.E)) == cudaSuccess &&
               cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
               cudaMemset(L->stats, 0, 64) == cudaSuccess &&
               cudaDeviceSynchronize() == cudaSuccess;
@@ -551,7 +551,7 @@ int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, in
   const Geo& g = L->g;
   if (n > 0) MOE_CUDA(L, cudaMemcpyAsync(L->list_dev, experts, (size_t)n * 4, cudaMemcpyHostToDevice, st));
   MOE_CUDA(L, launch_counts_from_list(g, L->list_dev, n, L->counts, st));
-  MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec,
+  MOE_CUDA(L, launch_lru_step(g, L->counts, nullptr, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec,
                               nullptr, st));
   MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
   MOE_CUDA(L, cudaStreamSynchronize(st));
@@ -647,8 +647,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     prof_end(pe, st);
     L->launches += 3;
     pe = prof_begin(L, MOE_PROF_LRU, st);
-    MOE_CUDA(L, launch_lru_step(g, L->counts, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec,
-                                L->stats, st));
+    MOE_CUDA(L, launch_lru_step(g, L->counts, L->offsets, L->slot_of, L->expert_of, L->stamp, L->clock,
+                                L->rec, L->stats, st));
     prof_end(pe, st);
     L->launches += 1;
   }

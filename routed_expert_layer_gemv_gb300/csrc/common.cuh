@@ -80,7 +80,16 @@ struct StepRecord {
 __host__ __device__ inline int* rec_expert(StepRecord* r) { return reinterpret_cast<int*>(r + 1); }
 __host__ __device__ inline int* rec_slot(StepRecord* r, int E) { return rec_expert(r) + E; }
 __host__ __device__ inline int* rec_evicted(StepRecord* r, int E) { return rec_expert(r) + 2 * E; }
+// bytes the host reads back (header and the three access arrays)
 inline size_t rec_bytes(int E) { return sizeof(StepRecord) + 3 * sizeof(int) * (size_t)E; }
+// Device-only tail: per access i, {physical slot (access_slot, -1 when the
+// record is inconsistent), first permuted row, rows, expert}, so a kernel
+// finds an access's weights and tokens with one 16-byte load.
+__host__ __device__ inline int4* rec_entry(StepRecord* r, int E) {
+  const size_t off = (sizeof(StepRecord) + 3 * sizeof(int) * (size_t)E + 15) & ~size_t(15);
+  return reinterpret_cast<int4*>(reinterpret_cast<char*>(r) + off);
+}
+inline size_t rec_dev_bytes(int E) { return ((rec_bytes(E) + 15) & ~size_t(15)) + sizeof(int4) * (size_t)E; }
 
 // ---------------------------------------------------------------- layer geometry
 struct Geo {
@@ -121,8 +130,10 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
                            int* row_of, int* tok_of, void* scratch, cudaStream_t st);
 // lru.cu
 // stats (may be null): steps, distinct experts, hits, misses, accumulated
-cudaError_t launch_lru_step(const Geo& g, const int* counts, int* slot_of, int* expert_of,
-                            unsigned long long* stamp, unsigned long long* clock,
+// offsets (may be null: entries then get no rows) = the permutation's
+// expert row offsets, for the record's entry table
+cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets, int* slot_of,
+                            int* expert_of, unsigned long long* stamp, unsigned long long* clock,
                             StepRecord* rec, unsigned long long* stats, cudaStream_t st);
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
                                unsigned long long* stamp, unsigned long long* clock,

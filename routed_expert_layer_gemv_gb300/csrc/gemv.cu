@@ -146,17 +146,14 @@ MOE_DEV int count_entries(const Geo& g, const GemvArgs& a, int* base, int* nr) {
 
 MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int ent, Entry& out) {
   if (ent < nr) {
-    StepRecord* rec = const_cast<StepRecord*>(a.rec);
-    const int acc = base + ent;
-    const int ex = rec_expert(rec)[acc];
-    const int ls = rec_slot(rec, g.E)[acc];
-    if (ex < 0 || ex >= g.E || ls < 0 || ls >= g.S || acc - g.S >= g.X) return false;
-    const int sl = access_slot(rec_slot(rec, g.E), g.S, acc);
-    out.slot = sl;
-    out.row0 = a.offsets[ex];
-    out.nrows = a.offsets[ex + 1] - out.row0;
+    // one 16-byte load: physical slot, first row, rows (the LRU step wrote it)
+    const int4 v = rec_entry(const_cast<StepRecord*>(a.rec), g.E)[base + ent];
+    const bool slot_ok = (v.x >= 0 && v.x < g.S) || (v.x > g.S && v.x <= g.S + g.X);
+    out.slot = v.x;
+    out.row0 = v.y;
+    out.nrows = v.z;
     out.shared = 0;
-    return out.nrows > 0 && out.row0 >= 0 && out.row0 + out.nrows <= a.N * g.k;
+    return slot_ok && out.nrows > 0 && out.row0 >= 0 && out.row0 + out.nrows <= a.N * g.k;
   }
   if (a.with_shared && ent == nr) {
     out.slot = g.S;
@@ -424,6 +421,15 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
   // own wait, so it starts streaming at once; everything else waits for the
   // predecessor.  The successor is released only after this wait, so what
   // the successor's producer reads without waiting is final by then.
+  if (warp == kProd && lane == 0) {
+    // descriptor fetches overlap the wait for the predecessor
+    tc::prefetch_tmap(&map0);
+    tc::prefetch_tmap(&map1);
+    if (p.smode) {
+      tc::prefetch_tmap(&smap0);
+      tc::prefetch_tmap(&smap1);
+    }
+  }
   if (PH == 1 || warp != kProd) pdl_wait();
   pdl_trigger();
   const Range rr = cta_range(g, a, p);

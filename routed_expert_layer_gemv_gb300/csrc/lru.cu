@@ -29,27 +29,30 @@ namespace {
 
 constexpr int kLruThreads = 1024;
 
-MOE_DEV int excl_scan_1024(int v, int* total, int* sh) {
+// Exclusive scan of a 64-bit value over the 1024 threads of the CTA (three
+// counters packed in 21-bit fields scan at once); *total gets the sum.
+MOE_DEV unsigned long long excl_scan_u64(unsigned long long v, unsigned long long* total,
+                                         unsigned long long* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
+  unsigned long long inc = v;
   for (int o = 1; o < 32; o <<= 1) {
-    int u = __shfl_up_sync(0xffffffffu, inc, o);
+    const unsigned long long u = __shfl_up_sync(0xffffffffu, inc, o);
     if (lane >= o) inc += u;
   }
   if (lane == 31) sh[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    int s = sh[lane];
-    int si = s;
+    const unsigned long long s = sh[lane];
+    unsigned long long si = s;
     for (int o = 1; o < 32; o <<= 1) {
-      int u = __shfl_up_sync(0xffffffffu, si, o);
+      const unsigned long long u = __shfl_up_sync(0xffffffffu, si, o);
       if (lane >= o) si += u;
     }
     sh[lane] = si - s;
     if (lane == 31) sh[32] = si;
   }
   __syncthreads();
-  int r = sh[warp] + inc - v;
+  const unsigned long long r = sh[warp] + inc - v;
   *total = sh[32];
   __syncthreads();
   return r;
@@ -58,6 +61,7 @@ MOE_DEV int excl_scan_1024(int v, int* total, int* sh) {
 // Shared-memory scratch of one LRU step.
 struct LruSmem {
   int sh[33];
+  unsigned long long sh64[33];
   unsigned long long clk;         // clock, staged
   int so[kMaxE];       // slot_of, staged
   int q[kMaxE];        // victim queue (slots)
@@ -96,24 +100,20 @@ MOE_DEV void lru_park(const LruRegs& r, int E, int S, LruSmem& m) {
 // One step of the table (blockDim.x == 1024) on the state parked in m (the
 // caller synchronises after lru_park).  counts may live in shared or global
 // memory.
-MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of,
+MOE_DEV void lru_body(const int* counts, const int* offs, int E, int S, int X, int* __restrict__ slot_of,
                       int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                       unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
                       unsigned long long* __restrict__ stats, LruSmem& m) {
   const int tid = threadIdx.x;
   const unsigned long long clk = m.clk;
 
-  // hits / misses over experts (E <= 1024: one expert per thread)
+  // hits / misses over experts (E <= 1024: one expert per thread) and the
+  // free / stale slots (S <= E: one slot per thread), counted by one scan of
+  // three packed 21-bit counters
   const int e = tid;
   const bool inU = e < E && counts[e] > 0;
   const int cur = e < E ? m.so[e] : -1;
   const bool hit = inU && cur >= 0, miss = inU && cur < 0;
-  int n_hit, n_miss;
-  const int hr = excl_scan_1024(hit ? 1 : 0, &n_hit, m.sh);
-  const int mr = excl_scan_1024(miss ? 1 : 0, &n_miss, m.sh);
-  const int U = n_hit + n_miss;
-
-  // victim queue over slots (S <= E <= 1024: one slot per thread)
   const int s = tid;
   int old = -1;
   bool fre = false, stale = false;
@@ -125,8 +125,16 @@ MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of
     st = m.st[s];
     m.stale[s] = stale ? 1 : 0;
   }
-  int n_free;
-  const int fr = excl_scan_1024(fre ? 1 : 0, &n_free, m.sh);   // (its barriers also publish m.*)
+  constexpr unsigned long long kF = 0x1FFFFFull;
+  unsigned long long tot;
+  const unsigned long long pre = excl_scan_u64(
+      (hit ? 1ull : 0ull) | (miss ? 1ull << 21 : 0ull) | (fre ? 1ull << 42 : 0ull), &tot, m.sh64);
+  const int hr = (int)(pre & kF), mr = (int)((pre >> 21) & kF), fr = (int)((pre >> 42) & kF);
+  const int n_hit = (int)(tot & kF), n_miss = (int)((tot >> 21) & kF), n_free = (int)((tot >> 42) & kF);
+  const int U = n_hit + n_miss;
+
+  // victim queue Q (its barriers published m.stale): free slots, then stale
+  // slots by ascending stamp; hits keep their slots
   if (fre) { m.q[fr] = s; m.q_old[fr] = -1; }
   if (stale) {
     int r = 0;
@@ -140,29 +148,37 @@ MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of
       m.q_old[n_free + r] = old;
     }
   }
+  if (hit) { m.acc_e[hr] = e; m.acc_s[hr] = cur; }
   __syncthreads();
 
-  // accesses 0 .. min(U, S)-1 first, then the later waves reuse slot(i - S)
-  if (hit) { m.acc_e[hr] = e; m.acc_s[hr] = cur; }
+  // misses of the first wave take Q in order; later waves reuse slot(i - S)
   if (miss) {
     const int i = n_hit + mr;
     m.acc_e[i] = e;
     if (i < S) m.acc_s[i] = m.q[i - n_hit];   // i - n_hit < S - n_hit = |Q|
   }
   __syncthreads();
-  for (int i = S + tid; i < U; i += kLruThreads) m.acc_s[i] = m.acc_s[i % S];
-  __syncthreads();
+  if (U > S) {
+    for (int i = S + tid; i < U; i += kLruThreads) m.acc_s[i] = m.acc_s[i % S];
+    __syncthreads();
+  }
 
   int* r_e = rec_expert(rec);
   int* r_s = rec_slot(rec, E);
   int* r_v = rec_evicted(rec, E);
+  int4* r_n = rec_entry(rec, E);
   for (int i = tid; i < U; i += kLruThreads) {
-    r_e[i] = m.acc_e[i];
-    r_s[i] = m.acc_s[i];
+    const int ex = m.acc_e[i], sl = m.acc_s[i];
+    r_e[i] = ex;
+    r_s[i] = sl;
     int ev = -1;
     if (i >= S) ev = m.acc_e[i - S];
     else if (i >= n_hit) ev = m.q_old[i - n_hit];
     r_v[i] = ev;
+    // physical slot: the LRU slot, or staging slot S + 1 + (i - S) for later waves
+    const bool ok = ex >= 0 && ex < E && sl >= 0 && sl < S && i - S < X;
+    const int ps = !ok ? -1 : i < S ? sl : S + 1 + (i - S);
+    r_n[i] = make_int4(ps, offs && ok ? offs[ex] : 0, offs && ok ? counts[ex] : 0, ex);
   }
   if (tid == 0) {
     rec->U = U;
@@ -170,12 +186,12 @@ MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of
     rec->n_miss = n_miss;
     rec->S = S;
   }
-  // table update: experts pushed out of Q lose their slot
+  // table update: experts pushed out of Q lose their slot (they are not in
+  // U, so these writes never meet the assignments below)
   for (int i = n_hit + tid; i < min(U, S); i += kLruThreads) {
     const int ev = m.q_old[i - n_hit];
     if (ev >= 0 && ev < E) slot_of[ev] = -1;
   }
-  __syncthreads();
   for (int i = tid; i < U; i += kLruThreads) {
     const int ex = m.acc_e[i], sl = m.acc_s[i];
     if (sl < 0 || sl >= S) continue;   // only a corrupted table gets here
@@ -199,20 +215,20 @@ MOE_DEV void lru_body(const int* counts, int E, int S, int* __restrict__ slot_of
 }
 
 __global__ void __launch_bounds__(kLruThreads)
-lru_step_kernel(const int* __restrict__ counts, int E, int S, int* __restrict__ slot_of,
-                int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
+lru_step_kernel(const int* __restrict__ counts, const int* __restrict__ offsets, int E, int S, int X,
+                int* __restrict__ slot_of, int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                 unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
                 unsigned long long* __restrict__ stats) {
   __shared__ LruSmem m;
   lru_park(lru_load(E, S, slot_of, expert_of, stamp, clock), E, S, m);
   __syncthreads();
-  lru_body(counts, E, S, slot_of, expert_of, stamp, clock, rec, stats, m);
+  lru_body(counts, offsets, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, m);
 }
 
 // Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
 // (as perm_single in permute.cu), then the LRU step on the counts it found.
 __global__ void __launch_bounds__(kLruThreads)
-route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int* __restrict__ counts,
+route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X, int* __restrict__ counts,
                   int* __restrict__ offsets, int* __restrict__ row_of, int* __restrict__ tok_of,
                   int* __restrict__ slot_of, int* __restrict__ expert_of,
                   unsigned long long* __restrict__ stamp, unsigned long long* __restrict__ clock,
@@ -223,6 +239,7 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int* 
   int* cnt = reinterpret_cast<int*>(cm + E * perm::kPermWarps);  // [E]
   int* off = cnt + E;                                            // [E]
   int* rows = off + E;                                           // [128][k]
+  uint32_t* tb = reinterpret_cast<uint32_t*>(rows + perm::kTokPerBlock * k);   // [128][ceil(E/32)]
   // the table was last written by the previous step's tail, which finished
   // before the router began: its loads go out before waiting for the router
   pdl_trigger();
@@ -231,8 +248,7 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int* 
   perm::stage_rows(idx, N, k, 0, rows);
   lru_park(lr, E, S, m);
   __syncthreads();
-  if (threadIdx.x < perm::kTokPerBlock) perm::build_ballots(rows, k, E, cm);
-  __syncthreads();
+  perm::build_ballots_par(rows, k, E, N, tb, cm);
   const int e = threadIdx.x;
   const int c = e < E ? perm::block_count(cm, e) : 0;
   int tot;
@@ -255,7 +271,7 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int* 
     }
   }
   __syncthreads();
-  lru_body(cnt, E, S, slot_of, expert_of, stamp, clock, rec, stats, m);
+  lru_body(cnt, off, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, m);
 }
 
 __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expert_of,
@@ -282,11 +298,11 @@ __global__ void counts_from_list_kernel(const int* __restrict__ list, int n, int
 
 }  // namespace
 
-cudaError_t launch_lru_step(const Geo& g, const int* counts, int* slot_of, int* expert_of,
-                            unsigned long long* stamp, unsigned long long* clock,
+cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets, int* slot_of,
+                            int* expert_of, unsigned long long* stamp, unsigned long long* clock,
                             StepRecord* rec, unsigned long long* stats, cudaStream_t st) {
-  lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, g.E, g.S, slot_of, expert_of, stamp, clock,
-                                             rec, stats);
+  lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, offsets, g.E, g.S, g.X, slot_of, expert_of, stamp,
+                                             clock, rec, stats);
   return cudaGetLastError();
 }
 
@@ -295,7 +311,7 @@ cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, 
                               unsigned long long* stamp, unsigned long long* clock,
                               StepRecord* rec, unsigned long long* stats, cudaStream_t st) {
   const size_t smem = (size_t)g.E * perm::kPermWarps * 4 + (size_t)2 * g.E * 4 +
-                      (size_t)perm::kTokPerBlock * g.k * 4;
+                      (size_t)perm::kTokPerBlock * g.k * 4 + (size_t)perm::kTokPerBlock * ((g.E + 31) / 32) * 4;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(route_tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -303,7 +319,7 @@ cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, counts,
+  return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, g.X, counts,
                     offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, rec, stats);
 }
 

@@ -42,6 +42,33 @@ MOE_DEV void build_ballots(const int* rows, int k, int E, uint32_t* cm) {
   }
 }
 
+// The same ballots built by a whole CTA (any blockDim) without a loop over
+// the experts: each token's expert set becomes a bitmap tb[t][E/32] (one
+// thread per token word, k compares), then thread (e, w) gathers bit e of
+// warp w's tokens.  nt = tokens of the block (<= 128); tb: 128 * ceil(E/32)
+// words of scratch.  Ends with the CTA synchronised.
+MOE_DEV void build_ballots_par(const int* rows, int k, int E, int nt, uint32_t* tb, uint32_t* cm) {
+  const int W = (E + 31) >> 5;
+  for (int v = threadIdx.x; v < nt * W; v += blockDim.x) {
+    const int t = v / W, wd = v % W;
+    uint32_t b = 0;
+    for (int j = 0; j < k; ++j) {
+      const int e = rows[t * k + j];
+      if ((e >> 5) == wd) b |= 1u << (e & 31);
+    }
+    tb[t * W + wd] = b;
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < E * kPermWarps; v += blockDim.x) {
+    const int e = v % E, w = v / E;   // consecutive threads: consecutive experts, one broadcast word
+    const int l1 = min(32, nt - 32 * w);
+    uint32_t b = 0;
+    for (int l = 0; l < l1; ++l) b |= ((tb[(32 * w + l) * W + (e >> 5)] >> (e & 31)) & 1u) << l;
+    cm[e * kPermWarps + w] = b;
+  }
+  __syncthreads();
+}
+
 // Rank of this thread's token among the block's earlier tokens routed to e
 // (thread t of the first 128 = token t of the block).
 MOE_DEV int rank_in_block(const uint32_t* cm, int e) {
