@@ -780,7 +780,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     }
   }
   pe = prof_begin(L, MOE_PROF_COMBINE, st);
-  MOE_CUDA(L, launch_combine(g, L->O, L->gates, L->row_of, N, yd, st));
+  MOE_CUDA(L, launch_combine(g, L->O, prefill, L->gates, L->row_of, N, yd, st));
   prof_end(pe, st);
   L->launches += 1;
   if (!y_dev) {

@@ -195,7 +195,15 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
 cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int max_staged, uint8_t* slots,
                                 cudaStream_t st);
 // combine.cu
-cudaError_t launch_combine(const Geo& g, const float* O, const float* gates, const int* row_of,
+// The prefill GEMM writes O as f16 rows [rows][d] in the first half of the
+// O buffer, each row's 128-column blocks scaled by 2^-s; the exponents s
+// (int8, [rows][d / 128]) follow the f16 rows.
+inline int8_t* prefill_o_exp(const Geo& g, const float* O, int N) {
+  const size_t rows = (size_t)N * g.k + (g.has_shared ? N : 0);
+  return reinterpret_cast<int8_t*>(const_cast<float*>(O)) + rows * g.d * 2;
+}
+// O: fp32 rows, or (o_f16) the prefill GEMM's scaled f16 rows
+cudaError_t launch_combine(const Geo& g, const float* O, bool o_f16, const float* gates, const int* row_of,
                            int N, __nv_bfloat16* y, cudaStream_t st);
 // debug.cu
 cudaError_t launch_dequant(const Geo& g, const uint8_t* expert, int m, float* out, cudaStream_t st);

@@ -166,7 +166,8 @@ struct GemmArgs {
   uint8_t* h_scales;
   float act_scale_h;
   // phase 2 output
-  float* O;
+  float* O;                    // phase 2: f16 rows [rows][O_ld] (the buffer's first half)
+  int8_t* O_exp;               // phase 2: power-of-two exponent per row and 128-column block
   int O_ld;
 };
 
@@ -194,8 +195,8 @@ constexpr int kSfBase = 256;            // TMEM columns 0..255: two 128-column a
 // time), rows padded by 4 floats so the row writes and reads spread over the
 // banks.
 template <int PH> constexpr int ws_stages() { return PH == 1 ? 6 : 5; }
-constexpr int kOStride = 68;
-constexpr size_t kOStage = 4 * 32 * kOStride * 4;
+constexpr int kOStrideB = 72;   // f16 elements per staged O row (144 bytes: conflict-free 16-byte stores)
+constexpr size_t kOStage = 4 * 32 * kOStrideB * 2;
 
 template <int PH>
 size_t ws_smem() { return 1024 + (size_t)ws_stages<PH>() * 2 * kOpBytes + (PH == 2 ? kOStage : 0); }
@@ -437,12 +438,31 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
           }
         }
       } else {
-        // lane = row in TMEM; go through shared memory, half a tile at a
-        // time, so that each store instruction writes 256 contiguous bytes
+        // lane = row in TMEM; O is written as f16 scaled by 2^-s, s per row
+        // and 128-column block (max |O| * 2^-s in [2^14, 2^15), so nothing
+        // overflows and the rounding is relative to the block's largest
+        // value); the combine multiplies by 2^s and accumulates in fp32.
+        // Rows go through shared memory, half a tile at a time, so that each
+        // store instruction writes four whole 128-byte row pieces
         const float sd = FMT == MOE_MXFP4 ? 1.0f : ts[2] * p.act_scale;
-        float* ost = reinterpret_cast<float*>(smem + (size_t)kWsStages * 2 * kOpBytes) +
-                     (size_t)(warp - 6) * 32 * kOStride;
-        float4* myrow = reinterpret_cast<float4*>(ost + lane * kOStride);
+        __half* Oh = reinterpret_cast<__half*>(p.O);
+        float mx = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < 32; ++i2)
+          mx = fmaxf(fmaxf(fmaxf(mx, fabsf(__uint_as_float(v0[i2]))), fabsf(__uint_as_float(v1[i2]))),
+                     fmaxf(fabsf(__uint_as_float(v2[i2])), fabsf(__uint_as_float(v3[i2]))));
+        mx *= fabsf(sd);
+        int se = 0;
+        if (mx > 0.f && mx < 3.0e38f) {
+          int ex;
+          frexpf(mx, &ex);
+          se = max(-100, min(100, ex - 15));
+        }
+        const float sc = sd * __int_as_float((127 - se) << 23);   // sd * 2^-se
+        if (live) p.O_exp[(size_t)r * (p.O_ld / 128) + n0 / 128] = (int8_t)se;
+        __half* ost = reinterpret_cast<__half*>(smem + (size_t)kWsStages * 2 * kOpBytes) +
+                      (size_t)(warp - 6) * 32 * kOStrideB;
+        uint4* myrow = reinterpret_cast<uint4*>(ost + lane * kOStrideB);
         const int row0 = tile.row_start + 32 * (warp & 3);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -450,17 +470,24 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
           for (int c = 0; c < 2; ++c) {
             const uint32_t* vv = hf == 0 ? (c == 0 ? v0 : v1) : (c == 0 ? v2 : v3);
 #pragma unroll
-            for (int i2 = 0; i2 < 8; ++i2)
-              myrow[8 * c + i2] = make_float4(__uint_as_float(vv[4 * i2]) * sd, __uint_as_float(vv[4 * i2 + 1]) * sd,
-                                              __uint_as_float(vv[4 * i2 + 2]) * sd, __uint_as_float(vv[4 * i2 + 3]) * sd);
+            for (int i2 = 0; i2 < 4; ++i2) {
+              uint32_t w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const __half2 h2 = __floats2half2_rn(__uint_as_float(vv[8 * i2 + 2 * j]) * sc,
+                                                     __uint_as_float(vv[8 * i2 + 2 * j + 1]) * sc);
+                w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              myrow[4 * c + i2] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
           __syncwarp();
-          // two rows per instruction: lanes 0-15 row rr, lanes 16-31 row rr + 1
-          for (int rr = 0; rr < 32; rr += 2) {
-            const int rw = rr + (lane >> 4), rg = row0 + rw;
+          // four rows per instruction: lanes 8j .. 8j + 7 take row rr + j
+          for (int rr = 0; rr < 32; rr += 4) {
+            const int rw = rr + (lane >> 3), rg = row0 + rw;
             if (rg < tile.row_end)
-              reinterpret_cast<float4*>(p.O + (size_t)rg * p.O_ld + n0 + 64 * hf)[lane & 15] =
-                  reinterpret_cast<const float4*>(ost + rw * kOStride)[lane & 15];
+              reinterpret_cast<uint4*>(Oh + (size_t)rg * p.O_ld + n0 + 64 * hf)[lane & 7] =
+                  reinterpret_cast<const uint4*>(ost + rw * kOStrideB)[lane & 7];
           }
           __syncwarp();
         }
@@ -620,6 +647,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.act_scale = g.fmt == MOE_MXFP4 ? 1.0f : gh;
   p.O = O;
   p.O_ld = g.d;
+  p.O_exp = prefill_o_exp(g, O, N);
   const int grid2 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.d / kTileRows));
   if (ev) cudaEventRecord(ev[2], st);
   if (g.fmt == MOE_MXFP4)
