@@ -33,7 +33,9 @@
 
 using namespace moe;
 
-constexpr int kFillStreams = 4;
+constexpr int kFillStreams = 1;   // one copy queue: more add no bandwidth on the host link
+constexpr int kMissChunks = 4;   // memcpy fills: the misses' expert FFN runs in up to this many chunks
+constexpr int kMissesPerChunk = 8;   // ... of at least this many misses each
 
 struct moe_layer {
   moe_layer_desc desc{};
@@ -88,8 +90,8 @@ struct moe_layer {
   size_t host_pool_bytes = 0;
   bool router_set = false;
   bool shared_set = false;
-  cudaStream_t fill[kFillStreams] = {};       // miss fills, round robin
-  cudaEvent_t ev_fills[kFillStreams] = {};
+  cudaStream_t fill[kFillStreams] = {};       // miss fills and the step record's copy to the host
+  cudaEvent_t ev_chunk[kMissChunks] = {};     // the fills of each miss chunk have landed
   cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_rec = nullptr;
   int fill_mode = MOE_FILL_MEMCPY;
   const uint8_t* pool_dev = nullptr;          // device address of the host pool
@@ -212,10 +214,12 @@ void release(moe_layer* L) {
   L->gplan = nullptr;
   if (L->ev_route) cudaEventDestroy(L->ev_route);
   if (L->ev_fill) cudaEventDestroy(L->ev_fill);
+  for (int i = 0; i < kMissChunks; ++i) {
+    if (L->ev_chunk[i]) cudaEventDestroy(L->ev_chunk[i]);
+    L->ev_chunk[i] = nullptr;
+  }
   for (int i = 0; i < kFillStreams; ++i) {
-    if (L->ev_fills[i]) cudaEventDestroy(L->ev_fills[i]);
     if (L->fill[i]) cudaStreamDestroy(L->fill[i]);
-    L->ev_fills[i] = nullptr;
     L->fill[i] = nullptr;
   }
   if (L->ev_rec) cudaEventDestroy(L->ev_rec);
@@ -403,8 +407,9 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     L->rec_host = static_cast<StepRecord*>(L->pinned_rec);
     bool sok = true;
     for (int i = 0; i < kFillStreams; ++i)
-      sok = sok && cudaStreamCreateWithFlags(&L->fill[i], cudaStreamNonBlocking) == cudaSuccess &&
-            cudaEventCreateWithFlags(&L->ev_fills[i], cudaEventDisableTiming) == cudaSuccess;
+      sok = sok && cudaStreamCreateWithFlags(&L->fill[i], cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; i < kMissChunks; ++i)
+      sok = sok && cudaEventCreateWithFlags(&L->ev_chunk[i], cudaEventDisableTiming) == cudaSuccess;
     if (!sok ||
         cudaEventCreateWithFlags(&L->ev_route, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
@@ -671,6 +676,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   a.tok_of = L->tok_of;
   a.N = N;
   a.mode = kRangeHits;
+  a.chunk = 0;
+  a.n_chunks = 1;
   a.with_shared = g.has_shared;
   a.err = L->err_dev;
   a.hmax = L->hmax;
@@ -715,7 +722,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   // expert-FFN launch then covers all misses, and the staged experts that
   // keep their LRU slot are committed into it on the caller stream.
   size_t fill_bytes = 0;
-  int U = -1, n_hit = -1, n_miss = 0, waves = 1;
+  int U = -1, n_hit = -1, n_miss = 0, waves = 1, n_chunks = 0;
   const int max_miss = std::min(g.E, N * g.k);
   const int max_staged = std::max(0, max_miss - g.S);
   bool any_miss = true, any_staged = max_staged > 0;
@@ -746,32 +753,53 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     any_miss = n_hit < U;
     any_staged = U > g.S;
     if (any_miss) {
-      const int nfs = std::min(kFillStreams, U - n_hit);
-      for (int j = 0; j < nfs; ++j) MOE_CUDA(L, cudaStreamWaitEvent(L->fill[j], L->ev_route, 0));
-      cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, L->fill[0]);
-      for (int i = n_hit; i < U; ++i) {
-        cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)access_slot(as, g.S, i) * g.ebytes,
-                                         L->host_pool + (size_t)ae[i] * g.ebytes, g.ebytes,
-                                         cudaMemcpyHostToDevice, L->fill[(i - n_hit) % kFillStreams]);
-        if (ce != cudaSuccess) return fail(L, MOE_ERR_FILL, "fill of expert %d: %s", ae[i], cudaGetErrorString(ce));
-        fill_bytes += g.ebytes;
+      // One copy engine queue in access order (more queues add no bandwidth
+      // on this link): consecutive experts bound for consecutive slots go as
+      // one copy, and each chunk of the misses records when its copies have
+      // landed, so its expert FFN starts while later fills still run.
+      // a chunk pays one expert-FFN launch ramp, so only long miss lists are cut
+      n_chunks = std::max(1, std::min(kMissChunks, (U - n_hit) / kMissesPerChunk));
+      cudaStream_t fs = L->fill[0];
+      MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
+      cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
+      const int nm = U - n_hit;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int c0 = n_hit + (int)((long long)nm * c / n_chunks), c1 = n_hit + (int)((long long)nm * (c + 1) / n_chunks);
+        for (int i = c0; i < c1;) {
+          int j = i + 1;
+          while (j < c1 && ae[j] == ae[j - 1] + 1 && access_slot(as, g.S, j) == access_slot(as, g.S, j - 1) + 1) ++j;
+          cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)access_slot(as, g.S, i) * g.ebytes,
+                                           L->host_pool + (size_t)ae[i] * g.ebytes, (size_t)(j - i) * g.ebytes,
+                                           cudaMemcpyHostToDevice, fs);
+          if (ce != cudaSuccess) return fail(L, MOE_ERR_FILL, "fill of expert %d: %s", ae[i], cudaGetErrorString(ce));
+          fill_bytes += (size_t)(j - i) * g.ebytes;
+          i = j;
+        }
+        MOE_CUDA(L, cudaEventRecord(L->ev_chunk[c], fs));
       }
-      // the timing bracket on stream 0 covers every fill: stream 0 waits for the others
-      for (int j = 1; j < nfs; ++j) {
-        MOE_CUDA(L, cudaEventRecord(L->ev_fills[j], L->fill[j]));
-        MOE_CUDA(L, cudaStreamWaitEvent(L->fill[0], L->ev_fills[j], 0));
-      }
-      prof_end(pf, L->fill[0]);
-      MOE_CUDA(L, cudaEventRecord(L->ev_fill, L->fill[0]));
-      MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
+      prof_end(pf, fs);
     }
     mirror_apply(L, r);
   }
   if (!resident && any_miss) {
     a.mode = kRangeMisses;
     a.with_shared = 0;
-    grc = gemv(max_miss);
-    if (grc) return grc;
+    if (n_chunks > 1 && !prefill) {
+      // memcpy fills: chunk c of the misses runs once its own copies landed
+      const int nm = U - n_hit;
+      a.n_chunks = n_chunks;
+      for (int c = 0; c < n_chunks; ++c) {
+        MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[c], 0));
+        a.chunk = c;
+        grc = gemv((int)((long long)nm * (c + 1) / n_chunks - (long long)nm * c / n_chunks));
+        if (grc) return grc;
+      }
+    } else {
+      // one launch over every miss once the last copy (one queue, in order) has landed
+      if (n_chunks > 0) MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[n_chunks - 1], 0));
+      grc = gemv(max_miss);
+      if (grc) return grc;
+    }
     if (any_staged) {
       pe = prof_begin(L, MOE_PROF_COMMIT, st);
       MOE_CUDA(L, launch_stage_commit(g, L->rec, max_staged, L->slots, st));

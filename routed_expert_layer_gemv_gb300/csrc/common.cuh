@@ -154,6 +154,7 @@ struct GemvArgs {
   const int* tok_of;           // [N*k]
   int N;
   int mode;                    // RangeMode
+  int chunk, n_chunks;         // kRangeMisses: the misses split in n_chunks equal runs, this launch takes one
   int with_shared;             // also run the shared expert (rows N*k .. N*k+N)
   int* err;                    // set to 1 when a bounded wait gives up
   float* hmax;                 // [rows][2][d_ff / 64]: max |W_g x|, |W_u x| per 64 columns

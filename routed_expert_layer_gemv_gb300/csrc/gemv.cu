@@ -138,7 +138,13 @@ MOE_DEV int count_entries(const Geo& g, const GemvArgs& a, int* base, int* nr) {
   const StepRecord* rec = a.rec;
   const int U = min(max(rec->U, 0), g.E), nh = min(max(rec->n_hit, 0), U), S = g.S;
   (void)S;
-  const int b = a.mode == kRangeHits ? 0 : nh, e = a.mode == kRangeHits ? nh : U;
+  int b = 0, e = nh;
+  if (a.mode != kRangeHits) {
+    // misses [nh, U), or chunk `chunk` of n_chunks equal runs of them
+    const int C = max(a.n_chunks, 1), c = min(max(a.chunk, 0), C - 1), nm = U - nh;
+    b = nh + (int)((long long)nm * c / C);
+    e = nh + (int)((long long)nm * (c + 1) / C);
+  }
   *base = b;
   *nr = max(0, e - b);
   return *nr + (a.with_shared ? 1 : 0);
