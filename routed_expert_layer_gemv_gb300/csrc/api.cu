@@ -24,6 +24,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <chrono>
 #include <cstring>
 #include <new>
 #include <string>
@@ -66,6 +67,8 @@ struct moe_layer {
   void* perm_scratch = nullptr;
   StepRecord* rec = nullptr;
   StepRecord* rec_host = nullptr;
+  StepRecord* rec_host_dev = nullptr;         // rec_host as the device sees it (mapped)
+  unsigned long long step_seq = 0;            // sequence number of the last polled record
   float* h = nullptr;
   float* hmax = nullptr;          // decode: per-row maxima of phase 1 per 64 columns
   float* O = nullptr;
@@ -92,7 +95,7 @@ struct moe_layer {
   bool shared_set = false;
   cudaStream_t fill[kFillStreams] = {};       // miss fills and the step record's copy to the host
   cudaEvent_t ev_chunk[kMissChunks] = {};     // the fills of each miss chunk have landed
-  cudaEvent_t ev_route = nullptr, ev_fill = nullptr, ev_rec = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_fill = nullptr;
   int fill_mode = MOE_FILL_MEMCPY;
   const uint8_t* pool_dev = nullptr;          // device address of the host pool
   unsigned long long* stats = nullptr;        // steps, distinct, hits, misses
@@ -222,8 +225,7 @@ void release(moe_layer* L) {
     if (L->fill[i]) cudaStreamDestroy(L->fill[i]);
     L->fill[i] = nullptr;
   }
-  if (L->ev_rec) cudaEventDestroy(L->ev_rec);
-  L->ev_route = L->ev_fill = L->ev_rec = nullptr;
+  L->ev_route = L->ev_fill = nullptr;
 }
 
 int pointer_kind(const void* p, bool* on_device, int device) {
@@ -399,12 +401,21 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
       L->plan = nullptr;   // prefill regime unavailable (tensor-map encoding failed)
     }
   }
-  if (rc == MOE_OK && cudaHostAlloc(&L->pinned_rec, rec_bytes(g.E), cudaHostAllocDefault) != cudaSuccess) {
+  if (rc == MOE_OK && cudaHostAlloc(&L->pinned_rec, rec_bytes(g.E), cudaHostAllocMapped) != cudaSuccess) {
     cudaGetLastError();
     rc = MOE_ERR_OOM;
   }
   if (rc == MOE_OK) {
     L->rec_host = static_cast<StepRecord*>(L->pinned_rec);
+    std::memset(L->pinned_rec, 0, rec_bytes(g.E));
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, L->pinned_rec, 0) != cudaSuccess) {
+      cudaGetLastError();
+      rc = MOE_ERR_CUDA;
+    }
+    L->rec_host_dev = static_cast<StepRecord*>(dp);
+  }
+  if (rc == MOE_OK) {
     bool sok = true;
     for (int i = 0; i < kFillStreams; ++i)
       sok = sok && cudaStreamCreateWithFlags(&L->fill[i], cudaStreamNonBlocking) == cudaSuccess;
@@ -412,8 +423,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
       sok = sok && cudaEventCreateWithFlags(&L->ev_chunk[i], cudaEventDisableTiming) == cudaSuccess;
     if (!sok ||
         cudaEventCreateWithFlags(&L->ev_route, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&L->ev_rec, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       rc = MOE_ERR_CUDA;
     }
@@ -557,7 +567,7 @@ int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, in
   if (n > 0) MOE_CUDA(L, cudaMemcpyAsync(L->list_dev, experts, (size_t)n * 4, cudaMemcpyHostToDevice, st));
   MOE_CUDA(L, launch_counts_from_list(g, L->list_dev, n, L->counts, st));
   MOE_CUDA(L, launch_lru_step(g, L->counts, nullptr, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec,
-                              nullptr, st));
+                              nullptr, nullptr, 0, st));
   MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
   MOE_CUDA(L, cudaStreamSynchronize(st));
   const StepRecord* r = L->rec_host;
@@ -586,6 +596,31 @@ int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, in
   }
   if (n_miss_out) *n_miss_out = r->n_miss;
   return MOE_OK;
+}
+
+// Wait for the LRU kernel's host copy of step `seq` (bounded).  Fails on an
+// error of the routing launches or when the record is not there well after
+// they finished.
+static int poll_record(moe_layer_t L, unsigned long long seq) {
+  using clk = std::chrono::steady_clock;
+  const clk::time_point t0 = clk::now();
+  clk::time_point done_at{};
+  bool done = false;
+  for (unsigned it = 1;; ++it) {
+    if (__atomic_load_n(&L->rec_host->seq, __ATOMIC_ACQUIRE) == seq) return MOE_OK;
+    if ((it & 255) == 0) {
+      const cudaError_t q = cudaEventQuery(L->ev_route);
+      if (q != cudaSuccess && q != cudaErrorNotReady) return cuda_fail(L, q, "routing");
+      if (q == cudaSuccess && !done) {
+        done = true;
+        done_at = clk::now();
+      }
+      if (done && clk::now() - done_at > std::chrono::milliseconds(200))
+        return fail(L, MOE_ERR_STATE, "the routing finished but step record %llu never reached the host", seq);
+      if (clk::now() - t0 > std::chrono::seconds(30))
+        return fail(L, MOE_ERR_TIMEOUT, "step record %llu did not arrive within 30 s", seq);
+    }
+  }
 }
 
 int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int regime,
@@ -637,12 +672,17 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
                             L->gates, L->xexp, L->rcounter, st));
   prof_end(pe, st);
   L->launches += N <= 64 ? 1 : 2;
+  // memcpy fills: the LRU kernel also writes the step record into mapped
+  // pinned host memory, sequence number last, and the host polls it
+  const bool host_poll = !resident && L->fill_mode != MOE_FILL_DEVICE;
+  StepRecord* hrec = host_poll ? L->rec_host_dev : nullptr;
+  const unsigned long long seq = host_poll ? ++L->step_seq : 0ull;
   if (N <= 128) {
     // permutation and LRU step in one CTA
     pe = prof_begin(L, MOE_PROF_PERMUTE, st);
     MOE_CUDA(L, launch_route_tail(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
                                   L->slot_of, L->expert_of, L->stamp, L->clock, L->rec, L->stats,
-                                  st));
+                                  hrec, seq, st));
     prof_end(pe, st);
     L->launches += 1;
   } else {
@@ -653,21 +693,12 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     L->launches += 3;
     pe = prof_begin(L, MOE_PROF_LRU, st);
     MOE_CUDA(L, launch_lru_step(g, L->counts, L->offsets, L->slot_of, L->expert_of, L->stamp, L->clock,
-                                L->rec, L->stats, st));
+                                L->rec, L->stats, hrec, seq, st));
     prof_end(pe, st);
     L->launches += 1;
   }
   const bool dev_fill = !resident && L->fill_mode == MOE_FILL_DEVICE;
-  if (!resident) {
-    MOE_CUDA(L, cudaEventRecord(L->ev_route, st));
-    if (!dev_fill) {
-      // the record goes to the host from a side stream, so the caller stream
-      // runs routing -> expert FFN kernel to kernel
-      MOE_CUDA(L, cudaStreamWaitEvent(L->fill[0], L->ev_route, 0));
-      MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, L->fill[0]));
-      MOE_CUDA(L, cudaEventRecord(L->ev_rec, L->fill[0]));
-    }
-  }
+  if (!resident) MOE_CUDA(L, cudaEventRecord(L->ev_route, st));
   GemvArgs a{};
   a.slots = L->slots;
   a.shared_w = L->shared_w;
@@ -737,7 +768,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
     waves = (max_miss + g.S - 1) / g.S;
   } else if (!resident) {
-    MOE_CUDA(L, cudaEventSynchronize(L->ev_rec));
+    int prc = poll_record(L, seq);
+    if (prc) return prc;
     const StepRecord* r = L->rec_host;
     U = r->U;
     n_hit = r->n_hit;

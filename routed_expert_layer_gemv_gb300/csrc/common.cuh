@@ -74,7 +74,8 @@ struct StepRecord {
   int n_hit;
   int n_miss;
   int S;        // slots (wave length)
-  int pad[4];
+  unsigned long long seq;   // host copy only: step number, written last
+  int pad[2];
   // followed by int acc_expert[E], acc_slot[E], acc_evicted[E]
 };
 __host__ __device__ inline int* rec_expert(StepRecord* r) { return reinterpret_cast<int*>(r + 1); }
@@ -132,9 +133,12 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
 // stats (may be null): steps, distinct experts, hits, misses, accumulated
 // offsets (may be null: entries then get no rows) = the permutation's
 // expert row offsets, for the record's entry table
+// host_rec (may be null): mapped pinned copy of the record, written by the
+// kernel itself, seq last, so the host can poll it instead of a copy + event
 cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets, int* slot_of,
                             int* expert_of, unsigned long long* stamp, unsigned long long* clock,
-                            StepRecord* rec, unsigned long long* stats, cudaStream_t st);
+                            StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                            unsigned long long seq, cudaStream_t st);
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
                                unsigned long long* stamp, unsigned long long* clock,
                                cudaStream_t st);
@@ -142,7 +146,8 @@ cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of,
 cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, int* offsets,
                               int* row_of, int* tok_of, int* slot_of, int* expert_of,
                               unsigned long long* stamp, unsigned long long* clock,
-                              StepRecord* rec, unsigned long long* stats, cudaStream_t st);
+                              StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                              unsigned long long seq, cudaStream_t st);
 cudaError_t launch_counts_from_list(const Geo& g, const int* experts, int n, int* counts,
                                     cudaStream_t st);
 // gemv.cu

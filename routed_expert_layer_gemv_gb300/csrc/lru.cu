@@ -103,7 +103,8 @@ MOE_DEV void lru_park(const LruRegs& r, int E, int S, LruSmem& m) {
 MOE_DEV void lru_body(const int* counts, const int* offs, int E, int S, int X, int* __restrict__ slot_of,
                       int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                       unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
-                      unsigned long long* __restrict__ stats, LruSmem& m) {
+                      unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq,
+                      LruSmem& m) {
   const int tid = threadIdx.x;
   const unsigned long long clk = m.clk;
 
@@ -179,6 +180,26 @@ MOE_DEV void lru_body(const int* counts, const int* offs, int E, int S, int X, i
     const bool ok = ex >= 0 && ex < E && sl >= 0 && sl < S && i - S < X;
     const int ps = !ok ? -1 : i < S ? sl : S + 1 + (i - S);
     r_n[i] = make_int4(ps, offs && ok ? offs[ex] : 0, offs && ok ? counts[ex] : 0, ex);
+    if (host_rec) {
+      rec_expert(host_rec)[i] = ex;
+      rec_slot(host_rec, E)[i] = sl;
+      rec_evicted(host_rec, E)[i] = ev;
+    }
+  }
+  if (host_rec) {
+    // the host polls seq: every writer's stores reach the system before it
+    if (tid == 0) {
+      host_rec->U = U;
+      host_rec->n_hit = n_hit;
+      host_rec->n_miss = n_miss;
+      host_rec->S = S;
+    }
+    __threadfence_system();
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence_system();
+      *reinterpret_cast<volatile unsigned long long*>(&host_rec->seq) = seq;
+    }
   }
   if (tid == 0) {
     rec->U = U;
@@ -218,11 +239,11 @@ __global__ void __launch_bounds__(kLruThreads)
 lru_step_kernel(const int* __restrict__ counts, const int* __restrict__ offsets, int E, int S, int X,
                 int* __restrict__ slot_of, int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                 unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
-                unsigned long long* __restrict__ stats) {
+                unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq) {
   __shared__ LruSmem m;
   lru_park(lru_load(E, S, slot_of, expert_of, stamp, clock), E, S, m);
   __syncthreads();
-  lru_body(counts, offsets, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, m);
+  lru_body(counts, offsets, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
 }
 
 // Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
@@ -232,7 +253,8 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
                   int* __restrict__ offsets, int* __restrict__ row_of, int* __restrict__ tok_of,
                   int* __restrict__ slot_of, int* __restrict__ expert_of,
                   unsigned long long* __restrict__ stamp, unsigned long long* __restrict__ clock,
-                  StepRecord* __restrict__ rec, unsigned long long* __restrict__ stats) {
+                  StepRecord* __restrict__ rec, unsigned long long* __restrict__ stats, StepRecord* host_rec,
+                  unsigned long long seq) {
   __shared__ LruSmem m;
   extern __shared__ uint32_t dsm[];
   uint32_t* cm = dsm;                                            // [E][4]
@@ -271,7 +293,7 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
     }
   }
   __syncthreads();
-  lru_body(cnt, off, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, m);
+  lru_body(cnt, off, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
 }
 
 __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expert_of,
@@ -300,16 +322,18 @@ __global__ void counts_from_list_kernel(const int* __restrict__ list, int n, int
 
 cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets, int* slot_of,
                             int* expert_of, unsigned long long* stamp, unsigned long long* clock,
-                            StepRecord* rec, unsigned long long* stats, cudaStream_t st) {
+                            StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                            unsigned long long seq, cudaStream_t st) {
   lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, offsets, g.E, g.S, g.X, slot_of, expert_of, stamp,
-                                             clock, rec, stats);
+                                             clock, rec, stats, host_rec, seq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, int* offsets,
                               int* row_of, int* tok_of, int* slot_of, int* expert_of,
                               unsigned long long* stamp, unsigned long long* clock,
-                              StepRecord* rec, unsigned long long* stats, cudaStream_t st) {
+                              StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                              unsigned long long seq, cudaStream_t st) {
   const size_t smem = (size_t)g.E * perm::kPermWarps * 4 + (size_t)2 * g.E * 4 +
                       (size_t)perm::kTokPerBlock * g.k * 4 + (size_t)perm::kTokPerBlock * ((g.E + 31) / 32) * 4;
   static bool attr = false;
@@ -320,7 +344,7 @@ cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, 
     attr = true;
   }
   return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, g.X, counts,
-                    offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, rec, stats);
+                    offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq);
 }
 
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
