@@ -116,7 +116,7 @@ typedef struct {
 int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out);
 
 /* Create a layer on the current device: validates the descriptor, allocates
- * the slot pool, table and workspaces, creates the fill streams.  The cache
+ * the slot pool, table and workspaces, creates the fill stream.  The cache
  * starts empty (every slot free).  MOE_ERR_ARG on an invalid descriptor,
  * MOE_ERR_UNSUPPORTED when d_model or d_ff exceeds 8192 (the decode kernels
  * stage one token group's activations in shared memory), MOE_ERR_OOM when
@@ -173,8 +173,10 @@ int moe_lru_set_state(moe_layer_t layer, const int* expert_of_slot,
  * through the layer's workspace, and the call returns after y is written).
  * N == 0 is a no-op; 0 < N <= max_tokens.  With misses (possible unless
  * every expert is resident) the call waits on the host for the step's routing
- * (one small device->host copy) and then issues the slot fills on the
- * layer's fill streams; otherwise it returns without waiting.  Misses beyond
+ * record, which the LRU kernel writes into mapped pinned memory (polled,
+ * bounded: MOE_ERR_STATE if the routing finished and no record arrived,
+ * MOE_ERR_TIMEOUT after 30 s), and then issues the slot fills on the layer's
+ * fill stream; otherwise it returns without waiting.  Misses beyond
  * the first n_slots accesses of a step are filled into staging slots at once
  * and copied into their LRU slots after the step's expert FFN, so the cache
  * state after the call is the LRU's either way.  regime:
@@ -183,8 +185,10 @@ int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
                 int regime, moe_forward_info* info);
 
 /* How misses reach their slots.  MOE_FILL_MEMCPY (default): the host reads
- * the step's routing record and issues one cudaMemcpyAsync per miss from the
- * pinned pool, spread over the layer's side streams, while the hits compute.
+ * the step's routing record and issues cudaMemcpyAsync from the pinned pool on
+ * the layer's fill stream (a run of consecutive experts bound for consecutive
+ * slots is one copy) while the hits compute; a long miss list runs its expert
+ * FFN in chunks, each after its own copies.
  * MOE_FILL_DEVICE: a copy kernel on a side stream reads the record on the GPU
  * and pulls the missed experts from the pinned pool itself (unified
  * addressing over the host link), so moe_forward never waits on the host;
