@@ -818,14 +818,25 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     a.with_shared = 0;
     if (n_chunks > 1 && !prefill) {
       // memcpy fills: chunk c of the misses runs once its own copies landed
+      // its staged experts that keep their slot are committed right after it:
+      // every access before the chunk's end (hits, earlier chunks) has run
       const int nm = U - n_hit;
       a.n_chunks = n_chunks;
       for (int c = 0; c < n_chunks; ++c) {
         MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[c], 0));
         a.chunk = c;
-        grc = gemv((int)((long long)nm * (c + 1) / n_chunks - (long long)nm * c / n_chunks));
+        const int c0 = n_hit + (int)((long long)nm * c / n_chunks), c1 = n_hit + (int)((long long)nm * (c + 1) / n_chunks);
+        grc = gemv(c1 - c0);
         if (grc) return grc;
+        const int f0 = std::max(c0, std::max(g.S, U - g.S));   // staged and final
+        if (c1 > f0) {
+          pe = prof_begin(L, MOE_PROF_COMMIT, st);
+          MOE_CUDA(L, launch_stage_commit(g, L->rec, f0, c1, c1 - f0, L->slots, st));
+          prof_end(pe, st);
+          L->launches += 1;
+        }
       }
+      any_staged = false;   // committed chunk by chunk
     } else {
       // one launch over every miss once the last copy (one queue, in order) has landed
       if (n_chunks > 0) MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[n_chunks - 1], 0));
@@ -834,7 +845,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     }
     if (any_staged) {
       pe = prof_begin(L, MOE_PROF_COMMIT, st);
-      MOE_CUDA(L, launch_stage_commit(g, L->rec, max_staged, L->slots, st));
+      MOE_CUDA(L, launch_stage_commit(g, L->rec, -1, -1, max_staged, L->slots, st));
       prof_end(pe, st);
       L->launches += 1;
     }

@@ -198,8 +198,10 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
                              const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
 // copy each staged miss that still owns its LRU slot at the end of the step
 // (access i >= S with i + S >= U) from its staging slot into that slot
-cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int max_staged, uint8_t* slots,
-                                cudaStream_t st);
+// Staged accesses in [max(S, a0), min(U, a1)) (a1 < 0: up to U); max_staged
+// bounds their number (grid size).
+cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int a0, int a1, int max_staged,
+                                uint8_t* slots, cudaStream_t st);
 // combine.cu
 // The prefill GEMM writes O as f16 rows [rows][d] in the first half of the
 // O buffer, each row's 128-column blocks scaled by 2^-s; the exponents s

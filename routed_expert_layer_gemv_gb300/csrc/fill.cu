@@ -48,15 +48,17 @@ fill_copy_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, const 
   copy_chunk(pool + (size_t)ex * ebytes, slots + (size_t)access_slot(as, S, i) * ebytes, ebytes, ch);
 }
 
-// CTA (staged miss m, chunk ch): access S + m still owns its LRU slot at the
-// end of the step (no later access of the step maps to that slot) -> copy its
-// staging slot into it.
+// CTA (staged access i = first + m, chunk ch): access i still owns its LRU
+// slot at the end of the step (no later access of the step maps to that slot)
+// -> copy its staging slot into it.  first = max(S, a0); accesses stop at
+// min(U, a1) (a1 < 0: at U).
 __global__ void __launch_bounds__(kFillThreads)
-stage_commit_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, uint8_t* __restrict__ slots,
-                    size_t ebytes, int chunks) {
-  const int U = min(max(rec->U, 0), E);
-  const int i = S + blockIdx.x / chunks, ch = blockIdx.x % chunks;
-  if (i >= U || i - S >= X || i + S < U) return;
+stage_commit_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int a0, int a1,
+                    uint8_t* __restrict__ slots, size_t ebytes, int chunks) {
+  const int U0 = min(max(rec->U, 0), E);
+  const int U = a1 < 0 ? U0 : min(U0, a1);
+  const int i = max(S, a0) + blockIdx.x / chunks, ch = blockIdx.x % chunks;
+  if (i >= U || i - S >= X || i + S < U0) return;
   const int sl = rec_slot(const_cast<StepRecord*>(rec), E)[i];
   if (sl < 0 || sl >= S) return;
   copy_chunk(slots + (size_t)(S + 1 + (i - S)) * ebytes, slots + (size_t)sl * ebytes, ebytes, ch);
@@ -74,12 +76,13 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
   return cudaGetLastError();
 }
 
-cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int max_staged, uint8_t* slots,
-                                cudaStream_t st) {
+cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int a0, int a1, int max_staged,
+                                uint8_t* slots, cudaStream_t st) {
   const int chunks = (int)((g.ebytes + kFillChunk - 1) / kFillChunk);
   const long long grid = (long long)chunks * max_staged;
   if (grid <= 0) return cudaSuccess;
-  stage_commit_kernel<<<(unsigned)grid, kFillThreads, 0, st>>>(rec, g.E, g.S, g.X, slots, g.ebytes, chunks);
+  stage_commit_kernel<<<(unsigned)grid, kFillThreads, 0, st>>>(rec, g.E, g.S, g.X, a0, a1, slots, g.ebytes,
+                                                               chunks);
   return cudaGetLastError();
 }
 
