@@ -77,6 +77,8 @@ struct SG {
   int RS, rbytes;     // partial-sum slots and bytes of one
   int off_x, off_red, off_bar, smem;
   int scale_row;      // scale bytes per weight row
+  int all;            // phase 1, N <= 8: every token staged once (NG groups), entries pick theirs
+  int NG;             // token groups staged (all) / 1
 };
 
 MOE_DEV float pow2i(int s) { return __int_as_float((127 + s) << 23); }  // |s| <= 126
@@ -130,6 +132,8 @@ MOE_DEV void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, 
 
 struct Entry {
   int slot, row0, nrows, shared;
+  int tok0;        // token of the first row (-1: read tok_of)
+  uint32_t gmask;  // groups of 8 tokens the rows touch
 };
 
 // Entries of this launch: the access-order range the mode selects (+ the
@@ -159,6 +163,9 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int en
     out.row0 = v.y;
     out.nrows = v.z;
     out.shared = 0;
+    const uint32_t tk = (uint32_t)v.w;
+    out.tok0 = (tk >> 16) == 0xffffu ? -1 : (int)(tk & 0xffffu);
+    out.gmask = tk >> 16;
     return slot_ok && out.nrows > 0 && out.row0 >= 0 && out.row0 + out.nrows <= a.N * g.k;
   }
   if (a.with_shared && ent == nr) {
@@ -166,6 +173,8 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int en
     out.row0 = a.N * g.k;
     out.nrows = a.N;
     out.shared = 1;
+    out.tok0 = 0;
+    out.gmask = 0xffffu;
     return a.N > 0;
   }
   return false;
@@ -211,7 +220,7 @@ MOE_DEV bool cursor_next(Cursor& c, const Geo& g, const GemvArgs& a, const SG& p
     c.t += c.ue1 - c.ue0;
     if (get_entry(g, a, rr.base, rr.nr, ent, c.en)) {
       c.tg = 0;
-      c.ntg = (c.en.nrows + kTG - 1) / kTG;
+      c.ntg = p.all ? 1 : (c.en.nrows + kTG - 1) / kTG;
       return true;
     }
   }
@@ -229,20 +238,22 @@ MOE_DEV int xslot(int fmt, int t, int k4) {
   return (J * 2 + s) * 32 + 4 * t + q;
 }
 
-// One warp's 16 x 256 MXFP4 tile: acc += W x.  Codes: 128-byte rows, 16-byte
+// One warp's 16 x 256 MXFP4 tile: acc[t] += W x_t for the token groups t < NG
+// set in gm, the codes dequantised once.  Codes: 128-byte rows, 16-byte
 // chunk j of row r stored at chunk j ^ (r & 7) (128-byte swizzle).  Lane
 // (g = lane / 4, q = lane % 4) takes word q of chunk j (codes 8q..8q+7 of
 // block j) of rows g and g + 8; MMA step s uses codes 8q + 4s .. + 3.
-// Blocks j >= nvb lie past K and are skipped.
-MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb, int nvb,
-                     int lane, float (&acc)[4]) {
+// Blocks j >= nvb lie past K and are skipped.  xb0, xb1: groups 0 and 1's
+// staged activations at this 256-K box.
+template <int NG>
+MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb0,
+                     const uint2* xb1, uint32_t gm, int nvb, int lane, float (&acc)[NG][4]) {
   const int g = lane >> 2, q = lane & 3;
   // scale rows are only 4-byte aligned when a whole unit's rows are staged
   const uint2 sc0 = make_uint2(lds32(s0p), lds32(s0p + 4)), sc1 = make_uint2(lds32(s1p), lds32(s1p + 4));
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < nvb) {
-      const uint2 b0 = xb[(2 * j) * 32 + lane], b1 = xb[(2 * j + 1) * 32 + lane];
       const int co = ((j ^ g) << 4) + 4 * q;
       uint32_t f0[4], f1[4];
       e2m1x8_to_f16x8(lds32(cs + 128 * g + co), f0);
@@ -253,13 +264,20 @@ MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
       else if ((j & 3) == 1) { sg = e8m0_byte<1>(w0); sg8 = e8m0_byte<1>(w1); }
       else if ((j & 3) == 2) { sg = e8m0_byte<2>(w0); sg8 = e8m0_byte<2>(w1); }
       else { sg = e8m0_byte<3>(w0); sg8 = e8m0_byte<3>(w1); }
-      float d[4];
-      mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
-      mma16816_acc(d, f0[2], f1[2], f0[3], f1[3], b1);
-      acc[0] = fmaf(d[0], sg, acc[0]);
-      acc[1] = fmaf(d[1], sg, acc[1]);
-      acc[2] = fmaf(d[2], sg8, acc[2]);
-      acc[3] = fmaf(d[3], sg8, acc[3]);
+#pragma unroll
+      for (int t = 0; t < NG; ++t) {
+        if ((gm >> t) & 1u) {
+          const uint2* xt = t == 0 ? xb0 : xb1;
+          const uint2 b0 = xt[(2 * j) * 32 + lane], b1 = xt[(2 * j + 1) * 32 + lane];
+          float d[4];
+          mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
+          mma16816_acc(d, f0[2], f1[2], f0[3], f1[3], b1);
+          acc[t][0] = fmaf(d[0], sg, acc[t][0]);
+          acc[t][1] = fmaf(d[1], sg, acc[t][1]);
+          acc[t][2] = fmaf(d[2], sg8, acc[t][2]);
+          acc[t][3] = fmaf(d[3], sg8, acc[t][3]);
+        }
+      }
     }
   }
 }
@@ -267,14 +285,14 @@ MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
 // NVFP4 tile: 16-code blocks, so each MMA must stay inside one.  Lane q takes
 // codes 4q..4q+3 of both blocks of chunk j (half q & 1 of words q / 2 and
 // 2 + q / 2); MMA step s covers block 2j + s.
-MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb, int nvb,
-                     int lane, float (&acc)[4]) {
+template <int NG>
+MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb0,
+                     const uint2* xb1, uint32_t gm, int nvb, int lane, float (&acc)[NG][4]) {
   const int g = lane >> 2, q = lane & 3;
   const uint32_t sel = (q & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < nvb) {
-      const uint2 b0 = xb[(2 * j) * 32 + lane], b1 = xb[(2 * j + 1) * 32 + lane];
       const int co = ((j ^ g) << 4) + 4 * (q >> 1);
       const uint8_t* r0 = cs + 128 * g + co;
       const uint8_t* r1 = cs + 128 * (g + 8) + co;
@@ -285,13 +303,20 @@ MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
       const uint32_t e1 = *reinterpret_cast<const uint16_t*>(s1p + 2 * j);
       const float sa0 = e4m3_to_f32(e0 & 0xffu), sb0 = e4m3_to_f32(e0 >> 8);
       const float sa1 = e4m3_to_f32(e1 & 0xffu), sb1 = e4m3_to_f32(e1 >> 8);
-      float d[4], e[4];
-      mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
-      mma16816(e, f0[2], f1[2], f0[3], f1[3], b1);
-      acc[0] = fmaf(d[0], sa0, fmaf(e[0], sb0, acc[0]));
-      acc[1] = fmaf(d[1], sa0, fmaf(e[1], sb0, acc[1]));
-      acc[2] = fmaf(d[2], sa1, fmaf(e[2], sb1, acc[2]));
-      acc[3] = fmaf(d[3], sa1, fmaf(e[3], sb1, acc[3]));
+#pragma unroll
+      for (int t = 0; t < NG; ++t) {
+        if ((gm >> t) & 1u) {
+          const uint2* xt = t == 0 ? xb0 : xb1;
+          const uint2 b0 = xt[(2 * j) * 32 + lane], b1 = xt[(2 * j + 1) * 32 + lane];
+          float d[4], e[4];
+          mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
+          mma16816(e, f0[2], f1[2], f0[3], f1[3], b1);
+          acc[t][0] = fmaf(d[0], sa0, fmaf(e[0], sb0, acc[t][0]));
+          acc[t][1] = fmaf(d[1], sa0, fmaf(e[1], sb0, acc[t][1]));
+          acc[t][2] = fmaf(d[2], sa1, fmaf(e[2], sb1, acc[t][2]));
+          acc[t][3] = fmaf(d[3], sa1, fmaf(e[3], sb1, acc[t][3]));
+        }
+      }
     }
   }
 }
@@ -315,6 +340,61 @@ MOE_DEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_f
 }
 
 MOE_DEV float silu_mul(float a, float u) { return a / (1.0f + __expf(-a)) * u; }
+
+// Stage all N <= 16 tokens of the step (phase 1, `all` geometry) into the NG
+// group buffers at xs, as stage_block does for one group, with the per-token
+// exponent computed here from x (the same rule as the router's: amax 2^-s in
+// [2^14, 2^15)); columns past N are zero.  x is final before the router
+// starts, so this runs before the programmatic wait.  By `nthr` threads
+// (index tid) meeting on named barrier `bar`.
+template <int FMT>
+MOE_DEV void stage_all(const SG& p, int N, const __nv_bfloat16* __restrict__ x, uint2* xs, int* sexp, int tid,
+                       int nthr, int bar) {
+  const int w = tid >> 5, l = tid & 31, nw = nthr >> 5;
+  for (int t = w; t < N; t += nw) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * p.K);
+    float m = 0.f;
+    for (int i = l; i < p.K / 8; i += 32) {
+      const uint4 v = xr[i];
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[e] << 16)), fabsf(__uint_as_float(wv[e] & 0xffff0000u))));
+    }
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (l == 0) {
+      int s = 0;
+      if (m > 0.f) {
+        int ex;
+        frexpf(m, &ex);
+        s = max(-100, min(100, ex - 15));
+      }
+      sexp[t] = s;
+    }
+  }
+  asm volatile("bar.sync %0, %1;" :: "r"(bar), "r"(nthr) : "memory");
+  const int k8n = p.K / 8, ntok = p.NG * kTG;
+  for (int it = tid; it < ntok * k8n; it += nthr) {
+    const int t = it / k8n, k8 = it % k8n;
+    uint2* xg = xs + (size_t)(t / kTG) * 2 * p.K;   // one group: K x 8 tokens of f16
+    const int c = t % kTG;
+    uint32_t o[4] = {0u, 0u, 0u, 0u};
+    if (t < N) {
+      const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)t * p.K)[k8];
+      const float sc = pow2i(-sexp[t]);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __half2 hh = __floats2half2_rn(__uint_as_float(wv[e] << 16) * sc,
+                                             __uint_as_float(wv[e] & 0xffff0000u) * sc);
+        o[e] = *reinterpret_cast<const uint32_t*>(&hh);
+      }
+    }
+    xg[xslot(FMT, c, 2 * k8)] = make_uint2(o[0], o[1]);
+    xg[xslot(FMT, c, 2 * k8 + 1)] = make_uint2(o[2], o[3]);
+  }
+  asm volatile("bar.sync %0, %1;" :: "r"(bar), "r"(nthr) : "memory");
+}
 
 // Stage one token group's activations into buffer xs as f16 in B-fragment
 // order, by `nthr` threads (index tid) that meet on named barrier `bar`.
@@ -404,7 +484,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
   S.xfull = S.rempty + 2;
   S.xempty = S.xfull + 2;
   __shared__ int sexp[2][kTG];
-  __shared__ int stok[kTG];
+  __shared__ int stok[2 * kTG];
   __shared__ volatile int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -436,12 +516,18 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
       tc::prefetch_tmap(&smap1);
     }
   }
+  const bool ALL = PH == 1 && p.all;
+  if (ALL && warp != kProd) {
+    // every token of the step, before the wait: x is final before the router starts
+    const int tid = warp < kCW ? threadIdx.x : threadIdx.x - 32;
+    stage_all<FMT>(p, a.N, x, reinterpret_cast<uint2*>(S.base + p.off_x), &sexp[0][0], tid, kThreads - 32, 2);
+  }
   if (PH == 1 || warp != kProd) pdl_wait();
   pdl_trigger();
   const Range rr = cta_range(g, a, p);
   // the first token group is staged by every warp but the producer (its
   // latency is on the critical path); the epilogue stages later ones ahead
-  if (warp != kProd) {
+  if (!ALL && warp != kProd) {
     Cursor c0;
     cursor_init(c0, rr);
     if (cursor_next(c0, g, a, p, rr)) {
@@ -505,7 +591,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     }
   } else if (warp < kCW) {
     // ------------------------------------------------------------ compute
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float* red = reinterpret_cast<float*>(S.base + p.off_red);
     const int bslot = warp >> 2, quarter = warp & 3, gq = lane >> 2;
     uint32_t n = 0, us = 0, bs = 0;
@@ -513,7 +599,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     cursor_init(cu, rr);
     while (cursor_next(cu, g, a, p, rr)) {
       const int xb = bs % p.XB;
-      wait_or_abort(&S.xfull[xb], (bs / p.XB) & 1, &s_abort, a.err);
+      if (!ALL) wait_or_abort(&S.xfull[xb], (bs / p.XB) & 1, &s_abort, a.err);
+      // token groups this entry needs (all staged groups when its tokens are unknown)
+      const uint32_t gm = ALL ? (cu.en.gmask & ((1u << p.NG) - 1u)) : 1u;
       const uint2* xs = reinterpret_cast<const uint2*>(S.base + p.off_x + (size_t)xb * p.xbytes);
       for (int u = cu.ue0; u < cu.ue1; ++u) {
         for (int st = 0; st < p.NS; ++st, ++n) {
@@ -525,9 +613,11 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
             const uint8_t* cs = stg + (size_t)bslot * kBoxBytes + quarter * (16 * kBoxK / 2);
             const uint8_t* sc = stg + p.codes_bytes + (16 * quarter + gq) * p.srow + (p.smode ? bslot : kb) * p.SBB;
             const int nvb = min(8, (p.K - kb * kBoxK) / 32);
-            const uint2* xk = xs + (size_t)kb * 512;   // 8 blocks x 2 steps x 32 lanes
-            if (FMT == MOE_MXFP4) tile_mx(cs, sc, sc + 8 * p.srow, xk, nvb, lane, acc);
-            else tile_nv(cs, sc, sc + 8 * p.srow, xk, nvb, lane, acc);
+            // 8 blocks x 2 steps x 32 lanes per box; group 1 (all tokens) one group further
+            const uint2* xk0 = xs + (size_t)kb * 512;
+            const uint2* xk1 = xk0 + 2 * (size_t)p.K;
+            if (FMT == MOE_MXFP4) tile_mx<2>(cs, sc, sc + 8 * p.srow, xk0, xk1, gm, nvb, lane, acc);
+            else tile_nv<2>(cs, sc, sc + 8 * p.srow, xk0, xk1, gm, nvb, lane, acc);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -535,15 +625,19 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         // unit done: hand the partial sums to the epilogue
         const int r = us % p.RS;
         if (us >= (uint32_t)p.RS) wait_or_abort(&S.rempty[r], (us / p.RS - 1) & 1, &s_abort, a.err);
-        reinterpret_cast<float4*>(red + (size_t)r * (p.rbytes / 4))[warp * 32 + lane] =
-            make_float4(acc[0], acc[1], acc[2], acc[3]);
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        float4* rdst = reinterpret_cast<float4*>(red + (size_t)r * (p.rbytes / 4));
+        rdst[warp * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        if (gm & 2u) rdst[kCW * 32 + warp * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.rfull[r]);
         ++us;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.xempty[xb]);
+      if (!ALL) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.xempty[xb]);
+      }
       ++bs;
     }
   } else {
@@ -566,13 +660,22 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     cursor_init(cs, rr);
     cursor_init(cr, rr);
     uint32_t bs_st = 1, bs_rd = 0, us = 0;   // block 0 was staged by all warps
-    cursor_next(cs, g, a, p, rr);
-    for (int i = 1; i < p.XB; ++i)
-      if (cursor_next(cs, g, a, p, rr)) stage(cs, bs_st++);
+    if (!ALL) {
+      cursor_next(cs, g, a, p, rr);
+      for (int i = 1; i < p.XB; ++i)
+        if (cursor_next(cs, g, a, p, rr)) stage(cs, bs_st++);
+    }
     while (cursor_next(cr, g, a, p, rr)) {
       const int xb = bs_rd % p.XB;
-      const int nt = min(kTG, cr.en.nrows - cr.tg * kTG);
+      const int nt = ALL ? cr.en.nrows : min(kTG, cr.en.nrows - cr.tg * kTG);
       const int rowt = cr.en.row0 + cr.tg * kTG;
+      if (ALL) {
+        // the entry's tokens (all N tokens are staged; entries pick theirs)
+        epi_sync();
+        if (te < nt)
+          stok[te] = cr.en.shared ? te : (te == 0 && cr.en.tok0 >= 0) ? cr.en.tok0 : a.tok_of[rowt + te];
+        epi_sync();
+      }
       const float* tsp = reinterpret_cast<const float*>(a.slots + (size_t)cr.en.slot * g.ebytes + g.off_tscale);
       for (int u = cr.ue0; u < cr.ue1; ++u) {
         const int m = PH == 1 ? u / p.RB : 0;
@@ -583,17 +686,20 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         const float4* rs = reinterpret_cast<const float4*>(red + (size_t)r * (p.rbytes / 4));
         // warp w takes tokens w, w + kEW, ...; lane c takes columns c, c + 32 of the block
         for (int tk = ew_; ok && tk < nt; tk += kEW) {
-          const float sc = pow2i(sexp[xb][tk]) * ts;
+          // (group, column) of this row's token among the staged ones
+          const int tok = ALL ? stok[tk] : tk;
+          const int gg = ALL ? tok / kTG : 0, cc = ALL ? tok % kTG : tk;
+          const float sc = pow2i(ALL ? (&sexp[0][0])[tok] : sexp[xb][tk]) * ts;
           float mx = 0.f;
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             const int col = lane + 32 * c2;
             const int qr = col >> 4, rr_ = col & 15;
-            const int lo = 4 * (rr_ & 7) + (tk >> 1), jj = 2 * (rr_ >> 3) + (tk & 1);
+            const int lo = 4 * (rr_ & 7) + (cc >> 1), jj = 2 * (rr_ >> 3) + (cc & 1);
             float s = 0.f;
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b) {
-              const float4 v = rs[(b * 4 + qr) * 32 + lo];
+              const float4 v = rs[gg * kCW * 32 + (b * 4 + qr) * 32 + lo];
               s += jj == 0 ? v.x : jj == 1 ? v.y : jj == 2 ? v.z : v.w;
             }
             const float val = s * sc;
@@ -612,15 +718,21 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         ++us;
       }
       ++bs_rd;
-      // every epilogue warp is done with this block's exponents before they are restaged
-      epi_sync();
-      if (cursor_next(cs, g, a, p, rr)) stage(cs, bs_st++);
+      if (!ALL) {
+        // every epilogue warp is done with this block's exponents before they are restaged
+        epi_sync();
+        if (cursor_next(cs, g, a, p, rr)) stage(cs, bs_st++);
+      }
     }
   }
   __syncthreads();
 }
 
-SG make_sg(const Geo& g, int ph) {
+// N: tokens of the launch (phase 1 with N <= 8 stages every token once, one
+// group, when a ring of at least 3 stages still fits; 0 = the per-group
+// geometry).  With more tokens an entry's own group is staged per block:
+// staging two groups per launch cost more than it saved.
+SG make_sg(const Geo& g, int ph, int N) {
   SG p{};
   p.K = ph == 1 ? g.d : g.f;
   p.R = ph == 1 ? g.f : g.d;
@@ -645,6 +757,19 @@ SG make_sg(const Geo& g, int ph) {
   if (2 * p.xbytes + 2 * p.rbytes + 3 * p.stage_bytes + bars > kSmemBudget) p.XB = 1;
   const int fixed = p.XB * p.xbytes + p.RS * p.rbytes + bars;
   p.D = std::min(kMaxD, (kSmemBudget - fixed) / p.stage_bytes);
+  p.all = 0;
+  p.NG = 1;
+  if (ph == 1 && N > 0 && N <= kTG) {
+    SG q = p;
+    q.all = 1;
+    q.NG = (N + kTG - 1) / kTG;
+    q.XB = 1;
+    q.xbytes = q.NG * p.K * 2 * kTG;           // every group, one buffer
+    q.rbytes = q.NG * kCW * 32 * 16;           // one float4 per compute lane and group
+    const int fq = q.xbytes + q.RS * q.rbytes + bars;
+    q.D = std::min(kMaxD, (kSmemBudget - fq) / q.stage_bytes);
+    if (q.D >= 3) p = q;
+  }
   p.off_x = p.D * p.stage_bytes;
   p.off_red = p.off_x + p.XB * p.xbytes;
   p.off_bar = p.off_red + p.RS * p.rbytes;
@@ -678,7 +803,7 @@ template <int FMT>
 cudaError_t launch_fmt(const Geo& g, const GemvPlan* pl, const GemvArgs& a, const __nv_bfloat16* x,
                        const int* xexp, float* h, float* O, int n_ent_max, int num_sms,
                        cudaStream_t st, const cudaEvent_t* ev) {
-  const SG p1 = make_sg(g, 1), p2 = make_sg(g, 2);
+  const SG p1 = make_sg(g, 1, a.N), p2 = make_sg(g, 2, a.N);
   if (ev) cudaEventRecord(ev[0], st);
   cudaError_t e = launch_phase<FMT, 1>(g, pl, a, p1, x, xexp, h, O, n_ent_max, num_sms, st);
   if (ev) cudaEventRecord(ev[1], st);
@@ -747,7 +872,7 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64
 // next to the staged activations.
 bool gemv_shape_ok(const Geo& g) {
   if (g.d > 8192 || g.f > 8192 || g.d % 128 || g.f % 128) return false;
-  return make_sg(g, 1).D >= 2 && make_sg(g, 2).D >= 2;
+  return make_sg(g, 1, 0).D >= 2 && make_sg(g, 2, 0).D >= 2;
 }
 
 GemvPlan* gemv_plan_create(const Geo& g, const uint8_t* slots) {
@@ -757,7 +882,7 @@ GemvPlan* gemv_plan_create(const Geo& g, const uint8_t* slots) {
               make_box_map(&pl->w[1], slots + g.off_codes[1], g.d / 2, g.f, ns, g.ebytes) &&
               make_box_map(&pl->w[2], slots + g.off_codes[2], g.f / 2, g.d, ns, g.ebytes);
   // scale maps only where a scale row is a 16-byte multiple (the phase uses them then)
-  const SG p1 = make_sg(g, 1), p2 = make_sg(g, 2);
+  const SG p1 = make_sg(g, 1, 0), p2 = make_sg(g, 2, 0);
   const uint32_t sb = kBoxes * (g.fmt == MOE_MXFP4 ? 8 : 16);
   if (pl->ready && p1.smode)
     pl->ready = make_scale_map(&pl->s[0], slots + g.off_scales[0], p1.scale_row, g.f, ns, g.ebytes, sb) &&

@@ -100,7 +100,8 @@ MOE_DEV void lru_park(const LruRegs& r, int E, int S, LruSmem& m) {
 // One step of the table (blockDim.x == 1024) on the state parked in m (the
 // caller synchronises after lru_park).  counts may live in shared or global
 // memory.
-MOE_DEV void lru_body(const int* counts, const int* offs, int E, int S, int X, int* __restrict__ slot_of,
+MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, int E, int S, int X,
+                      int* __restrict__ slot_of,
                       int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                       unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
                       unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq,
@@ -179,7 +180,22 @@ MOE_DEV void lru_body(const int* counts, const int* offs, int E, int S, int X, i
     // physical slot: the LRU slot, or staging slot S + 1 + (i - S) for later waves
     const bool ok = ex >= 0 && ex < E && sl >= 0 && sl < S && i - S < X;
     const int ps = !ok ? -1 : i < S ? sl : S + 1 + (i - S);
-    r_n[i] = make_int4(ps, offs && ok ? offs[ex] : 0, offs && ok ? counts[ex] : 0, ex);
+    const int row0 = offs && ok ? offs[ex] : 0, nrow = offs && ok ? counts[ex] : 0;
+    // first token and token groups of the access, from the per-warp token
+    // ballots of its expert (tokens 32 w + lane); unknown without them
+    uint32_t toks = 0xffff0000u;
+    if (cm && ok && nrow > 0) {
+      int t0 = -1;
+      uint32_t gm = 0;
+      for (int w = 0; w < perm::kPermWarps; ++w) {
+        const uint32_t b = cm[ex * perm::kPermWarps + w];
+        if (b && t0 < 0) t0 = 32 * w + __ffs(b) - 1;
+        for (int q = 0; q < 4; ++q)
+          if ((b >> (8 * q)) & 0xffu) gm |= 1u << min(4 * w + q, 15);
+      }
+      toks = ((uint32_t)t0 & 0xffffu) | (gm << 16);
+    }
+    r_n[i] = make_int4(ps, row0, nrow, (int)toks);
     if (host_rec) {
       rec_expert(host_rec)[i] = ex;
       rec_slot(host_rec, E)[i] = sl;
@@ -194,12 +210,11 @@ MOE_DEV void lru_body(const int* counts, const int* offs, int E, int S, int X, i
       host_rec->n_miss = n_miss;
       host_rec->S = S;
     }
-    __threadfence_system();
+    // each writer's fence completes before the barrier, so seq is stored
+    // after every other field is visible to the host
+    if (tid < U || tid == 0) __threadfence_system();
     __syncthreads();
-    if (tid == 0) {
-      __threadfence_system();
-      *reinterpret_cast<volatile unsigned long long*>(&host_rec->seq) = seq;
-    }
+    if (tid == 0) *reinterpret_cast<volatile unsigned long long*>(&host_rec->seq) = seq;
   }
   if (tid == 0) {
     rec->U = U;
@@ -243,7 +258,7 @@ lru_step_kernel(const int* __restrict__ counts, const int* __restrict__ offsets,
   __shared__ LruSmem m;
   lru_park(lru_load(E, S, slot_of, expert_of, stamp, clock), E, S, m);
   __syncthreads();
-  lru_body(counts, offsets, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
+  lru_body(counts, offsets, nullptr, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
 }
 
 // Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
@@ -293,7 +308,7 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
     }
   }
   __syncthreads();
-  lru_body(cnt, off, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
+  lru_body(cnt, off, cm, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
 }
 
 __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expert_of,
