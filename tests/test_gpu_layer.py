@@ -9,6 +9,7 @@ import torch
 from helpers import (CachedExperts, assert_close_layer, bf16_tensor, need_gpu, oracle_layer,
                      reject_near_ties, small_spec)
 from oracle import formats
+from oracle import layer as olayer
 from oracle.lru import SlotTable
 from routed_expert_layer_gemv_gb300 import capi
 from routed_expert_layer_gemv_gb300 import workloads as wl
@@ -287,6 +288,35 @@ def test_prefill_35b_shape_sampled_tokens():
     ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "prefill", tokens=sample)
     assert_close_layer(y[sample], ref, "prefill 35B shape")
     L.close()
+
+
+def _full_chunk_parity(work, n_sample):
+    # the bench's own prefill chunk (same generator, size and launch path),
+    # checked on sampled tokens the oracle computes one expert at a time;
+    # tokens whose k-th and (k+1)-th FP64 logits are within 1e-4 are skipped
+    # (their expert choice is not unique at that tolerance)
+    spec, N, seed = work.layer, work.n_tokens, work.seed
+    x, _ = wl.iid_tokens(seed, N, spec.d_model)
+    L = build_layer(spec, seed, N, install_all=True)
+    y, info = L.forward(bf16_tensor(x), regime=PRE)
+    torch.cuda.synchronize()
+    assert info.regime == PRE
+    W_r, b = wl.router_weights(spec, seed)
+    cand = np.unique(np.linspace(0, N - 1, 4 * n_sample).astype(np.int64))
+    tie = olayer.near_tie(wl.bf16_bits_to_f64(x[cand]), W_r, b, spec.k, 1e-4)
+    sample = [int(t) for t, bad in zip(cand, tie) if not bad][:n_sample]
+    assert len(sample) == n_sample
+    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x[sample]), "prefill")
+    assert_close_layer(y[sample], ref, "%s, sampled tokens" % work.name)
+    L.close()
+
+
+def test_prefill_35b_full_chunk_sampled():
+    _full_chunk_parity(wl.PREFILL_35B, 12)
+
+
+def test_prefill_753b_full_chunk_sampled():
+    _full_chunk_parity(wl.PREFILL_753B, 4)
 
 
 def test_prefill_with_misses_and_waves():
