@@ -717,7 +717,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   const float gh = g.fmt == MOE_NVFP4 ? L->desc.act_scale_h : 1.0f;
   if (prefill) {
     pe = prof_begin(L, MOE_PROF_PREFILL, st);
-    MOE_CUDA(L, launch_gather_quant(g, xd, L->tok_of, N, gx, L->xq_codes, L->xq_scales, st));
+    MOE_CUDA(L, launch_gather_quant(g, xd, L->row_of, N, gx, L->xq_codes, L->xq_scales, st));
     prof_end(pe, st);
     L->launches += 1;
   }

@@ -186,7 +186,8 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
 void prefill_plan_destroy(PrefillPlan* pl);
 bool prefill_plan_ready(const PrefillPlan* pl);
 size_t prefill_tile_bytes(const Geo& g, int N);
-cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* tok_of, int N,
+// row_of [N, k]: the permuted row of each (token, expert) pair
+cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* row_of, int N,
                                 float gx, uint8_t* codes, uint8_t* scales, cudaStream_t st);
 // ev (may be null): 4 events around phase 1 and phase 2
 cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const StepRecord* rec,

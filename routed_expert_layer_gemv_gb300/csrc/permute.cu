@@ -33,11 +33,11 @@ perm_hist_kernel(const int* __restrict__ idx, int N, int k, int E, int* __restri
   extern __shared__ uint32_t sm[];
   uint32_t* cm = sm;                                              // [E][kPermWarps]
   int* rows = reinterpret_cast<int*>(sm + E * kPermWarps);        // [128][k]
+  uint32_t* tb = reinterpret_cast<uint32_t*>(rows + kTokPerBlock * k);   // [128][ceil(E/32)]
   const int t_base = blockIdx.x * kTokPerBlock;
   perm::stage_rows(idx, N, k, t_base, rows);
   __syncthreads();
-  perm::build_ballots(rows, k, E, cm);
-  __syncthreads();
+  perm::build_ballots_par(rows, k, E, min(kTokPerBlock, N - t_base), tb, cm);
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = perm::block_count(cm, e);
   const int t = t_base + threadIdx.x;
   if (t < N)
@@ -52,10 +52,16 @@ perm_scan_kernel(int* __restrict__ hist, int nblk, int E, int* __restrict__ coun
   const int e = threadIdx.x;
   int tot = 0;
   if (e < E) {
-    for (int b = 0; b < nblk; ++b) {
-      int c = hist[(size_t)b * E + e];
-      hist[(size_t)b * E + e] = tot;  // exclusive prefix over blocks
-      tot += c;
+    // exclusive prefix over blocks, 16 loads in flight at a time
+    for (int b0 = 0; b0 < nblk; b0 += 16) {
+      int c[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c[i] = b0 + i < nblk ? hist[(size_t)(b0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (b0 + i < nblk) hist[(size_t)(b0 + i) * E + e] = tot;
+        tot += c[i];
+      }
     }
   }
   int all;
@@ -91,10 +97,10 @@ perm_single_kernel(const int* __restrict__ idx, int N, int k, int E, int* __rest
   int* off = reinterpret_cast<int*>(sm + E * kPermWarps);      // [E]
   int* sh = off + E;                                           // [33]
   int* rows = sh + 33;                                         // [128][k]
+  uint32_t* tb = reinterpret_cast<uint32_t*>(rows + kTokPerBlock * k);   // [128][ceil(E/32)]
   perm::stage_rows(idx, N, k, 0, rows);
   __syncthreads();
-  perm::build_ballots(rows, k, E, cm);
-  __syncthreads();
+  perm::build_ballots_par(rows, k, E, N, tb, cm);
   // exclusive scan of counts over e, kTokPerBlock experts at a time
   int carry = 0;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
@@ -133,7 +139,14 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
                            int* row_of, int* tok_of, void* scratch, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
   if (N <= kTokPerBlock) {
-    size_t smem = (size_t)g.E * kPermWarps * 4 + (size_t)g.E * 4 + 33 * 4 + (size_t)kTokPerBlock * g.k * 4;
+    size_t smem = (size_t)g.E * kPermWarps * 4 + (size_t)g.E * 4 + 33 * 4 + (size_t)kTokPerBlock * g.k * 4 +
+                  (size_t)kTokPerBlock * ((g.E + 31) / 32) * 4;
+    static bool attr = false;   // up to 53 KB at E = 1024, k = 32
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(perm_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
     perm_single_kernel<<<1, kTokPerBlock, smem, st>>>(idx, N, g.k, g.E, counts, offsets, row_of,
                                                       tok_of);
     return cudaGetLastError();
@@ -141,7 +154,8 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
   const int nblk = (N + kTokPerBlock - 1) / kTokPerBlock;
   int* hist = static_cast<int*>(scratch);
   int* rank = hist + (size_t)nblk * g.E;
-  perm_hist_kernel<<<nblk, kTokPerBlock, (size_t)g.E * kPermWarps * 4 + (size_t)kTokPerBlock * g.k * 4,
+  perm_hist_kernel<<<nblk, kTokPerBlock, (size_t)g.E * kPermWarps * 4 + (size_t)kTokPerBlock * g.k * 4 +
+                                          (size_t)kTokPerBlock * ((g.E + 31) / 32) * 4,
                      st>>>(idx, N, g.k, g.E, hist, rank);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;

@@ -1,11 +1,11 @@
 // Device pieces of the atomic-free permutation, shared by the permutation
 // kernels and the fused decode routing tail.
 //
-// Block b owns 128 consecutive tokens.  Each warp builds, for every expert e,
-// the 32-bit ballot of its tokens routed to e (a token's ids are sorted, so a
-// lane walks its k ids in step with e, reading them from shared memory).
-// Popcounts of the ballots give the block histogram and each pair's rank
-// among the block's earlier tokens routed to the same expert.
+// Block b owns 128 consecutive tokens.  For every expert e and warp-sized
+// group of 32 tokens the block holds the ballot of the tokens routed to e
+// (built from per-token expert bitmaps, no loop over the experts).  Popcounts
+// of the ballots give the block histogram and each pair's rank among the
+// block's earlier tokens routed to the same expert.
 #pragma once
 #include "common.cuh"
 
@@ -24,28 +24,11 @@ MOE_DEV void stage_rows(const int* __restrict__ idx, int N, int k, int t_base, i
   }
 }
 
-// Ballots of warp w's tokens per expert into cm[e * kPermWarps + w]; run by
-// the first kPermWarps warps.  rows = the staged id rows.
-MOE_DEV void build_ballots(const int* rows, int k, int E, uint32_t* cm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int* row = rows + (warp * 32 + lane) * k;
-  int ptr = 0;
-  int nxt = row[0];
-  for (int e = 0; e < E; ++e) {
-    const bool has = (nxt == e);
-    if (has) {
-      ++ptr;
-      nxt = ptr < k ? row[ptr] : 0x7fffffff;
-    }
-    const uint32_t b = __ballot_sync(0xffffffffu, has);
-    if (lane == 0) cm[e * kPermWarps + warp] = b;
-  }
-}
-
-// The same ballots built by a whole CTA (any blockDim) without a loop over
-// the experts: each token's expert set becomes a bitmap tb[t][E/32] (one
-// thread per token word, k compares), then thread (e, w) gathers bit e of
-// warp w's tokens.  nt = tokens of the block (<= 128); tb: 128 * ceil(E/32)
+// Ballots of the block's tokens per expert: cm[e * kPermWarps + w] bit l =
+// token 32 w + l is routed to e.  Built by the whole CTA (any blockDim)
+// without a loop over the experts: each token's expert set becomes a bitmap
+// tb[t][E/32] (one thread per token word, k compares), then thread (e, w)
+// gathers bit e of warp w's tokens.  nt = tokens of the block (<= 128); tb: 128 * ceil(E/32)
 // words of scratch.  Ends with the CTA synchronised.
 MOE_DEV void build_ballots_par(const int* rows, int k, int E, int nt, uint32_t* tb, uint32_t* cm) {
   const int W = (E + 31) >> 5;

@@ -43,17 +43,18 @@ struct Tile {
 };
 
 // ---------------------------------------------------------------- step 1
-__global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ tok_of,
+// FP4 activations of every (token, expert) row: each token's 32-value groups
+// are quantised once and the codes and scales written to the token's k
+// permuted rows (row_of) and its shared-expert row N k + t.  Thread = (token,
+// group).
+__global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ row_of,
                                     int N, int k, int d, int fmt, float gx, int with_shared,
                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const int nb = d / 32;                       // 32-value groups per row
-  const size_t rows = (size_t)N * k + (with_shared ? N : 0);
   const size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= rows * nb) return;
-  const size_t r = v / nb;
-  const int c = (int)(v % nb);
-  const int tok = r < (size_t)N * k ? tok_of[r] : (int)(r - (size_t)N * k);
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * d + (size_t)c * 32);
+  if (v >= (size_t)N * nb) return;
+  const int t = (int)(v / nb), c = (int)(v % nb);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + (size_t)c * 32);
   float vals[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -66,17 +67,28 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
     }
   }
   uint32_t words[4];
-  uint8_t* dst = codes + r * (d / 2) + (size_t)c * 16;
+  uint32_t s0, s1 = 0;
   if (fmt == MOE_MXFP4) {
-    scales[r * (d / 32) + c] = (uint8_t)quant_mx32(vals, words);
+    s0 = quant_mx32(vals, words);
   } else {
     uint32_t w2[2];
-    scales[r * (d / 16) + 2 * c] = (uint8_t)quant_nv16(vals, gx, words);
-    scales[r * (d / 16) + 2 * c + 1] = (uint8_t)quant_nv16(vals + 16, gx, w2);
+    s0 = quant_nv16(vals, gx, words);
+    s1 = quant_nv16(vals + 16, gx, w2);
     words[2] = w2[0];
     words[3] = w2[1];
   }
-  *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+  const uint4 cw = make_uint4(words[0], words[1], words[2], words[3]);
+  const int nr = k + (with_shared ? 1 : 0);
+  for (int j = 0; j < nr; ++j) {
+    const size_t r = j < k ? (size_t)row_of[(size_t)t * k + j] : (size_t)N * k + t;
+    *reinterpret_cast<uint4*>(codes + r * (d / 2) + (size_t)c * 16) = cw;
+    if (fmt == MOE_MXFP4) {
+      scales[r * (d / 32) + c] = (uint8_t)s0;
+    } else {
+      scales[r * (d / 16) + 2 * c] = (uint8_t)s0;
+      scales[r * (d / 16) + 2 * c + 1] = (uint8_t)s1;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- step 2
@@ -574,12 +586,11 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
 void prefill_plan_destroy(PrefillPlan* pl) { delete pl; }
 bool prefill_plan_ready(const PrefillPlan* pl) { return pl && pl->ready; }
 
-cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* tok_of, int N, float gx,
+cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* row_of, int N, float gx,
                                 uint8_t* codes, uint8_t* scales, cudaStream_t st) {
-  const size_t rows = (size_t)N * g.k + (g.has_shared ? N : 0);
-  const size_t total = rows * (g.d / 32);
+  const size_t total = (size_t)N * (g.d / 32);
   if (total == 0) return cudaSuccess;
-  gather_quant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(x, tok_of, N, g.k, g.d, g.fmt, gx,
+  gather_quant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(x, row_of, N, g.k, g.d, g.fmt, gx,
                                                                       g.has_shared, codes, scales);
   return cudaGetLastError();
 }
