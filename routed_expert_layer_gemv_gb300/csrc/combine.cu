@@ -12,20 +12,30 @@ namespace {
 
 // O rows are fp32 (decode) or f16 with a power-of-two exponent per row and
 // 128-column block (prefill: half the bytes of the largest intermediate);
-// either way the sum is formed in fp32.
+// either way the sum is formed in fp32.  A thread takes one 16-byte piece of
+// each O row: V = 4 (fp32) or 8 (f16) columns.
 struct OF32 {
+  static constexpr int V = 4;
   const float* O;
-  MOE_DEV float4 load(size_t row, int d, int c4) const { return reinterpret_cast<const float4*>(O + row * d)[c4]; }
+  MOE_DEV void load(size_t row, int d, int cv, float (&o)[4]) const {
+    const float4 v = reinterpret_cast<const float4*>(O + row * d)[cv];
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
 };
 struct OF16 {
+  static constexpr int V = 8;
   const __half* O;
   const int8_t* e;
-  MOE_DEV float4 load(size_t row, int d, int c4) const {
-    const uint2 v = reinterpret_cast<const uint2*>(O + row * d)[c4];
-    const float s = __int_as_float((127 + e[row * (d / 128) + c4 / 32]) << 23);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-    return make_float4(a.x * s, a.y * s, b.x * s, b.y * s);
+  MOE_DEV void load(size_t row, int d, int cv, float (&o)[8]) const {
+    const uint4 v = reinterpret_cast<const uint4*>(O + row * d)[cv];
+    const float s = __int_as_float((127 + e[row * (d / 128) + cv / 16]) << 23);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      o[2 * i] = f.x * s;
+      o[2 * i + 1] = f.y * s;
+    }
   }
 };
 
@@ -33,33 +43,38 @@ template <typename OT>
 __global__ void combine_kernel(const OT O, const float* __restrict__ gates,
                                const int* __restrict__ row_of, int N, int k, int d, int shared,
                                __nv_bfloat16* __restrict__ y) {
+  constexpr int V = OT::V;
   pdl_wait();
-  const int q = d / 4;
+  const int q = d / V;
   const int v = blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= N * q) return;
-  const int t = v / q, c4 = v % q;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int t = v / q, cv = v % q;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
   for (int j = 0; j < k; ++j) {
     const float gj = gates[(size_t)t * k + j];
-    const float4 o = O.load((size_t)row_of[(size_t)t * k + j], d, c4);
-    acc.x = fmaf(gj, o.x, acc.x);
-    acc.y = fmaf(gj, o.y, acc.y);
-    acc.z = fmaf(gj, o.z, acc.z);
-    acc.w = fmaf(gj, o.w, acc.w);
+    float o[V];
+    O.load((size_t)row_of[(size_t)t * k + j], d, cv, o);
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = fmaf(gj, o[i], acc[i]);
   }
   if (shared) {
-    const float4 o = O.load((size_t)N * k + t, d, c4);
-    acc.x += o.x;
-    acc.y += o.y;
-    acc.z += o.z;
-    acc.w += o.w;
+    float o[V];
+    O.load((size_t)N * k + t, d, cv, o);
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] += o[i];
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 out;
-  out.x = *reinterpret_cast<uint32_t*>(&lo);
-  out.y = *reinterpret_cast<uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(y + (size_t)t * d)[c4] = out;
+  uint32_t out[V / 2];
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    out[i] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  if constexpr (V == 8)
+    reinterpret_cast<uint4*>(y + (size_t)t * d)[cv] = make_uint4(out[0], out[1], out[2], out[3]);
+  else
+    reinterpret_cast<uint2*>(y + (size_t)t * d)[cv] = make_uint2(out[0], out[1]);
 }
 
 }  // namespace
@@ -67,11 +82,13 @@ __global__ void combine_kernel(const OT O, const float* __restrict__ gates,
 cudaError_t launch_combine(const Geo& g, const float* O, bool o_f16, const float* gates, const int* row_of,
                            int N, __nv_bfloat16* y, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
-  const int total = N * (g.d / 4);
-  if (o_f16)
+  if (o_f16) {
+    const int total = N * (g.d / OF16::V);
     return launch_pdl(combine_kernel<OF16>, dim3((total + 255) / 256), dim3(256), 0, st,
                       OF16{reinterpret_cast<const __half*>(O), prefill_o_exp(g, O, N)}, gates, row_of, N, g.k, g.d,
                       g.has_shared, y);
+  }
+  const int total = N * (g.d / OF32::V);
   return launch_pdl(combine_kernel<OF32>, dim3((total + 255) / 256), dim3(256), 0, st, OF32{O}, gates, row_of, N,
                     g.k, g.d, g.has_shared, y);
 }
