@@ -86,9 +86,8 @@ inline size_t rec_bytes(int E) { return sizeof(StepRecord) + 3 * sizeof(int) * (
 // Device-only tail: per access i, {physical slot (access_slot, -1 when the
 // record is inconsistent), first permuted row, rows, tokens}, so a kernel
 // finds an access's weights and tokens with one 16-byte load.  tokens = the
-// first row's token (low 16 bits) | a mask of the groups of 8 tokens its rows
-// touch (bits 16..31, groups >= 15 fold into bit 31; 0xffff in the high half
-// when the token list is not known).
+// first row's token (low 16 bits; 0xffff in the high half when it is not
+// known).
 __host__ __device__ inline int4* rec_entry(StepRecord* r, int E) {
   const size_t off = (sizeof(StepRecord) + 3 * sizeof(int) * (size_t)E + 15) & ~size_t(15);
   return reinterpret_cast<int4*>(reinterpret_cast<char*>(r) + off);

@@ -77,8 +77,7 @@ struct SG {
   int RS, rbytes;     // partial-sum slots and bytes of one
   int off_x, off_red, off_bar, smem;
   int scale_row;      // scale bytes per weight row
-  int all;            // phase 1, N <= 8: every token staged once (NG groups), entries pick theirs
-  int NG;             // token groups staged (all) / 1
+  int all;            // phase 1, N <= 8: every token staged once, entries pick theirs
 };
 
 MOE_DEV float pow2i(int s) { return __int_as_float((127 + s) << 23); }  // |s| <= 126
@@ -133,7 +132,6 @@ MOE_DEV void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, 
 struct Entry {
   int slot, row0, nrows, shared;
   int tok0;        // token of the first row (-1: read tok_of)
-  uint32_t gmask;  // groups of 8 tokens the rows touch
 };
 
 // Entries of this launch: the access-order range the mode selects (+ the
@@ -165,7 +163,6 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int en
     out.shared = 0;
     const uint32_t tk = (uint32_t)v.w;
     out.tok0 = (tk >> 16) == 0xffffu ? -1 : (int)(tk & 0xffffu);
-    out.gmask = tk >> 16;
     return slot_ok && out.nrows > 0 && out.row0 >= 0 && out.row0 + out.nrows <= a.N * g.k;
   }
   if (a.with_shared && ent == nr) {
@@ -174,7 +171,6 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int en
     out.nrows = a.N;
     out.shared = 1;
     out.tok0 = 0;
-    out.gmask = 0xffffu;
     return a.N > 0;
   }
   return false;
@@ -238,22 +234,20 @@ MOE_DEV int xslot(int fmt, int t, int k4) {
   return (J * 2 + s) * 32 + 4 * t + q;
 }
 
-// One warp's 16 x 256 MXFP4 tile: acc[t] += W x_t for the token groups t < NG
-// set in gm, the codes dequantised once.  Codes: 128-byte rows, 16-byte
+// One warp's 16 x 256 MXFP4 tile: acc += W x.  Codes: 128-byte rows, 16-byte
 // chunk j of row r stored at chunk j ^ (r & 7) (128-byte swizzle).  Lane
 // (g = lane / 4, q = lane % 4) takes word q of chunk j (codes 8q..8q+7 of
 // block j) of rows g and g + 8; MMA step s uses codes 8q + 4s .. + 3.
-// Blocks j >= nvb lie past K and are skipped.  xb0, xb1: groups 0 and 1's
-// staged activations at this 256-K box.
-template <int NG>
-MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb0,
-                     const uint2* xb1, uint32_t gm, int nvb, int lane, float (&acc)[NG][4]) {
+// Blocks j >= nvb lie past K and are skipped.
+MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb, int nvb,
+                     int lane, float (&acc)[4]) {
   const int g = lane >> 2, q = lane & 3;
   // scale rows are only 4-byte aligned when a whole unit's rows are staged
   const uint2 sc0 = make_uint2(lds32(s0p), lds32(s0p + 4)), sc1 = make_uint2(lds32(s1p), lds32(s1p + 4));
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < nvb) {
+      const uint2 b0 = xb[(2 * j) * 32 + lane], b1 = xb[(2 * j + 1) * 32 + lane];
       const int co = ((j ^ g) << 4) + 4 * q;
       uint32_t f0[4], f1[4];
       e2m1x8_to_f16x8(lds32(cs + 128 * g + co), f0);
@@ -264,20 +258,13 @@ MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
       else if ((j & 3) == 1) { sg = e8m0_byte<1>(w0); sg8 = e8m0_byte<1>(w1); }
       else if ((j & 3) == 2) { sg = e8m0_byte<2>(w0); sg8 = e8m0_byte<2>(w1); }
       else { sg = e8m0_byte<3>(w0); sg8 = e8m0_byte<3>(w1); }
-#pragma unroll
-      for (int t = 0; t < NG; ++t) {
-        if ((gm >> t) & 1u) {
-          const uint2* xt = t == 0 ? xb0 : xb1;
-          const uint2 b0 = xt[(2 * j) * 32 + lane], b1 = xt[(2 * j + 1) * 32 + lane];
-          float d[4];
-          mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
-          mma16816_acc(d, f0[2], f1[2], f0[3], f1[3], b1);
-          acc[t][0] = fmaf(d[0], sg, acc[t][0]);
-          acc[t][1] = fmaf(d[1], sg, acc[t][1]);
-          acc[t][2] = fmaf(d[2], sg8, acc[t][2]);
-          acc[t][3] = fmaf(d[3], sg8, acc[t][3]);
-        }
-      }
+      float d[4];
+      mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
+      mma16816_acc(d, f0[2], f1[2], f0[3], f1[3], b1);
+      acc[0] = fmaf(d[0], sg, acc[0]);
+      acc[1] = fmaf(d[1], sg, acc[1]);
+      acc[2] = fmaf(d[2], sg8, acc[2]);
+      acc[3] = fmaf(d[3], sg8, acc[3]);
     }
   }
 }
@@ -285,14 +272,14 @@ MOE_DEV void tile_mx(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
 // NVFP4 tile: 16-code blocks, so each MMA must stay inside one.  Lane q takes
 // codes 4q..4q+3 of both blocks of chunk j (half q & 1 of words q / 2 and
 // 2 + q / 2); MMA step s covers block 2j + s.
-template <int NG>
-MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb0,
-                     const uint2* xb1, uint32_t gm, int nvb, int lane, float (&acc)[NG][4]) {
+MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb, int nvb,
+                     int lane, float (&acc)[4]) {
   const int g = lane >> 2, q = lane & 3;
   const uint32_t sel = (q & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (j < nvb) {
+      const uint2 b0 = xb[(2 * j) * 32 + lane], b1 = xb[(2 * j + 1) * 32 + lane];
       const int co = ((j ^ g) << 4) + 4 * (q >> 1);
       const uint8_t* r0 = cs + 128 * g + co;
       const uint8_t* r1 = cs + 128 * (g + 8) + co;
@@ -303,20 +290,13 @@ MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
       const uint32_t e1 = *reinterpret_cast<const uint16_t*>(s1p + 2 * j);
       const float sa0 = e4m3_to_f32(e0 & 0xffu), sb0 = e4m3_to_f32(e0 >> 8);
       const float sa1 = e4m3_to_f32(e1 & 0xffu), sb1 = e4m3_to_f32(e1 >> 8);
-#pragma unroll
-      for (int t = 0; t < NG; ++t) {
-        if ((gm >> t) & 1u) {
-          const uint2* xt = t == 0 ? xb0 : xb1;
-          const uint2 b0 = xt[(2 * j) * 32 + lane], b1 = xt[(2 * j + 1) * 32 + lane];
-          float d[4], e[4];
-          mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
-          mma16816(e, f0[2], f1[2], f0[3], f1[3], b1);
-          acc[t][0] = fmaf(d[0], sa0, fmaf(e[0], sb0, acc[t][0]));
-          acc[t][1] = fmaf(d[1], sa0, fmaf(e[1], sb0, acc[t][1]));
-          acc[t][2] = fmaf(d[2], sa1, fmaf(e[2], sb1, acc[t][2]));
-          acc[t][3] = fmaf(d[3], sa1, fmaf(e[3], sb1, acc[t][3]));
-        }
-      }
+      float d[4], e[4];
+      mma16816(d, f0[0], f1[0], f0[1], f1[1], b0);
+      mma16816(e, f0[2], f1[2], f0[3], f1[3], b1);
+      acc[0] = fmaf(d[0], sa0, fmaf(e[0], sb0, acc[0]));
+      acc[1] = fmaf(d[1], sa0, fmaf(e[1], sb0, acc[1]));
+      acc[2] = fmaf(d[2], sa1, fmaf(e[2], sb1, acc[2]));
+      acc[3] = fmaf(d[3], sa1, fmaf(e[3], sb1, acc[3]));
     }
   }
 }
@@ -341,8 +321,8 @@ MOE_DEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_f
 
 MOE_DEV float silu_mul(float a, float u) { return a / (1.0f + __expf(-a)) * u; }
 
-// Stage all N <= 16 tokens of the step (phase 1, `all` geometry) into the NG
-// group buffers at xs, as stage_block does for one group, with the per-token
+// Stage all N <= 8 tokens of the step (phase 1, `all` geometry) into the group
+// buffer at xs, as stage_block does for one entry's group, with the per-token
 // exponent computed here from x (the same rule as the router's: amax 2^-s in
 // [2^14, 2^15)); columns past N are zero.  x is final before the router
 // starts, so this runs before the programmatic wait.  By `nthr` threads
@@ -373,11 +353,9 @@ MOE_DEV void stage_all(const SG& p, int N, const __nv_bfloat16* __restrict__ x, 
     }
   }
   asm volatile("bar.sync %0, %1;" :: "r"(bar), "r"(nthr) : "memory");
-  const int k8n = p.K / 8, ntok = p.NG * kTG;
-  for (int it = tid; it < ntok * k8n; it += nthr) {
+  const int k8n = p.K / 8;
+  for (int it = tid; it < kTG * k8n; it += nthr) {
     const int t = it / k8n, k8 = it % k8n;
-    uint2* xg = xs + (size_t)(t / kTG) * 2 * p.K;   // one group: K x 8 tokens of f16
-    const int c = t % kTG;
     uint32_t o[4] = {0u, 0u, 0u, 0u};
     if (t < N) {
       const uint4 v = reinterpret_cast<const uint4*>(x + (size_t)t * p.K)[k8];
@@ -390,8 +368,8 @@ MOE_DEV void stage_all(const SG& p, int N, const __nv_bfloat16* __restrict__ x, 
         o[e] = *reinterpret_cast<const uint32_t*>(&hh);
       }
     }
-    xg[xslot(FMT, c, 2 * k8)] = make_uint2(o[0], o[1]);
-    xg[xslot(FMT, c, 2 * k8 + 1)] = make_uint2(o[2], o[3]);
+    xs[xslot(FMT, t, 2 * k8)] = make_uint2(o[0], o[1]);
+    xs[xslot(FMT, t, 2 * k8 + 1)] = make_uint2(o[2], o[3]);
   }
   asm volatile("bar.sync %0, %1;" :: "r"(bar), "r"(nthr) : "memory");
 }
@@ -591,7 +569,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     }
   } else if (warp < kCW) {
     // ------------------------------------------------------------ compute
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float* red = reinterpret_cast<float*>(S.base + p.off_red);
     const int bslot = warp >> 2, quarter = warp & 3, gq = lane >> 2;
     uint32_t n = 0, us = 0, bs = 0;
@@ -600,8 +578,6 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     while (cursor_next(cu, g, a, p, rr)) {
       const int xb = bs % p.XB;
       if (!ALL) wait_or_abort(&S.xfull[xb], (bs / p.XB) & 1, &s_abort, a.err);
-      // token groups this entry needs (all staged groups when its tokens are unknown)
-      const uint32_t gm = ALL ? (cu.en.gmask & ((1u << p.NG) - 1u)) : 1u;
       const uint2* xs = reinterpret_cast<const uint2*>(S.base + p.off_x + (size_t)xb * p.xbytes);
       for (int u = cu.ue0; u < cu.ue1; ++u) {
         for (int st = 0; st < p.NS; ++st, ++n) {
@@ -613,11 +589,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
             const uint8_t* cs = stg + (size_t)bslot * kBoxBytes + quarter * (16 * kBoxK / 2);
             const uint8_t* sc = stg + p.codes_bytes + (16 * quarter + gq) * p.srow + (p.smode ? bslot : kb) * p.SBB;
             const int nvb = min(8, (p.K - kb * kBoxK) / 32);
-            // 8 blocks x 2 steps x 32 lanes per box; group 1 (all tokens) one group further
-            const uint2* xk0 = xs + (size_t)kb * 512;
-            const uint2* xk1 = xk0 + 2 * (size_t)p.K;
-            if (FMT == MOE_MXFP4) tile_mx<2>(cs, sc, sc + 8 * p.srow, xk0, xk1, gm, nvb, lane, acc);
-            else tile_nv<2>(cs, sc, sc + 8 * p.srow, xk0, xk1, gm, nvb, lane, acc);
+            const uint2* xk = xs + (size_t)kb * 512;   // 8 blocks x 2 steps x 32 lanes
+            if (FMT == MOE_MXFP4) tile_mx(cs, sc, sc + 8 * p.srow, xk, nvb, lane, acc);
+            else tile_nv(cs, sc, sc + 8 * p.srow, xk, nvb, lane, acc);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -625,11 +599,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         // unit done: hand the partial sums to the epilogue
         const int r = us % p.RS;
         if (us >= (uint32_t)p.RS) wait_or_abort(&S.rempty[r], (us / p.RS - 1) & 1, &s_abort, a.err);
-        float4* rdst = reinterpret_cast<float4*>(red + (size_t)r * (p.rbytes / 4));
-        rdst[warp * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-        if (gm & 2u) rdst[kCW * 32 + warp * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+        reinterpret_cast<float4*>(red + (size_t)r * (p.rbytes / 4))[warp * 32 + lane] =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.rfull[r]);
         ++us;
@@ -686,10 +658,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         const float4* rs = reinterpret_cast<const float4*>(red + (size_t)r * (p.rbytes / 4));
         // warp w takes tokens w, w + kEW, ...; lane c takes columns c, c + 32 of the block
         for (int tk = ew_; ok && tk < nt; tk += kEW) {
-          // (group, column) of this row's token among the staged ones
-          const int tok = ALL ? stok[tk] : tk;
-          const int gg = ALL ? tok / kTG : 0, cc = ALL ? tok % kTG : tk;
-          const float sc = pow2i(ALL ? (&sexp[0][0])[tok] : sexp[xb][tk]) * ts;
+          // column of this row's token among the staged ones
+          const int cc = ALL ? stok[tk] : tk;
+          const float sc = pow2i(ALL ? sexp[0][cc] : sexp[xb][tk]) * ts;
           float mx = 0.f;
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
@@ -699,7 +670,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
             float s = 0.f;
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b) {
-              const float4 v = rs[gg * kCW * 32 + (b * 4 + qr) * 32 + lo];
+              const float4 v = rs[(b * 4 + qr) * 32 + lo];
               s += jj == 0 ? v.x : jj == 1 ? v.y : jj == 2 ? v.z : v.w;
             }
             const float val = s * sc;
@@ -729,7 +700,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
 }
 
 // N: tokens of the launch (phase 1 with N <= 8 stages every token once, one
-// group, when a ring of at least 3 stages still fits; 0 = the per-group
+// MMA group, when a ring of at least 3 stages still fits; 0 = the per-group
 // geometry).  With more tokens an entry's own group is staged per block:
 // staging two groups per launch cost more than it saved.
 SG make_sg(const Geo& g, int ph, int N) {
@@ -758,14 +729,10 @@ SG make_sg(const Geo& g, int ph, int N) {
   const int fixed = p.XB * p.xbytes + p.RS * p.rbytes + bars;
   p.D = std::min(kMaxD, (kSmemBudget - fixed) / p.stage_bytes);
   p.all = 0;
-  p.NG = 1;
   if (ph == 1 && N > 0 && N <= kTG) {
     SG q = p;
     q.all = 1;
-    q.NG = (N + kTG - 1) / kTG;
     q.XB = 1;
-    q.xbytes = q.NG * p.K * 2 * kTG;           // every group, one buffer
-    q.rbytes = q.NG * kCW * 32 * 16;           // one float4 per compute lane and group
     const int fq = q.xbytes + q.RS * q.rbytes + bars;
     q.D = std::min(kMaxD, (kSmemBudget - fq) / q.stage_bytes);
     if (q.D >= 3) p = q;

@@ -181,19 +181,16 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
     const bool ok = ex >= 0 && ex < E && sl >= 0 && sl < S && i - S < X;
     const int ps = !ok ? -1 : i < S ? sl : S + 1 + (i - S);
     const int row0 = offs && ok ? offs[ex] : 0, nrow = offs && ok ? counts[ex] : 0;
-    // first token and token groups of the access, from the per-warp token
-    // ballots of its expert (tokens 32 w + lane); unknown without them
+    // first token of the access, from the per-warp token ballots of its
+    // expert (tokens 32 w + lane); unknown without them
     uint32_t toks = 0xffff0000u;
     if (cm && ok && nrow > 0) {
       int t0 = -1;
-      uint32_t gm = 0;
-      for (int w = 0; w < perm::kPermWarps; ++w) {
+      for (int w = 0; w < perm::kPermWarps && t0 < 0; ++w) {
         const uint32_t b = cm[ex * perm::kPermWarps + w];
-        if (b && t0 < 0) t0 = 32 * w + __ffs(b) - 1;
-        for (int q = 0; q < 4; ++q)
-          if ((b >> (8 * q)) & 0xffu) gm |= 1u << min(4 * w + q, 15);
+        if (b) t0 = 32 * w + __ffs(b) - 1;
       }
-      toks = ((uint32_t)t0 & 0xffffu) | (gm << 16);
+      toks = (uint32_t)t0 & 0xffffu;
     }
     r_n[i] = make_int4(ps, row0, nrow, (int)toks);
     if (host_rec) {
