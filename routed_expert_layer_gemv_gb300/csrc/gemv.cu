@@ -756,7 +756,10 @@ cudaError_t launch_phase(const Geo& g, const GemvPlan* pl, const GemvArgs& a, co
     attr = true;
   }
   const long long units = (long long)n_ent_max * p.UE;
-  const int grid = (int)std::min<long long>(num_sms, units);
+  // phase 1 is launched while the one-CTA routing tail still holds an SM, and
+  // a CTA of this size cannot share it: leave that SM out rather than have
+  // one CTA start after the tail and finish last
+  const int grid = (int)std::min<long long>(PH == 1 ? std::max(1, num_sms - 1) : num_sms, units);
   if (grid <= 0) return cudaSuccess;
   const CUtensorMap& m0 = PH == 1 ? pl->w[0] : pl->w[2];
   const CUtensorMap& m1 = PH == 1 ? pl->w[1] : pl->w[2];
