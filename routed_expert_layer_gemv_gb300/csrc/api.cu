@@ -35,6 +35,7 @@
 using namespace moe;
 
 constexpr int kFillStreams = 1;   // one copy queue: more add no bandwidth on the host link
+constexpr size_t kDirectHostBytes = 256 * 1024;   // host x / y read and written in place up to this size
 constexpr int kMissChunks = 4;   // memcpy fills: the misses' expert FFN runs in up to this many chunks
 constexpr int kMissesPerChunk = 8;   // ... of at least this many misses each
 
@@ -228,8 +229,12 @@ void release(moe_layer* L) {
   L->ev_route = L->ev_fill = nullptr;
 }
 
-int pointer_kind(const void* p, bool* on_device, int device) {
+// Where p lives: device memory of `device` (*on_device), or host memory;
+// *mapped = the device address of pinned host memory the device can reach
+// through unified addressing (null for pageable memory).
+int pointer_kind(const void* p, bool* on_device, int device, const void** mapped) {
   cudaPointerAttributes a{};
+  *mapped = nullptr;
   cudaError_t e = cudaPointerGetAttributes(&a, p);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -241,6 +246,7 @@ int pointer_kind(const void* p, bool* on_device, int device) {
     *on_device = true;
   } else {
     *on_device = false;
+    if (a.type == cudaMemoryTypeHost) *mapped = a.devicePointer;
   }
   return MOE_OK;
 }
@@ -650,13 +656,24 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   if (!resident && !L->host_pool)
     return fail(L, MOE_ERR_NOT_INSTALLED, "not every expert is resident and no host pool is registered");
   bool x_dev = false, y_dev = false;
-  if (pointer_kind(x, &x_dev, L->device) || pointer_kind(y, &y_dev, L->device))
+  const void* x_map = nullptr;
+  const void* y_map = nullptr;
+  if (pointer_kind(x, &x_dev, L->device, &x_map) || pointer_kind(y, &y_dev, L->device, &y_map))
     return fail(L, MOE_ERR_ARG, "x or y is device memory of another device");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t xbytes = (size_t)N * g.d * 2;
   const __nv_bfloat16* xd = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* yd = static_cast<__nv_bfloat16*>(y);
-  if (!x_dev) {
+  // decode-sized batches in pinned host buffers go through unified
+  // addressing: a copy kernel stages x (no DMA set-up on the critical path)
+  // and the combine writes y straight into the host buffer
+  const bool small = !prefill && xbytes <= kDirectHostBytes;
+  const bool x_direct = !x_dev && small && x_map && reinterpret_cast<uintptr_t>(x_map) % 16 == 0;
+  const bool y_direct = !y_dev && small && y_map && reinterpret_cast<uintptr_t>(y_map) % 16 == 0;
+  if (x_direct) {
+    MOE_CUDA(L, launch_copy16(L->x_stage, x_map, xbytes, st));
+    xd = L->x_stage;
+  } else if (!x_dev) {
     MOE_CUDA(L, cudaMemcpyAsync(L->x_stage, x, xbytes, cudaMemcpyHostToDevice, st));
     xd = L->x_stage;
   } else if (reinterpret_cast<uintptr_t>(x) % 16) {
@@ -664,9 +681,10 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     MOE_CUDA(L, cudaMemcpyAsync(L->x_stage, x, xbytes, cudaMemcpyDeviceToDevice, st));
     xd = L->x_stage;
   }
-  if (!y_dev) yd = L->y_stage;
+  if (y_direct) yd = static_cast<__nv_bfloat16*>(const_cast<void*>(y_map));
+  else if (!y_dev) yd = L->y_stage;
 
-  L->launches = 0;
+  L->launches = x_direct ? 1 : 0;
   cudaEvent_t* pe = prof_begin(L, MOE_PROF_ROUTER, st);
   MOE_CUDA(L, launch_router(g, xd, N, L->Wr, L->Wr_hl, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
                             L->gates, L->xexp, L->rcounter, st));
@@ -855,7 +873,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   prof_end(pe, st);
   L->launches += 1;
   if (!y_dev) {
-    MOE_CUDA(L, cudaMemcpyAsync(y, yd, xbytes, cudaMemcpyDeviceToHost, st));
+    if (!y_direct) MOE_CUDA(L, cudaMemcpyAsync(y, yd, xbytes, cudaMemcpyDeviceToHost, st));
     MOE_CUDA(L, cudaStreamSynchronize(st));
   }
   if (info) {

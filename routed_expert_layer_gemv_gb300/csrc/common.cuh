@@ -203,6 +203,8 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
 // (access i >= S with i + S >= U) from its staging slot into that slot
 // Staged accesses in [max(S, a0), min(U, a1)) (a1 < 0: up to U); max_staged
 // bounds their number (grid size).
+// dst <- src (bytes a multiple of 16, 16-byte aligned; src may be mapped host memory)
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);
 cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int a0, int a1, int max_staged,
                                 uint8_t* slots, cudaStream_t st);
 // combine.cu

@@ -7,6 +7,8 @@
 // side streams), which follows the pages' decode path: misses are loaded into
 // the GPU's expert cache from host memory ("FreeToken：把 284B MoE 塞进游戏 PC",
 // zhichai.net, §二 "Decode" paragraph).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -64,7 +66,22 @@ stage_commit_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int
   copy_chunk(slots + (size_t)(S + 1 + (i - S)) * ebytes, slots + (size_t)sl * ebytes, ebytes, ch);
 }
 
+// dst <- src, bytes a multiple of 16, both 16-byte aligned (src may be host
+// memory reached through unified addressing).
+__global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n16) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  const size_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<size_t>((n16 + 255) / 256, 64);
+  copy16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses,
                              const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st) {

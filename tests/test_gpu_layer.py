@@ -219,6 +219,9 @@ def test_host_buffers_and_empty_batch():
     yp = torch.empty(20, spec.d_model, dtype=torch.bfloat16)          # pageable
     capi.moe_forward(L.h, xh, 20, yp, None, DEC)
     assert torch.equal(yp.view(torch.int16), y_dev.cpu().view(torch.int16))
+    xp = bf16_tensor(x, device=None)                                   # pageable x: staged copy
+    capi.moe_forward(L.h, xp, 20, yh, None, DEC)
+    assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
     info = capi.moe_forward(L.h, xh, 0, yh, None, DEC)                # N = 0: no-op
     assert info.n_tokens == 0
     L.close()
