@@ -37,7 +37,7 @@ using namespace moe;
 constexpr int kFillStreams = 1;   // one copy queue: more add no bandwidth on the host link
 constexpr size_t kDirectHostBytes = 256 * 1024;   // host x / y read and written in place up to this size
 constexpr int kMissChunks = 4;   // memcpy fills: the misses' expert FFN runs in up to this many chunks
-constexpr int kMissesPerChunk = 8;   // ... of at least this many misses each
+constexpr int kMissesPerChunk = 3;   // ... of at least this many misses each
 
 struct moe_layer {
   moe_layer_desc desc{};
