@@ -7,7 +7,7 @@
 //   caller stream: router -> permute -> LRU step -> [record copy to host]
 //                  -> expert GEMV over the hits (+ shared expert)
 //   host:          wait for the record, then for every miss at once:
-//   fill streams:  cudaMemcpyAsync pinned host expert -> its slot (first wave
+//   fill stream:   cudaMemcpyAsync pinned host expert -> its slot (first wave
 //                  of n_slots accesses) or a staging slot (later accesses,
 //                  whose LRU slots this step still reads)
 //   caller stream: wait for the fills -> expert GEMV over all misses
@@ -34,7 +34,6 @@
 
 using namespace moe;
 
-constexpr int kFillStreams = 1;   // one copy queue: more add no bandwidth on the host link
 constexpr size_t kDirectHostBytes = 256 * 1024;   // host x / y read and written in place up to this size
 constexpr int kMissChunks = 4;   // memcpy fills: the misses' expert FFN runs in up to this many chunks
 constexpr int kMissesPerChunk = 3;   // ... of at least this many misses each
@@ -94,7 +93,7 @@ struct moe_layer {
   size_t host_pool_bytes = 0;
   bool router_set = false;
   bool shared_set = false;
-  cudaStream_t fill[kFillStreams] = {};       // miss fills and the step record's copy to the host
+  cudaStream_t fill = nullptr;                // miss fills: one copy queue (more add no bandwidth on the host link)
   cudaEvent_t ev_chunk[kMissChunks] = {};     // the fills of each miss chunk have landed
   cudaEvent_t ev_route = nullptr, ev_fill = nullptr;
   int fill_mode = MOE_FILL_MEMCPY;
@@ -222,10 +221,8 @@ void release(moe_layer* L) {
     if (L->ev_chunk[i]) cudaEventDestroy(L->ev_chunk[i]);
     L->ev_chunk[i] = nullptr;
   }
-  for (int i = 0; i < kFillStreams; ++i) {
-    if (L->fill[i]) cudaStreamDestroy(L->fill[i]);
-    L->fill[i] = nullptr;
-  }
+  if (L->fill) cudaStreamDestroy(L->fill);
+  L->fill = nullptr;
   L->ev_route = L->ev_fill = nullptr;
 }
 
@@ -423,8 +420,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   }
   if (rc == MOE_OK) {
     bool sok = true;
-    for (int i = 0; i < kFillStreams; ++i)
-      sok = sok && cudaStreamCreateWithFlags(&L->fill[i], cudaStreamNonBlocking) == cudaSuccess;
+    sok = sok && cudaStreamCreateWithFlags(&L->fill, cudaStreamNonBlocking) == cudaSuccess;
     for (int i = 0; i < kMissChunks; ++i)
       sok = sok && cudaEventCreateWithFlags(&L->ev_chunk[i], cudaEventDisableTiming) == cudaSuccess;
     if (!sok ||
@@ -776,7 +772,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   const int max_staged = std::max(0, max_miss - g.S);
   bool any_miss = true, any_staged = max_staged > 0;
   if (dev_fill) {
-    cudaStream_t fs = L->fill[0];
+    cudaStream_t fs = L->fill;
     MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
     cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
     MOE_CUDA(L, launch_fill_copy(g, L->rec, max_miss, L->pool_dev, L->slots, fs));
@@ -809,7 +805,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       // landed, so its expert FFN starts while later fills still run.
       // a chunk pays one expert-FFN launch ramp, so only long miss lists are cut
       n_chunks = std::max(1, std::min(kMissChunks, (U - n_hit) / kMissesPerChunk));
-      cudaStream_t fs = L->fill[0];
+      cudaStream_t fs = L->fill;
       MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
       cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
       const int nm = U - n_hit;
