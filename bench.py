@@ -5,7 +5,9 @@ Workload (default): the decode layer of a Qwen3-35B-A3B-shaped model --
 d_model 2048, 128 experts, top-8, d_ff 768, MXFP4 weights, 47 cache slots
 (37% of the experts) filled from pinned host memory -- run at 1, 4 and 16
 tokens per step on AR(1) hidden states (rho 0.9).  A step is one moe_forward:
-router, permutation, LRU update, miss fills, expert FFN, combine.
+router, permutation, LRU update, miss fills, expert FFN, combine.  Misses are
+filled by the library's default, a copy kernel on 12 SMs the expert GEMV leaves
+free; the copy-engine and GPU-read-record fills are timed beside it per batch.
 
 Timing: W warm-up steps, then K timed steps per batch size, each bracketed by
 CUDA events on the launching stream; the L2 is flushed (a 512 MiB write)
@@ -164,7 +166,8 @@ def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile, fi
     x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
     xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
     L = build_layer(spec, seed, batch)
-    capi.moe_set_fill_mode(L.h, capi.MOE_FILL_MEMCPY if fill is None else fill)
+    if fill is not None:
+        capi.moe_set_fill_mode(L.h, fill)
     y = torch.empty(batch, spec.d_model, dtype=torch.bfloat16, device="cuda")
     with torch.cuda.stream(st):
         for t in range(W):
@@ -187,13 +190,15 @@ def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile, fi
             fill_b += info.fill_bytes
             ffn_bytes += gateup_bytes(spec, L.layout, info.n_distinct, batch)
     torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms)
     prof = capi.moe_profile_read(L.h)
     capi.moe_profile(L.h, False)
     stats1 = capi.moe_stats(L.h)
     L.close()
     d_misses, d_distinct = stats1[3] - stats0[3], stats1[1] - stats0[1]
-    return dict(batch=batch, steps=K, ms=ms, tokens=K * batch, launches=launches,
+    return dict(batch=batch, steps=K, ms=ms, step_ms_p50=statistics.median(step_ms), tokens=K * batch,
+                launches=launches,
                 misses=d_misses, distinct=d_distinct, fill_bytes=fill_b, prof=prof,
                 gateup_bytes=ffn_bytes)
 
@@ -385,6 +390,8 @@ def main():
     pruns = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, True) for b in batches]
     druns = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False, capi.MOE_FILL_DEVICE)
              for b in batches]
+    mruns = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False, capi.MOE_FILL_MEMCPY)
+             for b in batches]
     e2e_runs = [run_decode_e2e(args, b, torch, capi, wl, build_layer, flush) for b in batches]
 
     ms = sum(r["ms"] for r in runs)
@@ -415,16 +422,18 @@ def main():
             "bytes_per_launch": g_bytes / max(g_n, 1), "ms_per_launch": g_ms / max(g_n, 1)}
 
     per_batch = {}
-    for r, e, pr, dr in zip(runs, e2e_runs, pruns, druns):
+    for r, e, pr, dr, mr in zip(runs, e2e_runs, pruns, druns, mruns):
         p = pr["prof"]
         per_batch[str(r["batch"])] = {
             "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
             "e2e_tokens_per_s": e["tokens"] / e["s"],
             "ms_per_step": r["ms"] / r["steps"],
+            "ms_per_step_median": r["step_ms_p50"],
             "miss_rate": r["misses"] / max(1, r["distinct"]),
             "fill_GB_per_s": r["fill_bytes"] / max(1e-9, p["fill"][0] / 1000.0) / 1e9 if p["fill"][0] else None,
             "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
             "device_fill_tokens_per_s": dr["tokens"] / (dr["ms"] / 1000.0),
+            "memcpy_fill_tokens_per_s": mr["tokens"] / (mr["ms"] / 1000.0),
         }
     prefill = None
     if not args.no_prefill:
@@ -444,6 +453,9 @@ def main():
         "data": "synthetic (seeded AR(1) hidden states, random FP4 weights)",
         "config": {"workload": "decode_35b_a3b_d2048_e128_top8_f768_mxfp4_s47",
                    "batches": batches, "l2": "flushed (512 MiB write) between timed steps",
+                   "fill": "copy kernel on 12 reserved SMs (MOE_FILL_KERNEL, the library default); "
+                           "per_batch also gives the copy-engine (MOE_FILL_MEMCPY) and "
+                           "GPU-read-record (MOE_FILL_DEVICE) variants",
                    "timing": "value from a pass without per-kernel events; kernel times and "
                              "roofline from a second, instrumented pass of the same steps",
                    "parallelism": "replicas" if ws > 1 else "single GPU",

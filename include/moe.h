@@ -184,7 +184,11 @@ int moe_lru_set_state(moe_layer_t layer, const int* expert_of_slot,
 int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
                 int regime, moe_forward_info* info);
 
-/* How misses reach their slots.  MOE_FILL_MEMCPY (default): the host reads
+/* How misses reach their slots.  Registering the host pool selects
+ * MOE_FILL_KERNEL when the device can address the pool (pinned memory under
+ * unified addressing) and MOE_FILL_MEMCPY otherwise, unless a mode was set
+ * here before; a pool the device cannot address always turns the mode to
+ * MOE_FILL_MEMCPY.  MOE_FILL_MEMCPY: the host reads
  * the step's routing record and issues cudaMemcpyAsync from the pinned pool on
  * the layer's fill stream (a run of consecutive experts bound for consecutive
  * slots is one copy) while the hits compute; a long miss list runs its expert
@@ -193,9 +197,19 @@ int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
  * and pulls the missed experts from the pinned pool itself (unified
  * addressing over the host link), so moe_forward never waits on the host;
  * moe_forward_info then reports n_distinct / n_hits = -1 (see moe_stats).
- * MOE_ERR_STATE if the registered pool is not device-addressable. */
+ * MOE_FILL_KERNEL: the copies are made by a copy kernel on 12 SMs that the
+ * decode expert GEMV leaves free, queued on the fill stream (created with the
+ * highest stream priority) behind the routing, one launch per chunk of the
+ * miss list, each reading its part of the list from the record on the device;
+ * the host still reads the record to launch the misses' expert FFN, so the
+ * copies start as soon as the routing ends and pay no per-copy cost of the
+ * copy engine.  The prefill regime fills with cudaMemcpyAsync in this mode,
+ * since its GEMM takes every SM.
+ * MOE_ERR_STATE if the registered pool is not device-addressable (DEVICE and
+ * KERNEL). */
 #define MOE_FILL_MEMCPY 0
 #define MOE_FILL_DEVICE 1
+#define MOE_FILL_KERNEL 2
 int moe_set_fill_mode(moe_layer_t layer, int mode);
 
 /* Totals since create, accumulated on the device by the LRU step of every

@@ -96,7 +96,8 @@ struct moe_layer {
   cudaStream_t fill = nullptr;                // miss fills: one copy queue (more add no bandwidth on the host link)
   cudaEvent_t ev_chunk[kMissChunks] = {};     // the fills of each miss chunk have landed
   cudaEvent_t ev_route = nullptr, ev_fill = nullptr;
-  int fill_mode = MOE_FILL_MEMCPY;
+  int fill_mode = MOE_FILL_MEMCPY;    // set by the pool's registration unless the caller chose one
+  bool fill_mode_chosen = false;
   const uint8_t* pool_dev = nullptr;          // device address of the host pool
   unsigned long long* stats = nullptr;        // steps, distinct, hits, misses
   std::vector<int> mirror;   // expert per slot as far as the host knows
@@ -420,7 +421,11 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   }
   if (rc == MOE_OK) {
     bool sok = true;
-    sok = sok && cudaStreamCreateWithFlags(&L->fill, cudaStreamNonBlocking) == cudaSuccess;
+    // the fill stream has the highest priority: a fill kernel's CTAs are
+    // dispatched before expert-GEMV CTAs waiting for SMs
+    int prio_lo = 0, prio_hi = 0;
+    sok = sok && cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi) == cudaSuccess;
+    sok = sok && cudaStreamCreateWithPriority(&L->fill, cudaStreamNonBlocking, prio_hi) == cudaSuccess;
     for (int i = 0; i < kMissChunks; ++i)
       sok = sok && cudaEventCreateWithFlags(&L->ev_chunk[i], cudaEventDisableTiming) == cudaSuccess;
     if (!sok ||
@@ -496,6 +501,10 @@ int moe_register_host_experts(moe_layer_t L, const void* pool, size_t bytes) {
     cudaGetLastError();
     L->pool_dev = nullptr;   // device-driven fills unavailable for this pool
   }
+  // the copy kernel on reserved SMs by default; the copy engine when the
+  // device cannot address the pool
+  if (!L->pool_dev) L->fill_mode = MOE_FILL_MEMCPY;
+  else if (!L->fill_mode_chosen) L->fill_mode = MOE_FILL_KERNEL;
   return MOE_OK;
 }
 
@@ -735,14 +744,20 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     prof_end(pe, st);
     L->launches += 1;
   }
-  auto gemv = [&](int n_ent) -> int {
-    cudaEvent_t ev[4];
+  // SM fills (decode): kFillSms SMs copy the misses, the expert GEMV takes
+  // the others, and the hits' phase 2 is launched after the host has read the
+  // record, so that its waiting CTAs cannot take the SMs the fills need
+  const bool sm_fill = !resident && !prefill && L->fill_mode == MOE_FILL_KERNEL;
+  const int gemv_sms = sm_fill ? L->num_sms - kFillSms : L->num_sms;
+  auto gemv = [&](int n_ent, int phases) -> int {
+    cudaEvent_t ev[4] = {};
     const bool room = L->prof_used + 4 <= L->prof_pool.size();
-    cudaEvent_t* p1 = room ? prof_begin(L, MOE_PROF_GATEUP, st) : nullptr;
-    cudaEvent_t* p2 = p1 ? prof_begin(L, MOE_PROF_DOWN, st) : nullptr;
+    cudaEvent_t* p1 = room && (phases & 1) ? prof_begin(L, MOE_PROF_GATEUP, st) : nullptr;
+    cudaEvent_t* p2 = room && (phases & 2) ? prof_begin(L, MOE_PROF_DOWN, st) : nullptr;
     const cudaEvent_t* evp = nullptr;
-    if (p1 && p2) {
-      ev[0] = p1[0]; ev[1] = p1[1]; ev[2] = p2[0]; ev[3] = p2[1];
+    if ((p1 || p2) && (p1 || !(phases & 1)) && (p2 || !(phases & 2))) {
+      if (p1) { ev[0] = p1[0]; ev[1] = p1[1]; }
+      if (p2) { ev[2] = p2[0]; ev[3] = p2[1]; }
       evp = ev;
     }
     cudaError_t ce;
@@ -752,14 +767,30 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
                                 L->hq_scales, L->O, gx, gh, L->err_dev, L->num_sms, st, evp);
       L->launches += 3;
     } else {
-      ce = launch_gemv_decode(g, L->gplan, a, xd, L->xexp, L->h, L->O, n_ent, L->num_sms, st, evp);
-      L->launches += 2;
+      ce = launch_gemv_decode(g, L->gplan, a, xd, L->xexp, L->h, L->O, n_ent, gemv_sms, st, evp, phases);
+      L->launches += (phases & 1) + (phases >> 1 & 1);
     }
     if (ce != cudaSuccess) return cuda_fail(L, ce, prefill ? "launch_prefill_gemms" : "launch_gemv_decode");
     return MOE_OK;
   };
-  int grc = gemv(cap + (g.has_shared ? 1 : 0));
+  int grc = gemv(cap + (g.has_shared ? 1 : 0), sm_fill ? 1 : 3);
   if (grc) return grc;
+  if (sm_fill) {
+    // every fill chunk a step can have is queued behind the routing (after the
+    // hits' phase 1, whose early start must not wait for these launches); each
+    // finds its part of the miss list in the record on the device, so the
+    // copies start when the routing ends, not after the host has read it
+    const int max_pre = std::max(1, std::min(kMissChunks, std::min(g.E, N * g.k) / kMissesPerChunk));
+    cudaStream_t fs = L->fill;
+    MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
+    cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
+    for (int c = 0; c < max_pre; ++c) {
+      MOE_CUDA(L, launch_fill_sm(g, L->rec, c, kMissChunks, kMissesPerChunk, L->pool_dev, L->slots, fs));
+      MOE_CUDA(L, cudaEventRecord(L->ev_chunk[c], fs));
+    }
+    prof_end(pf, fs);
+    L->launches += max_pre;
+  }
 
   // Misses.  Every fill starts as soon as the routing is known: first-wave
   // misses go straight into their (free or stale) LRU slots, later ones into
@@ -799,12 +830,17 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     any_miss = n_hit < U;
     any_staged = U > g.S;
     if (any_miss) {
-      // One copy engine queue in access order (more queues add no bandwidth
-      // on this link): consecutive experts bound for consecutive slots go as
-      // one copy, and each chunk of the misses records when its copies have
-      // landed, so its expert FFN starts while later fills still run.
-      // a chunk pays one expert-FFN launch ramp, so only long miss lists are cut
+      // the misses' expert FFN runs in chunks, each once its own fills have
+      // landed, while later fills still run; a chunk pays one expert-FFN
+      // launch ramp, so only long miss lists are cut
       n_chunks = std::max(1, std::min(kMissChunks, (U - n_hit) / kMissesPerChunk));
+    }
+    if (any_miss && sm_fill) {
+      fill_bytes = (size_t)(U - n_hit) * g.ebytes;   // the copy kernels were queued behind the routing
+    } else if (any_miss) {
+      // one copy engine queue in access order (more queues add no bandwidth
+      // on this link): consecutive experts bound for consecutive slots go as
+      // one copy, and each chunk records when its copies have landed
       cudaStream_t fs = L->fill;
       MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
       cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
@@ -827,6 +863,10 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     }
     mirror_apply(L, r);
   }
+  if (sm_fill) {
+    grc = gemv(cap + (g.has_shared ? 1 : 0), 2);
+    if (grc) return grc;
+  }
   if (!resident && any_miss) {
     a.mode = kRangeMisses;
     a.with_shared = 0;
@@ -840,7 +880,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
         MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[c], 0));
         a.chunk = c;
         const int c0 = n_hit + (int)((long long)nm * c / n_chunks), c1 = n_hit + (int)((long long)nm * (c + 1) / n_chunks);
-        grc = gemv(c1 - c0);
+        grc = gemv(c1 - c0, 3);
         if (grc) return grc;
         const int f0 = std::max(c0, std::max(g.S, U - g.S));   // staged and final
         if (c1 > f0) {
@@ -854,7 +894,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     } else {
       // one launch over every miss once the last copy (one queue, in order) has landed
       if (n_chunks > 0) MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[n_chunks - 1], 0));
-      grc = gemv(max_miss);
+      grc = gemv(max_miss, 3);
       if (grc) return grc;
     }
     if (any_staged) {
@@ -887,10 +927,12 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
 
 int moe_set_fill_mode(moe_layer_t L, int mode) {
   if (!L) return MOE_ERR_ARG;
-  if (mode != MOE_FILL_MEMCPY && mode != MOE_FILL_DEVICE) return fail(L, MOE_ERR_ARG, "unknown fill mode %d", mode);
-  if (mode == MOE_FILL_DEVICE && !L->pool_dev)
-    return fail(L, MOE_ERR_STATE, "device fills need a registered pinned host pool the device can address");
+  if (mode != MOE_FILL_MEMCPY && mode != MOE_FILL_DEVICE && mode != MOE_FILL_KERNEL)
+    return fail(L, MOE_ERR_ARG, "unknown fill mode %d", mode);
+  if (mode != MOE_FILL_MEMCPY && !L->pool_dev)
+    return fail(L, MOE_ERR_STATE, "copy-kernel fills need a registered pinned host pool the device can address");
   L->fill_mode = mode;
+  L->fill_mode_chosen = true;
   return MOE_OK;
 }
 

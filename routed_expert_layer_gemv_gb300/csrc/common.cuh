@@ -173,10 +173,12 @@ void gemv_plan_destroy(GemvPlan* pl);
 bool gemv_plan_ready(const GemvPlan* pl);
 // x must be 16-byte aligned; h holds 2 * d_ff floats per row (phase 1
 // writes W_g x and W_u x, phase 2 forms SiLU(a) * u from them).  ev (may be
-// null): 4 events recorded before/after phase 1 and phase 2
+// null): 4 events recorded before/after phase 1 and phase 2.  phases: 1, 2 or
+// 3 (both) -- the phases a call launches; num_sms: the SMs the grids may use
 cudaError_t launch_gemv_decode(const Geo& g, const GemvPlan* pl, const GemvArgs& a,
                                const __nv_bfloat16* x, const int* xexp, float* h, float* O,
-                               int n_ent_max, int num_sms, cudaStream_t st, const cudaEvent_t* ev);
+                               int n_ent_max, int num_sms, cudaStream_t st, const cudaEvent_t* ev,
+                               int phases);
 // prefill.cu
 struct PrefillPlan;
 bool prefill_shape_ok(const Geo& g);
@@ -199,6 +201,12 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
 // into the slot access_slot() names
 cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses,
                              const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
+// the same copy by kFillSms CTAs, one per SM, for chunk `chunk` of the miss
+// list cut into max(1, min(max_chunks, misses / per_chunk)) chunks; the decode
+// expert GEMV leaves those SMs free
+constexpr int kFillSms = 12;
+cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, int max_chunks, int per_chunk,
+                           const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
 // copy each staged miss that still owns its LRU slot at the end of the step
 // (access i >= S with i + S >= U) from its staging slot into that slot
 // Staged accesses in [max(S, a0), min(U, a1)) (a1 < 0: up to U); max_staged

@@ -66,6 +66,57 @@ stage_commit_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int
   copy_chunk(slots + (size_t)(S + 1 + (i - S)) * ebytes, slots + (size_t)sl * ebytes, ebytes, ch);
 }
 
+// SM fill of one chunk of the miss list: kFillSms CTAs, one per SM (the
+// shared memory they reserve, more than half an SM's, keeps two off one SM and
+// keeps the expert GEMV, which takes nearly all of it, off theirs), copy the
+// chunk's misses from the pinned host pool to access_slot().  The m = U - n_hit
+// misses form nch = max(1, min(max_chunks, m / per_chunk)) chunks, chunk c
+// being accesses [n_hit + m c / nch, n_hit + m (c + 1) / nch) -- the split the
+// host makes from its copy of the record -- and a launch for c >= nch copies
+// nothing.  Each expert is cut into pieces of kFillPiece bytes dealt
+// round-robin to the CTAs; a piece is one load of kFillSmUnroll x 16 bytes per
+// thread, all in flight before the stores.
+constexpr int kFillSmThreads = 1024;
+constexpr int kFillSmUnroll = 8;
+constexpr size_t kFillPiece = (size_t)kFillSmThreads * kFillSmUnroll * 16;
+constexpr int kFillSmSmem = 120 * 1024;
+
+__global__ void __launch_bounds__(kFillSmThreads, 1)
+fill_sm_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int chunk, int max_chunks,
+               int per_chunk, const uint8_t* __restrict__ pool, uint8_t* __restrict__ slots, size_t ebytes) {
+  const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
+  const int m = U - nh;
+  const int nch = max(1, min(max_chunks, m / per_chunk));
+  if (chunk >= nch) return;
+  const int i0 = nh + (int)((long long)m * chunk / nch);
+  const int i1 = min(nh + (int)((long long)m * (chunk + 1) / nch), S + X);
+  if (i1 <= i0) return;
+  const int* as = rec_slot(const_cast<StepRecord*>(rec), E);
+  const int* ae = rec_expert(const_cast<StepRecord*>(rec));
+  const long long P = (long long)((ebytes + kFillPiece - 1) / kFillPiece);
+  const long long total = (long long)(i1 - i0) * P;
+  for (long long q = blockIdx.x; q < total; q += gridDim.x) {
+    const int i = i0 + (int)(q / P);
+    const size_t off = (size_t)(q % P) * kFillPiece;
+    const int ex = ae[i];
+    if (ex < 0 || ex >= E || as[i] < 0 || as[i] >= S) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(pool + (size_t)ex * ebytes + off);
+    uint4* dst = reinterpret_cast<uint4*>(slots + (size_t)access_slot(as, S, i) * ebytes + off);
+    const int n16 = (int)(min(kFillPiece, ebytes - off) / 16);
+    uint4 r[kFillSmUnroll];
+#pragma unroll
+    for (int u = 0; u < kFillSmUnroll; ++u) {
+      const int v = threadIdx.x + u * kFillSmThreads;
+      if (v < n16) r[u] = src[v];
+    }
+#pragma unroll
+    for (int u = 0; u < kFillSmUnroll; ++u) {
+      const int v = threadIdx.x + u * kFillSmThreads;
+      if (v < n16) dst[v] = r[u];
+    }
+  }
+}
+
 // dst <- src, bytes a multiple of 16, both 16-byte aligned (src may be host
 // memory reached through unified addressing).
 __global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n16) {
@@ -90,6 +141,19 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
   if (grid <= 0) return cudaSuccess;
   fill_copy_kernel<<<(unsigned)grid, kFillThreads, 0, st>>>(rec, g.E, g.S, g.X, pool_dev, slots, g.ebytes,
                                                             chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, int max_chunks, int per_chunk,
+                           const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(fill_sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFillSmSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  fill_sm_kernel<<<kFillSms, kFillSmThreads, kFillSmSmem, st>>>(rec, g.E, g.S, g.X, chunk, max_chunks,
+                                                               per_chunk, pool_dev, slots, g.ebytes);
   return cudaGetLastError();
 }
 

@@ -772,15 +772,21 @@ cudaError_t launch_phase(const Geo& g, const GemvPlan* pl, const GemvArgs& a, co
 template <int FMT>
 cudaError_t launch_fmt(const Geo& g, const GemvPlan* pl, const GemvArgs& a, const __nv_bfloat16* x,
                        const int* xexp, float* h, float* O, int n_ent_max, int num_sms,
-                       cudaStream_t st, const cudaEvent_t* ev) {
-  const SG p1 = make_sg(g, 1, a.N), p2 = make_sg(g, 2, a.N);
-  if (ev) cudaEventRecord(ev[0], st);
-  cudaError_t e = launch_phase<FMT, 1>(g, pl, a, p1, x, xexp, h, O, n_ent_max, num_sms, st);
-  if (ev) cudaEventRecord(ev[1], st);
-  if (e != cudaSuccess) return e;
-  if (ev) cudaEventRecord(ev[2], st);
-  e = launch_phase<FMT, 2>(g, pl, a, p2, x, xexp, h, O, n_ent_max, num_sms, st);
-  if (ev) cudaEventRecord(ev[3], st);
+                       cudaStream_t st, const cudaEvent_t* ev, int phases) {
+  cudaError_t e = cudaSuccess;
+  if (phases & 1) {
+    const SG p1 = make_sg(g, 1, a.N);
+    if (ev) cudaEventRecord(ev[0], st);
+    e = launch_phase<FMT, 1>(g, pl, a, p1, x, xexp, h, O, n_ent_max, num_sms, st);
+    if (ev) cudaEventRecord(ev[1], st);
+    if (e != cudaSuccess) return e;
+  }
+  if (phases & 2) {
+    const SG p2 = make_sg(g, 2, a.N);
+    if (ev) cudaEventRecord(ev[2], st);
+    e = launch_phase<FMT, 2>(g, pl, a, p2, x, xexp, h, O, n_ent_max, num_sms, st);
+    if (ev) cudaEventRecord(ev[3], st);
+  }
   return e;
 }
 
@@ -867,10 +873,11 @@ bool gemv_plan_ready(const GemvPlan* pl) { return pl && pl->ready; }
 
 cudaError_t launch_gemv_decode(const Geo& g, const GemvPlan* pl, const GemvArgs& a,
                                const __nv_bfloat16* x, const int* xexp, float* h, float* O,
-                               int n_ent_max, int num_sms, cudaStream_t st, const cudaEvent_t* ev) {
+                               int n_ent_max, int num_sms, cudaStream_t st, const cudaEvent_t* ev,
+                               int phases) {
   if (g.fmt == MOE_MXFP4)
-    return launch_fmt<MOE_MXFP4>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev);
-  return launch_fmt<MOE_NVFP4>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev);
+    return launch_fmt<MOE_MXFP4>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev, phases);
+  return launch_fmt<MOE_NVFP4>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev, phases);
 }
 
 }  // namespace moe

@@ -68,7 +68,7 @@ def _decode_run(spec, seed, batch, steps, check_every=1, fill=capi.MOE_FILL_MEMC
         ref, idx, _ = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
         acc = T.step(idx.reshape(-1))
         n_miss = sum(1 for a in acc if not a[2])
-        if fill == capi.MOE_FILL_MEMCPY:
+        if fill in (capi.MOE_FILL_MEMCPY, capi.MOE_FILL_KERNEL):
             assert info.host_synced == 1
             assert info.n_distinct == len(acc)
             assert info.n_misses == n_miss
@@ -109,15 +109,25 @@ def test_decode_284b_shape_shared_and_waves():
     assert waves >= 2
 
 
-@pytest.mark.parametrize("batch,steps", [(4, 6), (16, 3)])
-def test_decode_device_fill(batch, steps):
-    # misses pulled from the pinned pool by a copy kernel: no host wait per step
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL])
+@pytest.mark.parametrize("batch,steps", [(1, 8), (4, 6), (16, 3)])
+def test_decode_copy_kernel_fill(batch, steps, fill):
+    # misses pulled from the pinned pool by a copy kernel: DEVICE reads the
+    # routing record on the GPU (no host wait), KERNEL on reserved SMs after
+    # the host read it (chunked at batch 16)
     spec = wl.DECODE_35B.layer
-    miss, u, waves = _decode_run(spec, 7, batch, steps, fill=capi.MOE_FILL_DEVICE)
+    miss, u, waves = _decode_run(spec, 7, batch, steps, fill=fill)
     assert miss > 0
 
 
-@pytest.mark.parametrize("fill", [capi.MOE_FILL_MEMCPY, capi.MOE_FILL_DEVICE])
+def test_decode_284b_shape_kernel_fill():
+    # shared expert, d_model 4096 MXFP4 experts, more distinct experts than slots
+    spec = wl.DECODE_284B.layer
+    miss, u, waves = _decode_run(spec, 5, 8, 3, fill=capi.MOE_FILL_KERNEL)
+    assert waves >= 2
+
+
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_MEMCPY, capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL])
 def test_staged_misses_land_in_their_lru_slots(fill):
     # more distinct experts per step than slots: misses past the first wave are
     # filled into staging slots and committed afterwards; every LRU slot must
@@ -154,18 +164,20 @@ def test_staged_misses_land_in_their_lru_slots(fill):
     L.close()
 
 
-def test_prefill_device_fill_waves():
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL])
+def test_prefill_copy_kernel_fill_waves(fill):
+    # KERNEL mode fills prefill misses with the copy engine (the GEMM holds every SM)
     spec = small_spec(E=24, k=3, d_model=512, d_ff=256, n_slots=5, fmt="nvfp4", has_shared=True,
                       has_bias=True)
     seed, N = 31, 96
     experts = CachedExperts(spec, seed)
     L = build_layer(spec, seed, N, experts_fn=experts)
-    capi.moe_set_fill_mode(L.h, capi.MOE_FILL_DEVICE)
+    capi.moe_set_fill_mode(L.h, fill)
     O = oracle_layer(spec, seed, experts)
     for step in range(2):
         x = _tokens(spec, seed + step, N)
         y, info = L.forward(bf16_tensor(x), regime=capi.MOE_REGIME_PREFILL)
-        assert info.host_synced == 0
+        assert info.host_synced == (0 if fill == capi.MOE_FILL_DEVICE else 1)
         ref, _, _ = O.forward(wl.bf16_bits_to_f64(x), "prefill")
         assert_close_layer(y, ref, "prefill device fill step %d" % step)
     L.close()
