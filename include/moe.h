@@ -185,7 +185,7 @@ int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
                 int regime, moe_forward_info* info);
 
 /* How misses reach their slots.  Registering the host pool selects
- * MOE_FILL_KERNEL when the device can address the pool (pinned memory under
+ * MOE_FILL_AUTO when the device can address the pool (pinned memory under
  * unified addressing) and MOE_FILL_MEMCPY otherwise, unless a mode was set
  * here before; a pool the device cannot address always turns the mode to
  * MOE_FILL_MEMCPY.  MOE_FILL_MEMCPY: the host reads
@@ -205,11 +205,21 @@ int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
  * copies start as soon as the routing ends and pay no per-copy cost of the
  * copy engine.  The prefill regime fills with cudaMemcpyAsync in this mode,
  * since its GEMM takes every SM.
- * MOE_ERR_STATE if the registered pool is not device-addressable (DEVICE and
- * KERNEL). */
+ * MOE_FILL_FUSED: no separate copy: one decode expert-FFN launch covers the
+ * step's hits and misses, reading each miss's weights from the pinned pool
+ * over the host link (the pool must be device-addressable) and writing them
+ * on to the miss's slot as it computes; the host never waits (as with
+ * MOE_FILL_DEVICE, moe_forward_info reports -1 counts).  The prefill regime
+ * fills with cudaMemcpyAsync in this mode.
+ * MOE_FILL_AUTO: per decode call, MOE_FILL_FUSED while min(E, N k) <= n_slots
+ * (no access can need a staging slot), else MOE_FILL_KERNEL.
+ * MOE_ERR_STATE if the registered pool is not device-addressable (every mode
+ * but MOE_FILL_MEMCPY). */
 #define MOE_FILL_MEMCPY 0
 #define MOE_FILL_DEVICE 1
 #define MOE_FILL_KERNEL 2
+#define MOE_FILL_FUSED 3
+#define MOE_FILL_AUTO 4
 int moe_set_fill_mode(moe_layer_t layer, int mode);
 
 /* Totals since create, accumulated on the device by the LRU step of every

@@ -34,6 +34,8 @@ MOE_PROF_NAMES = ["router", "permute", "lru", "gateup", "down", "combine", "fill
 MOE_FILL_MEMCPY = 0
 MOE_FILL_DEVICE = 1
 MOE_FILL_KERNEL = 2
+MOE_FILL_FUSED = 3
+MOE_FILL_AUTO = 4
 
 MOE_REGIME_AUTO = 0
 MOE_REGIME_DECODE = 1

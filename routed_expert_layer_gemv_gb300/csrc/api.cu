@@ -501,10 +501,10 @@ int moe_register_host_experts(moe_layer_t L, const void* pool, size_t bytes) {
     cudaGetLastError();
     L->pool_dev = nullptr;   // device-driven fills unavailable for this pool
   }
-  // the copy kernel on reserved SMs by default; the copy engine when the
-  // device cannot address the pool
+  // the automatic choice by default; the copy engine when the device cannot
+  // address the pool
   if (!L->pool_dev) L->fill_mode = MOE_FILL_MEMCPY;
-  else if (!L->fill_mode_chosen) L->fill_mode = MOE_FILL_KERNEL;
+  else if (!L->fill_mode_chosen) L->fill_mode = MOE_FILL_AUTO;
   return MOE_OK;
 }
 
@@ -697,7 +697,15 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   L->launches += N <= 64 ? 1 : 2;
   // memcpy fills: the LRU kernel also writes the step record into mapped
   // pinned host memory, sequence number last, and the host polls it
-  const bool host_poll = !resident && L->fill_mode != MOE_FILL_DEVICE;
+  // the automatic choice: fused fills while no access of the step can need a
+  // staging slot (then there is nothing to commit), SM-copy fills beyond
+  int fmode = L->fill_mode;
+  if (fmode == MOE_FILL_AUTO) fmode = std::min(g.E, N * g.k) <= g.S ? MOE_FILL_FUSED : MOE_FILL_KERNEL;
+  // fused fills (decode): one expert-FFN launch covers every access and reads
+  // the misses' weights from the host pool itself, writing them on to their
+  // slots, so no separate copy and no host round trip
+  const bool fused = !resident && !prefill && fmode == MOE_FILL_FUSED;
+  const bool host_poll = !resident && fmode != MOE_FILL_DEVICE && !fused;
   StepRecord* hrec = host_poll ? L->rec_host_dev : nullptr;
   const unsigned long long seq = host_poll ? ++L->step_seq : 0ull;
   if (N <= 128) {
@@ -720,7 +728,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     prof_end(pe, st);
     L->launches += 1;
   }
-  const bool dev_fill = !resident && L->fill_mode == MOE_FILL_DEVICE;
+  const bool dev_fill = !resident && fmode == MOE_FILL_DEVICE;
   if (!resident) MOE_CUDA(L, cudaEventRecord(L->ev_route, st));
   GemvArgs a{};
   a.slots = L->slots;
@@ -729,7 +737,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   a.offsets = L->offsets;
   a.tok_of = L->tok_of;
   a.N = N;
-  a.mode = kRangeHits;
+  a.mode = fused ? kRangeAll : kRangeHits;
+  a.host_pool = fused ? L->pool_dev : nullptr;
   a.chunk = 0;
   a.n_chunks = 1;
   a.with_shared = g.has_shared;
@@ -747,7 +756,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   // SM fills (decode): kFillSms SMs copy the misses, the expert GEMV takes
   // the others, and the hits' phase 2 is launched after the host has read the
   // record, so that its waiting CTAs cannot take the SMs the fills need
-  const bool sm_fill = !resident && !prefill && L->fill_mode == MOE_FILL_KERNEL;
+  const bool sm_fill = !resident && !prefill && fmode == MOE_FILL_KERNEL;
   const int gemv_sms = sm_fill ? L->num_sms - kFillSms : L->num_sms;
   auto gemv = [&](int n_ent, int phases) -> int {
     cudaEvent_t ev[4] = {};
@@ -773,7 +782,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     if (ce != cudaSuccess) return cuda_fail(L, ce, prefill ? "launch_prefill_gemms" : "launch_gemv_decode");
     return MOE_OK;
   };
-  int grc = gemv(cap + (g.has_shared ? 1 : 0), sm_fill ? 1 : 3);
+  int grc = gemv((fused ? std::min(g.E, N * g.k) : cap) + (g.has_shared ? 1 : 0), sm_fill ? 1 : 3);
   if (grc) return grc;
   if (sm_fill) {
     // every fill chunk a step can have is queued behind the routing (after the
@@ -812,6 +821,9 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     MOE_CUDA(L, cudaEventRecord(L->ev_fill, fs));
     MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
     waves = (max_miss + g.S - 1) / g.S;
+  } else if (fused) {
+    any_miss = false;   // computed (and filled) by the launch above
+    a.host_pool = nullptr;
   } else if (!resident) {
     int prc = poll_record(L, seq);
     if (prc) return prc;
@@ -904,6 +916,13 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       L->launches += 1;
     }
   }
+  if (fused && max_staged > 0) {
+    // staged misses that keep their LRU slot move into it (the device knows which)
+    pe = prof_begin(L, MOE_PROF_COMMIT, st);
+    MOE_CUDA(L, launch_stage_commit(g, L->rec, -1, -1, max_staged, L->slots, st));
+    prof_end(pe, st);
+    L->launches += 1;
+  }
   pe = prof_begin(L, MOE_PROF_COMBINE, st);
   MOE_CUDA(L, launch_combine(g, L->O, prefill, L->gates, L->row_of, N, yd, st));
   prof_end(pe, st);
@@ -919,7 +938,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     info->n_misses = n_miss;
     info->n_waves = resident ? 1 : waves;
     info->fill_bytes = fill_bytes;
-    info->host_synced = (resident || dev_fill) ? 0 : 1;
+    info->host_synced = (resident || dev_fill || fused) ? 0 : 1;
     info->n_launches = L->launches;
   }
   return MOE_OK;
@@ -927,7 +946,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
 
 int moe_set_fill_mode(moe_layer_t L, int mode) {
   if (!L) return MOE_ERR_ARG;
-  if (mode != MOE_FILL_MEMCPY && mode != MOE_FILL_DEVICE && mode != MOE_FILL_KERNEL)
+  if (mode != MOE_FILL_MEMCPY && mode != MOE_FILL_DEVICE && mode != MOE_FILL_KERNEL && mode != MOE_FILL_FUSED &&
+      mode != MOE_FILL_AUTO)
     return fail(L, MOE_ERR_ARG, "unknown fill mode %d", mode);
   if (mode != MOE_FILL_MEMCPY && !L->pool_dev)
     return fail(L, MOE_ERR_STATE, "copy-kernel fills need a registered pinned host pool the device can address");

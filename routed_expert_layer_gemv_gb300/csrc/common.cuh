@@ -105,8 +105,9 @@ struct Geo {
 
 // Work-range selectors of the expert FFN launches (resolved on the device
 // from the StepRecord so a launch needs no host round trip): the step's
-// hits, or all of its misses.
-enum RangeMode : int { kRangeHits = 0, kRangeMisses = 1 };
+// hits, its misses, or every access (with GemvArgs::host_pool set, the misses
+// are then read from the host pool and written on to their slots).
+enum RangeMode : int { kRangeHits = 0, kRangeMisses = 1, kRangeAll = 2 };
 
 // Slot whose bytes an access computes from.  Misses of the first wave
 // (access index < S) are filled straight into their LRU slot (a free or
@@ -162,6 +163,7 @@ struct GemvArgs {
   int N;
   int mode;                    // RangeMode
   int chunk, n_chunks;         // kRangeMisses: the misses split in n_chunks equal runs, this launch takes one
+  const uint8_t* host_pool;    // kRangeAll: device address of the pinned host pool the misses stream from
   int with_shared;             // also run the shared expert (rows N*k .. N*k+N)
   int* err;                    // set to 1 when a bounded wait gives up
   float* hmax;                 // [rows][2][d_ff / 64]: max |W_g x|, |W_u x| per 64 columns

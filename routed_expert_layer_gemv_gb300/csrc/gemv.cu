@@ -132,6 +132,7 @@ MOE_DEV void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, 
 struct Entry {
   int slot, row0, nrows, shared;
   int tok0;        // token of the first row (-1: read tok_of)
+  int ex;          // a miss read from the host pool (and written on to `slot`): its expert; else -1
 };
 
 // Entries of this launch: the access-order range the mode selects (+ the
@@ -141,7 +142,9 @@ MOE_DEV int count_entries(const Geo& g, const GemvArgs& a, int* base, int* nr) {
   const int U = min(max(rec->U, 0), g.E), nh = min(max(rec->n_hit, 0), U), S = g.S;
   (void)S;
   int b = 0, e = nh;
-  if (a.mode != kRangeHits) {
+  if (a.mode == kRangeAll) {
+    e = U;
+  } else if (a.mode != kRangeHits) {
     // misses [nh, U), or chunk `chunk` of n_chunks equal runs of them
     const int C = max(a.n_chunks, 1), c = min(max(a.chunk, 0), C - 1), nm = U - nh;
     b = nh + (int)((long long)nm * c / C);
@@ -163,6 +166,11 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int en
     out.shared = 0;
     const uint32_t tk = (uint32_t)v.w;
     out.tok0 = (tk >> 16) == 0xffffu ? -1 : (int)(tk & 0xffffu);
+    out.ex = -1;
+    if (a.host_pool && base + ent >= min(max(a.rec->n_hit, 0), g.E)) {
+      out.ex = rec_expert(const_cast<StepRecord*>(a.rec))[base + ent];
+      if (out.ex < 0 || out.ex >= g.E) return false;
+    }
     return slot_ok && out.nrows > 0 && out.row0 >= 0 && out.row0 + out.nrows <= a.N * g.k;
   }
   if (a.with_shared && ent == nr) {
@@ -171,12 +179,15 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, int base, int nr, int en
     out.nrows = a.N;
     out.shared = 1;
     out.tok0 = 0;
+    out.ex = -1;
     return a.N > 0;
   }
   return false;
 }
 
-// This CTA's unit range [u0, u1) of the launch's n_ent * UE units.
+// This CTA's unit range [u0, u1) of the launch's n_ent * UE units.  (A launch
+// that streams misses from the host pool keeps them in a contiguous run of
+// CTAs: spreading them over every CTA measured slower on the host link.)
 struct Range {
   int base, nr, u0, u1;
 };
@@ -299,6 +310,54 @@ MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
       acc[3] = fmaf(d[3], sa1, fmaf(e[3], sb1, acc[3]));
     }
   }
+}
+
+// The part of a stage that compute warp w = 4b + q reads -- rows 16q .. 16q + 15
+// of code box b and those rows' scale bytes of the box -- for a miss whose
+// weights stream from the host pool: loaded from the pool into the stage in
+// the layout the TMA boxes give (16-byte chunk c of a 128-byte code row r at
+// chunk c ^ (r & 7)) and stored on to the miss's slot.  Bytes past K are
+// neither read nor written.
+MOE_DEV void host_part(const Geo& g, const SG& p, const GemvArgs& a, const Entry& en, int mm, int rb, int st,
+                       uint8_t* stg, int warp, int lane) {
+  const int bslot = warp >> 2, quarter = warp & 3;
+  const int kb = st * kBoxes + bslot, rowb = p.K / 2;
+  if (kb < p.KB) {
+    const uint8_t* hw = a.host_pool + (size_t)en.ex * g.ebytes;
+    uint8_t* ew = const_cast<uint8_t*>(a.slots) + (size_t)en.slot * g.ebytes;
+    const size_t co = g.off_codes[mm] + (size_t)rb * kBoxRows * rowb + (size_t)kb * 128;
+    const int vb = min(128, rowb - kb * 128);
+    uint8_t* box = stg + (size_t)bslot * kBoxBytes;
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = lane + 32 * j, r = 16 * quarter + (i >> 3), c = i & 7;
+      if (c * 16 < vb) v[j] = *reinterpret_cast<const uint4*>(hw + co + (size_t)r * rowb + c * 16);
+    }
+    uint32_t sw[4];
+    const int r_s = 16 * quarter + (lane & 15);
+    const size_t so = g.off_scales[mm] + (size_t)(rb * kBoxRows + r_s) * p.scale_row + (size_t)kb * p.SBB;
+    const int vsw = min(p.SBB, p.scale_row - kb * p.SBB) / 4;   // 1, 2 or 4 words
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      if (lane < 16 && w < vsw) sw[w] = *reinterpret_cast<const uint32_t*>(hw + so + 4 * w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = lane + 32 * j, r = 16 * quarter + (i >> 3), c = i & 7;
+      if (c * 16 < vb) {
+        *reinterpret_cast<uint4*>(box + r * 128 + ((c ^ (r & 7)) << 4)) = v[j];
+        *reinterpret_cast<uint4*>(ew + co + (size_t)r * rowb + c * 16) = v[j];
+      }
+    }
+    uint8_t* sd = stg + p.codes_bytes + r_s * p.srow + (p.smode ? bslot : kb) * p.SBB;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      if (lane < 16 && w < vsw) {
+        *reinterpret_cast<uint32_t*>(sd + 4 * w) = sw[w];
+        *reinterpret_cast<uint32_t*>(ew + so + 4 * w) = sw[w];
+      }
+  }
+  __syncwarp();
 }
 
 // Shared state of one CTA.
@@ -525,6 +584,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     bool stop = false;
     while (!stop && cursor_next(cu, g, a, p, rr)) {
       const uint8_t* ew = a.slots + (size_t)cu.en.slot * g.ebytes;
+      const bool hw = cu.en.ex >= 0;
       for (int u = cu.ue0; u < cu.ue1 && !stop; ++u) {
         const int m = PH == 1 ? u / p.RB : 0;          // 0: gate / down, 1: up
         const int rb = PH == 1 ? u % p.RB : u;
@@ -541,6 +601,14 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
           uint8_t* stg = S.base + (size_t)slot * p.stage_bytes;
           const int nbx = min(kBoxes, p.KB - st * kBoxes);
           const uint32_t sbytes = kBoxRows * p.srow;
+          if (hw) {
+            // a miss streamed from the host pool: the compute warps load their
+            // own parts of the stage (one warp keeps far too few loads in
+            // flight over the host link), so the stage is theirs once it is free
+            if (lane == 0) mbar_arrive(&S.full[slot]);
+            ++n;
+            continue;
+          }
           if (lane == 0) tc::mbar_expect_tx(&S.full[slot], (uint32_t)(nbx * kBoxBytes) + sbytes);
           __syncwarp();
           if (lane < nbx)
@@ -584,6 +652,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
           const int slot = n % p.D;
           const bool ok = wait_or_abort(&S.full[slot], (n / p.D) & 1, &s_abort, a.err);
           const int kb = st * kBoxes + bslot;
+          if (ok && cu.en.ex >= 0)
+            host_part(g, p, a, cu.en, PH == 1 ? u / p.RB : 2, PH == 1 ? u % p.RB : u, st,
+                      S.base + (size_t)slot * p.stage_bytes, warp, lane);
           if (ok && kb < p.KB) {
             const uint8_t* stg = S.base + (size_t)slot * p.stage_bytes;
             const uint8_t* cs = stg + (size_t)bslot * kBoxBytes + quarter * (16 * kBoxK / 2);
@@ -648,7 +719,12 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
           stok[te] = cr.en.shared ? te : (te == 0 && cr.en.tok0 >= 0) ? cr.en.tok0 : a.tok_of[rowt + te];
         epi_sync();
       }
-      const float* tsp = reinterpret_cast<const float*>(a.slots + (size_t)cr.en.slot * g.ebytes + g.off_tscale);
+      const float* tsp = reinterpret_cast<const float*>(
+          (cr.en.ex >= 0 ? a.host_pool + (size_t)cr.en.ex * g.ebytes : a.slots + (size_t)cr.en.slot * g.ebytes) +
+          g.off_tscale);
+      if (PH == 1 && cr.en.ex >= 0 && te == 0)   // a miss's tensor scales go on to its slot too
+        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.slots) + (size_t)cr.en.slot * g.ebytes + g.off_tscale) =
+            *reinterpret_cast<const uint4*>(tsp);
       for (int u = cr.ue0; u < cr.ue1; ++u) {
         const int m = PH == 1 ? u / p.RB : 0;
         const int rb = PH == 1 ? u % p.RB : u;

@@ -68,7 +68,10 @@ def _decode_run(spec, seed, batch, steps, check_every=1, fill=capi.MOE_FILL_MEMC
         ref, idx, _ = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
         acc = T.step(idx.reshape(-1))
         n_miss = sum(1 for a in acc if not a[2])
-        if fill in (capi.MOE_FILL_MEMCPY, capi.MOE_FILL_KERNEL):
+        eff = fill
+        if fill == capi.MOE_FILL_AUTO:   # the library's per-call choice
+            eff = capi.MOE_FILL_FUSED if min(spec.E, N * spec.k) <= spec.n_slots else capi.MOE_FILL_KERNEL
+        if eff in (capi.MOE_FILL_MEMCPY, capi.MOE_FILL_KERNEL):
             assert info.host_synced == 1
             assert info.n_distinct == len(acc)
             assert info.n_misses == n_miss
@@ -109,30 +112,35 @@ def test_decode_284b_shape_shared_and_waves():
     assert waves >= 2
 
 
-@pytest.mark.parametrize("fill", [capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL])
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL, capi.MOE_FILL_FUSED,
+                                  capi.MOE_FILL_AUTO])
 @pytest.mark.parametrize("batch,steps", [(1, 8), (4, 6), (16, 3)])
 def test_decode_copy_kernel_fill(batch, steps, fill):
-    # misses pulled from the pinned pool by a copy kernel: DEVICE reads the
-    # routing record on the GPU (no host wait), KERNEL on reserved SMs after
-    # the host read it (chunked at batch 16)
+    # misses pulled from the pinned pool by the GPU: DEVICE by a copy kernel
+    # that reads the routing record on the GPU (no host wait), KERNEL by one on
+    # reserved SMs (chunked at batch 16), FUSED by the expert FFN itself, which
+    # writes them on to their slots (checked through the LRU state and later hits)
     spec = wl.DECODE_35B.layer
     miss, u, waves = _decode_run(spec, 7, batch, steps, fill=fill)
     assert miss > 0
 
 
-def test_decode_284b_shape_kernel_fill():
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_KERNEL, capi.MOE_FILL_FUSED])
+def test_decode_284b_shape_kernel_fill(fill):
     # shared expert, d_model 4096 MXFP4 experts, more distinct experts than slots
     spec = wl.DECODE_284B.layer
-    miss, u, waves = _decode_run(spec, 5, 8, 3, fill=capi.MOE_FILL_KERNEL)
+    miss, u, waves = _decode_run(spec, 5, 8, 3, fill=fill)
     assert waves >= 2
 
 
-@pytest.mark.parametrize("fill", [capi.MOE_FILL_MEMCPY, capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL])
-def test_staged_misses_land_in_their_lru_slots(fill):
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_MEMCPY, capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL,
+                                  capi.MOE_FILL_FUSED])
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+def test_staged_misses_land_in_their_lru_slots(fill, fmt):
     # more distinct experts per step than slots: misses past the first wave are
     # filled into staging slots and committed afterwards; every LRU slot must
     # then hold exactly the expert the slot table names
-    spec = small_spec(E=32, k=4, d_model=256, d_ff=256, n_slots=6, has_shared=True)
+    spec = small_spec(E=32, k=4, d_model=256, d_ff=256, n_slots=6, fmt=fmt, has_shared=True)
     seed, batch = 13, 8
     experts = CachedExperts(spec, seed)
     L = build_layer(spec, seed, batch, experts_fn=experts)
@@ -164,7 +172,7 @@ def test_staged_misses_land_in_their_lru_slots(fill):
     L.close()
 
 
-@pytest.mark.parametrize("fill", [capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL])
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL, capi.MOE_FILL_FUSED])
 def test_prefill_copy_kernel_fill_waves(fill):
     # KERNEL mode fills prefill misses with the copy engine (the GEMM holds every SM)
     spec = small_spec(E=24, k=3, d_model=512, d_ff=256, n_slots=5, fmt="nvfp4", has_shared=True,
@@ -183,10 +191,13 @@ def test_prefill_copy_kernel_fill_waves(fill):
     L.close()
 
 
-def test_decode_nvfp4_bias_small_cache():
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_MEMCPY, capi.MOE_FILL_KERNEL, capi.MOE_FILL_FUSED])
+def test_decode_nvfp4_bias_small_cache(fill):
+    # d_ff 384: the down rows end in a half-filled 256-K box; later steps hit
+    # the experts earlier misses left in the slots (tensor scales included)
     spec = small_spec(E=24, k=3, d_model=512, d_ff=384, n_slots=5, fmt="nvfp4", has_shared=True,
                       has_bias=True)
-    miss, u, waves = _decode_run(spec, 6, 3, 12)
+    miss, u, waves = _decode_run(spec, 6, 3, 12, fill=fill)
     assert miss > 0
 
 
