@@ -326,6 +326,8 @@ def main():
                          "print that prefill chunk's line instead")
     ap.add_argument("--prefill-steps", type=int, default=8)
     ap.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill result")
+    ap.add_argument("--fill-modes", default="memcpy,device,kernel,fused",
+                    help="fill modes timed beside the default per batch ('none': skip them)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = _dist()
@@ -395,6 +397,7 @@ def main():
              for b in batches]
     modes = {"memcpy": capi.MOE_FILL_MEMCPY, "device": capi.MOE_FILL_DEVICE, "kernel": capi.MOE_FILL_KERNEL,
              "fused": capi.MOE_FILL_FUSED}
+    modes = {m: modes[m] for m in args.fill_modes.split(",") if m in modes}
     fruns = {name: [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False, m) for b in batches]
              for name, m in modes.items()}
     e2e_runs = [run_decode_e2e(args, b, torch, capi, wl, build_layer, flush) for b in batches]

@@ -109,7 +109,8 @@ typedef struct {
 #define MOE_PROF_COMBINE     5
 #define MOE_PROF_FILL        6  /* host -> slot copies on the fill stream       */
 #define MOE_PROF_PREFILL     7  /* prefill: activation gather + FP4 quantiser   */
-#define MOE_PROF_COMMIT      8  /* staged misses copied into their LRU slots    */
+#define MOE_PROF_COMMIT      8  /* no launches: later-wave misses are remapped,
+                                   not copied (kept for the class numbering)   */
 #define MOE_PROF_KINDS       9
 
 /* Layout of one expert for a descriptor (no GPU work). */
@@ -177,9 +178,9 @@ int moe_lru_set_state(moe_layer_t layer, const int* expert_of_slot,
  * bounded: MOE_ERR_STATE if the routing finished and no record arrived,
  * MOE_ERR_TIMEOUT after 30 s), and then issues the slot fills on the layer's
  * fill stream; otherwise it returns without waiting.  Misses beyond
- * the first n_slots accesses of a step are filled into staging slots at once
- * and copied into their LRU slots after the step's expert FFN, so the cache
- * state after the call is the LRU's either way.  regime:
+ * the first n_slots accesses of a step are filled into spare buffers at once,
+ * and a spare whose expert keeps its LRU slot becomes that slot's buffer (no
+ * copy), so the cache state after the call is the LRU's either way.  regime:
  * MOE_REGIME_*.  MOE_ERR_NOT_INSTALLED if a miss has no host source. */
 int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
                 int regime, moe_forward_info* info);

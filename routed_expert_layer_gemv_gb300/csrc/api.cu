@@ -7,11 +7,12 @@
 //   caller stream: router -> permute -> LRU step -> [record copy to host]
 //                  -> expert GEMV over the hits (+ shared expert)
 //   host:          wait for the record, then for every miss at once:
-//   fill stream:   cudaMemcpyAsync pinned host expert -> its slot (first wave
-//                  of n_slots accesses) or a staging slot (later accesses,
-//                  whose LRU slots this step still reads)
+//   fill stream:   cudaMemcpyAsync pinned host expert -> its slot's buffer
+//                  (first wave of n_slots accesses) or a spare buffer (later
+//                  accesses, whose LRU slots this step still reads; the LRU
+//                  kernel makes the spare the slot's buffer for later steps)
 //   caller stream: wait for the fills -> expert GEMV over all misses
-//                  -> commit staged experts into their LRU slots -> combine -> y
+//                  -> combine -> y
 // The hits are computed while the host reads the record and the fills are in
 // flight.  When every expert is resident (n_slots >= E, all installed) no
 // miss can happen and the step runs without any host wait.
@@ -55,6 +56,7 @@ struct moe_layer {
   int* slot_of = nullptr;
   int* expert_of = nullptr;
   unsigned long long* stamp = nullptr;
+  int* buf = nullptr;                // slot -> pool buffer map, then the spare buffers (S + X)
   unsigned long long* clock = nullptr;
   float* logits = nullptr;
   int* idx = nullptr;
@@ -281,6 +283,18 @@ void prof_end(cudaEvent_t* e, cudaStream_t st) {
   if (e) cudaEventRecord(e[1], st);
 }
 
+// A buffer a fill may write: an LRU slot's or a spare, never the shared expert's.
+bool buf_ok(const Geo& g, int b) { return b >= 0 && b <= g.S + g.X && b != g.S; }
+
+// The pool buffer LRU slot `slot` lives in, read once the device is idle (a
+// step's LRU kernel may remap slots).
+int slot_buffer(moe_layer* L, int slot, int* b) {
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  MOE_CUDA(L, cudaMemcpy(b, L->buf + slot, 4, cudaMemcpyDeviceToHost));
+  if (!buf_ok(L->g, *b)) return fail(L, MOE_ERR_STATE, "slot %d maps to buffer %d", slot, *b);
+  return MOE_OK;
+}
+
 int n_ent_cap(const moe_layer* L, int N) {
   long long routed = (long long)N * L->g.k;
   return (int)std::min<long long>(std::min(L->g.S, L->g.E), routed);
@@ -338,14 +352,14 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     return MOE_ERR_CUDA;
   }
   const size_t Nm = desc->max_tokens;
-  // staging slots: one per miss a step can have beyond the first wave of n_slots
+  // spare buffers: one per miss a step can have beyond the first wave of n_slots
   L->g.X = (int)std::max<long long>(0, std::min<long long>(L->g.E, (long long)Nm * L->g.k) - L->g.S);
   const Geo& g = L->g;
   const size_t rows = Nm * g.k + (g.has_shared ? Nm : 0);
   rc = MOE_OK;
 #define MOE_ALLOC(ptr, bytes) \
   if (rc == MOE_OK) rc = dalloc(L, &L->ptr, (bytes))
-  // n_slots LRU slots, the shared expert (resident, not LRU), then the staging slots
+  // buffers of the n_slots LRU slots, the shared expert (resident, not LRU), the spares
   MOE_ALLOC(slots, (size_t)(g.S + 1 + g.X) * g.ebytes);
   if (rc == MOE_OK) L->shared_w = L->slots + (size_t)g.S * g.ebytes;
   MOE_ALLOC(Wr, (size_t)g.E * g.d * 4);
@@ -354,6 +368,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   MOE_ALLOC(slot_of, (size_t)g.E * 4);
   MOE_ALLOC(expert_of, (size_t)g.S * 4);
   MOE_ALLOC(stamp, (size_t)g.S * 8);
+  MOE_ALLOC(buf, (size_t)(g.S + g.X) * 4);
   MOE_ALLOC(clock, 8);
   MOE_ALLOC(logits, Nm * g.E * 4);
   MOE_ALLOC(idx, Nm * g.k * 4);
@@ -444,8 +459,13 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
               cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
               cudaMemset(L->rec, 0, rec_dev_bytes(g.E)) == cudaSuccess &&
               cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
-              cudaMemset(L->stats, 0, 64) == cudaSuccess &&
-              cudaDeviceSynchronize() == cudaSuccess;
+              cudaMemset(L->stats, 0, 64) == cudaSuccess;
+    // slot s in buffer s; the spares after the shared expert's buffer S
+    std::vector<int> b0(g.S + g.X);
+    for (int s = 0; s < g.S; ++s) b0[s] = s;
+    for (int j = 0; j < g.X; ++j) b0[g.S + j] = g.S + 1 + j;
+    ok = ok && (b0.empty() || cudaMemcpy(L->buf, b0.data(), b0.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess) &&
+         cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
       cudaGetLastError();
       rc = MOE_ERR_CUDA;
@@ -523,7 +543,10 @@ int moe_cache_install(moe_layer_t L, int expert, int slot, void* stream) {
   if (slot < 0 || slot >= L->g.S) return fail(L, MOE_ERR_ARG, "slot %d out of range", slot);
   if (!L->host_pool) return fail(L, MOE_ERR_NOT_INSTALLED, "no host expert pool registered");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)slot * L->g.ebytes,
+  int b = -1;
+  int rc = slot_buffer(L, slot, &b);
+  if (rc) return rc;
+  MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)b * L->g.ebytes,
                               L->host_pool + (size_t)expert * L->g.ebytes, L->g.ebytes,
                               cudaMemcpyHostToDevice, st));
   MOE_CUDA(L, launch_lru_install(L->g, expert, slot, L->slot_of, L->expert_of, L->stamp, L->clock, st));
@@ -577,21 +600,24 @@ int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, in
   const Geo& g = L->g;
   if (n > 0) MOE_CUDA(L, cudaMemcpyAsync(L->list_dev, experts, (size_t)n * 4, cudaMemcpyHostToDevice, st));
   MOE_CUDA(L, launch_counts_from_list(g, L->list_dev, n, L->counts, st));
-  MOE_CUDA(L, launch_lru_step(g, L->counts, nullptr, L->slot_of, L->expert_of, L->stamp, L->clock, L->rec,
-                              nullptr, nullptr, 0, st));
+  MOE_CUDA(L, launch_lru_step(g, L->counts, nullptr, L->slot_of, L->expert_of, L->stamp, L->clock, L->buf,
+                              L->rec, nullptr, nullptr, 0, st));
   MOE_CUDA(L, cudaMemcpyAsync(L->rec_host, L->rec, rec_bytes(g.E), cudaMemcpyDeviceToHost, st));
   MOE_CUDA(L, cudaStreamSynchronize(st));
   const StepRecord* r = L->rec_host;
   const int* ae = rec_expert(const_cast<StepRecord*>(r));
   const int* as = rec_slot(const_cast<StepRecord*>(r), g.E);
+  const int* ab = rec_buf(const_cast<StepRecord*>(r), g.E);
   if (r->U < 0 || r->U > g.E || r->n_hit < 0 || r->n_hit > r->U)
     return fail(L, MOE_ERR_STATE, "step record is inconsistent");
   for (int i = 0; i < r->U; ++i)
-    if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S)
+    if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S || !buf_ok(g, ab[i]))
       return fail(L, MOE_ERR_STATE, "step record entry %d is out of range", i);
   if (L->host_pool) {
+    // every miss into the buffer the step gave it (a later-wave miss's spare
+    // became its slot's buffer at the end of the step)
     for (int i = r->n_hit; i < r->U; ++i)
-      MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)as[i] * g.ebytes, L->host_pool + (size_t)ae[i] * g.ebytes,
+      MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)ab[i] * g.ebytes, L->host_pool + (size_t)ae[i] * g.ebytes,
                                   g.ebytes, cudaMemcpyHostToDevice, st));
     MOE_CUDA(L, cudaStreamSynchronize(st));
   }
@@ -698,7 +724,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   // memcpy fills: the LRU kernel also writes the step record into mapped
   // pinned host memory, sequence number last, and the host polls it
   // the automatic choice: fused fills while no access of the step can need a
-  // staging slot (then there is nothing to commit), SM-copy fills beyond
+  // spare buffer, SM-copy fills beyond
   int fmode = L->fill_mode;
   if (fmode == MOE_FILL_AUTO) fmode = std::min(g.E, N * g.k) <= g.S ? MOE_FILL_FUSED : MOE_FILL_KERNEL;
   // fused fills (decode): one expert-FFN launch covers every access and reads
@@ -712,7 +738,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     // permutation and LRU step in one CTA
     pe = prof_begin(L, MOE_PROF_PERMUTE, st);
     MOE_CUDA(L, launch_route_tail(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
-                                  L->slot_of, L->expert_of, L->stamp, L->clock, L->rec, L->stats,
+                                  L->slot_of, L->expert_of, L->stamp, L->clock, L->buf, L->rec, L->stats,
                                   hrec, seq, st));
     prof_end(pe, st);
     L->launches += 1;
@@ -724,7 +750,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     L->launches += 3;
     pe = prof_begin(L, MOE_PROF_LRU, st);
     MOE_CUDA(L, launch_lru_step(g, L->counts, L->offsets, L->slot_of, L->expert_of, L->stamp, L->clock,
-                                L->rec, L->stats, hrec, seq, st));
+                                L->buf, L->rec, L->stats, hrec, seq, st));
     prof_end(pe, st);
     L->launches += 1;
   }
@@ -802,15 +828,14 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   }
 
   // Misses.  Every fill starts as soon as the routing is known: first-wave
-  // misses go straight into their (free or stale) LRU slots, later ones into
-  // staging slots, since their LRU slots are still read by this step; one
-  // expert-FFN launch then covers all misses, and the staged experts that
-  // keep their LRU slot are committed into it on the caller stream.
+  // misses go straight into their (free or stale) LRU slots' buffers, later
+  // ones into spare buffers, since their LRU slots are still read by this
+  // step (the record names each access's buffer); expert-FFN launches over
+  // the misses follow their fills.
   size_t fill_bytes = 0;
   int U = -1, n_hit = -1, n_miss = 0, waves = 1, n_chunks = 0;
   const int max_miss = std::min(g.E, N * g.k);
-  const int max_staged = std::max(0, max_miss - g.S);
-  bool any_miss = true, any_staged = max_staged > 0;
+  bool any_miss = true;
   if (dev_fill) {
     cudaStream_t fs = L->fill;
     MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
@@ -834,13 +859,13 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     waves = (U + g.S - 1) / g.S;
     const int* ae = rec_expert(const_cast<StepRecord*>(r));
     const int* as = rec_slot(const_cast<StepRecord*>(r), g.E);
+    const int* ab = rec_buf(const_cast<StepRecord*>(r), g.E);
     if (U < 0 || U > g.E || n_hit < 0 || n_hit > U || U - g.S > g.X)
       return fail(L, MOE_ERR_STATE, "step record is inconsistent (U=%d, hits=%d)", U, n_hit);
     for (int i = 0; i < U; ++i)
-      if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S)
+      if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S || !buf_ok(g, ab[i]))
         return fail(L, MOE_ERR_STATE, "step record entry %d is out of range", i);
     any_miss = n_hit < U;
-    any_staged = U > g.S;
     if (any_miss) {
       // the misses' expert FFN runs in chunks, each once its own fills have
       // landed, while later fills still run; a chunk pays one expert-FFN
@@ -861,8 +886,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
         const int c0 = n_hit + (int)((long long)nm * c / n_chunks), c1 = n_hit + (int)((long long)nm * (c + 1) / n_chunks);
         for (int i = c0; i < c1;) {
           int j = i + 1;
-          while (j < c1 && ae[j] == ae[j - 1] + 1 && access_slot(as, g.S, j) == access_slot(as, g.S, j - 1) + 1) ++j;
-          cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)access_slot(as, g.S, i) * g.ebytes,
+          while (j < c1 && ae[j] == ae[j - 1] + 1 && ab[j] == ab[j - 1] + 1) ++j;
+          cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)ab[i] * g.ebytes,
                                            L->host_pool + (size_t)ae[i] * g.ebytes, (size_t)(j - i) * g.ebytes,
                                            cudaMemcpyHostToDevice, fs);
           if (ce != cudaSuccess) return fail(L, MOE_ERR_FILL, "fill of expert %d: %s", ae[i], cudaGetErrorString(ce));
@@ -883,9 +908,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     a.mode = kRangeMisses;
     a.with_shared = 0;
     if (n_chunks > 1 && !prefill) {
-      // memcpy fills: chunk c of the misses runs once its own copies landed
-      // its staged experts that keep their slot are committed right after it:
-      // every access before the chunk's end (hits, earlier chunks) has run
+      // chunk c of the misses runs once its own copies landed
       const int nm = U - n_hit;
       a.n_chunks = n_chunks;
       for (int c = 0; c < n_chunks; ++c) {
@@ -894,34 +917,13 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
         const int c0 = n_hit + (int)((long long)nm * c / n_chunks), c1 = n_hit + (int)((long long)nm * (c + 1) / n_chunks);
         grc = gemv(c1 - c0, 3);
         if (grc) return grc;
-        const int f0 = std::max(c0, std::max(g.S, U - g.S));   // staged and final
-        if (c1 > f0) {
-          pe = prof_begin(L, MOE_PROF_COMMIT, st);
-          MOE_CUDA(L, launch_stage_commit(g, L->rec, f0, c1, c1 - f0, L->slots, st));
-          prof_end(pe, st);
-          L->launches += 1;
-        }
       }
-      any_staged = false;   // committed chunk by chunk
     } else {
       // one launch over every miss once the last copy (one queue, in order) has landed
       if (n_chunks > 0) MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[n_chunks - 1], 0));
       grc = gemv(max_miss, 3);
       if (grc) return grc;
     }
-    if (any_staged) {
-      pe = prof_begin(L, MOE_PROF_COMMIT, st);
-      MOE_CUDA(L, launch_stage_commit(g, L->rec, -1, -1, max_staged, L->slots, st));
-      prof_end(pe, st);
-      L->launches += 1;
-    }
-  }
-  if (fused && max_staged > 0) {
-    // staged misses that keep their LRU slot move into it (the device knows which)
-    pe = prof_begin(L, MOE_PROF_COMMIT, st);
-    MOE_CUDA(L, launch_stage_commit(g, L->rec, -1, -1, max_staged, L->slots, st));
-    prof_end(pe, st);
-    L->launches += 1;
   }
   pe = prof_begin(L, MOE_PROF_COMBINE, st);
   MOE_CUDA(L, launch_combine(g, L->O, prefill, L->gates, L->row_of, N, yd, st));
@@ -1026,7 +1028,10 @@ int moe_debug_dequant(moe_layer_t L, int slot, int m, float* out, void* stream) 
     if (!L->g.has_shared) return fail(L, MOE_ERR_STATE, "no shared expert");
     base = L->shared_w;
   } else if (slot >= 0 && slot < L->g.S) {
-    base = L->slots + (size_t)slot * L->g.ebytes;
+    int b = -1;
+    int rc = slot_buffer(L, slot, &b);
+    if (rc) return rc;
+    base = L->slots + (size_t)b * L->g.ebytes;
   } else {
     return fail(L, MOE_ERR_ARG, "slot %d out of range", slot);
   }

@@ -68,7 +68,9 @@ MOE_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte) {
 // ---------------------------------------------------------------- step record
 // What one step's routing and LRU update decided; written by the LRU kernel,
 // copied to pinned host memory for the fill issue.  Arrays hold |U| entries
-// in access order (hits ascending id, then misses ascending id).
+// in access order (hits ascending id, then misses ascending id).  acc_slot is
+// the LRU slot an access ends up in (logical); acc_buf the buffer of the slot
+// pool it is computed from and, for a miss, filled into (physical).
 struct StepRecord {
   int U;        // distinct routed experts
   int n_hit;
@@ -76,20 +78,21 @@ struct StepRecord {
   int S;        // slots (wave length)
   unsigned long long seq;   // host copy only: step number, written last
   int pad[2];
-  // followed by int acc_expert[E], acc_slot[E], acc_evicted[E]
+  // followed by int acc_expert[E], acc_slot[E], acc_evicted[E], acc_buf[E]
 };
 __host__ __device__ inline int* rec_expert(StepRecord* r) { return reinterpret_cast<int*>(r + 1); }
 __host__ __device__ inline int* rec_slot(StepRecord* r, int E) { return rec_expert(r) + E; }
 __host__ __device__ inline int* rec_evicted(StepRecord* r, int E) { return rec_expert(r) + 2 * E; }
-// bytes the host reads back (header and the three access arrays)
-inline size_t rec_bytes(int E) { return sizeof(StepRecord) + 3 * sizeof(int) * (size_t)E; }
-// Device-only tail: per access i, {physical slot (access_slot, -1 when the
-// record is inconsistent), first permuted row, rows, tokens}, so a kernel
+__host__ __device__ inline int* rec_buf(StepRecord* r, int E) { return rec_expert(r) + 3 * E; }
+// bytes the host reads back (header and the four access arrays)
+inline size_t rec_bytes(int E) { return sizeof(StepRecord) + 4 * sizeof(int) * (size_t)E; }
+// Device-only tail: per access i, {buffer (acc_buf, -1 when the record is
+// inconsistent), first permuted row, rows, tokens}, so a kernel
 // finds an access's weights and tokens with one 16-byte load.  tokens = the
 // first row's token (low 16 bits; 0xffff in the high half when it is not
 // known).
 __host__ __device__ inline int4* rec_entry(StepRecord* r, int E) {
-  const size_t off = (sizeof(StepRecord) + 3 * sizeof(int) * (size_t)E + 15) & ~size_t(15);
+  const size_t off = (sizeof(StepRecord) + 4 * sizeof(int) * (size_t)E + 15) & ~size_t(15);
   return reinterpret_cast<int4*>(reinterpret_cast<char*>(r) + off);
 }
 inline size_t rec_dev_bytes(int E) { return ((rec_bytes(E) + 15) & ~size_t(15)) + sizeof(int4) * (size_t)E; }
@@ -97,7 +100,7 @@ inline size_t rec_dev_bytes(int E) { return ((rec_bytes(E) + 15) & ~size_t(15)) 
 // ---------------------------------------------------------------- layer geometry
 struct Geo {
   int E, k, d, f, S, fmt, has_shared, norm_topk, has_bias;
-  int X;                       // staging slots after the shared expert's (S + 1 ...)
+  int X;                       // spare buffers: the pool holds S + 1 + X (the shared expert's is S)
   int blk;                     // 32 (MXFP4) or 16 (NVFP4)
   size_t ebytes;               // padded bytes of one expert
   size_t off_codes[3], off_scales[3], off_tscale;
@@ -109,14 +112,15 @@ struct Geo {
 // are then read from the host pool and written on to their slots).
 enum RangeMode : int { kRangeHits = 0, kRangeMisses = 1, kRangeAll = 2 };
 
-// Slot whose bytes an access computes from.  Misses of the first wave
-// (access index < S) are filled straight into their LRU slot (a free or
-// stale one); later misses would evict a slot the same step still reads, so
-// they are filled into staging slot S + 1 + (i - S) at once and committed to
-// their LRU slot after the step's expert FFN (launch_stage_commit).
-__host__ __device__ inline int access_slot(const int* acc_slot, int S, int i) {
-  return i < S ? acc_slot[i] : S + 1 + (i - S);
-}
+// Buffers of the slot pool.  The pool holds S + 1 + X expert buffers (the
+// shared expert's is buffer S); LRU slot s lives in buffer buf[s] and
+// buf[S .. S + X) lists the spare ones (buf, S + X ints, kept by the LRU
+// kernel, initially s and S + 1 + j).  Misses of the first wave (access index
+// i < S) are filled into their LRU slot's buffer (a free or stale one); a
+// later miss would evict a slot the same step still reads, so it is filled
+// into spare buf[S + (i - S)], and when it keeps that slot at the end of the
+// step the LRU kernel swaps the two buffers: the slot's old buffer becomes
+// the spare.  No expert is ever copied within the pool.
 
 // ---------------------------------------------------------------- launchers
 // router.cu
@@ -138,9 +142,10 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
 // expert row offsets, for the record's entry table
 // host_rec (may be null): mapped pinned copy of the record, written by the
 // kernel itself, seq last, so the host can poll it instead of a copy + event
+// buf: the slot -> buffer map and spare list (S + X ints, updated in place)
 cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets, int* slot_of,
                             int* expert_of, unsigned long long* stamp, unsigned long long* clock,
-                            StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                            int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
                             unsigned long long seq, cudaStream_t st);
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
                                unsigned long long* stamp, unsigned long long* clock,
@@ -148,7 +153,7 @@ cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of,
 // permutation + LRU step in one CTA, for N <= 128 tokens
 cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, int* offsets,
                               int* row_of, int* tok_of, int* slot_of, int* expert_of,
-                              unsigned long long* stamp, unsigned long long* clock,
+                              unsigned long long* stamp, unsigned long long* clock, int* buf,
                               StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
                               unsigned long long seq, cudaStream_t st);
 cudaError_t launch_counts_from_list(const Geo& g, const int* experts, int n, int* counts,
@@ -200,7 +205,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
                                  const cudaEvent_t* ev);
 // fill.cu: copy every miss of the step from the (device-addressable) host pool
-// into the slot access_slot() names
+// into the buffer the record names (acc_buf)
 cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses,
                              const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
 // the same copy by kFillSms CTAs, one per SM, for chunk `chunk` of the miss
@@ -209,14 +214,8 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
 constexpr int kFillSms = 12;
 cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, int max_chunks, int per_chunk,
                            const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
-// copy each staged miss that still owns its LRU slot at the end of the step
-// (access i >= S with i + S >= U) from its staging slot into that slot
-// Staged accesses in [max(S, a0), min(U, a1)) (a1 < 0: up to U); max_staged
-// bounds their number (grid size).
 // dst <- src (bytes a multiple of 16, 16-byte aligned; src may be mapped host memory)
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);
-cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int a0, int a1, int max_staged,
-                                uint8_t* slots, cudaStream_t st);
 // combine.cu
 // The prefill GEMM writes O as f16 rows [rows][d] in the first half of the
 // O buffer, each row's 128-column blocks scaled by 2^-s; the exponents s

@@ -1,12 +1,11 @@
-// Device-driven miss fill: a copy kernel reads the step record on the GPU and
-// pulls every missed expert of the step from the pinned host pool (reached
-// over NVLink-C2C through unified addressing) into its slot or staging slot;
-// a second kernel commits staged experts to their LRU slots after the step's
-// expert FFN.  The host never waits for the routing, so a decode step runs
-// without a host round trip.  This is the variant of the default fill (cudaMemcpyAsync from pinned host memory on
-// side streams), which follows the pages' decode path: misses are loaded into
-// the GPU's expert cache from host memory ("FreeToken：把 284B MoE 塞进游戏 PC",
-// zhichai.net, §二 "Decode" paragraph).
+// Miss fills by copy kernels: each reads the step record on the GPU and pulls
+// missed experts from the pinned host pool (reached over NVLink-C2C through
+// unified addressing) into the buffers the record names.  fill_copy_kernel
+// (MOE_FILL_DEVICE) spreads one step's misses over the whole GPU;
+// fill_sm_kernel (MOE_FILL_KERNEL) copies one chunk of the miss list on a few
+// SMs the expert GEMV leaves free.  Both follow the pages' decode path: misses
+// are loaded into the GPU's expert cache from host memory ("FreeToken：把 284B
+// MoE 塞进游戏 PC", zhichai.net, §二 "Decode" paragraph).
 #include <algorithm>
 
 #include "common.cuh"
@@ -37,39 +36,26 @@ __device__ __forceinline__ void copy_chunk(const uint8_t* __restrict__ src, uint
   }
 }
 
-// CTA (miss m, chunk ch): access n_hit + m, from the pool to access_slot().
+// A buffer a fill may write: an LRU slot's or a spare, never the shared expert's.
+__device__ __forceinline__ bool fill_buf_ok(int b, int S, int X) { return b >= 0 && b <= S + X && b != S; }
+
+// CTA (miss m, chunk ch): access n_hit + m, from the pool to its buffer.
 __global__ void __launch_bounds__(kFillThreads)
 fill_copy_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, const uint8_t* __restrict__ pool,
                  uint8_t* __restrict__ slots, size_t ebytes, int chunks) {
   const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
   const int i = nh + blockIdx.x / chunks, ch = blockIdx.x % chunks;
   if (i >= U || i - S >= X) return;
-  const int* as = rec_slot(const_cast<StepRecord*>(rec), E);
   const int ex = rec_expert(const_cast<StepRecord*>(rec))[i];
-  if (ex < 0 || ex >= E || as[i] < 0 || as[i] >= S) return;
-  copy_chunk(pool + (size_t)ex * ebytes, slots + (size_t)access_slot(as, S, i) * ebytes, ebytes, ch);
-}
-
-// CTA (staged access i = first + m, chunk ch): access i still owns its LRU
-// slot at the end of the step (no later access of the step maps to that slot)
-// -> copy its staging slot into it.  first = max(S, a0); accesses stop at
-// min(U, a1) (a1 < 0: at U).
-__global__ void __launch_bounds__(kFillThreads)
-stage_commit_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int a0, int a1,
-                    uint8_t* __restrict__ slots, size_t ebytes, int chunks) {
-  const int U0 = min(max(rec->U, 0), E);
-  const int U = a1 < 0 ? U0 : min(U0, a1);
-  const int i = max(S, a0) + blockIdx.x / chunks, ch = blockIdx.x % chunks;
-  if (i >= U || i - S >= X || i + S < U0) return;
-  const int sl = rec_slot(const_cast<StepRecord*>(rec), E)[i];
-  if (sl < 0 || sl >= S) return;
-  copy_chunk(slots + (size_t)(S + 1 + (i - S)) * ebytes, slots + (size_t)sl * ebytes, ebytes, ch);
+  const int b = rec_buf(const_cast<StepRecord*>(rec), E)[i];
+  if (ex < 0 || ex >= E || !fill_buf_ok(b, S, X)) return;
+  copy_chunk(pool + (size_t)ex * ebytes, slots + (size_t)b * ebytes, ebytes, ch);
 }
 
 // SM fill of one chunk of the miss list: kFillSms CTAs, one per SM (the
 // shared memory they reserve, more than half an SM's, keeps two off one SM and
 // keeps the expert GEMV, which takes nearly all of it, off theirs), copy the
-// chunk's misses from the pinned host pool to access_slot().  The m = U - n_hit
+// chunk's misses from the pinned host pool to their buffers.  The m = U - n_hit
 // misses form nch = max(1, min(max_chunks, m / per_chunk)) chunks, chunk c
 // being accesses [n_hit + m c / nch, n_hit + m (c + 1) / nch) -- the split the
 // host makes from its copy of the record -- and a launch for c >= nch copies
@@ -91,17 +77,17 @@ fill_sm_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int chun
   const int i0 = nh + (int)((long long)m * chunk / nch);
   const int i1 = min(nh + (int)((long long)m * (chunk + 1) / nch), S + X);
   if (i1 <= i0) return;
-  const int* as = rec_slot(const_cast<StepRecord*>(rec), E);
+  const int* ab = rec_buf(const_cast<StepRecord*>(rec), E);
   const int* ae = rec_expert(const_cast<StepRecord*>(rec));
   const long long P = (long long)((ebytes + kFillPiece - 1) / kFillPiece);
   const long long total = (long long)(i1 - i0) * P;
   for (long long q = blockIdx.x; q < total; q += gridDim.x) {
     const int i = i0 + (int)(q / P);
     const size_t off = (size_t)(q % P) * kFillPiece;
-    const int ex = ae[i];
-    if (ex < 0 || ex >= E || as[i] < 0 || as[i] >= S) continue;
+    const int ex = ae[i], b = ab[i];
+    if (ex < 0 || ex >= E || !fill_buf_ok(b, S, X)) continue;
     const uint4* src = reinterpret_cast<const uint4*>(pool + (size_t)ex * ebytes + off);
-    uint4* dst = reinterpret_cast<uint4*>(slots + (size_t)access_slot(as, S, i) * ebytes + off);
+    uint4* dst = reinterpret_cast<uint4*>(slots + (size_t)b * ebytes + off);
     const int n16 = (int)(min(kFillPiece, ebytes - off) / 16);
     uint4 r[kFillSmUnroll];
 #pragma unroll
@@ -154,16 +140,6 @@ cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, int m
   }
   fill_sm_kernel<<<kFillSms, kFillSmThreads, kFillSmSmem, st>>>(rec, g.E, g.S, g.X, chunk, max_chunks,
                                                                per_chunk, pool_dev, slots, g.ebytes);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_stage_commit(const Geo& g, const StepRecord* rec, int a0, int a1, int max_staged,
-                                uint8_t* slots, cudaStream_t st) {
-  const int chunks = (int)((g.ebytes + kFillChunk - 1) / kFillChunk);
-  const long long grid = (long long)chunks * max_staged;
-  if (grid <= 0) return cudaSuccess;
-  stage_commit_kernel<<<(unsigned)grid, kFillThreads, 0, st>>>(rec, g.E, g.S, g.X, a0, a1, slots, g.ebytes,
-                                                               chunks);
   return cudaGetLastError();
 }
 

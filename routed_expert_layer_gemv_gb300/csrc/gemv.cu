@@ -505,7 +505,9 @@ MOE_DEV void stage_block(const Geo& g, const GemvArgs& a, const SG& p, const Ent
   }
 }
 
-template <int FMT, int PH>
+// HOST: the launch may stream misses from the host pool (GemvArgs::host_pool);
+// launches over resident weights only use the variant without that path.
+template <int FMT, int PH, bool HOST>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
                    const __grid_constant__ CUtensorMap smap0, const __grid_constant__ CUtensorMap smap1,
@@ -584,7 +586,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     bool stop = false;
     while (!stop && cursor_next(cu, g, a, p, rr)) {
       const uint8_t* ew = a.slots + (size_t)cu.en.slot * g.ebytes;
-      const bool hw = cu.en.ex >= 0;
+      const bool hw = HOST && cu.en.ex >= 0;
       for (int u = cu.ue0; u < cu.ue1 && !stop; ++u) {
         const int m = PH == 1 ? u / p.RB : 0;          // 0: gate / down, 1: up
         const int rb = PH == 1 ? u % p.RB : u;
@@ -652,7 +654,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
           const int slot = n % p.D;
           const bool ok = wait_or_abort(&S.full[slot], (n / p.D) & 1, &s_abort, a.err);
           const int kb = st * kBoxes + bslot;
-          if (ok && cu.en.ex >= 0)
+          if (HOST && ok && cu.en.ex >= 0)
             host_part(g, p, a, cu.en, PH == 1 ? u / p.RB : 2, PH == 1 ? u % p.RB : u, st,
                       S.base + (size_t)slot * p.stage_bytes, warp, lane);
           if (ok && kb < p.KB) {
@@ -720,9 +722,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         epi_sync();
       }
       const float* tsp = reinterpret_cast<const float*>(
-          (cr.en.ex >= 0 ? a.host_pool + (size_t)cr.en.ex * g.ebytes : a.slots + (size_t)cr.en.slot * g.ebytes) +
+          (HOST && cr.en.ex >= 0 ? a.host_pool + (size_t)cr.en.ex * g.ebytes : a.slots + (size_t)cr.en.slot * g.ebytes) +
           g.off_tscale);
-      if (PH == 1 && cr.en.ex >= 0 && te == 0)   // a miss's tensor scales go on to its slot too
+      if (HOST && PH == 1 && cr.en.ex >= 0 && te == 0)   // a miss's tensor scales go on to its slot too
         *reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.slots) + (size_t)cr.en.slot * g.ebytes + g.off_tscale) =
             *reinterpret_cast<const uint4*>(tsp);
       for (int u = cr.ue0; u < cr.ue1; ++u) {
@@ -820,13 +822,13 @@ SG make_sg(const Geo& g, int ph, int N) {
   return p;
 }
 
-template <int FMT, int PH>
+template <int FMT, int PH, bool HOST>
 cudaError_t launch_phase(const Geo& g, const GemvPlan* pl, const GemvArgs& a, const SG& p,
                          const __nv_bfloat16* x, const int* xexp, float* h, float* O, int n_ent_max,
                          int num_sms, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<FMT, PH>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<FMT, PH, HOST>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 1024);
     if (e != cudaSuccess) return e;
     attr = true;
@@ -841,8 +843,8 @@ cudaError_t launch_phase(const Geo& g, const GemvPlan* pl, const GemvArgs& a, co
   const CUtensorMap& m1 = PH == 1 ? pl->w[1] : pl->w[2];
   const CUtensorMap& s0 = PH == 1 ? pl->s[0] : pl->s[2];
   const CUtensorMap& s1 = PH == 1 ? pl->s[1] : pl->s[2];
-  return launch_pdl(gemv_stream_kernel<FMT, PH>, dim3(grid), dim3(kThreads), (size_t)p.smem, st, m0, m1, s0, s1, g,
-                    a, p, x, xexp, h, O);
+  return launch_pdl(gemv_stream_kernel<FMT, PH, HOST>, dim3(grid), dim3(kThreads), (size_t)p.smem, st, m0, m1, s0,
+                    s1, g, a, p, x, xexp, h, O);
 }
 
 template <int FMT>
@@ -853,14 +855,16 @@ cudaError_t launch_fmt(const Geo& g, const GemvPlan* pl, const GemvArgs& a, cons
   if (phases & 1) {
     const SG p1 = make_sg(g, 1, a.N);
     if (ev) cudaEventRecord(ev[0], st);
-    e = launch_phase<FMT, 1>(g, pl, a, p1, x, xexp, h, O, n_ent_max, num_sms, st);
+    e = a.host_pool ? launch_phase<FMT, 1, true>(g, pl, a, p1, x, xexp, h, O, n_ent_max, num_sms, st)
+                    : launch_phase<FMT, 1, false>(g, pl, a, p1, x, xexp, h, O, n_ent_max, num_sms, st);
     if (ev) cudaEventRecord(ev[1], st);
     if (e != cudaSuccess) return e;
   }
   if (phases & 2) {
     const SG p2 = make_sg(g, 2, a.N);
     if (ev) cudaEventRecord(ev[2], st);
-    e = launch_phase<FMT, 2>(g, pl, a, p2, x, xexp, h, O, n_ent_max, num_sms, st);
+    e = a.host_pool ? launch_phase<FMT, 2, true>(g, pl, a, p2, x, xexp, h, O, n_ent_max, num_sms, st)
+                    : launch_phase<FMT, 2, false>(g, pl, a, p2, x, xexp, h, O, n_ent_max, num_sms, st);
     if (ev) cudaEventRecord(ev[3], st);
   }
   return e;

@@ -68,6 +68,7 @@ struct LruSmem {
   int q_old[kMaxE];    // expert that held q[i] before the step (-1 free)
   int acc_e[kMaxE], acc_s[kMaxE];
   int eo[kMaxE];       // expert_of, staged
+  int buf[kMaxE];      // slot -> buffer map and spare buffers, staged
   unsigned long long st[kMaxE];   // stamps, staged
   unsigned char stale[kMaxE];     // occupied by an expert not routed this step
 };
@@ -76,24 +77,26 @@ struct LruSmem {
 // together (one memory round trip) and parks them in shared memory; callers
 // put other independent loads between lru_load and lru_park.
 struct LruRegs {
-  int so, eo;
+  int so, eo, buf;
   unsigned long long st, clk;
 };
-MOE_DEV LruRegs lru_load(int E, int S, const int* __restrict__ slot_of, const int* __restrict__ expert_of,
+MOE_DEV LruRegs lru_load(int E, int S, int X, const int* __restrict__ slot_of, const int* __restrict__ expert_of,
                          const unsigned long long* __restrict__ stamp,
-                         const unsigned long long* __restrict__ clock) {
+                         const unsigned long long* __restrict__ clock, const int* __restrict__ buf) {
   const int t = threadIdx.x;
   LruRegs r;
   r.so = t < E ? slot_of[t] : -1;
   r.eo = t < S ? expert_of[t] : -1;
+  r.buf = t < S + X ? buf[t] : -1;
   r.st = t < S ? stamp[t] : 0ull;
   r.clk = t == 0 ? *clock : 0ull;
   return r;
 }
-MOE_DEV void lru_park(const LruRegs& r, int E, int S, LruSmem& m) {
+MOE_DEV void lru_park(const LruRegs& r, int E, int S, int X, LruSmem& m) {
   const int t = threadIdx.x;
   if (t < E) m.so[t] = r.so;
   if (t < S) { m.eo[t] = r.eo; m.st[t] = r.st; }
+  if (t < S + X) m.buf[t] = r.buf;
   if (t == 0) m.clk = r.clk;
 }
 
@@ -103,7 +106,7 @@ MOE_DEV void lru_park(const LruRegs& r, int E, int S, LruSmem& m) {
 MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, int E, int S, int X,
                       int* __restrict__ slot_of,
                       int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
-                      unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
+                      unsigned long long* __restrict__ clock, int* __restrict__ buf, StepRecord* __restrict__ rec,
                       unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq,
                       LruSmem& m) {
   const int tid = threadIdx.x;
@@ -168,6 +171,7 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
   int* r_e = rec_expert(rec);
   int* r_s = rec_slot(rec, E);
   int* r_v = rec_evicted(rec, E);
+  int* r_b = rec_buf(rec, E);
   int4* r_n = rec_entry(rec, E);
   for (int i = tid; i < U; i += kLruThreads) {
     const int ex = m.acc_e[i], sl = m.acc_s[i];
@@ -177,9 +181,10 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
     if (i >= S) ev = m.acc_e[i - S];
     else if (i >= n_hit) ev = m.q_old[i - n_hit];
     r_v[i] = ev;
-    // physical slot: the LRU slot, or staging slot S + 1 + (i - S) for later waves
+    // buffer: the LRU slot's, or spare i - S for later waves
     const bool ok = ex >= 0 && ex < E && sl >= 0 && sl < S && i - S < X;
-    const int ps = !ok ? -1 : i < S ? sl : S + 1 + (i - S);
+    const int ps = !ok ? -1 : i < S ? m.buf[sl] : m.buf[S + (i - S)];
+    r_b[i] = ps;
     const int row0 = offs && ok ? offs[ex] : 0, nrow = offs && ok ? counts[ex] : 0;
     // first token of the access, from the per-warp token ballots of its
     // expert (tokens 32 w + lane); unknown without them
@@ -197,6 +202,7 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
       rec_expert(host_rec)[i] = ex;
       rec_slot(host_rec, E)[i] = sl;
       rec_evicted(host_rec, E)[i] = ev;
+      rec_buf(host_rec, E)[i] = ps;
     }
   }
   if (host_rec) {
@@ -236,6 +242,19 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
       stamp[sl] = clk + 1ull + (unsigned long long)i;
     }
   }
+  // a later-wave miss that keeps its slot takes over the spare buffer it was
+  // filled into, and the slot's old buffer becomes that spare (the slots and
+  // spares of these accesses are all distinct)
+  __syncthreads();   // every read of m.buf above is done
+  for (int i = max(S, U - S) + tid; i < U; i += kLruThreads) {
+    const int sl = m.acc_s[i], j = S + (i - S);
+    if (sl < 0 || sl >= S || i - S >= X) continue;
+    const int t = m.buf[sl];
+    m.buf[sl] = m.buf[j];
+    m.buf[j] = t;
+  }
+  __syncthreads();
+  if (U > S && tid < S + X) buf[tid] = m.buf[tid];
   if (tid == 0) {
     *clock = clk + (unsigned long long)U;
     if (stats) {   // fire-and-forget adds: no round trip
@@ -250,12 +269,13 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
 __global__ void __launch_bounds__(kLruThreads)
 lru_step_kernel(const int* __restrict__ counts, const int* __restrict__ offsets, int E, int S, int X,
                 int* __restrict__ slot_of, int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
-                unsigned long long* __restrict__ clock, StepRecord* __restrict__ rec,
+                unsigned long long* __restrict__ clock, int* __restrict__ buf, StepRecord* __restrict__ rec,
                 unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq) {
   __shared__ LruSmem m;
-  lru_park(lru_load(E, S, slot_of, expert_of, stamp, clock), E, S, m);
+  lru_park(lru_load(E, S, X, slot_of, expert_of, stamp, clock, buf), E, S, X, m);
   __syncthreads();
-  lru_body(counts, offsets, nullptr, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
+  lru_body(counts, offsets, nullptr, E, S, X, slot_of, expert_of, stamp, clock, buf, rec, stats, host_rec, seq,
+           m);
 }
 
 // Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
@@ -265,8 +285,8 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
                   int* __restrict__ offsets, int* __restrict__ row_of, int* __restrict__ tok_of,
                   int* __restrict__ slot_of, int* __restrict__ expert_of,
                   unsigned long long* __restrict__ stamp, unsigned long long* __restrict__ clock,
-                  StepRecord* __restrict__ rec, unsigned long long* __restrict__ stats, StepRecord* host_rec,
-                  unsigned long long seq) {
+                  int* __restrict__ buf, StepRecord* __restrict__ rec, unsigned long long* __restrict__ stats,
+                  StepRecord* host_rec, unsigned long long seq) {
   __shared__ LruSmem m;
   extern __shared__ uint32_t dsm[];
   uint32_t* cm = dsm;                                            // [E][4]
@@ -277,10 +297,10 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
   // the table was last written by the previous step's tail, which finished
   // before the router began: its loads go out before waiting for the router
   pdl_trigger();
-  const LruRegs lr = lru_load(E, S, slot_of, expert_of, stamp, clock);
+  const LruRegs lr = lru_load(E, S, X, slot_of, expert_of, stamp, clock, buf);
   pdl_wait();
   perm::stage_rows(idx, N, k, 0, rows);
-  lru_park(lr, E, S, m);
+  lru_park(lr, E, S, X, m);
   __syncthreads();
   perm::build_ballots_par(rows, k, E, N, tb, cm);
   const int e = threadIdx.x;
@@ -305,7 +325,7 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
     }
   }
   __syncthreads();
-  lru_body(cnt, off, cm, E, S, X, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq, m);
+  lru_body(cnt, off, cm, E, S, X, slot_of, expert_of, stamp, clock, buf, rec, stats, host_rec, seq, m);
 }
 
 __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expert_of,
@@ -334,16 +354,16 @@ __global__ void counts_from_list_kernel(const int* __restrict__ list, int n, int
 
 cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets, int* slot_of,
                             int* expert_of, unsigned long long* stamp, unsigned long long* clock,
-                            StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                            int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
                             unsigned long long seq, cudaStream_t st) {
   lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, offsets, g.E, g.S, g.X, slot_of, expert_of, stamp,
-                                             clock, rec, stats, host_rec, seq);
+                                             clock, buf, rec, stats, host_rec, seq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, int* offsets,
                               int* row_of, int* tok_of, int* slot_of, int* expert_of,
-                              unsigned long long* stamp, unsigned long long* clock,
+                              unsigned long long* stamp, unsigned long long* clock, int* buf,
                               StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
                               unsigned long long seq, cudaStream_t st) {
   const size_t smem = (size_t)g.E * perm::kPermWarps * 4 + (size_t)2 * g.E * 4 +
@@ -356,7 +376,7 @@ cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, 
     attr = true;
   }
   return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, g.X, counts,
-                    offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, rec, stats, host_rec, seq);
+                    offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, buf, rec, stats, host_rec, seq);
 }
 
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,

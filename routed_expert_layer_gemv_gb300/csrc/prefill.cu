@@ -106,13 +106,14 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
   __syncthreads();
   const int* ae = reinterpret_cast<const int*>(rec + 1);
   const int* as = ae + E;
+  const int* abuf = ae + 3 * E;
   for (int e0 = 0; e0 < n_ent; e0 += blockDim.x) {
     const int i = e0 + threadIdx.x;
     int slot = -1, r0 = 0, nrows = 0;
     if (i < nr) {
-      const int ex = ae[b + i], ls = as[b + i];
-      if (ex >= 0 && ex < E && ls >= 0 && ls < S && b + i - S < X) {
-        slot = access_slot(as, S, b + i);
+      const int ex = ae[b + i], ls = as[b + i], bb = abuf[b + i];
+      if (ex >= 0 && ex < E && ls >= 0 && ls < S && b + i - S < X && bb >= 0 && bb <= S + X && bb != S) {
+        slot = bb;
         r0 = offsets[ex];
         nrows = offsets[ex + 1] - r0;
       }
