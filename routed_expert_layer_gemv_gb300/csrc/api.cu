@@ -36,8 +36,6 @@
 using namespace moe;
 
 constexpr size_t kDirectHostBytes = 256 * 1024;   // host x / y read and written in place up to this size
-constexpr int kMissChunks = 4;   // memcpy fills: the misses' expert FFN runs in up to this many chunks
-constexpr int kMissesPerChunk = 3;   // ... of at least this many misses each
 
 struct moe_layer {
   moe_layer_desc desc{};
@@ -815,12 +813,12 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     // hits' phase 1, whose early start must not wait for these launches); each
     // finds its part of the miss list in the record on the device, so the
     // copies start when the routing ends, not after the host has read it
-    const int max_pre = std::max(1, std::min(kMissChunks, std::min(g.E, N * g.k) / kMissesPerChunk));
+    const int max_pre = miss_chunks(std::min(g.E, N * g.k));
     cudaStream_t fs = L->fill;
     MOE_CUDA(L, cudaStreamWaitEvent(fs, L->ev_route, 0));
     cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
     for (int c = 0; c < max_pre; ++c) {
-      MOE_CUDA(L, launch_fill_sm(g, L->rec, c, kMissChunks, kMissesPerChunk, L->pool_dev, L->slots, fs));
+      MOE_CUDA(L, launch_fill_sm(g, L->rec, c, L->pool_dev, L->slots, fs));
       MOE_CUDA(L, cudaEventRecord(L->ev_chunk[c], fs));
     }
     prof_end(pf, fs);
@@ -870,7 +868,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       // the misses' expert FFN runs in chunks, each once its own fills have
       // landed, while later fills still run; a chunk pays one expert-FFN
       // launch ramp, so only long miss lists are cut
-      n_chunks = std::max(1, std::min(kMissChunks, (U - n_hit) / kMissesPerChunk));
+      n_chunks = miss_chunks(U - n_hit);
     }
     if (any_miss && sm_fill) {
       fill_bytes = (size_t)(U - n_hit) * g.ebytes;   // the copy kernels were queued behind the routing
@@ -883,7 +881,9 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       cudaEvent_t* pf = prof_begin(L, MOE_PROF_FILL, fs);
       const int nm = U - n_hit;
       for (int c = 0; c < n_chunks; ++c) {
-        const int c0 = n_hit + (int)((long long)nm * c / n_chunks), c1 = n_hit + (int)((long long)nm * (c + 1) / n_chunks);
+        int lo, hi;
+        miss_chunk(nm, c, n_chunks, &lo, &hi);
+        const int c0 = n_hit + lo, c1 = n_hit + hi;
         for (int i = c0; i < c1;) {
           int j = i + 1;
           while (j < c1 && ae[j] == ae[j - 1] + 1 && ab[j] == ab[j - 1] + 1) ++j;
@@ -914,7 +914,9 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       for (int c = 0; c < n_chunks; ++c) {
         MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_chunk[c], 0));
         a.chunk = c;
-        const int c0 = n_hit + (int)((long long)nm * c / n_chunks), c1 = n_hit + (int)((long long)nm * (c + 1) / n_chunks);
+        int lo, hi;
+        miss_chunk(nm, c, n_chunks, &lo, &hi);
+        const int c0 = n_hit + lo, c1 = n_hit + hi;
         grc = gemv(c1 - c0, 3);
         if (grc) return grc;
       }

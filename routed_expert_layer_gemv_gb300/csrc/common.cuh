@@ -122,6 +122,35 @@ enum RangeMode : int { kRangeHits = 0, kRangeMisses = 1, kRangeAll = 2 };
 // step the LRU kernel swaps the two buffers: the slot's old buffer becomes
 // the spare.  No expert is ever copied within the pool.
 
+// A long miss list is cut into chunks, each filled and then computed on its
+// own so its expert FFN runs while later fills are still in flight: up to
+// kMissChunks chunks of at least kMissesPerChunk misses.  The last chunk takes
+// kMissesPerChunk misses (its expert FFN, which runs after the last fill, is
+// the step's tail) and the others share the rest equally.  Chunk c of nch over
+// m misses is [lo, hi) (offsets from the first miss); host and device use this
+// one split.
+constexpr int kMissChunks = 4;
+constexpr int kMissesPerChunk = 3;
+__host__ __device__ inline int miss_chunks(int m) {
+  const int n = m / kMissesPerChunk;
+  return n < 1 ? 1 : n > kMissChunks ? kMissChunks : n;
+}
+__host__ __device__ inline void miss_chunk(int m, int c, int nch, int* lo, int* hi) {
+  if (nch <= 1) {
+    *lo = 0;
+    *hi = m;
+    return;
+  }
+  const int rest = m - (m < kMissesPerChunk ? m : kMissesPerChunk);
+  if (c >= nch - 1) {
+    *lo = rest;
+    *hi = m;
+    return;
+  }
+  *lo = (int)((long long)rest * c / (nch - 1));
+  *hi = (int)((long long)rest * (c + 1) / (nch - 1));
+}
+
 // ---------------------------------------------------------------- launchers
 // router.cu
 // counter: a zeroed device word (enables the one-launch path for N <= 64), or null
@@ -167,7 +196,7 @@ struct GemvArgs {
   const int* tok_of;           // [N*k]
   int N;
   int mode;                    // RangeMode
-  int chunk, n_chunks;         // kRangeMisses: the misses split in n_chunks equal runs, this launch takes one
+  int chunk, n_chunks;         // kRangeMisses: chunk `chunk` of n_chunks (miss_chunk) of the misses
   const uint8_t* host_pool;    // kRangeAll: device address of the pinned host pool the misses stream from
   int with_shared;             // also run the shared expert (rows N*k .. N*k+N)
   int* err;                    // set to 1 when a bounded wait gives up
@@ -209,11 +238,10 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
 cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses,
                              const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
 // the same copy by kFillSms CTAs, one per SM, for chunk `chunk` of the miss
-// list cut into max(1, min(max_chunks, misses / per_chunk)) chunks; the decode
-// expert GEMV leaves those SMs free
+// list (miss_chunk); the decode expert GEMV leaves those SMs free
 constexpr int kFillSms = 12;
-cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, int max_chunks, int per_chunk,
-                           const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st);
+cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, const uint8_t* pool_dev,
+                           uint8_t* slots, cudaStream_t st);
 // dst <- src (bytes a multiple of 16, 16-byte aligned; src may be mapped host memory)
 cudaError_t launch_copy16(void* dst, const void* src, size_t bytes, cudaStream_t st);
 // combine.cu

@@ -56,10 +56,9 @@ fill_copy_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, const 
 // shared memory they reserve, more than half an SM's, keeps two off one SM and
 // keeps the expert GEMV, which takes nearly all of it, off theirs), copy the
 // chunk's misses from the pinned host pool to their buffers.  The m = U - n_hit
-// misses form nch = max(1, min(max_chunks, m / per_chunk)) chunks, chunk c
-// being accesses [n_hit + m c / nch, n_hit + m (c + 1) / nch) -- the split the
-// host makes from its copy of the record -- and a launch for c >= nch copies
-// nothing.  Each expert is cut into pieces of kFillPiece bytes dealt
+// misses form miss_chunks(m) chunks split by miss_chunk -- the split the host
+// makes from its copy of the record -- and a launch for a chunk past them
+// copies nothing.  Each expert is cut into pieces of kFillPiece bytes dealt
 // round-robin to the CTAs; a piece is one load of kFillSmUnroll x 16 bytes per
 // thread, all in flight before the stores.
 constexpr int kFillSmThreads = 1024;
@@ -68,14 +67,16 @@ constexpr size_t kFillPiece = (size_t)kFillSmThreads * kFillSmUnroll * 16;
 constexpr int kFillSmSmem = 120 * 1024;
 
 __global__ void __launch_bounds__(kFillSmThreads, 1)
-fill_sm_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int chunk, int max_chunks,
-               int per_chunk, const uint8_t* __restrict__ pool, uint8_t* __restrict__ slots, size_t ebytes) {
+fill_sm_kernel(const StepRecord* __restrict__ rec, int E, int S, int X, int chunk,
+               const uint8_t* __restrict__ pool, uint8_t* __restrict__ slots, size_t ebytes) {
   const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
   const int m = U - nh;
-  const int nch = max(1, min(max_chunks, m / per_chunk));
+  const int nch = miss_chunks(m);
   if (chunk >= nch) return;
-  const int i0 = nh + (int)((long long)m * chunk / nch);
-  const int i1 = min(nh + (int)((long long)m * (chunk + 1) / nch), S + X);
+  int lo, hi;
+  miss_chunk(m, chunk, nch, &lo, &hi);
+  const int i0 = nh + lo;
+  const int i1 = min(nh + hi, S + X);
   if (i1 <= i0) return;
   const int* ab = rec_buf(const_cast<StepRecord*>(rec), E);
   const int* ae = rec_expert(const_cast<StepRecord*>(rec));
@@ -130,16 +131,16 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
   return cudaGetLastError();
 }
 
-cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, int max_chunks, int per_chunk,
-                           const uint8_t* pool_dev, uint8_t* slots, cudaStream_t st) {
+cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, const uint8_t* pool_dev,
+                           uint8_t* slots, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(fill_sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFillSmSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  fill_sm_kernel<<<kFillSms, kFillSmThreads, kFillSmSmem, st>>>(rec, g.E, g.S, g.X, chunk, max_chunks,
-                                                               per_chunk, pool_dev, slots, g.ebytes);
+  fill_sm_kernel<<<kFillSms, kFillSmThreads, kFillSmSmem, st>>>(rec, g.E, g.S, g.X, chunk, pool_dev, slots,
+                                                               g.ebytes);
   return cudaGetLastError();
 }
 

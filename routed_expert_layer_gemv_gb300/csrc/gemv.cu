@@ -145,10 +145,12 @@ MOE_DEV int count_entries(const Geo& g, const GemvArgs& a, int* base, int* nr) {
   if (a.mode == kRangeAll) {
     e = U;
   } else if (a.mode != kRangeHits) {
-    // misses [nh, U), or chunk `chunk` of n_chunks equal runs of them
-    const int C = max(a.n_chunks, 1), c = min(max(a.chunk, 0), C - 1), nm = U - nh;
-    b = nh + (int)((long long)nm * c / C);
-    e = nh + (int)((long long)nm * (c + 1) / C);
+    // misses [nh, U), or chunk `chunk` of n_chunks of them
+    const int C = max(a.n_chunks, 1), c = min(max(a.chunk, 0), C - 1);
+    int lo, hi;
+    miss_chunk(U - nh, c, C, &lo, &hi);
+    b = nh + lo;
+    e = nh + hi;
   }
   *base = b;
   *nr = max(0, e - b);
