@@ -8,7 +8,8 @@ tokens per step on AR(1) hidden states (rho 0.9).  A step is one moe_forward:
 router, permutation, LRU update, miss fills, expert FFN, combine.  Misses are
 filled the library's default way (at batch 1 and 4 the expert GEMV reads them
 from host memory itself, at batch 16 a copy kernel on 12 reserved SMs does);
-the other fill modes are timed beside it per batch.
+the other fill modes are timed beside it per batch, and so is an all-resident
+warm run (n_slots = E, every expert installed: no fills, HBM bytes only).
 
 Timing: W warm-up steps, then K timed steps per batch size, each bracketed by
 CUDA events on the launching stream; the L2 is flushed (a 512 MiB write)
@@ -202,6 +203,60 @@ def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile, fi
                 launches=launches,
                 misses=d_misses, distinct=d_distinct, fill_bytes=fill_b, prof=prof,
                 gateup_bytes=ffn_bytes)
+
+
+def run_decode_resident(args, batch, torch, capi, wl, build_layer, flush, st):
+    """The same decode steps with every expert resident (n_slots = E, expert e
+    installed in slot e): no misses and no fills, so a step moves only HBM
+    bytes.  Returns the step time and the step's algorithmic bytes: the
+    distinct experts' weights (B_e = 3 d f (1/2 + 1/32) each), W_r in fp32
+    (4 E d) and x in / y out (4 N d)."""
+    import dataclasses
+    spec = dataclasses.replace(wl.DECODE_35B.layer, n_slots=wl.DECODE_35B.layer.E)
+    seed = wl.DECODE_35B.seed
+    W, K = args.warmup, args.steps
+    x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
+    xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
+    L = build_layer(spec, seed, batch, install_all=True)
+    y = torch.empty(batch, spec.d_model, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(st):
+        for t in range(W):
+            L.forward(xs[t], y, stream=st)
+    torch.cuda.synchronize()
+    stats0 = capi.moe_stats(L.h)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(st):
+        for t in range(K):
+            flush.zero_()
+            ev[t][0].record(st)
+            L.forward(xs[W + t], y, stream=st)
+            ev[t][1].record(st)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    stats1 = capi.moe_stats(L.h)
+    L.close()
+    d, f, E = spec.d_model, spec.d_ff, spec.E
+    b_e = 3 * d * f * (1 / 2 + 1 / spec.block)
+    nbytes = (stats1[1] - stats0[1]) * b_e + K * (4 * E * d + 4 * batch * d)
+    return dict(batch=batch, steps=K, ms=ms, tokens=K * batch, bytes=nbytes,
+                misses=stats1[3] - stats0[3])
+
+
+def measure_h2d(torch, nbytes=256 << 20):
+    """Host-to-device GB/s of one copy from pinned memory (best of 3): the
+    ceiling the miss fills are held against."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = None
+    for _ in range(4):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b)
+        best = t if best is None else min(best, t)
+    return nbytes / (best / 1000.0) / 1e9
 
 
 def run_decode_e2e(args, batch, torch, capi, wl, build_layer, flush):
@@ -401,6 +456,8 @@ def main():
     fruns = {name: [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False, m) for b in batches]
              for name, m in modes.items()}
     e2e_runs = [run_decode_e2e(args, b, torch, capi, wl, build_layer, flush) for b in batches]
+    rruns = [run_decode_resident(args, b, torch, capi, wl, build_layer, flush, st) for b in batches]
+    h2d = measure_h2d(torch)
 
     ms = sum(r["ms"] for r in runs)
     tokens = sum(r["tokens"] for r in runs)
@@ -430,7 +487,7 @@ def main():
             "bytes_per_launch": g_bytes / max(g_n, 1), "ms_per_launch": g_ms / max(g_n, 1)}
 
     per_batch = {}
-    for i, (r, e, pr) in enumerate(zip(runs, e2e_runs, pruns)):
+    for i, (r, e, pr, rr) in enumerate(zip(runs, e2e_runs, pruns, rruns)):
         p = pr["prof"]
         per_batch[str(r["batch"])] = {
             "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
@@ -442,6 +499,12 @@ def main():
             "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
             "tokens_per_s_by_fill_mode": {name: fr[i]["tokens"] / (fr[i]["ms"] / 1000.0)
                                           for name, fr in fruns.items()},
+            "all_resident": {
+                "tokens_per_s": rr["tokens"] / (rr["ms"] / 1000.0),
+                "ms_per_step": rr["ms"] / rr["steps"],
+                "hbm_GB_per_s": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9,
+                "frac_of_measured_hbm": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9 / peak,
+                "misses": rr["misses"]},
         }
     prefill = None
     if not args.no_prefill:
@@ -468,6 +531,10 @@ def main():
                              "roofline from a second, instrumented pass of the same steps with "
                              "MOE_FILL_KERNEL fills",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "h2d_GB_per_s_measured": h2d,
+                   "all_resident": "per_batch.all_resident: the same steps with n_slots = E and every "
+                                   "expert installed (no fills); bytes = distinct experts' weights + "
+                                   "W_r (fp32) + x / y per step",
                    "per_batch": per_batch},
         "roofline": roof,
         "cpu_baseline": cpu,
