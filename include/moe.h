@@ -205,7 +205,7 @@ int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
  * the host still reads the record to launch the misses' expert FFN, so the
  * copies start as soon as the routing ends and pay no per-copy cost of the
  * copy engine.  The prefill regime fills with cudaMemcpyAsync in this mode,
- * since its GEMM takes every SM.
+ * since its GEMM takes every SM, and so does a GPU of at most 24 SMs.
  * MOE_FILL_FUSED: no separate copy: one decode expert-FFN launch covers the
  * step's hits and misses, reading each miss's weights from the pinned pool
  * over the host link (the pool must be device-addressable) and writing them

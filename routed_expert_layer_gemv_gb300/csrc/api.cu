@@ -725,6 +725,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   // spare buffer, SM-copy fills beyond
   int fmode = L->fill_mode;
   if (fmode == MOE_FILL_AUTO) fmode = std::min(g.E, N * g.k) <= g.S ? MOE_FILL_FUSED : MOE_FILL_KERNEL;
+  // SM fills need the GPU to keep most of its SMs for the expert GEMV
+  if (fmode == MOE_FILL_KERNEL && L->num_sms <= 2 * kFillSms) fmode = MOE_FILL_MEMCPY;
   // fused fills (decode): one expert-FFN launch covers every access and reads
   // the misses' weights from the host pool itself, writing them on to their
   // slots, so no separate copy and no host round trip
