@@ -164,6 +164,34 @@ def test_lru_touch_matches_slot_table(E, S, per_step, steps):
     L.close()
 
 
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+def test_lru_touch_fills_land_in_their_slots(fmt):
+    # touches of more distinct experts than slots (several waves) with a host
+    # pool: every slot must then hold, bit for bit, the expert the table names
+    spec = small_spec(E=20, k=4, d_model=256, d_ff=256, n_slots=5, fmt=fmt)
+    seed = 17
+    L = build_layer(spec, seed, 16)
+    T = SlotTable(spec.E, spec.n_slots)
+    g = np.random.default_rng(5)
+    for step in range(6):
+        routed = [int(v) for v in g.choice(spec.E, int(g.integers(3, 14)), replace=False)]
+        capi.moe_lru_touch(L.h, routed)
+        T.step(routed)
+        eo, _, _ = _state(L, spec.n_slots)
+        assert eo == T.expert_of
+        for slot, e in enumerate(eo):
+            if e < 0:
+                continue
+            w = wl.expert_weights(spec, seed, e)
+            for m, name in enumerate(("gate", "up", "down")):
+                mat = w[name]
+                out = torch.empty(mat.rows, mat.K, dtype=torch.float32, device="cuda")
+                capi.moe_debug_dequant(L.h, slot, m, out)
+                ref = formats.dequant(mat.codes, mat.scales, mat.tscale, fmt)
+                assert np.array_equal(out.cpu().numpy().astype(np.float64), ref), (step, slot, e, name)
+    L.close()
+
+
 def test_lru_install_and_state_roundtrip():
     spec = small_spec(E=10, k=2, n_slots=4)
     L = build_layer(spec, 1, 8)
