@@ -213,7 +213,7 @@ int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
  * MOE_FILL_DEVICE, moe_forward_info reports -1 counts).  The prefill regime
  * fills with cudaMemcpyAsync in this mode.
  * MOE_FILL_AUTO: per decode call, MOE_FILL_FUSED while min(E, N k) <= n_slots
- * (no access can need a staging slot), else MOE_FILL_KERNEL.
+ * (no access can need a spare buffer), else MOE_FILL_KERNEL.
  * MOE_ERR_STATE if the registered pool is not device-addressable (every mode
  * but MOE_FILL_MEMCPY). */
 #define MOE_FILL_MEMCPY 0

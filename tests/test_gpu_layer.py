@@ -138,8 +138,8 @@ def test_decode_284b_shape_kernel_fill(fill):
 @pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
 def test_staged_misses_land_in_their_lru_slots(fill, fmt):
     # more distinct experts per step than slots: misses past the first wave are
-    # filled into staging slots and committed afterwards; every LRU slot must
-    # then hold exactly the expert the slot table names
+    # filled into spare buffers that then become their slots' buffers; every
+    # LRU slot must then hold exactly the expert the slot table names
     spec = small_spec(E=32, k=4, d_model=256, d_ff=256, n_slots=6, fmt=fmt, has_shared=True)
     seed, batch = 13, 8
     experts = CachedExperts(spec, seed)
