@@ -118,7 +118,15 @@ int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out);
 
 /* Create a layer on the current device: validates the descriptor, allocates
  * the slot pool, table and workspaces, creates the fill stream.  The cache
- * starts empty (every slot free).  MOE_ERR_ARG on an invalid descriptor,
+ * starts empty (every slot free).  The arguments are the layer's shape (E
+ * routed experts, top-k, d_model, d_ff: the MoE layer the FreeToken pages
+ * serve, "FreeToken：把 284B MoE 塞进游戏 PC", zhichai.net, §二 "Decode"
+ * paragraph: per token only a few of many experts run) and the number of
+ * GPU expert-cache slots (the same page's LRU expert cache, §二 "LRU 为什么赢";
+ * juejin.cn overview, §二 "全局 LRU 专家缓存"), plus the weight format (MXFP4
+ * or NVFP4 checkpoints, zhichai.net §五) and the optional shared expert
+ * (ananclaw.com explainer, §核心方法 4, shared experts as an architecture
+ * axis).  MOE_ERR_ARG on an invalid descriptor,
  * MOE_ERR_UNSUPPORTED when d_model or d_ff exceeds 8192 (the decode kernels
  * stage one token group's activations in shared memory), MOE_ERR_OOM when
  * device memory runs out (nothing is leaked). */
@@ -147,7 +155,11 @@ int moe_set_shared_expert(moe_layer_t layer, const void* weights);
  * is registered.  (The expert cache of the zhichai.net page, §二.) */
 int moe_cache_install(moe_layer_t layer, int expert, int slot, void* stream);
 
-/* Apply one step's accesses to the device slot table, as moe_forward does:
+/* Apply one step's accesses to the device slot table, as moe_forward does
+ * (the per-step update of the LRU expert cache: "FreeToken：把 284B MoE 塞进游戏
+ * PC", zhichai.net, §二 "LRU 为什么赢" -- recently routed experts stay on the
+ * GPU, misses are loaded from host memory; the per-step access order below is
+ * this library's reading, the pages leave it open):
  * the distinct experts of experts[0..n) are accessed hits first (ascending
  * id), then misses (ascending id); a miss takes the lowest free slot, else
  * evicts the least recently used expert.  Misses are filled from the host
@@ -170,7 +182,12 @@ int moe_lru_set_state(moe_layer_t layer, const int* expert_of_slot,
                       const uint64_t* stamp, uint64_t clock);
 
 /* One forward pass: x bf16 [N, d_model] -> y bf16 [N, d_model], ordered on
- * `stream`.  x and y may be device pointers or host pointers (then staged
+ * `stream`.  One step of the pages' MoE layer: route each token to k experts,
+ * serve the routed experts from the GPU expert cache (hits) or load them from
+ * host memory first (misses), run them and combine ("FreeToken：把 284B MoE
+ * 塞进游戏 PC", zhichai.net, §二 "Decode" for a decode step, "Prefill：把计算
+ * 藏进传输" for a prefill chunk; the layer formula is the standard one given at
+ * the top of this file, since the pages print none).  x and y may be device pointers or host pointers (then staged
  * through the layer's workspace, and the call returns after y is written).
  * N == 0 is a no-op; 0 < N <= max_tokens.  With misses (possible unless
  * every expert is resident) the call waits on the host for the step's routing
@@ -254,6 +271,52 @@ int moe_debug_router(moe_layer_t layer, const void* x, int N, int* idx,
 int moe_debug_permute(moe_layer_t layer, const int* idx, int N, int* counts,
                       int* offsets, int* row_of, int* tok_of, void* stream);
 
+/* What the last moe_forward on this layer decided, copied from the layer's
+ * workspaces into caller device arrays (any may be NULL), ordered on
+ * `stream`: idx int32 [N, k] and gates fp32 [N, k] of its router, counts
+ * [E], offsets [E+1], row_of [N*k] and tok_of [N*k] of its permutation (the
+ * arrays the expert FFN and the combine of that call used), N = that call's
+ * token count (*n_out, may be NULL).  MOE_ERR_STATE before the first
+ * moe_forward. */
+int moe_debug_last_step(moe_layer_t layer, int* idx, float* gates, int* counts, int* offsets,
+                        int* row_of, int* tok_of, int* n_out, void* stream);
+
+/* The expert FFN's intermediate values of the last moe_forward, copied into
+ * caller device arrays (any may be NULL), ordered on `stream`; rows =
+ * N*k permuted rows (+ N shared-expert rows, token order, when the layer has
+ * one).  After a decode call: h fp32 [rows, 2*d_ff] = W_g x | W_u x of each
+ * row (block scales and tensor scales applied).  After a prefill call:
+ * hq_codes [rows, d_ff/2] and hq_scales [rows, d_ff/block], the FP4 codes and
+ * block scales of h = SiLU(W_g x) * (W_u x) that the down GEMM consumed.
+ * MOE_ERR_STATE when the requested arrays were not produced by that call. */
+int moe_debug_last_hidden(moe_layer_t layer, float* h, uint8_t* hq_codes, uint8_t* hq_scales,
+                          void* stream);
+
+/* Error-path hooks for tests.  They act on the host only: nothing makes the
+ * GPU fault, trap or wait without bound.
+ * MOE_INJECT_FILL: the next host-issued fill of this layer (moe_forward in
+ * MOE_FILL_MEMCPY mode, moe_lru_touch, moe_cache_install) fails before its
+ * cudaMemcpyAsync is issued.  The call returns MOE_ERR_FILL; a forward or
+ * touch step's misses are then dropped from the cache (their slots become
+ * free, so a later step fills them again) and y is not written.
+ * MOE_INJECT_WAIT_LIMIT: the bounded device waits of the next moe_forward's
+ * decode expert-FFN launches give up after `arg` SM clock cycles (instead of
+ * about 2 s); a launch whose wait gives up sets the layer's error word,
+ * finishes without further work, and the next moe_forward returns
+ * MOE_ERR_TIMEOUT (the slot table, updated before the expert FFN, stays
+ * consistent).  MOE_INJECT_NONE clears both. */
+#define MOE_INJECT_NONE 0
+#define MOE_INJECT_FILL 1
+#define MOE_INJECT_WAIT_LIMIT 2
+int moe_debug_inject(moe_layer_t layer, int what, long long arg);
+
+/* Process-wide test hook: the nth device or pinned-host allocation the
+ * library makes from now on fails without being attempted (1 = the next one,
+ * 0 = none), as if the memory had run out.  live_out (2 entries, may be NULL)
+ * receives the number of device and pinned-host allocations the library holds
+ * at the time of the call, for leak checks. */
+int moe_debug_alloc_fault(long long nth, long long* live_out);
+
 /* Dequantised fp32 weights of matrix m (0 gate, 1 up, 2 down) of the expert
  * in slot `slot` (slot -1: the shared expert), written row-major to out. */
 int moe_debug_dequant(moe_layer_t layer, int slot, int m, float* out, void* stream);
@@ -274,12 +337,17 @@ int moe_debug_actquant(moe_layer_t layer, const float* v, int rows, int K,
  * ids idx [N, k]; all device pointers, owned by the caller) without a layer
  * handle and without allocating anything: its scratch is one fixed 2 MiB array
  * in the library's device memory, held on every GPU that loads the library
- * until the process exits.  Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32),
+ * until the process exits.  Each row of idx must hold k distinct ids in
+ * [0, E), ascending; ids outside [0, E) are skipped (their row_of entry is -1)
+ * and duplicate ids in a row give an unspecified permutation, but neither
+ * makes the kernels read or write outside the caller's arrays.  Limits:
+ * 1 <= E <= 1024, 1 <= k <= min(E, 32),
  * N * k <= 262144 and ceil(N / 128) * E <= 262144; a larger request returns
  * MOE_ERR_ARG and, when errbuf is not NULL, the reason as text in the caller's
- * errbuf (errbuf_len bytes, NUL-terminated).  The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress); make that first call
- * before any stream capture.  Every call shares the one array and finds the
+ * errbuf (errbuf_len bytes, NUL-terminated).  The first call on a device (and
+ * the first after that device's context was destroyed and re-created, e.g. by
+ * cudaDeviceReset) looks up the array's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  Every call shares the one array and finds the
  * previous call's contents in it (each entry a call reads, that call has
  * written first, so nothing needs clearing); calls that overlap on the GPU --
  * on different streams or from different threads -- race, so the caller must

@@ -37,6 +37,10 @@ MOE_FILL_KERNEL = 2
 MOE_FILL_FUSED = 3
 MOE_FILL_AUTO = 4
 
+MOE_INJECT_NONE = 0
+MOE_INJECT_FILL = 1
+MOE_INJECT_WAIT_LIMIT = 2
+
 MOE_REGIME_AUTO = 0
 MOE_REGIME_DECODE = 1
 MOE_REGIME_PREFILL = 2
@@ -84,6 +88,10 @@ _SIGS = {
     "moe_status_string": ([_I], C.c_char_p),
     "moe_debug_router": ([_P, _P, _I, _P, _P, _P, _P], _I),
     "moe_debug_permute": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
+    "moe_debug_last_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P], _I),
+    "moe_debug_last_hidden": ([_P, _P, _P, _P, _P], _I),
+    "moe_debug_inject": ([_P, _I, C.c_longlong], _I),
+    "moe_debug_alloc_fault": ([C.c_longlong, _P], _I),
     "moe_debug_dequant": ([_P, _I, _I, _P, _P], _I),
     "moe_debug_actquant": ([_P, _P, _I, _I, _P, _P, _I, _P], _I),
     "moe_permute_noalloc": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, C.c_char_p, C.c_size_t], _I),
@@ -248,6 +256,32 @@ def moe_debug_router(h, x, N, idx, gates, logits=None, stream=None) -> None:
 def moe_debug_permute(h, idx, N, counts, offsets, row_of, tok_of, stream=None) -> None:
     check(lib().moe_debug_permute(h, _ptr(idx), N, _ptr(counts), _ptr(offsets), _ptr(row_of),
                                   _ptr(tok_of), _stream(stream)), h)
+
+
+def moe_debug_last_step(h, idx=None, gates=None, counts=None, offsets=None, row_of=None,
+                        tok_of=None, stream=None) -> int:
+    """Copies the last moe_forward's router and permutation arrays into the
+    given device tensors; returns that call's token count."""
+    n = C.c_int(0)
+    check(lib().moe_debug_last_step(h, _ptr(idx), _ptr(gates), _ptr(counts), _ptr(offsets),
+                                    _ptr(row_of), _ptr(tok_of), C.byref(n), _stream(stream)), h)
+    return n.value
+
+
+def moe_debug_last_hidden(h, hidden=None, hq_codes=None, hq_scales=None, stream=None) -> None:
+    check(lib().moe_debug_last_hidden(h, _ptr(hidden), _ptr(hq_codes), _ptr(hq_scales),
+                                      _stream(stream)), h)
+
+
+def moe_debug_inject(h, what: int, arg: int = 0) -> None:
+    check(lib().moe_debug_inject(h, what, arg), h)
+
+
+def moe_debug_alloc_fault(nth: int):
+    """Arms the allocation fault (0 disarms); returns the live (device, pinned) allocation counts."""
+    live = (C.c_longlong * 2)()
+    check(lib().moe_debug_alloc_fault(nth, live))
+    return live[0], live[1]
 
 
 def moe_debug_dequant(h, slot: int, m: int, out, stream=None) -> None:

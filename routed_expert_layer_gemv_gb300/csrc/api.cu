@@ -27,6 +27,9 @@
 #include <cstdio>
 #include <chrono>
 #include <cstring>
+#include <atomic>
+#include <map>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -34,6 +37,25 @@
 #include "common.cuh"
 
 using namespace moe;
+
+namespace moe {
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;   // (kernel, device) -> limit set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kernel, dev);
+  const auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[key] = bytes;
+  return e;
+}
+
+}  // namespace moe
 
 constexpr size_t kDirectHostBytes = 256 * 1024;   // host x / y read and written in place up to this size
 
@@ -108,9 +130,26 @@ struct moe_layer {
   size_t prof_used = 0;
   std::vector<int> prof_kind;          // one entry per timed launch (pair of events)
   int launches = 0;                    // kernels launched by the current call
+  int last_N = 0;                      // tokens of the last moe_forward (0: none yet)
+  bool inject_fill = false;            // test hook: the next host-issued fill fails before its copy
+  long long inject_wait = 0;           // test hook: wait limit (cycles) of the next forward's expert FFN
+  bool last_prefill = false;           // regime of the last moe_forward
 };
 
 namespace {
+
+// Test hooks of the error paths (moe_debug_alloc_fault): the nth allocation
+// from now fails without being attempted; live counts of what the library
+// holds, for leak checks.
+std::atomic<long long> g_alloc_countdown{0};
+std::atomic<long long> g_live_dev{0}, g_live_host{0};
+
+bool alloc_fault_due() {
+  long long c = g_alloc_countdown.load();
+  while (c > 0)
+    if (g_alloc_countdown.compare_exchange_weak(c, c - 1)) return c == 1;
+  return false;
+}
 
 int fail(moe_layer* L, int code, const char* fmt, ...) {
   if (L) {
@@ -193,24 +232,49 @@ Geo make_geo(const moe_layer_desc* d, const moe_expert_layout* l) {
 template <class T>
 int dalloc(moe_layer* L, T** p, size_t bytes) {
   void* q = nullptr;
+  if (alloc_fault_due()) return fail(L, MOE_ERR_OOM, "cudaMalloc(%zu) failed: injected by the test hook", bytes);
   cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(L, MOE_ERR_OOM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
   }
   L->dev_allocs.push_back(q);
+  g_live_dev++;
   *p = static_cast<T*>(q);
   return MOE_OK;
+}
+
+// Mapped pinned host memory (the device address is looked up by the caller).
+int halloc(moe_layer* L, void** p, size_t bytes) {
+  *p = nullptr;
+  if (alloc_fault_due()) return fail(L, MOE_ERR_OOM, "cudaHostAlloc(%zu) failed: injected by the test hook", bytes);
+  if (cudaHostAlloc(p, bytes, cudaHostAllocMapped) != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return fail(L, MOE_ERR_OOM, "cudaHostAlloc(%zu) failed", bytes);
+  }
+  g_live_host++;
+  return MOE_OK;
+}
+
+void hfree(void* p) {
+  if (p) {
+    cudaFreeHost(p);
+    g_live_host--;
+  }
 }
 
 void release(moe_layer* L) {
   for (cudaEvent_t e : L->prof_pool) cudaEventDestroy(e);
   L->prof_pool.clear();
-  for (void* p : L->dev_allocs) cudaFree(p);
+  for (void* p : L->dev_allocs) {
+    cudaFree(p);
+    g_live_dev--;
+  }
   L->dev_allocs.clear();
-  if (L->pinned_rec) cudaFreeHost(L->pinned_rec);
+  hfree(L->pinned_rec);
   L->pinned_rec = nullptr;
-  if (L->err_host) cudaFreeHost(L->err_host);
+  hfree(L->err_host);
   L->err_host = nullptr;
   if (L->plan) prefill_plan_destroy(L->plan);
   L->plan = nullptr;
@@ -399,13 +463,14 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   }
 #undef MOE_ALLOC
   if (rc == MOE_OK) {
-    if (cudaHostAlloc(reinterpret_cast<void**>(&L->err_host), 16, cudaHostAllocMapped) != cudaSuccess ||
-        cudaHostGetDevicePointer(reinterpret_cast<void**>(&L->err_dev), L->err_host, 0) != cudaSuccess) {
+    void* eh = nullptr;
+    rc = halloc(L, &eh, 16);
+    L->err_host = static_cast<int*>(eh);
+    if (rc == MOE_OK && cudaHostGetDevicePointer(reinterpret_cast<void**>(&L->err_dev), L->err_host, 0) != cudaSuccess) {
       cudaGetLastError();
-      rc = MOE_ERR_OOM;
-    } else {
-      *L->err_host = 0;
+      rc = MOE_ERR_CUDA;
     }
+    if (rc == MOE_OK) *L->err_host = 0;
   }
   if (rc == MOE_OK) {
     L->gplan = gemv_plan_create(g, L->slots);
@@ -418,10 +483,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
       L->plan = nullptr;   // prefill regime unavailable (tensor-map encoding failed)
     }
   }
-  if (rc == MOE_OK && cudaHostAlloc(&L->pinned_rec, rec_bytes(g.E), cudaHostAllocMapped) != cudaSuccess) {
-    cudaGetLastError();
-    rc = MOE_ERR_OOM;
-  }
+  if (rc == MOE_OK) rc = halloc(L, &L->pinned_rec, rec_bytes(g.E));
   if (rc == MOE_OK) {
     L->rec_host = static_cast<StepRecord*>(L->pinned_rec);
     std::memset(L->pinned_rec, 0, rec_bytes(g.E));
@@ -544,6 +606,11 @@ int moe_cache_install(moe_layer_t L, int expert, int slot, void* stream) {
   int b = -1;
   int rc = slot_buffer(L, slot, &b);
   if (rc) return rc;
+  if (L->inject_fill) {
+    L->inject_fill = false;
+    return fail(L, MOE_ERR_FILL, "fill of expert %d could not be issued (injected by the test hook); the "
+                "table is unchanged", expert);
+  }
   MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)b * L->g.ebytes,
                               L->host_pool + (size_t)expert * L->g.ebytes, L->g.ebytes,
                               cudaMemcpyHostToDevice, st));
@@ -614,9 +681,26 @@ int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, in
   if (L->host_pool) {
     // every miss into the buffer the step gave it (a later-wave miss's spare
     // became its slot's buffer at the end of the step)
-    for (int i = r->n_hit; i < r->U; ++i)
-      MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)ab[i] * g.ebytes, L->host_pool + (size_t)ae[i] * g.ebytes,
-                                  g.ebytes, cudaMemcpyHostToDevice, st));
+    for (int i = r->n_hit; i < r->U; ++i) {
+      cudaError_t ce = cudaSuccess;
+      if (L->inject_fill) {
+        L->inject_fill = false;
+        ce = cudaErrorInvalidValue;
+      } else {
+        ce = cudaMemcpyAsync(L->slots + (size_t)ab[i] * g.ebytes, L->host_pool + (size_t)ae[i] * g.ebytes,
+                             g.ebytes, cudaMemcpyHostToDevice, st);
+      }
+      if (ce != cudaSuccess) {
+        cudaGetLastError();
+        mirror_apply(L, r);
+        for (int q = r->n_hit; q < r->U; ++q)
+          if (L->mirror[as[q]] == ae[q]) L->mirror[as[q]] = -1;
+        MOE_CUDA(L, launch_lru_drop_misses(g, L->rec, L->slot_of, L->expert_of, st));
+        MOE_CUDA(L, cudaStreamSynchronize(st));
+        return fail(L, MOE_ERR_FILL, "fill of expert %d could not be issued (%s); the %d misses were dropped "
+                    "from the cache", ae[i], cudaGetErrorString(ce), r->U - r->n_hit);
+      }
+    }
     MOE_CUDA(L, cudaStreamSynchronize(st));
   }
   mirror_apply(L, r);
@@ -770,6 +854,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   a.with_shared = g.has_shared;
   a.err = L->err_dev;
   a.hmax = L->hmax;
+  a.wait_cycles = L->inject_wait;   // 0: the default limit
+  L->inject_wait = 0;
   const int cap = n_ent_cap(L, N);
   const float gx = g.fmt == MOE_NVFP4 ? L->desc.act_scale_x : 1.0f;
   const float gh = g.fmt == MOE_NVFP4 ? L->desc.act_scale_h : 1.0f;
@@ -824,6 +910,10 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       MOE_CUDA(L, cudaEventRecord(L->ev_chunk[c], fs));
     }
     prof_end(pf, fs);
+    // every chunk launch, including those this step's miss list leaves
+    // without work, reads the step record: the step ends (and the next one
+    // may rewrite the record and the buffer map) only after all of them
+    MOE_CUDA(L, cudaEventRecord(L->ev_fill, fs));
     L->launches += max_pre;
   }
 
@@ -889,10 +979,26 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
         for (int i = c0; i < c1;) {
           int j = i + 1;
           while (j < c1 && ae[j] == ae[j - 1] + 1 && ab[j] == ab[j - 1] + 1) ++j;
-          cudaError_t ce = cudaMemcpyAsync(L->slots + (size_t)ab[i] * g.ebytes,
-                                           L->host_pool + (size_t)ae[i] * g.ebytes, (size_t)(j - i) * g.ebytes,
-                                           cudaMemcpyHostToDevice, fs);
-          if (ce != cudaSuccess) return fail(L, MOE_ERR_FILL, "fill of expert %d: %s", ae[i], cudaGetErrorString(ce));
+          cudaError_t ce = cudaSuccess;
+          if (L->inject_fill) {
+            L->inject_fill = false;
+            ce = cudaErrorInvalidValue;
+          } else {
+            ce = cudaMemcpyAsync(L->slots + (size_t)ab[i] * g.ebytes, L->host_pool + (size_t)ae[i] * g.ebytes,
+                                 (size_t)(j - i) * g.ebytes, cudaMemcpyHostToDevice, fs);
+          }
+          if (ce != cudaSuccess) {
+            // the step's misses leave the cache (their slots become free, so a
+            // later step fills them again); the fills already issued and the
+            // hits' expert FFN finish on their own; y is not written
+            cudaGetLastError();
+            mirror_apply(L, r);
+            for (int q = n_hit; q < U; ++q)
+              if (L->mirror[as[q]] == ae[q]) L->mirror[as[q]] = -1;
+            MOE_CUDA(L, launch_lru_drop_misses(g, L->rec, L->slot_of, L->expert_of, st));
+            return fail(L, MOE_ERR_FILL, "fill of expert %d could not be issued (%s); the step's %d misses were "
+                        "dropped from the cache and y was not written", ae[i], cudaGetErrorString(ce), U - n_hit);
+          }
           fill_bytes += (size_t)(j - i) * g.ebytes;
           i = j;
         }
@@ -929,6 +1035,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       if (grc) return grc;
     }
   }
+  if (sm_fill) MOE_CUDA(L, cudaStreamWaitEvent(st, L->ev_fill, 0));
   pe = prof_begin(L, MOE_PROF_COMBINE, st);
   MOE_CUDA(L, launch_combine(g, L->O, prefill, L->gates, L->row_of, N, yd, st));
   prof_end(pe, st);
@@ -937,6 +1044,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     if (!y_direct) MOE_CUDA(L, cudaMemcpyAsync(y, yd, xbytes, cudaMemcpyDeviceToHost, st));
     MOE_CUDA(L, cudaStreamSynchronize(st));
   }
+  L->last_N = N;
+  L->last_prefill = prefill;
   if (info) {
     info->regime = prefill ? MOE_REGIME_PREFILL : MOE_REGIME_DECODE;
     info->n_distinct = U;
@@ -1021,6 +1130,70 @@ int moe_debug_permute(moe_layer_t L, const int* idx, int N, int* counts, int* of
   if (!idx || !counts || !offsets || !row_of || !tok_of) return fail(L, MOE_ERR_ARG, "NULL pointer");
   MOE_CUDA(L, launch_permute(L->g, idx, N, counts, offsets, row_of, tok_of, L->perm_scratch,
                              static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_debug_inject(moe_layer_t L, int what, long long arg) {
+  if (!L) return MOE_ERR_ARG;
+  switch (what) {
+    case MOE_INJECT_NONE:
+      L->inject_fill = false;
+      L->inject_wait = 0;
+      return MOE_OK;
+    case MOE_INJECT_FILL:
+      L->inject_fill = true;
+      return MOE_OK;
+    case MOE_INJECT_WAIT_LIMIT:
+      if (arg <= 0) return fail(L, MOE_ERR_ARG, "the wait limit must be positive");
+      L->inject_wait = arg;
+      return MOE_OK;
+    default:
+      return fail(L, MOE_ERR_ARG, "unknown injection %d", what);
+  }
+}
+
+int moe_debug_alloc_fault(long long nth, long long* live_out) {
+  if (nth < 0) return MOE_ERR_ARG;
+  g_alloc_countdown.store(nth);
+  if (live_out) {
+    live_out[0] = g_live_dev.load();
+    live_out[1] = g_live_host.load();
+  }
+  return MOE_OK;
+}
+
+int moe_debug_last_step(moe_layer_t L, int* idx, float* gates, int* counts, int* offsets, int* row_of,
+                        int* tok_of, int* n_out, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  const int N = L->last_N;
+  if (N <= 0) return fail(L, MOE_ERR_STATE, "no moe_forward has run on this layer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Geo& g = L->g;
+  const size_t nk = (size_t)N * g.k;
+  if (idx) MOE_CUDA(L, cudaMemcpyAsync(idx, L->idx, nk * 4, cudaMemcpyDeviceToDevice, st));
+  if (gates) MOE_CUDA(L, cudaMemcpyAsync(gates, L->gates, nk * 4, cudaMemcpyDeviceToDevice, st));
+  if (counts) MOE_CUDA(L, cudaMemcpyAsync(counts, L->counts, (size_t)g.E * 4, cudaMemcpyDeviceToDevice, st));
+  if (offsets) MOE_CUDA(L, cudaMemcpyAsync(offsets, L->offsets, (size_t)(g.E + 1) * 4, cudaMemcpyDeviceToDevice, st));
+  if (row_of) MOE_CUDA(L, cudaMemcpyAsync(row_of, L->row_of, nk * 4, cudaMemcpyDeviceToDevice, st));
+  if (tok_of) MOE_CUDA(L, cudaMemcpyAsync(tok_of, L->tok_of, nk * 4, cudaMemcpyDeviceToDevice, st));
+  if (n_out) *n_out = N;
+  return MOE_OK;
+}
+
+int moe_debug_last_hidden(moe_layer_t L, float* h, uint8_t* hq_codes, uint8_t* hq_scales, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  const int N = L->last_N;
+  if (N <= 0) return fail(L, MOE_ERR_STATE, "no moe_forward has run on this layer");
+  if (h && L->last_prefill) return fail(L, MOE_ERR_STATE, "the last call ran the prefill regime (no fp32 h)");
+  if ((hq_codes || hq_scales) && !L->last_prefill)
+    return fail(L, MOE_ERR_STATE, "the last call ran the decode regime (no quantised h)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Geo& g = L->g;
+  const size_t rows = (size_t)N * g.k + (g.has_shared ? N : 0);
+  if (h) MOE_CUDA(L, cudaMemcpyAsync(h, L->h, rows * 2 * g.f * 4, cudaMemcpyDeviceToDevice, st));
+  if (hq_codes) MOE_CUDA(L, cudaMemcpyAsync(hq_codes, L->hq_codes, rows * g.f / 2, cudaMemcpyDeviceToDevice, st));
+  if (hq_scales)
+    MOE_CUDA(L, cudaMemcpyAsync(hq_scales, L->hq_scales, rows * (g.f / g.blk), cudaMemcpyDeviceToDevice, st));
   return MOE_OK;
 }
 

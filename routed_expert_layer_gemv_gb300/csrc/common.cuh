@@ -40,6 +40,13 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  Function attributes are per device, so this is done once
+// per (kernel, device) pair -- a process that drives several GPUs sets them on
+// each -- under a lock, so concurrent first launches from several threads are
+// safe.  Defined in api.cu.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 constexpr int kWarp = 32;
@@ -179,6 +186,10 @@ cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets,
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
                                unsigned long long* stamp, unsigned long long* clock,
                                cudaStream_t st);
+// Drop the misses of the step in `rec` from the table (their slots become
+// free): the recovery of a step whose fills could not be issued.
+cudaError_t launch_lru_drop_misses(const Geo& g, const StepRecord* rec, int* slot_of, int* expert_of,
+                                   cudaStream_t st);
 // permutation + LRU step in one CTA, for N <= 128 tokens
 cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, int* offsets,
                               int* row_of, int* tok_of, int* slot_of, int* expert_of,
@@ -201,6 +212,7 @@ struct GemvArgs {
   int with_shared;             // also run the shared expert (rows N*k .. N*k+N)
   int* err;                    // set to 1 when a bounded wait gives up
   float* hmax;                 // [rows][2][d_ff / 64]: max |W_g x|, |W_u x| per 64 columns
+  long long wait_cycles;       // limit of the launch's bounded waits (SM clock cycles; <= 0: ~2 s)
 };
 struct GemvPlan;               // tensor maps of the slot pool's weight codes
 bool gemv_shape_ok(const Geo& g);

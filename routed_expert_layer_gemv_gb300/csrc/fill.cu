@@ -133,12 +133,8 @@ cudaError_t launch_fill_copy(const Geo& g, const StepRecord* rec, int max_misses
 
 cudaError_t launch_fill_sm(const Geo& g, const StepRecord* rec, int chunk, const uint8_t* pool_dev,
                            uint8_t* slots, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(fill_sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFillSmSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = ensure_smem_limit((const void*)fill_sm_kernel, kFillSmSmem);
+  if (e != cudaSuccess) return e;
   fill_sm_kernel<<<kFillSms, kFillSmThreads, kFillSmSmem, st>>>(rec, g.E, g.S, g.X, chunk, pool_dev, slots,
                                                                g.ebytes);
   return cudaGetLastError();

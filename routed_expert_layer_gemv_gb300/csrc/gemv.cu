@@ -372,9 +372,10 @@ struct Smem {
 
 // Bounded wait that gives up at once after an earlier timeout anywhere in
 // the CTA; a timeout sets the CTA abort flag and the launch error word.
-MOE_DEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+MOE_DEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                           long long limit) {
   if (*abort_flag) return false;
-  if (tc::mbar_wait(bar, parity)) return true;
+  if (tc::mbar_wait(bar, parity, limit)) return true;
   *abort_flag = 1;
   atomicExch(err, 1);
   return false;
@@ -528,6 +529,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
   __shared__ int stok[2 * kTG];
   __shared__ volatile int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // operational waits give up after wl cycles; the final wait for the
+  // producer's own copies in flight keeps the default limit
+  const long long wl = a.wait_cycles > 0 ? a.wait_cycles : tc::kWaitCycles;
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.D; ++i) {
       tc::mbar_init(&S.full[i], 1);
@@ -598,7 +602,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         for (int st = 0; st < p.NS; ++st) {
           const int slot = n % p.D;
           const uint32_t k = n / p.D;
-          if (k > 0 && !wait_or_abort(&S.empty[slot], (k - 1) & 1, &s_abort, a.err)) {
+          if (k > 0 && !wait_or_abort(&S.empty[slot], (k - 1) & 1, &s_abort, a.err, wl)) {
             stop = true;
             break;
           }
@@ -649,12 +653,12 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     cursor_init(cu, rr);
     while (cursor_next(cu, g, a, p, rr)) {
       const int xb = bs % p.XB;
-      if (!ALL) wait_or_abort(&S.xfull[xb], (bs / p.XB) & 1, &s_abort, a.err);
+      if (!ALL) wait_or_abort(&S.xfull[xb], (bs / p.XB) & 1, &s_abort, a.err, wl);
       const uint2* xs = reinterpret_cast<const uint2*>(S.base + p.off_x + (size_t)xb * p.xbytes);
       for (int u = cu.ue0; u < cu.ue1; ++u) {
         for (int st = 0; st < p.NS; ++st, ++n) {
           const int slot = n % p.D;
-          const bool ok = wait_or_abort(&S.full[slot], (n / p.D) & 1, &s_abort, a.err);
+          const bool ok = wait_or_abort(&S.full[slot], (n / p.D) & 1, &s_abort, a.err, wl);
           const int kb = st * kBoxes + bslot;
           if (HOST && ok && cu.en.ex >= 0)
             host_part(g, p, a, cu.en, PH == 1 ? u / p.RB : 2, PH == 1 ? u % p.RB : u, st,
@@ -673,7 +677,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         }
         // unit done: hand the partial sums to the epilogue
         const int r = us % p.RS;
-        if (us >= (uint32_t)p.RS) wait_or_abort(&S.rempty[r], (us / p.RS - 1) & 1, &s_abort, a.err);
+        if (us >= (uint32_t)p.RS) wait_or_abort(&S.rempty[r], (us / p.RS - 1) & 1, &s_abort, a.err, wl);
         reinterpret_cast<float4*>(red + (size_t)r * (p.rbytes / 4))[warp * 32 + lane] =
             make_float4(acc[0], acc[1], acc[2], acc[3]);
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -697,7 +701,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
     auto stage = [&](const Cursor& c, uint32_t bs_st) {
       const int xb = bs_st % p.XB;
       epi_sync();   // the previous staging's token list and exponents are no longer read
-      if (bs_st >= (uint32_t)p.XB) wait_or_abort(&S.xempty[xb], (bs_st / p.XB - 1) & 1, &s_abort, a.err);
+      if (bs_st >= (uint32_t)p.XB) wait_or_abort(&S.xempty[xb], (bs_st / p.XB - 1) & 1, &s_abort, a.err, wl);
       stage_block<FMT, PH>(g, a, p, c.en, c.tg, reinterpret_cast<uint2*>(S.base + p.off_x + (size_t)xb * p.xbytes),
                            sexp[xb], stok, x, xexp, h, te, kET, 1);
       __syncwarp();
@@ -734,7 +738,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap map0, const __grid_consta
         const int rb = PH == 1 ? u % p.RB : u;
         const float ts = tsp[PH == 1 ? m : 2];
         const int r = us % p.RS;
-        const bool ok = wait_or_abort(&S.rfull[r], (us / p.RS) & 1, &s_abort, a.err);
+        const bool ok = wait_or_abort(&S.rfull[r], (us / p.RS) & 1, &s_abort, a.err, wl);
         const float4* rs = reinterpret_cast<const float4*>(red + (size_t)r * (p.rbytes / 4));
         // warp w takes tokens w, w + kEW, ...; lane c takes columns c, c + 32 of the block
         for (int tk = ew_; ok && tk < nt; tk += kEW) {
@@ -828,13 +832,8 @@ template <int FMT, int PH, bool HOST>
 cudaError_t launch_phase(const Geo& g, const GemvPlan* pl, const GemvArgs& a, const SG& p,
                          const __nv_bfloat16* x, const int* xexp, float* h, float* O, int n_ent_max,
                          int num_sms, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<FMT, PH, HOST>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget + 1024);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = ensure_smem_limit((const void*)gemv_stream_kernel<FMT, PH, HOST>, kSmemBudget + 1024);
+  if (e != cudaSuccess) return e;
   const long long units = (long long)n_ent_max * p.UE;
   // phase 1 is launched while the one-CTA routing tail still holds an SM, and
   // a CTA of this size cannot share it: leave that SM out rather than have

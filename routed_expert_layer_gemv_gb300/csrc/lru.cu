@@ -341,6 +341,21 @@ __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expe
   stamp[slot] = c;
 }
 
+__global__ void lru_drop_misses_kernel(const StepRecord* __restrict__ rec, int E, int S, int* slot_of,
+                                       int* expert_of) {
+  const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
+  const int* ae = rec_expert(const_cast<StepRecord*>(rec));
+  for (int i = nh + (int)threadIdx.x; i < U; i += blockDim.x) {
+    const int e = ae[i];
+    if (e < 0 || e >= E) continue;
+    const int s = slot_of[e];
+    if (s >= 0 && s < S) {
+      expert_of[s] = -1;
+      slot_of[e] = -1;
+    }
+  }
+}
+
 __global__ void counts_from_list_kernel(const int* __restrict__ list, int n, int E,
                                         int* __restrict__ counts) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -368,13 +383,8 @@ cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, 
                               unsigned long long seq, cudaStream_t st) {
   const size_t smem = (size_t)g.E * perm::kPermWarps * 4 + (size_t)2 * g.E * 4 +
                       (size_t)perm::kTokPerBlock * g.k * 4 + (size_t)perm::kTokPerBlock * ((g.E + 31) / 32) * 4;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(route_tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         64 * 1024);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = ensure_smem_limit((const void*)route_tail_kernel, 64 * 1024);
+  if (e != cudaSuccess) return e;
   return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, g.X, counts,
                     offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, buf, rec, stats, host_rec, seq);
 }
@@ -384,6 +394,12 @@ cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of,
                                cudaStream_t st) {
   (void)g;
   lru_install_kernel<<<1, 1, 0, st>>>(expert, slot, slot_of, expert_of, stamp, clock);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lru_drop_misses(const Geo& g, const StepRecord* rec, int* slot_of, int* expert_of,
+                                   cudaStream_t st) {
+  lru_drop_misses_kernel<<<1, 256, 0, st>>>(rec, g.E, g.S, slot_of, expert_of);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,8 @@
 // Block b owns tokens [b*128, b*128+128) (ballot scheme: permute_dev.cuh); a
 // scan over blocks and experts turns block histograms and in-block ranks into
 // the final rows.  No atomics anywhere.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -41,7 +43,10 @@ perm_hist_kernel(const int* __restrict__ idx, int N, int k, int E, int* __restri
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = perm::block_count(cm, e);
   const int t = t_base + threadIdx.x;
   if (t < N)
-    for (int j = 0; j < k; ++j) rank[(size_t)t * k + j] = perm::rank_in_block(cm, rows[threadIdx.x * k + j]);
+    for (int j = 0; j < k; ++j) {
+      const int e = rows[threadIdx.x * k + j];
+      rank[(size_t)t * k + j] = e >= 0 && e < E ? perm::rank_in_block(cm, e) : 0;
+    }
 }
 
 // Step 2 (one CTA of 1024 threads): per-expert block prefix, counts, offsets.
@@ -82,10 +87,14 @@ __global__ void perm_scatter_kernel(const int* __restrict__ idx, int N, int k, i
   if (p >= N * k) return;
   const int t = p / k;
   const int e = idx[p];
+  if (e < 0 || e >= E) {   // invalid id: no row (the outputs are then unspecified, but in bounds)
+    row_of[p] = -1;
+    return;
+  }
   const int b = t / kTokPerBlock;
   const int r = offsets[e] + base[(size_t)b * E + e] + rank[p];
   row_of[p] = r;
-  tok_of[r] = t;
+  if (r >= 0 && r < N * k) tok_of[r] = t;
 }
 
 // Whole permutation in one CTA (N <= 128 tokens).
@@ -121,9 +130,13 @@ perm_single_kernel(const int* __restrict__ idx, int N, int k, int E, int* __rest
   if (t < N) {
     for (int j = 0; j < k; ++j) {
       const int e = rows[t * k + j];
+      if (e < 0 || e >= E) {   // invalid id: no row (outputs unspecified, but in bounds)
+        row_of[(size_t)t * k + j] = -1;
+        continue;
+      }
       const int r = off[e] + perm::rank_in_block(cm, e);
       row_of[(size_t)t * k + j] = r;
-      tok_of[r] = t;
+      if (r >= 0 && r < N * k) tok_of[r] = t;
     }
   }
 }
@@ -141,12 +154,9 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
   if (N <= kTokPerBlock) {
     size_t smem = (size_t)g.E * kPermWarps * 4 + (size_t)g.E * 4 + 33 * 4 + (size_t)kTokPerBlock * g.k * 4 +
                   (size_t)kTokPerBlock * ((g.E + 31) / 32) * 4;
-    static bool attr = false;   // up to 53 KB at E = 1024, k = 32
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(perm_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
+    // up to 53 KB at E = 1024, k = 32
+    cudaError_t e = ensure_smem_limit((const void*)perm_single_kernel, 64 * 1024);
+    if (e != cudaSuccess) return e;
     perm_single_kernel<<<1, kTokPerBlock, smem, st>>>(idx, N, g.k, g.E, counts, offsets, row_of,
                                                       tok_of);
     return cudaGetLastError();
@@ -182,6 +192,36 @@ static __device__ __align__(256) int g_noalloc_scratch[kNoAllocInts];
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 int* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};   // context the address belongs to
+
+// Unique id of the current CUDA context (cuCtxGetId, through the runtime's
+// driver entry points), 0 if it cannot be had.  A device's context can be
+// destroyed and re-created (cudaDeviceReset), and the array's address in the
+// new context need not be the old one, so the cached address is keyed by it.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+    cudaGetLastError();
+    looked_up = true;
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 int noalloc_fail(int code, const char* msg, char* errbuf, size_t errbuf_len) {
   if (errbuf && errbuf_len > 0) snprintf(errbuf, errbuf_len, "%s", msg);
@@ -218,16 +258,21 @@ extern "C" int moe_permute_noalloc(const int* idx, int N, int k, int E, int* cou
   }
   int* scratch = nullptr;
   {
-    // set-up, once per device, with that device current
+    // set-up, once per device (and again after its context was re-created),
+    // with that device current
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    // (0 before the runtime created the device's context, or when the id
+    // cannot be read: then the address is looked up on every call)
+    const unsigned long long ctx = current_context_id();
+    if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
       void* p = nullptr;
-      cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // creates the context if needed
       if (e != cudaSuccess) {
         cudaGetLastError();
         return noalloc_fail(MOE_ERR_CUDA, cudaGetErrorString(e), errbuf, errbuf_len);
       }
       g_noalloc_ptr[dev] = static_cast<int*>(p);
+      g_noalloc_ctx[dev] = current_context_id();
     }
     scratch = g_noalloc_ptr[dev];
   }

@@ -613,15 +613,13 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int max_tiles = prefill_max_tiles(g, N);
-  static bool attr = false;
-  if (!attr) {
+  {
     const int s1 = (int)ws_smem<1>(), s2 = (int)ws_smem<2>();
-    e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_MXFP4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_NVFP4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, s1);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_MXFP4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_ws_kernel<MOE_NVFP4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, s2);
+    e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 1>, s1);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 1>, s1);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 2>, s2);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 2>, s2);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   GemmArgs p{};
   p.tiles = tl;

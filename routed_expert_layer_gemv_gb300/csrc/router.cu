@@ -387,12 +387,8 @@ cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const flo
   if (N > 64) {
     // large batches: tensor-core logits, then the top-k kernel
     const size_t smem = (size_t)2 * kTcStage * sizeof(__nv_bfloat16);
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
+    cudaError_t e = ensure_smem_limit((const void*)router_tc_kernel, (int)smem);
+    if (e != cudaSuccess) return e;
     const dim3 grid((N + kTcM - 1) / kTcM, (g.E + kTcN - 1) / kTcN);
     router_tc_kernel<<<grid, 256, smem, st>>>(x, N, g.d, g.E, Whl, bias, logits, xexp);
     cudaError_t err = cudaGetLastError();

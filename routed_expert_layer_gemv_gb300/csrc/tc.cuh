@@ -45,11 +45,15 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t phase) {
   return ok != 0;
 }
 
-// Wait for `phase` of the barrier, at most ~2 s of SM clock; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase) {
+// Default limit of a bounded wait: ~2 s of SM clock.
+constexpr long long kWaitCycles = 4000000000LL;
+
+// Wait for `phase` of the barrier, at most `limit` SM clock cycles; false on
+// timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, long long limit = kWaitCycles) {
   const long long t0 = clock64();
   while (!mbar_try(bar, phase))
-    if (clock64() - t0 > 4000000000LL) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 

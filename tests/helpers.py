@@ -73,3 +73,27 @@ def small_spec(**kw):
 def bf16_tensor(bits: np.ndarray, device="cuda"):
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
     return t.to(device) if device else t
+
+
+def check_last_step(L, spec, N, idx_ref, gates_ref):
+    """The router and permutation arrays of the layer's last moe_forward --
+    the ones its expert FFN and combine used -- against the oracle: ids and
+    permutation bit for bit, gates to fp32 rounding."""
+    from routed_expert_layer_gemv_gb300 import capi
+    k, E = spec.k, spec.E
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx = torch.full((N * k,), -7, **i32)
+    gates = torch.full((N * k,), -7.0, dtype=torch.float32, device="cuda")
+    counts, offsets = torch.full((E,), -7, **i32), torch.full((E + 1,), -7, **i32)
+    row_of, tok_of = torch.full((N * k,), -7, **i32), torch.full((N * k,), -7, **i32)
+    n = capi.moe_debug_last_step(L.h, idx, gates, counts, offsets, row_of, tok_of)
+    torch.cuda.synchronize()
+    assert n == N
+    idx_ref = np.asarray(idx_ref).reshape(N, k)
+    assert np.array_equal(idx.cpu().numpy().reshape(N, k), idx_ref)
+    rc, ro, rr, rt = olayer.permute(idx_ref, E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(row_of.cpu().numpy(), rr.reshape(-1))
+    assert np.array_equal(tok_of.cpu().numpy(), rt)
+    assert np.allclose(gates.cpu().numpy().reshape(N, k), gates_ref, rtol=2e-6, atol=1e-7)

@@ -210,3 +210,59 @@ def test_lru_install_and_state_roundtrip():
     with pytest.raises(capi.MoeError):
         L.install(10, 0)                                                # expert out of range
     L.close()
+
+
+# ---------------------------------------------------------------- decode GEMV decode
+
+@pytest.mark.parametrize("spec,N", [
+    (small_spec(E=8, k=2, d_model=512, d_ff=256, n_slots=8, has_shared=True), 8),
+    (small_spec(E=16, k=4, d_model=512, d_ff=384, n_slots=16, fmt="nvfp4", has_shared=True), 12),
+    (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 4),
+])
+def test_decode_gemv_decodes_weights_bit_exact(spec, N):
+    # one-hot tokens x_t = c_t e_{i_t} (c_t a power of two): phase 1 of the
+    # decode expert GEMV then writes, for each row of expert e and token t,
+    # exactly c_t times column i_t of e's dequantised gate and up matrices --
+    # the GEMV's own FP4 decode (E2M1 codes, block scales, tensor scale) is
+    # checked bit for bit, not through the output tolerance
+    seed = 41
+    L = build_layer(spec, seed, N, install_all=True)
+    g = np.random.default_rng(3)
+    cols = g.choice(spec.d_model, N, replace=False)
+    mags = [1.0, 0.125, 32.0, -2.0, -0.25, 4.0]
+    xf = np.zeros((N, spec.d_model), dtype=np.float32)
+    for t in range(N):
+        xf[t, cols[t]] = mags[t % len(mags)]
+    bits = (xf.view(np.uint32) >> 16).astype(np.uint16)          # exact in bf16
+    L.forward(bf16_tensor(bits), regime=capi.MOE_REGIME_DECODE)
+    rows = N * spec.k + (N if spec.has_shared else 0)
+    hid = torch.empty(rows, 2 * spec.d_ff, dtype=torch.float32, device="cuda")
+    capi.moe_debug_last_hidden(L.h, hid)
+    idx = torch.empty(N * spec.k, dtype=torch.int32, device="cuda")
+    row_of = torch.empty(N * spec.k, dtype=torch.int32, device="cuda")
+    capi.moe_debug_last_step(L.h, idx=idx, row_of=row_of)
+    torch.cuda.synchronize()
+    H, I, R = hid.cpu().numpy().astype(np.float64), idx.cpu().numpy(), row_of.cpu().numpy()
+    f = spec.d_ff
+    cache = {}
+
+    def deq(e, shared=False):
+        key = (e, shared)
+        if key not in cache:
+            w = wl.expert_weights(spec, seed, e, shared=shared)
+            cache[key] = {n: formats.dequant(m.codes, m.scales, m.tscale, spec.fmt) for n, m in w.items()}
+        return cache[key]
+
+    for t in range(N):
+        c = float(xf[t, cols[t]])
+        for j in range(spec.k):
+            W = deq(int(I[t * spec.k + j]))
+            r = R[t * spec.k + j]
+            assert np.array_equal(H[r, :f], c * W["gate"][:, cols[t]]), (t, j, "gate")
+            assert np.array_equal(H[r, f:], c * W["up"][:, cols[t]]), (t, j, "up")
+        if spec.has_shared:
+            W = deq(0, shared=True)
+            r = N * spec.k + t
+            assert np.array_equal(H[r, :f], c * W["gate"][:, cols[t]]), (t, "shared gate")
+            assert np.array_equal(H[r, f:], c * W["up"][:, cols[t]]), (t, "shared up")
+    L.close()

@@ -6,9 +6,9 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import (CachedExperts, assert_close_layer, bf16_tensor, need_gpu, oracle_layer,
-                     reject_near_ties, small_spec)
-from oracle import formats
+from helpers import (CachedExperts, assert_close_layer, bf16_tensor, check_last_step, need_gpu,
+                     oracle_layer, reject_near_ties, small_spec)
+from oracle import formats, quant
 from oracle import layer as olayer
 from oracle.lru import SlotTable
 from routed_expert_layer_gemv_gb300 import capi
@@ -48,8 +48,9 @@ def test_forward_all_resident(spec, N):
     y, info = L.forward(bf16_tensor(x), regime=DEC)
     torch.cuda.synchronize()
     assert info.host_synced == 0 and info.n_misses == 0
-    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "decode")
+    ref, idx, gates = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "decode")
     assert_close_layer(y, ref, "%s N=%d" % (spec, N))
+    check_last_step(L, spec, N, idx, gates)
     L.close()
 
 
@@ -65,7 +66,7 @@ def _decode_run(spec, seed, batch, steps, check_every=1, fill=capi.MOE_FILL_MEMC
     for t in range(steps):
         xt = bf16_tensor(xs[t])
         y, info = L.forward(xt, regime=DEC)
-        ref, idx, _ = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
+        ref, idx, gates = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
         acc = T.step(idx.reshape(-1))
         n_miss = sum(1 for a in acc if not a[2])
         eff = fill
@@ -84,6 +85,7 @@ def _decode_run(spec, seed, batch, steps, check_every=1, fill=capi.MOE_FILL_MEMC
         tot_u += len(acc)
         if t % check_every == 0 or t == steps - 1:
             assert_close_layer(y, ref, "step %d" % t)
+            check_last_step(L, spec, N, idx, gates)
             eo, st, clk = capi.moe_lru_get_state(L.h, spec.n_slots)
             assert eo == T.expert_of and st == T.stamp and clk == T.clock
     steps_d, u_d, hits_d, miss_d = capi.moe_stats(L.h)
@@ -110,6 +112,16 @@ def test_decode_284b_shape_shared_and_waves():
     spec = wl.DECODE_284B.layer
     miss, u, waves = _decode_run(spec, 5, 8, 3)
     assert waves >= 2
+
+
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_AUTO, capi.MOE_FILL_MEMCPY])
+def test_decode_284b_shape_batch1(fill):
+    # the 284B-A13B-class decode layer at its configured batch of 1: 28 slots,
+    # shared expert, 16 steps from a cold cache (misses, then hits as the
+    # AR(1) tokens keep routing to overlapping experts)
+    spec = wl.DECODE_284B.layer
+    miss, u, waves = _decode_run(spec, 9, 1, 16, fill=fill)
+    assert 0 < miss < u
 
 
 @pytest.mark.parametrize("fill", [capi.MOE_FILL_DEVICE, capi.MOE_FILL_KERNEL, capi.MOE_FILL_FUSED,
@@ -278,6 +290,103 @@ def test_error_paths():
     L.close()
 
 
+def test_allocation_failure_at_each_allocation_leaks_nothing():
+    # every device or pinned allocation of a create made to fail in turn: the
+    # create returns MOE_ERR_OOM and gives back everything it took; a normal
+    # layer afterwards still matches the oracle
+    spec = small_spec(E=8, k=2, d_model=256, d_ff=256, n_slots=4, has_shared=True)
+    desc = MoELayer(spec, 16).desc   # (creates and drops one layer: warms up the runtime)
+    torch.cuda.synchronize()
+    base = capi.moe_debug_alloc_fault(0)
+    free0 = torch.cuda.mem_get_info()[0]
+    h = capi.moe_layer_create(desc)
+    live = capi.moe_debug_alloc_fault(0)
+    capi.moe_layer_destroy(h)
+    n_alloc = (live[0] - base[0]) + (live[1] - base[1])
+    assert n_alloc >= 20
+    assert capi.moe_debug_alloc_fault(0) == base
+    for nth in range(1, n_alloc + 1):
+        capi.moe_debug_alloc_fault(nth)
+        with pytest.raises(capi.MoeError) as e:
+            capi.moe_layer_create(desc)
+        assert e.value.status == capi.MOE_ERR_OOM, nth
+        assert capi.moe_debug_alloc_fault(0) == base, nth
+    torch.cuda.synchronize()
+    assert abs(torch.cuda.mem_get_info()[0] - free0) <= 2 << 20
+    seed = 3
+    L = build_layer(spec, seed, 16, install_all=True)
+    x = _tokens(spec, seed, 16)
+    y, _ = L.forward(bf16_tensor(x), regime=DEC)
+    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "decode")
+    assert_close_layer(y, ref, "after the allocation failures")
+    L.close()
+
+
+def test_fill_failure_drops_the_step_misses_and_later_steps_match():
+    # MEMCPY fills: the copy of a step's first miss cannot be issued (injected
+    # on the host, before cudaMemcpyAsync).  The call returns MOE_ERR_FILL, the
+    # step's misses leave the cache (slots free), and later steps -- which
+    # fill them again -- match the oracle, with the slot table equal to the
+    # naive one with that step's misses dropped
+    spec = small_spec(E=32, k=4, d_model=256, d_ff=256, n_slots=8, has_shared=True)
+    seed, batch, steps, bad = 19, 4, 5, 2
+    experts = CachedExperts(spec, seed)
+    L = build_layer(spec, seed, batch, experts_fn=experts)
+    capi.moe_set_fill_mode(L.h, capi.MOE_FILL_MEMCPY)
+    O = oracle_layer(spec, seed, experts)
+    T = SlotTable(spec.E, spec.n_slots)
+    xs, _ = wl.ar1_tokens(seed, batch, steps, spec.d_model, 0.9, reject_near_ties(spec, seed))
+    for t in range(steps):
+        ref, idx, gates = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
+        acc = T.step(idx.reshape(-1))
+        if t == bad:
+            assert any(not hit for _, _, hit, _ in acc), "the chosen step must have misses"
+            capi.moe_debug_inject(L.h, capi.MOE_INJECT_FILL)
+            with pytest.raises(capi.MoeError) as e:
+                L.forward(bf16_tensor(xs[t]), regime=DEC)
+            assert e.value.status == capi.MOE_ERR_FILL
+            for ex, sl, hit, _ in acc:
+                if not hit and T.slot_of[ex] == sl:
+                    T.expert_of[sl] = -1
+                    T.slot_of[ex] = -1
+        else:
+            y, info = L.forward(bf16_tensor(xs[t]), regime=DEC)
+            assert_close_layer(y, ref, "step %d" % t)
+            check_last_step(L, spec, batch, idx, gates)
+        eo, st, clk = capi.moe_lru_get_state(L.h, spec.n_slots)
+        assert eo == T.expert_of and st == T.stamp and clk == T.clock, t
+    # a failed install leaves the table as it was
+    capi.moe_debug_inject(L.h, capi.MOE_INJECT_FILL)
+    with pytest.raises(capi.MoeError) as e:
+        L.install(0, 0)
+    assert e.value.status == capi.MOE_ERR_FILL
+    eo, st, clk = capi.moe_lru_get_state(L.h, spec.n_slots)
+    assert eo == T.expert_of and st == T.stamp and clk == T.clock
+    L.close()
+
+
+@pytest.mark.parametrize("batch", [1, 8, 16])
+def test_device_wait_timeout_is_reported_and_the_layer_recovers(batch):
+    # the bounded waits of one forward's decode expert FFN are cut to one
+    # cycle, so its first wait gives up: the launch records the timeout and
+    # returns normally (no trap, no unbounded wait), the next moe_forward
+    # reports MOE_ERR_TIMEOUT, and the one after that matches the oracle
+    spec = small_spec(E=16, k=2, d_model=512, d_ff=256, n_slots=16, has_shared=True)
+    seed = 23
+    L = build_layer(spec, seed, batch, install_all=True)
+    x0, x1 = _tokens(spec, seed, batch), _tokens(spec, seed + 1, batch)
+    capi.moe_debug_inject(L.h, capi.MOE_INJECT_WAIT_LIMIT, 1)
+    L.forward(bf16_tensor(x0), regime=DEC)
+    torch.cuda.synchronize()
+    with pytest.raises(capi.MoeError) as e:
+        L.forward(bf16_tensor(x1), regime=DEC)
+    assert e.value.status == capi.MOE_ERR_TIMEOUT
+    y, _ = L.forward(bf16_tensor(x1), regime=DEC)
+    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x1), "decode")
+    assert_close_layer(y, ref, "after the timeout")
+    L.close()
+
+
 # ---------------------------------------------------------------- prefill regime
 
 PRE = capi.MOE_REGIME_PREFILL
@@ -316,33 +425,157 @@ def test_prefill_35b_shape_sampled_tokens():
     L.close()
 
 
+def _chunk_sample(counts, offsets, row_of, N, k, n_sample, rng):
+    """Tokens that reach the extremes of the grouped GEMM: the largest and the
+    smallest non-empty expert group, rows in the ragged last 128-row tile of
+    an expert, the first and last token, then evenly spaced others."""
+    nz = np.nonzero(counts)[0]
+    big, small = nz[np.argmax(counts[nz])], nz[np.argmin(counts[nz])]
+    rows = row_of.reshape(N, k)
+    e_of_row = np.repeat(np.arange(len(counts)), counts)
+    pick = []
+
+    def tokens_of(e):
+        return np.nonzero((rows >= offsets[e]) & (rows < offsets[e + 1]))[0]
+
+    for e in (big, small):
+        tk = tokens_of(e)
+        pick += list(rng.choice(tk, min(len(tk), max(2, n_sample // 8)), replace=False))
+    # ragged tails: rows past the last full 128-row tile of their expert
+    rr = rows.reshape(-1)
+    e_pair = e_of_row[rr]
+    tail = rr >= offsets[e_pair] + 128 * (counts[e_pair] // 128)
+    ragged = np.nonzero(tail & (counts[e_pair] % 128 != 0))[0] // k
+    if len(ragged):
+        pick += list(rng.choice(np.unique(ragged), min(len(np.unique(ragged)), n_sample // 4), replace=False))
+    pick += [0, N - 1]
+    pick = list(dict.fromkeys(int(t) for t in pick))
+    for t in np.linspace(0, N - 1, 4 * n_sample).astype(np.int64):
+        if len(pick) >= n_sample:
+            break
+        if int(t) not in pick:
+            pick.append(int(t))
+    return sorted(pick[:max(n_sample, len(pick))]), (int(big), int(counts[big]), int(small), int(counts[small]))
+
+
 def _full_chunk_parity(work, n_sample):
-    # the bench's own prefill chunk (same generator, size and launch path),
-    # checked on sampled tokens the oracle computes one expert at a time;
-    # tokens whose k-th and (k+1)-th FP64 logits are within 1e-4 are skipped
-    # (their expert choice is not unique at that tolerance)
+    # the bench's prefill chunk shape, layer and launch path; tokens whose k-th
+    # and (k+1)-th FP64 logits are within 1e-4 are redrawn by the generator
+    # (their expert choice is not unique at that tolerance); sampled tokens
+    # cover the largest and smallest expert groups and ragged last tiles, and
+    # are checked against the oracle, which computes them one expert at a time
     spec, N, seed = work.layer, work.n_tokens, work.seed
-    x, _ = wl.iid_tokens(seed, N, spec.d_model)
+    x, redraws = wl.iid_tokens(seed, N, spec.d_model, reject_near_ties(spec, seed))
     L = build_layer(spec, seed, N, install_all=True)
     y, info = L.forward(bf16_tensor(x), regime=PRE)
-    torch.cuda.synchronize()
     assert info.regime == PRE
-    W_r, b = wl.router_weights(spec, seed)
-    cand = np.unique(np.linspace(0, N - 1, 4 * n_sample).astype(np.int64))
-    tie = olayer.near_tie(wl.bf16_bits_to_f64(x[cand]), W_r, b, spec.k, 1e-4)
-    sample = [int(t) for t, bad in zip(cand, tie) if not bad][:n_sample]
-    assert len(sample) == n_sample
-    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x[sample]), "prefill")
-    assert_close_layer(y[sample], ref, "%s, sampled tokens" % work.name)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx, counts = torch.empty(N * spec.k, **i32), torch.empty(spec.E, **i32)
+    offsets, row_of = torch.empty(spec.E + 1, **i32), torch.empty(N * spec.k, **i32)
+    capi.moe_debug_last_step(L.h, idx=idx, counts=counts, offsets=offsets, row_of=row_of)
+    torch.cuda.synchronize()
+    I = idx.cpu().numpy().reshape(N, spec.k)
+    C, Off, R = counts.cpu().numpy(), offsets.cpu().numpy(), row_of.cpu().numpy()
+    sample, ext = _chunk_sample(C, Off, R, N, spec.k, n_sample, np.random.default_rng(seed))
+    assert len(sample) >= n_sample
+    ref, ridx, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x[sample]), "prefill")
+    assert np.array_equal(I[sample], ridx)
+    assert_close_layer(y[sample], ref, "%s, %d sampled tokens (groups %s)" % (work.name, len(sample), ext))
+    print("%s: %d tokens redrawn; largest group %d (%d rows), smallest %d (%d rows)"
+          % (work.name, redraws, ext[0], ext[1], ext[2], ext[3]))
     L.close()
 
 
 def test_prefill_35b_full_chunk_sampled():
-    _full_chunk_parity(wl.PREFILL_35B, 12)
+    _full_chunk_parity(wl.PREFILL_35B, 128)
 
 
 def test_prefill_753b_full_chunk_sampled():
-    _full_chunk_parity(wl.PREFILL_753B, 4)
+    _full_chunk_parity(wl.PREFILL_753B, 32)
+
+
+_E2M1_MID = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def _near(v, marks, rel=1e-4):
+    """True where v lies within `rel` (relative) of one of the marks."""
+    v = np.asarray(v, np.float64)[..., None]
+    return (np.abs(v - marks) <= rel * marks).any(axis=-1)
+
+
+@pytest.mark.parametrize("spec,N", [
+    (small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True), 300),
+    (small_spec(E=32, k=4, d_model=512, d_ff=512, n_slots=32, fmt="nvfp4", has_shared=True,
+                has_bias=True), 200),
+    (wl.PREFILL_35B.layer, 256),
+])
+def test_prefill_quantised_h_codes(spec, N):
+    # The prefill GEMM quantises h = SiLU(W_g x) * (W_u x) to FP4 from fp32
+    # sums; the oracle quantises the same h from FP64 sums.  A code (or block
+    # scale) may differ only where the oracle's value lies within 1e-4
+    # (relative) of an E2M1 rounding midpoint, or the block's scale input
+    # within 1e-4 of a scale boundary (a power of two for MXFP4, an E4M3
+    # rounding midpoint for NVFP4); the count of such codes is reported.
+    seed = 37
+    L = build_layer(spec, seed, N, install_all=True)
+    x = _tokens(spec, seed, N)
+    L.forward(bf16_tensor(x), regime=PRE)
+    k, f, blk = spec.k, spec.d_ff, spec.block
+    rows = N * k + (N if spec.has_shared else 0)
+    hc = torch.empty(rows, f // 2, dtype=torch.uint8, device="cuda")
+    hs = torch.empty(rows, f // blk, dtype=torch.uint8, device="cuda")
+    capi.moe_debug_last_hidden(L.h, hq_codes=hc, hq_scales=hs)
+    idx = torch.empty(N * k, dtype=torch.int32, device="cuda")
+    row_of = torch.empty(N * k, dtype=torch.int32, device="cuda")
+    capi.moe_debug_last_step(L.h, idx=idx, row_of=row_of)
+    torch.cuda.synchronize()
+    HC = formats.unpack_codes(hc.cpu().numpy())
+    HS = hs.cpu().numpy()
+    I, R = idx.cpu().numpy().reshape(N, k), row_of.cpu().numpy().reshape(N, k)
+    O = oracle_layer(spec, seed)
+    X = wl.bf16_bits_to_f64(x)
+    xq = olayer.act_roundtrip(X, spec.fmt, 1.0)
+    groups = [(e, np.nonzero(I == e)) for e in np.unique(I)]
+    jobs = [(O.expert(int(e)), tt, R[tt, jj]) for e, (tt, jj) in groups]
+    if spec.has_shared:
+        jobs.append((olayer.dequant_expert(O.shared_w, spec.fmt), np.arange(N), N * k + np.arange(N)))
+    total = mism = 0
+    for W, toks, rws in jobs:
+        h = olayer.silu(xq[toks] @ W["gate"].T) * (xq[toks] @ W["up"].T)
+        h32 = h.astype(np.float32)
+        if spec.fmt == "mxfp4":
+            rc, rsc = quant.quant_mxfp4(h)
+            amax = np.abs(h32.reshape(len(toks), -1, blk)).max(axis=-1).astype(np.float64)
+            with np.errstate(divide="ignore"):
+                lg = np.log2(np.where(amax > 0, amax, 1.0))
+            scale_edge = np.abs(amax - np.exp2(np.round(lg))) <= 1e-4 * amax
+            unit = formats.E8M0_TABLE[rsc]
+        else:
+            rc, rsc = quant.quant_nvfp4(h, 1.0)
+            amax = np.abs(h32.reshape(len(toks), -1, blk)).max(axis=-1).astype(np.float64)
+            e4 = np.sort(np.unique(formats.E4M3_TABLE[:0x7F]))
+            mids = (e4[1:] + e4[:-1]) / 2
+            scale_edge = _near(amax / 6.0, mids[mids > 0])
+            unit = formats.E4M3_TABLE[rsc]
+        rcu = formats.unpack_codes(rc)
+        gc, gs = HC[rws], HS[rws]
+        total += rcu.size
+        bad_scale = gs != rsc
+        assert not (bad_scale & ~scale_edge).any(), "block scale differs away from a scale boundary"
+        diff = gc != rcu
+        in_bad_block = np.repeat(bad_scale, blk, axis=1)
+        zero_both = (rcu & 7) == 0
+        zero_both &= (gc & 7) == 0
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = np.abs(h) / np.repeat(unit, blk, axis=1)
+        near_mid = _near(q, _E2M1_MID)
+        unexplained = diff & ~in_bad_block & ~zero_both & ~near_mid
+        assert not unexplained.any(), "%d FP4 codes of h differ away from a rounding midpoint" % unexplained.sum()
+        mism += int((diff & ~zero_both).sum())
+    print("%s N=%d: %d of %d quantised-h codes differ from the oracle, all at rounding boundaries"
+          % (spec, N, mism, total))
+    assert mism <= 1e-3 * total
+    L.close()
 
 
 def test_prefill_with_misses_and_waves():
