@@ -97,6 +97,7 @@ typedef struct {
     size_t fill_bytes; /* bytes copied host -> slots this step                */
     int host_synced;   /* 1 if the call waited for the routing on the host    */
     int n_launches;    /* kernels this call launched                          */
+    int fused_step;    /* 1 if the step ran as one fused launch               */
 } moe_forward_info;
 
 /* Kernel classes of moe_profile_read. */
@@ -111,7 +112,8 @@ typedef struct {
 #define MOE_PROF_PREFILL     7  /* prefill: activation gather + FP4 quantiser   */
 #define MOE_PROF_COMMIT      8  /* no launches: later-wave misses are remapped,
                                    not copied (kept for the class numbering)   */
-#define MOE_PROF_KINDS       9
+#define MOE_PROF_STEP        9  /* the fused decode step (one launch)           */
+#define MOE_PROF_KINDS      10
 
 /* Layout of one expert for a descriptor (no GPU work). */
 int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out);
@@ -239,6 +241,21 @@ int moe_forward(moe_layer_t layer, const void* x, int N, void* y, void* stream,
 #define MOE_FILL_FUSED 3
 #define MOE_FILL_AUTO 4
 int moe_set_fill_mode(moe_layer_t layer, int mode);
+
+/* How a decode step runs.  MOE_DECODE_AUTO (default): as one fused,
+ * cooperative launch -- routing, LRU step, expert FFN over hits and misses,
+ * shared expert and combine, one CTA per SM meeting at grid barriers --
+ * whenever the step allows it, else as the chain of launches.  The fused
+ * launch takes steps of at most 16 tokens with N * k <= 256, E <= 640,
+ * d_model a multiple of 128, whose misses (if any) are filled by the expert
+ * FFN itself (every expert resident, or MOE_FILL_FUSED, or MOE_FILL_AUTO
+ * choosing it).  Both paths compute the same values bit for bit.
+ * MOE_DECODE_CHAIN: always the chain.  MOE_DECODE_STEP: always fused;
+ * moe_forward returns MOE_ERR_UNSUPPORTED for a step that cannot be. */
+#define MOE_DECODE_AUTO  0
+#define MOE_DECODE_CHAIN 1
+#define MOE_DECODE_STEP  2
+int moe_set_decode_path(moe_layer_t layer, int path);
 
 /* Totals since create, accumulated on the device by the LRU step of every
  * moe_forward: out4 = {steps, distinct experts, hits, misses}.  Synchronizes

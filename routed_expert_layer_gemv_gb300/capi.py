@@ -29,7 +29,12 @@ MOE_ERR_UNSUPPORTED = -8
 MOE_MXFP4 = 0
 MOE_NVFP4 = 1
 
-MOE_PROF_NAMES = ["router", "permute", "lru", "gateup", "down", "combine", "fill", "prefill", "commit"]
+MOE_PROF_NAMES = ["router", "permute", "lru", "gateup", "down", "combine", "fill", "prefill", "commit",
+                  "step"]
+
+MOE_DECODE_AUTO = 0
+MOE_DECODE_CHAIN = 1
+MOE_DECODE_STEP = 2
 
 MOE_FILL_MEMCPY = 0
 MOE_FILL_DEVICE = 1
@@ -63,7 +68,8 @@ class moe_expert_layout(C.Structure):
 class moe_forward_info(C.Structure):
     _fields_ = [("regime", C.c_int), ("n_tokens", C.c_int), ("n_distinct", C.c_int),
                 ("n_hits", C.c_int), ("n_misses", C.c_int), ("n_waves", C.c_int),
-                ("fill_bytes", C.c_size_t), ("host_synced", C.c_int), ("n_launches", C.c_int)]
+                ("fill_bytes", C.c_size_t), ("host_synced", C.c_int), ("n_launches", C.c_int),
+                ("fused_step", C.c_int)]
 
 
 _P = C.c_void_p
@@ -81,6 +87,7 @@ _SIGS = {
     "moe_lru_set_state": ([_P, _P, _P, C.c_uint64], _I),
     "moe_forward": ([_P, _P, _I, _P, _P, _I, C.POINTER(moe_forward_info)], _I),
     "moe_set_fill_mode": ([_P, _I], _I),
+    "moe_set_decode_path": ([_P, _I], _I),
     "moe_stats": ([_P, _P], _I),
     "moe_profile": ([_P, _I], _I),
     "moe_profile_read": ([_P, _P, _P], _I),
@@ -226,6 +233,10 @@ def moe_forward(h, x, N: int, y, stream=None, regime: int = MOE_REGIME_AUTO) -> 
 
 def moe_set_fill_mode(h, mode: int) -> None:
     check(lib().moe_set_fill_mode(h, mode), h)
+
+
+def moe_set_decode_path(h, path: int) -> None:
+    check(lib().moe_set_decode_path(h, path), h)
 
 
 def moe_stats(h):

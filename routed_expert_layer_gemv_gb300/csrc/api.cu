@@ -35,6 +35,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "step.cuh"
 
 using namespace moe;
 
@@ -131,6 +132,13 @@ struct moe_layer {
   std::vector<int> prof_kind;          // one entry per timed launch (pair of events)
   int launches = 0;                    // kernels launched by the current call
   int last_N = 0;                      // tokens of the last moe_forward (0: none yet)
+  // fused decode step
+  int decode_path = MOE_DECODE_AUTO;
+  bool step_failed = false;            // a cooperative launch was refused once: use the chain
+  unsigned long long* gbar = nullptr;  // grid-barrier arrival counter (device)
+  unsigned long long gbar_base = 0;    // its value before the next fused step
+  unsigned long long* ready = nullptr; // publication word of a fused step's miss buffers (device)
+  unsigned long long ready_seq = 0;
   bool inject_fill = false;            // test hook: the next host-issued fill fails before its copy
   long long inject_wait = 0;           // test hook: wait limit (cycles) of the next forward's expert FFN
   bool last_prefill = false;           // regime of the last moe_forward
@@ -450,6 +458,8 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   L->list_cap = (int)std::max<size_t>(Nm * g.k, (size_t)g.E);
   MOE_ALLOC(list_dev, (size_t)L->list_cap * 4);
   MOE_ALLOC(rcounter, 16);
+  MOE_ALLOC(gbar, 8);
+  MOE_ALLOC(ready, 8);
   MOE_ALLOC(stats, 64);
   const bool prefill_ok = prefill_shape_ok(g);
   const size_t prows = Nm * g.k + Nm + 128;   // permuted rows (+ shared) + one tile of padding
@@ -519,6 +529,8 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
               cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
               cudaMemset(L->rec, 0, rec_dev_bytes(g.E)) == cudaSuccess &&
               cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
+              cudaMemset(L->gbar, 0, 8) == cudaSuccess &&
+              cudaMemset(L->ready, 0, 8) == cudaSuccess &&
               cudaMemset(L->stats, 0, 64) == cudaSuccess;
     // slot s in buffer s; the spares after the shared expert's buffer S
     std::vector<int> b0(g.S + g.X);
@@ -763,6 +775,11 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   const bool prefill = regime == MOE_REGIME_PREFILL || (regime == MOE_REGIME_AUTO && N > 64 && L->plan);
   if (*L->err_host) {
     *L->err_host = 0;
+    // a fused step that gave up may have left its barrier counter short:
+    // start it again from zero, after every launch already queued
+    cudaStream_t st0 = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(L->gbar, 0, 8, st0) != cudaSuccess) cudaGetLastError();
+    L->gbar_base = 0;
     return fail(L, MOE_ERR_TIMEOUT, "a wait inside an earlier step's kernel timed out; its output is invalid");
   }
   const bool resident = all_resident(L);
@@ -798,6 +815,85 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   else if (!y_dev) yd = L->y_stage;
 
   L->launches = x_direct ? 1 : 0;
+  {
+    // the whole decode step as one launch (step.cu), when every expert is
+    // resident or misses are filled by the expert FFN itself
+    int fm = L->fill_mode;
+    if (fm == MOE_FILL_AUTO) fm = std::min(g.E, N * g.k) <= g.S ? MOE_FILL_FUSED : MOE_FILL_KERNEL;
+    const bool fused_fill = !resident && fm == MOE_FILL_FUSED && L->pool_dev;
+    StepPlan plan{};
+    const bool want = !prefill && L->decode_path != MOE_DECODE_CHAIN && !L->step_failed && L->num_sms >= 2;
+    const bool can = want && (resident || fused_fill) && step_plan(g, N, &plan);
+    if (L->decode_path == MOE_DECODE_STEP && !can)
+      return fail(L, MOE_ERR_UNSUPPORTED, "this step cannot run as one fused launch (N = %d, fill mode %d)", N, fm);
+    if (can) {
+      GemvArgs a{};
+      a.slots = L->slots;
+      a.shared_w = L->shared_w;
+      a.rec = L->rec;
+      a.N = N;
+      a.mode = kRangeAll;
+      a.host_pool = fused_fill ? L->pool_dev : nullptr;
+      a.with_shared = g.has_shared;
+      a.err = L->err_dev;
+      a.hmax = L->hmax;
+      a.wait_cycles = L->inject_wait;
+      L->inject_wait = 0;
+      StepArgs sa{};
+      sa.x = xd;
+      sa.Wr = L->Wr;
+      sa.bias = g.has_bias ? L->bias : nullptr;
+      sa.logits = L->logits;
+      sa.idx = L->idx;
+      sa.gates = L->gates;
+      sa.counts = L->counts;
+      sa.offsets = L->offsets;
+      sa.row_of = L->row_of;
+      sa.tok_of = L->tok_of;
+      sa.slot_of = L->slot_of;
+      sa.expert_of = L->expert_of;
+      sa.buf = L->buf;
+      sa.stamp = L->stamp;
+      sa.clock = L->clock;
+      sa.rec = L->rec;
+      sa.stats = L->stats;
+      sa.ready = L->ready;
+      sa.seq = ++L->ready_seq;
+      sa.gbar = L->gbar;
+      sa.gbar_base = L->gbar_base;
+      sa.h = L->h;
+      sa.O = L->O;
+      sa.y = yd;
+      cudaEvent_t* ps = prof_begin(L, MOE_PROF_STEP, st);
+      const cudaError_t ce = launch_step(g, L->gplan, a, sa, plan, L->num_sms, st);
+      prof_end(ps, st);
+      if (ce == cudaSuccess) {
+        L->gbar_base += 3ull * (unsigned long long)L->num_sms;
+        L->launches += 1;
+        if (!y_dev) {
+          if (!y_direct) MOE_CUDA(L, cudaMemcpyAsync(y, yd, xbytes, cudaMemcpyDeviceToHost, st));
+          MOE_CUDA(L, cudaStreamSynchronize(st));
+        }
+        L->last_N = N;
+        L->last_prefill = false;
+        if (info) {
+          info->regime = MOE_REGIME_DECODE;
+          info->n_distinct = info->n_hits = -1;
+          info->n_misses = resident ? 0 : -1;
+          info->n_waves = 1;
+          info->fill_bytes = 0;
+          info->host_synced = 0;
+          info->n_launches = L->launches;
+          info->fused_step = 1;
+        }
+        return MOE_OK;
+      }
+      // a device that cannot hold the cooperative grid: the chained launches from now on
+      cudaGetLastError();
+      if (L->decode_path == MOE_DECODE_STEP) return cuda_fail(L, ce, "launch_step");
+      L->step_failed = true;
+    }
+  }
   cudaEvent_t* pe = prof_begin(L, MOE_PROF_ROUTER, st);
   MOE_CUDA(L, launch_router(g, xd, N, L->Wr, L->Wr_hl, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
                             L->gates, L->xexp, L->rcounter, st));
@@ -1068,6 +1164,14 @@ int moe_set_fill_mode(moe_layer_t L, int mode) {
     return fail(L, MOE_ERR_STATE, "copy-kernel fills need a registered pinned host pool the device can address");
   L->fill_mode = mode;
   L->fill_mode_chosen = true;
+  return MOE_OK;
+}
+
+int moe_set_decode_path(moe_layer_t L, int path) {
+  if (!L) return MOE_ERR_ARG;
+  if (path != MOE_DECODE_AUTO && path != MOE_DECODE_CHAIN && path != MOE_DECODE_STEP)
+    return fail(L, MOE_ERR_ARG, "unknown decode path %d", path);
+  L->decode_path = path;
   return MOE_OK;
 }
 

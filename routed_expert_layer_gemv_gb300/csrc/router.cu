@@ -16,67 +16,15 @@
 // topk: one warp per token on its logits row staged in shared memory; k
 // rounds of a warp-wide argmax.
 #include "common.cuh"
+#include "router_dev.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kRouterWarps = 8;
-
-MOE_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
-
-// One warp: the k largest of the logits row L (shared memory, E <= 1024
-// entries; ties to the lower expert id), gates, written in ascending id order.
-MOE_DEV void topk_row(const float* L, int E, int k, int norm_topk, int* idx, float* gates) {
-  const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;  // bit i: entry lane + 32 i already selected
-  int my_e = -1;
-  float my_v = 0.f, top = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int i = 0, e = lane; e < E; ++i, e += 32) {
-      if (taken & (1u << i)) continue;
-      const float v = L[e];
-      if (better(v, e, bv, be)) { bv = v; be = e; }
-    }
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (j == 0) top = bv;
-    if (lane == j) { my_e = be; my_v = bv; }
-  }
-  // gates (fp32): softmax over the selected logits, or the full softmax
-  const float num = lane < k ? expf(my_v - top) : 0.f;
-  float den = 0.f;
-  if (norm_topk) {
-    den = num;
-  } else {
-    for (int e = lane; e < E; e += 32) den += expf(L[e] - top);
-  }
-  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  // ascending expert order: rank of my_e among the k selected
-  int rank = 0;
-  for (int i = 0; i < k; ++i) {
-    const int oe = __shfl_sync(0xffffffffu, my_e, i);
-    rank += (lane < k && oe < my_e) ? 1 : 0;
-  }
-  if (lane < k) {
-    idx[rank] = my_e;
-    gates[rank] = num / den;
-  }
-}
-
-// Stage row t of the logits into this warp's shared row, bypassing L1 (the
-// row may have been written by other CTAs of the same launch).
-MOE_DEV void stage_logits(const float* logits, int t, int E, float* Ls) {
-  const int lane = threadIdx.x & 31;
-  for (int e = lane; e < E; e += 32) Ls[e] = __ldcg(logits + (size_t)t * E + e);
-  __syncwarp();
-}
+using rt::kRouterWarps;
+using rt::stage_logits;
+using rt::topk_row;
 
 // Decode-sized batches (N <= 64): one CTA per expert and token tile, its 8
 // warps splitting K, so each lane issues all of its W_r loads at once (2
@@ -97,77 +45,23 @@ router_dec_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
   const int e = blockIdx.x, t0 = blockIdx.y * TN;
   const int nt = min(TN, N - t0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ks = d / kRouterWarps;          // this warp's K slice (a multiple of 16)
-  const int k0 = warp * ks;
-  // W_r: 4 floats per load, every load of the slice issued before any use
-  const float4* w4 = reinterpret_cast<const float4*>(Wr + (size_t)e * d + k0);
-  const int nv = ks / 4;                     // float4 per warp slice
-  float acc[TN];
+  {
+    float sum[TN];
+    rt::router_dot<TN>(x, t0, nt, d, Wr + (size_t)e * d, warp, sum);
 #pragma unroll
-  for (int t = 0; t < TN; ++t) acc[t] = 0.f;
-  for (int base = 0; base < nv; base += 4 * 32) {
-    float4 w[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = base + u * 32 + lane;
-      w[u] = i < nv ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int t = 0; t < TN; ++t) {
-      if (t < nt) {
-        const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * d + k0);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = base + u * 32 + lane;
-          if (i < nv) {
-            const uint2 xv = xr[i];
-            acc[t] = fmaf(w[u].x, __uint_as_float(xv.x << 16), acc[t]);
-            acc[t] = fmaf(w[u].y, __uint_as_float(xv.x & 0xffff0000u), acc[t]);
-            acc[t] = fmaf(w[u].z, __uint_as_float(xv.y << 16), acc[t]);
-            acc[t] = fmaf(w[u].w, __uint_as_float(xv.y & 0xffff0000u), acc[t]);
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < TN; ++t) {
-    float v = acc[t];
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) part[warp][t] = v;
+    for (int t = 0; t < TN; ++t)
+      if (lane == 0) part[warp][t] = sum[t];
   }
   if (e == 0 && xexp != nullptr) {
-    // per-token exponent s with amax(|x|) * 2^-s in [2^14, 2^15): warp t takes token t
+    // per-token exponent of x (the decode GEMV's f16 conversion): warp t takes token t
     for (int t = warp; t < nt; t += kRouterWarps) {
-      const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d);
-      float m = 0.f;
-      for (int i = lane; i < d / 8; i += 32) {
-        const uint4 v = xr[i];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xffff0000u))));
-      }
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) {
-        int s = 0;
-        if (m > 0.f) {
-          int ex;
-          frexpf(m, &ex);
-          s = max(-100, min(100, ex - 15));
-        }
-        xexp[t0 + t] = s;
-      }
+      const int s = rt::token_exp(x + (size_t)(t0 + t) * d, d);
+      if (lane == 0) xexp[t0 + t] = s;
     }
   }
   __syncthreads();
-  if (threadIdx.x < nt) {
-    float v = bias ? bias[e] : 0.f;
-    float sum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kRouterWarps; ++w) sum += part[w][threadIdx.x];
-    logits[(size_t)(t0 + threadIdx.x) * E + e] = sum + v;
-  }
+  if (threadIdx.x < nt)
+    logits[(size_t)(t0 + threadIdx.x) * E + e] = rt::logit_from_parts(&part[0][threadIdx.x], TN, bias ? bias[e] : 0.f);
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -333,29 +227,12 @@ router_tc_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E, const
         }
       }
   if (blockIdx.y == 0 && xexp != nullptr) {
-    // per-token exponent s with amax(|x|) * 2^-s in [2^14, 2^15): warp w takes tokens w, w + 8, ...
+    // per-token exponent of x (the decode GEMV's f16 conversion): warp w takes tokens w, w + 8, ...
     for (int tl = warp; tl < kTcM; tl += 8) {
       const int t = t0 + tl;
       if (t >= N) break;
-      const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-      float m = 0.f;
-      for (int i2 = lane; i2 < d / 8; i2 += 32) {
-        const uint4 v = xr[i2];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq)
-          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[qq] << 16)), fabsf(__uint_as_float(wv[qq] & 0xffff0000u))));
-      }
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) {
-        int s = 0;
-        if (m > 0.f) {
-          int ex;
-          frexpf(m, &ex);
-          s = max(-100, min(100, ex - 15));
-        }
-        xexp[t] = s;
-      }
+      const int s = rt::token_exp(x + (size_t)t * d, d);
+      if (lane == 0) xexp[t] = s;
     }
   }
 }

@@ -1,0 +1,159 @@
+// Device pieces of the router shared by the router kernels and the fused
+// decode step: the decode-size dot products (one expert's K split over 8
+// warps), the per-token f16 exponent of x, and the warp top-k with gates.
+//
+// The pages do not define the router (they only say routing picks a few
+// experts per token and varies per layer and token: "FreeToken：把 284B MoE
+// 塞进游戏 PC", zhichai.net, §二 "Decode" paragraph; ananclaw.com explainer,
+// §核心方法 1); this is the standard softmax top-k router.  Both the chained
+// decode path and the fused step call these functions, so their logits, ids
+// and gates agree bit for bit.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+namespace rt {
+
+constexpr int kRouterWarps = 8;
+
+MOE_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+
+// One warp: the k largest of the logits row L (shared memory, E <= 1024
+// entries; ties to the lower expert id), gates, written in ascending id order.
+MOE_DEV void topk_row(const float* L, int E, int k, int norm_topk, int* idx, float* gates) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;  // bit i: entry lane + 32 i already selected
+  int my_e = -1;
+  float my_v = 0.f, top = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int i = 0, e = lane; e < E; ++i, e += 32) {
+      if (taken & (1u << i)) continue;
+      const float v0 = L[e];
+      const float v = v0 == v0 ? v0 : -INFINITY;   // a NaN logit ranks last, so every id stays valid
+      if (better(v, e, bv, be)) { bv = v; be = e; }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (j == 0) top = bv;
+    if (lane == j) { my_e = be; my_v = bv; }
+  }
+  // gates (fp32): softmax over the selected logits, or the full softmax
+  const float num = lane < k ? expf(my_v - top) : 0.f;
+  float den = 0.f;
+  if (norm_topk) {
+    den = num;
+  } else {
+    for (int e = lane; e < E; e += 32) den += expf(L[e] - top);
+  }
+  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  // ascending expert order: rank of my_e among the k selected
+  int rank = 0;
+  for (int i = 0; i < k; ++i) {
+    const int oe = __shfl_sync(0xffffffffu, my_e, i);
+    rank += (lane < k && oe < my_e) ? 1 : 0;
+  }
+  if (lane < k) {
+    idx[rank] = my_e;
+    gates[rank] = num / den;
+  }
+}
+
+// Stage row t of the logits into this warp's shared row, bypassing L1 (the
+// row may have been written by other CTAs of the same launch).
+MOE_DEV void stage_logits(const float* logits, int t, int E, float* Ls) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < E; e += 32) Ls[e] = __ldcg(logits + (size_t)t * E + e);
+  __syncwarp();
+}
+
+// Power-of-two exponent s of one token row (d bf16 values) with
+// max|x| 2^-s in [2^14, 2^15) (0 for a zero row), computed by one warp; every
+// lane returns it.  The decode expert GEMV converts x 2^-s to f16, which then
+// neither overflows nor loses precision to subnormals.
+MOE_DEV int token_exp(const __nv_bfloat16* __restrict__ xr, int d) {
+  const int lane = threadIdx.x & 31;
+  const uint4* x4 = reinterpret_cast<const uint4*>(xr);
+  float m = 0.f;
+  for (int i = lane; i < d / 8; i += 32) {
+    const uint4 v = x4[i];
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xffff0000u))));
+  }
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int s = 0;
+  if (m > 0.f) {
+    int ex;
+    frexpf(m, &ex);
+    s = max(-100, min(100, ex - 15));
+  }
+  return s;
+}
+
+// Warp `warp` (of kRouterWarps) of one expert's dot products with tokens
+// t0 .. t0 + nt - 1 (nt <= TN): the warp's K slice d / 8 (a multiple of 16),
+// every W_r load of the slice issued before any use (2 float4 per lane for
+// d = 2048), x straight from L2.  sum[t] (every lane) = the warp's partial
+// dot product of token t0 + t; the caller adds the 8 partials in warp order.
+template <int TN>
+MOE_DEV void router_dot(const __nv_bfloat16* __restrict__ x, int t0, int nt, int d, const float* __restrict__ wrow,
+                        int warp, float (&sum)[TN]) {
+  const int lane = threadIdx.x & 31;
+  const int ks = d / kRouterWarps;
+  const int k0 = warp * ks;
+  const float4* w4 = reinterpret_cast<const float4*>(wrow + k0);
+  const int nv = ks / 4;
+  float acc[TN];
+#pragma unroll
+  for (int t = 0; t < TN; ++t) acc[t] = 0.f;
+  for (int base = 0; base < nv; base += 4 * 32) {
+    float4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * 32 + lane;
+      w[u] = i < nv ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int t = 0; t < TN; ++t) {
+      if (t < nt) {
+        const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * d + k0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = base + u * 32 + lane;
+          if (i < nv) {
+            const uint2 xv = xr[i];
+            acc[t] = fmaf(w[u].x, __uint_as_float(xv.x << 16), acc[t]);
+            acc[t] = fmaf(w[u].y, __uint_as_float(xv.x & 0xffff0000u), acc[t]);
+            acc[t] = fmaf(w[u].z, __uint_as_float(xv.y << 16), acc[t]);
+            acc[t] = fmaf(w[u].w, __uint_as_float(xv.y & 0xffff0000u), acc[t]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TN; ++t) {
+    float v = acc[t];
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    sum[t] = v;
+  }
+}
+
+// The logit of expert e from its 8 warp partials part[w] (warp order) and
+// the bias: the same sum on every path.
+MOE_DEV float logit_from_parts(const float* part, int stride, float bias) {
+  float sum = 0.f;
+#pragma unroll
+  for (int w = 0; w < kRouterWarps; ++w) sum += part[w * stride];
+  return sum + bias;
+}
+
+}  // namespace rt
+}  // namespace moe

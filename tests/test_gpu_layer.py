@@ -54,11 +54,12 @@ def test_forward_all_resident(spec, N):
     L.close()
 
 
-def _decode_run(spec, seed, batch, steps, check_every=1, fill=capi.MOE_FILL_MEMCPY):
+def _decode_run(spec, seed, batch, steps, check_every=1, fill=capi.MOE_FILL_MEMCPY, path=capi.MOE_DECODE_AUTO):
     N = batch
     experts = CachedExperts(spec, seed, cap=96)
     L = build_layer(spec, seed, N, experts_fn=experts)
     capi.moe_set_fill_mode(L.h, fill)
+    capi.moe_set_decode_path(L.h, path)
     O = oracle_layer(spec, seed, experts)
     T = SlotTable(spec.E, spec.n_slots)
     xs, _ = wl.ar1_tokens(seed, batch, steps, spec.d_model, 0.9, reject_near_ties(spec, seed))
@@ -135,6 +136,131 @@ def test_decode_copy_kernel_fill(batch, steps, fill):
     spec = wl.DECODE_35B.layer
     miss, u, waves = _decode_run(spec, 7, batch, steps, fill=fill)
     assert miss > 0
+
+
+@pytest.mark.parametrize("batch,steps", [(1, 6), (4, 4), (16, 3)])
+def test_chained_fused_fill(batch, steps):
+    # the chained path's own fused fills (the expert GEMV reads misses from the
+    # host pool), which the fused decode step otherwise takes over
+    spec = wl.DECODE_35B.layer
+    miss, u, waves = _decode_run(spec, 7, batch, steps, fill=capi.MOE_FILL_FUSED, path=capi.MOE_DECODE_CHAIN)
+    assert miss > 0
+
+
+def _step_pair(spec, seed, N, **kw):
+    chain = build_layer(spec, seed, N, **kw)
+    step = build_layer(spec, seed, N, **kw)
+    capi.moe_set_decode_path(chain.h, capi.MOE_DECODE_CHAIN)
+    capi.moe_set_decode_path(step.h, capi.MOE_DECODE_STEP)
+    return chain, step
+
+
+def _last(L, spec, N):
+    i32 = dict(dtype=torch.int32, device="cuda")
+    out = [torch.empty(N * spec.k, **i32), torch.empty(N * spec.k, dtype=torch.float32, device="cuda"),
+           torch.empty(spec.E, **i32), torch.empty(spec.E + 1, **i32), torch.empty(N * spec.k, **i32),
+           torch.empty(N * spec.k, **i32)]
+    capi.moe_debug_last_step(L.h, *out)
+    torch.cuda.synchronize()
+    return [o.cpu() for o in out]
+
+
+@pytest.mark.parametrize("spec,N", [
+    (wl.TINY.layer, 1),
+    (wl.TINY.layer, 16),
+    (small_spec(E=8, k=2, d_model=256, d_ff=512, n_slots=8, has_shared=True), 13),
+    (small_spec(E=32, k=4, d_model=512, d_ff=256, n_slots=32, fmt="nvfp4", has_shared=True,
+                has_bias=True), 9),
+    (small_spec(E=16, k=16, d_model=384, d_ff=384, n_slots=16), 3),       # k = E
+    (small_spec(E=1, k=1, d_model=256, d_ff=128, n_slots=1), 5),          # E = 1
+    (small_spec(E=4, k=2, d_model=6144, d_ff=256, n_slots=4, fmt="nvfp4", has_shared=True,
+                has_bias=True), 12),                                      # wide K, 2 token groups
+    (small_spec(E=300, k=8, d_model=512, d_ff=256, n_slots=300), 16),     # E > 2 x the SM count
+    (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 1),     # the 35B-A3B layer
+    (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 16),
+    (small_spec(E=256, k=8, d_model=4096, d_ff=2048, n_slots=256, has_shared=True), 8),   # 284B-class
+])
+def test_fused_step_matches_chain_bitwise_all_resident(spec, N):
+    # one fused launch computes the chained launches' values bit for bit
+    # (same router sums, same GEMV arithmetic, same combine order), and both
+    # match the oracle
+    seed = 29
+    chain, step = _step_pair(spec, seed, N, install_all=True)
+    x = _tokens(spec, seed, N)
+    for rep in range(2):
+        yc, ic = chain.forward(bf16_tensor(x), regime=DEC)
+        ys, is_ = step.forward(bf16_tensor(x), regime=DEC)
+        torch.cuda.synchronize()
+        assert ic.fused_step == 0 and is_.fused_step == 1 and is_.n_launches == 1
+        assert torch.equal(ys.cpu().view(torch.int16), yc.cpu().view(torch.int16)), rep
+        for a, b in zip(_last(step, spec, N), _last(chain, spec, N)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ref, idx, gates = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x), "decode")
+    assert_close_layer(ys, ref, "fused step %s N=%d" % (spec, N))
+    check_last_step(step, spec, N, idx, gates)
+    assert capi.moe_stats(step.h)[:2] == capi.moe_stats(chain.h)[:2]
+    chain.close()
+    step.close()
+
+
+@pytest.mark.parametrize("spec,batch,steps", [
+    (wl.DECODE_35B.layer, 1, 8),
+    (wl.DECODE_35B.layer, 4, 5),
+    (wl.DECODE_35B.layer, 16, 3),                                          # U > 47 slots: spares
+    (small_spec(E=32, k=4, d_model=256, d_ff=256, n_slots=6, fmt="nvfp4", has_shared=True), 8, 4),
+    (wl.DECODE_284B.layer, 1, 6),
+])
+def test_fused_step_with_misses_matches_chain_bitwise(spec, batch, steps):
+    # misses read from the pinned host pool inside the fused launch and
+    # written on to the buffers its LRU CTA publishes: outputs, slot table and
+    # later hits (the filled slots) match the chained path bit for bit
+    seed = 31
+    experts = CachedExperts(spec, seed, cap=96)
+    chain, step = _step_pair(spec, seed, batch, experts_fn=experts)
+    capi.moe_set_fill_mode(chain.h, capi.MOE_FILL_FUSED)
+    capi.moe_set_fill_mode(step.h, capi.MOE_FILL_FUSED)
+    O = oracle_layer(spec, seed, experts)
+    T = SlotTable(spec.E, spec.n_slots)
+    xs, _ = wl.ar1_tokens(seed, batch, steps, spec.d_model, 0.9, reject_near_ties(spec, seed))
+    miss = 0
+    for t in range(steps):
+        yc, _ = chain.forward(bf16_tensor(xs[t]), regime=DEC)
+        ys, info = step.forward(bf16_tensor(xs[t]), regime=DEC)
+        torch.cuda.synchronize()
+        assert info.fused_step == 1
+        assert torch.equal(ys.cpu().view(torch.int16), yc.cpu().view(torch.int16)), t
+        ref, idx, gates = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
+        acc = T.step(idx.reshape(-1))
+        miss += sum(1 for a in acc if not a[2])
+        assert_close_layer(ys, ref, "step %d" % t)
+        check_last_step(step, spec, batch, idx, gates)
+        eo, st, clk = capi.moe_lru_get_state(step.h, spec.n_slots)
+        assert eo == T.expert_of and st == T.stamp and clk == T.clock
+        assert (eo, st, clk) == capi.moe_lru_get_state(chain.h, spec.n_slots)
+    assert miss > 0
+    assert capi.moe_stats(step.h) == capi.moe_stats(chain.h)
+    chain.close()
+    step.close()
+
+
+def test_decode_path_selection():
+    spec = wl.TINY.layer
+    L = build_layer(spec, 3, 64, install_all=True)
+    x = _tokens(spec, 3, 64)
+    _, info = L.forward(bf16_tensor(x[:8]), regime=DEC)
+    assert info.fused_step == 1                          # AUTO: eligible steps run fused
+    _, info = L.forward(bf16_tensor(x[:17]), regime=DEC)
+    assert info.fused_step == 0                          # more than 16 tokens: the chain
+    capi.moe_set_decode_path(L.h, capi.MOE_DECODE_STEP)
+    with pytest.raises(capi.MoeError) as e:
+        L.forward(bf16_tensor(x[:17]), regime=DEC)
+    assert e.value.status == capi.MOE_ERR_UNSUPPORTED
+    capi.moe_set_decode_path(L.h, capi.MOE_DECODE_CHAIN)
+    _, info = L.forward(bf16_tensor(x[:8]), regime=DEC)
+    assert info.fused_step == 0
+    with pytest.raises(capi.MoeError):
+        capi.moe_set_decode_path(L.h, 7)
+    L.close()
 
 
 @pytest.mark.parametrize("fill", [capi.MOE_FILL_KERNEL, capi.MOE_FILL_FUSED])
@@ -294,7 +420,7 @@ def test_allocation_failure_at_each_allocation_leaks_nothing():
     # every device or pinned allocation of a create made to fail in turn: the
     # create returns MOE_ERR_OOM and gives back everything it took; a normal
     # layer afterwards still matches the oracle
-    spec = small_spec(E=8, k=2, d_model=256, d_ff=256, n_slots=4, has_shared=True)
+    spec = small_spec(E=8, k=2, d_model=256, d_ff=256, n_slots=8, has_shared=True)
     desc = MoELayer(spec, 16).desc   # (creates and drops one layer: warms up the runtime)
     torch.cuda.synchronize()
     base = capi.moe_debug_alloc_fault(0)
@@ -365,8 +491,9 @@ def test_fill_failure_drops_the_step_misses_and_later_steps_match():
     L.close()
 
 
+@pytest.mark.parametrize("path", [capi.MOE_DECODE_CHAIN, capi.MOE_DECODE_STEP])
 @pytest.mark.parametrize("batch", [1, 8, 16])
-def test_device_wait_timeout_is_reported_and_the_layer_recovers(batch):
+def test_device_wait_timeout_is_reported_and_the_layer_recovers(batch, path):
     # the bounded waits of one forward's decode expert FFN are cut to one
     # cycle, so its first wait gives up: the launch records the timeout and
     # returns normally (no trap, no unbounded wait), the next moe_forward
@@ -374,6 +501,7 @@ def test_device_wait_timeout_is_reported_and_the_layer_recovers(batch):
     spec = small_spec(E=16, k=2, d_model=512, d_ff=256, n_slots=16, has_shared=True)
     seed = 23
     L = build_layer(spec, seed, batch, install_all=True)
+    capi.moe_set_decode_path(L.h, path)
     x0, x1 = _tokens(spec, seed, batch), _tokens(spec, seed + 1, batch)
     capi.moe_debug_inject(L.h, capi.MOE_INJECT_WAIT_LIMIT, 1)
     L.forward(bf16_tensor(x0), regime=DEC)
@@ -381,9 +509,10 @@ def test_device_wait_timeout_is_reported_and_the_layer_recovers(batch):
     with pytest.raises(capi.MoeError) as e:
         L.forward(bf16_tensor(x1), regime=DEC)
     assert e.value.status == capi.MOE_ERR_TIMEOUT
-    y, _ = L.forward(bf16_tensor(x1), regime=DEC)
-    ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x1), "decode")
-    assert_close_layer(y, ref, "after the timeout")
+    for rep in range(2):   # (the fused step's barrier counter restarts after the timeout)
+        y, _ = L.forward(bf16_tensor(x1), regime=DEC)
+        ref, _, _ = oracle_layer(spec, seed).forward(wl.bf16_bits_to_f64(x1), "decode")
+        assert_close_layer(y, ref, "after the timeout, call %d" % rep)
     L.close()
 
 
