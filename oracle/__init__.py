@@ -19,8 +19,18 @@ so the oracle writes out the standard definitions the pages' names refer to:
   gate-weighted combine and the optional shared expert;
 * ``lru``      the per-step LRU slot table of the expert cache.
 
+Two implementations of the same definitions:
+
+* ``oracle.native`` -- plain C++ in FP64 (``moe_oracle.cpp``, built by
+  ``oracle/build.py`` into ``oracle/_lib/liboracle.so``): fixed-order loops,
+  OpenMP over tokens and rows.  This is the oracle the GPU parity tests, the
+  smoke check and the bench's CPU baseline use.
+* the numpy modules of this package (``formats``, ``quant``, ``layer``,
+  ``lru``), kept as a cross-check.
+
 Every function names the passage it follows and, where the pages are silent,
-the reading taken.  Parity pins (tests marked ``not gpu``) check each piece
-against closed forms, library routines and brute force.
+the reading taken.  Parity pins (tests marked ``not gpu``) check each piece of
+both implementations against closed forms, library routines and brute force,
+and the two against each other.
 """
 from . import formats, quant, layer, lru  # noqa: F401

@@ -418,7 +418,7 @@ bool step_plan(const Geo& g, int N, StepPlan* out) {
   // dynamic shared memory: 1 KB alignment slack, the GEMV layout, the routing copy
   const int budget = kStepSmemMax - 1024 - (int)sizeof(Ctl) - 16;
   const int D = std::min(kMaxD, (budget - xregion - red - bars) / stage);
-  if (D < 3) return false;
+  if (D < 2) return false;
   for (SG* q : {&a, &b}) {
     q->stage_bytes = stage;
     q->D = D;

@@ -23,3 +23,25 @@ def read_golden(name):
             if line:
                 rows.append(line.split())
     return rows
+
+
+# The oracle's two implementations: the C++ FP64 one (oracle/moe_oracle.cpp,
+# the reference every GPU parity test uses) and the numpy one it is
+# cross-checked against.  The pins run against both.
+ORACLES = ("native", "numpy")
+
+
+def oracle_ns(name):
+    import importlib
+    return importlib.import_module("oracle.native" if name == "native" else "oracle")
+
+
+def swap_oracle(module_name, request, monkeypatch, names):
+    """Rebind the test module's oracle modules (``formats``, ``quant``,
+    ``layer``) and ``SlotTable`` to the implementation the fixture
+    parameter names."""
+    mod = sys.modules[module_name]
+    ns = oracle_ns(request.param)
+    for n in names:
+        monkeypatch.setattr(mod, n, ns.lru.SlotTable if n == "SlotTable" else getattr(ns, n))
+    return request.param

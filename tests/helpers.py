@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import layer as olayer
+from oracle.native import layer as olayer
 from routed_expert_layer_gemv_gb300 import workloads as wl
 
 # Output tolerance of the layer (bf16 activations, fp32 accumulation):

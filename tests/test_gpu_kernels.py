@@ -7,9 +7,9 @@ import pytest
 import torch
 
 from helpers import bf16_tensor, need_gpu, oracle_layer, reject_near_ties, small_spec
-from oracle import formats, quant
-from oracle import layer as olayer
-from oracle.lru import SlotTable
+from oracle.native import formats, quant
+from oracle.native import layer as olayer
+from oracle.native.lru import SlotTable
 from routed_expert_layer_gemv_gb300 import capi
 from routed_expert_layer_gemv_gb300 import workloads as wl
 from routed_expert_layer_gemv_gb300.layer import build_layer

@@ -8,9 +8,9 @@ import torch
 
 from helpers import (CachedExperts, assert_close_layer, bf16_tensor, check_last_step, need_gpu,
                      oracle_layer, reject_near_ties, small_spec)
-from oracle import formats, quant
-from oracle import layer as olayer
-from oracle.lru import SlotTable
+from oracle.native import formats, quant
+from oracle.native import layer as olayer
+from oracle.native.lru import SlotTable
 from routed_expert_layer_gemv_gb300 import capi
 from routed_expert_layer_gemv_gb300 import workloads as wl
 from routed_expert_layer_gemv_gb300.layer import MoELayer, build_layer
@@ -174,7 +174,7 @@ def _last(L, spec, N):
     (small_spec(E=16, k=16, d_model=384, d_ff=384, n_slots=16), 3),       # k = E
     (small_spec(E=1, k=1, d_model=256, d_ff=128, n_slots=1), 5),          # E = 1
     (small_spec(E=4, k=2, d_model=6144, d_ff=256, n_slots=4, fmt="nvfp4", has_shared=True,
-                has_bias=True), 12),                                      # wide K, 2 token groups
+                has_bias=True), 8),                                       # wide K (a 2-stage ring)
     (small_spec(E=300, k=8, d_model=512, d_ff=256, n_slots=300), 16),     # E > 2 x the SM count
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 1),     # the 35B-A3B layer
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 16),
@@ -472,9 +472,8 @@ def test_fill_failure_drops_the_step_misses_and_later_steps_match():
                 L.forward(bf16_tensor(xs[t]), regime=DEC)
             assert e.value.status == capi.MOE_ERR_FILL
             for ex, sl, hit, _ in acc:
-                if not hit and T.slot_of[ex] == sl:
-                    T.expert_of[sl] = -1
-                    T.slot_of[ex] = -1
+                if not hit:
+                    T.drop(ex)
         else:
             y, info = L.forward(bf16_tensor(xs[t]), regime=DEC)
             assert_close_layer(y, ref, "step %d" % t)

@@ -4,10 +4,18 @@ import math
 
 import numpy as np
 import pytest
+
+from conftest import ORACLES, swap_oracle
 import scipy.special
 
 from oracle import formats, layer
 from routed_expert_layer_gemv_gb300 import workloads as wl
+
+
+@pytest.fixture(autouse=True, params=ORACLES)
+def oracle_impl(request, monkeypatch):
+    return swap_oracle(__name__, request, monkeypatch, ("formats", "layer"))
+
 
 
 # ---------------------------------------------------------------- router
@@ -211,3 +219,25 @@ def test_prefill_regime_is_decode_on_quantised_activations(fmt):
     # quantised x differs from x, but not by more than the FP4 grid allows
     assert not np.array_equal(xq, x)
     assert np.abs(xq - x).max() <= np.abs(x).max() / 3
+
+
+def test_native_and_numpy_oracles_agree():
+    # the two implementations of the oracle, on layers with every option:
+    # ids, permutation and quantiser codes exactly, values to FP64 rounding
+    from oracle import layer as np_layer
+    from oracle.native import layer as cpp_layer
+    for fmt, shared, bias in (("mxfp4", False, False), ("nvfp4", True, True)):
+        spec = wl.LayerSpec(E=12, k=3, d_model=128, d_ff=64, n_slots=12, fmt=fmt, has_shared=shared,
+                            has_bias=bias)
+        W_r, b = wl.router_weights(spec, 8)
+        ex = {e: wl.expert_weights(spec, 8, e) for e in range(spec.E)}
+        sh = wl.expert_weights(spec, 8, 0, shared=True) if shared else None
+        x = wl.bf16_bits_to_f64(wl.iid_tokens(8, 17, spec.d_model)[0])
+        for regime in ("decode", "prefill"):
+            y1, i1, g1 = cpp_layer.Layer(spec, lambda e: ex[e], W_r, b, sh).forward(x, regime)
+            y2, i2, g2 = np_layer.Layer(spec, lambda e: ex[e], W_r, b, sh).forward(x, regime)
+            assert np.array_equal(i1, i2)
+            assert np.allclose(g1, g2, rtol=1e-14, atol=0)
+            assert np.allclose(y1, y2, rtol=1e-12, atol=1e-12 * np.abs(y2).max())
+            for a, c in zip(cpp_layer.permute(i1, spec.E), np_layer.permute(i2, spec.E)):
+                assert np.array_equal(a, c)

@@ -3,7 +3,15 @@ simulation (no GPU)."""
 import numpy as np
 import pytest
 
+from conftest import ORACLES, swap_oracle
+
 from oracle.lru import SlotTable
+
+
+@pytest.fixture(autouse=True, params=ORACLES)
+def oracle_impl(request, monkeypatch):
+    return swap_oracle(__name__, request, monkeypatch, ("SlotTable",))
+
 
 
 class NaiveLRU:

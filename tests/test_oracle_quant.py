@@ -6,8 +6,14 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import read_golden
+from conftest import ORACLES, read_golden, swap_oracle
 from oracle import formats, quant
+
+
+@pytest.fixture(autouse=True, params=ORACLES)
+def oracle_impl(request, monkeypatch):
+    return swap_oracle(__name__, request, monkeypatch, ("formats", "quant"))
+
 
 
 def test_e2m1_roundtrip_all_codes():

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 from helpers import need_gpu, small_spec
-from oracle import layer as olayer
+from oracle.native import layer as olayer
 from routed_expert_layer_gemv_gb300 import capi
 from routed_expert_layer_gemv_gb300.layer import MoELayer
 
