@@ -1,32 +1,44 @@
 #!/usr/bin/env python3
 """Benchmark of one routed MoE layer's forward pass on GB300.
 
-Workload (default): the decode layer of a Qwen3-35B-A3B-shaped model --
-d_model 2048, 128 experts, top-8, d_ff 768, MXFP4 weights, 47 cache slots
-(37% of the experts) filled from pinned host memory -- run at 1, 4 and 16
-tokens per step on AR(1) hidden states (rho 0.9).  A step is one moe_forward:
-router, permutation, LRU update, miss fills, expert FFN, combine.  Misses are
-filled the library's default way (at batch 1 and 4 the expert GEMV reads them
-from host memory itself, at batch 16 a copy kernel on 12 reserved SMs does);
-the other fill modes are timed beside it per batch, and so is an all-resident
-warm run (n_slots = E, every expert installed: no fills, HBM bytes only).
+Default workload (the headline line): the decode layer of a Qwen3-35B-A3B-
+shaped model -- d_model 2048, 128 experts, top-8, d_ff 768, MXFP4 weights, 47
+cache slots (37% of the experts) filled from pinned host memory -- at 1, 4
+and 16 tokens per step on AR(1) hidden states (rho 0.9).  A step is one
+moe_forward: router, permutation, LRU update, miss fills, expert FFN,
+combine, in the library's default modes (a decode step of <= 16 tokens whose
+misses the expert FFN itself can fill runs as one fused launch; batch 16,
+whose distinct experts outnumber the slots, fills with a copy kernel on 12
+reserved SMs and runs the chain of launches).
+
+Beside it, in the same JSON line:
+  * per batch: miss rate of the timed steps and of the whole 512-step trace,
+    e2e, kernel times, every fill mode, and an all-resident run (n_slots = E,
+    no fills: HBM bytes only) -- the roofline entry is the fused decode step
+    kernel on those all-resident steps;
+  * decode_284b_a13b: the DeepSeek-V4-Flash-shaped decode layer (d 4096, 256
+    experts, top-8 + shared, d_ff 2048, 28 slots) at batch 1 and 8, the same
+    figures;
+  * prefill_35b_a3b_n8192 and prefill_753b_n16384: the two prefill chunks
+    (tokens/s, grouped-GEMM TFLOP/s against the dense FP4 peak);
+  * cpu_baseline: the C++ FP64 oracle on the host cores (and one thread).
 
 Timing: W warm-up steps, then K timed steps per batch size, each bracketed by
 CUDA events on the launching stream; the L2 is flushed (a 512 MiB write)
 between timed steps, outside the events.  `value` = tokens / summed step time
 over the three batch sizes, inputs resident in HBM.  `e2e` repeats the run
 through the C ABI with pinned host x / y buffers (copies inside the timed
-call, host wall clock).  The roofline entry is the expert FFN phase-1 kernel
-(gate/up GEMV), timed with the library's per-launch CUDA events in a second
-pass over the same steps (the events cost host time per launch, so the pass
-behind `value` runs without them).
+call, host wall clock).  Kernel times come from a second, instrumented pass
+(the library's per-launch events cost host time, so the pass behind `value`
+runs without them).
 
---impl reference times the CPU oracle (FP64, numpy) on a bounded sample of the
-same workload on the host cores.
+--impl reference times the CPU oracle (C++, FP64, OpenMP) on a bounded sample
+of the same workload on the host cores.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -42,37 +54,36 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (decode, prefill); % of HBM BW / % of dense FP4 tensor peak"
 FALLBACK_HBM_GBS = 6800.0
-
-
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_PER_BF16 = 6.0        # nominal dense ratio: 13.5 PF/s FP4 vs 2.25 PF/s bf16
 
 
-def _peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _measured():
     try:
-        with open(p) as fh:
-            d = json.load(fh)
-        return float(d["hbm_gbs"]), "measured"
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return None
+
+
+def _peaks():
+    d = _measured()
+    if d and "hbm_gbs" in d:
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
 
 
 def _fp4_peak():
     """Dense FP4 TF/s: measured bf16 GEMM burst x the nominal FP4/bf16 ratio."""
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(p) as fh:
-            return float(json.load(fh)["bf16_tflops"]) * FP4_PER_BF16, "measured bf16 x 6"
-    except Exception:
-        return FALLBACK_BF16_TFLOPS * FP4_PER_BF16, "fallback bf16 x 6"
+    d = _measured()
+    if d and "bf16_tflops" in d:
+        return float(d["bf16_tflops"]) * FP4_PER_BF16, "measured bf16 x 6"
+    return FALLBACK_BF16_TFLOPS * FP4_PER_BF16, "fallback bf16 x 6"
 
 
 def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
 
 
 # ---------------------------------------------------------------- clocks
@@ -128,26 +139,21 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-# ---------------------------------------------------------------- workload
+# ---------------------------------------------------------------- helpers
 
-def decode_tokens(wl, spec, seed, batch, steps):
-    x, _ = wl.ar1_tokens(seed, batch, steps, spec.d_model, 0.9)
-    return x
-
-
-def gateup_bytes(spec, layout, n_experts, n_tokens):
-    """Algorithmic bytes of phase 1 for one step: the gate and up codes and
-    scales of each expert read once, x read, W_g x and W_u x written (fp32)."""
-    d, f = spec.d_model, spec.d_ff
-    w = 2 * (f * d // 2 + f * d // spec.block)
-    rows = n_tokens * spec.k + (n_tokens if spec.has_shared else 0)
-    return n_experts * w + n_tokens * d * 2 + rows * 2 * f * 4
+def step_bytes(spec, n_distinct, n_tokens):
+    """Algorithmic HBM bytes of one decode step: each distinct routed expert's
+    weights once (B_e = 3 d f (1/2 + 1/B) + tensor scales), the shared
+    expert's, W_r in fp32 (4 E d) and x in / y out (2 N d each)."""
+    d, f, E = spec.d_model, spec.d_ff, spec.E
+    b_e = 3 * d * f * (1 / 2 + 1 / spec.block)
+    return (n_distinct + (1 if spec.has_shared else 0)) * b_e + 4 * E * d + 4 * n_tokens * d
 
 
 def traffic_ratio(kernel, workload):
     """DRAM bytes / algorithmic bytes of a launch, from the ncu capture listed
     in profiles/traffic.txt (None when the kernel has no current capture)."""
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.txt")
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         for line in open(path):
             f = line.split()
@@ -158,154 +164,138 @@ def traffic_ratio(kernel, workload):
     return None
 
 
-def run_decode(args, batch, torch, capi, wl, build_layer, flush, st, profile, fill=None):
-    """K timed decode steps after W warm-up steps on a fresh layer (cold cache).
-    profile=False: the clean pass behind `value`; profile=True: the same steps
-    with the library's per-launch events on (kernel times for the roofline)."""
-    spec = wl.DECODE_35B.layer
-    seed = wl.DECODE_35B.seed
-    W, K = args.warmup, args.steps
-    x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
-    xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
-    L = build_layer(spec, seed, batch)
+class Ctx:
+    """What every run needs: torch, the binding, the generator, a flush
+    buffer, the stream, and one packed host pool per workload."""
+
+    def __init__(self, args):
+        import torch
+        from routed_expert_layer_gemv_gb300 import capi
+        from routed_expert_layer_gemv_gb300 import workloads as wl
+        from routed_expert_layer_gemv_gb300.layer import build_layer, make_desc, pack_pool
+        self.torch, self.capi, self.wl, self.args = torch, capi, wl, args
+        self.build_layer, self.make_desc, self.pack_pool = build_layer, make_desc, pack_pool
+        capi.lib()
+        self.flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+        self.st = torch.cuda.Stream()
+        self.pools = {}
+
+    def layer(self, work, max_tokens, n_slots=None, install_all=False):
+        spec = work.layer if n_slots is None else dataclasses.replace(work.layer, n_slots=n_slots)
+        key = work.name
+        if key not in self.pools:
+            lay = self.capi.moe_expert_layout_for(self.make_desc(spec, max_tokens))
+            self.pools[key] = self.pack_pool(lay, spec.E, lambda e: self.wl.expert_weights(spec, work.seed, e))
+        return self.build_layer(spec, work.seed, max_tokens, install_all=install_all, pool=self.pools[key]), spec
+
+    def tokens(self, work, batch, steps, device="cuda"):
+        x, _ = self.wl.ar1_tokens(work.seed + batch, batch, steps, work.layer.d_model, work.rho)
+        t = self.torch.from_numpy(x.view(np.int16)).view(self.torch.bfloat16)
+        return t.cuda() if device == "cuda" else t
+
+
+def run_decode(c, work, batch, profile=False, fill=None, resident=None):
+    """K timed decode steps after W warm-up steps on a fresh layer (cold
+    cache), or on `resident` = (layer, spec), a layer that holds every
+    expert.  profile: the library's per-launch events on (kernel times)."""
+    torch, capi = c.torch, c.capi
+    W, K = c.args.warmup, c.args.steps
+    xs = c.tokens(work, batch, W + K)
+    L, spec = resident or c.layer(work, batch)
     if fill is not None:
         capi.moe_set_fill_mode(L.h, fill)
     y = torch.empty(batch, spec.d_model, dtype=torch.bfloat16, device="cuda")
-    with torch.cuda.stream(st):
+    with torch.cuda.stream(c.st):
         for t in range(W):
-            L.forward(xs[t], y, stream=st)
+            L.forward(xs[t], y, stream=c.st)
     torch.cuda.synchronize()
-    stats0 = capi.moe_stats(L.h)
-    torch.cuda.synchronize()
+    s0 = capi.moe_stats(L.h)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     capi.moe_profile(L.h, profile)
-    launches = 0
-    fill_b = 0
-    ffn_bytes = 0
-    with torch.cuda.stream(st):
+    launches = fused = 0
+    with torch.cuda.stream(c.st):
         for t in range(K):
-            flush.zero_()
-            ev[t][0].record(st)
-            _, info = L.forward(xs[W + t], y, stream=st)
-            ev[t][1].record(st)
+            c.flush.zero_()
+            ev[t][0].record(c.st)
+            _, info = L.forward(xs[W + t], y, stream=c.st)
+            ev[t][1].record(c.st)
             launches += info.n_launches
-            fill_b += info.fill_bytes
-            ffn_bytes += gateup_bytes(spec, L.layout, info.n_distinct, batch)
+            fused += info.fused_step
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms)
     prof = capi.moe_profile_read(L.h)
     capi.moe_profile(L.h, False)
-    stats1 = capi.moe_stats(L.h)
-    L.close()
-    d_misses, d_distinct = stats1[3] - stats0[3], stats1[1] - stats0[1]
-    return dict(batch=batch, steps=K, ms=ms, step_ms_p50=statistics.median(step_ms), tokens=K * batch,
-                launches=launches,
-                misses=d_misses, distinct=d_distinct, fill_bytes=fill_b, prof=prof,
-                gateup_bytes=ffn_bytes)
+    s1 = capi.moe_stats(L.h)
+    if resident is None:
+        L.close()
+    distinct, misses = s1[1] - s0[1], s1[3] - s0[3]
+    return dict(batch=batch, steps=K, ms=sum(step_ms), p50=statistics.median(step_ms), tokens=K * batch,
+                launches=launches, fused_steps=fused, distinct=distinct, misses=misses, prof=prof,
+                bytes=K * step_bytes(spec, 0, batch) + distinct * 3 * spec.d_model * spec.d_ff *
+                (1 / 2 + 1 / spec.block))
 
 
-def run_decode_resident(args, batch, torch, capi, wl, build_layer, flush, st):
-    """The same decode steps with every expert resident (n_slots = E, expert e
-    installed in slot e): no misses and no fills, so a step moves only HBM
-    bytes.  Returns the step time and the step's algorithmic bytes: the
-    distinct experts' weights (B_e = 3 d f (1/2 + 1/32) each), W_r in fp32
-    (4 E d) and x in / y out (4 N d)."""
-    import dataclasses
-    spec = dataclasses.replace(wl.DECODE_35B.layer, n_slots=wl.DECODE_35B.layer.E)
-    seed = wl.DECODE_35B.seed
-    W, K = args.warmup, args.steps
-    x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
-    xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
-    L = build_layer(spec, seed, batch, install_all=True)
+def trace_miss_rate(c, work, batch):
+    """Miss rate over the workload's whole trace (its configured number of
+    steps from a cold cache), untimed."""
+    torch, capi = c.torch, c.capi
+    xs = c.tokens(work, batch, work.steps)
+    L, spec = c.layer(work, batch)
     y = torch.empty(batch, spec.d_model, dtype=torch.bfloat16, device="cuda")
-    with torch.cuda.stream(st):
-        for t in range(W):
-            L.forward(xs[t], y, stream=st)
+    for t in range(work.steps):
+        L.forward(xs[t], y)
     torch.cuda.synchronize()
-    stats0 = capi.moe_stats(L.h)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    with torch.cuda.stream(st):
-        for t in range(K):
-            flush.zero_()
-            ev[t][0].record(st)
-            L.forward(xs[W + t], y, stream=st)
-            ev[t][1].record(st)
-    torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev)
-    stats1 = capi.moe_stats(L.h)
+    s = capi.moe_stats(L.h)
     L.close()
-    d, f, E = spec.d_model, spec.d_ff, spec.E
-    b_e = 3 * d * f * (1 / 2 + 1 / spec.block)
-    nbytes = (stats1[1] - stats0[1]) * b_e + K * (4 * E * d + 4 * batch * d)
-    return dict(batch=batch, steps=K, ms=ms, tokens=K * batch, bytes=nbytes,
-                misses=stats1[3] - stats0[3])
+    return s[3] / max(1, s[1]), work.steps
 
 
-def measure_h2d(torch, nbytes=256 << 20):
-    """Host-to-device GB/s of one copy from pinned memory (best of 3): the
-    ceiling the miss fills are held against."""
-    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    best = None
-    for _ in range(4):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        dst.copy_(src, non_blocking=True)
-        b.record()
-        torch.cuda.synchronize()
-        t = a.elapsed_time(b)
-        best = t if best is None else min(best, t)
-    return nbytes / (best / 1000.0) / 1e9
-
-
-def run_decode_e2e(args, batch, torch, capi, wl, build_layer, flush):
-    spec = wl.DECODE_35B.layer
-    seed = wl.DECODE_35B.seed
-    W, K = args.warmup, args.steps
-    x_host = decode_tokens(wl, spec, seed + batch, batch, W + K)
-    xs = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
-    ys = torch.empty(W + K, batch, spec.d_model, dtype=torch.bfloat16).pin_memory()
-    L = build_layer(spec, seed, batch)
+def run_e2e(c, work, batch):
+    torch, capi = c.torch, c.capi
+    W, K = c.args.warmup, c.args.steps
+    xs = c.tokens(work, batch, W + K, device="cpu").pin_memory()
+    ys = torch.empty(W + K, batch, work.layer.d_model, dtype=torch.bfloat16).pin_memory()
+    L, spec = c.layer(work, batch)
     for t in range(W):
         capi.moe_forward(L.h, xs[t], batch, ys[t], None, capi.MOE_REGIME_AUTO)
     torch.cuda.synchronize()
     total = 0.0
     for t in range(K):
-        flush.zero_()
+        c.flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         capi.moe_forward(L.h, xs[W + t], batch, ys[W + t], None, capi.MOE_REGIME_AUTO)
         total += time.perf_counter() - t0
     L.close()
-    return dict(batch=batch, s=total, tokens=K * batch,
-                h2d=K * batch * spec.d_model * 2, d2h=K * batch * spec.d_model * 2)
+    nb = K * batch * spec.d_model * 2
+    return dict(batch=batch, s=total, tokens=K * batch, h2d=nb, d2h=nb)
 
 
-def run_prefill(args, work, torch, capi, wl, build_layer, flush, st):
+def run_prefill(c, work):
     """One prefill chunk per step, every expert resident (slot e = expert e).
     Tokens/s from a pass without per-kernel events, kernel times from a second
     instrumented pass."""
-    spec, N, seed = work.layer, work.n_tokens, work.seed
-    x_host, _ = wl.iid_tokens(seed, N, spec.d_model)
+    torch, capi, wl = c.torch, c.capi, c.wl
+    spec, N = work.layer, work.n_tokens
+    x_host, _ = wl.iid_tokens(work.seed, N, spec.d_model)
     x = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
-    L = build_layer(spec, seed, N, install_all=True)
+    L, _ = c.layer(work, N, n_slots=spec.E, install_all=True)
     y = torch.empty(N, spec.d_model, dtype=torch.bfloat16, device="cuda")
-    W, K = max(3, args.warmup // 4), max(3, args.prefill_steps)
-    with torch.cuda.stream(st):
+    W, K = max(3, c.args.warmup // 4), max(3, c.args.prefill_steps)
+    with torch.cuda.stream(c.st):
         for _ in range(W):
-            L.forward(x, y, stream=st, regime=capi.MOE_REGIME_PREFILL)
+            L.forward(x, y, stream=c.st, regime=capi.MOE_REGIME_PREFILL)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for profile in (False, True):
         capi.moe_profile(L.h, profile)
         launches = 0
-        with torch.cuda.stream(st):
+        with torch.cuda.stream(c.st):
             for t in range(K):
-                flush.zero_()
-                ev[t][0].record(st)
-                _, info = L.forward(x, y, stream=st, regime=capi.MOE_REGIME_PREFILL)
-                ev[t][1].record(st)
+                c.flush.zero_()
+                ev[t][0].record(c.st)
+                _, info = L.forward(x, y, stream=c.st, regime=capi.MOE_REGIME_PREFILL)
+                ev[t][1].record(c.st)
                 launches += info.n_launches
         torch.cuda.synchronize()
         if not profile:
@@ -315,53 +305,104 @@ def run_prefill(args, work, torch, capi, wl, build_layer, flush, st):
     L.close()
     rows = N * spec.k + (N if spec.has_shared else 0)
     d, f = spec.d_model, spec.d_ff
-    flops1, flops2 = 2.0 * rows * d * 2 * f, 2.0 * rows * f * d
-    return dict(workload=work.name, steps=K, ms=ms, tokens=K * N, launches=launches, prof=prof,
-                flops1=flops1 * K, flops2=flops2 * K)
+    return dict(workload=work.name, steps=K, warmup=W, ms=ms, tokens=K * N, launches=launches, prof=prof,
+                flops1=2.0 * rows * d * 2 * f * K, flops2=2.0 * rows * f * d * K)
 
 
 def prefill_summary(r, fp4_peak):
     p = r["prof"]
-    g_ms, g_n = p["gateup"]
-    d_ms, d_n = p["down"]
+    g_ms, d_ms = p["gateup"][0], p["down"][0]
     t1 = r["flops1"] / (g_ms / 1000.0) / 1e12 if g_ms else None
     t2 = r["flops2"] / (d_ms / 1000.0) / 1e12 if d_ms else None
     tboth = (r["flops1"] + r["flops2"]) / ((g_ms + d_ms) / 1000.0) / 1e12 if g_ms + d_ms else None
     return {
         "workload": r["workload"], "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
-        "ms_per_step": r["ms"] / r["steps"],
+        "ms_per_step": r["ms"] / r["steps"], "steps": r["steps"],
         "gemm_tflops": {"gateup": t1, "down": t2, "both": tboth},
         "frac_fp4_peak": (tboth / fp4_peak) if tboth else None,
         "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
     }
 
 
+def decode_workload(c, work, batches, peak, with_modes=True, timed=None):
+    """Everything reported for one decode workload: the timed default pass
+    (`timed`, when already run), kernel times, fill modes, e2e, miss rates and
+    the all-resident pass whose fused step is the roofline kernel."""
+    capi = c.capi
+    runs = timed or [run_decode(c, work, b) for b in batches]
+    pruns = [run_decode(c, work, b, profile=True) for b in batches]
+    modes = {}
+    if with_modes:
+        names = {"memcpy": capi.MOE_FILL_MEMCPY, "device": capi.MOE_FILL_DEVICE, "kernel": capi.MOE_FILL_KERNEL,
+                 "fused": capi.MOE_FILL_FUSED}
+        modes = {n: [run_decode(c, work, b, fill=names[n]) for b in batches]
+                 for n in c.args.fill_modes.split(",") if n in names}
+    e2e = [run_e2e(c, work, b) for b in batches]
+    resident = c.layer(work, max(batches), n_slots=work.layer.E, install_all=True)
+    res = [run_decode(c, work, b, profile=True, resident=resident) for b in batches]
+    resident[0].close()
+    trace = [trace_miss_rate(c, work, b) for b in batches]
+    per = {}
+    for i, b in enumerate(batches):
+        r, pr, e, rr, tr = runs[i], pruns[i], e2e[i], res[i], trace[i]
+        st_ms, st_n = rr["prof"]["step"]
+        per[str(b)] = {
+            "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
+            "e2e_tokens_per_s": e["tokens"] / e["s"],
+            "ms_per_step": r["ms"] / r["steps"],
+            "ms_per_step_median": r["p50"],
+            "miss_rate": r["misses"] / max(1, r["distinct"]),
+            "miss_rate_full_trace": tr[0],
+            "trace_steps": tr[1],
+            "fused_step_share": r["fused_steps"] / r["steps"],
+            "kernel_ms_per_step": {k: v[0] / pr["steps"] for k, v in pr["prof"].items() if v[1]},
+            "tokens_per_s_by_fill_mode": {n: fr[i]["tokens"] / (fr[i]["ms"] / 1000.0) for n, fr in modes.items()},
+            "all_resident": {
+                "tokens_per_s": rr["tokens"] / (rr["ms"] / 1000.0),
+                "ms_per_step": rr["ms"] / rr["steps"],
+                "step_kernel_us": 1000.0 * st_ms / max(1, st_n),
+                "hbm_GB_per_s": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9,
+                "frac_of_measured_hbm": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9 / peak,
+                "kernel_frac_of_measured_hbm":
+                    rr["bytes"] / (st_ms / 1000.0) / 1e9 / peak if st_n == rr["steps"] and st_ms else None,
+                "misses": rr["misses"]},
+        }
+    return dict(runs=runs, e2e=e2e, res=res, per_batch=per)
+
+
 # ---------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_sample(budget_s: float):
-    """Time the oracle on the decode workload (batch 1, 4, 16 in turn) until
-    the budget is spent; returns (tokens/s, tokens, steps, seconds, cores)."""
-    from oracle import layer as olayer
+def cpu_oracle_sample(budget_s: float, threads: int = 0, batches=(1, 4, 16), work_name="decode35b"):
+    """Time the C++ FP64 oracle on decode steps of the workload (each batch
+    size in turn) until the budget is spent; returns (tokens/s, tokens,
+    steps, seconds, threads)."""
+    from oracle import native
+    from oracle.native import layer as olayer
     from routed_expert_layer_gemv_gb300 import workloads as wl
-    spec = wl.DECODE_35B.layer
-    seed = wl.DECODE_35B.seed
-    W_r, b = wl.router_weights(spec, seed)
-    O = olayer.Layer(spec, lambda e: wl.expert_weights(spec, seed, e), W_r, b)
+    work = wl.DECODE_35B if work_name == "decode35b" else wl.TINY
+    spec = work.layer
+    W_r, b = wl.router_weights(spec, work.seed)
+    native.set_threads(threads)
+    used = native.threads()
+    O = olayer.Layer(spec, lambda e: wl.expert_weights(spec, work.seed, e), W_r, b)
     tokens = steps = 0
     t0 = time.perf_counter()
-    per_batch = budget_s / 3.0
-    for batch in (1, 4, 16):
-        xb = decode_tokens(wl, spec, seed + batch, batch, 8)
+    per = budget_s / len(batches)
+    for batch in batches:
+        if work_name == "decode35b":
+            xb, _ = wl.ar1_tokens(work.seed + batch, batch, 8, spec.d_model, work.rho)
+        else:
+            xb = wl.iid_tokens(work.seed, work.n_tokens, spec.d_model)[0][None]
         tb = time.perf_counter()
         t = 0
-        while time.perf_counter() - tb < per_batch and t < len(xb):
+        while time.perf_counter() - tb < per and t < len(xb):
             O.forward(wl.bf16_bits_to_f64(xb[t]), "decode")
-            tokens += batch
+            tokens += xb[t].shape[0]
             steps += 1
             t += 1
     el = time.perf_counter() - t0
-    cores = len(os.sched_getaffinity(0))
-    return tokens / el, tokens, steps, el, cores
+    native.set_threads(0)
+    return tokens / el, tokens, steps, el, used
 
 
 # ---------------------------------------------------------------- main
@@ -369,18 +410,18 @@ def cpu_oracle_sample(budget_s: float):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batches", default="1,4,16")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="decode35b",
-                    choices=["decode35b", "prefill35b", "prefill753b"],
+    ap.add_argument("--workload", default="decode35b", choices=["decode35b", "prefill35b", "prefill753b"],
                     help="decode35b = the headline decode configuration; the prefill ones "
                          "print that prefill chunk's line instead")
     ap.add_argument("--prefill-steps", type=int, default=8)
-    ap.add_argument("--no-prefill", action="store_true", help="skip the secondary prefill result")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 284B-class decode and the two prefill chunks")
     ap.add_argument("--fill-modes", default="memcpy,device,kernel,fused",
                     help="fill modes timed beside the default per batch ('none': skip them)")
     args = ap.parse_args()
@@ -393,12 +434,12 @@ def main():
             return
         v, tok, steps, el, cores = cpu_oracle_sample(args.cpu_budget)
         cfg = {"workload": "decode_35b_a3b_d2048_e128_top8_f768_mxfp4_s47", "batches": batches}
+        sample = "%d decode steps (%d tokens) of batches 1/4/16, %.1f s, C++ FP64 oracle" % (steps, tok, el)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
                 "n_gpus": 0, "steps": steps, "warmup": 0, "ms_per_step": 1000.0 * el / max(1, steps),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": cfg,
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                 "sample": "%d decode steps (%d tokens) of batches 1/4/16, %.1f s" % (steps, tok, el)},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -408,60 +449,47 @@ def main():
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    from routed_expert_layer_gemv_gb300 import capi
-    from routed_expert_layer_gemv_gb300 import workloads as wl
-    from routed_expert_layer_gemv_gb300.layer import build_layer
-    capi.lib()
-
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
-    st = torch.cuda.Stream()
+    c = Ctx(args)
+    wl, capi = c.wl, c.capi
+    peak, peak_kind = _peaks()
+    fp4, fp4_kind = _fp4_peak()
     clocks = ClockSampler(local)
+
     if args.workload != "decode35b":
         work = wl.PREFILL_35B if args.workload == "prefill35b" else wl.PREFILL_753B
         clocks.start()
-        r = run_prefill(args, work, torch, capi, wl, build_layer, flush, st)
+        r = run_prefill(c, work)
         clk = clocks.stop()
-        fp4, fp4_kind = _fp4_peak()
         sm = prefill_summary(r, fp4)
         tboth = sm["gemm_tflops"]["both"]
         line = {"metric": METRIC, "value": sm["tokens_per_s"] * ws, "unit": "tokens/s", "n_gpus": ws,
-                "steps": r["steps"], "warmup": max(3, args.warmup // 4), "ms_per_step": sm["ms_per_step"],
+                "steps": r["steps"], "warmup": r["warmup"], "ms_per_step": sm["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "fp4(e2m1)xfp4(e2m1)->f32", "data": "synthetic (seeded i.i.d. hidden states, random FP4 weights)",
+                "dtype": "fp4(e2m1)xfp4(e2m1)->f32",
+                "data": "synthetic (seeded i.i.d. hidden states, random FP4 weights)",
                 "config": {"workload": work.name, "l2": "flushed (512 MiB write) between timed steps",
                            "detail": sm},
                 "roofline": {"bound": "tensor", "kernel": "prefill grouped GEMM (gate/up + down)",
                              "achieved": tboth, "peak": fp4, "unit": "TFLOP/s",
-                             "frac": (tboth / fp4) if tboth else None, "traffic": None,
-                             "peak_kind": fp4_kind},
+                             "frac": (tboth / fp4) if tboth else None, "traffic": None, "peak_kind": fp4_kind},
                 "gpu_launches": r["launches"], "clocks": clk}
         if rank == 0:
             print(json.dumps(line))
         return
+
+    work = wl.DECODE_35B
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    c.layer(work, 16)[0].close()      # pack the host pool before the timed region
     clocks.start()
-    runs = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False) for b in batches]
+    runs = [run_decode(c, work, b) for b in batches]
     torch.cuda.synchronize()
     clk = clocks.stop()
-    # the instrumented pass fills with the SM copy kernel, so every gate/up
-    # launch reads HBM-resident weights (the fused mode streams misses over
-    # the host link inside the GEMV, which is not an HBM roofline)
-    pruns = [run_decode(args, b, torch, capi, wl, build_layer, flush, st, True, capi.MOE_FILL_KERNEL)
-             for b in batches]
-    modes = {"memcpy": capi.MOE_FILL_MEMCPY, "device": capi.MOE_FILL_DEVICE, "kernel": capi.MOE_FILL_KERNEL,
-             "fused": capi.MOE_FILL_FUSED}
-    modes = {m: modes[m] for m in args.fill_modes.split(",") if m in modes}
-    fruns = {name: [run_decode(args, b, torch, capi, wl, build_layer, flush, st, False, m) for b in batches]
-             for name, m in modes.items()}
-    e2e_runs = [run_decode_e2e(args, b, torch, capi, wl, build_layer, flush) for b in batches]
-    rruns = [run_decode_resident(args, b, torch, capi, wl, build_layer, flush, st) for b in batches]
-    h2d = measure_h2d(torch)
-
     ms = sum(r["ms"] for r in runs)
     tokens = sum(r["tokens"] for r in runs)
-    e2e_s = sum(r["s"] for r in e2e_runs)
+    dec = decode_workload(c, work, batches, peak, timed=runs)
+    e2e_s = sum(r["s"] for r in dec["e2e"])
     if ws > 1:
         t = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -472,79 +500,78 @@ def main():
     value = ws * tokens / (ms / 1000.0)
     e2e_value = ws * tokens / e2e_s
 
-    peak, peak_kind = _peaks()
-    g_ms = sum(r["prof"]["gateup"][0] for r in pruns)
-    g_n = sum(r["prof"]["gateup"][1] for r in pruns)
-    g_bytes = sum(r["gateup_bytes"] for r in pruns)
-    achieved = (g_bytes / max(g_n, 1)) / ((g_ms / max(g_n, 1)) / 1000.0) / 1e9 if g_ms > 0 else None
-    ratio = traffic_ratio("gemv_gateup", "decode35b")
-    roof = {"bound": "hbm", "kernel": "gemv_gateup (expert FFN phase 1)", "achieved": achieved,
-            "peak": peak, "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
-            "traffic": ratio * g_bytes / max(g_n, 1) if ratio else None, "peak_kind": peak_kind,
-            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one captured launch "
-                              "(profiles/gemv_stream_decode35b_b16.md) scaled to this run's bytes per launch"
+    # roofline: the fused decode step kernel on the all-resident steps (one
+    # launch per step, so its per-launch events time exactly the kernel)
+    r_bytes = sum(r["bytes"] for r in dec["res"])
+    r_ms = sum(r["prof"]["step"][0] for r in dec["res"])
+    r_n = sum(r["prof"]["step"][1] for r in dec["res"])
+    achieved = (r_bytes / max(r_n, 1)) / ((r_ms / max(r_n, 1)) / 1000.0) / 1e9 if r_ms > 0 else None
+    ratio = traffic_ratio("step_kernel", "decode35b_resident_b16")
+    roof = {"bound": "hbm", "kernel": "fused decode step (step_kernel), all-resident decode 35B-A3B steps of "
+                                      "batches %s" % "/".join(map(str, batches)),
+            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+            "traffic": ratio * r_bytes / max(r_n, 1) if ratio else None, "peak_kind": peak_kind,
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the fused step kernel, "
+                              "decode 35B-A3B batch 16 all-resident, scaled to this run's bytes per launch"
                               if ratio else None,
-            "bytes_per_launch": g_bytes / max(g_n, 1), "ms_per_launch": g_ms / max(g_n, 1)}
+            "bytes_per_launch": r_bytes / max(r_n, 1), "ms_per_launch": r_ms / max(r_n, 1),
+            "launches": r_n}
 
-    per_batch = {}
-    for i, (r, e, pr, rr) in enumerate(zip(runs, e2e_runs, pruns, rruns)):
-        p = pr["prof"]
-        per_batch[str(r["batch"])] = {
-            "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
-            "e2e_tokens_per_s": e["tokens"] / e["s"],
-            "ms_per_step": r["ms"] / r["steps"],
-            "ms_per_step_median": r["step_ms_p50"],
-            "miss_rate": r["misses"] / max(1, r["distinct"]),
-            "fill_GB_per_s": pr["fill_bytes"] / max(1e-9, p["fill"][0] / 1000.0) / 1e9 if p["fill"][0] else None,
-            "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
-            "tokens_per_s_by_fill_mode": {name: fr[i]["tokens"] / (fr[i]["ms"] / 1000.0)
-                                          for name, fr in fruns.items()},
-            "all_resident": {
-                "tokens_per_s": rr["tokens"] / (rr["ms"] / 1000.0),
-                "ms_per_step": rr["ms"] / rr["steps"],
-                "hbm_GB_per_s": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9,
-                "frac_of_measured_hbm": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9 / peak,
-                "misses": rr["misses"]},
-        }
-    prefill = None
-    if not args.no_prefill:
-        fp4, _ = _fp4_peak()
-        prefill = prefill_summary(run_prefill(args, wl.PREFILL_35B, torch, capi, wl, build_layer,
-                                              flush, st), fp4)
+    extra = {}
+    if not args.no_extra:
+        w3 = wl.DECODE_284B
+        d3 = decode_workload(c, w3, list(w3.batches), peak, with_modes=False)
+        t3 = sum(r["tokens"] for r in d3["runs"])
+        m3 = sum(r["ms"] for r in d3["runs"])
+        extra["decode_284b_a13b"] = {
+            "workload": w3.name, "batches": list(w3.batches), "steps": args.steps,
+            "tokens_per_s": t3 / (m3 / 1000.0),
+            "e2e_tokens_per_s": t3 / sum(r["s"] for r in d3["e2e"]),
+            "miss_rate": sum(r["misses"] for r in d3["runs"]) / max(1, sum(r["distinct"] for r in d3["runs"])),
+            "per_batch": d3["per_batch"]}
+        c.pools.clear()
+        for key, w in (("prefill_35b_a3b_n8192", wl.PREFILL_35B), ("prefill_753b_n16384", wl.PREFILL_753B)):
+            extra[key] = prefill_summary(run_prefill(c, w), fp4)
+            c.pools.clear()
+
     cpu = None
     if not args.no_cpu_baseline:
         v, tok, steps, el, cores = cpu_oracle_sample(args.cpu_budget)
+        v1, tok1, steps1, el1, _ = cpu_oracle_sample(min(10.0, args.cpu_budget / 2), threads=1)
+        v0, tok0, steps0, el0, _ = cpu_oracle_sample(3.0, threads=1, batches=(64,), work_name="tiny")
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": "%d decode steps (%d tokens) of batches 1/4/16, %.1f s" % (steps, tok, el)}
+               "sample": "%d decode steps (%d tokens) of batches 1/4/16 of the decode 35B-A3B layer, %.1f s, "
+                         "C++ FP64 oracle on %d threads" % (steps, tok, el, cores),
+               "one_thread": {"decode_35b_a3b": {"value": v1, "unit": "tokens/s", "steps": steps1},
+                              "tiny_n64": {"value": v0, "unit": "tokens/s", "steps": steps0}}}
+    fused = sum(r["fused_steps"] for r in runs)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps * len(batches), "warmup": args.warmup,
+        "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / (args.steps * len(batches)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)xbf16->f32",
         "data": "synthetic (seeded AR(1) hidden states, random FP4 weights)",
-        "config": {"workload": "decode_35b_a3b_d2048_e128_top8_f768_mxfp4_s47",
-                   "batches": batches, "l2": "flushed (512 MiB write) between timed steps",
-                   "fill": "the library default MOE_FILL_AUTO: misses streamed from host memory by the "
-                           "expert GEMV itself (MOE_FILL_FUSED) at batch 1 and 4, a copy kernel on 12 "
-                           "reserved SMs (MOE_FILL_KERNEL) at batch 16; per_batch times every mode",
-                   "timing": "value from a pass without per-kernel events; kernel times and "
-                             "roofline from a second, instrumented pass of the same steps with "
-                             "MOE_FILL_KERNEL fills",
+        "config": {"workload": work.name, "batches": batches,
+                   "steps_per_batch": args.steps,
+                   "miss_rate_per_batch": {b: dec["per_batch"][b]["miss_rate"] for b in dec["per_batch"]},
+                   "l2": "flushed (512 MiB write) between timed steps",
+                   "path": "library defaults: %d of %d timed steps ran as one fused launch (batch <= 16 with "
+                           "misses filled by the expert FFN itself); batch 16 (distinct experts > slots) fills "
+                           "with a copy kernel on 12 reserved SMs and runs the chain of launches"
+                           % (fused, args.steps * len(batches)),
+                   "timing": "value from a pass without per-kernel events; kernel times and roofline from "
+                             "instrumented passes of the same steps",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
-                   "h2d_GB_per_s_measured": h2d,
-                   "all_resident": "per_batch.all_resident: the same steps with n_slots = E and every "
-                                   "expert installed (no fills); bytes = distinct experts' weights + "
-                                   "W_r (fp32) + x / y per step",
-                   "per_batch": per_batch},
+                   "per_batch": dec["per_batch"]},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s",
-                "h2d_bytes_per_step": sum(e["h2d"] for e in e2e_runs) / (args.steps * len(batches)),
-                "d2h_bytes_per_step": sum(e["d2h"] for e in e2e_runs) / (args.steps * len(batches))},
+                "h2d_bytes_per_step": sum(e["h2d"] for e in dec["e2e"]) / (args.steps * len(batches)),
+                "d2h_bytes_per_step": sum(e["d2h"] for e in dec["e2e"]) / (args.steps * len(batches))},
         "gpu_launches": sum(r["launches"] for r in runs),
         "clocks": clk,
-        "prefill_35b_a3b_n8192": prefill,
     }
+    line.update(extra)
     print(json.dumps(line))
 
 

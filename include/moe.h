@@ -334,6 +334,16 @@ int moe_debug_inject(moe_layer_t layer, int what, long long arg);
  * at the time of the call, for leak checks. */
 int moe_debug_alloc_fault(long long nth, long long* live_out);
 
+/* Timeline of the last fused decode step run while kernel timing
+ * (moe_profile) was on: per CTA, kStepMarks = 9 global-timer stamps (ns) --
+ * kernel start, logits written, grid barrier 1 passed, access table built,
+ * phase-1 (gate/up) outputs written, barrier 2 passed, phase-2 (down)
+ * outputs written, barrier 3 passed, combine done (marks a CTA does not
+ * reach stay from an earlier step).  out: host array of at least
+ * n_cta * n_marks entries, CTA-major; *n_cta, *n_marks (may be NULL) get the
+ * sizes.  MOE_ERR_STATE if no such step ran. */
+int moe_debug_step_trace(moe_layer_t layer, uint64_t* out, int cap, int* n_cta, int* n_marks);
+
 /* Dequantised fp32 weights of matrix m (0 gate, 1 up, 2 down) of the expert
  * in slot `slot` (slot -1: the shared expert), written row-major to out. */
 int moe_debug_dequant(moe_layer_t layer, int slot, int m, float* out, void* stream);

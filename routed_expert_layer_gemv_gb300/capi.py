@@ -99,6 +99,7 @@ _SIGS = {
     "moe_debug_last_hidden": ([_P, _P, _P, _P, _P], _I),
     "moe_debug_inject": ([_P, _I, C.c_longlong], _I),
     "moe_debug_alloc_fault": ([C.c_longlong, _P], _I),
+    "moe_debug_step_trace": ([_P, _P, _I, _P, _P], _I),
     "moe_debug_dequant": ([_P, _I, _I, _P, _P], _I),
     "moe_debug_actquant": ([_P, _P, _I, _I, _P, _P, _I, _P], _I),
     "moe_permute_noalloc": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, C.c_char_p, C.c_size_t], _I),
@@ -293,6 +294,16 @@ def moe_debug_alloc_fault(nth: int):
     live = (C.c_longlong * 2)()
     check(lib().moe_debug_alloc_fault(nth, live))
     return live[0], live[1]
+
+
+def moe_debug_step_trace(h):
+    """Per-CTA global-timer marks (ns) of the last fused step run under
+    moe_profile, as a list of rows (one per CTA)."""
+    G, M = C.c_int(0), C.c_int(0)
+    lib().moe_debug_step_trace(h, None, 0, C.byref(G), C.byref(M))
+    buf = (C.c_uint64 * max(1, G.value * M.value))()
+    check(lib().moe_debug_step_trace(h, buf, G.value * M.value, None, None), h)
+    return [list(buf[c * M.value:(c + 1) * M.value]) for c in range(G.value)]
 
 
 def moe_debug_dequant(h, slot: int, m: int, out, stream=None) -> None:

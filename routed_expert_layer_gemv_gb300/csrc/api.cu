@@ -135,9 +135,11 @@ struct moe_layer {
   // fused decode step
   int decode_path = MOE_DECODE_AUTO;
   bool step_failed = false;            // a cooperative launch was refused once: use the chain
-  unsigned long long* gbar = nullptr;  // grid-barrier arrival counter (device)
+  unsigned long long* gbar = nullptr;  // arrival counters of the fused step's three grid barriers (device)
   unsigned long long gbar_base = 0;    // its value before the next fused step
   unsigned long long* ready = nullptr; // publication word of a fused step's miss buffers (device)
+  unsigned long long* step_trace = nullptr;   // per-CTA timeline of the last fused step (device, under moe_profile)
+  int step_trace_grid = 0;
   unsigned long long ready_seq = 0;
   bool inject_fill = false;            // test hook: the next host-issued fill fails before its copy
   long long inject_wait = 0;           // test hook: wait limit (cycles) of the next forward's expert FFN
@@ -458,8 +460,9 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   L->list_cap = (int)std::max<size_t>(Nm * g.k, (size_t)g.E);
   MOE_ALLOC(list_dev, (size_t)L->list_cap * 4);
   MOE_ALLOC(rcounter, 16);
-  MOE_ALLOC(gbar, 8);
+  MOE_ALLOC(gbar, 24);
   MOE_ALLOC(ready, 8);
+  MOE_ALLOC(step_trace, (size_t)std::max(L->num_sms, 1) * kStepMarks * 8);
   MOE_ALLOC(stats, 64);
   const bool prefill_ok = prefill_shape_ok(g);
   const size_t prows = Nm * g.k + Nm + 128;   // permuted rows (+ shared) + one tile of padding
@@ -529,7 +532,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
               cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
               cudaMemset(L->rec, 0, rec_dev_bytes(g.E)) == cudaSuccess &&
               cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
-              cudaMemset(L->gbar, 0, 8) == cudaSuccess &&
+              cudaMemset(L->gbar, 0, 24) == cudaSuccess &&
               cudaMemset(L->ready, 0, 8) == cudaSuccess &&
               cudaMemset(L->stats, 0, 64) == cudaSuccess;
     // slot s in buffer s; the spares after the shared expert's buffer S
@@ -778,7 +781,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     // a fused step that gave up may have left its barrier counter short:
     // start it again from zero, after every launch already queued
     cudaStream_t st0 = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(L->gbar, 0, 8, st0) != cudaSuccess) cudaGetLastError();
+    if (cudaMemsetAsync(L->gbar, 0, 24, st0) != cudaSuccess) cudaGetLastError();
     L->gbar_base = 0;
     return fail(L, MOE_ERR_TIMEOUT, "a wait inside an earlier step's kernel timed out; its output is invalid");
   }
@@ -864,11 +867,13 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
       sa.h = L->h;
       sa.O = L->O;
       sa.y = yd;
+      sa.trace = L->prof_on ? L->step_trace : nullptr;
+      if (sa.trace) L->step_trace_grid = L->num_sms;
       cudaEvent_t* ps = prof_begin(L, MOE_PROF_STEP, st);
       const cudaError_t ce = launch_step(g, L->gplan, a, sa, plan, L->num_sms, st);
       prof_end(ps, st);
       if (ce == cudaSuccess) {
-        L->gbar_base += 3ull * (unsigned long long)L->num_sms;
+        L->gbar_base += (unsigned long long)L->num_sms;
         L->launches += 1;
         if (!y_dev) {
           if (!y_direct) MOE_CUDA(L, cudaMemcpyAsync(y, yd, xbytes, cudaMemcpyDeviceToHost, st));
@@ -1298,6 +1303,18 @@ int moe_debug_last_hidden(moe_layer_t L, float* h, uint8_t* hq_codes, uint8_t* h
   if (hq_codes) MOE_CUDA(L, cudaMemcpyAsync(hq_codes, L->hq_codes, rows * g.f / 2, cudaMemcpyDeviceToDevice, st));
   if (hq_scales)
     MOE_CUDA(L, cudaMemcpyAsync(hq_scales, L->hq_scales, rows * (g.f / g.blk), cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
+int moe_debug_step_trace(moe_layer_t L, uint64_t* out, int cap, int* n_cta, int* n_marks) {
+  if (!L) return MOE_ERR_ARG;
+  const int G = L->step_trace_grid;
+  if (n_cta) *n_cta = G;
+  if (n_marks) *n_marks = kStepMarks;
+  if (G == 0) return fail(L, MOE_ERR_STATE, "no fused step ran while kernel timing was on");
+  if (!out || cap < G * kStepMarks) return fail(L, MOE_ERR_ARG, "out must hold %d entries", G * kStepMarks);
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  MOE_CUDA(L, cudaMemcpy(out, L->step_trace, (size_t)G * kStepMarks * 8, cudaMemcpyDeviceToHost));
   return MOE_OK;
 }
 

@@ -358,15 +358,9 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const int s = it % kWsStages;
         const uint32_t k = it / kWsStages;
-        if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) continue;
         if (s_abort) continue;
-        if (kt + 4 < nkt) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            prefetch_l1(pa[j] + (kt + 4) * SB);
-            prefetch_l1(pb[j] + (kt + 4) * SB);
-          }
-        }
+        // the stage's scale loads go out before the wait for its TMEM slot,
+        // so their latency overlaps the MMAs still reading the slot
         uint32_t wa[4][G], wv[4][G];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -383,6 +377,14 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             for (int g = 0; g < G; ++g) { wa[j][g] = ta4[g & 3]; wv[j][g] = tb4[g & 3]; }
           }
         }
+        if (kt + 4 < nkt) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            prefetch_l1(pa[j] + (kt + 4) * SB);
+            prefetch_l1(pb[j] + (kt + 4) * SB);
+          }
+        }
+        if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) continue;
         const uint32_t col = tb + lq + kSfBase + (uint32_t)(s * SFC);
 #pragma unroll
         for (int g = 0; g < G; ++g) {

@@ -34,10 +34,12 @@
 // need nothing from CTA 0.  The routing, the GEMV arithmetic and the combine
 // are the chained path's own, so both paths give bit-identical outputs.
 //
-// Grid barriers: one 64-bit arrival counter per layer that only grows; the
-// host passes the count the launch starts from, each barrier adds G, and
-// every CTA arrives at every barrier exactly once, even after a timeout, so
-// the count stays aligned with the host's.  Every wait is bounded (~2 s); a
+// Grid barriers: one 64-bit arrival counter per barrier that only grows; the
+// host passes the count the launch starts from, each launch adds G to each,
+// and every CTA arrives at every barrier exactly once, even after a timeout,
+// so the counts stay aligned with the host's.  CTA 0 computes no expert rows,
+// so it arrives at barriers 2 and 3 before its LRU step: the table update is
+// never on the path of a step whose experts all hit.  Every wait is bounded (~2 s); a
 // timeout sets the layer's error word and the CTA skips the rest of its work.
 #include "gemv_dev.cuh"
 #include "lru_dev.cuh"
@@ -91,6 +93,12 @@ MOE_DEV bool wait_word(const unsigned long long* w, unsigned long long seq, vola
 
 // Grid barrier: arrive (one thread per CTA), then wait until all G CTAs of
 // this barrier have arrived (count >= target).  Bounded.
+MOE_DEV unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
 MOE_DEV void gbar_arrive(unsigned long long* cnt) {
   __threadfence();
   atomicAdd(cnt, 1ull);
@@ -132,6 +140,8 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
   const int cta = blockIdx.x, G = gridDim.x;
   const int N = a.N, E = g.E, k = g.k, d = g.d;
   const long long wl = a.wait_cycles > 0 ? a.wait_cycles : tc::kWaitCycles;
+  unsigned long long* mark = s.trace ? s.trace + (size_t)cta * kStepMarks : nullptr;
+  if (mark && tid == 0) mark[0] = gtimer();
   if (tid == 0) {
     for (int i = 0; i < p1.D; ++i) {
       tc::mbar_init(&S.full[i], 1);
@@ -206,9 +216,12 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     if (ALL) stage_all<FMT>(p1, N, s.x, reinterpret_cast<uint2*>(S.base + p1.off_x), &sm.sexp[0][0], t4, 128, 3);
   }
   __syncthreads();
+  const unsigned long long target = s.gbar_base + (unsigned long long)G;   // of each barrier
   if (tid == 0) {
-    gbar_arrive(s.gbar);
-    gbar_wait(s.gbar, s.gbar_base + (unsigned long long)G, &sm.abort, a.err);
+    if (mark) mark[1] = gtimer();
+    gbar_arrive(s.gbar + 0);
+    gbar_wait(s.gbar + 0, target, &sm.abort, a.err);
+    if (mark) mark[2] = gtimer();
   }
   __syncthreads();
   const bool routed = !sm.abort;
@@ -268,7 +281,9 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     }
   }
   __syncthreads();
-  if (cta == 0 && routed) {
+  if (mark && tid == 0) mark[3] = gtimer();
+  const bool lru_cta = cta == 0 && routed;   // arrives at barriers 2 and 3 below, before the LRU step
+  if (lru_cta) {
     // the layer's copy of the routing (what moe_debug_last_step returns)
     for (int q = tid; q < N * k; q += kThreads) {
       s.idx[q] = C.idx[q];
@@ -280,7 +295,12 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
       s.counts[e] = C.counts[e];
       s.offsets[e] = C.offs[e];
     }
-    if (tid == 0) s.offsets[E] = C.offs[E];
+    if (tid == 0) {
+      s.offsets[E] = C.offs[E];
+      // no expert rows here: barriers 2 and 3 need nothing more from this CTA
+      gbar_arrive(s.gbar + 1);
+      gbar_arrive(s.gbar + 2);
+    }
     // the LRU step (its shared state in the ring area, after the top-k rows)
     lru::LruSmem& m = *reinterpret_cast<lru::LruSmem*>(S.base);
     lru::lru_park(lr, E, g.S, g.X, m);
@@ -353,16 +373,24 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     // this CTA's h rows are written: barrier 2, then phase 2 stages h of any CTA
     epi_sync();
     if (warp == kCW + 1 && lane == 0) {
-      gbar_arrive(s.gbar);
-      gbar_wait(s.gbar, s.gbar_base + 2ull * G, &sm.abort, a.err);
+      if (mark) mark[4] = gtimer();
+      if (!lru_cta) gbar_arrive(s.gbar + 1);
+      gbar_wait(s.gbar + 1, target, &sm.abort, a.err);
+      if (mark) mark[5] = gtimer();
     }
     epi_sync();
     reduce<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, false, s.x, C.xexp, s.h, s.O, wl);
     epi_sync();
-    if (warp == kCW + 1 && lane == 0) gbar_arrive(s.gbar);
+    if (warp == kCW + 1 && lane == 0) {
+      if (mark) mark[6] = gtimer();
+      if (!lru_cta) gbar_arrive(s.gbar + 2);
+    }
   }
   __syncthreads();
-  if (tid == 0) gbar_wait(s.gbar, s.gbar_base + 3ull * G, &sm.abort, a.err);
+  if (tid == 0) {
+    gbar_wait(s.gbar + 2, target, &sm.abort, a.err);
+    if (mark) mark[7] = gtimer();
+  }
   __syncthreads();
 
   // ---------------------------------------------------------------- combine
@@ -395,6 +423,10 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
       reinterpret_cast<uint2*>(s.y + (size_t)t * d)[cv] =
           make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
     }
+  }
+  if (mark) {
+    __syncthreads();
+    if (tid == 0) mark[8] = gtimer();
   }
 }
 

@@ -25,13 +25,19 @@ struct StepArgs {
   unsigned long long* stats;
   unsigned long long* ready;   // publication word of the misses' buffers
   unsigned long long seq;      // this step's value of it
-  unsigned long long* gbar;    // grid-barrier arrival counter
-  unsigned long long gbar_base;   // its value when the launch starts (the launch adds 3 G)
+  unsigned long long* gbar;    // the three grid barriers' arrival counters
+  unsigned long long gbar_base;   // their value when the launch starts (the launch adds G to each)
   float* h;                    // [rows, 2 d_ff] phase-1 outputs
   float* O;                    // [rows, d] phase-2 outputs
   __nv_bfloat16* y;            // [N, d] (device or mapped pinned host memory)
+  unsigned long long* trace;   // [G][kStepMarks] global-timer stamps per CTA, or null
   int ctl_off;                 // set by launch_step
 };
+
+// Marks of the per-CTA timeline (moe_debug_step_trace): kernel start, logits
+// written, barrier 1 passed, access table built, phase-1 outputs written,
+// barrier 2 passed, phase-2 outputs written, barrier 3 passed, done.
+constexpr int kStepMarks = 9;
 
 struct StepPlan {
   gv::SG p1, p2;   // the two phases' geometry, sharing one ring layout
@@ -44,7 +50,7 @@ bool step_plan(const Geo& g, int N, StepPlan* out);
 
 // One fused step on `grid` CTAs (the SM count: one per SM, all resident).
 // a: the expert-FFN arguments (slots, N, err, hmax, host pool for fused
-// fills, wait limit); the launch adds 3 * grid to the barrier counter.
+// fills, wait limit); the launch adds `grid` to each barrier counter.
 cudaError_t launch_step(const Geo& g, const GemvPlan* pl, const GemvArgs& a, StepArgs s, const StepPlan& P,
                         int grid, cudaStream_t st);
 

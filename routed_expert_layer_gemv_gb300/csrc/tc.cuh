@@ -45,13 +45,29 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t phase) {
   return ok != 0;
 }
 
+// Non-blocking test of the barrier's phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(su32(bar)), "r"(phase) : "memory");
+  return ok != 0;
+}
+
 // Default limit of a bounded wait: ~2 s of SM clock.
 constexpr long long kWaitCycles = 4000000000LL;
 
 // Wait for `phase` of the barrier, at most `limit` SM clock cycles; false on
-// timeout.
+// timeout.  try_wait may suspend the thread inside the instruction until the
+// phase completes, so a short limit (a test's) polls with test_wait, which
+// returns at once.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, long long limit = kWaitCycles) {
   const long long t0 = clock64();
+  if (limit < 1000000) {
+    while (!mbar_test(bar, phase))
+      if (clock64() - t0 > limit) return false;
+    return true;
+  }
   while (!mbar_try(bar, phase))
     if (clock64() - t0 > limit) return false;
   return true;

@@ -40,6 +40,16 @@ def pack_expert(layout: capi.moe_expert_layout, w: Dict[str, Matrix], out: np.nd
     out[t0:t0 + 12] = ts.view(np.uint8)
 
 
+def pack_pool(layout: capi.moe_expert_layout, E: int, experts_fn) -> torch.Tensor:
+    """All E experts packed back to back in pinned host memory."""
+    nb = layout.bytes
+    pool = torch.empty(E * nb, dtype=torch.uint8, pin_memory=True)
+    view = pool.numpy()
+    for e in range(E):
+        pack_expert(layout, experts_fn(e), view[e * nb:(e + 1) * nb])
+    return pool
+
+
 class MoELayer:
     """One layer on the current CUDA device, driven through the C ABI."""
 
@@ -71,13 +81,14 @@ class MoELayer:
         b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
         capi.moe_set_router(self.h, W.ctypes.data, None if b is None else b.ctypes.data)
 
-    def load_host_pool(self, experts_fn: Callable[[int], Dict[str, Matrix]]) -> None:
-        """Pack all E experts into a pinned pool and register it."""
+    def load_host_pool(self, experts_fn: Callable[[int], Dict[str, Matrix]], pool=None) -> None:
+        """Pack all E experts into a pinned pool and register it (or register
+        ``pool``, a pool packed before for the same layout: several layers
+        may share one host pool)."""
         nb = self.layout.bytes
-        self.pool = torch.empty(self.spec.E * nb, dtype=torch.uint8, pin_memory=True)
-        view = self.pool.numpy()
-        for e in range(self.spec.E):
-            pack_expert(self.layout, experts_fn(e), view[e * nb:(e + 1) * nb])
+        if pool is None:
+            pool = pack_pool(self.layout, self.spec.E, experts_fn)
+        self.pool = pool
         capi.moe_register_host_experts(self.h, self.pool.data_ptr(), self.pool.numel())
 
     def set_shared(self, w: Dict[str, Matrix]) -> None:
@@ -103,14 +114,15 @@ class MoELayer:
 
 
 def build_layer(spec: LayerSpec, seed: int, max_tokens: int, experts_fn=None,
-                install_all: bool = False) -> MoELayer:
-    """A layer with the seeded weights of ``workloads`` (router, pool, shared)."""
+                install_all: bool = False, pool=None) -> MoELayer:
+    """A layer with the seeded weights of ``workloads`` (router, pool, shared);
+    ``pool``: an already packed host pool of the same layer shape to share."""
     from . import workloads as wl
     L = MoELayer(spec, max_tokens)
     W_r, b = wl.router_weights(spec, seed)
     L.set_router(W_r, b)
     fn = experts_fn or (lambda e: wl.expert_weights(spec, seed, e))
-    L.load_host_pool(fn)
+    L.load_host_pool(fn, pool)
     if spec.has_shared:
         L.set_shared(wl.expert_weights(spec, seed, 0, shared=True))
     if install_all:

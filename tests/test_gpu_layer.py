@@ -255,6 +255,15 @@ def test_decode_path_selection():
     with pytest.raises(capi.MoeError) as e:
         L.forward(bf16_tensor(x[:17]), regime=DEC)
     assert e.value.status == capi.MOE_ERR_UNSUPPORTED
+    # the fused step's per-CTA timeline while kernel timing is on: every CTA
+    # passes the nine marks in order
+    capi.moe_profile(L.h, True)
+    L.forward(bf16_tensor(x[:8]), regime=DEC)
+    tr = capi.moe_debug_step_trace(L.h)
+    capi.moe_profile(L.h, False)
+    assert len(tr) == torch.cuda.get_device_properties(0).multi_processor_count
+    for row in tr:
+        assert len(row) == 9 and all(b >= a for a, b in zip(row, row[1:]))
     capi.moe_set_decode_path(L.h, capi.MOE_DECODE_CHAIN)
     _, info = L.forward(bf16_tensor(x[:8]), regime=DEC)
     assert info.fused_step == 0
