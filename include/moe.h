@@ -245,8 +245,9 @@ int moe_set_fill_mode(moe_layer_t layer, int mode);
 /* How a decode step runs.  MOE_DECODE_AUTO (default): as one fused,
  * cooperative launch -- routing, LRU step, expert FFN over hits and misses,
  * shared expert and combine, one CTA per SM meeting at grid barriers --
- * whenever the step allows it, else as the chain of launches.  The fused
- * launch takes steps of at most 16 tokens with N * k <= 256, E <= 640,
+ * for small steps (N * k <= 32) that allow it, else as the chain of
+ * launches.  The fused launch takes steps of at most 16 tokens with
+ * N * k <= 256, E <= 640,
  * d_model a multiple of 128, whose misses (if any) are filled by the expert
  * FFN itself (every expert resident, or MOE_FILL_FUSED, or MOE_FILL_AUTO
  * choosing it).  Both paths compute the same values bit for bit.
@@ -335,11 +336,14 @@ int moe_debug_inject(moe_layer_t layer, int what, long long arg);
 int moe_debug_alloc_fault(long long nth, long long* live_out);
 
 /* Timeline of the last fused decode step run while kernel timing
- * (moe_profile) was on: per CTA, kStepMarks = 9 global-timer stamps (ns) --
- * kernel start, logits written, grid barrier 1 passed, access table built,
- * phase-1 (gate/up) outputs written, barrier 2 passed, phase-2 (down)
- * outputs written, barrier 3 passed, combine done (marks a CTA does not
- * reach stay from an earlier step).  out: host array of at least
+ * (moe_profile) was on: per CTA, 11 global-timer stamps (ns) -- kernel
+ * start, logits written, grid barrier 1 passed, top-k done, permutation
+ * done, access table built, phase-1 (gate/up) outputs written, barrier 2
+ * passed, phase-2 (down) outputs written, barrier 3 passed, combine done
+ * (marks a CTA does not reach stay from an earlier step) -- then the SM clock
+ * counter at the first and at the last stamp, then the global timer when the
+ * CTA's first phase-1 weight stage had landed and when its last one was
+ * consumed (15 entries per CTA).  out: host array of at least
  * n_cta * n_marks entries, CTA-major; *n_cta, *n_marks (may be NULL) get the
  * sizes.  MOE_ERR_STATE if no such step ran. */
 int moe_debug_step_trace(moe_layer_t layer, uint64_t* out, int cap, int* n_cta, int* n_marks);

@@ -825,7 +825,13 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     if (fm == MOE_FILL_AUTO) fm = std::min(g.E, N * g.k) <= g.S ? MOE_FILL_FUSED : MOE_FILL_KERNEL;
     const bool fused_fill = !resident && fm == MOE_FILL_FUSED && L->pool_dev;
     StepPlan plan{};
-    const bool want = !prefill && L->decode_path != MOE_DECODE_CHAIN && !L->step_failed && L->num_sms >= 2;
+    // AUTO takes the fused launch for steps of at most kStepAutoPairs (token,
+    // expert) pairs: there it is the faster path (measured on GB300: batch 1
+    // and 4 of the 35B-A3B-shaped layer, batch 1 of the 284B-A13B-shaped one);
+    // for larger steps the chained launches' GEMV keeps pace and the chain
+    // is used
+    const bool want = !prefill && L->decode_path != MOE_DECODE_CHAIN && !L->step_failed && L->num_sms >= 2 &&
+                      (L->decode_path == MOE_DECODE_STEP || N * g.k <= kStepAutoPairs);
     const bool can = want && (resident || fused_fill) && step_plan(g, N, &plan);
     if (L->decode_path == MOE_DECODE_STEP && !can)
       return fail(L, MOE_ERR_UNSUPPORTED, "this step cannot run as one fused launch (N = %d, fill mode %d)", N, fm);

@@ -621,9 +621,11 @@ MOE_DEV void produce_drain(const Smem& S, int D, const Ring& ring, int* err) {
 // b of every stage; a unit's partial sums go to the epilogue through one of
 // RS slots.  ALL: every token is staged once (phase 1, N <= 8), so no
 // activation-buffer waits.
+// mk (may be null): warp 0 stamps the global timer when its first stage has
+// landed (mk[0]) and when it has consumed its last (mk[1]).
 template <int FMT, int PH, bool HOST>
 MOE_DEV void compute(const Geo& g, const GemvArgs& a, const SG& p, const EntryTable& T, const Range& rr,
-                     const Smem& S, Small& sm, Ring& ring, long long wl) {
+                     const Smem& S, Small& sm, Ring& ring, long long wl, unsigned long long* mk = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool ALL = PH == 1 && p.all;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -640,6 +642,7 @@ MOE_DEV void compute(const Geo& g, const GemvArgs& a, const SG& p, const EntryTa
       for (int st = 0; st < p.NS; ++st, ++n) {
         const int slot = n % p.D;
         const bool ok = wait_or_abort(&S.full[slot], (n / p.D) & 1, &sm.abort, a.err, wl);
+        if (mk && warp == 0 && lane == 0 && n == ring.n) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(mk[0]));
         const int kb = st * kBoxes + bslot;
         if (HOST && ok && cu.en.ex >= 0)
           host_part(g, p, a, cu.en, PH == 1 ? u / p.RB : 2, PH == 1 ? u % p.RB : u, st,
@@ -672,6 +675,7 @@ MOE_DEV void compute(const Geo& g, const GemvArgs& a, const SG& p, const EntryTa
       ++bs;   // (ALL blocks use no activation buffer of the ring)
     }
   }
+  if (mk && warp == 0 && lane == 0 && n != ring.n) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(mk[1]));
   ring.n = n;
   ring.us = us;
   ring.bs = bs;

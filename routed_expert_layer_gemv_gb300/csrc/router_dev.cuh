@@ -16,34 +16,50 @@ namespace rt {
 
 constexpr int kRouterWarps = 8;
 
-MOE_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+// Order-preserving 32-bit key of a logit: a > b (as floats) <=> key(a) >
+// key(b), equal floats give equal keys (-0 is +0), and a NaN ranks as -inf.
+MOE_DEV uint32_t logit_key(float v) {
+  if (!(v == v)) v = -INFINITY;
+  if (v == 0.f) v = 0.f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 // One warp: the k largest of the logits row L (shared memory, E <= 1024
 // entries; ties to the lower expert id), gates, written in ascending id order.
+// Each of the k rounds takes the largest key a lane still holds, then two
+// warp reductions (redux.sync): the largest key, and the lowest id holding it.
+MOE_DEV void topk_gates(const float* L, int E, int k, int norm_topk, int my_e, int* idx, float* gates);
+
 MOE_DEV void topk_row(const float* L, int E, int k, int norm_topk, int* idx, float* gates) {
   const int lane = threadIdx.x & 31;
   uint32_t taken = 0;  // bit i: entry lane + 32 i already selected
   int my_e = -1;
-  float my_v = 0.f, top = 0.f;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
+    uint32_t bk = 0;
     int be = 0x7fffffff;
     for (int i = 0, e = lane; e < E; ++i, e += 32) {
       if (taken & (1u << i)) continue;
-      const float v0 = L[e];
-      const float v = v0 == v0 ? v0 : -INFINITY;   // a NaN logit ranks last, so every id stays valid
-      if (better(v, e, bv, be)) { bv = v; be = e; }
+      const uint32_t key = logit_key(L[e]);
+      if (key > bk) { bk = key; be = e; }   // ascending e: the first of equal keys is kept
     }
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (j == 0) top = bv;
-    if (lane == j) { my_e = be; my_v = bv; }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const int w = (int)__reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)be : 0xffffffffu);
+    if ((w & 31) == lane) taken |= 1u << (w >> 5);
+    if (lane == j) my_e = w;
   }
-  // gates (fp32): softmax over the selected logits, or the full softmax
+  topk_gates(L, E, k, norm_topk, my_e, idx, gates);
+}
+
+// The selected experts' gates (one warp): lane j < k holds my_e = the j-th
+// largest logit's expert (selection order); writes idx and gates in ascending
+// expert order.  Gates (fp32) = softmax over the selected logits, or the full
+// softmax probabilities.  Every top-k of the library ends here, so the
+// chained and the fused decode paths compute the same gates bit for bit.
+MOE_DEV void topk_gates(const float* L, int E, int k, int norm_topk, int my_e, int* idx, float* gates) {
+  const int lane = threadIdx.x & 31;
+  const float top = L[__shfl_sync(0xffffffffu, my_e, 0)];
+  const float my_v = lane < k ? L[my_e] : 0.f;
   const float num = lane < k ? expf(my_v - top) : 0.f;
   float den = 0.f;
   if (norm_topk) {

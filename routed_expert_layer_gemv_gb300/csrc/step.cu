@@ -141,7 +141,10 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
   const int N = a.N, E = g.E, k = g.k, d = g.d;
   const long long wl = a.wait_cycles > 0 ? a.wait_cycles : tc::kWaitCycles;
   unsigned long long* mark = s.trace ? s.trace + (size_t)cta * kStepMarks : nullptr;
-  if (mark && tid == 0) mark[0] = gtimer();
+  if (mark && tid == 0) {
+    mark[11] = (unsigned long long)clock64();
+    mark[0] = gtimer();
+  }
   if (tid == 0) {
     for (int i = 0; i < p1.D; ++i) {
       tc::mbar_init(&S.full[i], 1);
@@ -167,9 +170,10 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     if (p2.smode) tc::prefetch_tmap(&sd);
   }
   // the slot table as it was before the step (the LRU CTA rewrites it only
-  // after barrier 1, when every CTA has read it)
-  for (int i = tid; i < E; i += kThreads) C.so[i] = s.slot_of[i];
-  for (int i = tid; i < g.S + g.X; i += kThreads) C.bufm[i] = s.buf[i];
+  // after barrier 1, when every CTA has read it): loaded now, parked in
+  // shared memory after the router, so the loads overlap its work
+  const int so_r = tid < E ? s.slot_of[tid] : -1;            // E <= kThreads
+  const int bm_r = tid < g.S + g.X ? s.buf[tid] : -1;        // S + X <= E
   lru::LruRegs lr{};
   if (cta == 0) lr = lru::lru_load(E, g.S, g.X, s.slot_of, s.expert_of, s.stamp, s.clock, s.buf);
   __syncthreads();
@@ -188,13 +192,11 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
       for (int t = 0; t < kStepMaxTokens; ++t)
         if (lane == 0) part[grp][warp & 7][t] = sum[t];
     } else if (warp >= 2 * rt::kRouterWarps && eb == cta) {
-      // warps 16..19: the tokens' exponents, and (N <= 8) every token staged for phase 1
-      const int t4 = tid - 2 * rt::kRouterWarps * 32;
-      for (int t = t4 >> 5; t < N; t += 4) {
+      // warps 16..19: the tokens' exponents (f16 staging of x)
+      for (int t = warp - 2 * rt::kRouterWarps; t < N; t += 4) {
         const int se = rt::token_exp(s.x + (size_t)t * d, d);
         if (lane == 0) C.xexp[t] = se;
       }
-      if (ALL) stage_all<FMT>(p1, N, s.x, reinterpret_cast<uint2*>(S.base + p1.off_x), &sm.sexp[0][0], t4, 128, 3);
     }
     __syncthreads();
     for (int q = tid; q < 2 * N; q += kThreads) {
@@ -207,14 +209,14 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     __syncthreads();
   }
   if (cta >= E && warp >= 2 * rt::kRouterWarps) {
-    // CTAs without an expert still compute the exponents and stage the tokens
-    const int t4 = tid - 2 * rt::kRouterWarps * 32;
-    for (int t = t4 >> 5; t < N; t += 4) {
+    // CTAs without an expert still compute the exponents
+    for (int t = warp - 2 * rt::kRouterWarps; t < N; t += 4) {
       const int se = rt::token_exp(s.x + (size_t)t * d, d);
       if (lane == 0) C.xexp[t] = se;
     }
-    if (ALL) stage_all<FMT>(p1, N, s.x, reinterpret_cast<uint2*>(S.base + p1.off_x), &sm.sexp[0][0], t4, 128, 3);
   }
+  if (tid < E) C.so[tid] = so_r;
+  if (tid < g.S + g.X) C.bufm[tid] = bm_r;
   __syncthreads();
   const unsigned long long target = s.gbar_base + (unsigned long long)G;   // of each barrier
   if (tid == 0) {
@@ -223,17 +225,24 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     gbar_wait(s.gbar + 0, target, &sm.abort, a.err);
     if (mark) mark[2] = gtimer();
   }
+  __syncwarp();   // lane 0 waited alone: the warp runs the top-k below converged
   __syncthreads();
   const bool routed = !sm.abort;
 
-  // every CTA: top-k and gates of every token (warp per token; the logits
-  // row is staged in the ring area, which no copy uses yet)
+  // every CTA: top-k and gates of every token (warps 0..15, one token each;
+  // the logits row is staged in the ring area, which no copy uses yet) while
+  // warps 16..19 stage every token (N <= 8) for phase 1
   if (routed) {
-    float* Ls = reinterpret_cast<float*>(S.base) + (size_t)warp * E;
-    for (int t = warp; t < N; t += kThreads / 32) {
-      rt::stage_logits(s.logits, t, E, Ls);
-      rt::topk_row(Ls, E, k, g.norm_topk, C.idx + t * k, C.gates + t * k);
-      __syncwarp();
+    if (warp < 2 * rt::kRouterWarps) {
+      float* Ls = reinterpret_cast<float*>(S.base) + (size_t)warp * E;
+      for (int t = warp; t < N; t += 2 * rt::kRouterWarps) {
+        rt::stage_logits(s.logits, t, E, Ls);
+        rt::topk_row(Ls, E, k, g.norm_topk, C.idx + t * k, C.gates + t * k);
+        __syncwarp();
+      }
+    } else if (ALL) {
+      stage_all<FMT>(p1, N, s.x, reinterpret_cast<uint2*>(S.base + p1.off_x), &sm.sexp[0][0],
+                     tid - 2 * rt::kRouterWarps * 32, 128, 3);
     }
   }
   __syncthreads();
@@ -262,6 +271,7 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     C.tok_of[r] = t;
   }
   __syncthreads();
+  if (mark && tid == 0) mark[4] = gtimer();
   // access table: hits ascending id, then misses ascending id
   {
     const bool inU = routed && tid < E && cnt > 0;
@@ -281,7 +291,7 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     }
   }
   __syncthreads();
-  if (mark && tid == 0) mark[3] = gtimer();
+  if (mark && tid == 0) mark[5] = gtimer();
   const bool lru_cta = cta == 0 && routed;   // arrives at barriers 2 and 3 below, before the LRU step
   if (lru_cta) {
     // the layer's copy of the routing (what moe_debug_last_step returns)
@@ -366,31 +376,33 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     produce<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, &md, &md, &sd, &sd, wl);
     produce_drain(S, p1.D, ring, a.err);
   } else if (warp < kCW) {
-    compute<FMT, 1, HOST>(g, ga, p1, T, r1, S, sm, ring, wl);
+    compute<FMT, 1, HOST>(g, ga, p1, T, r1, S, sm, ring, wl, mark ? mark + 13 : nullptr);
     compute<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, wl);
   } else {
     reduce<FMT, 1, HOST>(g, ga, p1, T, r1, S, sm, ring, first_staged, s.x, C.xexp, s.h, s.O, wl);
     // this CTA's h rows are written: barrier 2, then phase 2 stages h of any CTA
     epi_sync();
     if (warp == kCW + 1 && lane == 0) {
-      if (mark) mark[4] = gtimer();
+      if (mark) mark[6] = gtimer();
       if (!lru_cta) gbar_arrive(s.gbar + 1);
       gbar_wait(s.gbar + 1, target, &sm.abort, a.err);
-      if (mark) mark[5] = gtimer();
+      if (mark) mark[7] = gtimer();
     }
+    __syncwarp();
     epi_sync();
     reduce<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, false, s.x, C.xexp, s.h, s.O, wl);
     epi_sync();
     if (warp == kCW + 1 && lane == 0) {
-      if (mark) mark[6] = gtimer();
+      if (mark) mark[8] = gtimer();
       if (!lru_cta) gbar_arrive(s.gbar + 2);
     }
   }
   __syncthreads();
   if (tid == 0) {
     gbar_wait(s.gbar + 2, target, &sm.abort, a.err);
-    if (mark) mark[7] = gtimer();
+    if (mark) mark[9] = gtimer();
   }
+  __syncwarp();
   __syncthreads();
 
   // ---------------------------------------------------------------- combine
@@ -426,7 +438,10 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
   }
   if (mark) {
     __syncthreads();
-    if (tid == 0) mark[8] = gtimer();
+    if (tid == 0) {
+      mark[10] = gtimer();
+      mark[12] = (unsigned long long)clock64();
+    }
   }
 }
 
@@ -463,7 +478,7 @@ bool step_plan(const Geo& g, int N, StepPlan* out) {
   // the routing scratch (a logits row per warp) and the LRU CTA's state live
   // in the ring area before any copy starts
   const size_t ring_bytes = (size_t)D * stage;
-  if ((size_t)(kThreads / 32) * g.E * 4 > ring_bytes || sizeof(lru::LruSmem) > ring_bytes) return false;
+  if ((size_t)(2 * rt::kRouterWarps) * g.E * 4 > ring_bytes || sizeof(lru::LruSmem) > ring_bytes) return false;
   P.p1 = a;
   P.p2 = b;
   P.ctl_off = (a.off_bar + bars + 15) & ~15;

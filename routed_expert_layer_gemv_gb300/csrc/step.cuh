@@ -10,6 +10,7 @@ constexpr int kStepMaxTokens = 16;        // tokens of one fused step
 constexpr int kStepMaxE = gv::kThreads;   // experts: one per thread of a CTA in the routing and the LRU step
 constexpr int kStepMaxPairs = 256;        // N * k (so also the step's distinct experts)
 constexpr int kStepSmemMax = 232448 - 2048;   // dynamic shared memory (227 KB less the static part)
+constexpr int kStepAutoPairs = 32;        // MOE_DECODE_AUTO fuses steps of at most this many (token, expert) pairs
 
 // Buffers of one fused step (device pointers unless noted).
 struct StepArgs {
@@ -35,9 +36,14 @@ struct StepArgs {
 };
 
 // Marks of the per-CTA timeline (moe_debug_step_trace): kernel start, logits
-// written, barrier 1 passed, access table built, phase-1 outputs written,
-// barrier 2 passed, phase-2 outputs written, barrier 3 passed, done.
-constexpr int kStepMarks = 9;
+// written, barrier 1 passed, top-k done, permutation done, access table
+// built, phase-1 outputs written, barrier 2 passed, phase-2 outputs written,
+// barrier 3 passed, done (global timer, ns); then the SM clock (clock64) at
+// the first and the last mark, which give the clock rate the step ran at;
+// then (global timer) the first phase-1 stage landed and the last consumed,
+// as compute warp 0 saw them (left from an earlier step when the CTA had no
+// phase-1 work).
+constexpr int kStepMarks = 15;
 
 struct StepPlan {
   gv::SG p1, p2;   // the two phases' geometry, sharing one ring layout

@@ -248,7 +248,13 @@ def test_decode_path_selection():
     L = build_layer(spec, 3, 64, install_all=True)
     x = _tokens(spec, 3, 64)
     _, info = L.forward(bf16_tensor(x[:8]), regime=DEC)
-    assert info.fused_step == 1                          # AUTO: eligible steps run fused
+    assert info.fused_step == 1                          # AUTO: small eligible steps run fused
+    _, info = L.forward(bf16_tensor(x[:16]), regime=DEC)
+    assert info.fused_step == 0                          # more than 32 (token, expert) pairs: the chain
+    capi.moe_set_decode_path(L.h, capi.MOE_DECODE_STEP)
+    _, info = L.forward(bf16_tensor(x[:16]), regime=DEC)
+    assert info.fused_step == 1                          # STEP: fused whenever it fits
+    capi.moe_set_decode_path(L.h, capi.MOE_DECODE_AUTO)
     _, info = L.forward(bf16_tensor(x[:17]), regime=DEC)
     assert info.fused_step == 0                          # more than 16 tokens: the chain
     capi.moe_set_decode_path(L.h, capi.MOE_DECODE_STEP)
@@ -256,14 +262,14 @@ def test_decode_path_selection():
         L.forward(bf16_tensor(x[:17]), regime=DEC)
     assert e.value.status == capi.MOE_ERR_UNSUPPORTED
     # the fused step's per-CTA timeline while kernel timing is on: every CTA
-    # passes the nine marks in order
+    # passes the eleven marks in order
     capi.moe_profile(L.h, True)
     L.forward(bf16_tensor(x[:8]), regime=DEC)
     tr = capi.moe_debug_step_trace(L.h)
     capi.moe_profile(L.h, False)
     assert len(tr) == torch.cuda.get_device_properties(0).multi_processor_count
     for row in tr:
-        assert len(row) == 9 and all(b >= a for a, b in zip(row, row[1:]))
+        assert len(row) == 15 and all(b >= a for a, b in zip(row[:11], row[1:11])) and row[12] > row[11]
     capi.moe_set_decode_path(L.h, capi.MOE_DECODE_CHAIN)
     _, info = L.forward(bf16_tensor(x[:8]), regime=DEC)
     assert info.fused_step == 0
