@@ -250,11 +250,7 @@ def test_decode_path_selection():
     _, info = L.forward(bf16_tensor(x[:8]), regime=DEC)
     assert info.fused_step == 1                          # AUTO: small eligible steps run fused
     _, info = L.forward(bf16_tensor(x[:16]), regime=DEC)
-    assert info.fused_step == 0                          # more than 32 (token, expert) pairs: the chain
-    capi.moe_set_decode_path(L.h, capi.MOE_DECODE_STEP)
-    _, info = L.forward(bf16_tensor(x[:16]), regime=DEC)
-    assert info.fused_step == 1                          # STEP: fused whenever it fits
-    capi.moe_set_decode_path(L.h, capi.MOE_DECODE_AUTO)
+    assert info.fused_step == 1                          # 16 tokens x top-2 = 32 pairs: still fused
     _, info = L.forward(bf16_tensor(x[:17]), regime=DEC)
     assert info.fused_step == 0                          # more than 16 tokens: the chain
     capi.moe_set_decode_path(L.h, capi.MOE_DECODE_STEP)
@@ -275,6 +271,17 @@ def test_decode_path_selection():
     assert info.fused_step == 0
     with pytest.raises(capi.MoeError):
         capi.moe_set_decode_path(L.h, 7)
+    L.close()
+    # AUTO leaves steps of more than 32 (token, expert) pairs to the chain;
+    # STEP fuses them when they fit
+    spec = small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=16)
+    L = build_layer(spec, 3, 16, install_all=True)
+    x = _tokens(spec, 3, 16)
+    _, info = L.forward(bf16_tensor(x[:9]), regime=DEC)
+    assert info.fused_step == 0
+    capi.moe_set_decode_path(L.h, capi.MOE_DECODE_STEP)
+    _, info = L.forward(bf16_tensor(x[:9]), regime=DEC)
+    assert info.fused_step == 1
     L.close()
 
 
