@@ -339,13 +339,14 @@ def decode_workload(c, work, batches, peak, with_modes=True, timed=None):
                  for n in c.args.fill_modes.split(",") if n in names}
     e2e = [run_e2e(c, work, b) for b in batches]
     resident = c.layer(work, max(batches), n_slots=work.layer.E, install_all=True)
-    res = [run_decode(c, work, b, profile=True, resident=resident) for b in batches]
+    res = [run_decode(c, work, b, resident=resident) for b in batches]            # tokens/s
+    pres = [run_decode(c, work, b, profile=True, resident=resident) for b in batches]   # kernel times
     resident[0].close()
     trace = [trace_miss_rate(c, work, b) for b in batches]
     per = {}
     for i, b in enumerate(batches):
         r, pr, e, rr, tr = runs[i], pruns[i], e2e[i], res[i], trace[i]
-        st_ms, st_n = rr["prof"]["step"]
+        st_ms, st_n = pres[i]["prof"]["step"]
         per[str(b)] = {
             "tokens_per_s": r["tokens"] / (r["ms"] / 1000.0),
             "e2e_tokens_per_s": e["tokens"] / e["s"],
@@ -364,10 +365,11 @@ def decode_workload(c, work, batches, peak, with_modes=True, timed=None):
                 "hbm_GB_per_s": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9,
                 "frac_of_measured_hbm": rr["bytes"] / (rr["ms"] / 1000.0) / 1e9 / peak,
                 "kernel_frac_of_measured_hbm":
-                    rr["bytes"] / (st_ms / 1000.0) / 1e9 / peak if st_n == rr["steps"] and st_ms else None,
+                    pres[i]["bytes"] / (st_ms / 1000.0) / 1e9 / peak if st_n == pres[i]["steps"] and st_ms else None,
+                "kernel_ms_per_step": {k: v[0] / pres[i]["steps"] for k, v in pres[i]["prof"].items() if v[1]},
                 "misses": rr["misses"]},
         }
-    return dict(runs=runs, e2e=e2e, res=res, per_batch=per)
+    return dict(runs=runs, e2e=e2e, res=res, pres=pres, per_batch=per)
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -500,19 +502,21 @@ def main():
     value = ws * tokens / (ms / 1000.0)
     e2e_value = ws * tokens / e2e_s
 
-    # roofline: the fused decode step kernel on the all-resident steps (one
-    # launch per step, so its per-launch events time exactly the kernel)
-    r_bytes = sum(r["bytes"] for r in dec["res"])
-    r_ms = sum(r["prof"]["step"][0] for r in dec["res"])
-    r_n = sum(r["prof"]["step"][1] for r in dec["res"])
+    # roofline: the fused decode step kernel on the all-resident steps of the
+    # batches that ran fused (one launch per step, so its per-launch events
+    # time exactly the kernel)
+    fb = [r for r in dec["pres"] if r["prof"]["step"][1] == r["steps"]]
+    r_bytes = sum(r["bytes"] for r in fb)
+    r_ms = sum(r["prof"]["step"][0] for r in fb)
+    r_n = sum(r["prof"]["step"][1] for r in fb)
     achieved = (r_bytes / max(r_n, 1)) / ((r_ms / max(r_n, 1)) / 1000.0) / 1e9 if r_ms > 0 else None
-    ratio = traffic_ratio("step_kernel", "decode35b_resident_b16")
+    ratio = traffic_ratio("step_kernel", "decode35b_resident_b4")
     roof = {"bound": "hbm", "kernel": "fused decode step (step_kernel), all-resident decode 35B-A3B steps of "
-                                      "batches %s" % "/".join(map(str, batches)),
+                                      "batches %s" % "/".join(str(r["batch"]) for r in fb),
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
             "traffic": ratio * r_bytes / max(r_n, 1) if ratio else None, "peak_kind": peak_kind,
             "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the fused step kernel, "
-                              "decode 35B-A3B batch 16 all-resident, scaled to this run's bytes per launch"
+                              "decode 35B-A3B batch 4 all-resident, scaled to this run's bytes per launch"
                               if ratio else None,
             "bytes_per_launch": r_bytes / max(r_n, 1), "ms_per_launch": r_ms / max(r_n, 1),
             "launches": r_n}

@@ -246,6 +246,7 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     }
   }
   __syncthreads();
+  if (mark && tid == 0) mark[3] = gtimer();
   // permutation: counts, offsets, rows in ascending token order per expert
   int cnt = 0;
   if (routed && tid < E)
