@@ -174,6 +174,20 @@ int moe_lru_touch(moe_layer_t layer, const int* experts, int n, int* slot_of_out
                   int* miss_experts_out, int* miss_slots_out, int* n_miss_out,
                   void* stream);
 
+/* Change the number of GPU expert-cache slots between steps, without
+ * reloading any expert from host memory (the pages' elastic expert cache:
+ * "FreeToken：把 284B MoE 塞进游戏 PC", zhichai.net, §二 "弹性显存" -- the cache
+ * is a runtime variable, rebuilt at scheduler safe points).  The
+ * min(n_slots, resident) most recently used experts stay, with their recency
+ * stamps, in slots 0, 1, ... in the order of their old slots; the other
+ * slots are free; the clock is unchanged.  The slot pool is reallocated to
+ * the new size (n_slots + 1 + spare buffers) and the kept experts and the
+ * shared expert are copied into it on the device, so device memory is given
+ * back when the cache shrinks.  Synchronizes the device (a step boundary).
+ * MOE_ERR_ARG unless 1 <= n_slots <= E; MOE_ERR_OOM (cache unchanged) if the
+ * new pool cannot be allocated. */
+int moe_cache_resize(moe_layer_t layer, int n_slots, void* stream);
+
 /* Read / replace the slot table (host arrays of n_slots entries; expert -1 =
  * free slot; stamps are recency counters, larger = more recent; *clock is
  * the last stamp issued).  set_state does not move weights: the caller

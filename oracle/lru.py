@@ -75,6 +75,26 @@ class SlotTable:
             out.append((e, s, False, ev))
         return out
 
+    def resize(self, S_new: int) -> None:
+        """Change the number of slots between steps without reloading any
+        expert (the pages' elastic expert cache, zhichai.net, §二 "弹性显存":
+        the GPU expert cache is resized at scheduler safe points).  Reading
+        taken: the min(S_new, occupied) most recently used experts stay, with
+        their recency stamps; they move to slots 0, 1, ... in the order of
+        their old slots; the other slots are free; the clock is unchanged."""
+        occ = [s for s in range(self.S) if self.expert_of[s] >= 0]
+        keep = sorted(sorted(occ, key=lambda s: self.stamp[s], reverse=True)[:S_new])
+        experts = [self.expert_of[s] for s in keep]
+        stamps = [self.stamp[s] for s in keep]
+        self.S = S_new
+        self.slot_of = [-1] * self.E
+        self.expert_of = [-1] * S_new
+        self.stamp = [0] * S_new
+        for i, (e, st) in enumerate(zip(experts, stamps)):
+            self.expert_of[i] = e
+            self.stamp[i] = st
+            self.slot_of[e] = i
+
     def recency(self) -> List[int]:
         """Occupied slots from least to most recently used."""
         occ = [s for s in range(self.S) if self.expert_of[s] >= 0]

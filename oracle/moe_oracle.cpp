@@ -413,6 +413,40 @@ int orc_lru_step(void* h, const int* routed, int n, int* acc_e, int* acc_s, int*
   return a;
 }
 
+// Resize between steps (the pages' elastic expert cache: resized at safe
+// points, nothing reloaded): the min(S_new, occupied) most recently used
+// experts stay with their stamps, moved to slots 0, 1, ... in the order of
+// their old slots; the other slots are free; the clock is unchanged.
+void orc_lru_resize(void* h, int S_new) {
+  OrcLru* L = static_cast<OrcLru*>(h);
+  std::vector<int> occ;
+  for (int s = 0; s < L->S; ++s)
+    if (L->expert_of[s] >= 0) occ.push_back(s);
+  // the S_new largest stamps (stamps of occupied slots are distinct)
+  std::vector<char> keep(L->S, 0);
+  for (int n = 0; n < S_new && n < (int)occ.size(); ++n) {
+    int best = -1;
+    for (int s : occ)
+      if (!keep[s] && (best < 0 || L->stamp[s] > L->stamp[best])) best = s;
+    keep[best] = 1;
+  }
+  std::vector<int> eo(S_new, -1);
+  std::vector<unsigned long long> st(S_new, 0);
+  int i = 0;
+  for (int s = 0; s < L->S; ++s)
+    if (keep[s]) {
+      eo[i] = L->expert_of[s];
+      st[i] = L->stamp[s];
+      ++i;
+    }
+  L->S = S_new;
+  L->expert_of = eo;
+  L->stamp = st;
+  L->slot_of.assign(L->E, -1);
+  for (int s = 0; s < S_new; ++s)
+    if (eo[s] >= 0) L->slot_of[eo[s]] = s;
+}
+
 void orc_lru_state(void* h, int* expert_of, unsigned long long* stamp, unsigned long long* clock, int* slot_of) {
   OrcLru* L = static_cast<OrcLru*>(h);
   if (expert_of) std::memcpy(expert_of, L->expert_of.data(), sizeof(int) * L->S);

@@ -50,6 +50,7 @@ _SIGS = {
     "orc_lru_step": ([C.c_void_p, _I, C.c_int, _I, _I, _I, _I], C.c_int),
     "orc_lru_state": ([C.c_void_p, _I, _ULL, _ULL, _I], None),
     "orc_lru_set": ([C.c_void_p, _I, _ULL, C.c_ulonglong], None),
+    "orc_lru_resize": ([C.c_void_p, C.c_int], None),
 }
 
 

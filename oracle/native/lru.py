@@ -67,6 +67,12 @@ class SlotTable:
             eo[so[e]] = -1
             lib().orc_lru_set(self._h, ptr(arr(eo, np.int32), C.c_int), ptr(arr(st, np.uint64), C.c_ulonglong), clk)
 
+    def resize(self, S_new: int) -> None:
+        """Between steps: the min(S_new, occupied) most recently used experts
+        stay (stamps kept), in slots 0, 1, ... by old slot order."""
+        lib().orc_lru_resize(self._h, int(S_new))
+        self.S = int(S_new)
+
     def recency(self) -> List[int]:
         """Occupied slots from least to most recently used."""
         eo, st, _, _ = self._state()

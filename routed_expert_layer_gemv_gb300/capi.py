@@ -82,6 +82,7 @@ _SIGS = {
     "moe_register_host_experts": ([_P, _P, C.c_size_t], _I),
     "moe_set_shared_expert": ([_P, _P], _I),
     "moe_cache_install": ([_P, _I, _I, _P], _I),
+    "moe_cache_resize": ([_P, _I, _P], _I),
     "moe_lru_touch": ([_P, _P, _I, _P, _P, _P, _P, _P], _I),
     "moe_lru_get_state": ([_P, _P, _P, _P], _I),
     "moe_lru_set_state": ([_P, _P, _P, C.c_uint64], _I),
@@ -197,6 +198,10 @@ def moe_set_shared_expert(h, weights) -> None:
 
 def moe_cache_install(h, expert: int, slot: int, stream=None) -> None:
     check(lib().moe_cache_install(h, expert, slot, _stream(stream)), h)
+
+
+def moe_cache_resize(h, n_slots: int, stream=None) -> None:
+    check(lib().moe_cache_resize(h, n_slots, _stream(stream)), h)
 
 
 def moe_lru_touch(h, experts, stream=None):

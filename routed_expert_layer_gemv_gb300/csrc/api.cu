@@ -646,6 +646,122 @@ int moe_lru_get_state(moe_layer_t L, int* expert_of_slot, uint64_t* stamp, uint6
   return MOE_OK;
 }
 
+int moe_cache_resize(moe_layer_t L, int n_slots, void* stream) {
+  if (!L) return MOE_ERR_ARG;
+  const Geo g0 = L->g;
+  if (n_slots < 1 || n_slots > g0.E) return fail(L, MOE_ERR_ARG, "n_slots must be in [1, E = %d]", g0.E);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // a step boundary: nothing of an earlier call may still read the pool
+  MOE_CUDA(L, cudaDeviceSynchronize());
+  const int S0 = g0.S, S1 = n_slots;
+  std::vector<int> eo(S0), bufm(S0 + g0.X);
+  std::vector<unsigned long long> stp(S0);
+  MOE_CUDA(L, cudaMemcpy(eo.data(), L->expert_of, (size_t)S0 * 4, cudaMemcpyDeviceToHost));
+  MOE_CUDA(L, cudaMemcpy(stp.data(), L->stamp, (size_t)S0 * 8, cudaMemcpyDeviceToHost));
+  if (!bufm.empty()) MOE_CUDA(L, cudaMemcpy(bufm.data(), L->buf, bufm.size() * 4, cudaMemcpyDeviceToHost));
+  // the S1 most recently used experts stay, in the order of their old slots
+  std::vector<int> occ;
+  for (int s = 0; s < S0; ++s)
+    if (eo[s] >= 0 && eo[s] < g0.E) occ.push_back(s);
+  std::vector<int> by_stamp = occ;
+  std::sort(by_stamp.begin(), by_stamp.end(), [&](int a, int b) { return stp[a] > stp[b]; });
+  if ((int)by_stamp.size() > S1) by_stamp.resize(S1);
+  std::vector<int> keep = by_stamp;
+  std::sort(keep.begin(), keep.end());
+  for (int s : keep)
+    if (!buf_ok(g0, bufm[s])) return fail(L, MOE_ERR_STATE, "slot %d maps to buffer %d", s, bufm[s]);
+  // the new geometry and its buffers: slot i in buffer i, the shared expert
+  // in buffer S1, the spares after it
+  Geo g1 = g0;
+  g1.S = S1;
+  g1.X = (int)std::max<long long>(0, std::min<long long>(g1.E, (long long)L->desc.max_tokens * g1.k) - S1);
+  const size_t nb1 = (size_t)g1.S + 1 + g1.X;
+  uint8_t* pool = nullptr;
+  int *eo_d = nullptr, *buf_d = nullptr;
+  unsigned long long* st_d = nullptr;
+  auto undo = [&]() {
+    if (pool) cudaFree(pool);
+    if (eo_d) cudaFree(eo_d);
+    if (buf_d) cudaFree(buf_d);
+    if (st_d) cudaFree(st_d);
+    cudaGetLastError();
+  };
+  if (alloc_fault_due() || cudaMalloc(&pool, nb1 * g1.ebytes) != cudaSuccess ||
+      cudaMalloc(&eo_d, (size_t)S1 * 4) != cudaSuccess || cudaMalloc(&st_d, (size_t)S1 * 8) != cudaSuccess ||
+      cudaMalloc(&buf_d, std::max<size_t>(16, (size_t)(S1 + g1.X) * 4)) != cudaSuccess) {
+    undo();
+    return fail(L, MOE_ERR_OOM, "resizing the expert cache to %d slots: out of device memory (cache unchanged)", S1);
+  }
+  // kept experts and the shared expert move buffer to buffer on the device
+  cudaError_t ce = cudaSuccess;
+  for (size_t i = 0; i < keep.size() && ce == cudaSuccess; ++i)
+    ce = cudaMemcpyAsync(pool + i * g1.ebytes, L->slots + (size_t)bufm[keep[i]] * g0.ebytes, g0.ebytes,
+                         cudaMemcpyDeviceToDevice, st);
+  if (ce == cudaSuccess && g1.has_shared)
+    ce = cudaMemcpyAsync(pool + (size_t)S1 * g1.ebytes, L->slots + (size_t)S0 * g0.ebytes, g0.ebytes,
+                         cudaMemcpyDeviceToDevice, st);
+  std::vector<int> eo1(S1, -1), buf1(S1 + g1.X), so1(g1.E, -1);
+  std::vector<unsigned long long> st1(S1, 0);
+  for (size_t i = 0; i < keep.size(); ++i) {
+    eo1[i] = eo[keep[i]];
+    st1[i] = stp[keep[i]];
+    so1[eo1[i]] = (int)i;
+  }
+  for (int s = 0; s < S1; ++s) buf1[s] = s;
+  for (int j = 0; j < g1.X; ++j) buf1[S1 + j] = S1 + 1 + j;
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(eo_d, eo1.data(), (size_t)S1 * 4, cudaMemcpyHostToDevice, st);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(st_d, st1.data(), (size_t)S1 * 8, cudaMemcpyHostToDevice, st);
+  if (ce == cudaSuccess && !buf1.empty())
+    ce = cudaMemcpyAsync(buf_d, buf1.data(), buf1.size() * 4, cudaMemcpyHostToDevice, st);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(L->slot_of, so1.data(), (size_t)g1.E * 4, cudaMemcpyHostToDevice, st);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
+  GemvPlan* gp = ce == cudaSuccess ? gemv_plan_create(g1, pool) : nullptr;
+  if (ce != cudaSuccess || !gemv_plan_ready(gp)) {
+    if (gp) gemv_plan_destroy(gp);
+    undo();
+    // slot_of may already hold the new table: put the old one back
+    std::vector<int> so0(g0.E, -1);
+    for (int s = 0; s < S0; ++s)
+      if (eo[s] >= 0 && eo[s] < g0.E) so0[eo[s]] = s;
+    cudaMemcpy(L->slot_of, so0.data(), (size_t)g0.E * 4, cudaMemcpyHostToDevice);
+    return ce != cudaSuccess ? cuda_fail(L, ce, "resizing the expert cache") :
+                               fail(L, MOE_ERR_CUDA, "tensor maps of the resized pool could not be encoded");
+  }
+  // swap in the new pool and table
+  auto swap_alloc = [&](void* old_p, void* new_p) {
+    for (auto& p : L->dev_allocs)
+      if (p == old_p) {
+        cudaFree(old_p);
+        p = new_p;
+        return;
+      }
+  };
+  swap_alloc(L->slots, pool);
+  swap_alloc(L->expert_of, eo_d);
+  swap_alloc(L->stamp, st_d);
+  swap_alloc(L->buf, buf_d);
+  L->slots = pool;
+  L->shared_w = pool + (size_t)S1 * g1.ebytes;
+  L->expert_of = eo_d;
+  L->stamp = st_d;
+  L->buf = buf_d;
+  gemv_plan_destroy(L->gplan);
+  L->gplan = gp;
+  L->g = g1;
+  L->desc.n_slots = S1;
+  if (L->plan) {
+    prefill_plan_destroy(L->plan);
+    const size_t Nm = L->desc.max_tokens;
+    L->plan = prefill_plan_create(g1, L->slots, L->xq_codes, Nm * g1.k + Nm + 128, L->hq_codes);
+    if (!prefill_plan_ready(L->plan)) {
+      prefill_plan_destroy(L->plan);
+      L->plan = nullptr;
+    }
+  }
+  L->mirror = eo1;
+  return MOE_OK;
+}
+
 int moe_lru_set_state(moe_layer_t L, const int* expert_of_slot, const uint64_t* stamp, uint64_t clock) {
   if (!L) return MOE_ERR_ARG;
   if (!expert_of_slot || !stamp) return fail(L, MOE_ERR_ARG, "NULL state array");

@@ -438,6 +438,54 @@ def test_error_paths():
     L.close()
 
 
+@pytest.mark.parametrize("fill", [capi.MOE_FILL_AUTO, capi.MOE_FILL_MEMCPY])
+def test_cache_resize_between_steps(fill):
+    # the expert cache shrinks and grows between decode steps: the slot table
+    # follows the oracle's resize (most recent experts kept, recency kept),
+    # every slot holds the expert it names, later steps match the oracle, and
+    # a smaller cache gives device memory back
+    spec = small_spec(E=48, k=4, d_model=256, d_ff=256, n_slots=20, has_shared=True)
+    seed, batch = 37, 2
+    experts = CachedExperts(spec, seed)
+    L = build_layer(spec, seed, batch, experts_fn=experts)
+    capi.moe_set_fill_mode(L.h, fill)
+    O = oracle_layer(spec, seed, experts)
+    T = SlotTable(spec.E, spec.n_slots)
+    xs, _ = wl.ar1_tokens(seed, batch, 24, spec.d_model, 0.9, reject_near_ties(spec, seed))
+    sizes = {5: 6, 11: 30, 17: 3}
+    S = spec.n_slots
+    for t in range(24):
+        if t in sizes:
+            torch.cuda.synchronize()
+            free0 = torch.cuda.mem_get_info()[0]
+            S = sizes[t]
+            capi.moe_cache_resize(L.h, S)
+            T.resize(S)
+            torch.cuda.synchronize()
+            if t == 5:
+                assert torch.cuda.mem_get_info()[0] > free0      # the pool shrank
+            eo, st, clk = capi.moe_lru_get_state(L.h, S)
+            assert eo == T.expert_of and st == T.stamp and clk == T.clock
+            for slot, e in enumerate(eo):
+                if e < 0:
+                    continue
+                mat = experts(e)["down"]
+                out = torch.empty(mat.rows, mat.K, dtype=torch.float32, device="cuda")
+                capi.moe_debug_dequant(L.h, slot, 2, out)
+                want = formats.dequant(mat.codes, mat.scales, mat.tscale, spec.fmt)
+                assert np.array_equal(out.cpu().numpy().astype(np.float64), want), (t, slot, e)
+        y, _ = L.forward(bf16_tensor(xs[t]), regime=DEC)
+        ref, idx, gates = O.forward(wl.bf16_bits_to_f64(xs[t]), "decode")
+        T.step(idx.reshape(-1))
+        assert_close_layer(y, ref, "step %d (%d slots)" % (t, S))
+        eo, st, clk = capi.moe_lru_get_state(L.h, S)
+        assert eo == T.expert_of and st == T.stamp and clk == T.clock
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_cache_resize(L.h, 0)
+    assert e.value.status == capi.MOE_ERR_ARG
+    L.close()
+
+
 def test_allocation_failure_at_each_allocation_leaks_nothing():
     # every device or pinned allocation of a create made to fail in turn: the
     # create returns MOE_ERR_OOM and gives back everything it took; a normal

@@ -86,3 +86,46 @@ def test_install_then_hit():
     acc = T.step([3, 2])
     assert acc == [(3, 1, True, -1), (2, 0, False, 0)]
     assert T.recency() == [1, 0]
+
+
+class NaiveLRUResizable(NaiveLRU):
+    def resize(self, S):
+        # keep the S most recently used (the end of the order list), then
+        # give them slots 0, 1, ... in the order of their old slots
+        kept = self.order[-S:] if S > 0 else []
+        by_slot = sorted(kept, key=lambda e: self.where[e])
+        self.S = S
+        self.where = {e: i for i, e in enumerate(by_slot)}
+        self.order = [e for e in self.order if e in self.where]
+
+
+@pytest.mark.parametrize("E,S,per_step", [(16, 6, 3), (128, 47, 8), (256, 28, 20)])
+def test_resize_matches_naive_list(E, S, per_step):
+    g = np.random.default_rng(E + 7 * S)
+    T, N = SlotTable(E, S), NaiveLRUResizable(E, S)
+    cur = S
+    for step in range(200):
+        if step % 23 == 22:
+            cur = int(g.integers(1, E + 1))
+            T.resize(cur)
+            N.resize(cur)
+            assert T.expert_of == N.expert_of()
+            assert [T.expert_of[s] for s in T.recency()] == N.order
+        routed = g.choice(E, min(per_step, E), replace=False)
+        assert T.step(routed) == N.step(list(routed))
+        assert T.expert_of == N.expert_of()
+        assert [T.expert_of[s] for s in T.recency()] == N.order
+
+
+def test_resize_keeps_stamps_and_clock():
+    T = SlotTable(8, 4)
+    for routed in ([0, 1], [2, 3], [4], [1]):
+        T.step(routed)
+    clk, stamps = T.clock, dict(zip(T.expert_of, T.stamp))
+    # 4 evicted 0 from slot 0, so the two most recent are 4 (slot 0, stamp 5)
+    # and 1 (slot 1, stamp 6), kept in that slot order
+    T.resize(2)
+    assert T.expert_of == [4, 1] and T.clock == clk
+    assert T.stamp == [stamps[4], stamps[1]]
+    T.resize(5)                       # growing: same experts, new free slots
+    assert T.expert_of == [4, 1, -1, -1, -1] and T.clock == clk
