@@ -239,15 +239,16 @@ def trace_miss_rate(c, work, batch):
     """Miss rate over the workload's whole trace (its configured number of
     steps from a cold cache), untimed."""
     torch, capi = c.torch, c.capi
-    xs = c.tokens(work, batch, work.steps)
+    steps = c.args.trace_steps or work.steps
+    xs = c.tokens(work, batch, steps)
     L, spec = c.layer(work, batch)
     y = torch.empty(batch, spec.d_model, dtype=torch.bfloat16, device="cuda")
-    for t in range(work.steps):
+    for t in range(steps):
         L.forward(xs[t], y)
     torch.cuda.synchronize()
     s = capi.moe_stats(L.h)
     L.close()
-    return s[3] / max(1, s[1]), work.steps
+    return s[3] / max(1, s[1]), steps
 
 
 def run_e2e(c, work, batch):
@@ -426,6 +427,11 @@ def main():
                     help="skip the 284B-class decode and the two prefill chunks")
     ap.add_argument("--fill-modes", default="memcpy,device,kernel,fused",
                     help="fill modes timed beside the default per batch ('none': skip them)")
+    ap.add_argument("--trace-steps", type=int, default=0,
+                    help="steps of the untimed full-trace miss-rate replay (0: the workload's own count)")
+    ap.add_argument("--resident-only", action="store_true",
+                    help="time only all-resident decode steps of the headline layer (a short run for "
+                         "profiler captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = _dist()
@@ -480,6 +486,16 @@ def main():
         return
 
     work = wl.DECODE_35B
+    if args.resident_only:
+        resident = c.layer(work, max(batches), n_slots=work.layer.E, install_all=True)
+        rr = [run_decode(c, work, b, resident=resident) for b in batches]
+        resident[0].close()
+        out = {str(r["batch"]): {"tokens_per_s": r["tokens"] / (r["ms"] / 1000.0), "ms_per_step": r["ms"] / r["steps"],
+                                 "frac_of_measured_hbm": r["bytes"] / (r["ms"] / 1000.0) / 1e9 / peak,
+                                 "fused_steps": r["fused_steps"]} for r in rr}
+        print(json.dumps({"workload": work.name + "_all_resident", "steps": args.steps, "warmup": args.warmup,
+                          "per_batch": out}))
+        return
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
