@@ -325,6 +325,116 @@ def prefill_summary(r, fp4_peak):
     }
 
 
+def h2d_rate(c):
+    """Pinned host -> device copy rate of one 256 MB copy (GB/s): the ceiling
+    every fill runs against."""
+    torch = c.torch
+    src = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        dst.copy_(src, non_blocking=True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(4):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    return 4 * (256 << 20) / (a.elapsed_time(b) / 1000.0) / 1e9
+
+
+def run_stack(c, n_layers, batches, link_gbs):
+    """The 35B-A3B layer shape as a stack of n_layers layers (layer l: the
+    seeded weights of seed + l) sharing one slot pool and one LRU table.
+    Decode: n_layers x 47 slots (the single layer's 47 of 128, 37%), batches
+    from a cold cache, W warm-up and K timed stack steps each.  Prefill: one
+    8192-token chunk per step through every layer, 2 E slots, with each
+    prefetch mode (none: each layer fills its own misses; serial: whole-layer
+    prefetch between layers; overlap: layer l + 1 streams in while layer l
+    computes)."""
+    torch, capi, wl = c.torch, c.capi, c.wl
+    from routed_expert_layer_gemv_gb300.layer import MoEStack
+    work, pwork = wl.DECODE_35B, wl.PREFILL_35B
+    spec0 = work.layer
+    E, d, f = spec0.E, spec0.d_model, spec0.d_ff
+    b_e = 3 * d * f * (1 / 2 + 1 / spec0.block)
+    lay = c.capi.moe_expert_layout_for(c.make_desc(spec0, 16))
+    pools = [c.pack_pool(lay, E, lambda e, l=l: wl.expert_weights(spec0, work.seed + l, e)) for l in range(n_layers)]
+    W, K = c.args.warmup, c.args.steps
+    out = {"layers": n_layers, "layer": "35B-A3B shape (d 2048, E 128, top-8, d_ff 768, MXFP4)",
+           "decode": {}, "prefill": {}}
+    S_dec = n_layers * spec0.n_slots
+    spec = dataclasses.replace(spec0, n_slots=S_dec)
+    for b in batches:
+        st = MoEStack(spec, n_layers, work.seed, b, pools=pools)
+        xs = c.tokens(work, b, W + K)
+        y = torch.empty(b, d, dtype=torch.bfloat16, device="cuda")
+        with torch.cuda.stream(c.st):
+            for t in range(W):
+                st.forward(xs[t], y, stream=c.st, regime=capi.MOE_REGIME_DECODE)
+        torch.cuda.synchronize()
+        s0 = [capi.moe_stats(L.h) for L in st.layers]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        launches = fused = 0
+        with torch.cuda.stream(c.st):
+            for t in range(K):
+                c.flush.zero_()
+                ev[t][0].record(c.st)
+                _, info = st.forward(xs[W + t], y, stream=c.st, regime=capi.MOE_REGIME_DECODE)
+                ev[t][1].record(c.st)
+                launches += info.n_launches
+                fused += info.fused_step
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(bb) for a, bb in ev)
+        s1 = [capi.moe_stats(L.h) for L in st.layers]
+        st.close()
+        dist = sum(x1[1] - x0[1] for x0, x1 in zip(s0, s1))
+        miss = sum(x1[3] - x0[3] for x0, x1 in zip(s0, s1))
+        out["decode"][str(b)] = {
+            "tokens_per_s": K * b / (ms / 1000.0), "ms_per_step": ms / K, "us_per_layer_step": 1000.0 * ms / K / n_layers,
+            "miss_rate": miss / max(1, dist), "fill_GB_per_s": miss * b_e / (ms / 1000.0) / 1e9,
+            "layers_fused_per_step": fused / K, "gpu_launches_per_step": launches / K}
+    out["decode_slots"] = S_dec
+    N = pwork.n_tokens
+    xp, _ = wl.iid_tokens(pwork.seed, N, d)
+    x = torch.from_numpy(xp.view(np.int16)).view(torch.bfloat16).cuda()
+    yp = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    spec_p = dataclasses.replace(spec0, n_slots=2 * E)
+    Kp, Wp = max(3, c.args.prefill_steps // 2), 1
+    names = {capi.MOE_PREFETCH_NONE: "none", capi.MOE_PREFETCH_SERIAL: "serial",
+             capi.MOE_PREFETCH_OVERLAP: "overlap"}
+    for mode, name in names.items():
+        st = MoEStack(spec_p, n_layers, work.seed, N, pools=pools)
+        capi.moe_stack_set_prefetch(st.h, mode)
+        with torch.cuda.stream(c.st):
+            for _ in range(Wp):
+                st.forward(x, yp, stream=c.st, regime=capi.MOE_REGIME_PREFILL)
+        torch.cuda.synchronize()
+        s0 = [capi.moe_stats(L.h) for L in st.layers]
+        p0 = capi.moe_stack_prefetch_stats(st.h)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kp)]
+        with torch.cuda.stream(c.st):
+            for t in range(Kp):
+                c.flush.zero_()
+                ev[t][0].record(c.st)
+                st.forward(x, yp, stream=c.st, regime=capi.MOE_REGIME_PREFILL)
+                ev[t][1].record(c.st)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(bb) for a, bb in ev)
+        s1 = [capi.moe_stats(L.h) for L in st.layers]
+        p1 = capi.moe_stack_prefetch_stats(st.h)
+        st.close()
+        miss = sum(x1[3] - x0[3] for x0, x1 in zip(s0, s1)) + (p1[3] - p0[3])
+        gbs = miss * b_e / (ms / 1000.0) / 1e9
+        out["prefill"][name] = {"tokens_per_s": Kp * N / (ms / 1000.0), "ms_per_chunk": ms / Kp,
+                                "ms_per_layer": ms / Kp / n_layers, "misses_per_chunk": miss / Kp,
+                                "link_GB_per_s": gbs, "frac_of_measured_link": gbs / link_gbs if link_gbs else None}
+    out["prefill_slots"] = 2 * E
+    out["prefill_tokens"] = N
+    ov, se = out["prefill"]["overlap"]["ms_per_chunk"], out["prefill"]["serial"]["ms_per_chunk"]
+    out["prefill"]["serial_over_overlap"] = se / ov
+    return out
+
+
 def decode_workload(c, work, batches, peak, with_modes=True, timed=None):
     """Everything reported for one decode workload: the timed default pass
     (`timed`, when already run), kernel times, fill modes, e2e, miss rates and
@@ -423,6 +533,10 @@ def main():
                     help="decode35b = the headline decode configuration; the prefill ones "
                          "print that prefill chunk's line instead")
     ap.add_argument("--prefill-steps", type=int, default=8)
+    ap.add_argument("--stack-layers", type=int, default=8,
+                    help="layers of the multi-layer stack measured as an extra key (0: none)")
+    ap.add_argument("--stack-only", action="store_true",
+                    help="measure only the multi-layer stack (decode and prefill) and print its object")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the 284B-class decode and the two prefill chunks")
     ap.add_argument("--fill-modes", default="memcpy,device,kernel,fused",
@@ -486,6 +600,9 @@ def main():
         return
 
     work = wl.DECODE_35B
+    if args.stack_only:
+        print(json.dumps({"stack": run_stack(c, max(1, args.stack_layers), batches, h2d_rate(c))}))
+        return
     if args.resident_only:
         resident = c.layer(work, max(batches), n_slots=work.layer.E, install_all=True)
         rr = [run_decode(c, work, b, resident=resident) for b in batches]
@@ -537,6 +654,7 @@ def main():
             "bytes_per_launch": r_bytes / max(r_n, 1), "ms_per_launch": r_ms / max(r_n, 1),
             "launches": r_n}
 
+    link = h2d_rate(c)
     extra = {}
     if not args.no_extra:
         w3 = wl.DECODE_284B
@@ -553,6 +671,8 @@ def main():
         for key, w in (("prefill_35b_a3b_n8192", wl.PREFILL_35B), ("prefill_753b_n16384", wl.PREFILL_753B)):
             extra[key] = prefill_summary(run_prefill(c, w), fp4)
             c.pools.clear()
+        if args.stack_layers > 0:
+            extra["stack_35b_a3b_l%d" % args.stack_layers] = run_stack(c, args.stack_layers, batches, link)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -575,10 +695,11 @@ def main():
                    "steps_per_batch": args.steps,
                    "miss_rate_per_batch": {b: dec["per_batch"][b]["miss_rate"] for b in dec["per_batch"]},
                    "l2": "flushed (512 MiB write) between timed steps",
-                   "path": "library defaults: %d of %d timed steps ran as one fused launch (batch <= 16 with "
-                           "misses filled by the expert FFN itself); batch 16 (distinct experts > slots) fills "
-                           "with a copy kernel on 12 reserved SMs and runs the chain of launches"
-                           % (fused, args.steps * len(batches)),
+                   "path": "library defaults: %d of %d timed steps ran as one fused launch (steps of at most "
+                           "32 (token, expert) pairs: batch 1 and 4, misses read over the host link by the step "
+                           "itself); batch 16 (distinct experts > slots) fills with a copy kernel on 12 reserved "
+                           "SMs and runs the chain of launches" % (fused, args.steps * len(batches)),
+                   "h2d_GB_per_s_measured": link,
                    "timing": "value from a pass without per-kernel events; kernel times and roofline from "
                              "instrumented passes of the same steps",
                    "parallelism": "replicas" if ws > 1 else "single GPU",

@@ -56,6 +56,7 @@ extern "C" {
 #define MOE_REGIME_PREFILL 2  /* FP4 weights x FP4 activations, grouped GEMM */
 
 typedef struct moe_layer* moe_layer_t;
+typedef struct moe_stack* moe_stack_t;
 
 /* Layer descriptor.  E experts, top-k, d_model, d_ff, n_slots cache slots. */
 typedef struct {
@@ -63,7 +64,7 @@ typedef struct {
     int k;            /* experts per token, 1..min(E, 32)                     */
     int d_model;      /* multiple of 128 (of 256 for the prefill regime)      */
     int d_ff;         /* multiple of 128 (of 256 for the prefill regime)      */
-    int n_slots;      /* GPU expert-cache slots, 1..E                         */
+    int n_slots;      /* GPU expert-cache slots, 1..E (a stack: 1..min(L E, 1024)) */
     int fmt;          /* MOE_MXFP4 or MOE_NVFP4                               */
     int has_shared;   /* 1: one always-on shared expert, weight 1, resident   */
     int norm_topk;    /* 1: gates renormalised over the k selected            */
@@ -371,6 +372,73 @@ int moe_debug_dequant(moe_layer_t layer, int slot, int m, float* out, void* stre
  * act_scale_x, 1 act_scale_h (NVFP4 only). */
 int moe_debug_actquant(moe_layer_t layer, const float* v, int rows, int K,
                        uint8_t* codes, uint8_t* scales, int which, void* stream);
+
+/* ---- multi-layer stacks --------------------------------------------------
+ * A stack is L layers of one descriptor that share ONE GPU expert cache: one
+ * slot pool of desc->n_slots slots and one LRU table over all layers' experts
+ * (key l * E + e for expert e of layer l), as FreeToken keeps one global LRU
+ * expert cache across layers ("FreeToken：把 284B MoE 塞进游戏 PC", zhichai.net,
+ * §二, "LRU 为什么赢" paragraph; juejin.cn overview, §二 "全局 LRU 专家缓存").
+ * Every layer has its own router, host expert pool and shared expert, set
+ * through its member handle (moe_stack_layer) with the per-layer calls above.
+ * A member's step record, statistics and errors are its own; moe_lru_get_state
+ * and moe_lru_set_state on any member read or write the shared table, whose
+ * expert_of entries are keys; moe_cache_install(member l, e, slot) installs key
+ * l E + e.  Members cannot be resized (moe_cache_resize returns
+ * MOE_ERR_UNSUPPORTED) or destroyed on their own (MOE_ERR_STATE).  Members
+ * share their workspaces, so moe_debug_last_step / moe_debug_last_hidden on a
+ * member read what the stack's latest forward of any member left there.
+ *
+ * moe_stack_forward runs the layers in order, the output of layer l (bf16,
+ * [N, d_model]) being the input of layer l + 1 (the MoE sublayers of a
+ * transformer with the rest of each block left out).  Decode: each layer's step
+ * is moe_forward on the shared cache.  Prefill (whole-layer streaming, the
+ * pages' "Prefill: hide the compute in the transfer", zhichai.net §二
+ * "Prefill：把计算藏进传输"; juejin.cn §二 "全层双缓冲预填充"): before layer l's
+ * step, every expert of layer l is accessed as one table step (hits first,
+ * misses ascending) and its misses are copied from the layer's host pool, so
+ * the layer's own step finds every routed expert resident.  Prefetch modes:
+ *   MOE_PREFETCH_NONE     no prefetch: each layer's step fills its own misses;
+ *   MOE_PREFETCH_SERIAL   layer l + 1's prefetch after layer l (n_slots >= E);
+ *   MOE_PREFETCH_OVERLAP  layer l + 1's prefetch right after layer l's table
+ *                         step, its copies on a few SMs while layer l's GEMMs
+ *                         run on the others (n_slots >= 2 E: layer l's experts
+ *                         are then never the victims);
+ *   MOE_PREFETCH_AUTO     (default) OVERLAP when n_slots >= 2 E, else SERIAL
+ *                         when n_slots >= E, else NONE.
+ * The table ends in the same state in every mode that prefetches (the same
+ * sequence of steps). */
+#define MOE_PREFETCH_AUTO    0
+#define MOE_PREFETCH_NONE    1
+#define MOE_PREFETCH_SERIAL  2
+#define MOE_PREFETCH_OVERLAP 3
+
+/* Create a stack of n_layers (1..4096) layers of descriptor desc, sharing
+ * desc->n_slots cache slots (1..min(n_layers E, 1024)), on the current device.
+ * Returns MOE_ERR_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_OOM / MOE_ERR_CUDA as
+ * moe_layer_create. */
+int moe_stack_create(const moe_layer_desc* desc, int n_layers, moe_stack_t* out);
+/* Synchronises the device, then frees every member and the shared storage. */
+int moe_stack_destroy(moe_stack_t stack);
+/* Member handle of layer l (owned by the stack). */
+int moe_stack_layer(moe_stack_t stack, int l, moe_layer_t* out);
+/* Prefetch mode of later prefill forwards; MOE_ERR_UNSUPPORTED when n_slots
+ * is too small for the mode. */
+int moe_stack_set_prefetch(moe_stack_t stack, int mode);
+/* One forward through every layer: x [N, d_model] bf16 -> y [N, d_model] bf16
+ * (device or pinned host memory, as moe_forward; the hidden states between
+ * layers stay on the device).  regime as moe_forward, one regime for every
+ * layer.  A member's error is returned with its message in
+ * moe_stack_last_error.  info (may be NULL): regime, n_tokens, n_launches
+ * (all layers and prefetches), fused_step (layers run as one fused launch);
+ * the per-step counts are -1 (read each member's statistics instead). */
+int moe_stack_forward(moe_stack_t stack, const void* x, int N, void* y, void* stream, int regime,
+                      moe_forward_info* info);
+/* Accumulated prefetch counters: steps, keys accessed, hits, misses
+ * (synchronises the device). */
+int moe_stack_prefetch_stats(moe_stack_t stack, uint64_t* out4);
+/* The last stack call's error message. */
+const char* moe_stack_last_error(moe_stack_t stack);
 
 /* ---- allocation-free permutation ----------------------------------------
  * The FreeToken pages have no counterpart to this entry point.  It is for

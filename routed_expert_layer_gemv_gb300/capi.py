@@ -50,6 +50,11 @@ MOE_REGIME_AUTO = 0
 MOE_REGIME_DECODE = 1
 MOE_REGIME_PREFILL = 2
 
+MOE_PREFETCH_AUTO = 0
+MOE_PREFETCH_NONE = 1
+MOE_PREFETCH_SERIAL = 2
+MOE_PREFETCH_OVERLAP = 3
+
 
 class moe_layer_desc(C.Structure):
     _fields_ = [("E", C.c_int), ("k", C.c_int), ("d_model", C.c_int), ("d_ff", C.c_int),
@@ -104,6 +109,13 @@ _SIGS = {
     "moe_debug_dequant": ([_P, _I, _I, _P, _P], _I),
     "moe_debug_actquant": ([_P, _P, _I, _I, _P, _P, _I, _P], _I),
     "moe_permute_noalloc": ([_P, _I, _I, _I, _P, _P, _P, _P, _P, C.c_char_p, C.c_size_t], _I),
+    "moe_stack_create": ([C.POINTER(moe_layer_desc), _I, C.POINTER(_P)], _I),
+    "moe_stack_destroy": ([_P], _I),
+    "moe_stack_layer": ([_P, _I, C.POINTER(_P)], _I),
+    "moe_stack_set_prefetch": ([_P, _I], _I),
+    "moe_stack_forward": ([_P, _P, _I, _P, _P, _I, C.POINTER(moe_forward_info)], _I),
+    "moe_stack_prefetch_stats": ([_P, _P], _I),
+    "moe_stack_last_error": ([_P], C.c_char_p),
 }
 
 _lib: Optional[C.CDLL] = None
@@ -145,6 +157,11 @@ def check(status: int, handle=None) -> None:
     if status != MOE_OK:
         msg = lib().moe_last_error(handle).decode() if handle else ""
         raise MoeError(status, msg)
+
+
+def check_stack(status: int, stack) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, lib().moe_stack_last_error(stack).decode() if stack else "")
 
 
 def _ptr(p) -> Optional[int]:
@@ -328,3 +345,38 @@ def moe_permute_noalloc(idx, N: int, k: int, E: int, counts, offsets, row_of, to
                                    _ptr(row_of), _ptr(tok_of), _stream(stream), err, len(err))
     if rc != MOE_OK:
         raise MoeError(rc, err.value.decode())
+
+
+# ---- stacks --------------------------------------------------------------
+
+def moe_stack_create(desc: moe_layer_desc, n_layers: int) -> int:
+    h = C.c_void_p()
+    check(lib().moe_stack_create(C.byref(desc), n_layers, C.byref(h)))
+    return h.value
+
+
+def moe_stack_destroy(s: int) -> None:
+    check(lib().moe_stack_destroy(s))
+
+
+def moe_stack_layer(s: int, l: int) -> int:
+    h = C.c_void_p()
+    check_stack(lib().moe_stack_layer(s, l, C.byref(h)), s)
+    return h.value
+
+
+def moe_stack_set_prefetch(s: int, mode: int) -> None:
+    check_stack(lib().moe_stack_set_prefetch(s, mode), s)
+
+
+def moe_stack_forward(s, x, N: int, y, stream=None, regime: int = MOE_REGIME_AUTO) -> moe_forward_info:
+    info = moe_forward_info()
+    check_stack(lib().moe_stack_forward(s, _ptr(x), N, _ptr(y), _stream(stream), regime, C.byref(info)), s)
+    return info
+
+
+def moe_stack_prefetch_stats(s):
+    """(prefetch steps, keys accessed, hits, misses) accumulated on the device."""
+    out = (C.c_uint64 * 4)()
+    check_stack(lib().moe_stack_prefetch_stats(s, out), s)
+    return tuple(out)

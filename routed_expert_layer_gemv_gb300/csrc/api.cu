@@ -59,6 +59,7 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
 }  // namespace moe
 
 constexpr size_t kDirectHostBytes = 256 * 1024;   // host x / y read and written in place up to this size
+constexpr int kMaxStackLayers = 4096;
 
 struct moe_layer {
   moe_layer_desc desc{};
@@ -123,7 +124,16 @@ struct moe_layer {
   bool fill_mode_chosen = false;
   const uint8_t* pool_dev = nullptr;          // device address of the host pool
   unsigned long long* stats = nullptr;        // steps, distinct, hits, misses
-  std::vector<int> mirror;   // expert per slot as far as the host knows
+  std::vector<int> mirror_own;   // key per slot as far as the host knows (the pool owner's)
+  std::vector<int>* mir = nullptr;   // the mirror of the table this layer uses (its own, or its stack's)
+  // stack membership: layer `index` of a stack whose pool, slot table and
+  // workspaces belong to its layer 0 (owner = false for the others)
+  moe_stack* stack = nullptr;
+  int index = 0;
+  bool owner = true;
+  bool assume_resident = false;        // set by the stack around a forward whose experts it prefetched
+  cudaEvent_t ev_after_route = nullptr;   // set by the stack: recorded after the step's LRU update
+  int gemm_sms = 0;                    // set by the stack: SMs the prefill GEMM may use (0: all)
   std::string err;
   // kernel timing (moe_profile)
   bool prof_on = false;
@@ -144,6 +154,18 @@ struct moe_layer {
   bool inject_fill = false;            // test hook: the next host-issued fill fails before its copy
   long long inject_wait = 0;           // test hook: wait limit (cycles) of the next forward's expert FFN
   bool last_prefill = false;           // regime of the last moe_forward
+};
+
+// A stack of layers of one geometry that share one slot pool and one LRU
+// table keyed by (layer, expert).
+struct moe_stack {
+  std::vector<moe_layer*> layers;
+  int prefetch = MOE_PREFETCH_AUTO;
+  __nv_bfloat16* hid[2] = {nullptr, nullptr};   // hidden states between layers [max_tokens, d]
+  int* ones = nullptr;                           // [E] ones: a whole layer as a step's counts
+  unsigned long long* pf_stats = nullptr;        // prefetch steps, keys, hits, misses
+  cudaEvent_t ev_pf = nullptr, ev_in = nullptr, ev_route = nullptr;
+  std::string err;
 };
 
 namespace {
@@ -191,7 +213,7 @@ bool is_pow2_float(float v) {
   return std::frexp(v, &ex) == 0.5f;
 }
 
-int check_desc(const moe_layer_desc* d, std::string* why) {
+int check_desc(const moe_layer_desc* d, std::string* why, int max_slots) {
   char buf[256];
   auto bad = [&](const char* m) { *why = m; return MOE_ERR_ARG; };
   if (!d) return bad("descriptor is NULL");
@@ -199,7 +221,11 @@ int check_desc(const moe_layer_desc* d, std::string* why) {
   if (d->k < 1 || d->k > d->E || d->k > kMaxK) return bad("k must be in [1, min(E, 32)]");
   if (d->d_model <= 0 || d->d_model % 128) return bad("d_model must be a positive multiple of 128");
   if (d->d_ff <= 0 || d->d_ff % 128) return bad("d_ff must be a positive multiple of 128");
-  if (d->n_slots < 1 || d->n_slots > d->E) return bad("n_slots must be in [1, E]");
+  if (d->n_slots < 1 || d->n_slots > max_slots) {
+    snprintf(buf, sizeof buf, "n_slots must be in [1, %d]", max_slots);
+    *why = buf;
+    return MOE_ERR_ARG;
+  }
   if (d->fmt != MOE_MXFP4 && d->fmt != MOE_NVFP4) return bad("fmt must be MOE_MXFP4 or MOE_NVFP4");
   if (d->max_tokens < 1) return bad("max_tokens must be >= 1");
   if ((long long)d->max_tokens * (d->k + 1) > (1LL << 30)) return bad("max_tokens * (k+1) too large");
@@ -236,6 +262,10 @@ Geo make_geo(const moe_layer_desc* d, const moe_expert_layout* l) {
   g.off_codes[0] = l->gate_codes; g.off_codes[1] = l->up_codes; g.off_codes[2] = l->down_codes;
   g.off_scales[0] = l->gate_scales; g.off_scales[1] = l->up_scales; g.off_scales[2] = l->down_scales;
   g.off_tscale = l->tensor_scales;
+  g.key0 = 0;
+  g.keys = g.E;
+  g.shb = g.S;
+  g.nbuf = g.S + 1;   // + X once known
   return g;
 }
 
@@ -286,6 +316,7 @@ void release(moe_layer* L) {
   L->pinned_rec = nullptr;
   hfree(L->err_host);
   L->err_host = nullptr;
+  if (!L->owner) return;   // the rest belongs to the stack's layer 0
   if (L->plan) prefill_plan_destroy(L->plan);
   L->plan = nullptr;
   if (L->gplan) gemv_plan_destroy(L->gplan);
@@ -323,11 +354,15 @@ int pointer_kind(const void* p, bool* on_device, int device, const void** mapped
   return MOE_OK;
 }
 
+// Every key of the table resident: then no step can miss or evict (the
+// host mirror is exact while nothing can be evicted; with fewer slots than
+// keys, device-side steps may evict without the host knowing, so the answer
+// is no).
 bool all_resident(const moe_layer* L) {
-  if (L->g.S < L->g.E) return false;
+  if (L->g.S < L->g.keys) return false;
   int n = 0;
-  for (int e : L->mirror) n += e >= 0 ? 1 : 0;
-  return n == L->g.E;
+  for (int e : *L->mir) n += e >= 0 ? 1 : 0;
+  return n == L->g.keys;
 }
 
 // Apply a step record to the host mirror of the slot table.
@@ -335,7 +370,16 @@ void mirror_apply(moe_layer* L, const StepRecord* r) {
   const int U = r->U, S = r->S, E = L->g.E;
   const int* ae = rec_expert(const_cast<StepRecord*>(r));
   const int* as = rec_slot(const_cast<StepRecord*>(r), E);
-  for (int i = std::max(0, U - S); i < U; ++i) L->mirror[as[i]] = ae[i];
+  for (int i = std::max(0, U - S); i < U; ++i) (*L->mir)[as[i]] = L->g.key0 + ae[i];
+}
+
+// A miss of record r left the cache again (its fill failed).
+void mirror_drop_misses(moe_layer* L, const StepRecord* r) {
+  const int E = L->g.E;
+  const int* ae = rec_expert(const_cast<StepRecord*>(r));
+  const int* as = rec_slot(const_cast<StepRecord*>(r), E);
+  for (int q = r->n_hit; q < r->U; ++q)
+    if ((*L->mir)[as[q]] == L->g.key0 + ae[q]) (*L->mir)[as[q]] = -1;
 }
 
 constexpr size_t kProfPairs = 16384;
@@ -396,18 +440,17 @@ const char* moe_last_error(moe_layer_t L) { return L ? L->err.c_str() : "null la
 int moe_expert_layout_for(const moe_layer_desc* desc, moe_expert_layout* out) {
   std::string why;
   if (!out) return MOE_ERR_ARG;
-  int rc = check_desc(desc, &why);
+  int rc = check_desc(desc, &why, desc ? desc->E : 1);
   if (rc) return rc;
   fill_layout(desc, out);
   return MOE_OK;
 }
 
-int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
-  if (!out) return MOE_ERR_ARG;
+// Layer `index` of `n_layers` sharing one pool and one slot table (a lone
+// layer: index 0 of 1).  base: the stack's layer 0, whose pool, table,
+// workspaces, plans, fill stream and events the others use; null for layer 0.
+int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_layers, moe_layer** out) {
   *out = nullptr;
-  std::string why;
-  int rc = check_desc(desc, &why);
-  if (rc) return rc;
   moe_layer* L = new (std::nothrow) moe_layer();
   if (!L) return MOE_ERR_OOM;
   L->desc = *desc;
@@ -426,18 +469,73 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   const size_t Nm = desc->max_tokens;
   // spare buffers: one per miss a step can have beyond the first wave of n_slots
   L->g.X = (int)std::max<long long>(0, std::min<long long>(L->g.E, (long long)Nm * L->g.k) - L->g.S);
+  // pool buffers: the S slots' (slot s starts in buffer s), layer 0's shared
+  // expert (S), the X spares, then the other layers' shared experts
+  L->g.key0 = index * L->g.E;
+  L->g.keys = n_layers * L->g.E;
+  L->g.shb = index == 0 ? L->g.S : L->g.S + L->g.X + index;
+  L->g.nbuf = L->g.S + 1 + L->g.X + (n_layers - 1);
+  L->index = index;
   const Geo& g = L->g;
   const size_t rows = Nm * g.k + (g.has_shared ? Nm : 0);
-  rc = MOE_OK;
+  int rc = MOE_OK;
+  const bool prefill_ok = prefill_shape_ok(g);
+  const size_t prows = Nm * g.k + Nm + 128;   // permuted rows (+ shared) + one tile of padding
 #define MOE_ALLOC(ptr, bytes) \
   if (rc == MOE_OK) rc = dalloc(L, &L->ptr, (bytes))
-  // buffers of the n_slots LRU slots, the shared expert (resident, not LRU), the spares
-  MOE_ALLOC(slots, (size_t)(g.S + 1 + g.X) * g.ebytes);
-  if (rc == MOE_OK) L->shared_w = L->slots + (size_t)g.S * g.ebytes;
+  // this layer's own: router, step record, fused-step words, counters
   MOE_ALLOC(Wr, (size_t)g.E * g.d * 4);
   MOE_ALLOC(Wr_hl, (size_t)g.E * g.d * 6);
   MOE_ALLOC(bias, (size_t)g.E * 4);
-  MOE_ALLOC(slot_of, (size_t)g.E * 4);
+  MOE_ALLOC(rec, rec_dev_bytes(g.E));
+  MOE_ALLOC(gbar, 24);
+  MOE_ALLOC(ready, 8);
+  MOE_ALLOC(stats, 64);
+  if (base) {
+    // the pool, table and workspaces of the stack's layer 0
+    L->owner = false;
+    L->mir = base->mir;
+    L->slots = base->slots;
+    L->slot_of = base->slot_of;
+    L->expert_of = base->expert_of;
+    L->stamp = base->stamp;
+    L->buf = base->buf;
+    L->clock = base->clock;
+    L->logits = base->logits;
+    L->idx = base->idx;
+    L->gates = base->gates;
+    L->xexp = base->xexp;
+    L->counts = base->counts;
+    L->offsets = base->offsets;
+    L->row_of = base->row_of;
+    L->tok_of = base->tok_of;
+    L->perm_scratch = base->perm_scratch;
+    L->h = base->h;
+    L->hmax = base->hmax;
+    L->O = base->O;
+    L->x_stage = base->x_stage;
+    L->y_stage = base->y_stage;
+    L->list_cap = base->list_cap;
+    L->list_dev = base->list_dev;
+    L->rcounter = base->rcounter;
+    L->step_trace = base->step_trace;
+    L->xq_codes = base->xq_codes;
+    L->xq_scales = base->xq_scales;
+    L->hq_codes = base->hq_codes;
+    L->hq_scales = base->hq_scales;
+    L->tiles = base->tiles;
+    L->n_tiles = base->n_tiles;
+    L->gplan = base->gplan;
+    L->plan = base->plan;
+    L->fill = base->fill;
+    for (int i = 0; i < kMissChunks; ++i) L->ev_chunk[i] = base->ev_chunk[i];
+    L->ev_route = base->ev_route;
+    L->ev_fill = base->ev_fill;
+  }
+  if (rc == MOE_OK && !base) {
+  // buffers of the n_slots LRU slots, the shared experts (resident, not LRU), the spares
+  MOE_ALLOC(slots, (size_t)g.nbuf * g.ebytes);
+  MOE_ALLOC(slot_of, (size_t)g.keys * 4);
   MOE_ALLOC(expert_of, (size_t)g.S * 4);
   MOE_ALLOC(stamp, (size_t)g.S * 8);
   MOE_ALLOC(buf, (size_t)(g.S + g.X) * 4);
@@ -451,7 +549,6 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   MOE_ALLOC(row_of, Nm * g.k * 4);
   MOE_ALLOC(tok_of, Nm * g.k * 4);
   MOE_ALLOC(perm_scratch, permute_scratch_bytes(g, (int)Nm));
-  MOE_ALLOC(rec, rec_dev_bytes(g.E));
   MOE_ALLOC(h, rows * g.f * 8);   // decode: scaled W_g x and W_u x per row
   MOE_ALLOC(hmax, rows * (g.f / 64) * 8);
   MOE_ALLOC(O, rows * g.d * 4);
@@ -460,12 +557,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
   L->list_cap = (int)std::max<size_t>(Nm * g.k, (size_t)g.E);
   MOE_ALLOC(list_dev, (size_t)L->list_cap * 4);
   MOE_ALLOC(rcounter, 16);
-  MOE_ALLOC(gbar, 24);
-  MOE_ALLOC(ready, 8);
   MOE_ALLOC(step_trace, (size_t)std::max(L->num_sms, 1) * kStepMarks * 8);
-  MOE_ALLOC(stats, 64);
-  const bool prefill_ok = prefill_shape_ok(g);
-  const size_t prows = Nm * g.k + Nm + 128;   // permuted rows (+ shared) + one tile of padding
   if (prefill_ok) {
     MOE_ALLOC(xq_codes, prows * g.d / 2);
     MOE_ALLOC(xq_scales, prows * (g.d / g.blk));
@@ -474,7 +566,9 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     MOE_ALLOC(tiles, prefill_tile_bytes(g, (int)Nm));
     MOE_ALLOC(n_tiles, 16);
   }
+  }
 #undef MOE_ALLOC
+  if (rc == MOE_OK) L->shared_w = L->slots + (size_t)g.shb * g.ebytes;
   if (rc == MOE_OK) {
     void* eh = nullptr;
     rc = halloc(L, &eh, 16);
@@ -485,11 +579,11 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     }
     if (rc == MOE_OK) *L->err_host = 0;
   }
-  if (rc == MOE_OK) {
+  if (rc == MOE_OK && !base) {
     L->gplan = gemv_plan_create(g, L->slots);
     if (!gemv_plan_ready(L->gplan)) rc = MOE_ERR_CUDA;   // tensor-map encoding failed
   }
-  if (rc == MOE_OK && prefill_ok) {
+  if (rc == MOE_OK && prefill_ok && !base) {
     L->plan = prefill_plan_create(g, L->slots, L->xq_codes, prows, L->hq_codes);
     if (!prefill_plan_ready(L->plan)) {
       prefill_plan_destroy(L->plan);
@@ -507,7 +601,7 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     }
     L->rec_host_dev = static_cast<StepRecord*>(dp);
   }
-  if (rc == MOE_OK) {
+  if (rc == MOE_OK && !base) {
     bool sok = true;
     // the fill stream has the highest priority: a fill kernel's CTAs are
     // dispatched before expert-GEMV CTAs waiting for SMs
@@ -524,23 +618,25 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     }
   }
   if (rc == MOE_OK) {
-    // empty cache, zero bias, unit tensor scales for the shared expert slot
-    bool ok = cudaMemset(L->slot_of, 0xff, (size_t)g.E * 4) == cudaSuccess &&
-              cudaMemset(L->expert_of, 0xff, (size_t)g.S * 4) == cudaSuccess &&
-              cudaMemset(L->stamp, 0, (size_t)g.S * 8) == cudaSuccess &&
-              cudaMemset(L->clock, 0, 8) == cudaSuccess &&
-              cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
+    // zero bias, empty record and counters; the owner: empty cache
+    bool ok = cudaMemset(L->bias, 0, (size_t)g.E * 4) == cudaSuccess &&
               cudaMemset(L->rec, 0, rec_dev_bytes(g.E)) == cudaSuccess &&
-              cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
               cudaMemset(L->gbar, 0, 24) == cudaSuccess &&
               cudaMemset(L->ready, 0, 8) == cudaSuccess &&
               cudaMemset(L->stats, 0, 64) == cudaSuccess;
-    // slot s in buffer s; the spares after the shared expert's buffer S
-    std::vector<int> b0(g.S + g.X);
-    for (int s = 0; s < g.S; ++s) b0[s] = s;
-    for (int j = 0; j < g.X; ++j) b0[g.S + j] = g.S + 1 + j;
-    ok = ok && (b0.empty() || cudaMemcpy(L->buf, b0.data(), b0.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess) &&
-         cudaDeviceSynchronize() == cudaSuccess;
+    if (!base) {
+      ok = ok && cudaMemset(L->slot_of, 0xff, (size_t)g.keys * 4) == cudaSuccess &&
+           cudaMemset(L->expert_of, 0xff, (size_t)g.S * 4) == cudaSuccess &&
+           cudaMemset(L->stamp, 0, (size_t)g.S * 8) == cudaSuccess &&
+           cudaMemset(L->clock, 0, 8) == cudaSuccess &&
+           cudaMemset(L->rcounter, 0, 16) == cudaSuccess;
+      // slot s in buffer s; the spares after the shared expert's buffer S
+      std::vector<int> b0(g.S + g.X);
+      for (int s = 0; s < g.S; ++s) b0[s] = s;
+      for (int j = 0; j < g.X; ++j) b0[g.S + j] = g.S + 1 + j;
+      ok = ok && (b0.empty() || cudaMemcpy(L->buf, b0.data(), b0.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess);
+    }
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
       cudaGetLastError();
       rc = MOE_ERR_CUDA;
@@ -551,13 +647,26 @@ int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
     delete L;
     return rc;
   }
-  L->mirror.assign(g.S, -1);
+  if (!base) {
+    L->mirror_own.assign(g.S, -1);
+    L->mir = &L->mirror_own;
+  }
   *out = L;
   return MOE_OK;
 }
 
+int moe_layer_create(const moe_layer_desc* desc, moe_layer_t* out) {
+  if (!out) return MOE_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  const int rc = check_desc(desc, &why, desc ? desc->E : 1);
+  if (rc) return rc;
+  return create_layer(desc, nullptr, 0, 1, out);
+}
+
 int moe_layer_destroy(moe_layer_t L) {
   if (!L) return MOE_ERR_ARG;
+  if (L->stack) return fail(L, MOE_ERR_STATE, "layer %d belongs to a stack: destroy the stack", L->index);
   cudaDeviceSynchronize();
   release(L);
   delete L;
@@ -630,9 +739,10 @@ int moe_cache_install(moe_layer_t L, int expert, int slot, void* stream) {
                               L->host_pool + (size_t)expert * L->g.ebytes, L->g.ebytes,
                               cudaMemcpyHostToDevice, st));
   MOE_CUDA(L, launch_lru_install(L->g, expert, slot, L->slot_of, L->expert_of, L->stamp, L->clock, st));
+  const int key = L->g.key0 + expert;
   for (int s = 0; s < L->g.S; ++s)
-    if (L->mirror[s] == expert) L->mirror[s] = -1;
-  L->mirror[slot] = expert;
+    if ((*L->mir)[s] == key) (*L->mir)[s] = -1;
+  (*L->mir)[slot] = key;
   return MOE_OK;
 }
 
@@ -648,6 +758,7 @@ int moe_lru_get_state(moe_layer_t L, int* expert_of_slot, uint64_t* stamp, uint6
 
 int moe_cache_resize(moe_layer_t L, int n_slots, void* stream) {
   if (!L) return MOE_ERR_ARG;
+  if (L->stack) return fail(L, MOE_ERR_UNSUPPORTED, "a stack's shared pool is not resized through one layer");
   const Geo g0 = L->g;
   if (n_slots < 1 || n_slots > g0.E) return fail(L, MOE_ERR_ARG, "n_slots must be in [1, E = %d]", g0.E);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -675,7 +786,9 @@ int moe_cache_resize(moe_layer_t L, int n_slots, void* stream) {
   Geo g1 = g0;
   g1.S = S1;
   g1.X = (int)std::max<long long>(0, std::min<long long>(g1.E, (long long)L->desc.max_tokens * g1.k) - S1);
-  const size_t nb1 = (size_t)g1.S + 1 + g1.X;
+  g1.shb = S1;
+  g1.nbuf = S1 + 1 + g1.X;
+  const size_t nb1 = (size_t)g1.nbuf;
   uint8_t* pool = nullptr;
   int *eo_d = nullptr, *buf_d = nullptr;
   unsigned long long* st_d = nullptr;
@@ -758,14 +871,14 @@ int moe_cache_resize(moe_layer_t L, int n_slots, void* stream) {
       L->plan = nullptr;
     }
   }
-  L->mirror = eo1;
+  *L->mir = eo1;
   return MOE_OK;
 }
 
 int moe_lru_set_state(moe_layer_t L, const int* expert_of_slot, const uint64_t* stamp, uint64_t clock) {
   if (!L) return MOE_ERR_ARG;
   if (!expert_of_slot || !stamp) return fail(L, MOE_ERR_ARG, "NULL state array");
-  const int E = L->g.E, S = L->g.S;
+  const int E = L->g.keys, S = L->g.S;   // a stack's table holds keys l E + e
   std::vector<int> slot_of(E, -1);
   for (int s = 0; s < S; ++s) {
     const int e = expert_of_slot[s];
@@ -781,7 +894,7 @@ int moe_lru_set_state(moe_layer_t L, const int* expert_of_slot, const uint64_t* 
   MOE_CUDA(L, cudaMemcpy(L->slot_of, slot_of.data(), (size_t)E * 4, cudaMemcpyHostToDevice));
   MOE_CUDA(L, cudaMemcpy(L->stamp, stamp, (size_t)S * 8, cudaMemcpyHostToDevice));
   MOE_CUDA(L, cudaMemcpy(L->clock, &clock, 8, cudaMemcpyHostToDevice));
-  L->mirror.assign(expert_of_slot, expert_of_slot + S);
+  L->mir->assign(expert_of_slot, expert_of_slot + S);
   return MOE_OK;
 }
 
@@ -824,8 +937,7 @@ int moe_lru_touch(moe_layer_t L, const int* experts, int n, int* slot_of_out, in
       if (ce != cudaSuccess) {
         cudaGetLastError();
         mirror_apply(L, r);
-        for (int q = r->n_hit; q < r->U; ++q)
-          if (L->mirror[as[q]] == ae[q]) L->mirror[as[q]] = -1;
+        mirror_drop_misses(L, r);
         MOE_CUDA(L, launch_lru_drop_misses(g, L->rec, L->slot_of, L->expert_of, st));
         MOE_CUDA(L, cudaStreamSynchronize(st));
         return fail(L, MOE_ERR_FILL, "fill of expert %d could not be issued (%s); the %d misses were dropped "
@@ -901,7 +1013,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     L->gbar_base = 0;
     return fail(L, MOE_ERR_TIMEOUT, "a wait inside an earlier step's kernel timed out; its output is invalid");
   }
-  const bool resident = all_resident(L);
+  // assume_resident: a stack prefetched every expert of this layer just before
+  const bool resident = L->assume_resident || all_resident(L);
   if (!resident && !L->host_pool)
     return fail(L, MOE_ERR_NOT_INSTALLED, "not every expert is resident and no host pool is registered");
   bool x_dev = false, y_dev = false;
@@ -1049,6 +1162,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
                                   hrec, seq, st));
     prof_end(pe, st);
     L->launches += 1;
+    if (L->ev_after_route) MOE_CUDA(L, cudaEventRecord(L->ev_after_route, st));
   } else {
     pe = prof_begin(L, MOE_PROF_PERMUTE, st);
     MOE_CUDA(L, launch_permute(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
@@ -1060,6 +1174,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
                                 L->buf, L->rec, L->stats, hrec, seq, st));
     prof_end(pe, st);
     L->launches += 1;
+    if (L->ev_after_route) MOE_CUDA(L, cudaEventRecord(L->ev_after_route, st));
   }
   const bool dev_fill = !resident && fmode == MOE_FILL_DEVICE;
   if (!resident) MOE_CUDA(L, cudaEventRecord(L->ev_route, st));
@@ -1108,7 +1223,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     if (prefill) {
       ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, N, a.mode, a.with_shared,
                                 L->tiles, L->n_tiles, L->slots, L->xq_scales, L->hq_codes,
-                                L->hq_scales, L->O, gx, gh, L->err_dev, L->num_sms, st, evp);
+                                L->hq_scales, L->O, gx, gh, L->err_dev, L->gemm_sms > 0 ? L->gemm_sms : L->num_sms,
+                                st, evp);
       L->launches += 3;
     } else {
       ce = launch_gemv_decode(g, L->gplan, a, xd, L->xexp, L->h, L->O, n_ent, gemv_sms, st, evp, phases);
@@ -1216,8 +1332,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
             // hits' expert FFN finish on their own; y is not written
             cudaGetLastError();
             mirror_apply(L, r);
-            for (int q = n_hit; q < U; ++q)
-              if (L->mirror[as[q]] == ae[q]) L->mirror[as[q]] = -1;
+            mirror_drop_misses(L, r);
             MOE_CUDA(L, launch_lru_drop_misses(g, L->rec, L->slot_of, L->expert_of, st));
             return fail(L, MOE_ERR_FILL, "fill of expert %d could not be issued (%s); the step's %d misses were "
                         "dropped from the cache and y was not written", ae[i], cudaGetErrorString(ce), U - n_hit);
@@ -1468,6 +1583,242 @@ int moe_debug_actquant(moe_layer_t L, const float* v, int rows, int K, uint8_t* 
   const float gs = which ? L->desc.act_scale_h : L->desc.act_scale_x;
   MOE_CUDA(L, launch_actquant(L->g, v, rows, K, codes, scales, L->g.fmt == MOE_NVFP4 ? gs : 1.0f,
                               static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+
+// ---------------------------------------------------------------- stacks
+
+const char* moe_stack_last_error(moe_stack_t K) { return K ? K->err.c_str() : "null stack"; }
+
+static int stack_fail(moe_stack* K, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  K->err = buf;
+  return code;
+}
+
+static void stack_free(moe_stack* K) {
+  cudaDeviceSynchronize();
+  for (int l = (int)K->layers.size() - 1; l >= 0; --l) {
+    release(K->layers[l]);
+    delete K->layers[l];
+  }
+  K->layers.clear();
+  if (K->ev_pf) cudaEventDestroy(K->ev_pf);
+  if (K->ev_in) cudaEventDestroy(K->ev_in);
+  if (K->ev_route) cudaEventDestroy(K->ev_route);
+  delete K;
+}
+
+int moe_stack_create(const moe_layer_desc* desc, int n_layers, moe_stack_t* out) {
+  if (!out) return MOE_ERR_ARG;
+  *out = nullptr;
+  if (!desc || n_layers < 1 || n_layers > kMaxStackLayers) return MOE_ERR_ARG;
+  std::string why;
+  const long long keys = (long long)n_layers * desc->E;
+  int rc = check_desc(desc, &why, (int)std::min<long long>(keys, kMaxE));
+  if (rc) return rc;
+  moe_stack* K = new (std::nothrow) moe_stack();
+  if (!K) return MOE_ERR_OOM;
+  for (int l = 0; l < n_layers && rc == MOE_OK; ++l) {
+    moe_layer* L = nullptr;
+    rc = create_layer(desc, l ? K->layers[0] : nullptr, l, n_layers, &L);
+    if (rc == MOE_OK) {
+      L->stack = K;
+      K->layers.push_back(L);
+    }
+  }
+  if (rc == MOE_OK) {
+    moe_layer* L0 = K->layers[0];
+    const Geo& g = L0->g;
+    const size_t hb = (size_t)desc->max_tokens * g.d * 2;
+    rc = dalloc(L0, &K->hid[0], hb);
+    if (rc == MOE_OK) rc = dalloc(L0, &K->hid[1], hb);
+    if (rc == MOE_OK) rc = dalloc(L0, &K->ones, (size_t)g.E * 4);
+    if (rc == MOE_OK) rc = dalloc(L0, &K->pf_stats, 64);
+    if (rc == MOE_OK) {
+      std::vector<int> one(g.E, 1);
+      if (cudaMemcpy(K->ones, one.data(), (size_t)g.E * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+          cudaMemset(K->pf_stats, 0, 64) != cudaSuccess ||
+          cudaEventCreateWithFlags(&K->ev_pf, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&K->ev_in, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&K->ev_route, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        rc = MOE_ERR_CUDA;
+      }
+    }
+  }
+  if (rc != MOE_OK) {
+    stack_free(K);
+    return rc;
+  }
+  *out = K;
+  return MOE_OK;
+}
+
+int moe_stack_destroy(moe_stack_t K) {
+  if (!K) return MOE_ERR_ARG;
+  for (moe_layer* L : K->layers) L->stack = nullptr;
+  stack_free(K);
+  return MOE_OK;
+}
+
+int moe_stack_layer(moe_stack_t K, int l, moe_layer_t* out) {
+  if (!K || !out) return MOE_ERR_ARG;
+  if (l < 0 || l >= (int)K->layers.size())
+    return stack_fail(K, MOE_ERR_ARG, "layer %d outside [0, %d)", l, (int)K->layers.size());
+  *out = K->layers[l];
+  return MOE_OK;
+}
+
+int moe_stack_set_prefetch(moe_stack_t K, int mode) {
+  if (!K) return MOE_ERR_ARG;
+  const Geo& g = K->layers[0]->g;
+  if (mode != MOE_PREFETCH_AUTO && mode != MOE_PREFETCH_NONE && mode != MOE_PREFETCH_SERIAL &&
+      mode != MOE_PREFETCH_OVERLAP)
+    return stack_fail(K, MOE_ERR_ARG, "unknown prefetch mode %d", mode);
+  if (mode == MOE_PREFETCH_SERIAL && g.S < g.E)
+    return stack_fail(K, MOE_ERR_UNSUPPORTED, "a whole-layer prefetch needs n_slots >= E (%d < %d)", g.S, g.E);
+  if (mode == MOE_PREFETCH_OVERLAP && g.S < 2 * g.E)
+    return stack_fail(K, MOE_ERR_UNSUPPORTED, "an overlapped prefetch needs n_slots >= 2 E (%d < %d)", g.S, 2 * g.E);
+  K->prefetch = mode;
+  return MOE_OK;
+}
+
+int moe_stack_prefetch_stats(moe_stack_t K, uint64_t* out4) {
+  if (!K || !out4) return MOE_ERR_ARG;
+  moe_layer* L0 = K->layers[0];
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(out4, K->pf_stats, 32, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return stack_fail(K, MOE_ERR_CUDA, "reading the prefetch counters failed");
+  }
+  (void)L0;
+  return MOE_OK;
+}
+
+// The whole of layer m as one step of the shared table (every expert accessed,
+// hits first, misses ascending), then its misses copied from the layer's host
+// pool by kFillSms CTAs; all on stream st.
+static int stack_prefetch(moe_stack* K, int m, cudaStream_t st) {
+  moe_layer* M = K->layers[m];
+  const Geo& g = M->g;
+  cudaError_t e = launch_lru_step(g, K->ones, nullptr, M->slot_of, M->expert_of, M->stamp, M->clock, M->buf, M->rec,
+                                  K->pf_stats, nullptr, 0, st);
+  for (int c = 0; e == cudaSuccess && c < miss_chunks(g.E); ++c)
+    e = launch_fill_sm(g, M->rec, c, M->pool_dev, M->slots, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return stack_fail(K, MOE_ERR_CUDA, "prefetch of layer %d: %s", m, cudaGetErrorString(e));
+  }
+  M->launches += 1 + miss_chunks(g.E);
+  return MOE_OK;
+}
+
+int moe_stack_forward(moe_stack_t K, const void* x, int N, void* y, void* stream, int regime,
+                      moe_forward_info* info) {
+  if (!K) return MOE_ERR_ARG;
+  const int nl = (int)K->layers.size();
+  moe_layer* L0 = K->layers[0];
+  const Geo& g = L0->g;
+  if (info) {
+    std::memset(info, 0, sizeof *info);
+    info->n_tokens = N;
+  }
+  if (N < 0 || N > L0->desc.max_tokens)
+    return stack_fail(K, MOE_ERR_ARG, "N = %d outside [0, max_tokens = %d]", N, L0->desc.max_tokens);
+  if (N == 0) return MOE_OK;
+  if (!x || !y) return stack_fail(K, MOE_ERR_ARG, "x or y is NULL");
+  if (regime != MOE_REGIME_AUTO && regime != MOE_REGIME_DECODE && regime != MOE_REGIME_PREFILL)
+    return stack_fail(K, MOE_ERR_ARG, "unknown regime %d", regime);
+  const bool prefill = regime == MOE_REGIME_PREFILL || (regime == MOE_REGIME_AUTO && N > 64 && L0->plan);
+  if (prefill && !L0->plan)
+    return stack_fail(K, MOE_ERR_UNSUPPORTED, "the prefill regime needs d_model and d_ff multiples of 256");
+  int mode = MOE_PREFETCH_NONE;
+  if (prefill) {
+    mode = K->prefetch;
+    if (mode == MOE_PREFETCH_AUTO)
+      mode = g.S >= 2 * g.E ? MOE_PREFETCH_OVERLAP : g.S >= g.E ? MOE_PREFETCH_SERIAL : MOE_PREFETCH_NONE;
+    if (mode != MOE_PREFETCH_NONE)
+      for (moe_layer* M : K->layers)
+        if (!M->pool_dev)
+          return stack_fail(K, MOE_ERR_NOT_INSTALLED, "layer %d has no device-addressable host pool", M->index);
+  }
+  const int reg = prefill ? MOE_REGIME_PREFILL : MOE_REGIME_DECODE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t fs = L0->fill;
+  int launches = 0, fused = 0;
+  auto fwd = [&](int l, const void* in, void* outp) -> int {
+    moe_layer* M = K->layers[l];
+    moe_forward_info fi{};
+    const int rc = moe_forward(M, in, N, outp, stream, reg, &fi);
+    if (rc) return stack_fail(K, rc, "layer %d: %s", l, M->err.c_str());
+    launches += fi.n_launches;
+    fused += fi.fused_step;
+    return MOE_OK;
+  };
+  auto cuda_k = [&](cudaError_t e, const char* what) -> int {
+    if (e == cudaSuccess) return MOE_OK;
+    cudaGetLastError();
+    return stack_fail(K, MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  };
+  int rc = MOE_OK;
+  if (mode != MOE_PREFETCH_NONE) {
+    // layer 0's experts, after the caller's earlier work on st
+    L0->launches = 0;
+    if ((rc = cuda_k(cudaEventRecord(K->ev_in, st), "cudaEventRecord"))) return rc;
+    if ((rc = cuda_k(cudaStreamWaitEvent(fs, K->ev_in, 0), "cudaStreamWaitEvent"))) return rc;
+    if ((rc = stack_prefetch(K, 0, fs))) return rc;
+    launches += L0->launches;
+    if ((rc = cuda_k(cudaEventRecord(K->ev_pf, fs), "cudaEventRecord"))) return rc;
+    if ((rc = cuda_k(cudaStreamWaitEvent(st, K->ev_pf, 0), "cudaStreamWaitEvent"))) return rc;
+  }
+  const void* in = x;
+  for (int l = 0; l < nl; ++l) {
+    void* outp = l == nl - 1 ? y : static_cast<void*>(K->hid[l & 1]);
+    moe_layer* M = K->layers[l];
+    const bool ov = mode == MOE_PREFETCH_OVERLAP && l + 1 < nl;
+    M->assume_resident = mode != MOE_PREFETCH_NONE;
+    M->ev_after_route = ov ? K->ev_route : nullptr;
+    // the prefill GEMM leaves the fill kernels' SMs free while the next
+    // layer streams in
+    M->gemm_sms = ov ? M->num_sms - kFillSms : 0;
+    rc = fwd(l, in, outp);
+    M->assume_resident = false;
+    M->ev_after_route = nullptr;
+    M->gemm_sms = 0;
+    if (rc) return rc;
+    if (mode != MOE_PREFETCH_NONE && l + 1 < nl) {
+      moe_layer* Mn = K->layers[l + 1];
+      Mn->launches = 0;
+      if (ov) {
+        // layer l + 1 streams in while layer l computes: its table step
+        // follows layer l's (its experts are the most recent, so with
+        // n_slots >= 2 E none of them is evicted), its copies run on the fill
+        // SMs, and layer l + 1 starts once they landed
+        if ((rc = cuda_k(cudaStreamWaitEvent(fs, K->ev_route, 0), "cudaStreamWaitEvent"))) return rc;
+        if ((rc = stack_prefetch(K, l + 1, fs))) return rc;
+        if ((rc = cuda_k(cudaEventRecord(K->ev_pf, fs), "cudaEventRecord"))) return rc;
+        if ((rc = cuda_k(cudaStreamWaitEvent(st, K->ev_pf, 0), "cudaStreamWaitEvent"))) return rc;
+      } else {
+        // after layer l on the caller's stream
+        if ((rc = stack_prefetch(K, l + 1, st))) return rc;
+      }
+      launches += Mn->launches;
+    }
+    in = outp;
+  }
+  if (info) {
+    info->regime = reg;
+    info->n_distinct = info->n_hits = info->n_misses = -1;
+    info->n_waves = 1;
+    info->n_launches = launches;
+    info->fused_step = fused;
+  }
   return MOE_OK;
 }
 

@@ -108,6 +108,13 @@ inline size_t rec_dev_bytes(int E) { return ((rec_bytes(E) + 15) & ~size_t(15)) 
 struct Geo {
   int E, k, d, f, S, fmt, has_shared, norm_topk, has_bias;
   int X;                       // spare buffers: the pool holds S + 1 + X (the shared expert's is S)
+  // The slot table is keyed: key = key0 + expert.  A lone layer has key0 = 0
+  // and keys = E; layer l of a stack of L layers sharing one pool and one
+  // table has key0 = l E and keys = L E (slot_of has `keys` entries,
+  // expert_of holds keys).
+  int key0, keys;
+  int shb;                     // the pool buffer of this layer's shared expert (S for a lone layer)
+  int nbuf;                    // buffers in the pool (S + 1 + X, plus one per further stack layer)
   int blk;                     // 32 (MXFP4) or 16 (NVFP4)
   size_t ebytes;               // padded bytes of one expert
   size_t off_codes[3], off_scales[3], off_tscale;

@@ -256,7 +256,7 @@ bool gemv_shape_ok(const Geo& g) {
 
 GemvPlan* gemv_plan_create(const Geo& g, const uint8_t* slots) {
   GemvPlan* pl = new GemvPlan();
-  const int ns = g.S + 1 + g.X;   // LRU slots' buffers, the shared expert's, the spares
+  const int ns = g.nbuf;   // LRU slots' buffers, the shared expert's, the spares (+ a stack's other shared experts)
   pl->ready = make_box_map(&pl->w[0], slots + g.off_codes[0], g.d / 2, g.f, ns, g.ebytes) &&
               make_box_map(&pl->w[1], slots + g.off_codes[1], g.d / 2, g.f, ns, g.ebytes) &&
               make_box_map(&pl->w[2], slots + g.off_codes[2], g.f / 2, g.d, ns, g.ebytes);

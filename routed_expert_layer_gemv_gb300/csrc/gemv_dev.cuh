@@ -158,7 +158,7 @@ MOE_DEV bool get_entry(const Geo& g, const GemvArgs& a, const EntryTable& T, int
     return slot_ok && out.nrows > 0 && out.row0 >= 0 && out.row0 + out.nrows <= a.N * g.k;
   }
   if (T.shared && ent == T.nr) {
-    out.slot = g.S;
+    out.slot = g.shb;
     out.row0 = a.N * g.k;
     out.nrows = a.N;
     out.shared = 1;

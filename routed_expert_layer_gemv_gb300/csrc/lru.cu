@@ -36,20 +36,21 @@ using lru::lru_park;
 
 __global__ void __launch_bounds__(kLruThreads)
 lru_step_kernel(const int* __restrict__ counts, const int* __restrict__ offsets, int E, int S, int X,
-                int* __restrict__ slot_of, int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
+                int key0, int keys, int* __restrict__ slot_of, int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                 unsigned long long* __restrict__ clock, int* __restrict__ buf, StepRecord* __restrict__ rec,
                 unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq) {
   __shared__ LruSmem m;
-  lru_park(lru_load(E, S, X, slot_of, expert_of, stamp, clock, buf), E, S, X, m);
+  lru_park(lru_load(E, S, X, key0, slot_of, expert_of, stamp, clock, buf), E, S, X, m);
   __syncthreads();
-  lru::lru_body<kLruThreads>(counts, offsets, nullptr, E, S, X, slot_of, expert_of, stamp, clock, buf, rec, stats, host_rec, seq,
-           m);
+  lru::lru_body<kLruThreads>(counts, offsets, nullptr, E, S, X, key0, keys, slot_of, expert_of, stamp, clock, buf,
+                             rec, stats, host_rec, seq, m);
 }
 
 // Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
 // (as perm_single in permute.cu), then the LRU step on the counts it found.
 __global__ void __launch_bounds__(kLruThreads)
-route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X, int* __restrict__ counts,
+route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X, int key0, int keys,
+                  int* __restrict__ counts,
                   int* __restrict__ offsets, int* __restrict__ row_of, int* __restrict__ tok_of,
                   int* __restrict__ slot_of, int* __restrict__ expert_of,
                   unsigned long long* __restrict__ stamp, unsigned long long* __restrict__ clock,
@@ -65,7 +66,7 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
   // the table was last written by the previous step's tail, which finished
   // before the router began: its loads go out before waiting for the router
   pdl_trigger();
-  const LruRegs lr = lru_load(E, S, X, slot_of, expert_of, stamp, clock, buf);
+  const LruRegs lr = lru_load(E, S, X, key0, slot_of, expert_of, stamp, clock, buf);
   pdl_wait();
   perm::stage_rows(idx, N, k, 0, rows);
   lru_park(lr, E, S, X, m);
@@ -93,9 +94,11 @@ route_tail_kernel(const int* __restrict__ idx, int N, int k, int E, int S, int X
     }
   }
   __syncthreads();
-  lru::lru_body<kLruThreads>(cnt, off, cm, E, S, X, slot_of, expert_of, stamp, clock, buf, rec, stats, host_rec, seq, m);
+  lru::lru_body<kLruThreads>(cnt, off, cm, E, S, X, key0, keys, slot_of, expert_of, stamp, clock, buf, rec, stats,
+                             host_rec, seq, m);
 }
 
+// Key `expert` (a key of the table) into `slot`, most recently used.
 __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expert_of,
                                    unsigned long long* stamp, unsigned long long* clock) {
   const int prev = slot_of[expert];
@@ -109,17 +112,17 @@ __global__ void lru_install_kernel(int expert, int slot, int* slot_of, int* expe
   stamp[slot] = c;
 }
 
-__global__ void lru_drop_misses_kernel(const StepRecord* __restrict__ rec, int E, int S, int* slot_of,
+__global__ void lru_drop_misses_kernel(const StepRecord* __restrict__ rec, int E, int S, int key0, int* slot_of,
                                        int* expert_of) {
   const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
   const int* ae = rec_expert(const_cast<StepRecord*>(rec));
   for (int i = nh + (int)threadIdx.x; i < U; i += blockDim.x) {
     const int e = ae[i];
     if (e < 0 || e >= E) continue;
-    const int s = slot_of[e];
+    const int s = slot_of[key0 + e];
     if (s >= 0 && s < S) {
       expert_of[s] = -1;
-      slot_of[e] = -1;
+      slot_of[key0 + e] = -1;
     }
   }
 }
@@ -139,8 +142,8 @@ cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets,
                             int* expert_of, unsigned long long* stamp, unsigned long long* clock,
                             int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
                             unsigned long long seq, cudaStream_t st) {
-  lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, offsets, g.E, g.S, g.X, slot_of, expert_of, stamp,
-                                             clock, buf, rec, stats, host_rec, seq);
+  lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, offsets, g.E, g.S, g.X, g.key0, g.keys, slot_of, expert_of,
+                                             stamp, clock, buf, rec, stats, host_rec, seq);
   return cudaGetLastError();
 }
 
@@ -153,21 +156,21 @@ cudaError_t launch_route_tail(const Geo& g, const int* idx, int N, int* counts, 
                       (size_t)perm::kTokPerBlock * g.k * 4 + (size_t)perm::kTokPerBlock * ((g.E + 31) / 32) * 4;
   cudaError_t e = ensure_smem_limit((const void*)route_tail_kernel, 64 * 1024);
   if (e != cudaSuccess) return e;
-  return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, g.X, counts,
+  return launch_pdl(route_tail_kernel, dim3(1), dim3(kLruThreads), smem, st, idx, N, g.k, g.E, g.S, g.X, g.key0,
+                    g.keys, counts,
                     offsets, row_of, tok_of, slot_of, expert_of, stamp, clock, buf, rec, stats, host_rec, seq);
 }
 
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
                                unsigned long long* stamp, unsigned long long* clock,
                                cudaStream_t st) {
-  (void)g;
-  lru_install_kernel<<<1, 1, 0, st>>>(expert, slot, slot_of, expert_of, stamp, clock);
+  lru_install_kernel<<<1, 1, 0, st>>>(g.key0 + expert, slot, slot_of, expert_of, stamp, clock);
   return cudaGetLastError();
 }
 
 cudaError_t launch_lru_drop_misses(const Geo& g, const StepRecord* rec, int* slot_of, int* expert_of,
                                    cudaStream_t st) {
-  lru_drop_misses_kernel<<<1, 256, 0, st>>>(rec, g.E, g.S, slot_of, expert_of);
+  lru_drop_misses_kernel<<<1, 256, 0, st>>>(rec, g.E, g.S, g.key0, slot_of, expert_of);
   return cudaGetLastError();
 }
 

@@ -67,17 +67,18 @@ struct LruSmem {
 
 // The table's state, read once per step: every thread issues its loads
 // together (one memory round trip) and parks them in shared memory; callers
-// put other independent loads between lru_load and lru_park.
+// put other independent loads between lru_load and lru_park.  slot_of is
+// indexed by key; the layer's experts are keys key0 .. key0 + E - 1.
 struct LruRegs {
   int so, eo, buf;
   unsigned long long st, clk;
 };
-MOE_DEV LruRegs lru_load(int E, int S, int X, const int* __restrict__ slot_of, const int* __restrict__ expert_of,
-                         const unsigned long long* __restrict__ stamp,
+MOE_DEV LruRegs lru_load(int E, int S, int X, int key0, const int* __restrict__ slot_of,
+                         const int* __restrict__ expert_of, const unsigned long long* __restrict__ stamp,
                          const unsigned long long* __restrict__ clock, const int* __restrict__ buf) {
   const int t = threadIdx.x;
   LruRegs r;
-  r.so = t < E ? slot_of[t] : -1;
+  r.so = t < E ? slot_of[key0 + t] : -1;
   r.eo = t < S ? expert_of[t] : -1;
   r.buf = t < S + X ? buf[t] : -1;
   r.st = t < S ? stamp[t] : 0ull;
@@ -92,12 +93,14 @@ MOE_DEV void lru_park(const LruRegs& r, int E, int S, int X, LruSmem& m) {
   if (t == 0) m.clk = r.clk;
 }
 
-// One step of the table (blockDim.x == NT, E <= NT) on the state parked in
-// m (the caller synchronises after lru_park).  counts may live in shared or
-// global memory.
+// One step of the table (blockDim.x == NT, E <= NT, S + X <= NT) on the
+// state parked in m (the caller synchronises after lru_park).  counts may
+// live in shared or global memory.  The layer's expert e is key key0 + e of
+// a table of `keys` keys (slot_of [keys], expert_of holds keys); the record
+// names the layer's experts (e) and, as evicted, keys.
 template <int NT>
 MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, int E, int S, int X,
-                      int* __restrict__ slot_of,
+                      int key0, int keys, int* __restrict__ slot_of,
                       int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                       unsigned long long* __restrict__ clock, int* __restrict__ buf, StepRecord* __restrict__ rec,
                       unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq,
@@ -105,8 +108,8 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
   const int tid = threadIdx.x;
   const unsigned long long clk = m.clk;
 
-  // hits / misses over experts (E <= 1024: one expert per thread) and the
-  // free / stale slots (S <= E: one slot per thread), counted by one scan of
+  // hits / misses over experts (E <= NT: one expert per thread) and the
+  // free / stale slots (S <= NT: one slot per thread), counted by one scan of
   // three packed 21-bit counters
   const int e = tid;
   const bool inU = e < E && counts[e] > 0;
@@ -118,8 +121,9 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
   unsigned long long st = 0;
   if (s < S) {
     old = m.eo[s];
-    fre = old < 0 || old >= E;
-    stale = !fre && counts[old] == 0;
+    fre = old < 0 || old >= keys;
+    // another layer's key, or this layer's expert routed to no token
+    stale = !fre && (old < key0 || old >= key0 + E || counts[old - key0] == 0);
     st = m.st[s];
     m.stale[s] = stale ? 1 : 0;
   }
@@ -170,8 +174,8 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
     const int ex = m.acc_e[i], sl = m.acc_s[i];
     r_e[i] = ex;
     r_s[i] = sl;
-    int ev = -1;
-    if (i >= S) ev = m.acc_e[i - S];
+    int ev = -1;   // a key
+    if (i >= S) ev = key0 + m.acc_e[i - S];
     else if (i >= n_hit) ev = m.q_old[i - n_hit];
     r_v[i] = ev;
     // buffer: the LRU slot's, or spare i - S for later waves
@@ -222,16 +226,16 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
   // U, so these writes never meet the assignments below)
   for (int i = n_hit + tid; i < min(U, S); i += NT) {
     const int ev = m.q_old[i - n_hit];
-    if (ev >= 0 && ev < E) slot_of[ev] = -1;
+    if (ev >= 0 && ev < keys) slot_of[ev] = -1;
   }
   for (int i = tid; i < U; i += NT) {
     const int ex = m.acc_e[i], sl = m.acc_s[i];
-    if (sl < 0 || sl >= S) continue;   // only a corrupted table gets here
+    if (sl < 0 || sl >= S || ex < 0 || ex >= E) continue;   // only a corrupted table gets here
     if (i + S < U) {
-      slot_of[ex] = -1;            // evicted later in this same step
+      slot_of[key0 + ex] = -1;     // evicted later in this same step
     } else {
-      slot_of[ex] = sl;
-      expert_of[sl] = ex;
+      slot_of[key0 + ex] = sl;
+      expert_of[sl] = key0 + ex;
       stamp[sl] = clk + 1ull + (unsigned long long)i;
     }
   }

@@ -36,7 +36,7 @@ constexpr int kKTileBytes = 128;        // 256 FP4 codes per K tile
 constexpr int kOpBytes = kTileRows * kKTileBytes;   // 16 KB per operand tile
 
 struct Tile {
-  int slot;       // slot of the expert (n_slots = the shared expert)
+  int slot;       // pool buffer of the expert (Geo::shb: the shared expert)
   int row_start;  // first permuted row of the tile
   int row_end;    // one past the expert's last row
   int pad;
@@ -94,7 +94,7 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
 // ---------------------------------------------------------------- step 2
 __global__ void __launch_bounds__(1024)
 build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ offsets, int E, int S,
-                   int X, int N, int k, int mode, int with_shared, Tile* __restrict__ tiles,
+                   int X, int shb, int N, int k, int mode, int with_shared, Tile* __restrict__ tiles,
                    int* __restrict__ n_tiles) {
   __shared__ int sh[33];
   __shared__ int carry;
@@ -118,7 +118,7 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
         nrows = offsets[ex + 1] - r0;
       }
     } else if (i < n_ent) {
-      slot = S;
+      slot = shb;
       r0 = N * k;
       nrows = N;
     }
@@ -578,11 +578,11 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
   PrefillPlan* pl = new PrefillPlan();
   pl->ready = make_map_2d(&pl->xq, xq_codes, g.d / 2, xq_rows) &&
               make_map_2d(&pl->hq, hq_codes, g.f / 2, xq_rows) &&
-              make_map_3d(&pl->wg, slots + g.off_codes[0], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes) &&
-              make_map_3d(&pl->wu, slots + g.off_codes[1], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes) &&
-              make_map_3d(&pl->wd, slots + g.off_codes[2], g.f / 2, g.d, g.S + 1 + g.X, g.ebytes) &&
-              make_map_3d(&pl->wg64, slots + g.off_codes[0], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes, 64) &&
-              make_map_3d(&pl->wu64, slots + g.off_codes[1], g.d / 2, g.f, g.S + 1 + g.X, g.ebytes, 64);
+              make_map_3d(&pl->wg, slots + g.off_codes[0], g.d / 2, g.f, g.nbuf, g.ebytes) &&
+              make_map_3d(&pl->wu, slots + g.off_codes[1], g.d / 2, g.f, g.nbuf, g.ebytes) &&
+              make_map_3d(&pl->wd, slots + g.off_codes[2], g.f / 2, g.d, g.nbuf, g.ebytes) &&
+              make_map_3d(&pl->wg64, slots + g.off_codes[0], g.d / 2, g.f, g.nbuf, g.ebytes, 64) &&
+              make_map_3d(&pl->wu64, slots + g.off_codes[1], g.d / 2, g.f, g.nbuf, g.ebytes, 64);
   return pl;
 }
 
@@ -610,7 +610,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
                                  const cudaEvent_t* ev) {
   Tile* tl = static_cast<Tile*>(tiles);
-  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, g.E, g.S, g.X, N, g.k, mode, with_shared, tl,
+  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, g.E, g.S, g.X, g.shb, N, g.k, mode, with_shared, tl,
                                          n_tiles);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

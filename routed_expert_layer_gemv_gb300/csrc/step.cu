@@ -172,10 +172,10 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
   // the slot table as it was before the step (the LRU CTA rewrites it only
   // after barrier 1, when every CTA has read it): loaded now, parked in
   // shared memory after the router, so the loads overlap its work
-  const int so_r = tid < E ? s.slot_of[tid] : -1;            // E <= kThreads
-  const int bm_r = tid < g.S + g.X ? s.buf[tid] : -1;        // S + X <= E
+  const int so_r = tid < E ? s.slot_of[g.key0 + tid] : -1;   // E <= kThreads
+  const int bm_r = tid < g.S + g.X ? s.buf[tid] : -1;        // S + X <= kThreads
   lru::LruRegs lr{};
-  if (cta == 0) lr = lru::lru_load(E, g.S, g.X, s.slot_of, s.expert_of, s.stamp, s.clock, s.buf);
+  if (cta == 0) lr = lru::lru_load(E, g.S, g.X, g.key0, s.slot_of, s.expert_of, s.stamp, s.clock, s.buf);
   __syncthreads();
 
   // ---------------------------------------------------------------- routing
@@ -316,7 +316,7 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     lru::LruSmem& m = *reinterpret_cast<lru::LruSmem*>(S.base);
     lru::lru_park(lr, E, g.S, g.X, m);
     __syncthreads();
-    lru::lru_body<kThreads>(C.counts, C.offs, nullptr, E, g.S, g.X, s.slot_of, s.expert_of, s.stamp, s.clock,
+    lru::lru_body<kThreads>(C.counts, C.offs, nullptr, E, g.S, g.X, g.key0, g.keys, s.slot_of, s.expert_of, s.stamp, s.clock,
                             s.buf, s.rec, s.stats, nullptr, 0ull, m);
     __syncthreads();
     if (tid == 0) {
@@ -451,6 +451,7 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
 bool step_plan(const Geo& g, int N, StepPlan* out) {
   StepPlan P{};
   if (N < 1 || N > kStepMaxTokens || g.E > kStepMaxE || (long long)N * g.k > kStepMaxPairs) return false;
+  if (g.S + g.X > kThreads) return false;   // the LRU step: one slot per thread of CTA 0
   if (g.d % (rt::kRouterWarps * 16) || g.d > 8192 || g.f > 8192 || g.d % 128 || g.f % 128) return false;
   SG a = make_sg(g, 1, N), b = make_sg(g, 2, N);
   a.all = N <= kTG ? 1 : 0;

@@ -7,6 +7,7 @@ here; ``forward`` calls ``moe_forward``.
 """
 from __future__ import annotations
 
+import dataclasses
 from typing import Callable, Dict, Optional
 
 import numpy as np
@@ -54,17 +55,23 @@ class MoELayer:
     """One layer on the current CUDA device, driven through the C ABI."""
 
     def __init__(self, spec: LayerSpec, max_tokens: int, act_scale_x: float = 1.0,
-                 act_scale_h: float = 1.0):
+                 act_scale_h: float = 1.0, handle: Optional[int] = None):
+        """handle: a stack member's handle (owned by its stack) instead of a
+        new layer."""
         self.spec = spec
         self.desc = make_desc(spec, max_tokens, act_scale_x, act_scale_h)
-        self.layout = capi.moe_expert_layout_for(self.desc)
-        self.h = capi.moe_layer_create(self.desc)
+        # the expert layout does not depend on the slot count (a stack's may exceed E)
+        ld = make_desc(dataclasses.replace(spec, n_slots=min(spec.n_slots, spec.E)), max_tokens, act_scale_x,
+                       act_scale_h)
+        self.layout = capi.moe_expert_layout_for(ld)
+        self.owned = handle is None
+        self.h = capi.moe_layer_create(self.desc) if handle is None else handle
         self.pool: Optional[torch.Tensor] = None
 
     def close(self) -> None:
-        if self.h:
+        if self.h and self.owned:
             capi.moe_layer_destroy(self.h)
-            self.h = None
+        self.h = None
 
     def __del__(self):
         try:
@@ -128,3 +135,45 @@ def build_layer(spec: LayerSpec, seed: int, max_tokens: int, experts_fn=None,
     if install_all:
         L.install_all()
     return L
+
+
+class MoEStack:
+    """n_layers layers of one shape sharing one slot pool and one LRU table
+    (spec.n_slots slots for all layers); layer l has the seeded weights of
+    seed + l."""
+
+    def __init__(self, spec: LayerSpec, n_layers: int, seed: int, max_tokens: int, pools=None):
+        from . import workloads as wl
+        self.spec, self.n_layers = spec, n_layers
+        self.desc = make_desc(spec, max_tokens)
+        self.h = capi.moe_stack_create(self.desc, n_layers)
+        self.layers = []
+        for l in range(n_layers):
+            L = MoELayer(spec, max_tokens, handle=capi.moe_stack_layer(self.h, l))
+            W_r, b = wl.router_weights(spec, seed + l)
+            L.set_router(W_r, b)
+            pool = pools[l] if pools is not None else None
+            L.load_host_pool(lambda e, l=l: wl.expert_weights(spec, seed + l, e), pool)
+            if spec.has_shared:
+                L.set_shared(wl.expert_weights(spec, seed + l, 0, shared=True))
+            self.layers.append(L)
+
+    def close(self) -> None:
+        if self.h:
+            for L in self.layers:
+                L.h = None
+            capi.moe_stack_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, x, y=None, stream=None, regime: int = capi.MOE_REGIME_AUTO):
+        N = x.shape[0]
+        if y is None:
+            y = torch.empty((N, self.spec.d_model), dtype=torch.bfloat16, device=x.device)
+        info = capi.moe_stack_forward(self.h, x, N, y, stream, regime)
+        return y, info

@@ -12,9 +12,12 @@ from oracle.native import layer as olayer
 from routed_expert_layer_gemv_gb300 import workloads as wl
 
 # Output tolerance of the layer (bf16 activations, fp32 accumulation):
-# relative Frobenius error <= 5e-3 and per-element |err| <= 3e-2 * RMS(ref).
+# relative Frobenius error <= 5e-3 and per-element |err| <= 3e-2 * RMS(ref)
+# plus the output's own rounding to bf16 (half a bf16 ulp, 2^-9 |ref|), which
+# dominates for the largest elements of heavy-tailed outputs.
 REL_FRO = 5e-3
 MAX_ABS_RMS = 3e-2
+BF16_HALF_ULP = 2.0 ** -9
 
 
 def need_gpu():
@@ -31,7 +34,11 @@ def assert_close_layer(y_gpu, y_ref, what=""):
     fro = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300)
     mx = np.abs(err).max() if err.size else 0.0
     assert fro <= REL_FRO, "%s rel Frobenius %.3e > %.1e" % (what, fro, REL_FRO)
-    assert mx <= MAX_ABS_RMS * rms, "%s max |err| %.3e > %.1e * RMS %.3e" % (what, mx, MAX_ABS_RMS, rms)
+    excess = np.abs(err) - (MAX_ABS_RMS * rms + BF16_HALF_ULP * np.abs(ref))
+    if err.size and excess.max() > 0:
+        i = np.unravel_index(excess.argmax(), err.shape)
+        raise AssertionError("%s |err| %.3e at %s (ref %.4e) > %.1e * RMS %.3e + half a bf16 ulp"
+                             % (what, abs(err[i]), i, ref[i], MAX_ABS_RMS, rms))
     return fro, mx / max(rms, 1e-300)
 
 
@@ -97,3 +104,72 @@ def check_last_step(L, spec, N, idx_ref, gates_ref):
     assert np.array_equal(row_of.cpu().numpy(), rr.reshape(-1))
     assert np.array_equal(tok_of.cpu().numpy(), rt)
     assert np.allclose(gates.cpu().numpy().reshape(N, k), gates_ref, rtol=2e-6, atol=1e-7)
+
+
+_E2M1_MID = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def near_marks(v, marks, rel=1e-4):
+    """True where v lies within `rel` (relative) of one of the marks."""
+    v = np.asarray(v, np.float64)[..., None]
+    return (np.abs(v - marks) <= rel * marks).any(axis=-1)
+
+
+def prefill_h_flip_tokens(L, spec, O, X, idx):
+    """After a prefill moe_forward of layer handle L on bf16-exact X [N, d]:
+    the tokens some of whose FP4 codes of h = SiLU(W_g x) (W_u x) (a routed
+    expert's row or the shared one) differ between the kernel (fp32 sums) and
+    the oracle (FP64).  Every such difference must lie where the oracle's
+    value is within 1e-4 (relative) of an E2M1 rounding midpoint or its
+    block's scale input within 1e-4 of a scale boundary: two correct
+    roundings of sums that differ in the last bits.  Returns a bool per token."""
+    import torch
+    from routed_expert_layer_gemv_gb300 import capi
+    from oracle.native import formats, quant
+    from oracle.native import layer as olayer
+    N, k, blk, f = X.shape[0], spec.k, spec.block, spec.d_ff
+    rows = N * k + (N if spec.has_shared else 0)
+    hc = torch.empty(rows, f // 2, dtype=torch.uint8, device="cuda")
+    hs = torch.empty(rows, f // blk, dtype=torch.uint8, device="cuda")
+    capi.moe_debug_last_hidden(L.h, hq_codes=hc, hq_scales=hs)
+    row_of = torch.empty(N * k, dtype=torch.int32, device="cuda")
+    capi.moe_debug_last_step(L.h, row_of=row_of)
+    torch.cuda.synchronize()
+    HC = formats.unpack_codes(hc.cpu().numpy())
+    HS = hs.cpu().numpy()
+    R = row_of.cpu().numpy().reshape(N, k)
+    xq = olayer.act_roundtrip(X, spec.fmt, 1.0)
+    flag = np.zeros(N, dtype=bool)
+    jobs = []
+    for e in np.unique(idx):
+        tt, jj = np.nonzero(idx == e)
+        jobs.append((O.expert(int(e)), tt, R[tt, jj]))
+    if spec.has_shared:
+        jobs.append((olayer.dequant_expert(O.shared_w, spec.fmt), np.arange(N), N * k + np.arange(N)))
+    for W, toks, rws in jobs:
+        h = olayer.silu(xq[toks] @ W["gate"].T) * (xq[toks] @ W["up"].T)
+        amax = np.abs(h.astype(np.float32).reshape(len(toks), -1, blk)).max(axis=-1).astype(np.float64)
+        if spec.fmt == "mxfp4":
+            rc, rsc = quant.quant_mxfp4(h)
+            with np.errstate(divide="ignore"):
+                lg = np.log2(np.where(amax > 0, amax, 1.0))
+            edge = np.abs(amax - np.exp2(np.round(lg))) <= 1e-4 * amax
+            unit = formats.E8M0_TABLE[rsc]
+        else:
+            rc, rsc = quant.quant_nvfp4(h, 1.0)
+            e4 = np.sort(np.unique(formats.E4M3_TABLE[:0x7F]))
+            mids = (e4[1:] + e4[:-1]) / 2
+            edge = near_marks(amax / 6.0, mids[mids > 0])
+            unit = formats.E4M3_TABLE[rsc]
+        rcu = formats.unpack_codes(rc)
+        gc, gs = HC[rws], HS[rws]
+        bad_scale = gs != rsc
+        assert not (bad_scale & ~edge).any(), "a block scale of h differs away from a scale boundary"
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = np.abs(h) / np.repeat(unit, blk, axis=1)
+        both_zero = ((rcu & 7) == 0) & ((gc & 7) == 0)
+        diff = (gc != rcu) & ~both_zero
+        unexplained = diff & ~np.repeat(bad_scale, blk, axis=1) & ~near_marks(q, _E2M1_MID)
+        assert not unexplained.any(), "%d FP4 codes of h differ away from a rounding midpoint" % unexplained.sum()
+        flag[toks[diff.any(axis=1) | bad_scale.any(axis=1)]] = True
+    return flag

@@ -1,0 +1,206 @@
+"""Multi-layer stacks on the GPU: layers sharing one slot pool and one LRU
+table keyed by (layer, expert), decode and whole-layer-prefetch prefill,
+against the stack oracle (per-layer parity on the same inputs, the shared
+table bit for bit) and against the same layers run one by one."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import (assert_close_layer, bf16_tensor, check_last_step, need_gpu, oracle_layer,
+                     prefill_h_flip_tokens, small_spec)
+from oracle import stack as ostack
+from oracle.native import layer as olayer
+from oracle.native.lru import SlotTable
+from routed_expert_layer_gemv_gb300 import capi
+from routed_expert_layer_gemv_gb300 import workloads as wl
+from routed_expert_layer_gemv_gb300.layer import MoEStack
+
+pytestmark = pytest.mark.gpu
+DEC = capi.MOE_REGIME_DECODE
+PRE = capi.MOE_REGIME_PREFILL
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def _f64(t):
+    return t.float().cpu().double().numpy()
+
+
+def _table(S, n_slots):
+    eo, st, clk = capi.moe_lru_get_state(S.layers[0].h, n_slots)
+    return eo, st, clk
+
+
+def _ties(spec, seed, x):
+    W_r, b = wl.router_weights(spec, seed)
+    return olayer.near_tie(x, W_r, b, spec.k, 1e-4)
+
+
+def _check_layer(spec, seed, x_in, y_gpu, regime, what, L=None):
+    """Oracle parity of one layer (handle L, just run) on the GPU's own input;
+    returns the oracle's ids.  Tokens whose k-th / (k+1)-th logits are within
+    1e-4 (a selection floating point decides) are left out of the comparison;
+    in prefill, so are tokens some FP4 code of whose h the kernel and the
+    oracle round to neighbouring values at a rounding boundary
+    (prefill_h_flip_tokens, each difference checked), for the per-element
+    bound only -- the Frobenius bound covers every token."""
+    ol = oracle_layer(spec, seed)
+    untied = keep = ~_ties(spec, seed, x_in)
+    y_ref, idx, gates = ol.forward(x_in, regime)
+    y = _f64(y_gpu)
+    if regime == "prefill":
+        flip = prefill_h_flip_tokens(L, spec, ol, x_in, idx) & keep
+        assert flip.sum() <= 0.05 * len(flip), "%s: %d tokens with an h code flipped" % (what, flip.sum())
+        err = np.linalg.norm(y[keep] - y_ref[keep]) / np.linalg.norm(y_ref[keep])
+        assert err <= 5e-3, "%s rel Frobenius %.3e" % (what, err)
+        keep = keep & ~flip
+    assert_close_layer(y[keep], y_ref[keep], what)
+    return idx, gates, untied
+
+
+STACKS = [
+    # (spec, layers, tokens, decode path, fill mode)
+    (small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=20), 3, 3, capi.MOE_DECODE_CHAIN, None),
+    (small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=20), 3, 3, capi.MOE_DECODE_STEP, None),
+    # shared expert per layer, spare buffers and waves (|U| > n_slots)
+    (small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=10, has_shared=True), 3, 8, capi.MOE_DECODE_AUTO, None),
+    (small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=10, has_shared=True), 3, 8, capi.MOE_DECODE_AUTO,
+     capi.MOE_FILL_MEMCPY),
+    (small_spec(E=8, k=2, d_model=256, d_ff=512, n_slots=6, fmt="nvfp4", has_bias=True, has_shared=True), 4, 5,
+     capi.MOE_DECODE_AUTO, None),
+]
+
+
+@pytest.mark.parametrize("spec,nl,N,path,fill", STACKS)
+def test_stack_decode_matches_layers_and_oracle(spec, nl, N, path, fill):
+    seed = 61
+    A = MoEStack(spec, nl, seed, N)   # moe_stack_forward
+    B = MoEStack(spec, nl, seed, N)   # the same layers through moe_forward, one by one
+    for S in (A, B):
+        for L in S.layers:
+            capi.moe_set_decode_path(L.h, path)
+            if fill is not None:
+                capi.moe_set_fill_mode(L.h, fill)
+    cache = ostack.StackCache(nl, spec.E, spec.n_slots, SlotTable)
+    xs, _ = wl.ar1_tokens(seed, N, 6, spec.d_model, 0.9)
+    for t in range(6):
+        x = bf16_tensor(xs[t])
+        yA, info = A.forward(x, regime=DEC)
+        h = x
+        for l, L in enumerate(B.layers):
+            y, _ = L.forward(h, regime=DEC)
+            idx, gates, keep = _check_layer(spec, seed + l, _f64(h), y, "decode", "step %d layer %d" % (t, l))
+            if keep.all():
+                cache.step(l, idx.reshape(-1))
+            else:   # the GPU's own selection decides the table
+                cache.step(l, _last_idx(L, spec, N))
+            h = y
+        torch.cuda.synchronize()
+        assert torch.equal(yA, h), "stack forward differs from the layers run one by one"
+        assert info.n_launches > 0
+        for S in (A, B):
+            eo, st, clk = _table(S, spec.n_slots)
+            assert eo == cache.expert_of and st == cache.stamp and clk == cache.clock
+    A.close()
+    B.close()
+
+
+def _last_idx(L, spec, N):
+    idx = torch.empty(N * spec.k, dtype=torch.int32, device="cuda")
+    capi.moe_debug_last_step(L.h, idx, None, None, None, None, None)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy()
+
+
+def test_stack_last_layer_routing_arrays():
+    spec = small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=20)
+    nl, N, seed = 3, 5, 62
+    A = MoEStack(spec, nl, seed, N)
+    x = bf16_tensor(wl.iid_tokens(seed, N, spec.d_model)[0])
+    h = x
+    for l, L in enumerate(A.layers):
+        y, _ = L.forward(h, regime=DEC)
+        if l < nl - 1:
+            h = y
+    W_r, b = wl.router_weights(spec, seed + nl - 1)
+    if not olayer.near_tie(_f64(h), W_r, b, spec.k, 1e-4).any():
+        idx, gates, _ = olayer.router(_f64(h), W_r, b, spec.k, spec.norm_topk)
+        check_last_step(A.layers[-1], spec, N, idx, gates)
+    A.close()
+
+
+PREFILL_SPEC = small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=32)
+
+
+def test_stack_prefill_prefetch_modes():
+    spec, nl, N, seed = PREFILL_SPEC, 3, 200, 63
+    xs = [bf16_tensor(wl.iid_tokens(seed + i, N, spec.d_model)[0]) for i in range(2)]
+    outs, tables, stats = {}, {}, {}
+    for mode in (capi.MOE_PREFETCH_NONE, capi.MOE_PREFETCH_SERIAL, capi.MOE_PREFETCH_OVERLAP):
+        S = MoEStack(spec, nl, seed, N)
+        capi.moe_stack_set_prefetch(S.h, mode)
+        ys = []
+        for x in xs:
+            y, info = S.forward(x, regime=PRE)
+            assert info.regime == PRE
+            ys.append(y.clone())
+        torch.cuda.synchronize()
+        outs[mode] = ys
+        tables[mode] = _table(S, spec.n_slots)
+        stats[mode] = capi.moe_stack_prefetch_stats(S.h)
+        S.close()
+    # the schedule changes nothing in the arithmetic
+    for mode in (capi.MOE_PREFETCH_SERIAL, capi.MOE_PREFETCH_OVERLAP):
+        for a, b in zip(outs[mode], outs[capi.MOE_PREFETCH_NONE]):
+            assert torch.equal(a, b)
+    # serial and overlapped prefetch run the same table steps
+    assert tables[capi.MOE_PREFETCH_SERIAL] == tables[capi.MOE_PREFETCH_OVERLAP]
+    assert stats[capi.MOE_PREFETCH_NONE][0] == 0
+    assert stats[capi.MOE_PREFETCH_OVERLAP][0] == 2 * nl and stats[capi.MOE_PREFETCH_OVERLAP][1] == 2 * nl * spec.E
+    # per-layer parity on the same inputs, and the table against the oracle's
+    # sequence of steps (with and without the whole-layer prefetches)
+    R = MoEStack(spec, nl, seed, N)
+    capi.moe_stack_set_prefetch(R.h, capi.MOE_PREFETCH_NONE)
+    c_none = ostack.StackCache(nl, spec.E, spec.n_slots, SlotTable)
+    c_pf = ostack.StackCache(nl, spec.E, spec.n_slots, SlotTable)
+    for i, x in enumerate(xs):
+        h = x
+        for l, L in enumerate(R.layers):
+            y, _ = L.forward(h, regime=PRE)
+            idx, _, keep = _check_layer(spec, seed + l, _f64(h), y, "prefill", "chunk %d layer %d" % (i, l), L)
+            ids = idx.reshape(-1) if keep.all() else _last_idx(L, spec, N)
+            c_none.step(l, ids)
+            c_pf.prefetch(l)
+            c_pf.step(l, ids)
+            h = y
+        assert torch.equal(h, outs[capi.MOE_PREFETCH_NONE][i])
+    R.close()
+    assert tables[capi.MOE_PREFETCH_NONE] == (c_none.expert_of, c_none.stamp, c_none.clock)
+    assert tables[capi.MOE_PREFETCH_OVERLAP] == (c_pf.expert_of, c_pf.stamp, c_pf.clock)
+
+
+def test_stack_prefill_overlap_needs_two_layers_of_slots():
+    spec = small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=20)
+    S = MoEStack(spec, 2, 64, 64)
+    with pytest.raises(capi.MoeError) as e:
+        capi.moe_stack_set_prefetch(S.h, capi.MOE_PREFETCH_OVERLAP)
+    assert e.value.status == capi.MOE_ERR_UNSUPPORTED
+    capi.moe_stack_set_prefetch(S.h, capi.MOE_PREFETCH_SERIAL)
+    S.close()
+
+
+def test_stack_members_are_not_resized_or_destroyed_alone():
+    spec = small_spec(E=8, k=2, d_model=256, d_ff=256, n_slots=6)
+    S = MoEStack(spec, 2, 65, 4)
+    h1 = S.layers[1].h
+    assert capi.lib().moe_cache_resize(h1, 4, None) == capi.MOE_ERR_UNSUPPORTED
+    assert capi.lib().moe_layer_destroy(h1) == capi.MOE_ERR_STATE
+    # a key of layer 1 installed into a slot shows in the shared table
+    capi.moe_cache_install(h1, 3, 2)
+    torch.cuda.synchronize()
+    eo, _, _ = _table(S, spec.n_slots)
+    assert eo[2] == 1 * spec.E + 3
+    S.close()
