@@ -11,10 +11,11 @@ import torch
 from oracle.native import layer as olayer
 from routed_expert_layer_gemv_gb300 import workloads as wl
 
-# Output tolerance of the layer (bf16 activations, fp32 accumulation):
-# relative Frobenius error <= 5e-3 and per-element |err| <= 3e-2 * RMS(ref)
-# plus the output's own rounding to bf16 (half a bf16 ulp, 2^-9 |ref|), which
-# dominates for the largest elements of heavy-tailed outputs.
+# Output tolerance of the layer (bf16 activations, fp32 accumulation), as the
+# task states it: relative Frobenius error <= 5e-3 and per-element
+# |err| <= 3e-2 * RMS(ref).  bf16_ulp=True (the multi-layer stack's deeper
+# layers only, whose outputs are heavy-tailed) adds the output's own rounding
+# to bf16, half an ulp (2^-9 |ref|), to the per-element bound.
 REL_FRO = 5e-3
 MAX_ABS_RMS = 3e-2
 BF16_HALF_ULP = 2.0 ** -9
@@ -25,7 +26,7 @@ def need_gpu():
         pytest.skip("needs a CUDA GPU")
 
 
-def assert_close_layer(y_gpu, y_ref, what=""):
+def assert_close_layer(y_gpu, y_ref, what="", bf16_ulp=False):
     y = y_gpu.float().cpu().double().numpy() if isinstance(y_gpu, torch.Tensor) else np.asarray(y_gpu, np.float64)
     ref = np.asarray(y_ref, np.float64)
     assert y.shape == ref.shape, (y.shape, ref.shape)
@@ -34,11 +35,12 @@ def assert_close_layer(y_gpu, y_ref, what=""):
     fro = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300)
     mx = np.abs(err).max() if err.size else 0.0
     assert fro <= REL_FRO, "%s rel Frobenius %.3e > %.1e" % (what, fro, REL_FRO)
-    excess = np.abs(err) - (MAX_ABS_RMS * rms + BF16_HALF_ULP * np.abs(ref))
+    excess = np.abs(err) - (MAX_ABS_RMS * rms + (BF16_HALF_ULP * np.abs(ref) if bf16_ulp else 0.0))
     if err.size and excess.max() > 0:
         i = np.unravel_index(excess.argmax(), err.shape)
-        raise AssertionError("%s |err| %.3e at %s (ref %.4e) > %.1e * RMS %.3e + half a bf16 ulp"
-                             % (what, abs(err[i]), i, ref[i], MAX_ABS_RMS, rms))
+        raise AssertionError("%s |err| %.3e at %s (ref %.4e) > %.1e * RMS %.3e%s"
+                             % (what, abs(err[i]), i, ref[i], MAX_ABS_RMS, rms,
+                                " + half a bf16 ulp" if bf16_ulp else ""))
     return fro, mx / max(rms, 1e-300)
 
 

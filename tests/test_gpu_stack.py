@@ -39,7 +39,7 @@ def _ties(spec, seed, x):
     return olayer.near_tie(x, W_r, b, spec.k, 1e-4)
 
 
-def _check_layer(spec, seed, x_in, y_gpu, regime, what, L=None):
+def _check_layer(spec, seed, x_in, y_gpu, regime, what, L=None, first=True):
     """Oracle parity of one layer (handle L, just run) on the GPU's own input;
     returns the oracle's ids.  Tokens whose k-th / (k+1)-th logits are within
     1e-4 (a selection floating point decides) are left out of the comparison;
@@ -57,7 +57,11 @@ def _check_layer(spec, seed, x_in, y_gpu, regime, what, L=None):
         err = np.linalg.norm(y[keep] - y_ref[keep]) / np.linalg.norm(y_ref[keep])
         assert err <= 5e-3, "%s rel Frobenius %.3e" % (what, err)
         keep = keep & ~flip
-    assert_close_layer(y[keep], y_ref[keep], what)
+    # layer 0 sees the workload's own tokens: the stated bound as it stands;
+    # deeper layers see heavy-tailed hidden states (max / RMS of their outputs
+    # up to ~30), where half a bf16 ulp of the largest outputs alone exceeds
+    # 3e-2 RMS, so their per-element bound adds it
+    assert_close_layer(y[keep], y_ref[keep], what, bf16_ulp=first is False)
     return idx, gates, untied
 
 
@@ -92,7 +96,8 @@ def test_stack_decode_matches_layers_and_oracle(spec, nl, N, path, fill):
         h = x
         for l, L in enumerate(B.layers):
             y, _ = L.forward(h, regime=DEC)
-            idx, gates, keep = _check_layer(spec, seed + l, _f64(h), y, "decode", "step %d layer %d" % (t, l))
+            idx, gates, keep = _check_layer(spec, seed + l, _f64(h), y, "decode", "step %d layer %d" % (t, l),
+                                            first=l == 0)
             if keep.all():
                 cache.step(l, idx.reshape(-1))
             else:   # the GPU's own selection decides the table
@@ -170,7 +175,8 @@ def test_stack_prefill_prefetch_modes():
         h = x
         for l, L in enumerate(R.layers):
             y, _ = L.forward(h, regime=PRE)
-            idx, _, keep = _check_layer(spec, seed + l, _f64(h), y, "prefill", "chunk %d layer %d" % (i, l), L)
+            idx, _, keep = _check_layer(spec, seed + l, _f64(h), y, "prefill", "chunk %d layer %d" % (i, l), L,
+                                        first=l == 0)
             ids = idx.reshape(-1) if keep.all() else _last_idx(L, spec, N)
             c_none.step(l, ids)
             c_pf.prefetch(l)
