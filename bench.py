@@ -400,11 +400,15 @@ def run_stack(c, n_layers, batches, link_gbs):
     yp = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
     spec_p = dataclasses.replace(spec0, n_slots=2 * E)
     Kp, Wp = max(3, c.args.prefill_steps // 2), 1
-    names = {capi.MOE_PREFETCH_NONE: "none", capi.MOE_PREFETCH_SERIAL: "serial",
-             capi.MOE_PREFETCH_OVERLAP: "overlap"}
-    for mode, name in names.items():
+    names = {"none": (capi.MOE_PREFETCH_NONE, capi.MOE_FILL_KERNEL),
+             "serial": (capi.MOE_PREFETCH_SERIAL, capi.MOE_FILL_KERNEL),
+             "overlap": (capi.MOE_PREFETCH_OVERLAP, capi.MOE_FILL_KERNEL),
+             "serial_memcpy": (capi.MOE_PREFETCH_SERIAL, capi.MOE_FILL_MEMCPY),
+             "overlap_memcpy": (capi.MOE_PREFETCH_OVERLAP, capi.MOE_FILL_MEMCPY)}
+    for name, (mode, copy) in names.items():
         st = MoEStack(spec_p, n_layers, work.seed, N, pools=pools)
         capi.moe_stack_set_prefetch(st.h, mode)
+        capi.moe_stack_set_prefetch_copy(st.h, copy)
         with torch.cuda.stream(c.st):
             for _ in range(Wp):
                 st.forward(x, yp, stream=c.st, regime=capi.MOE_REGIME_PREFILL)

@@ -434,6 +434,14 @@ int moe_stack_set_prefetch(moe_stack_t stack, int mode);
  * the per-step counts are -1 (read each member's statistics instead). */
 int moe_stack_forward(moe_stack_t stack, const void* x, int N, void* y, void* stream, int regime,
                       moe_forward_info* info);
+/* How prefetched experts are copied: MOE_FILL_MEMCPY (default; AUTO means
+ * it) -- the host reads the prefetch's step record (mapped pinned memory,
+ * polled, bounded) and issues cudaMemcpyAsync per run of consecutive experts
+ * on the prefetch's stream (the fill stream when overlapped), so the GEMMs
+ * keep every SM; MOE_FILL_KERNEL -- copy kernels on 12 SMs read the step
+ * record on the device (no host wait), and an overlapped prefill GEMM leaves
+ * those SMs free.  MOE_ERR_ARG for other values. */
+int moe_stack_set_prefetch_copy(moe_stack_t stack, int fill);
 /* Accumulated prefetch counters: steps, keys accessed, hits, misses
  * (synchronises the device). */
 int moe_stack_prefetch_stats(moe_stack_t stack, uint64_t* out4);

@@ -113,6 +113,7 @@ _SIGS = {
     "moe_stack_destroy": ([_P], _I),
     "moe_stack_layer": ([_P, _I, C.POINTER(_P)], _I),
     "moe_stack_set_prefetch": ([_P, _I], _I),
+    "moe_stack_set_prefetch_copy": ([_P, _I], _I),
     "moe_stack_forward": ([_P, _P, _I, _P, _P, _I, C.POINTER(moe_forward_info)], _I),
     "moe_stack_prefetch_stats": ([_P, _P], _I),
     "moe_stack_last_error": ([_P], C.c_char_p),
@@ -367,6 +368,10 @@ def moe_stack_layer(s: int, l: int) -> int:
 
 def moe_stack_set_prefetch(s: int, mode: int) -> None:
     check_stack(lib().moe_stack_set_prefetch(s, mode), s)
+
+
+def moe_stack_set_prefetch_copy(s: int, fill: int) -> None:
+    check_stack(lib().moe_stack_set_prefetch_copy(s, fill), s)
 
 
 def moe_stack_forward(s, x, N: int, y, stream=None, regime: int = MOE_REGIME_AUTO) -> moe_forward_info:

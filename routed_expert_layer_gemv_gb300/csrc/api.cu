@@ -161,6 +161,7 @@ struct moe_layer {
 struct moe_stack {
   std::vector<moe_layer*> layers;
   int prefetch = MOE_PREFETCH_AUTO;
+  int prefetch_copy = MOE_FILL_MEMCPY;           // how prefetched experts are copied (MOE_FILL_MEMCPY / KERNEL)
   __nv_bfloat16* hid[2] = {nullptr, nullptr};   // hidden states between layers [max_tokens, d]
   int* ones = nullptr;                           // [E] ones: a whole layer as a step's counts
   unsigned long long* pf_stats = nullptr;        // prefetch steps, keys, hits, misses
@@ -1675,6 +1676,15 @@ int moe_stack_layer(moe_stack_t K, int l, moe_layer_t* out) {
   return MOE_OK;
 }
 
+int moe_stack_set_prefetch_copy(moe_stack_t K, int fill) {
+  if (!K) return MOE_ERR_ARG;
+  if (fill == MOE_FILL_AUTO) fill = MOE_FILL_MEMCPY;
+  if (fill != MOE_FILL_KERNEL && fill != MOE_FILL_MEMCPY)
+    return stack_fail(K, MOE_ERR_ARG, "prefetch copies are MOE_FILL_KERNEL or MOE_FILL_MEMCPY (got %d)", fill);
+  K->prefetch_copy = fill;
+  return MOE_OK;
+}
+
 int moe_stack_set_prefetch(moe_stack_t K, int mode) {
   if (!K) return MOE_ERR_ARG;
   const Geo& g = K->layers[0]->g;
@@ -1703,19 +1713,51 @@ int moe_stack_prefetch_stats(moe_stack_t K, uint64_t* out4) {
 
 // The whole of layer m as one step of the shared table (every expert accessed,
 // hits first, misses ascending), then its misses copied from the layer's host
-// pool by kFillSms CTAs; all on stream st.
-static int stack_prefetch(moe_stack* K, int m, cudaStream_t st) {
+// pool, all on stream st: by kFillSms CTAs reading the step record on the
+// device, or (copy_engine) by cudaMemcpyAsync once the host has read the
+// record the LRU kernel writes into mapped pinned memory (runs of experts
+// bound for consecutive buffers as one copy).
+static int stack_prefetch(moe_stack* K, int m, cudaStream_t st, bool copy_engine) {
   moe_layer* M = K->layers[m];
   const Geo& g = M->g;
+  const unsigned long long seq = copy_engine ? ++M->step_seq : 0ull;
   cudaError_t e = launch_lru_step(g, K->ones, nullptr, M->slot_of, M->expert_of, M->stamp, M->clock, M->buf, M->rec,
-                                  K->pf_stats, nullptr, 0, st);
-  for (int c = 0; e == cudaSuccess && c < miss_chunks(g.E); ++c)
-    e = launch_fill_sm(g, M->rec, c, M->pool_dev, M->slots, st);
+                                  K->pf_stats, copy_engine ? M->rec_host_dev : nullptr, seq, st);
+  M->launches += 1;
+  if (e == cudaSuccess && !copy_engine) {
+    for (int c = 0; e == cudaSuccess && c < miss_chunks(g.E); ++c)
+      e = launch_fill_sm(g, M->rec, c, M->pool_dev, M->slots, st);
+    M->launches += miss_chunks(g.E);
+  }
+  if (e == cudaSuccess && copy_engine) e = cudaEventRecord(M->ev_route, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return stack_fail(K, MOE_ERR_CUDA, "prefetch of layer %d: %s", m, cudaGetErrorString(e));
   }
-  M->launches += 1 + miss_chunks(g.E);
+  if (!copy_engine) return MOE_OK;
+  const int prc = poll_record(M, seq);
+  if (prc) return stack_fail(K, prc, "prefetch of layer %d: %s", m, M->err.c_str());
+  const StepRecord* r = M->rec_host;
+  const int U = r->U, nh = r->n_hit;
+  const int* ae = rec_expert(const_cast<StepRecord*>(r));
+  const int* as = rec_slot(const_cast<StepRecord*>(r), g.E);
+  const int* ab = rec_buf(const_cast<StepRecord*>(r), g.E);
+  if (U != g.E || nh < 0 || nh > U)
+    return stack_fail(K, MOE_ERR_STATE, "prefetch record of layer %d is inconsistent (U=%d, hits=%d)", m, U, nh);
+  for (int i = 0; i < U; ++i)
+    if (ae[i] < 0 || ae[i] >= g.E || as[i] < 0 || as[i] >= g.S || !buf_ok(g, ab[i]))
+      return stack_fail(K, MOE_ERR_STATE, "prefetch record entry %d of layer %d is out of range", i, m);
+  for (int i = nh; i < U;) {
+    int j = i + 1;
+    while (j < U && ae[j] == ae[j - 1] + 1 && ab[j] == ab[j - 1] + 1) ++j;
+    e = cudaMemcpyAsync(M->slots + (size_t)ab[i] * g.ebytes, M->host_pool + (size_t)ae[i] * g.ebytes,
+                        (size_t)(j - i) * g.ebytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return stack_fail(K, MOE_ERR_FILL, "prefetch copy of layer %d, expert %d: %s", m, ae[i], cudaGetErrorString(e));
+    }
+    i = j;
+  }
   return MOE_OK;
 }
 
@@ -1767,12 +1809,13 @@ int moe_stack_forward(moe_stack_t K, const void* x, int N, void* y, void* stream
     return stack_fail(K, MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   };
   int rc = MOE_OK;
+  const bool ce = K->prefetch_copy == MOE_FILL_MEMCPY;
   if (mode != MOE_PREFETCH_NONE) {
     // layer 0's experts, after the caller's earlier work on st
     L0->launches = 0;
     if ((rc = cuda_k(cudaEventRecord(K->ev_in, st), "cudaEventRecord"))) return rc;
     if ((rc = cuda_k(cudaStreamWaitEvent(fs, K->ev_in, 0), "cudaStreamWaitEvent"))) return rc;
-    if ((rc = stack_prefetch(K, 0, fs))) return rc;
+    if ((rc = stack_prefetch(K, 0, fs, ce))) return rc;
     launches += L0->launches;
     if ((rc = cuda_k(cudaEventRecord(K->ev_pf, fs), "cudaEventRecord"))) return rc;
     if ((rc = cuda_k(cudaStreamWaitEvent(st, K->ev_pf, 0), "cudaStreamWaitEvent"))) return rc;
@@ -1785,8 +1828,8 @@ int moe_stack_forward(moe_stack_t K, const void* x, int N, void* y, void* stream
     M->assume_resident = mode != MOE_PREFETCH_NONE;
     M->ev_after_route = ov ? K->ev_route : nullptr;
     // the prefill GEMM leaves the fill kernels' SMs free while the next
-    // layer streams in
-    M->gemm_sms = ov ? M->num_sms - kFillSms : 0;
+    // layer streams in (copy-engine prefetches need no SM)
+    M->gemm_sms = ov && !ce ? M->num_sms - kFillSms : 0;
     rc = fwd(l, in, outp);
     M->assume_resident = false;
     M->ev_after_route = nullptr;
@@ -1801,12 +1844,12 @@ int moe_stack_forward(moe_stack_t K, const void* x, int N, void* y, void* stream
         // n_slots >= 2 E none of them is evicted), its copies run on the fill
         // SMs, and layer l + 1 starts once they landed
         if ((rc = cuda_k(cudaStreamWaitEvent(fs, K->ev_route, 0), "cudaStreamWaitEvent"))) return rc;
-        if ((rc = stack_prefetch(K, l + 1, fs))) return rc;
+        if ((rc = stack_prefetch(K, l + 1, fs, ce))) return rc;
         if ((rc = cuda_k(cudaEventRecord(K->ev_pf, fs), "cudaEventRecord"))) return rc;
         if ((rc = cuda_k(cudaStreamWaitEvent(st, K->ev_pf, 0), "cudaStreamWaitEvent"))) return rc;
       } else {
         // after layer l on the caller's stream
-        if ((rc = stack_prefetch(K, l + 1, st))) return rc;
+        if ((rc = stack_prefetch(K, l + 1, st, ce))) return rc;
       }
       launches += Mn->launches;
     }

@@ -143,32 +143,38 @@ PREFILL_SPEC = small_spec(E=16, k=4, d_model=256, d_ff=256, n_slots=32)
 def test_stack_prefill_prefetch_modes():
     spec, nl, N, seed = PREFILL_SPEC, 3, 200, 63
     xs = [bf16_tensor(wl.iid_tokens(seed + i, N, spec.d_model)[0]) for i in range(2)]
+    NONE, SER, OV = capi.MOE_PREFETCH_NONE, capi.MOE_PREFETCH_SERIAL, capi.MOE_PREFETCH_OVERLAP
+    KER, MEM = capi.MOE_FILL_KERNEL, capi.MOE_FILL_MEMCPY
+    runs = [(NONE, KER), (SER, KER), (OV, KER), (SER, MEM), (OV, MEM)]
     outs, tables, stats = {}, {}, {}
-    for mode in (capi.MOE_PREFETCH_NONE, capi.MOE_PREFETCH_SERIAL, capi.MOE_PREFETCH_OVERLAP):
+    for mode, copy in runs:
         S = MoEStack(spec, nl, seed, N)
         capi.moe_stack_set_prefetch(S.h, mode)
+        capi.moe_stack_set_prefetch_copy(S.h, copy)
         ys = []
         for x in xs:
             y, info = S.forward(x, regime=PRE)
             assert info.regime == PRE
             ys.append(y.clone())
         torch.cuda.synchronize()
-        outs[mode] = ys
-        tables[mode] = _table(S, spec.n_slots)
-        stats[mode] = capi.moe_stack_prefetch_stats(S.h)
+        outs[mode, copy] = ys
+        tables[mode, copy] = _table(S, spec.n_slots)
+        stats[mode, copy] = capi.moe_stack_prefetch_stats(S.h)
         S.close()
-    # the schedule changes nothing in the arithmetic
-    for mode in (capi.MOE_PREFETCH_SERIAL, capi.MOE_PREFETCH_OVERLAP):
-        for a, b in zip(outs[mode], outs[capi.MOE_PREFETCH_NONE]):
-            assert torch.equal(a, b)
-    # serial and overlapped prefetch run the same table steps
-    assert tables[capi.MOE_PREFETCH_SERIAL] == tables[capi.MOE_PREFETCH_OVERLAP]
-    assert stats[capi.MOE_PREFETCH_NONE][0] == 0
-    assert stats[capi.MOE_PREFETCH_OVERLAP][0] == 2 * nl and stats[capi.MOE_PREFETCH_OVERLAP][1] == 2 * nl * spec.E
+    # the schedule and the copy engine change nothing in the arithmetic
+    for r in runs[1:]:
+        for a, b in zip(outs[r], outs[NONE, KER]):
+            assert torch.equal(a, b), r
+    # every prefetching run takes the same table steps
+    for r in runs[2:]:
+        assert tables[r] == tables[SER, KER], r
+    assert stats[NONE, KER][0] == 0
+    for r in runs[1:]:
+        assert stats[r][0] == 2 * nl and stats[r][1] == 2 * nl * spec.E
     # per-layer parity on the same inputs, and the table against the oracle's
     # sequence of steps (with and without the whole-layer prefetches)
     R = MoEStack(spec, nl, seed, N)
-    capi.moe_stack_set_prefetch(R.h, capi.MOE_PREFETCH_NONE)
+    capi.moe_stack_set_prefetch(R.h, NONE)
     c_none = ostack.StackCache(nl, spec.E, spec.n_slots, SlotTable)
     c_pf = ostack.StackCache(nl, spec.E, spec.n_slots, SlotTable)
     for i, x in enumerate(xs):
@@ -182,10 +188,10 @@ def test_stack_prefill_prefetch_modes():
             c_pf.prefetch(l)
             c_pf.step(l, ids)
             h = y
-        assert torch.equal(h, outs[capi.MOE_PREFETCH_NONE][i])
+        assert torch.equal(h, outs[NONE, KER][i])
     R.close()
-    assert tables[capi.MOE_PREFETCH_NONE] == (c_none.expert_of, c_none.stamp, c_none.clock)
-    assert tables[capi.MOE_PREFETCH_OVERLAP] == (c_pf.expert_of, c_pf.stamp, c_pf.clock)
+    assert tables[NONE, KER] == (c_none.expert_of, c_none.stamp, c_none.clock)
+    assert tables[OV, KER] == (c_pf.expert_of, c_pf.stamp, c_pf.clock)
 
 
 def test_stack_prefill_overlap_needs_two_layers_of_slots():
