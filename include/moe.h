@@ -358,7 +358,8 @@ int moe_debug_alloc_fault(long long nth, long long* live_out);
  * (marks a CTA does not reach stay from an earlier step) -- then the SM clock
  * counter at the first and at the last stamp, then the global timer when the
  * CTA's first phase-1 weight stage had landed and when its last one was
- * consumed (15 entries per CTA).  out: host array of at least
+ * consumed, the same two for phase 2, and when the CTA's first phase-2
+ * activation block was staged (18 entries per CTA).  out: host array of at least
  * n_cta * n_marks entries, CTA-major; *n_cta, *n_marks (may be NULL) get the
  * sizes.  MOE_ERR_STATE if no such step ran. */
 int moe_debug_step_trace(moe_layer_t layer, uint64_t* out, int cap, int* n_cta, int* n_marks);

@@ -449,12 +449,22 @@ MOE_DEV void stage_block(const Geo& g, const GemvArgs& a, const SG& p, const Ent
     }
   } else {
     const int nrb = p.K / kBoxRows;   // phase-1 column blocks per matrix
-    if (tid < nt) {
-      const float* hm = a.hmax + (size_t)(rowt + tid) * 2 * nrb;
+    // a warp per row (tid is warp-aligned): its lanes load the row's 2 nrb
+    // block maxima together -- one round trip, not one per block -- and
+    // combine them by a warp max (the same maximum in any order)
+    const int lane = tid & 31;
+    for (int t = tid >> 5; t < nt; t += nthr >> 5) {
+      const float* hm = a.hmax + (size_t)(rowt + t) * 2 * nrb;
       float ma = 0.f, mu = 0.f;
-      for (int i = 0; i < nrb; ++i) {
+#pragma unroll 4
+      for (int i = lane; i < nrb; i += 32) {
         ma = fmaxf(ma, __ldcg(hm + i));
         mu = fmaxf(mu, __ldcg(hm + nrb + i));
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, o));
+        mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, o));
       }
       const float bound = ma * mu;
       int s = 0;
@@ -463,7 +473,7 @@ MOE_DEV void stage_block(const Geo& g, const GemvArgs& a, const SG& p, const Ent
         frexpf(bound, &ex);
         s = max(-100, min(100, ex - 15));
       }
-      sexp_b[tid] = s;
+      if (lane == 0) sexp_b[t] = s;
     }
     asm volatile("bar.sync %0, %1;" :: "r"(bar), "r"(nthr) : "memory");
     const int k4n = p.K / 4;
@@ -690,7 +700,8 @@ MOE_DEV void compute(const Geo& g, const GemvArgs& a, const SG& p, const EntryTa
 template <int FMT, int PH, bool HOST>
 MOE_DEV void reduce(const Geo& g, const GemvArgs& a, const SG& p, const EntryTable& T, const Range& rr,
                     const Smem& S, Small& sm, Ring& ring, bool first_staged, const __nv_bfloat16* __restrict__ x,
-                    const int* __restrict__ xexp, float* __restrict__ h, float* __restrict__ O, long long wl) {
+                    const int* __restrict__ xexp, float* __restrict__ h, float* __restrict__ O, long long wl,
+                    unsigned long long* mk = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool ALL = PH == 1 && p.all;
   const int te = threadIdx.x - (kCW + 1) * 32;   // 0 .. kET - 1
@@ -717,8 +728,11 @@ MOE_DEV void reduce(const Geo& g, const GemvArgs& a, const SG& p, const EntryTab
       ++bs_st;
       i = 1;
     }
-    for (; i < p.XB; ++i)
+    for (; i < p.XB; ++i) {
       if (cursor_next(cs, g, a, T, p, rr)) stage(cs, bs_st++);
+      // mk (may be null): the first block staged, stamped by thread 0
+      if (mk && i == 0 && te == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(mk[0]));
+    }
   }
   while (cursor_next(cr, g, a, T, p, rr)) {
     const int xb = bs_rd % p.XB;

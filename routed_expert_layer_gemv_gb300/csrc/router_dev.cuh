@@ -95,13 +95,24 @@ MOE_DEV void stage_logits(const float* logits, int t, int E, float* Ls) {
 MOE_DEV int token_exp(const __nv_bfloat16* __restrict__ xr, int d) {
   const int lane = threadIdx.x & 31;
   const uint4* x4 = reinterpret_cast<const uint4*>(xr);
+  const int n = d / 8;
   float m = 0.f;
-  for (int i = lane; i < d / 8; i += 32) {
-    const uint4 v = x4[i];
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  // eight 16-byte loads per lane in flight before any use (one round trip
+  // for d <= 2048); zero padding leaves the maximum unchanged
+  for (int i0 = lane; i0 < n; i0 += 8 * 32) {
+    uint4 v[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xffff0000u))));
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 32 * u;
+      v[u] = i < n ? x4[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[q] << 16)), fabsf(__uint_as_float(wv[q] & 0xffff0000u))));
+    }
   }
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   int s = 0;

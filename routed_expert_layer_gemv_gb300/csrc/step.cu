@@ -378,7 +378,7 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     produce_drain(S, p1.D, ring, a.err);
   } else if (warp < kCW) {
     compute<FMT, 1, HOST>(g, ga, p1, T, r1, S, sm, ring, wl, mark ? mark + 13 : nullptr);
-    compute<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, wl);
+    compute<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, wl, mark ? mark + 15 : nullptr);
   } else {
     reduce<FMT, 1, HOST>(g, ga, p1, T, r1, S, sm, ring, first_staged, s.x, C.xexp, s.h, s.O, wl);
     // this CTA's h rows are written: barrier 2, then phase 2 stages h of any CTA
@@ -391,7 +391,7 @@ step_kernel(const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUte
     }
     __syncwarp();
     epi_sync();
-    reduce<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, false, s.x, C.xexp, s.h, s.O, wl);
+    reduce<FMT, 2, HOST>(g, ga, p2, T, r2, S, sm, ring, false, s.x, C.xexp, s.h, s.O, wl, mark ? mark + 17 : nullptr);
     epi_sync();
     if (warp == kCW + 1 && lane == 0) {
       if (mark) mark[8] = gtimer();

@@ -41,9 +41,10 @@ struct StepArgs {
 // barrier 3 passed, done (global timer, ns); then the SM clock (clock64) at
 // the first and the last mark, which give the clock rate the step ran at;
 // then (global timer) the first phase-1 stage landed and the last consumed,
-// as compute warp 0 saw them (left from an earlier step when the CTA had no
-// phase-1 work).
-constexpr int kStepMarks = 15;
+// as compute warp 0 saw them, the same for phase 2, and the first phase-2
+// activation block staged by the epilogue (left from an earlier step when the
+// CTA had no such work).
+constexpr int kStepMarks = 18;
 
 struct StepPlan {
   gv::SG p1, p2;   // the two phases' geometry, sharing one ring layout

@@ -265,7 +265,7 @@ def test_decode_path_selection():
     capi.moe_profile(L.h, False)
     assert len(tr) == torch.cuda.get_device_properties(0).multi_processor_count
     for row in tr:
-        assert len(row) == 15 and all(b >= a for a, b in zip(row[:11], row[1:11])) and row[12] > row[11]
+        assert len(row) == 18 and all(b >= a for a, b in zip(row[:11], row[1:11])) and row[12] > row[11]
     capi.moe_set_decode_path(L.h, capi.MOE_DECODE_CHAIN)
     _, info = L.forward(bf16_tensor(x[:8]), regime=DEC)
     assert info.fused_step == 0
