@@ -14,9 +14,14 @@ below are the public ones:
 * MXFP4 = E2M1 elements, one E8M0 scale per 32 consecutive K elements.
 * NVFP4 = E2M1 elements, one E4M3 scale per 16 K elements, one fp32 scale per
   tensor.
+* MXFP8 (the "FP8" format, OCP MX v1.0) = E4M3 elements, one E8M0 scale per
+  32 K elements.
+* BF16 = the upper 16 bits of an IEEE fp32 value (sign, 8 exponent bits, 7
+  mantissa bits), no scales.
 
-Packing (pages silent; this build's layout): two codes per byte, the low
-nibble holds the even K index; scales are row-major [rows, K / block].
+Packing (pages silent; this build's layout): FP4 codes two per byte, the low
+nibble holds the even K index; E4M3 codes one byte per element; bf16 elements
+as little-endian byte pairs; scales are row-major [rows, K / block].
 """
 from __future__ import annotations
 
@@ -63,12 +68,25 @@ def unpack_codes(codes: np.ndarray) -> np.ndarray:
     return out
 
 
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    """Values of bf16 bit patterns: the fp32 whose upper half they are."""
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def dequant(codes: np.ndarray, scales: np.ndarray, tscale: float, fmt: str) -> np.ndarray:
-    """FP64 [rows, K] values of one block-scaled FP4 matrix.
+    """FP64 [rows, K] values of one weight matrix.
 
     MXFP4: w[r, i] = E2M1(c[r, i]) * E8M0(s[r, i // 32]).
     NVFP4: w[r, i] = E2M1(c[r, i]) * E4M3(s[r, i // 16]) * tscale.
+    MXFP8: w[r, i] = E4M3(c[r, i]) * E8M0(s[r, i // 32]).
+    BF16:  w[r, i] = bf16(bits of element i).
     """
+    if fmt == "bf16":
+        b = np.ascontiguousarray(codes, dtype=np.uint8)
+        return bf16_value(b.view("<u2").reshape(b.shape[0], b.shape[1] // 2))
+    if fmt == "mxfp8":
+        vals = E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+        return vals * np.repeat(E8M0_TABLE[scales], 32, axis=1)
     c = unpack_codes(codes)
     vals = E2M1_TABLE[c]
     if fmt == "mxfp4":

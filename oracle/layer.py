@@ -112,7 +112,14 @@ def dequant_expert(w: Dict, fmt: str) -> Dict[str, np.ndarray]:
 
 
 def act_roundtrip(v: np.ndarray, fmt: str, g: float) -> np.ndarray:
-    """The values the FP4 activation quantiser hands to the MMA (FP64)."""
+    """The values the prefill activation quantiser hands to the MMA (FP64):
+    the weight's block format (FP4 weights), MXFP8 (MXFP8 weights), bf16
+    (BF16 weights)."""
+    if fmt == "bf16":
+        return quant.round_bf16(v)
+    if fmt == "mxfp8":
+        c, s = quant.quant_mxfp8(v)
+        return formats.dequant(c, s, 1.0, "mxfp8")
     if fmt == "mxfp4":
         c, s = quant.quant_mxfp4(v)
         return formats.dequant(c, s, 1.0, "mxfp4")

@@ -42,6 +42,8 @@ namespace {
 
 constexpr int kMXFP4 = 0;
 constexpr int kNVFP4 = 1;
+constexpr int kMXFP8 = 2;   // E4M3 elements, E8M0 per 32
+constexpr int kBF16 = 3;    // bf16 elements, no scales
 
 double e2m1_value(int c) {
   const int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
@@ -93,6 +95,22 @@ int e4m3_encode_satfinite(double v) {
   return pick;
 }
 
+// bf16 bits -> value: the fp32 whose upper half they are.
+double bf16_value(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+// fp32 -> bf16 bits, nearest even (NaN stays NaN).
+uint16_t bf16_round_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x7FFFFFu)) return (uint16_t)((u >> 16) | 0x40);
+  return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
 double silu(double z) { return z / (1.0 + std::exp(-z)); }
 
 int nthreads(int want) {
@@ -119,10 +137,26 @@ double orc_e2m1(int code) { return e2m1_value(code & 15); }
 double orc_e8m0(int x) { return e8m0_value(x & 255); }
 double orc_e4m3(int b) { return e4m3_value(b & 255); }
 
-// One block-scaled FP4 matrix [rows, K] to FP64:
-// MXFP4 w = E2M1(c) E8M0(s) (block 32), NVFP4 w = E2M1(c) E4M3(s) t (block 16).
+// One weight matrix [rows, K] to FP64:
+// MXFP4 w = E2M1(c) E8M0(s) (block 32), NVFP4 w = E2M1(c) E4M3(s) t (block 16),
+// MXFP8 w = E4M3(c) E8M0(s) (block 32, one byte per element), BF16 w = the
+// bf16 value of each little-endian byte pair.
 void orc_dequant(const uint8_t* codes, const uint8_t* scales, int rows, int K, int fmt, float tscale,
                  double* out) {
+  if (fmt == kMXFP8 || fmt == kBF16) {
+#pragma omp parallel for num_threads(nthreads(g_threads)) schedule(static)
+    for (int r = 0; r < rows; ++r)
+      for (int i = 0; i < K; ++i) {
+        if (fmt == kBF16) {
+          const uint8_t* b = codes + (size_t)r * K * 2 + (size_t)i * 2;
+          out[(size_t)r * K + i] = bf16_value((uint16_t)(b[0] | (b[1] << 8)));
+        } else {
+          out[(size_t)r * K + i] =
+              e4m3_value(codes[(size_t)r * K + i]) * e8m0_value(scales[(size_t)r * (K / 32) + i / 32]);
+        }
+      }
+    return;
+  }
   const int blk = fmt == kMXFP4 ? 32 : 16;
   const double t = fmt == kMXFP4 ? 1.0 : (double)tscale;
 #pragma omp parallel for num_threads(nthreads(g_threads)) schedule(static)
@@ -200,11 +234,56 @@ void orc_quant_nvfp4(const float* v, int rows, int K, float g, uint8_t* codes, u
   }
 }
 
-// The values the FP4 activation quantiser hands to the MMA, in FP64: v
-// (rows x K, FP64) rounded to fp32, quantised, dequantised (x g for NVFP4).
+// MXFP8 activation quantiser (OCP MX v1.0 conversion) of fp32 rows v [rows, K]:
+// per 32-block X = floor(log2(amax)) - 8 clamped to [-127, 127] (-127 for an
+// all-zero block), codes = E4M3(v / 2^X) (nearest even, saturating at 448,
+// sign kept) formed in fp32; one code byte per element.
+void orc_quant_mxfp8(const float* v, int rows, int K, uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for num_threads(nthreads(g_threads)) schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    for (int b = 0; b < K / 32; ++b) {
+      const float* blk = v + (size_t)r * K + (size_t)b * 32;
+      float amax = 0.f;
+      for (int i = 0; i < 32; ++i) amax = std::fmax(amax, std::fabs(blk[i]));
+      int X = -127;
+      if (amax > 0.f) {
+        int ex;
+        std::frexp((double)amax, &ex);
+        X = (ex - 1) - 8;
+        X = X < -127 ? -127 : X > 127 ? 127 : X;
+      }
+      scales[(size_t)r * (K / 32) + b] = (uint8_t)(X + 127);
+      for (int i = 0; i < 32; ++i) {
+        const float q = (float)((double)blk[i] * std::ldexp(1.0, -X));
+        codes[(size_t)r * K + (size_t)b * 32 + i] =
+            (uint8_t)(e4m3_encode_satfinite(std::fabs((double)q)) | (std::signbit(q) ? 0x80 : 0));
+      }
+    }
+  }
+}
+
+// v (FP64) rounded to fp32, then to bf16, nearest even, as FP64.
+void orc_round_bf16_n(const double* v, long long n, double* out) {
+  for (long long i = 0; i < n; ++i) out[i] = bf16_value(bf16_round_bits((float)v[i]));
+}
+
+// The values the prefill activation quantiser hands to the MMA, in FP64: v
+// (rows x K, FP64) rounded to fp32, quantised to the weight's block format
+// (FP4 weights), MXFP8 (MXFP8 weights) or rounded to bf16 (BF16 weights),
+// dequantised (x g for NVFP4).
 void orc_act_roundtrip(const double* v, int rows, int K, int fmt, float g, double* out) {
+  if (fmt == kBF16) {
+    orc_round_bf16_n(v, (long long)rows * K, out);
+    return;
+  }
   std::vector<float> v32((size_t)rows * K);
   for (size_t i = 0; i < v32.size(); ++i) v32[i] = (float)v[i];
+  if (fmt == kMXFP8) {
+    std::vector<uint8_t> c((size_t)rows * K), s((size_t)rows * K / 32);
+    orc_quant_mxfp8(v32.data(), rows, K, c.data(), s.data());
+    orc_dequant(c.data(), s.data(), rows, K, fmt, 1.0f, out);
+    return;
+  }
   const int blk = fmt == kMXFP4 ? 32 : 16;
   std::vector<uint8_t> c((size_t)rows * K / 2), s((size_t)rows * K / blk);
   if (fmt == kMXFP4) orc_quant_mxfp4(v32.data(), rows, K, c.data(), s.data());

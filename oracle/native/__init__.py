@@ -38,6 +38,8 @@ _SIGS = {
     "orc_silu_n": ([_D, C.c_longlong, _D], None),
     "orc_quant_mxfp4": ([_F, C.c_int, C.c_int, _U8, _U8], None),
     "orc_quant_nvfp4": ([_F, C.c_int, C.c_int, C.c_float, _U8, _U8], None),
+    "orc_quant_mxfp8": ([_F, C.c_int, C.c_int, _U8, _U8], None),
+    "orc_round_bf16_n": ([_D, C.c_longlong, _D], None),
     "orc_act_roundtrip": ([_D, C.c_int, C.c_int, C.c_int, C.c_float, _D], None),
     "orc_router": ([_D, _F, _F, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _I, _D, _D], None),
     "orc_permute": ([_I, C.c_int, C.c_int, C.c_int, _LL, _LL, _LL, _LL], None),

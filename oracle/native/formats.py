@@ -35,12 +35,18 @@ def unpack_codes(codes: np.ndarray) -> np.ndarray:
     return out
 
 
+FMT_ID = {"mxfp4": 0, "nvfp4": 1, "mxfp8": 2, "bf16": 3}
+_ELEMS_PER_BYTE = {"mxfp4": 2.0, "nvfp4": 2.0, "mxfp8": 1.0, "bf16": 0.5}
+
+
 def dequant(codes: np.ndarray, scales: np.ndarray, tscale: float, fmt: str) -> np.ndarray:
-    """FP64 [rows, K] of one block-scaled FP4 matrix (C++ orc_dequant)."""
+    """FP64 [rows, K] of one weight matrix (C++ orc_dequant)."""
     c = arr(codes, np.uint8)
     s = arr(scales, np.uint8)
-    rows, K = c.shape[0], c.shape[1] * 2
+    rows, K = c.shape[0], int(c.shape[1] * _ELEMS_PER_BYTE[fmt])
+    if s.size == 0:
+        s = np.zeros(1, dtype=np.uint8)
     out = np.empty((rows, K), dtype=np.float64)
-    lib().orc_dequant(ptr(c, C.c_uint8), ptr(s, C.c_uint8), rows, K, 0 if fmt == "mxfp4" else 1,
+    lib().orc_dequant(ptr(c, C.c_uint8), ptr(s, C.c_uint8), rows, K, FMT_ID[fmt],
                       float(np.float32(tscale)), ptr(out, C.c_double))
     return out

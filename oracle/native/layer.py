@@ -20,7 +20,7 @@ from . import formats
 
 
 def _fmt(fmt: str) -> int:
-    return 0 if fmt == "mxfp4" else 1
+    return formats.FMT_ID[fmt]
 
 
 def router(x, W_r, bias, k: int, norm_topk: bool = True):

@@ -43,3 +43,21 @@ def quant_nvfp4(v: np.ndarray, g: float):
     lib().orc_quant_nvfp4(ptr(v32, C.c_float), rows, K, float(np.float32(g)), ptr(codes, C.c_uint8),
                           ptr(scales, C.c_uint8))
     return codes, scales
+
+
+def quant_mxfp8(v: np.ndarray):
+    """(E4M3 bytes uint8 [rows, K], E8M0 bytes [rows, K/32]) of rows v."""
+    v32 = arr(v, np.float32)
+    rows, K = v32.shape
+    codes = np.empty((rows, K), dtype=np.uint8)
+    scales = np.empty((rows, K // 32), dtype=np.uint8)
+    lib().orc_quant_mxfp8(ptr(v32, C.c_float), rows, K, ptr(codes, C.c_uint8), ptr(scales, C.c_uint8))
+    return codes, scales
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """v rounded to fp32, then to bf16 (each nearest even), as FP64."""
+    v = arr(v, np.float64)
+    out = np.empty(v.shape, dtype=np.float64)
+    lib().orc_round_bf16_n(ptr(v, C.c_double), v.size, ptr(out, C.c_double))
+    return out

@@ -17,6 +17,13 @@ quantised to the weight's block format:
   elements are v / (scale * g) rounded to E2M1.  A block whose scale is 0
   gets all-zero codes.
 
+For the FP8 and BF16 weight formats (juejin.cn §五 lists FP8 and BF16 next to
+the FP4 ones) the prefill regime's activations take the weight's element
+type: MXFP8 weights meet MXFP8 activations (W8A8; OCP MX v1.0 conversion: per
+32-block X = floor(log2(amax)) - 8 (8 = the largest E4M3 exponent), elements
+v / 2^X rounded to E4M3, nearest even, saturating at 448), BF16 weights meet
+bf16 activations (W16A16; v rounded to bf16, nearest even).
+
 Where a floating-point value decides a code, the quotient is formed in fp32
 (as the CUDA kernels form it), with IEEE round-to-nearest division, so both
 sides take the same decision from the same input.  Rounding keeps the sign: a
@@ -61,6 +68,38 @@ def e4m3_encode_satfinite(v: np.ndarray) -> np.ndarray:
     pick = np.where(even.any(axis=-1), np.argmax(even, axis=-1), np.argmax(cand, axis=-1))
     pick = np.where(v >= 448.0, 0x7E, pick)
     return pick.astype(np.uint8)
+
+
+def e4m3_encode_signed(q: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 byte of each value (ties to the even byte, magnitudes of
+    448 and above saturate to 448, sign kept: -0 is 0x80)."""
+    q = np.asarray(q, dtype=np.float64)
+    mag = e4m3_encode_satfinite(np.abs(q))
+    return (mag | (np.signbit(q).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def quant_mxfp8(v: np.ndarray):
+    """Quantise rows v [rows, K] (values exact in fp32) to MXFP8.
+
+    Returns (E4M3 bytes uint8 [rows, K], E8M0 bytes [rows, K/32])."""
+    v32 = np.asarray(v, dtype=np.float32)
+    rows, K = v32.shape
+    blk = v32.reshape(rows, K // 32, 32)
+    amax = np.abs(blk).max(axis=-1).astype(np.float64)
+    _, ex = np.frexp(amax)                          # amax = m * 2^ex, m in [0.5, 1)
+    X = np.where(amax > 0, (ex - 1) - 8, -127)      # floor(log2 amax) - 8
+    X = np.clip(X, -127, 127)
+    q = (blk.astype(np.float64) * np.exp2(-X)[..., None]).astype(np.float32)   # exact (power of two)
+    codes = e4m3_encode_signed(q.astype(np.float64)).reshape(rows, K)
+    return codes, (X + 127).astype(np.uint8)
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """v (FP64) rounded to fp32, then to bf16 (each nearest even): the bf16
+    activations the W16A16 MMA takes (FP64 values)."""
+    u = np.ascontiguousarray(np.asarray(v, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint32)
+    return (r << 16).astype(np.uint32).view(np.float32).astype(np.float64)
 
 
 def _pack(codes: np.ndarray) -> np.ndarray:

@@ -28,6 +28,12 @@ import numpy as np
 
 MXFP4 = "mxfp4"
 NVFP4 = "nvfp4"
+MXFP8 = "mxfp8"
+BF16 = "bf16"
+
+# bits per weight code, and the K elements one block scale covers (0: none)
+CODE_BITS = {MXFP4: 4, NVFP4: 4, MXFP8: 8, BF16: 16}
+SCALE_BLOCK = {MXFP4: 32, NVFP4: 16, MXFP8: 32, BF16: 0}
 
 # substream ids (one per tensor kind)
 _SID_EXPERT = 1
@@ -48,7 +54,8 @@ class LayerSpec:
     d_model: int
     d_ff: int
     n_slots: int           # expert-cache slots on the GPU
-    fmt: str = MXFP4       # MXFP4 (E8M0 per 32) or NVFP4 (E4M3 per 16 + fp32 per tensor)
+    fmt: str = MXFP4       # MXFP4 (E8M0 per 32), NVFP4 (E4M3 per 16 + fp32 per tensor),
+                           # MXFP8 (E4M3 elements, E8M0 per 32) or BF16 (no scales)
     has_shared: bool = False
     has_bias: bool = False
     norm_topk: bool = True
@@ -57,7 +64,8 @@ class LayerSpec:
 
     @property
     def block(self) -> int:
-        return 32 if self.fmt == MXFP4 else 16
+        """K elements per block scale (0: the format has none)."""
+        return SCALE_BLOCK[self.fmt]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -122,15 +130,20 @@ def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
 
 @dataclasses.dataclass
 class Matrix:
-    """One FP4 weight matrix [rows, K], K contiguous.
+    """One weight matrix [rows, K], K contiguous.
 
-    codes  uint8 [rows, K/2]   two E2M1 codes per byte, low nibble = even K
-    scales uint8 [rows, K/B]   E8M0 (MXFP4, B=32) or E4M3 (NVFP4, B=16) bytes
-    tscale float32             per-tensor scale (NVFP4; 1.0 for MXFP4)
+    codes  uint8 [rows, K bits / 8]  MXFP4 / NVFP4: two E2M1 codes per byte,
+                                     low nibble = even K; MXFP8: one E4M3 byte
+                                     per element; BF16: the bf16 bits of each
+                                     element, little-endian byte pairs
+    scales uint8 [rows, K/B]         E8M0 (MXFP4, MXFP8: B=32) or E4M3 (NVFP4,
+                                     B=16) bytes; [rows, 0] for BF16
+    tscale float32                   per-tensor scale (NVFP4; 1.0 otherwise)
     """
     codes: np.ndarray
     scales: np.ndarray
     tscale: np.float32
+    fmt: str = MXFP4
 
     @property
     def rows(self) -> int:
@@ -138,10 +151,25 @@ class Matrix:
 
     @property
     def K(self) -> int:
-        return self.codes.shape[1] * 2
+        return self.codes.shape[1] * 8 // CODE_BITS[self.fmt]
 
 
 def _draw_matrix(g: np.random.Generator, rows: int, K: int, fmt: str) -> Matrix:
+    if fmt == MXFP8:
+        # E4M3 elements: random sign, exponent field 4..10 (values 2^-3 .. 15),
+        # any mantissa; E8M0 exponent uniform over -10..-8 (biased 117..119):
+        # a weight RMS near the FP4 formats'
+        sgn = g.integers(0, 2, size=(rows, K), dtype=np.uint8)
+        e = g.integers(4, 11, size=(rows, K), dtype=np.uint8)
+        m = g.integers(0, 8, size=(rows, K), dtype=np.uint8)
+        codes = ((sgn << 7) | (e << 3) | m).astype(np.uint8)
+        scales = g.integers(127 - 10, 127 - 8 + 1, size=(rows, K // 32), dtype=np.uint8)
+        return Matrix(codes, scales, np.float32(1.0), fmt)
+    if fmt == BF16:
+        # bf16 (RNE) of N(0, 0.05^2) draws
+        bits = f64_to_bf16_bits(g.standard_normal((rows, K)) * 0.05)
+        return Matrix(np.ascontiguousarray(bits).view(np.uint8).reshape(rows, 2 * K),
+                      np.zeros((rows, 0), dtype=np.uint8), np.float32(1.0), fmt)
     # E2M1 codes uniform over all 16 values -> packed bytes uniform over 256
     codes = np.frombuffer(g.bytes(rows * (K // 2)), dtype=np.uint8).reshape(rows, K // 2).copy()
     if fmt == MXFP4:
@@ -154,7 +182,7 @@ def _draw_matrix(g: np.random.Generator, rows: int, K: int, fmt: str) -> Matrix:
         m = g.integers(0, 8, size=(rows, K // 16), dtype=np.uint8)
         scales = ((e << 3) | m).astype(np.uint8)
         tscale = np.float32(2.0 ** -6)
-    return Matrix(codes, scales, tscale)
+    return Matrix(codes, scales, tscale, fmt)
 
 
 def expert_weights(spec: LayerSpec, seed: int, e: int, shared: bool = False) -> Dict[str, Matrix]:

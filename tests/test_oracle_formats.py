@@ -105,3 +105,25 @@ def test_dequant_matches_elementwise_loop(fmt):
         ts = np.float32(2.0 ** -6)
     got = formats.dequant(codes, scales, ts, fmt)
     assert np.array_equal(got, _loop_dequant(codes, scales, ts, fmt))
+
+
+def test_mxfp8_dequant_against_torch_float8_and_ldexp():
+    # E4M3 elements through torch's float8_e4m3fn decoding, times 2^(s - 127)
+    g = np.random.default_rng(5)
+    rows, K = 6, 96
+    codes = g.integers(0, 256, (rows, K), dtype=np.uint8)
+    codes[codes & 0x7F == 0x7F] = 0x10   # no NaN codes
+    scales = g.integers(100, 150, (rows, K // 32), dtype=np.uint8)
+    e = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ref = np.array([[math.ldexp(e[r, i], int(scales[r, i // 32]) - 127) for i in range(K)] for r in range(rows)])
+    assert np.array_equal(formats.dequant(codes, scales, 1.0, "mxfp8"), ref)
+
+
+def test_bf16_dequant_against_torch_bfloat16():
+    # little-endian bf16 byte pairs decode as torch's bfloat16 of the same bits
+    g = np.random.default_rng(6)
+    bits = g.integers(0, 1 << 16, (4, 40), dtype=np.uint16)
+    bits[(bits & 0x7F80) == 0x7F80] = 0x3F80   # no inf / NaN
+    ref = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = formats.dequant(bits.view(np.uint8).reshape(4, 80), np.zeros((4, 0), np.uint8), 1.0, "bf16")
+    assert np.array_equal(got, ref)

@@ -226,7 +226,8 @@ def test_native_and_numpy_oracles_agree():
     # ids, permutation and quantiser codes exactly, values to FP64 rounding
     from oracle import layer as np_layer
     from oracle.native import layer as cpp_layer
-    for fmt, shared, bias in (("mxfp4", False, False), ("nvfp4", True, True)):
+    for fmt, shared, bias in (("mxfp4", False, False), ("nvfp4", True, True), ("mxfp8", True, False),
+                              ("bf16", False, True)):
         spec = wl.LayerSpec(E=12, k=3, d_model=128, d_ff=64, n_slots=12, fmt=fmt, has_shared=shared,
                             has_bias=bias)
         W_r, b = wl.router_weights(spec, 8)

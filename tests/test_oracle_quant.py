@@ -132,3 +132,41 @@ def test_quant_error_bounded_by_half_step():
     err = np.abs(w - v) / scale
     inside = np.abs(q) <= 6
     assert (err[inside] <= np.where(np.abs(q[inside]) < 2, 0.25, np.where(np.abs(q[inside]) < 4, 0.5, 1.0)) + 1e-12).all()
+
+
+def test_mxfp8_scale_exponent_and_codes_against_torch():
+    # X = floor(log2 amax) - 8 (math.frexp); elements v / 2^X rounded by torch's
+    # float8_e4m3fn conversion (nearest even) after clamping to +-448
+    g = np.random.default_rng(8)
+    v = (g.standard_normal((7, 64)) * np.exp2(g.integers(-20, 20, (7, 1)))).astype(np.float32)
+    v[3, :32] = 0.0
+    codes, scales = quant.quant_mxfp8(v)
+    for r in range(7):
+        for b in range(2):
+            blk = v[r, 32 * b:32 * (b + 1)].astype(np.float64)
+            amax = np.abs(blk).max()
+            X = -127 if amax == 0 else math.frexp(amax)[1] - 1 - 8
+            assert scales[r, b] == X + 127
+            q = np.clip(blk * 2.0 ** -X, -448.0, 448.0).astype(np.float32)
+            ref = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            got = codes[r, 32 * b:32 * (b + 1)]
+            nz = q != 0   # torch's sign of a zero result follows the input; compare magnitudes there
+            assert np.array_equal(got[nz], ref[nz]) and np.array_equal(got[~nz] & 0x7F, ref[~nz] & 0x7F)
+
+
+def test_mxfp8_exact_roundtrip_of_grid_values():
+    # values on the E4M3 grid times 2^X come back unchanged
+    g = np.random.default_rng(9)
+    e4 = formats.E4M3_TABLE[:0x7F]
+    mags = e4[(e4 >= 2.0 ** -6) & (e4 <= 448)]
+    v = g.choice(mags, size=(4, 64)) * g.choice([-1.0, 1.0], size=(4, 64))
+    v[:, ::32] = 448.0   # pins the block exponent: floor(log2 448) - 8 = 0
+    c, s = quant.quant_mxfp8((v * 2.0 ** -5).astype(np.float32))
+    assert np.array_equal(formats.dequant(c, s, 1.0, "mxfp8"), v * 2.0 ** -5)
+
+
+def test_bf16_rounding_against_torch():
+    g = np.random.default_rng(10)
+    v = g.standard_normal(2000) * np.exp2(g.integers(-30, 30, 2000))
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(quant.round_bf16(v), ref)
