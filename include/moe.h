@@ -46,14 +46,21 @@ extern "C" {
 #define MOE_ERR_STATE         -7  /* call made in the wrong state           */
 #define MOE_ERR_UNSUPPORTED   -8  /* valid request this build cannot serve  */
 
-/* ---- weight formats ---------------------------------------------------- */
+/* ---- weight formats ----------------------------------------------------
+ * The engine runs MXFP4, NVFP4, FP8 and BF16 checkpoints (juejin.cn overview,
+ * §五 模型生态与硬件支持; zhichai.net §五 for the FP4 ones). */
 #define MOE_MXFP4 0  /* E2M1 codes, one E8M0 scale per 32 along K            */
 #define MOE_NVFP4 1  /* E2M1 codes, one E4M3 scale per 16 along K, fp32/tensor */
+#define MOE_MXFP8 2  /* E4M3 codes (one byte each), one E8M0 scale per 32    */
+#define MOE_BF16  3  /* bf16 elements, no scales                             */
 
-/* ---- regimes ----------------------------------------------------------- */
+/* ---- regimes -----------------------------------------------------------
+ * Decode: the weights x bf16-class activations (A16), a GEMV.  Prefill: a
+ * tensor-core grouped GEMM whose activations take the weight's element type:
+ * FP4 x FP4 (MXFP4 / NVFP4), MXFP8 x MXFP8 (W8A8), bf16 x bf16 (W16A16). */
 #define MOE_REGIME_AUTO    0  /* decode for N <= 64, prefill otherwise       */
-#define MOE_REGIME_DECODE  1  /* FP4 weights x bf16 activations, GEMV        */
-#define MOE_REGIME_PREFILL 2  /* FP4 weights x FP4 activations, grouped GEMM */
+#define MOE_REGIME_DECODE  1  /* weights x bf16 activations, GEMV            */
+#define MOE_REGIME_PREFILL 2  /* weights x activations of their type, GEMM   */
 
 typedef struct moe_layer* moe_layer_t;
 typedef struct moe_stack* moe_stack_t;
@@ -65,7 +72,7 @@ typedef struct {
     int d_model;      /* multiple of 128 (of 256 for the prefill regime)      */
     int d_ff;         /* multiple of 128 (of 256 for the prefill regime)      */
     int n_slots;      /* GPU expert-cache slots, 1..E (a stack: 1..min(L E, 1024)) */
-    int fmt;          /* MOE_MXFP4 or MOE_NVFP4                               */
+    int fmt;          /* MOE_MXFP4, MOE_NVFP4, MOE_MXFP8 or MOE_BF16          */
     int has_shared;   /* 1: one always-on shared expert, weight 1, resident   */
     int norm_topk;    /* 1: gates renormalised over the k selected            */
     int has_bias;     /* 1: per-expert router bias added to the logits        */
@@ -76,9 +83,11 @@ typedef struct {
 
 /* Byte layout of one expert (identical in the host pool and in a slot).
  * Matrices are K-contiguous: gate [d_ff, d_model], up [d_ff, d_model],
- * down [d_model, d_ff].  Codes: two E2M1 per byte, low nibble = even K.
- * Scales: row-major [rows, K/32] E8M0 (MXFP4) or [rows, K/16] E4M3 (NVFP4).
- * tensor_scales: three fp32 (gate, up, down; 1.0 for MXFP4).  All offsets
+ * down [d_model, d_ff].  Codes: two E2M1 per byte, low nibble = even K
+ * (MXFP4, NVFP4); one E4M3 byte per element (MXFP8); bf16 elements as
+ * little-endian byte pairs (BF16).  Scales: row-major [rows, K/32] E8M0 (MXFP4,
+ * MXFP8) or [rows, K/16] E4M3 (NVFP4); none for BF16 (the scale offsets then
+ * coincide).  tensor_scales: three fp32 (gate, up, down; 1.0 except NVFP4).  All offsets
  * are multiples of 256 bytes; `bytes` is the padded size of one expert. */
 typedef struct {
     size_t bytes;

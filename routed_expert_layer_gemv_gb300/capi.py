@@ -28,6 +28,8 @@ MOE_ERR_UNSUPPORTED = -8
 
 MOE_MXFP4 = 0
 MOE_NVFP4 = 1
+MOE_MXFP8 = 2
+MOE_BF16 = 3
 
 MOE_PROF_NAMES = ["router", "permute", "lru", "gateup", "down", "combine", "fill", "prefill", "commit",
                   "step"]

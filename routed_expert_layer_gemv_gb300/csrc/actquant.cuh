@@ -1,4 +1,10 @@
-// FP4 activation quantisers of the prefill regime (block-scaled FP4 x FP4).
+// Activation quantisers of the prefill regime: FP4 for FP4 weights
+// (block-scaled FP4 x FP4), MXFP8 for MXFP8 weights (W8A8).
+//
+// MXFP8 (OCP MX v1.0 conversion, E4M3 elements): per 32 values X =
+// floor(log2(amax)) - 8, clamped to [-127, 127] (-127 for an all-zero block);
+// elements v * 2^-X rounded to E4M3, nearest even, saturating at 448, sign
+// kept.
 //
 // MXFP4 (OCP Microscaling v1.0 conversion): per 32 values along K the shared
 // exponent is X = floor(log2(amax)) - 2, clamped to [-127, 127] (-127 for an
@@ -80,6 +86,33 @@ MOE_DEV uint32_t quant_nv16(const float* v, float g, uint32_t* words) {
     words[w] = word;
   }
   return sb;
+}
+
+// Two E4M3 bytes of (lo, hi), lo in bits 0..7, nearest even, saturating at
+// 448; a negative value that rounds to zero keeps its sign (0x80).
+MOE_DEV uint32_t e4m3_pack2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return ((uint32_t)r | ((__float_as_uint(lo) >> 31) << 7) | ((__float_as_uint(hi) >> 31) << 15)) & 0xffffu;
+}
+
+// 32 values -> 32 E4M3 bytes (as 8 words) + E8M0 byte.
+MOE_DEV uint32_t quant_mx8_32(const float* v, uint32_t* words) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int X = -127;
+  if (amax > 0.f) {
+    int ex;
+    frexpf(amax, &ex);          // amax = m 2^ex, m in [0.5, 1)
+    X = max(-127, min(127, (ex - 1) - 8));
+  }
+  const float inv = pow2_any(-X);
+#pragma unroll
+  for (int w = 0; w < 8; ++w)
+    words[w] = e4m3_pack2(v[4 * w] * inv, v[4 * w + 1] * inv) |
+               (e4m3_pack2(v[4 * w + 2] * inv, v[4 * w + 3] * inv) << 16);
+  return (uint32_t)(X + 127);
 }
 
 }  // namespace moe

@@ -227,7 +227,8 @@ int check_desc(const moe_layer_desc* d, std::string* why, int max_slots) {
     *why = buf;
     return MOE_ERR_ARG;
   }
-  if (d->fmt != MOE_MXFP4 && d->fmt != MOE_NVFP4) return bad("fmt must be MOE_MXFP4 or MOE_NVFP4");
+  if (d->fmt != MOE_MXFP4 && d->fmt != MOE_NVFP4 && d->fmt != MOE_MXFP8 && d->fmt != MOE_BF16)
+    return bad("fmt must be MOE_MXFP4, MOE_NVFP4, MOE_MXFP8 or MOE_BF16");
   if (d->max_tokens < 1) return bad("max_tokens must be >= 1");
   if ((long long)d->max_tokens * (d->k + 1) > (1LL << 30)) return bad("max_tokens * (k+1) too large");
   if (d->fmt == MOE_NVFP4 && (!is_pow2_float(d->act_scale_x) || !is_pow2_float(d->act_scale_h))) {
@@ -240,15 +241,16 @@ int check_desc(const moe_layer_desc* d, std::string* why, int max_slots) {
 
 void fill_layout(const moe_layer_desc* d, moe_expert_layout* l) {
   const size_t D = d->d_model, F = d->d_ff;
-  const size_t blk = d->fmt == MOE_MXFP4 ? 32 : 16;
+  const size_t blk = fmt_block(d->fmt);          // 0: no scales
+  const size_t cb2 = fmt_code_bits(d->fmt);      // bits per element
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
-  l->gate_codes = take(F * D / 2);
-  l->up_codes = take(F * D / 2);
-  l->down_codes = take(D * F / 2);
-  l->gate_scales = take(F * D / blk);
-  l->up_scales = take(F * D / blk);
-  l->down_scales = take(D * F / blk);
+  l->gate_codes = take(F * D * cb2 / 8);
+  l->up_codes = take(F * D * cb2 / 8);
+  l->down_codes = take(D * F * cb2 / 8);
+  l->gate_scales = take(blk ? F * D / blk : 0);
+  l->up_scales = take(blk ? F * D / blk : 0);
+  l->down_scales = take(blk ? D * F / blk : 0);
   l->tensor_scales = take(16);
   l->bytes = off;
 }
@@ -258,7 +260,7 @@ Geo make_geo(const moe_layer_desc* d, const moe_expert_layout* l) {
   g.E = d->E; g.k = d->k; g.d = d->d_model; g.f = d->d_ff; g.S = d->n_slots; g.fmt = d->fmt;
   g.has_shared = d->has_shared ? 1 : 0; g.norm_topk = d->norm_topk ? 1 : 0;
   g.has_bias = d->has_bias ? 1 : 0;
-  g.blk = d->fmt == MOE_MXFP4 ? 32 : 16;
+  g.blk = fmt_block(d->fmt);
   g.ebytes = l->bytes;
   g.off_codes[0] = l->gate_codes; g.off_codes[1] = l->up_codes; g.off_codes[2] = l->down_codes;
   g.off_scales[0] = l->gate_scales; g.off_scales[1] = l->up_scales; g.off_scales[2] = l->down_scales;
@@ -560,10 +562,11 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
   MOE_ALLOC(rcounter, 16);
   MOE_ALLOC(step_trace, (size_t)std::max(L->num_sms, 1) * kStepMarks * 8);
   if (prefill_ok) {
-    MOE_ALLOC(xq_codes, prows * g.d / 2);
-    MOE_ALLOC(xq_scales, prows * (g.d / g.blk));
-    MOE_ALLOC(hq_codes, prows * g.f / 2);
-    MOE_ALLOC(hq_scales, prows * (g.f / g.blk));
+    // prefill activations in the weights' element type (codes, then block scales)
+    MOE_ALLOC(xq_codes, prows * g.d * fmt_code_bits(g.fmt) / 8);
+    MOE_ALLOC(xq_scales, prows * std::max(16, fmt_scale_row(g.fmt, g.d)));
+    MOE_ALLOC(hq_codes, prows * g.f * fmt_code_bits(g.fmt) / 8);
+    MOE_ALLOC(hq_scales, prows * std::max(16, fmt_scale_row(g.fmt, g.f)));
     MOE_ALLOC(tiles, prefill_tile_bytes(g, (int)Nm));
     MOE_ALLOC(n_tiles, 16);
   }
@@ -1538,9 +1541,12 @@ int moe_debug_last_hidden(moe_layer_t L, float* h, uint8_t* hq_codes, uint8_t* h
   const Geo& g = L->g;
   const size_t rows = (size_t)N * g.k + (g.has_shared ? N : 0);
   if (h) MOE_CUDA(L, cudaMemcpyAsync(h, L->h, rows * 2 * g.f * 4, cudaMemcpyDeviceToDevice, st));
-  if (hq_codes) MOE_CUDA(L, cudaMemcpyAsync(hq_codes, L->hq_codes, rows * g.f / 2, cudaMemcpyDeviceToDevice, st));
-  if (hq_scales)
-    MOE_CUDA(L, cudaMemcpyAsync(hq_scales, L->hq_scales, rows * (g.f / g.blk), cudaMemcpyDeviceToDevice, st));
+  if (hq_codes)
+    MOE_CUDA(L, cudaMemcpyAsync(hq_codes, L->hq_codes, rows * g.f * fmt_code_bits(g.fmt) / 8,
+                                cudaMemcpyDeviceToDevice, st));
+  if (hq_scales && fmt_scale_row(g.fmt, g.f))
+    MOE_CUDA(L, cudaMemcpyAsync(hq_scales, L->hq_scales, rows * fmt_scale_row(g.fmt, g.f),
+                                cudaMemcpyDeviceToDevice, st));
   return MOE_OK;
 }
 

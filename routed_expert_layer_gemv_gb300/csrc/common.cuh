@@ -104,6 +104,21 @@ __host__ __device__ inline int4* rec_entry(StepRecord* r, int E) {
 }
 inline size_t rec_dev_bytes(int E) { return ((rec_bytes(E) + 15) & ~size_t(15)) + sizeof(int4) * (size_t)E; }
 
+// ---------------------------------------------------------------- formats
+// Bits per weight element and the K elements one block scale covers (0: the
+// format has no block scales).  The prefill regime's activations take the
+// same element type and block (FP4 x FP4, MXFP8 x MXFP8, bf16 x bf16).
+__host__ __device__ constexpr int fmt_code_bits(int fmt) {
+  return fmt == MOE_MXFP8 ? 8 : fmt == MOE_BF16 ? 16 : 4;
+}
+__host__ __device__ constexpr int fmt_block(int fmt) {
+  return fmt == MOE_NVFP4 ? 16 : fmt == MOE_BF16 ? 0 : 32;
+}
+// Scale bytes of a K-long row (0 without block scales).
+__host__ __device__ constexpr int fmt_scale_row(int fmt, int K) {
+  return fmt_block(fmt) ? K / fmt_block(fmt) : 0;
+}
+
 // ---------------------------------------------------------------- layer geometry
 struct Geo {
   int E, k, d, f, S, fmt, has_shared, norm_topk, has_bias;

@@ -24,6 +24,41 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t*
   out[(size_t)r * K + i + 1] = __high2float(hv) * s;
 }
 
+// MXFP8 / BF16 matrices: one thread per element (E4M3 x E8M0, or the bf16 value).
+__global__ void dequant8_16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int rows,
+                                   int K, int fmt, float* __restrict__ out) {
+  const size_t p = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= (size_t)rows * K) return;
+  const int r = (int)(p / K), i = (int)(p % K);
+  if (fmt == MOE_BF16) {
+    const uint32_t lo = codes[2 * p], hi = codes[2 * p + 1];
+    out[p] = __uint_as_float((lo | (hi << 8)) << 16);
+  } else {
+    out[p] = e4m3_to_f32(codes[p]) * e8m0_to_f32(scales[(size_t)r * (K / 32) + i / 32]);
+  }
+}
+
+// Rows of 32-element blocks through the MXFP8 quantiser, or rounded to bf16.
+__global__ void actquant8_16_kernel(const float* __restrict__ v, int rows, int K, int fmt,
+                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int nb = K / 32;
+  const size_t b = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= (size_t)rows * nb) return;
+  const int r = (int)(b / nb), c = (int)(b % nb);
+  const float* src = v + (size_t)r * K + (size_t)c * 32;
+  if (fmt == MOE_BF16) {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(codes) + (size_t)r * K + (size_t)c * 32;
+    for (int i = 0; i < 32; ++i) dst[i] = __float2bfloat16_rn(src[i]);
+    return;
+  }
+  float vals[32];
+  for (int i = 0; i < 32; ++i) vals[i] = src[i];
+  uint32_t words[8];
+  scales[b] = (uint8_t)quant_mx8_32(vals, words);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(codes + (size_t)r * K + (size_t)c * 32);
+  for (int w = 0; w < 8; ++w) dst[w] = words[w];
+}
+
 __global__ void actquant_kernel(const float* __restrict__ v, int rows, int K, int fmt, float g,
                                 uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const int blk = fmt == MOE_MXFP4 ? 32 : 16;
@@ -57,6 +92,12 @@ cudaError_t launch_dequant(const Geo& g, const uint8_t* expert, int m, float* ou
   if (err != cudaSuccess) return err;
   err = cudaStreamSynchronize(st);
   if (err != cudaSuccess) return err;
+  if (g.fmt == MOE_MXFP8 || g.fmt == MOE_BF16) {
+    const size_t n = (size_t)rows * K;
+    dequant8_16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(expert + g.off_codes[m],
+                                                                    expert + g.off_scales[m], rows, K, g.fmt, out);
+    return cudaGetLastError();
+  }
   const size_t nbytes = (size_t)rows * (K / 2);
   dequant_kernel<<<(unsigned)((nbytes + 255) / 256), 256, 0, st>>>(
       expert + g.off_codes[m], expert + g.off_scales[m], tscale, rows, K, g.fmt, out);
@@ -65,6 +106,12 @@ cudaError_t launch_dequant(const Geo& g, const uint8_t* expert, int m, float* ou
 
 cudaError_t launch_actquant(const Geo& g, const float* v, int rows, int K, uint8_t* codes,
                             uint8_t* scales, float gscale, cudaStream_t st) {
+  if (g.fmt == MOE_MXFP8 || g.fmt == MOE_BF16) {
+    const size_t total = (size_t)rows * (K / 32);
+    if (total == 0) return cudaSuccess;
+    actquant8_16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(v, rows, K, g.fmt, codes, scales);
+    return cudaGetLastError();
+  }
   const int nb = K / g.blk;
   const size_t total = (size_t)rows * nb;
   if (total == 0) return cudaSuccess;

@@ -222,7 +222,7 @@ bool make_box_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t
   if (!fn) return false;
   cuuint64_t dims[3] = {row_bytes, rows, slots};
   cuuint64_t strides[2] = {row_bytes, slot_stride};
-  cuuint32_t box[3] = {kBoxK / 2, kBoxRows, 1};
+  cuuint32_t box[3] = {kBoxRowBytes, kBoxRows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -257,12 +257,14 @@ bool gemv_shape_ok(const Geo& g) {
 GemvPlan* gemv_plan_create(const Geo& g, const uint8_t* slots) {
   GemvPlan* pl = new GemvPlan();
   const int ns = g.nbuf;   // LRU slots' buffers, the shared expert's, the spares (+ a stack's other shared experts)
-  pl->ready = make_box_map(&pl->w[0], slots + g.off_codes[0], g.d / 2, g.f, ns, g.ebytes) &&
-              make_box_map(&pl->w[1], slots + g.off_codes[1], g.d / 2, g.f, ns, g.ebytes) &&
-              make_box_map(&pl->w[2], slots + g.off_codes[2], g.f / 2, g.d, ns, g.ebytes);
+  const int cb = fmt_code_bits(g.fmt);   // row bytes = K * cb / 8
+  pl->ready = make_box_map(&pl->w[0], slots + g.off_codes[0], (size_t)g.d * cb / 8, g.f, ns, g.ebytes) &&
+              make_box_map(&pl->w[1], slots + g.off_codes[1], (size_t)g.d * cb / 8, g.f, ns, g.ebytes) &&
+              make_box_map(&pl->w[2], slots + g.off_codes[2], (size_t)g.f * cb / 8, g.d, ns, g.ebytes);
   // scale maps only where a scale row is a 16-byte multiple (the phase uses them then)
   const SG p1 = make_sg(g, 1, 0), p2 = make_sg(g, 2, 0);
-  const uint32_t sb = kBoxes * (g.fmt == MOE_MXFP4 ? 8 : 16);
+  const uint32_t sb = kBoxes * p1.SBB;
+  if (sb == 0) return pl;   // no block scales
   if (pl->ready && p1.smode)
     pl->ready = make_scale_map(&pl->s[0], slots + g.off_scales[0], p1.scale_row, g.f, ns, g.ebytes, sb) &&
                 make_scale_map(&pl->s[1], slots + g.off_scales[1], p1.scale_row, g.f, ns, g.ebytes, sb);
@@ -280,7 +282,11 @@ cudaError_t launch_gemv_decode(const Geo& g, const GemvPlan* pl, const GemvArgs&
                                int phases) {
   if (g.fmt == MOE_MXFP4)
     return launch_fmt<MOE_MXFP4>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev, phases);
-  return launch_fmt<MOE_NVFP4>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev, phases);
+  if (g.fmt == MOE_NVFP4)
+    return launch_fmt<MOE_NVFP4>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev, phases);
+  if (g.fmt == MOE_MXFP8)
+    return launch_fmt<MOE_MXFP8>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev, phases);
+  return launch_fmt<MOE_BF16>(g, pl, a, x, xexp, h, O, n_ent_max, num_sms, st, ev, phases);
 }
 
 }  // namespace moe

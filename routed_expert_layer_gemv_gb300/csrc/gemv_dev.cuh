@@ -44,8 +44,8 @@ constexpr int kThreads = (kCW + 1 + kEW) * 32;
 constexpr int kET = kEW * 32;                // epilogue threads
 constexpr int kTG = 8;                       // tokens per group (one MMA N)
 constexpr int kBoxRows = 64;
-constexpr int kBoxK = 256;                   // codes per box row (128 bytes)
-constexpr int kBoxBytes = kBoxRows * kBoxK / 2;
+constexpr int kBoxRowBytes = 128;           // bytes per box row (256 FP4, 128 FP8, 64 bf16 elements)
+constexpr int kBoxBytes = kBoxRows * kBoxRowBytes;
 constexpr int kBoxes = 4;                    // boxes per stage
 constexpr int kMaxD = 8;                     // ring stages at most
 constexpr int kSmemBudget = 220 * 1024;
@@ -53,11 +53,12 @@ constexpr int kSmemBudget = 220 * 1024;
 // Geometry of one phase (host-computed, passed by value).
 struct SG {
   int K, R;           // reduction length, output rows per matrix
-  int KB;             // 256-K boxes per row (the last one may be half valid)
+  int bk;             // K elements per 128-byte box row: 256 (FP4), 128 (MXFP8), 64 (BF16)
+  int KB;             // boxes per row (an FP4 row's last one may be half valid)
   int NS;             // stages per unit
   int RB;             // 64-row blocks per matrix
   int UE;             // units per entry (RB per matrix, gate and up separately in phase 1)
-  int SBB;            // scale bytes per box row (8 MXFP4, 16 NVFP4)
+  int SBB;            // scale bytes per box row (8 MXFP4, 16 NVFP4, 4 MXFP8, 0 BF16)
   int smode;          // 1: a TMA box of the stage's scales; 0: the unit's whole scale rows
   int srow;           // staged scale bytes per row (4 * SBB, or scale_row)
   int codes_bytes;    // kBoxes code boxes
@@ -224,6 +225,8 @@ MOE_DEV bool cursor_next(Cursor& c, const Geo& g, const GemvArgs& a, const Entry
 // B-fragment order [32-K block][MMA step][lane = 4 t + q].  MXFP4 steps take
 // K 32J + 8q + 4s .. + 3, NVFP4 steps (one 16-block each) 32J + 16s + 4q ...
 MOE_DEV int xslot(int fmt, int t, int k4) {
+  // MXFP8 and BF16: one MMA step per 16 K, lane q holding K 4q .. 4q + 3
+  if (fmt == MOE_MXFP8 || fmt == MOE_BF16) return (k4 >> 2) * 32 + 4 * t + (k4 & 3);
   const int J = k4 >> 3, i = k4 & 7;
   const int s = fmt == MOE_MXFP4 ? (i & 1) : (i >> 2);
   const int q = fmt == MOE_MXFP4 ? (i >> 1) : (i & 3);
@@ -297,6 +300,74 @@ MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
   }
 }
 
+// Four E4M3 codes (one word, low byte = lowest K) -> two f16x2, exact (every
+// E4M3 value is an f16 value).
+MOE_DEV void e4m3x4_to_f16x4(uint32_t w, uint32_t (&o)[2]) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]) : "r"(w));
+}
+
+// One warp's 16 x 128 MXFP8 tile: acc += W x.  Codes: 128-byte rows of E4M3
+// bytes, 16-byte chunk j of row r at chunk j ^ (r & 7).  Lane (g, q) takes
+// word q of chunk j (codes 16 j + 4q .. + 3) of rows g and g + 8; as f16
+// pairs they are the MMA's K slots 2q, 2q + 1 and 2q + 8, 2q + 9, so chunk j
+// is one m16n8k16 step (the activations are staged in that order, xslot).
+// Chunks 2p and 2p + 1 share E8M0 scale byte p of the box.
+MOE_DEV void tile_mx8(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, const uint2* xb, int lane,
+                      float (&acc)[4]) {
+  const int g = lane >> 2, q = lane & 3;
+  const uint32_t w0 = lds32(s0p), w1 = lds32(s1p);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float d[4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int j = 2 * p + hh;
+      const int co = ((j ^ g) << 4) + 4 * q;
+      uint32_t f0[2], f1[2];
+      e4m3x4_to_f16x4(lds32(cs + 128 * g + co), f0);
+      e4m3x4_to_f16x4(lds32(cs + 128 * (g + 8) + co), f1);
+      const uint2 b = xb[j * 32 + lane];
+      if (hh == 0) mma16816(d, f0[0], f1[0], f0[1], f1[1], b);
+      else mma16816_acc(d, f0[0], f1[0], f0[1], f1[1], b);
+    }
+    float sg, sg8;
+    if (p == 0) { sg = e8m0_byte<0>(w0); sg8 = e8m0_byte<0>(w1); }
+    else if (p == 1) { sg = e8m0_byte<1>(w0); sg8 = e8m0_byte<1>(w1); }
+    else if (p == 2) { sg = e8m0_byte<2>(w0); sg8 = e8m0_byte<2>(w1); }
+    else { sg = e8m0_byte<3>(w0); sg8 = e8m0_byte<3>(w1); }
+    acc[0] = fmaf(d[0], sg, acc[0]);
+    acc[1] = fmaf(d[1], sg, acc[1]);
+    acc[2] = fmaf(d[2], sg8, acc[2]);
+    acc[3] = fmaf(d[3], sg8, acc[3]);
+  }
+}
+
+MOE_DEV void mma16816_bf16_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint2 b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
+}
+
+// One warp's 16 x 64 bf16 tile: acc += W x (bf16 MMA, fp32 sums).  Rows of
+// 128 bytes (64 elements, 16-byte chunks swizzled as above); for each 16-K
+// group G lane (g, q) takes 8 bytes -- elements 16 G + 4q .. + 3 -- of rows g
+// and g + 8: the MMA's K slots 2q, 2q + 1 and 2q + 8, 2q + 9.
+MOE_DEV void tile_bf16(const uint8_t* cs, const uint2* xb, int lane, float (&acc)[4]) {
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int G = 0; G < 4; ++G) {
+    const int c = 2 * G + (q >> 1);
+    const int co = ((c ^ g) << 4) + 8 * (q & 1);
+    const uint2 r0 = *reinterpret_cast<const uint2*>(cs + 128 * g + co);
+    const uint2 r1 = *reinterpret_cast<const uint2*>(cs + 128 * (g + 8) + co);
+    mma16816_bf16_acc(acc, r0.x, r1.x, r0.y, r1.y, xb[G * 32 + lane]);
+  }
+}
+
 // The part of a stage that compute warp w = 4b + q reads -- rows 16q .. 16q + 15
 // of code box b and those rows' scale bytes of the box -- for a miss whose
 // weights stream from the host pool: loaded from the pool into the stage in
@@ -306,7 +377,7 @@ MOE_DEV void tile_nv(const uint8_t* cs, const uint8_t* s0p, const uint8_t* s1p, 
 MOE_DEV void host_part(const Geo& g, const SG& p, const GemvArgs& a, const Entry& en, int mm, int rb, int st,
                        uint8_t* stg, int warp, int lane) {
   const int bslot = warp >> 2, quarter = warp & 3;
-  const int kb = st * kBoxes + bslot, rowb = p.K / 2;
+  const int kb = st * kBoxes + bslot, rowb = p.K * fmt_code_bits(g.fmt) / 8;
   if (kb < p.KB) {
     const uint8_t* hw = a.host_pool + (size_t)en.ex * g.ebytes;
     uint8_t* ew = const_cast<uint8_t*>(a.slots) + (size_t)en.slot * g.ebytes;
@@ -384,7 +455,7 @@ MOE_DEV void stage_all(const SG& p, int N, const __nv_bfloat16* __restrict__ x, 
                        int nthr, int bar) {
   const int w = tid >> 5, l = tid & 31, nw = nthr >> 5;
   for (int t = w; t < N; t += nw) {
-    const int s = rt::token_exp(x + (size_t)t * p.K, p.K);
+    const int s = FMT == MOE_BF16 ? 0 : rt::token_exp(x + (size_t)t * p.K, p.K);   // bf16 MMA: x as it is
     if (l == 0) sexp[t] = s;
   }
   asm volatile("bar.sync %0, %1;" :: "r"(bar), "r"(nthr) : "memory");
@@ -398,9 +469,13 @@ MOE_DEV void stage_all(const SG& p, int N, const __nv_bfloat16* __restrict__ x, 
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const __half2 hh = __floats2half2_rn(__uint_as_float(wv[e] << 16) * sc,
-                                             __uint_as_float(wv[e] & 0xffff0000u) * sc);
-        o[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        if (FMT == MOE_BF16) {
+          o[e] = wv[e];
+        } else {
+          const __half2 hh = __floats2half2_rn(__uint_as_float(wv[e] << 16) * sc,
+                                               __uint_as_float(wv[e] & 0xffff0000u) * sc);
+          o[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
       }
     }
     xs[xslot(FMT, t, 2 * k8)] = make_uint2(o[0], o[1]);
@@ -427,7 +502,7 @@ MOE_DEV void stage_block(const Geo& g, const GemvArgs& a, const SG& p, const Ent
       const int row = rowt + tid;
       const int tok = en.shared ? row - en.row0 : a.tok_of[row];
       stok[tid] = tok;
-      sexp_b[tid] = xexp[tok];
+      sexp_b[tid] = FMT == MOE_BF16 ? 0 : xexp[tok];
     }
     asm volatile("bar.sync %0, %1;" :: "r"(bar), "r"(nthr) : "memory");
     const int k8n = p.K / 8;
@@ -440,9 +515,13 @@ MOE_DEV void stage_block(const Geo& g, const GemvArgs& a, const SG& p, const Ent
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const __half2 hh = __floats2half2_rn(__uint_as_float(wv[e] << 16) * sc,
-                                             __uint_as_float(wv[e] & 0xffff0000u) * sc);
-        o[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        if (FMT == MOE_BF16) {
+          o[e] = wv[e];
+        } else {
+          const __half2 hh = __floats2half2_rn(__uint_as_float(wv[e] << 16) * sc,
+                                               __uint_as_float(wv[e] & 0xffff0000u) * sc);
+          o[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
       }
       xs[xslot(FMT, t, 2 * k8)] = make_uint2(o[0], o[1]);
       xs[xslot(FMT, t, 2 * k8 + 1)] = make_uint2(o[2], o[3]);
@@ -468,7 +547,7 @@ MOE_DEV void stage_block(const Geo& g, const GemvArgs& a, const SG& p, const Ent
       }
       const float bound = ma * mu;
       int s = 0;
-      if (bound > 0.f && bound < 3.0e38f) {
+      if (FMT != MOE_BF16 && bound > 0.f && bound < 3.0e38f) {   // bf16 h needs no scaling
         int ex;
         frexpf(bound, &ex);
         s = max(-100, min(100, ex - 15));
@@ -483,10 +562,17 @@ MOE_DEV void stage_block(const Geo& g, const GemvArgs& a, const SG& p, const Ent
       const float4* ar = reinterpret_cast<const float4*>(h + (size_t)(rowt + t) * 2 * p.K);
       const float4 av = __ldcg(ar + k4), uv = __ldcg(ar + k4 + p.K / 4);
       const float sc = pow2i(-sexp_b[t]);
-      const __half2 lo = __floats2half2_rn(silu_mul(av.x, uv.x) * sc, silu_mul(av.y, uv.y) * sc);
-      const __half2 hi = __floats2half2_rn(silu_mul(av.z, uv.z) * sc, silu_mul(av.w, uv.w) * sc);
-      xs[xslot(FMT, t, k4)] =
-          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      if (FMT == MOE_BF16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(silu_mul(av.x, uv.x), silu_mul(av.y, uv.y));
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(silu_mul(av.z, uv.z), silu_mul(av.w, uv.w));
+        xs[xslot(FMT, t, k4)] =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      } else {
+        const __half2 lo = __floats2half2_rn(silu_mul(av.x, uv.x) * sc, silu_mul(av.y, uv.y) * sc);
+        const __half2 hi = __floats2half2_rn(silu_mul(av.z, uv.z) * sc, silu_mul(av.w, uv.w) * sc);
+        xs[xslot(FMT, t, k4)] =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      }
     }
   }
 }
@@ -498,15 +584,16 @@ inline SG make_sg(const Geo& g, int ph, int N) {
   SG p{};
   p.K = ph == 1 ? g.d : g.f;
   p.R = ph == 1 ? g.f : g.d;
-  p.KB = (p.K + kBoxK - 1) / kBoxK;
+  p.bk = 1024 / fmt_code_bits(g.fmt);          // elements in 128 bytes
+  p.KB = (p.K + p.bk - 1) / p.bk;
   p.NS = (p.KB + kBoxes - 1) / kBoxes;
   p.RB = p.R / kBoxRows;
   p.UE = p.RB * (ph == 1 ? 2 : 1);
-  p.SBB = g.fmt == MOE_MXFP4 ? 8 : 16;
-  p.scale_row = p.K / g.blk;
+  p.SBB = g.blk ? p.bk / g.blk : 0;
+  p.scale_row = fmt_scale_row(g.fmt, p.K);
   // scale rows that are 16-byte multiples can be cut into TMA boxes; others
   // are bulk-copied whole (a stage then carries the unit's full scale rows)
-  p.smode = p.scale_row % 16 == 0 ? 1 : 0;
+  p.smode = p.SBB > 0 && p.scale_row % 16 == 0 ? 1 : 0;   // (no scales at all: 0, with 0 bytes)
   p.srow = p.smode ? kBoxes * p.SBB : p.scale_row;
   p.codes_bytes = kBoxes * kBoxBytes;
   p.stage_bytes = (p.codes_bytes + kBoxRows * p.srow + 1023) & ~1023;
@@ -595,9 +682,9 @@ MOE_DEV void produce(const Geo& g, const GemvArgs& a, const SG& p, const EntryTa
         if (lane == 0) tc::mbar_expect_tx(&S.full[slot], (uint32_t)(nbx * kBoxBytes) + sbytes);
         __syncwarp();
         if (lane < nbx)
-          tc::tma_load_3d(stg + (size_t)lane * kBoxBytes, map, &S.full[slot], (st * kBoxes + lane) * (kBoxK / 2),
+          tc::tma_load_3d(stg + (size_t)lane * kBoxBytes, map, &S.full[slot], (st * kBoxes + lane) * 128,
                           rb * kBoxRows, cu.en.slot);
-        else if (lane == kBoxes) {
+        else if (lane == kBoxes && p.SBB > 0) {
           // the scales of the stage's boxes: 64 rows x (4 boxes' bytes), or the unit's whole rows
           if (p.smode)
             tc::tma_load_3d(stg + p.codes_bytes, smap, &S.full[slot], st * kBoxes * p.SBB, rb * kBoxRows,
@@ -659,12 +746,14 @@ MOE_DEV void compute(const Geo& g, const GemvArgs& a, const SG& p, const EntryTa
                     S.base + (size_t)slot * p.stage_bytes, warp, lane);
         if (ok && kb < p.KB) {
           const uint8_t* stg = S.base + (size_t)slot * p.stage_bytes;
-          const uint8_t* cs = stg + (size_t)bslot * kBoxBytes + quarter * (16 * kBoxK / 2);
+          const uint8_t* cs = stg + (size_t)bslot * kBoxBytes + quarter * (16 * kBoxRowBytes);
           const uint8_t* sc = stg + p.codes_bytes + (16 * quarter + gq) * p.srow + (p.smode ? bslot : kb) * p.SBB;
-          const int nvb = min(8, (p.K - kb * kBoxK) / 32);
-          const uint2* xk = xs + (size_t)kb * 512;   // 8 blocks x 2 steps x 32 lanes
+          const int nvb = min(8, (p.K - kb * p.bk) / 32);
+          const uint2* xk = xs + (size_t)kb * 2 * p.bk;   // bk / 16 MMA steps x 32 lanes
           if (FMT == MOE_MXFP4) tile_mx(cs, sc, sc + 8 * p.srow, xk, nvb, lane, acc);
-          else tile_nv(cs, sc, sc + 8 * p.srow, xk, nvb, lane, acc);
+          else if (FMT == MOE_NVFP4) tile_nv(cs, sc, sc + 8 * p.srow, xk, nvb, lane, acc);
+          else if (FMT == MOE_MXFP8) tile_mx8(cs, sc, sc + 8 * p.srow, xk, lane, acc);
+          else tile_bf16(cs, xk, lane, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);

@@ -570,6 +570,7 @@ struct PrefillPlan {
 };
 
 bool prefill_shape_ok(const Geo& g) {
+  if (g.fmt != MOE_MXFP4 && g.fmt != MOE_NVFP4) return false;
   return g.d % 256 == 0 && g.f % 256 == 0 && g.d >= 256 && g.f >= 256;
 }
 

@@ -497,7 +497,9 @@ cudaError_t launch_step(const Geo& g, const GemvPlan* pl, const GemvArgs& a, Ste
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                const CUtensorMap, Geo, GemvArgs, StepArgs, SG, SG);
   if (g.fmt == MOE_MXFP4) kern = host ? step_kernel<MOE_MXFP4, true> : step_kernel<MOE_MXFP4, false>;
-  else kern = host ? step_kernel<MOE_NVFP4, true> : step_kernel<MOE_NVFP4, false>;
+  else if (g.fmt == MOE_NVFP4) kern = host ? step_kernel<MOE_NVFP4, true> : step_kernel<MOE_NVFP4, false>;
+  else if (g.fmt == MOE_MXFP8) kern = host ? step_kernel<MOE_MXFP8, true> : step_kernel<MOE_MXFP8, false>;
+  else kern = host ? step_kernel<MOE_BF16, true> : step_kernel<MOE_BF16, false>;
   cudaError_t e = ensure_smem_limit((const void*)kern, P.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -14,14 +14,16 @@ import numpy as np
 import torch
 
 from . import capi
-from .workloads import LayerSpec, Matrix, MXFP4
+from .workloads import BF16, LayerSpec, Matrix, MXFP4, MXFP8, NVFP4
+
+FMT_IDS = {MXFP4: capi.MOE_MXFP4, NVFP4: capi.MOE_NVFP4, MXFP8: capi.MOE_MXFP8, BF16: capi.MOE_BF16}
 
 
 def make_desc(spec: LayerSpec, max_tokens: int, act_scale_x: float = 1.0,
               act_scale_h: float = 1.0) -> capi.moe_layer_desc:
     return capi.moe_layer_desc(
         E=spec.E, k=spec.k, d_model=spec.d_model, d_ff=spec.d_ff, n_slots=spec.n_slots,
-        fmt=capi.MOE_MXFP4 if spec.fmt == MXFP4 else capi.MOE_NVFP4,
+        fmt=FMT_IDS[spec.fmt],
         has_shared=int(spec.has_shared), norm_topk=int(spec.norm_topk),
         has_bias=int(spec.has_bias), max_tokens=max_tokens,
         act_scale_x=act_scale_x, act_scale_h=act_scale_h)

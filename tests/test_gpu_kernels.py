@@ -24,7 +24,7 @@ def _gpu():
 
 # ---------------------------------------------------------------- formats
 
-@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4", "mxfp8", "bf16"])
 def test_dequant_slot_bit_exact(fmt):
     spec = small_spec(E=4, n_slots=3, d_model=384, d_ff=256, fmt=fmt, has_shared=True)
     L = build_layer(spec, 21, 8)
@@ -218,6 +218,8 @@ def test_lru_install_and_state_roundtrip():
     (small_spec(E=8, k=2, d_model=512, d_ff=256, n_slots=8, has_shared=True), 8),
     (small_spec(E=16, k=4, d_model=512, d_ff=384, n_slots=16, fmt="nvfp4", has_shared=True), 12),
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 4),
+    (small_spec(E=8, k=2, d_model=512, d_ff=384, n_slots=8, fmt="mxfp8", has_shared=True), 8),
+    (small_spec(E=8, k=2, d_model=384, d_ff=256, n_slots=8, fmt="bf16", has_shared=True), 6),
 ])
 def test_decode_gemv_decodes_weights_bit_exact(spec, N):
     # one-hot tokens x_t = c_t e_{i_t} (c_t a power of two): phase 1 of the

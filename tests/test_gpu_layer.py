@@ -40,6 +40,10 @@ def _tokens(spec, seed, N):
     (small_spec(E=4, k=2, d_model=6144, d_ff=256, n_slots=4, fmt="nvfp4", has_shared=True,
                 has_bias=True), 12),                                  # wide K, 2 token groups
     (small_spec(E=4, k=2, d_model=6144, d_ff=384, n_slots=4), 3),     # wide K, odd tile count
+    (small_spec(E=16, k=4, d_model=512, d_ff=384, n_slots=16, fmt="mxfp8", has_shared=True), 13),
+    (small_spec(E=16, k=4, d_model=384, d_ff=512, n_slots=16, fmt="bf16", has_bias=True), 9),
+    (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, fmt="mxfp8"), 4),   # the 35B-A3B shape
+    (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, fmt="bf16"), 16),
 ])
 def test_forward_all_resident(spec, N):
     seed = 11
@@ -179,6 +183,8 @@ def _last(L, spec, N):
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 1),     # the 35B-A3B layer
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128), 16),
     (small_spec(E=256, k=8, d_model=4096, d_ff=2048, n_slots=256, has_shared=True), 8),   # 284B-class
+    (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, fmt="mxfp8"), 4),
+    (small_spec(E=32, k=4, d_model=384, d_ff=512, n_slots=32, fmt="bf16", has_shared=True), 12),
 ])
 def test_fused_step_matches_chain_bitwise_all_resident(spec, N):
     # one fused launch computes the chained launches' values bit for bit
@@ -358,6 +364,22 @@ def test_decode_nvfp4_bias_small_cache(fill):
     spec = small_spec(E=24, k=3, d_model=512, d_ff=384, n_slots=5, fmt="nvfp4", has_shared=True,
                       has_bias=True)
     miss, u, waves = _decode_run(spec, 6, 3, 12, fill=fill)
+    assert miss > 0
+
+
+@pytest.mark.parametrize("fmt,fill,path", [
+    ("mxfp8", capi.MOE_FILL_MEMCPY, capi.MOE_DECODE_CHAIN),
+    ("mxfp8", capi.MOE_FILL_FUSED, capi.MOE_DECODE_STEP),
+    ("mxfp8", capi.MOE_FILL_KERNEL, capi.MOE_DECODE_CHAIN),
+    ("bf16", capi.MOE_FILL_FUSED, capi.MOE_DECODE_AUTO),
+    ("bf16", capi.MOE_FILL_DEVICE, capi.MOE_DECODE_CHAIN),
+])
+def test_decode_fp8_bf16_weights_with_misses(fmt, fill, path):
+    # FP8 (MXFP8) and BF16 weights through the cache: misses filled from host
+    # memory in each mode, waves, the shared expert, both decode paths
+    spec = small_spec(E=24, k=3, d_model=512, d_ff=384, n_slots=5 if path != capi.MOE_DECODE_STEP else 12,
+                      fmt=fmt, has_shared=True, has_bias=fmt == "bf16")
+    miss, u, waves = _decode_run(spec, 7, 4 if path == capi.MOE_DECODE_STEP else 3, 10, fill=fill, path=path)
     assert miss > 0
 
 
