@@ -66,6 +66,30 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
       vals[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
   }
+  const int nr = k + (with_shared ? 1 : 0);
+  if (fmt == MOE_MXFP8 || fmt == MOE_BF16) {
+    // W8A8: the group as 32 E4M3 bytes + an E8M0 byte; W16A16: x as it is
+    uint4 cw[4];
+    uint32_t s8 = 0;
+    if (fmt == MOE_MXFP8) {
+      uint32_t w8[8];
+      s8 = quant_mx8_32(vals, w8);
+      cw[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+      cw[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cw[q] = src[q];
+    }
+    const int nv = fmt == MOE_MXFP8 ? 2 : 4;            // 16-byte pieces of the group
+    const size_t rowb = (size_t)d * (fmt == MOE_MXFP8 ? 1 : 2);
+    for (int j = 0; j < nr; ++j) {
+      const size_t r = j < k ? (size_t)row_of[(size_t)t * k + j] : (size_t)N * k + t;
+      uint4* dst = reinterpret_cast<uint4*>(codes + r * rowb + (size_t)c * 16 * nv);
+      for (int q = 0; q < nv; ++q) dst[q] = cw[q];
+      if (fmt == MOE_MXFP8) scales[r * (d / 32) + c] = (uint8_t)s8;
+    }
+    return;
+  }
   uint32_t words[4];
   uint32_t s0, s1 = 0;
   if (fmt == MOE_MXFP4) {
@@ -78,7 +102,6 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
     words[3] = w2[1];
   }
   const uint4 cw = make_uint4(words[0], words[1], words[2], words[3]);
-  const int nr = k + (with_shared ? 1 : 0);
   for (int j = 0; j < nr; ++j) {
     const size_t r = j < k ? (size_t)row_of[(size_t)t * k + j] : (size_t)N * k + t;
     *reinterpret_cast<uint4*>(codes + r * (d / 2) + (size_t)c * 16) = cw;
@@ -234,9 +257,12 @@ template <int FMT, int PH>
 __global__ void __launch_bounds__(kWsThreads, 1)
 gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
                const __grid_constant__ CUtensorMap tb1, GemmArgs p) {
-  constexpr int G = FMT == MOE_MXFP4 ? 2 : 4;    // 4-byte scale groups per row per 256-K stage
+  // K elements per 128-byte stage row and 4-byte scale groups per row per stage:
+  // MXFP4 256 / 2, NVFP4 256 / 4, MXFP8 128 / 1, bf16 64 / 0 (no scales)
+  constexpr int KST = 1024 / fmt_code_bits(FMT);
+  constexpr int G = FMT == MOE_MXFP4 ? 2 : FMT == MOE_NVFP4 ? 4 : FMT == MOE_MXFP8 ? 1 : 0;
   constexpr int SB = 4 * G;                       // scale bytes per row per stage
-  constexpr int SFC = 2 * 4 * G;                  // TMEM columns of one scale slot (A, then B)
+  constexpr int SFC = 2 * 4 * (G > 0 ? G : 1);    // TMEM columns of one scale slot (A, then B)
   constexpr int NCOL = PH == 1 ? 64 : 128;        // output columns of one tile
   constexpr int kWsStages = ws_stages<PH>();
   extern __shared__ uint8_t smem_raw[];
@@ -267,8 +293,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int n_m = *p.n_tiles;
   const int NT = p.rows_out / NCOL;
   const long long T = (long long)n_m * NT;
-  const int nkt = p.K / 256;
-  const int srow = p.K / (FMT == MOE_MXFP4 ? 32 : 16);   // scale bytes per row
+  const int nkt = p.K / KST;
+  const int srow = fmt_scale_row(FMT, p.K);   // scale bytes per row
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -311,7 +337,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         for (int kt = 0; kt < nkt; ++kt, ++it) {
           const int s = it % kWsStages;
           const uint32_t ph = (it / kWsStages) & 1;
-          if (!ws_wait(&full[s], ph, &s_abort, p.err) || !ws_wait(&sfull[s], ph, &s_abort, p.err)) {
+          if (!ws_wait(&full[s], ph, &s_abort, p.err) || (G > 0 && !ws_wait(&sfull[s], ph, &s_abort, p.err))) {
             stop = true;
             break;
           }
@@ -325,8 +351,13 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             if (FMT == MOE_MXFP4) {
               const uint32_t id = 2 * (kk & 1), g = kk >> 1;
               tc::mma_mxf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, true, id, id), sfa + 4 * g, sfb + 4 * g, acc);
-            } else {
+            } else if (FMT == MOE_NVFP4) {
               tc::mma_nvf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, false, 0, 0), sfa + 4 * kk, sfb + 4 * kk, acc);
+            } else if (FMT == MOE_MXFP8) {
+              // one E8M0 scale per 32-K MMA: byte kk of the stage's group
+              tc::mma_mxf8(tb + 128 * b, ad, bd, tc::idesc_mxf8(128, kk, kk), sfa, sfb, acc);
+            } else {
+              tc::mma_bf16(tb + 128 * b, ad, bd, tc::idesc_bf16(128), acc);
             }
           }
           tc::mma_commit(&empty[s]);   // the stage's smem and scale slot are free once these MMAs finish
@@ -341,6 +372,9 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ block scales -> TMEM
+    if (G == 0) {
+      // bf16 operands carry no scales
+    } else {
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's lane quarter
     uint32_t it = 0;
     for (long long t = blockIdx.x; t < T; t += gridDim.x) {
@@ -361,10 +395,13 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         if (s_abort) continue;
         // the stage's scale loads go out before the wait for its TMEM slot,
         // so their latency overlaps the MMAs still reading the slot
-        uint32_t wa[4][G], wv[4][G];
+        uint32_t wa[4][G > 0 ? G : 1], wv[4][G > 0 ? G : 1];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (FMT == MOE_MXFP4) {
+          if (FMT == MOE_MXFP8) {
+            wa[j][0] = *reinterpret_cast<const uint32_t*>(pa[j] + kt * SB);
+            wv[j][0] = *reinterpret_cast<const uint32_t*>(pb[j] + kt * SB);
+          } else if (FMT == MOE_MXFP4) {
             const uint2 va = *reinterpret_cast<const uint2*>(pa[j] + kt * SB);
             const uint2 vb = *reinterpret_cast<const uint2*>(pb[j] + kt * SB);
             wa[j][0] = va.x; wa[j][G - 1] = va.y;
@@ -397,6 +434,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         if (lane == 0) ws_arrive(&sfull[s]);
       }
     }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
@@ -423,8 +461,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       if (lane == 0) ws_arrive(&acce[b]);   // the accumulator is free for the tile after next
       if (PH == 1) {
         // columns 0..63: W_g rows n0.., 64..127: W_u rows n0..
-        const float sg = FMT == MOE_MXFP4 ? 1.0f : ts[0] * p.act_scale;
-        const float su = FMT == MOE_MXFP4 ? 1.0f : ts[1] * p.act_scale;
+        const float sg = FMT == MOE_NVFP4 ? ts[0] * p.act_scale : 1.0f;
+        const float su = FMT == MOE_NVFP4 ? ts[1] * p.act_scale : 1.0f;
         const int f = p.rows_out;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -436,7 +474,26 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             const float a = __uint_as_float(gv[i2]) * sg, u = __uint_as_float(uv[i2]) * su;
             hv[i2] = a / (1.0f + __expf(-a)) * u;
           }
-          if (live) {
+          if (live && (FMT == MOE_MXFP8 || FMT == MOE_BF16)) {
+            const int col = n0 + 32 * c;
+            if (FMT == MOE_MXFP8) {
+              uint32_t w8[8];
+              p.h_scales[(size_t)r * (f / 32) + col / 32] = (uint8_t)quant_mx8_32(hv, w8);
+              uint4* dst = reinterpret_cast<uint4*>(p.h_codes + (size_t)r * f + col);
+              dst[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+              dst[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+            } else {
+              uint32_t wb[16];
+#pragma unroll
+              for (int i2 = 0; i2 < 16; ++i2) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[2 * i2], hv[2 * i2 + 1]);
+                wb[i2] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(p.h_codes + ((size_t)r * f + col) * 2);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) dst[q] = make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2], wb[4 * q + 3]);
+            }
+          } else if (live) {
             const int col = n0 + 32 * c;
             uint32_t words[4];
             if (FMT == MOE_MXFP4) {
@@ -459,7 +516,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         // value); the combine multiplies by 2^s and accumulates in fp32.
         // Rows go through shared memory, half a tile at a time, so that each
         // store instruction writes four whole 128-byte row pieces
-        const float sd = FMT == MOE_MXFP4 ? 1.0f : ts[2] * p.act_scale;
+        const float sd = FMT == MOE_NVFP4 ? ts[2] * p.act_scale : 1.0f;
         __half* Oh = reinterpret_cast<__half*>(p.O);
         float mx = 0.f;
 #pragma unroll
@@ -570,20 +627,20 @@ struct PrefillPlan {
 };
 
 bool prefill_shape_ok(const Geo& g) {
-  if (g.fmt != MOE_MXFP4 && g.fmt != MOE_NVFP4) return false;
   return g.d % 256 == 0 && g.f % 256 == 0 && g.d >= 256 && g.f >= 256;
 }
 
 PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8_t* xq_codes, size_t xq_rows,
                                  const uint8_t* hq_codes) {
   PrefillPlan* pl = new PrefillPlan();
-  pl->ready = make_map_2d(&pl->xq, xq_codes, g.d / 2, xq_rows) &&
-              make_map_2d(&pl->hq, hq_codes, g.f / 2, xq_rows) &&
-              make_map_3d(&pl->wg, slots + g.off_codes[0], g.d / 2, g.f, g.nbuf, g.ebytes) &&
-              make_map_3d(&pl->wu, slots + g.off_codes[1], g.d / 2, g.f, g.nbuf, g.ebytes) &&
-              make_map_3d(&pl->wd, slots + g.off_codes[2], g.f / 2, g.d, g.nbuf, g.ebytes) &&
-              make_map_3d(&pl->wg64, slots + g.off_codes[0], g.d / 2, g.f, g.nbuf, g.ebytes, 64) &&
-              make_map_3d(&pl->wu64, slots + g.off_codes[1], g.d / 2, g.f, g.nbuf, g.ebytes, 64);
+  const uint64_t db = (uint64_t)g.d * fmt_code_bits(g.fmt) / 8, fb = (uint64_t)g.f * fmt_code_bits(g.fmt) / 8;
+  pl->ready = make_map_2d(&pl->xq, xq_codes, db, xq_rows) &&
+              make_map_2d(&pl->hq, hq_codes, fb, xq_rows) &&
+              make_map_3d(&pl->wg, slots + g.off_codes[0], db, g.f, g.nbuf, g.ebytes) &&
+              make_map_3d(&pl->wu, slots + g.off_codes[1], db, g.f, g.nbuf, g.ebytes) &&
+              make_map_3d(&pl->wd, slots + g.off_codes[2], fb, g.d, g.nbuf, g.ebytes) &&
+              make_map_3d(&pl->wg64, slots + g.off_codes[0], db, g.f, g.nbuf, g.ebytes, 64) &&
+              make_map_3d(&pl->wu64, slots + g.off_codes[1], db, g.f, g.nbuf, g.ebytes, 64);
   return pl;
 }
 
@@ -620,8 +677,12 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
     const int s1 = (int)ws_smem<1>(), s2 = (int)ws_smem<2>();
     e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 1>, s1);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 1>, s1);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 1>, s1);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_BF16, 1>, s1);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 2>, s2);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 2>, s2);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 2>, s2);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_BF16, 2>, s2);
     if (e != cudaSuccess) return e;
   }
   GemmArgs p{};
@@ -638,7 +699,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.w_scales_off[2] = g.off_tscale;
   p.K = g.d;
   p.rows_out = g.f;
-  p.act_scale = g.fmt == MOE_MXFP4 ? 1.0f : gx;
+  p.act_scale = g.fmt == MOE_NVFP4 ? gx : 1.0f;
   p.h_codes = hq_codes;
   p.h_scales = hq_scales;
   p.act_scale_h = gh;
@@ -646,8 +707,12 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   if (ev) cudaEventRecord(ev[0], st);
   if (g.fmt == MOE_MXFP4)
     gemm_ws_kernel<MOE_MXFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
-  else
+  else if (g.fmt == MOE_NVFP4)
     gemm_ws_kernel<MOE_NVFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+  else if (g.fmt == MOE_MXFP8)
+    gemm_ws_kernel<MOE_MXFP8, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+  else
+    gemm_ws_kernel<MOE_BF16, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[1], st);
   if (e != cudaSuccess) return e;
@@ -657,7 +722,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.w_scales_off[2] = g.off_tscale;
   p.K = g.f;
   p.rows_out = g.d;
-  p.act_scale = g.fmt == MOE_MXFP4 ? 1.0f : gh;
+  p.act_scale = g.fmt == MOE_NVFP4 ? gh : 1.0f;
   p.O = O;
   p.O_ld = g.d;
   p.O_exp = prefill_o_exp(g, O, N);
@@ -665,8 +730,12 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   if (ev) cudaEventRecord(ev[2], st);
   if (g.fmt == MOE_MXFP4)
     gemm_ws_kernel<MOE_MXFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
-  else
+  else if (g.fmt == MOE_NVFP4)
     gemm_ws_kernel<MOE_NVFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+  else if (g.fmt == MOE_MXFP8)
+    gemm_ws_kernel<MOE_MXFP8, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+  else
+    gemm_ws_kernel<MOE_BF16, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[3], st);
   return e;

@@ -1,6 +1,8 @@
 // Blackwell (sm_100 family) primitives used by the prefill grouped GEMM:
 // mbarriers with bounded waits, TMA tensor loads, tcgen05 TMEM allocation,
-// block-scaled FP4 MMAs, TMEM loads/stores.  All inline PTX.
+// block-scaled FP4 and MXFP8 MMAs, bf16 MMAs, TMEM loads/stores.  All inline
+// PTX.  Every kind takes 128-byte operand rows per K tile (256 FP4, 128 FP8
+// or 64 bf16 elements) and 32 bytes of them per MMA (K = 64, 32, 16).
 //
 // Layouts these wrappers assume (checked on GB300 against a CPU product of
 // a 128x128x256 tile, both FP4 kinds):
@@ -143,6 +145,42 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a, uint64_t b
                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
                :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
                   "r"((uint32_t)accumulate));
+}
+
+// Instruction descriptor of a block-scaled MXFP8 MMA (E4M3 x E4M3, UE8M0
+// scales, M = 128, dense, K-major); sf_a / sf_b select the scale byte of the
+// 4-byte group (one scale per 32-K MMA).
+__device__ __forceinline__ uint32_t idesc_mxf8(int N, uint32_t sf_a, uint32_t sf_b) {
+  uint32_t d = 0;                                 // A and B E4M3 (type 0)
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= 1u << 23;                                  // UE8M0 scales
+  d |= (128u >> 4) << 24;
+  d |= (sf_b & 3u) << 4;
+  d |= (sf_a & 3u) << 29;
+  return d;
+}
+
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+               :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+                  "r"((uint32_t)accumulate));
+}
+
+// Instruction descriptor of a bf16 x bf16 -> fp32 MMA (M = 128, dense, K-major).
+__device__ __forceinline__ uint32_t idesc_bf16(int N) {
+  uint32_t d = 1u << 4;                           // D fp32
+  d |= (1u << 7) | (1u << 10);                    // A and B bf16
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= (128u >> 4) << 24;
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate));
 }
 
 // Arrive on `bar` when all previously issued MMAs of this thread complete.

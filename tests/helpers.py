@@ -119,29 +119,34 @@ def near_marks(v, marks, rel=1e-4):
 
 def prefill_h_flip_tokens(L, spec, O, X, idx):
     """After a prefill moe_forward of layer handle L on bf16-exact X [N, d]:
-    the tokens some of whose FP4 codes of h = SiLU(W_g x) (W_u x) (a routed
-    expert's row or the shared one) differ between the kernel (fp32 sums) and
-    the oracle (FP64).  Every such difference must lie where the oracle's
-    value is within 1e-4 (relative) of an E2M1 rounding midpoint or its
-    block's scale input within 1e-4 of a scale boundary: two correct
-    roundings of sums that differ in the last bits.  Returns a bool per token."""
+    the tokens some of whose FP4 / E4M3 codes of h = SiLU(W_g x) (W_u x) (a
+    routed expert's row or the shared one) differ between the kernel (fp32
+    sums) and the oracle (FP64).  Every such difference must lie where the
+    oracle's value is within 1e-4 (relative) of a rounding midpoint of the
+    element grid or its block's scale input within 1e-4 of a scale boundary:
+    two correct roundings of sums that differ in the last bits.  Returns a
+    bool per token; at most 1e-4 of the h codes may differ."""
     import torch
     from routed_expert_layer_gemv_gb300 import capi
     from oracle.native import formats, quant
     from oracle.native import layer as olayer
     N, k, blk, f = X.shape[0], spec.k, spec.block, spec.d_ff
     rows = N * k + (N if spec.has_shared else 0)
-    hc = torch.empty(rows, f // 2, dtype=torch.uint8, device="cuda")
+    mx8 = spec.fmt == "mxfp8"
+    hc = torch.empty(rows, f if mx8 else f // 2, dtype=torch.uint8, device="cuda")
     hs = torch.empty(rows, f // blk, dtype=torch.uint8, device="cuda")
     capi.moe_debug_last_hidden(L.h, hq_codes=hc, hq_scales=hs)
     row_of = torch.empty(N * k, dtype=torch.int32, device="cuda")
     capi.moe_debug_last_step(L.h, row_of=row_of)
     torch.cuda.synchronize()
-    HC = formats.unpack_codes(hc.cpu().numpy())
+    HC = hc.cpu().numpy() if mx8 else formats.unpack_codes(hc.cpu().numpy())
+    e4 = np.sort(np.unique(formats.E4M3_TABLE[:0x7F]))
+    e4_mid = ((e4[1:] + e4[:-1]) / 2)[1:]                  # E4M3 rounding midpoints (> 0)
     HS = hs.cpu().numpy()
     R = row_of.cpu().numpy().reshape(N, k)
     xq = olayer.act_roundtrip(X, spec.fmt, 1.0)
     flag = np.zeros(N, dtype=bool)
+    n_codes = n_diff = 0
     jobs = []
     for e in np.unique(idx):
         tt, jj = np.nonzero(idx == e)
@@ -151,8 +156,8 @@ def prefill_h_flip_tokens(L, spec, O, X, idx):
     for W, toks, rws in jobs:
         h = olayer.silu(xq[toks] @ W["gate"].T) * (xq[toks] @ W["up"].T)
         amax = np.abs(h.astype(np.float32).reshape(len(toks), -1, blk)).max(axis=-1).astype(np.float64)
-        if spec.fmt == "mxfp4":
-            rc, rsc = quant.quant_mxfp4(h)
+        if spec.fmt in ("mxfp4", "mxfp8"):
+            rc, rsc = quant.quant_mxfp4(h) if spec.fmt == "mxfp4" else quant.quant_mxfp8(h)
             with np.errstate(divide="ignore"):
                 lg = np.log2(np.where(amax > 0, amax, 1.0))
             edge = np.abs(amax - np.exp2(np.round(lg))) <= 1e-4 * amax
@@ -163,15 +168,27 @@ def prefill_h_flip_tokens(L, spec, O, X, idx):
             mids = (e4[1:] + e4[:-1]) / 2
             edge = near_marks(amax / 6.0, mids[mids > 0])
             unit = formats.E4M3_TABLE[rsc]
-        rcu = formats.unpack_codes(rc)
+        rcu = rc if mx8 else formats.unpack_codes(rc)
         gc, gs = HC[rws], HS[rws]
         bad_scale = gs != rsc
         assert not (bad_scale & ~edge).any(), "a block scale of h differs away from a scale boundary"
         with np.errstate(divide="ignore", invalid="ignore"):
             q = np.abs(h) / np.repeat(unit, blk, axis=1)
-        both_zero = ((rcu & 7) == 0) & ((gc & 7) == 0)
+        mag = 0x7F if mx8 else 7
+        both_zero = ((rcu & mag) == 0) & ((gc & mag) == 0)
         diff = (gc != rcu) & ~both_zero
-        unexplained = diff & ~np.repeat(bad_scale, blk, axis=1) & ~near_marks(q, _E2M1_MID)
-        assert not unexplained.any(), "%d FP4 codes of h differ away from a rounding midpoint" % unexplained.sum()
+        if mx8:
+            # E4M3's grid reaches 2^-9 of the block unit near zero, but the
+            # difference between fp32 and FP64 sums scales with the block's
+            # magnitudes (up to 512 units): the window is relative, with a
+            # floor of 5e-3 units (~1e-5 of the block maximum)
+            near = (np.abs(q[..., None] - e4_mid) <= np.maximum(1e-4 * e4_mid, 5e-3)).any(axis=-1)
+        else:
+            near = near_marks(q, _E2M1_MID)
+        unexplained = diff & ~np.repeat(bad_scale, blk, axis=1) & ~near
+        assert not unexplained.any(), "%d codes of h differ away from a rounding midpoint" % unexplained.sum()
         flag[toks[diff.any(axis=1) | bad_scale.any(axis=1)]] = True
+        n_codes += diff.size
+        n_diff += int(diff.sum())
+    assert n_diff <= 1e-4 * n_codes, "%d of %d codes of h differ" % (n_diff, n_codes)
     return flag

@@ -53,20 +53,35 @@ def _quant_inputs(rows, K, seed):
     return v.astype(np.float32)
 
 
-@pytest.mark.parametrize("fmt,g_x", [("mxfp4", 1.0), ("nvfp4", 1.0), ("nvfp4", 0.25)])
+@pytest.mark.parametrize("fmt,g_x", [("mxfp4", 1.0), ("nvfp4", 1.0), ("nvfp4", 0.25), ("mxfp8", 1.0), ("bf16", 1.0)])
 def test_activation_quantiser_bit_exact(fmt, g_x):
     spec = small_spec(fmt=fmt)
     from routed_expert_layer_gemv_gb300.layer import MoELayer
     L = MoELayer(spec, 8, act_scale_x=g_x, act_scale_h=g_x)
     rows, K = 64, 512
     v = _quant_inputs(rows, K, 4)
-    blk = 32 if fmt == "mxfp4" else 16
+    if fmt == "mxfp8":
+        # E4M3 ties (1.0625, 1.1875), a value between grid points (248) and one
+        # past the largest (464, saturating at 448); block exponent 0 for row 3
+        g = np.random.default_rng(1)
+        v[3, :] = g.choice([1.0625, 1.1875, 248.0, 464.0], K) * np.sign(g.standard_normal(K))
+        v[5, :32] = 500.0
+    blk = {"mxfp4": 32, "nvfp4": 16, "mxfp8": 32, "bf16": 32}[fmt]
+    cbytes = {"mxfp4": K // 2, "nvfp4": K // 2, "mxfp8": K, "bf16": 2 * K}[fmt]
     vt = torch.from_numpy(v).cuda()
-    codes = torch.empty(rows, K // 2, dtype=torch.uint8, device="cuda")
+    codes = torch.empty(rows, cbytes, dtype=torch.uint8, device="cuda")
     scales = torch.empty(rows, K // blk, dtype=torch.uint8, device="cuda")
     capi.moe_debug_actquant(L.h, vt, rows, K, codes, scales, 0)
+    if fmt == "bf16":
+        # bf16 activations: the rounding of each value, nearest even
+        got = codes.cpu().numpy().view("<u2").astype(np.uint32) << 16
+        assert np.array_equal(got.view(np.float32).astype(np.float64), quant.round_bf16(v.astype(np.float64)))
+        L.close()
+        return
     if fmt == "mxfp4":
         rc, rs = quant.quant_mxfp4(v)
+    elif fmt == "mxfp8":
+        rc, rs = quant.quant_mxfp8(v)
     else:
         rc, rs = quant.quant_nvfp4(v, g_x)
     assert np.array_equal(scales.cpu().numpy(), rs)

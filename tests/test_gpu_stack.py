@@ -53,7 +53,7 @@ def _check_layer(spec, seed, x_in, y_gpu, regime, what, L=None, first=True):
     y = _f64(y_gpu)
     if regime == "prefill":
         flip = prefill_h_flip_tokens(L, spec, ol, x_in, idx) & keep
-        assert flip.sum() <= 0.05 * len(flip), "%s: %d tokens with an h code flipped" % (what, flip.sum())
+        assert flip.sum() <= 0.1 * len(flip), "%s: %d tokens with an h code flipped" % (what, flip.sum())
         err = np.linalg.norm(y[keep] - y_ref[keep]) / np.linalg.norm(y_ref[keep])
         assert err <= 5e-3, "%s rel Frobenius %.3e" % (what, err)
         keep = keep & ~flip
