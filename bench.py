@@ -73,6 +73,16 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _dtype_peak(fmt):
+    """Dense tensor TF/s of the prefill MMAs of a weight format: the measured
+    bf16 GEMM burst x the nominal ratio (FP4 13.5 : 2.25, FP8 4.5 : 2.25)."""
+    d = _measured()
+    ratio = {"mxfp4": FP4_PER_BF16, "nvfp4": FP4_PER_BF16, "mxfp8": 2.0, "bf16": 1.0}[fmt]
+    if d and "bf16_tflops" in d:
+        return float(d["bf16_tflops"]) * ratio, "measured bf16 x %g" % ratio
+    return FALLBACK_BF16_TFLOPS * ratio, "fallback bf16 x %g" % ratio
+
+
 def _fp4_peak():
     """Dense FP4 TF/s: measured bf16 GEMM burst x the nominal FP4/bf16 ratio."""
     d = _measured()
@@ -141,13 +151,20 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
+def expert_bytes(spec):
+    """Weight bytes of one expert: B_e = 3 d f (code bits / 8 + 1 / B), B the
+    elements per block scale (no scale term for BF16)."""
+    from routed_expert_layer_gemv_gb300.workloads import CODE_BITS
+    per = CODE_BITS[spec.fmt] / 8 + (1 / spec.block if spec.block else 0)
+    return 3 * spec.d_model * spec.d_ff * per
+
+
 def step_bytes(spec, n_distinct, n_tokens):
     """Algorithmic HBM bytes of one decode step: each distinct routed expert's
-    weights once (B_e = 3 d f (1/2 + 1/B) + tensor scales), the shared
-    expert's, W_r in fp32 (4 E d) and x in / y out (2 N d each)."""
-    d, f, E = spec.d_model, spec.d_ff, spec.E
-    b_e = 3 * d * f * (1 / 2 + 1 / spec.block)
-    return (n_distinct + (1 if spec.has_shared else 0)) * b_e + 4 * E * d + 4 * n_tokens * d
+    weights once (B_e, expert_bytes), the shared expert's, W_r in fp32
+    (4 E d) and x in / y out (2 N d each)."""
+    d, E = spec.d_model, spec.E
+    return (n_distinct + (1 if spec.has_shared else 0)) * expert_bytes(spec) + 4 * E * d + 4 * n_tokens * d
 
 
 def traffic_ratio(kernel, workload):
@@ -231,8 +248,7 @@ def run_decode(c, work, batch, profile=False, fill=None, resident=None):
     distinct, misses = s1[1] - s0[1], s1[3] - s0[3]
     return dict(batch=batch, steps=K, ms=sum(step_ms), p50=statistics.median(step_ms), tokens=K * batch,
                 launches=launches, fused_steps=fused, distinct=distinct, misses=misses, prof=prof,
-                bytes=K * step_bytes(spec, 0, batch) + distinct * 3 * spec.d_model * spec.d_ff *
-                (1 / 2 + 1 / spec.block))
+                bytes=K * step_bytes(spec, 0, batch) + distinct * expert_bytes(spec))
 
 
 def trace_miss_rate(c, work, batch):
@@ -439,6 +455,36 @@ def run_stack(c, n_layers, batches, link_gbs):
     return out
 
 
+def run_formats(c, batches, peak):
+    """The 35B-A3B layer shape with FP8 (MXFP8) and BF16 expert weights, every
+    expert resident: decode steps at each batch size (A16; tokens/s and the
+    step's HBM bytes over its time) and one prefill chunk of 8192 tokens (W8A8,
+    W16A16; GEMM TFLOP/s against the dtype's dense tensor peak)."""
+    wl = c.wl
+    out = {}
+    for fmt in (wl.MXFP8, wl.BF16):
+        work = dataclasses.replace(wl.DECODE_35B, name="%s_%s" % (wl.DECODE_35B.name, fmt),
+                                   layer=dataclasses.replace(wl.DECODE_35B.layer, fmt=fmt))
+        resident = c.layer(work, max(batches), n_slots=work.layer.E, install_all=True)
+        dec = {}
+        for b in batches:
+            r = run_decode(c, work, b, resident=resident)
+            dec[str(b)] = {"tokens_per_s": r["tokens"] / (r["ms"] / 1000.0), "ms_per_step": r["ms"] / r["steps"],
+                           "frac_of_measured_hbm": r["bytes"] / (r["ms"] / 1000.0) / 1e9 / peak,
+                           "fused_steps": r["fused_steps"]}
+        resident[0].close()
+        pwork = dataclasses.replace(wl.PREFILL_35B, name="%s_%s" % (wl.PREFILL_35B.name, fmt),
+                                    layer=dataclasses.replace(wl.PREFILL_35B.layer, fmt=fmt))
+        c.pools[pwork.name] = c.pools[work.name]    # the same weights (same seed and shape)
+        dpeak, dkind = _dtype_peak(fmt)
+        pre = prefill_summary(run_prefill(c, pwork), dpeak)
+        pre["peak_TFLOP_s"] = dpeak
+        pre["peak_kind"] = dkind
+        out[fmt] = {"expert_bytes": expert_bytes(work.layer), "decode_all_resident": dec, "prefill_n8192": pre}
+        c.pools.clear()
+    return out
+
+
 def decode_workload(c, work, batches, peak, with_modes=True, timed=None):
     """Everything reported for one decode workload: the timed default pass
     (`timed`, when already run), kernel times, fill modes, e2e, miss rates and
@@ -539,6 +585,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=8)
     ap.add_argument("--stack-layers", type=int, default=8,
                     help="layers of the multi-layer stack measured as an extra key (0: none)")
+    ap.add_argument("--formats-only", action="store_true",
+                    help="measure only the FP8 / BF16 weight formats and print their object")
     ap.add_argument("--stack-only", action="store_true",
                     help="measure only the multi-layer stack (decode and prefill) and print its object")
     ap.add_argument("--no-extra", action="store_true",
@@ -606,6 +654,9 @@ def main():
     work = wl.DECODE_35B
     if args.stack_only:
         print(json.dumps({"stack": run_stack(c, max(1, args.stack_layers), batches, h2d_rate(c))}))
+        return
+    if args.formats_only:
+        print(json.dumps({"formats": run_formats(c, batches, peak)}))
         return
     if args.resident_only:
         resident = c.layer(work, max(batches), n_slots=work.layer.E, install_all=True)
@@ -677,6 +728,7 @@ def main():
             c.pools.clear()
         if args.stack_layers > 0:
             extra["stack_35b_a3b_l%d" % args.stack_layers] = run_stack(c, args.stack_layers, batches, link)
+        extra["formats_35b_a3b"] = run_formats(c, batches, peak)
 
     cpu = None
     if not args.no_cpu_baseline:
