@@ -751,10 +751,11 @@ def main():
                    "steps_per_batch": args.steps,
                    "miss_rate_per_batch": {b: dec["per_batch"][b]["miss_rate"] for b in dec["per_batch"]},
                    "l2": "flushed (512 MiB write) between timed steps",
-                   "path": "library defaults: %d of %d timed steps ran as one fused launch (steps of at most "
-                           "32 (token, expert) pairs: batch 1 and 4, misses read over the host link by the step "
-                           "itself); batch 16 (distinct experts > slots) fills with a copy kernel on 12 reserved "
-                           "SMs and runs the chain of launches" % (fused, args.steps * len(batches)),
+                   "path": "library defaults: a step with misses possible runs the chain of launches -- at "
+                           "batch 1 and 4 the expert FFN reads misses over the host link and writes them to their "
+                           "slots, at batch 16 (distinct experts > slots) a copy kernel on 12 reserved SMs fills "
+                           "them; %d of %d timed steps ran as one fused launch (only a layer holding every expert "
+                           "fuses its small steps)" % (fused, args.steps * len(batches)),
                    "h2d_GB_per_s_measured": link,
                    "timing": "value from a pass without per-kernel events; kernel times and roofline from "
                              "instrumented passes of the same steps",

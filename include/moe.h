@@ -269,8 +269,8 @@ int moe_set_fill_mode(moe_layer_t layer, int mode);
 /* How a decode step runs.  MOE_DECODE_AUTO (default): as one fused,
  * cooperative launch -- routing, LRU step, expert FFN over hits and misses,
  * shared expert and combine, one CTA per SM meeting at grid barriers --
- * for small steps (N * k <= 32) that allow it, else as the chain of
- * launches.  The fused launch takes steps of at most 16 tokens with
+ * for small steps (N * k <= 32) of a layer that holds every expert or of a
+ * stack's layer, else as the chain of launches.  The fused launch takes steps of at most 16 tokens with
  * N * k <= 256, E <= 640,
  * d_model a multiple of 128, whose misses (if any) are filled by the expert
  * FFN itself (every expert resident, or MOE_FILL_FUSED, or MOE_FILL_AUTO

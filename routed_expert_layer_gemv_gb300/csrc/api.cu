@@ -1059,12 +1059,18 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     const bool fused_fill = !resident && fm == MOE_FILL_FUSED && L->pool_dev;
     StepPlan plan{};
     // AUTO takes the fused launch for steps of at most kStepAutoPairs (token,
-    // expert) pairs: there it is the faster path (measured on GB300: batch 1
-    // and 4 of the 35B-A3B-shaped layer, batch 1 of the 284B-A13B-shaped one);
-    // for larger steps the chained launches' GEMV keeps pace and the chain
-    // is used
+    // expert) pairs (measured on GB300): with every expert resident it is the
+    // faster path (batch 1 and 4 of the 35B-A3B-shaped layer, batch 1 of the
+    // 284B-A13B-shaped one; larger steps keep pace on the chain); with misses,
+    // a lone layer is faster on the chain with fused fills (58.5 vs 64.3 us at
+    // batch 1, 121 vs 131 us at batch 4, 35B-A3B layer, 47 slots, miss rate
+    // 0.16-0.2), a stack's layers -- with twice the miss rate on the shared
+    // pool -- in the fused launch (76 vs 111 us per layer step at batch 1, 150
+    // vs 177 at batch 4: the chain's two expert-FFN launches each pay the host
+    // link's latency for the misses)
     const bool want = !prefill && L->decode_path != MOE_DECODE_CHAIN && !L->step_failed && L->num_sms >= 2 &&
-                      (L->decode_path == MOE_DECODE_STEP || N * g.k <= kStepAutoPairs);
+                      (L->decode_path == MOE_DECODE_STEP ||
+                       (N * g.k <= kStepAutoPairs && (resident || L->stack != nullptr)));
     const bool can = want && (resident || fused_fill) && step_plan(g, N, &plan);
     if (L->decode_path == MOE_DECODE_STEP && !can)
       return fail(L, MOE_ERR_UNSUPPORTED, "this step cannot run as one fused launch (N = %d, fill mode %d)", N, fm);

@@ -136,16 +136,21 @@ MOE_DEV void lru_body(const int* counts, const int* offs, const uint32_t* cm, in
   const int U = n_hit + n_miss;
 
   // victim queue Q (its barriers published m.stale): free slots, then stale
-  // slots by ascending stamp; hits keep their slots
+  // slots by ascending stamp; hits keep their slots.  The step reads only
+  // Q[0 .. min(U, S) - n_hit): a stale slot needs its exact rank only while
+  // that rank is below the n_need stale victims, so it stops counting there
+  // (a pool of hundreds of slots and a handful of misses scans a few entries
+  // per slot, not all of them)
   if (fre) { m.q[fr] = s; m.q_old[fr] = -1; }
-  if (stale) {
+  const int n_need = max(0, min(U, S) - n_hit - n_free);
+  if (stale && n_need > 0) {
     int r = 0;
-    for (int s2 = 0; s2 < S; ++s2) {
+    for (int s2 = 0; s2 < S && r < n_need; ++s2) {
       if (!m.stale[s2]) continue;
       const unsigned long long t2 = m.st[s2];
       r += (t2 < st || (t2 == st && s2 < s)) ? 1 : 0;
     }
-    if (n_free + r < S) {
+    if (r < n_need) {
       m.q[n_free + r] = s;
       m.q_old[n_free + r] = old;
     }
