@@ -482,6 +482,30 @@ def run_formats(c, batches, peak):
         pre["peak_kind"] = dkind
         out[fmt] = {"expert_bytes": expert_bytes(work.layer), "decode_all_resident": dec, "prefill_n8192": pre}
         c.pools.clear()
+    # W4A16 on a prefill chunk: the MXFP4 layer's 8192-token chunk through the
+    # decode regime (FP4 weights x bf16-class activations, mma.sync GEMV),
+    # next to its W4A4 tcgen05 prefill
+    torch, capi = c.torch, c.capi
+    pw = wl.PREFILL_35B
+    N = pw.n_tokens
+    xp, _ = wl.iid_tokens(pw.seed, N, pw.layer.d_model)
+    x = torch.from_numpy(xp.view(np.int16)).view(torch.bfloat16).cuda()
+    L, spec = c.layer(pw, N, n_slots=pw.layer.E, install_all=True)
+    y = torch.empty(N, spec.d_model, dtype=torch.bfloat16, device="cuda")
+    L.forward(x, y, regime=capi.MOE_REGIME_DECODE)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 2
+    a.record()
+    for _ in range(reps):
+        L.forward(x, y, regime=capi.MOE_REGIME_DECODE)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    L.close()
+    c.pools.clear()
+    out["w4a16_prefill_n8192"] = {"workload": pw.name, "regime": "decode (A16) on the prefill chunk",
+                                  "tokens_per_s": N / (ms / 1000.0), "ms_per_chunk": ms}
     return out
 
 

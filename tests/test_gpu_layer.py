@@ -45,6 +45,9 @@ def _tokens(spec, seed, N):
     (small_spec(E=16, k=4, d_model=384, d_ff=512, n_slots=16, fmt="bf16", has_bias=True), 9),
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, fmt="mxfp8"), 4),   # the 35B-A3B shape
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, fmt="bf16"), 16),
+    # a prefill-sized chunk through the decode regime: FP4 weights x bf16-class
+    # activations (W4A16), the tensor-core router, three permutation launches
+    (small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True), 300),
 ])
 def test_forward_all_resident(spec, N):
     seed = 11
