@@ -20,7 +20,9 @@ permute  counts[e], offsets = exclusive prefix sum over ascending e, and the
          rows of one expert in ascending token order (unique).
 expert   out_e(x) = W_d (SiLU(W_g x) * (W_u x)), SiLU(z) = z / (1 + e^-z).
          Decode regime: x used as bf16-exact values.  Prefill regime: x and h
-         pass through the FP4 activation quantiser of ``quant`` first.
+         pass through the block quantiser of the activation format first
+         (``quant``): the weights' own format, or MXFP8 on MXFP4 weights
+         (W4A8, the spec's ``prefill_act``).
 combine  y[t] = sum_j g[t, j] out_{e_j}(x_t) + shared(x_t)  (shared expert
          always on, weight 1).
 """
@@ -129,7 +131,8 @@ def act_roundtrip(v: np.ndarray, fmt: str, g: float) -> np.ndarray:
 
 def expert_ffn(X: np.ndarray, W: Dict[str, np.ndarray], regime: str = "decode",
                fmt: str = "mxfp4", g_x: float = 1.0, g_h: float = 1.0) -> np.ndarray:
-    """SwiGLU expert on rows X [n, d] with dequantised weights W (FP64)."""
+    """SwiGLU expert on rows X [n, d] with dequantised weights W (FP64); in
+    the prefill regime x and h are quantised to the activation format `fmt`."""
     X = np.asarray(X, np.float64)
     if regime == "prefill":
         X = act_roundtrip(X, fmt, g_x)
@@ -156,6 +159,12 @@ def combine(O: np.ndarray, gates: np.ndarray, row_of: np.ndarray,
 
 
 # ------------------------------------------------------------------ layer
+
+def _act_fmt(spec) -> str:
+    """Activation format of the prefill regime: the weights' own format, or
+    the spec's prefill_act (MXFP8 on MXFP4 weights: W4A8)."""
+    return getattr(spec, "prefill_act", None) or spec.fmt
+
 
 class Layer:
     """The layer's parameters as the oracle sees them: per-matrix FP4 arrays
@@ -191,10 +200,10 @@ class Layer:
                 continue
             rows = np.arange(offsets[e], offsets[e + 1])
             O[rows] = expert_ffn(x[tok_of[rows]], self.expert(e), regime,
-                                 spec.fmt, self.g_x, self.g_h)
+                                 _act_fmt(spec), self.g_x, self.g_h)
         shared = None
         if spec.has_shared:
             Ws = dequant_expert(self.shared_w, spec.fmt)
-            shared = expert_ffn(x, Ws, regime, spec.fmt, self.g_x, self.g_h)
+            shared = expert_ffn(x, Ws, regime, _act_fmt(spec), self.g_x, self.g_h)
         y = combine(O, gates, row_of, shared)
         return y, idx, gates

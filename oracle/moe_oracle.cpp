@@ -359,7 +359,8 @@ void orc_permute(const int* idx, int N, int k, int E, long long* counts, long lo
 // ---------------------------------------------------------------- expert
 // out[r] = W_d (SiLU(W_g X[r]) * (W_u X[r])) for n rows X [n, d] (FP64
 // dequantised weights Wg, Wu [f, d], Wd [d, f]).  regime 1 (prefill): X and
-// h pass through the FP4 activation quantiser first (scales gx, gh).
+// h pass through the block quantiser of the activation format `fmt` first
+// (the weights' own format, or MXFP8 on MXFP4 weights; NVFP4 scales gx, gh).
 void orc_expert_ffn(const double* X, int n, int d, int f, const double* Wg, const double* Wu, const double* Wd,
                     int regime, int fmt, float gx, float gh, double* out) {
   std::vector<double> Xq;

@@ -111,6 +111,12 @@ def combine(O: np.ndarray, gates: np.ndarray, row_of: np.ndarray, shared: Option
     return y
 
 
+def _act_fmt(spec) -> str:
+    """Activation format of the prefill regime: the weights' own format, or
+    the spec's prefill_act (MXFP8 on MXFP4 weights: W4A8)."""
+    return getattr(spec, "prefill_act", None) or spec.fmt
+
+
 class Layer:
     """The layer's parameters as the oracle sees them: per-matrix FP4 arrays
     from the generator, dequantised on demand, one expert at a time."""
@@ -139,8 +145,8 @@ class Layer:
             if counts[e] == 0:
                 continue
             rows = np.arange(offsets[e], offsets[e + 1])
-            O[rows] = expert_ffn(x[tok_of[rows]], self.expert(e), regime, spec.fmt, self.g_x, self.g_h)
+            O[rows] = expert_ffn(x[tok_of[rows]], self.expert(e), regime, _act_fmt(spec), self.g_x, self.g_h)
         shared = None
         if spec.has_shared:
-            shared = expert_ffn(x, dequant_expert(self.shared_w, spec.fmt), regime, spec.fmt, self.g_x, self.g_h)
+            shared = expert_ffn(x, dequant_expert(self.shared_w, spec.fmt), regime, _act_fmt(spec), self.g_x, self.g_h)
         return combine(O, gates, row_of, shared), idx, gates

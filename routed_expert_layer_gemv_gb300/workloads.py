@@ -61,11 +61,18 @@ class LayerSpec:
     norm_topk: bool = True
     router_std: Optional[float] = None   # default 1/sqrt(d_model)
     bias_var: float = 0.5
+    prefill_act: Optional[str] = None    # prefill activations: None = the weights' format;
+                                         # MXFP8 on MXFP4 weights = W4A8
 
     @property
     def block(self) -> int:
         """K elements per block scale (0: the format has none)."""
         return SCALE_BLOCK[self.fmt]
+
+    @property
+    def act_fmt(self) -> str:
+        """Format the prefill regime quantises x and h to."""
+        return self.prefill_act or self.fmt
 
 
 @dataclasses.dataclass(frozen=True)

@@ -1,5 +1,6 @@
 """Pins of the oracle's router, permutation, SwiGLU experts and combine
 against brute force, textbook loops, library routines and invariants (no GPU)."""
+import dataclasses
 import math
 
 import numpy as np
@@ -221,15 +222,49 @@ def test_prefill_regime_is_decode_on_quantised_activations(fmt):
     assert np.abs(xq - x).max() <= np.abs(x).max() / 3
 
 
+def test_w4a8_prefill_is_dense_swiglu_on_mxfp8_activations():
+    # MXFP4 weights with MXFP8 activations: x and h rounded by the MXFP8
+    # quantiser (pinned on its own in test_oracle_quant), the FFN written out
+    # with loops; the result is not the W4A4 one
+    from oracle import quant
+    spec = wl.LayerSpec(E=1, k=1, d_model=64, d_ff=64, n_slots=1, prefill_act=wl.MXFP8)
+    w = wl.expert_weights(spec, 17, 0)
+    W_r, _ = wl.router_weights(spec, 17)
+    L = layer.Layer(spec, lambda e: w, W_r, None)
+    x = wl.bf16_bits_to_f64(wl.iid_tokens(17, 4, spec.d_model)[0])
+    y, _, _ = L.forward(x, "prefill")
+    Wd = {n: formats.dequant(m.codes, m.scales, m.tscale, "mxfp4") for n, m in w.items()}
+
+    def rt8(v):
+        c, s = quant.quant_mxfp8(np.asarray(v, np.float64)[None, :])
+        return formats.dequant(c, s, 1.0, "mxfp8")[0]
+
+    for t in range(4):
+        xq = rt8(x[t])
+        f = spec.d_ff
+        h = np.zeros(f)
+        for r in range(f):
+            a = sum(Wd["gate"][r, i] * xq[i] for i in range(spec.d_model))
+            u = sum(Wd["up"][r, i] * xq[i] for i in range(spec.d_model))
+            h[r] = a / (1.0 + math.exp(-a)) * u
+        hq = rt8(h)
+        ref = np.array([sum(Wd["down"][r, j] * hq[j] for j in range(f)) for r in range(spec.d_model)])
+        assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    L4 = layer.Layer(dataclasses.replace(spec, prefill_act=None), lambda e: w, W_r, None)
+    y4, _, _ = L4.forward(x, "prefill")
+    assert not np.allclose(y, y4, rtol=1e-3)
+
+
 def test_native_and_numpy_oracles_agree():
     # the two implementations of the oracle, on layers with every option:
     # ids, permutation and quantiser codes exactly, values to FP64 rounding
     from oracle import layer as np_layer
     from oracle.native import layer as cpp_layer
-    for fmt, shared, bias in (("mxfp4", False, False), ("nvfp4", True, True), ("mxfp8", True, False),
-                              ("bf16", False, True)):
+    for fmt, shared, bias, act in (("mxfp4", False, False, None), ("nvfp4", True, True, None),
+                                   ("mxfp8", True, False, None), ("bf16", False, True, None),
+                                   ("mxfp4", True, False, "mxfp8")):
         spec = wl.LayerSpec(E=12, k=3, d_model=128, d_ff=64, n_slots=12, fmt=fmt, has_shared=shared,
-                            has_bias=bias)
+                            has_bias=bias, prefill_act=act)
         W_r, b = wl.router_weights(spec, 8)
         ex = {e: wl.expert_weights(spec, 8, e) for e in range(spec.E)}
         sh = wl.expert_weights(spec, 8, 0, shared=True) if shared else None
