@@ -459,7 +459,9 @@ def run_formats(c, batches, peak):
     """The 35B-A3B layer shape with FP8 (MXFP8) and BF16 expert weights, every
     expert resident: decode steps at each batch size (A16; tokens/s and the
     step's HBM bytes over its time) and one prefill chunk of 8192 tokens (W8A8,
-    W16A16; GEMM TFLOP/s against the dtype's dense tensor peak)."""
+    W16A16; GEMM TFLOP/s against the dtype's dense tensor peak); then the
+    MXFP4 layer's chunk as W4A8 (GEMM against the FP8 peak) and as W4A16
+    (through the decode regime)."""
     wl = c.wl
     out = {}
     for fmt in (wl.MXFP8, wl.BF16):
@@ -482,6 +484,16 @@ def run_formats(c, batches, peak):
         pre["peak_kind"] = dkind
         out[fmt] = {"expert_bytes": expert_bytes(work.layer), "decode_all_resident": dec, "prefill_n8192": pre}
         c.pools.clear()
+    # W4A8 on the prefill chunk: the MXFP4 layer with MXFP8 activations
+    # (tcgen05 kind::mxf8f6f4, E4M3 x E2M1, at the FP8 rate)
+    pw8 = dataclasses.replace(wl.PREFILL_35B, name=wl.PREFILL_35B.name + "_w4a8",
+                              layer=dataclasses.replace(wl.PREFILL_35B.layer, prefill_act=wl.MXFP8))
+    dpeak, dkind = _dtype_peak("mxfp8")
+    pre = prefill_summary(run_prefill(c, pw8), dpeak)
+    pre["peak_TFLOP_s"] = dpeak
+    pre["peak_kind"] = dkind
+    out["w4a8_prefill_n8192"] = pre
+    c.pools.clear()
     # W4A16 on a prefill chunk: the MXFP4 layer's 8192-token chunk through the
     # decode regime (FP4 weights x bf16-class activations, mma.sync GEMV),
     # next to its W4A4 tcgen05 prefill

@@ -79,6 +79,15 @@ typedef struct {
     int max_tokens;   /* largest N of one moe_forward (sizes the workspaces)  */
     float act_scale_x;/* NVFP4 prefill: static fp32 scale of x (power of 2)   */
     float act_scale_h;/* NVFP4 prefill: static fp32 scale of h (power of 2)   */
+    int prefill_act_bits; /* activations of the prefill regime: 0 (or the
+                       * weights' own code bits: 4, 8, 16) = the weights' own
+                       * format; 8 on MOE_MXFP4 weights = MXFP8 activations,
+                       * W4A8 (x and h quantised to MXFP8; tcgen05
+                       * kind::mxf8f6f4 with E4M3 x E2M1 operands).  The
+                       * FreeToken engine serves MXFP4, NVFP4, FP8 and BF16
+                       * precisions (juejin.cn overview, §五 "模型生态与硬件支持");
+                       * FP4 weights under FP8 activations pair two of them.
+                       * Other values: MOE_ERR_ARG.                          */
 } moe_layer_desc;
 
 /* Byte layout of one expert (identical in the host pool and in a slot).
@@ -328,8 +337,10 @@ int moe_debug_last_step(moe_layer_t layer, int* idx, float* gates, int* counts, 
  * N*k permuted rows (+ N shared-expert rows, token order, when the layer has
  * one).  After a decode call: h fp32 [rows, 2*d_ff] = W_g x | W_u x of each
  * row (block scales and tensor scales applied).  After a prefill call:
- * hq_codes [rows, d_ff/2] and hq_scales [rows, d_ff/block], the FP4 codes and
- * block scales of h = SiLU(W_g x) * (W_u x) that the down GEMM consumed.
+ * hq_codes and hq_scales, the codes and block scales of h = SiLU(W_g x) *
+ * (W_u x) that the down GEMM consumed, in the prefill activation format:
+ * FP4 [rows, d_ff/2] + [rows, d_ff/block]; MXFP8 [rows, d_ff] + [rows,
+ * d_ff/32]; bf16 [rows, 2 d_ff] bytes, no scales.
  * MOE_ERR_STATE when the requested arrays were not produced by that call. */
 int moe_debug_last_hidden(moe_layer_t layer, float* h, uint8_t* hq_codes, uint8_t* hq_scales,
                           void* stream);
@@ -377,9 +388,11 @@ int moe_debug_step_trace(moe_layer_t layer, uint64_t* out, int cap, int* n_cta, 
  * in slot `slot` (slot -1: the shared expert), written row-major to out. */
 int moe_debug_dequant(moe_layer_t layer, int slot, int m, float* out, void* stream);
 
-/* FP4 activation quantiser of the prefill regime on fp32 rows v [rows, K]:
- * packed codes [rows, K/2], scale bytes [rows, K/block]; `which` 0 uses
- * act_scale_x, 1 act_scale_h (NVFP4 only). */
+/* Activation quantiser of the prefill regime (the layer's prefill activation
+ * format) on fp32 rows v [rows, K]: FP4 packed codes [rows, K/2] + scale
+ * bytes [rows, K/block]; MXFP8 codes [rows, K] + E8M0 bytes [rows, K/32];
+ * bf16 [rows, 2K] bytes (scales untouched).  `which` 0 uses act_scale_x, 1
+ * act_scale_h (NVFP4 only). */
 int moe_debug_actquant(moe_layer_t layer, const float* v, int rows, int K,
                        uint8_t* codes, uint8_t* scales, int which, void* stream);
 

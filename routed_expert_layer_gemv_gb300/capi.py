@@ -62,7 +62,7 @@ class moe_layer_desc(C.Structure):
     _fields_ = [("E", C.c_int), ("k", C.c_int), ("d_model", C.c_int), ("d_ff", C.c_int),
                 ("n_slots", C.c_int), ("fmt", C.c_int), ("has_shared", C.c_int),
                 ("norm_topk", C.c_int), ("has_bias", C.c_int), ("max_tokens", C.c_int),
-                ("act_scale_x", C.c_float), ("act_scale_h", C.c_float)]
+                ("act_scale_x", C.c_float), ("act_scale_h", C.c_float), ("prefill_act_bits", C.c_int)]
 
 
 class moe_expert_layout(C.Structure):

@@ -229,6 +229,9 @@ int check_desc(const moe_layer_desc* d, std::string* why, int max_slots) {
   }
   if (d->fmt != MOE_MXFP4 && d->fmt != MOE_NVFP4 && d->fmt != MOE_MXFP8 && d->fmt != MOE_BF16)
     return bad("fmt must be MOE_MXFP4, MOE_NVFP4, MOE_MXFP8 or MOE_BF16");
+  if (d->prefill_act_bits != 0 && d->prefill_act_bits != fmt_code_bits(d->fmt) &&
+      !(d->fmt == MOE_MXFP4 && d->prefill_act_bits == 8))
+    return bad("prefill_act_bits must be 0, the weights' code bits, or 8 on MOE_MXFP4 weights");
   if (d->max_tokens < 1) return bad("max_tokens must be >= 1");
   if ((long long)d->max_tokens * (d->k + 1) > (1LL << 30)) return bad("max_tokens * (k+1) too large");
   if (d->fmt == MOE_NVFP4 && (!is_pow2_float(d->act_scale_x) || !is_pow2_float(d->act_scale_h))) {
@@ -258,6 +261,7 @@ void fill_layout(const moe_layer_desc* d, moe_expert_layout* l) {
 Geo make_geo(const moe_layer_desc* d, const moe_expert_layout* l) {
   Geo g{};
   g.E = d->E; g.k = d->k; g.d = d->d_model; g.f = d->d_ff; g.S = d->n_slots; g.fmt = d->fmt;
+  g.afmt = d->fmt == MOE_MXFP4 && d->prefill_act_bits == 8 ? MOE_MXFP8 : d->fmt;
   g.has_shared = d->has_shared ? 1 : 0; g.norm_topk = d->norm_topk ? 1 : 0;
   g.has_bias = d->has_bias ? 1 : 0;
   g.blk = fmt_block(d->fmt);
@@ -562,11 +566,12 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
   MOE_ALLOC(rcounter, 16);
   MOE_ALLOC(step_trace, (size_t)std::max(L->num_sms, 1) * kStepMarks * 8);
   if (prefill_ok) {
-    // prefill activations in the weights' element type (codes, then block scales)
-    MOE_ALLOC(xq_codes, prows * g.d * fmt_code_bits(g.fmt) / 8);
-    MOE_ALLOC(xq_scales, prows * std::max(16, fmt_scale_row(g.fmt, g.d)));
-    MOE_ALLOC(hq_codes, prows * g.f * fmt_code_bits(g.fmt) / 8);
-    MOE_ALLOC(hq_scales, prows * std::max(16, fmt_scale_row(g.fmt, g.f)));
+    // prefill activations in their format (the weights' own, or MXFP8 for
+    // W4A8): codes, then block scales
+    MOE_ALLOC(xq_codes, prows * g.d * fmt_code_bits(g.afmt) / 8);
+    MOE_ALLOC(xq_scales, prows * std::max(16, fmt_scale_row(g.afmt, g.d)));
+    MOE_ALLOC(hq_codes, prows * g.f * fmt_code_bits(g.afmt) / 8);
+    MOE_ALLOC(hq_scales, prows * std::max(16, fmt_scale_row(g.afmt, g.f)));
     MOE_ALLOC(tiles, prefill_tile_bytes(g, (int)Nm));
     MOE_ALLOC(n_tiles, 16);
   }
@@ -1548,10 +1553,10 @@ int moe_debug_last_hidden(moe_layer_t L, float* h, uint8_t* hq_codes, uint8_t* h
   const size_t rows = (size_t)N * g.k + (g.has_shared ? N : 0);
   if (h) MOE_CUDA(L, cudaMemcpyAsync(h, L->h, rows * 2 * g.f * 4, cudaMemcpyDeviceToDevice, st));
   if (hq_codes)
-    MOE_CUDA(L, cudaMemcpyAsync(hq_codes, L->hq_codes, rows * g.f * fmt_code_bits(g.fmt) / 8,
+    MOE_CUDA(L, cudaMemcpyAsync(hq_codes, L->hq_codes, rows * g.f * fmt_code_bits(g.afmt) / 8,
                                 cudaMemcpyDeviceToDevice, st));
-  if (hq_scales && fmt_scale_row(g.fmt, g.f))
-    MOE_CUDA(L, cudaMemcpyAsync(hq_scales, L->hq_scales, rows * fmt_scale_row(g.fmt, g.f),
+  if (hq_scales && fmt_scale_row(g.afmt, g.f))
+    MOE_CUDA(L, cudaMemcpyAsync(hq_scales, L->hq_scales, rows * fmt_scale_row(g.afmt, g.f),
                                 cudaMemcpyDeviceToDevice, st));
   return MOE_OK;
 }

@@ -122,6 +122,7 @@ __host__ __device__ constexpr int fmt_scale_row(int fmt, int K) {
 // ---------------------------------------------------------------- layer geometry
 struct Geo {
   int E, k, d, f, S, fmt, has_shared, norm_topk, has_bias;
+  int afmt;                    // activation format of the prefill regime (fmt, or MXFP8 on MXFP4: W4A8)
   int X;                       // spare buffers: the pool holds S + 1 + X (the shared expert's is S)
   // The slot table is keyed: key = key0 + expert.  A lone layer has key0 = 0
   // and keys = E; layer l of a stack of L layers sharing one pool and one

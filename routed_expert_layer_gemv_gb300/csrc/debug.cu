@@ -106,16 +106,17 @@ cudaError_t launch_dequant(const Geo& g, const uint8_t* expert, int m, float* ou
 
 cudaError_t launch_actquant(const Geo& g, const float* v, int rows, int K, uint8_t* codes,
                             uint8_t* scales, float gscale, cudaStream_t st) {
-  if (g.fmt == MOE_MXFP8 || g.fmt == MOE_BF16) {
+  const int af = g.afmt;   // the prefill regime's activation format
+  if (af == MOE_MXFP8 || af == MOE_BF16) {
     const size_t total = (size_t)rows * (K / 32);
     if (total == 0) return cudaSuccess;
-    actquant8_16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(v, rows, K, g.fmt, codes, scales);
+    actquant8_16_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(v, rows, K, af, codes, scales);
     return cudaGetLastError();
   }
-  const int nb = K / g.blk;
+  const int nb = K / fmt_block(af);
   const size_t total = (size_t)rows * nb;
   if (total == 0) return cudaSuccess;
-  actquant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(v, rows, K, g.fmt, gscale, codes,
+  actquant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(v, rows, K, af, gscale, codes,
                                                                   scales);
   return cudaGetLastError();
 }

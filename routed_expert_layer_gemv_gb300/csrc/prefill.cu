@@ -32,6 +32,15 @@ namespace moe {
 namespace {
 
 constexpr int kTileRows = 128;          // M and N of one MMA tile
+
+// Kernel variant of W4A8: MXFP4 weights under MXFP8 activations.  The MMA is
+// kind::mxf8f6f4 with E4M3 A and E2M1 B; the FP4 weight tiles are loaded by
+// TMA as 16 x U4 packed values per 16-byte shared-memory chunk (the unpacked
+// layout that kind reads), so both operands have 128-byte rows of 128
+// elements per stage and one E8M0 scale per 32 along K.
+constexpr int kW4A8 = 100;
+// The activation (A) operand's format of a kernel variant.
+__host__ __device__ constexpr int act_op_fmt(int F) { return F == kW4A8 ? MOE_MXFP8 : F; }
 constexpr int kKTileBytes = 128;        // 256 FP4 codes per K tile
 constexpr int kOpBytes = kTileRows * kKTileBytes;   // 16 KB per operand tile
 
@@ -259,12 +268,17 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
                const __grid_constant__ CUtensorMap tb1, GemmArgs p) {
   // K elements per 128-byte stage row and 4-byte scale groups per row per stage:
   // MXFP4 256 / 2, NVFP4 256 / 4, MXFP8 128 / 1, bf16 64 / 0 (no scales)
-  constexpr int KST = 1024 / fmt_code_bits(FMT);
-  constexpr int G = FMT == MOE_MXFP4 ? 2 : FMT == MOE_NVFP4 ? 4 : FMT == MOE_MXFP8 ? 1 : 0;
+  constexpr int AF = act_op_fmt(FMT);
+  constexpr int KST = 1024 / fmt_code_bits(AF);
+  constexpr int G = FMT == MOE_MXFP4 ? 2 : FMT == MOE_NVFP4 ? 4 : AF == MOE_MXFP8 ? 1 : 0;
   constexpr int SB = 4 * G;                       // scale bytes per row per stage
   constexpr int SFC = 2 * 4 * (G > 0 ? G : 1);    // TMEM columns of one scale slot (A, then B)
   constexpr int NCOL = PH == 1 ? 64 : 128;        // output columns of one tile
   constexpr int kWsStages = ws_stages<PH>();
+  // bytes the B loads of a stage count on its barrier: the 16 x U4 loads of
+  // W4A8 count the packed bytes they read (8 KB of codes for the 16 KB they
+  // fill with their padding)
+  constexpr uint32_t kBTxBytes = FMT == kW4A8 ? kOpBytes / 2 : kOpBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kWsStages], empty[kWsStages], sfull[kWsStages], accf[2], acce[2], fin;
@@ -294,7 +308,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int NT = p.rows_out / NCOL;
   const long long T = (long long)n_m * NT;
   const int nkt = p.K / KST;
-  const int srow = fmt_scale_row(FMT, p.K);   // scale bytes per row
+  const int srow = fmt_scale_row(AF, p.K);    // scale bytes per row (A and B alike)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -309,7 +323,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
           const uint32_t k = it / kWsStages;
           if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) { stop = true; break; }
           uint8_t* st = smem + (size_t)s * 2 * kOpBytes;
-          tc::mbar_expect_tx(&full[s], 2 * kOpBytes);
+          tc::mbar_expect_tx(&full[s], kOpBytes + kBTxBytes);
           tc::tma_load_2d(st, &ta, &full[s], kt * kKTileBytes, tile.row_start);
           if (PH == 1) {
             tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
@@ -353,9 +367,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
               tc::mma_mxf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, true, id, id), sfa + 4 * g, sfb + 4 * g, acc);
             } else if (FMT == MOE_NVFP4) {
               tc::mma_nvf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, false, 0, 0), sfa + 4 * kk, sfb + 4 * kk, acc);
-            } else if (FMT == MOE_MXFP8) {
-              // one E8M0 scale per 32-K MMA: byte kk of the stage's group
-              tc::mma_mxf8(tb + 128 * b, ad, bd, tc::idesc_mxf8(128, kk, kk), sfa, sfb, acc);
+            } else if (AF == MOE_MXFP8) {
+              // one E8M0 scale per 32-K MMA: byte kk of the stage's group;
+              // B E4M3 (W8A8) or E2M1 (W4A8)
+              tc::mma_mxf8(tb + 128 * b, ad, bd, tc::idesc_mxf8(128, kk, kk, FMT == kW4A8), sfa, sfb, acc);
             } else {
               tc::mma_bf16(tb + 128 * b, ad, bd, tc::idesc_bf16(128), acc);
             }
@@ -398,7 +413,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         uint32_t wa[4][G > 0 ? G : 1], wv[4][G > 0 ? G : 1];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (FMT == MOE_MXFP8) {
+          if (AF == MOE_MXFP8) {
             wa[j][0] = *reinterpret_cast<const uint32_t*>(pa[j] + kt * SB);
             wv[j][0] = *reinterpret_cast<const uint32_t*>(pb[j] + kt * SB);
           } else if (FMT == MOE_MXFP4) {
@@ -474,9 +489,9 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             const float a = __uint_as_float(gv[i2]) * sg, u = __uint_as_float(uv[i2]) * su;
             hv[i2] = a / (1.0f + __expf(-a)) * u;
           }
-          if (live && (FMT == MOE_MXFP8 || FMT == MOE_BF16)) {
+          if (live && (AF == MOE_MXFP8 || AF == MOE_BF16)) {
             const int col = n0 + 32 * c;
-            if (FMT == MOE_MXFP8) {
+            if (AF == MOE_MXFP8) {
               uint32_t w8[8];
               p.h_scales[(size_t)r * (f / 32) + col / 32] = (uint8_t)quant_mx8_32(hv, w8);
               uint4* dst = reinterpret_cast<uint4*>(p.h_codes + (size_t)r * f + col);
@@ -603,6 +618,24 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed FP4 rows [slots][rows][K] (K / 2 bytes per row) loaded unpacked for
+// kind::mxf8f6f4: boxes of 128 codes x box_rows rows, each 16 codes landing
+// in a 16-byte chunk (128 shared-memory bytes per box row), 128B swizzle.
+// The encoder checks what this type needs: a 32-byte aligned base, K a
+// multiple of 128, strides multiples of 32 bytes.
+bool make_map_3d_u4(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t slots,
+                    uint64_t slot_stride, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {K, rows, slots};
+  cuuint64_t strides[2] = {K / 2, slot_stride};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
                  uint64_t slot_stride, uint32_t box_rows = kTileRows) {
   EncodeTiledFn fn = encode_fn();
@@ -621,7 +654,7 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
 
 // ---------------------------------------------------------------- host side
 struct PrefillPlan {
-  CUtensorMap xq, hq, wg, wu, wd;
+  CUtensorMap xq, hq, wd;
   CUtensorMap wg64, wu64;   // gate / up in 64-row boxes (stacked into one 128-row B tile)
   bool ready;
 };
@@ -633,11 +666,19 @@ bool prefill_shape_ok(const Geo& g) {
 PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8_t* xq_codes, size_t xq_rows,
                                  const uint8_t* hq_codes) {
   PrefillPlan* pl = new PrefillPlan();
+  // activation rows in the prefill activation format, weight rows in the
+  // weights' own (W4A8: FP4 weights loaded unpacked)
+  const uint64_t da = (uint64_t)g.d * fmt_code_bits(g.afmt) / 8, fa = (uint64_t)g.f * fmt_code_bits(g.afmt) / 8;
+  pl->ready = make_map_2d(&pl->xq, xq_codes, da, xq_rows) && make_map_2d(&pl->hq, hq_codes, fa, xq_rows);
+  if (g.afmt != g.fmt) {
+    pl->ready = pl->ready && g.fmt == MOE_MXFP4 && g.afmt == MOE_MXFP8 &&
+                make_map_3d_u4(&pl->wd, slots + g.off_codes[2], g.f, g.d, g.nbuf, g.ebytes, kTileRows) &&
+                make_map_3d_u4(&pl->wg64, slots + g.off_codes[0], g.d, g.f, g.nbuf, g.ebytes, 64) &&
+                make_map_3d_u4(&pl->wu64, slots + g.off_codes[1], g.d, g.f, g.nbuf, g.ebytes, 64);
+    return pl;
+  }
   const uint64_t db = (uint64_t)g.d * fmt_code_bits(g.fmt) / 8, fb = (uint64_t)g.f * fmt_code_bits(g.fmt) / 8;
-  pl->ready = make_map_2d(&pl->xq, xq_codes, db, xq_rows) &&
-              make_map_2d(&pl->hq, hq_codes, fb, xq_rows) &&
-              make_map_3d(&pl->wg, slots + g.off_codes[0], db, g.f, g.nbuf, g.ebytes) &&
-              make_map_3d(&pl->wu, slots + g.off_codes[1], db, g.f, g.nbuf, g.ebytes) &&
+  pl->ready = pl->ready &&
               make_map_3d(&pl->wd, slots + g.off_codes[2], fb, g.d, g.nbuf, g.ebytes) &&
               make_map_3d(&pl->wg64, slots + g.off_codes[0], db, g.f, g.nbuf, g.ebytes, 64) &&
               make_map_3d(&pl->wu64, slots + g.off_codes[1], db, g.f, g.nbuf, g.ebytes, 64);
@@ -651,7 +692,7 @@ cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int*
                                 uint8_t* codes, uint8_t* scales, cudaStream_t st) {
   const size_t total = (size_t)N * (g.d / 32);
   if (total == 0) return cudaSuccess;
-  gather_quant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(x, row_of, N, g.k, g.d, g.fmt, gx,
+  gather_quant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(x, row_of, N, g.k, g.d, g.afmt, gx,
                                                                       g.has_shared, codes, scales);
   return cudaGetLastError();
 }
@@ -679,6 +720,8 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 1>, s1);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 1>, s1);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_BF16, 1>, s1);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<kW4A8, 1>, s1);
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<kW4A8, 2>, s2);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 2>, s2);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 2>, s2);
     if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 2>, s2);
@@ -705,7 +748,9 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.act_scale_h = gh;
   const int grid1 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.f / 64));
   if (ev) cudaEventRecord(ev[0], st);
-  if (g.fmt == MOE_MXFP4)
+  if (g.afmt != g.fmt)
+    gemm_ws_kernel<kW4A8, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+  else if (g.fmt == MOE_MXFP4)
     gemm_ws_kernel<MOE_MXFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   else if (g.fmt == MOE_NVFP4)
     gemm_ws_kernel<MOE_NVFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
@@ -728,7 +773,9 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.O_exp = prefill_o_exp(g, O, N);
   const int grid2 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.d / kTileRows));
   if (ev) cudaEventRecord(ev[2], st);
-  if (g.fmt == MOE_MXFP4)
+  if (g.afmt != g.fmt)
+    gemm_ws_kernel<kW4A8, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+  else if (g.fmt == MOE_MXFP4)
     gemm_ws_kernel<MOE_MXFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else if (g.fmt == MOE_NVFP4)
     gemm_ws_kernel<MOE_NVFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);

@@ -147,11 +147,15 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a, uint64_t b
                   "r"((uint32_t)accumulate));
 }
 
-// Instruction descriptor of a block-scaled MXFP8 MMA (E4M3 x E4M3, UE8M0
-// scales, M = 128, dense, K-major); sf_a / sf_b select the scale byte of the
-// 4-byte group (one scale per 32-K MMA).
-__device__ __forceinline__ uint32_t idesc_mxf8(int N, uint32_t sf_a, uint32_t sf_b) {
-  uint32_t d = 0;                                 // A and B E4M3 (type 0)
+// Instruction descriptor of a block-scaled kind::mxf8f6f4 MMA (A E4M3; B
+// E4M3, or E2M1 when b_e2m1; UE8M0 scales, M = 128, dense, K-major); sf_a /
+// sf_b select the scale byte of the 4-byte group (one scale per 32-K MMA).
+// An E2M1 operand sits in shared memory unpacked, 16 codes (8 bytes) per
+// 16-byte chunk as the TMA's 16 x U4 load writes them, so its rows have the
+// byte extent of an E4M3 tile (128 elements per 128-byte row).
+__device__ __forceinline__ uint32_t idesc_mxf8(int N, uint32_t sf_a, uint32_t sf_b, bool b_e2m1 = false) {
+  uint32_t d = 0;                                 // A E4M3 (type 0)
+  if (b_e2m1) d |= 5u << 10;                      // B E2M1 (type 5 of this kind)
   d |= (uint32_t)(N >> 3) << 17;
   d |= 1u << 23;                                  // UE8M0 scales
   d |= (128u >> 4) << 24;

@@ -14,7 +14,7 @@ import numpy as np
 import torch
 
 from . import capi
-from .workloads import BF16, LayerSpec, Matrix, MXFP4, MXFP8, NVFP4
+from .workloads import BF16, CODE_BITS, LayerSpec, Matrix, MXFP4, MXFP8, NVFP4
 
 FMT_IDS = {MXFP4: capi.MOE_MXFP4, NVFP4: capi.MOE_NVFP4, MXFP8: capi.MOE_MXFP8, BF16: capi.MOE_BF16}
 
@@ -26,7 +26,8 @@ def make_desc(spec: LayerSpec, max_tokens: int, act_scale_x: float = 1.0,
         fmt=FMT_IDS[spec.fmt],
         has_shared=int(spec.has_shared), norm_topk=int(spec.norm_topk),
         has_bias=int(spec.has_bias), max_tokens=max_tokens,
-        act_scale_x=act_scale_x, act_scale_h=act_scale_h)
+        act_scale_x=act_scale_x, act_scale_h=act_scale_h,
+        prefill_act_bits=CODE_BITS[spec.prefill_act] if spec.prefill_act else 0)
 
 
 def pack_expert(layout: capi.moe_expert_layout, w: Dict[str, Matrix], out: np.ndarray) -> None:

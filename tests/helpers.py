@@ -132,7 +132,8 @@ def prefill_h_flip_tokens(L, spec, O, X, idx):
     from oracle.native import layer as olayer
     N, k, blk, f = X.shape[0], spec.k, spec.block, spec.d_ff
     rows = N * k + (N if spec.has_shared else 0)
-    mx8 = spec.fmt == "mxfp8"
+    af = spec.act_fmt                      # the prefill activation format
+    mx8 = af == "mxfp8"
     hc = torch.empty(rows, f if mx8 else f // 2, dtype=torch.uint8, device="cuda")
     hs = torch.empty(rows, f // blk, dtype=torch.uint8, device="cuda")
     capi.moe_debug_last_hidden(L.h, hq_codes=hc, hq_scales=hs)
@@ -144,7 +145,7 @@ def prefill_h_flip_tokens(L, spec, O, X, idx):
     e4_mid = ((e4[1:] + e4[:-1]) / 2)[1:]                  # E4M3 rounding midpoints (> 0)
     HS = hs.cpu().numpy()
     R = row_of.cpu().numpy().reshape(N, k)
-    xq = olayer.act_roundtrip(X, spec.fmt, 1.0)
+    xq = olayer.act_roundtrip(X, af, 1.0)
     flag = np.zeros(N, dtype=bool)
     n_codes = n_diff = 0
     jobs = []
@@ -156,8 +157,8 @@ def prefill_h_flip_tokens(L, spec, O, X, idx):
     for W, toks, rws in jobs:
         h = olayer.silu(xq[toks] @ W["gate"].T) * (xq[toks] @ W["up"].T)
         amax = np.abs(h.astype(np.float32).reshape(len(toks), -1, blk)).max(axis=-1).astype(np.float64)
-        if spec.fmt in ("mxfp4", "mxfp8"):
-            rc, rsc = quant.quant_mxfp4(h) if spec.fmt == "mxfp4" else quant.quant_mxfp8(h)
+        if af in ("mxfp4", "mxfp8"):
+            rc, rsc = quant.quant_mxfp4(h) if af == "mxfp4" else quant.quant_mxfp8(h)
             with np.errstate(divide="ignore"):
                 lg = np.log2(np.where(amax > 0, amax, 1.0))
             edge = np.abs(amax - np.exp2(np.round(lg))) <= 1e-4 * amax

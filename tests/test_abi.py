@@ -73,6 +73,21 @@ def test_invalid_descriptor_rejected_without_gpu(libpath, field, value):
     assert capi.lib().moe_expert_layout_for(d, out) == capi.MOE_ERR_ARG
 
 
+@pytest.mark.parametrize("fmt,bits,ok", [(capi.MOE_MXFP4, 0, True), (capi.MOE_MXFP4, 4, True),
+                                         (capi.MOE_MXFP4, 8, True), (capi.MOE_NVFP4, 8, False),
+                                         (capi.MOE_NVFP4, 4, True), (capi.MOE_MXFP8, 8, True),
+                                         (capi.MOE_MXFP8, 4, False), (capi.MOE_BF16, 8, False),
+                                         (capi.MOE_BF16, 16, True), (capi.MOE_MXFP4, 16, False)])
+def test_prefill_activation_format_checked_without_gpu(libpath, fmt, bits, ok):
+    # W4A8 (MXFP8 activations) exists for MXFP4 weights only: NVFP4's E4M3
+    # scales per 16 have no kind::mxf8f6f4 block-scale form
+    d = capi.moe_layer_desc(E=8, k=2, d_model=256, d_ff=512, n_slots=8, fmt=fmt,
+                            has_shared=0, norm_topk=1, has_bias=0, max_tokens=16,
+                            act_scale_x=1.0, act_scale_h=1.0, prefill_act_bits=bits)
+    out = capi.moe_expert_layout()
+    assert capi.lib().moe_expert_layout_for(d, out) == (capi.MOE_OK if ok else capi.MOE_ERR_ARG)
+
+
 def test_nvfp4_scales_must_be_powers_of_two(libpath):
     d = capi.moe_layer_desc(E=8, k=2, d_model=256, d_ff=512, n_slots=8, fmt=capi.MOE_NVFP4,
                             has_shared=0, norm_topk=1, has_bias=0, max_tokens=16,

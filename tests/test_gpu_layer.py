@@ -627,6 +627,9 @@ PRE = capi.MOE_REGIME_PREFILL
     (small_spec(E=16, k=4, d_model=512, d_ff=512, n_slots=16, fmt="bf16", has_bias=True), 200),
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, fmt="mxfp8"), 256),   # the 35B-A3B shape
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, fmt="bf16"), 256),
+    # FP4 weights x FP8 activations (W4A8)
+    (small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True, prefill_act="mxfp8"), 300),
+    (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, prefill_act="mxfp8"), 256),
 ])
 def test_prefill_all_resident(spec, N):
     seed = 17
@@ -638,8 +641,8 @@ def test_prefill_all_resident(spec, N):
     O = oracle_layer(spec, seed)
     X = wl.bf16_bits_to_f64(x)
     ref, idx, _ = O.forward(X, "prefill")
-    if spec.fmt == "mxfp8":
-        # W8A8: E4M3's grid is 8x finer than E2M1's, so at this size some h
+    if spec.act_fmt == "mxfp8":
+        # W8A8 and W4A8: E4M3's grid is 8x finer than E2M1's, so at this size some h
         # values lie where fp32 and FP64 sums round to neighbouring E4M3 codes;
         # each such code is checked to sit at a rounding boundary and its tokens
         # are left out of the per-element bound (the Frobenius bound keeps all)
@@ -820,9 +823,10 @@ def test_prefill_quantised_h_codes(spec, N):
     L.close()
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "bf16"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "bf16", "w4a8"])
 def test_prefill_fp8_bf16_with_misses_and_waves(fmt):
-    spec = small_spec(E=24, k=3, d_model=512, d_ff=256, n_slots=5, fmt=fmt, has_shared=True, has_bias=True)
+    kw = dict(prefill_act="mxfp8") if fmt == "w4a8" else dict(fmt=fmt)
+    spec = small_spec(E=24, k=3, d_model=512, d_ff=256, n_slots=5, has_shared=True, has_bias=True, **kw)
     seed, N = 24, 96
     experts = CachedExperts(spec, seed)
     L = build_layer(spec, seed, N, experts_fn=experts)
