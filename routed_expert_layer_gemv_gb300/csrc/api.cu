@@ -105,6 +105,8 @@ struct moe_layer {
   uint8_t* xq_scales = nullptr;
   uint8_t* hq_codes = nullptr;   // FP4 h [(rows + 128), f/2]
   uint8_t* hq_scales = nullptr;
+  int* pbase = nullptr;          // padded 128-row block of each expert's rows (E + 2)
+  uint8_t* wsf = nullptr;        // one launch's weight scales, interleaved for tcgen05.cp
   void* tiles = nullptr;
   int* n_tiles = nullptr;
   PrefillPlan* plan = nullptr;
@@ -530,6 +532,8 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
     L->xq_scales = base->xq_scales;
     L->hq_codes = base->hq_codes;
     L->hq_scales = base->hq_scales;
+    L->pbase = base->pbase;
+    L->wsf = base->wsf;
     L->tiles = base->tiles;
     L->n_tiles = base->n_tiles;
     L->gplan = base->gplan;
@@ -569,9 +573,11 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
     // prefill activations in their format (the weights' own, or MXFP8 for
     // W4A8): codes, then block scales
     MOE_ALLOC(xq_codes, prows * g.d * fmt_code_bits(g.afmt) / 8);
-    MOE_ALLOC(xq_scales, prows * std::max(16, fmt_scale_row(g.afmt, g.d)));
+    MOE_ALLOC(xq_scales, prefill_act_scale_bytes(g, (int)Nm, g.d));
     MOE_ALLOC(hq_codes, prows * g.f * fmt_code_bits(g.afmt) / 8);
-    MOE_ALLOC(hq_scales, prows * std::max(16, fmt_scale_row(g.afmt, g.f)));
+    MOE_ALLOC(hq_scales, prefill_act_scale_bytes(g, (int)Nm, g.f));
+    MOE_ALLOC(pbase, (size_t)(g.E + 2) * 4);
+    MOE_ALLOC(wsf, prefill_wscale_bytes(g));
     MOE_ALLOC(tiles, prefill_tile_bytes(g, (int)Nm));
     MOE_ALLOC(n_tiles, 16);
   }
@@ -1214,9 +1220,10 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   const float gh = g.fmt == MOE_NVFP4 ? L->desc.act_scale_h : 1.0f;
   if (prefill) {
     pe = prof_begin(L, MOE_PROF_PREFILL, st);
-    MOE_CUDA(L, launch_gather_quant(g, xd, L->row_of, N, gx, L->xq_codes, L->xq_scales, st));
+    MOE_CUDA(L, launch_gather_quant(g, xd, L->idx, L->row_of, L->counts, L->offsets, N, gx, L->pbase, L->xq_codes,
+                                    L->xq_scales, st));
     prof_end(pe, st);
-    L->launches += 1;
+    L->launches += 2;
   }
   // SM fills (decode): kFillSms SMs copy the misses, the expert GEMV takes
   // the others, and the hits' phase 2 is launched after the host has read the
@@ -1236,11 +1243,11 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     }
     cudaError_t ce;
     if (prefill) {
-      ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, N, a.mode, a.with_shared,
+      ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, L->pbase, N, a.mode, a.with_shared,
                                 L->tiles, L->n_tiles, L->slots, L->xq_scales, L->hq_codes,
-                                L->hq_scales, L->O, gx, gh, L->err_dev, L->gemm_sms > 0 ? L->gemm_sms : L->num_sms,
-                                st, evp);
-      L->launches += 3;
+                                L->hq_scales, L->wsf, L->O, gx, gh, L->err_dev,
+                                L->gemm_sms > 0 ? L->gemm_sms : L->num_sms, st, evp);
+      L->launches += fmt_block(g.afmt) ? 4 : 3;
     } else {
       ce = launch_gemv_decode(g, L->gplan, a, xd, L->xexp, L->h, L->O, n_ent, gemv_sms, st, evp, phases);
       L->launches += (phases & 1) + (phases >> 1 & 1);
@@ -1555,9 +1562,8 @@ int moe_debug_last_hidden(moe_layer_t L, float* h, uint8_t* hq_codes, uint8_t* h
   if (hq_codes)
     MOE_CUDA(L, cudaMemcpyAsync(hq_codes, L->hq_codes, rows * g.f * fmt_code_bits(g.afmt) / 8,
                                 cudaMemcpyDeviceToDevice, st));
-  if (hq_scales && fmt_scale_row(g.afmt, g.f))
-    MOE_CUDA(L, cudaMemcpyAsync(hq_scales, L->hq_scales, rows * fmt_scale_row(g.afmt, g.f),
-                                cudaMemcpyDeviceToDevice, st));
+  if (hq_scales && fmt_scale_row(g.afmt, g.f))   // stored by padded block: back to rows
+    MOE_CUDA(L, launch_untile_hscales(g, L->hq_scales, L->offsets, L->pbase, N, hq_scales, st));
   return MOE_OK;
 }
 

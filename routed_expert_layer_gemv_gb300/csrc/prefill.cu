@@ -48,17 +48,78 @@ struct Tile {
   int slot;       // pool buffer of the expert (Geo::shb: the shared expert)
   int row_start;  // first permuted row of the tile
   int row_end;    // one past the expert's last row
-  int pad;
+  int pb;         // padded 128-row block of the tile's activation scales
+  int ent;        // the expert's entry in the launch (its interleaved weight scales)
+  int pad[3];
 };
+
+// Block scales in the layout tcgen05.cp copies into TMEM (32x128b, one copy
+// per lane quarter): per 128-row block and per group of 4 scale bytes along
+// K, 512 bytes, byte 16 i + 4 j + b holding the scale of block row 32 j + i
+// and K-block 4 g + b.  ng: groups per row.
+__host__ __device__ inline size_t sf_off(size_t blk, int ng, int g, int row, int b) {
+  return (blk * ng + g) * 512 + 16 * (row & 31) + 4 * (row >> 5) + b;
+}
+__host__ __device__ constexpr int sf_groups(int fmt, int K) { return fmt_block(fmt) ? K / fmt_block(fmt) / 4 : 0; }
+
+// Exclusive scan of one int per thread over a block of up to 1024 threads;
+// returns the thread's prefix, *total gets the sum.
+__device__ int block_excl_scan(int v, int* sh33, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  if (lane == 31) sh33[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    const int x = lane < nw ? sh33[lane] : 0;
+    int xi = x;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += u;
+    }
+    if (lane < nw) sh33[lane] = xi - x;
+    if (lane == 31) sh33[32] = xi;
+  }
+  __syncthreads();
+  const int r = sh33[warp] + inc - v;
+  *total = sh33[32];
+  __syncthreads();
+  return r;
+}
+
+// pbase[e]: the first padded 128-row block of expert e's rows (experts in
+// ascending order, each taking ceil(count / 128) blocks); pbase[E]: the
+// shared expert's first block; pbase[E + 1]: the total.
+__global__ void __launch_bounds__(1024)
+pad_base_kernel(const int* __restrict__ counts, int E, int N, int with_shared, int* __restrict__ pbase) {
+  __shared__ int sh[33];
+  const int e = threadIdx.x;
+  const int nb = e < E ? (max(counts[e], 0) + kTileRows - 1) / kTileRows : 0;
+  int total;
+  const int pre = block_excl_scan(nb, sh, &total);
+  if (e < E) pbase[e] = pre;
+  if (e == 0) {
+    pbase[E] = total;
+    pbase[E + 1] = total + (with_shared ? (N + kTileRows - 1) / kTileRows : 0);
+  }
+}
 
 // ---------------------------------------------------------------- step 1
 // FP4 activations of every (token, expert) row: each token's 32-value groups
 // are quantised once and the codes and scales written to the token's k
 // permuted rows (row_of) and its shared-expert row N k + t.  Thread = (token,
 // group).
-__global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ row_of,
-                                    int N, int k, int d, int fmt, float gx, int with_shared,
-                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+// The scales go to the tcgen05.cp layout (sf_off) by padded block: row r of
+// expert e is row (r - offsets[e]) % 128 of block pbase[e] + (r - offsets[e]) / 128.
+__global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ idx,
+                                    const int* __restrict__ row_of, const int* __restrict__ offsets,
+                                    const int* __restrict__ pbase, int N, int k, int E, int d, int fmt,
+                                    float gx, int with_shared, uint8_t* __restrict__ codes,
+                                    uint8_t* __restrict__ scales) {
   const int nb = d / 32;                       // 32-value groups per row
   const size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= (size_t)N * nb) return;
@@ -76,6 +137,21 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
     }
   }
   const int nr = k + (with_shared ? 1 : 0);
+  const int ng = sf_groups(fmt, d);
+  // (padded block, row in the block) of the j-th row of token t
+  auto place = [&](int j, size_t* blk, int* rib) {
+    int local, b0;
+    if (j < k) {
+      const int e = idx[(size_t)t * k + j];
+      local = row_of[(size_t)t * k + j] - offsets[e];
+      b0 = pbase[e];
+    } else {
+      local = t;
+      b0 = pbase[E];
+    }
+    *blk = (size_t)b0 + local / kTileRows;
+    *rib = local % kTileRows;
+  };
   if (fmt == MOE_MXFP8 || fmt == MOE_BF16) {
     // W8A8: the group as 32 E4M3 bytes + an E8M0 byte; W16A16: x as it is
     uint4 cw[4];
@@ -95,7 +171,12 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
       const size_t r = j < k ? (size_t)row_of[(size_t)t * k + j] : (size_t)N * k + t;
       uint4* dst = reinterpret_cast<uint4*>(codes + r * rowb + (size_t)c * 16 * nv);
       for (int q = 0; q < nv; ++q) dst[q] = cw[q];
-      if (fmt == MOE_MXFP8) scales[r * (d / 32) + c] = (uint8_t)s8;
+      if (fmt == MOE_MXFP8) {
+        size_t blk;
+        int rib;
+        place(j, &blk, &rib);
+        scales[sf_off(blk, ng, c >> 2, rib, c & 3)] = (uint8_t)s8;
+      }
     }
     return;
   }
@@ -114,20 +195,23 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
   for (int j = 0; j < nr; ++j) {
     const size_t r = j < k ? (size_t)row_of[(size_t)t * k + j] : (size_t)N * k + t;
     *reinterpret_cast<uint4*>(codes + r * (d / 2) + (size_t)c * 16) = cw;
+    size_t blk;
+    int rib;
+    place(j, &blk, &rib);
     if (fmt == MOE_MXFP4) {
-      scales[r * (d / 32) + c] = (uint8_t)s0;
-    } else {
-      scales[r * (d / 16) + 2 * c] = (uint8_t)s0;
-      scales[r * (d / 16) + 2 * c + 1] = (uint8_t)s1;
+      scales[sf_off(blk, ng, c >> 2, rib, c & 3)] = (uint8_t)s0;
+    } else {   // K-blocks 2c and 2c + 1 of 16 values
+      scales[sf_off(blk, ng, c >> 1, rib, (2 * c) & 3)] = (uint8_t)s0;
+      scales[sf_off(blk, ng, c >> 1, rib, (2 * c + 1) & 3)] = (uint8_t)s1;
     }
   }
 }
 
 // ---------------------------------------------------------------- step 2
 __global__ void __launch_bounds__(1024)
-build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ offsets, int E, int S,
-                   int X, int shb, int N, int k, int mode, int with_shared, Tile* __restrict__ tiles,
-                   int* __restrict__ n_tiles) {
+build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ offsets,
+                   const int* __restrict__ pbase, int E, int S, int X, int shb, int N, int k, int mode,
+                   int with_shared, Tile* __restrict__ tiles, int* __restrict__ ents, int* __restrict__ n_tiles) {
   __shared__ int sh[33];
   __shared__ int carry;
   const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
@@ -141,19 +225,22 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
   const int* abuf = ae + 3 * E;
   for (int e0 = 0; e0 < n_ent; e0 += blockDim.x) {
     const int i = e0 + threadIdx.x;
-    int slot = -1, r0 = 0, nrows = 0;
+    int slot = -1, r0 = 0, nrows = 0, pb0 = 0;
     if (i < nr) {
       const int ex = ae[b + i], ls = as[b + i], bb = abuf[b + i];
       if (ex >= 0 && ex < E && ls >= 0 && ls < S && b + i - S < X && bb >= 0 && bb <= S + X && bb != S) {
         slot = bb;
         r0 = offsets[ex];
         nrows = offsets[ex + 1] - r0;
+        pb0 = pbase[ex];
       }
     } else if (i < n_ent) {
       slot = shb;
       r0 = N * k;
       nrows = N;
+      pb0 = pbase[E];
     }
+    if (i < n_ent) ents[i] = nrows > 0 ? slot : -1;
     const int nt = (nrows + kTileRows - 1) / kTileRows;
     // block exclusive scan of nt
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -182,21 +269,96 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
       tl.slot = slot;
       tl.row_start = r0 + t * kTileRows;
       tl.row_end = r0 + nrows;
-      tl.pad = 0;
+      tl.pb = pb0 + t;
+      tl.ent = i;
+      tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
       tiles[base + t] = tl;
     }
     __syncthreads();
     if (threadIdx.x == 0) carry += sh[32];
     __syncthreads();
   }
-  if (threadIdx.x == 0) *n_tiles = carry;
+  if (threadIdx.x == 0) {
+    n_tiles[0] = carry;
+    n_tiles[1] = n_ent;
+  }
+}
+
+// Weight block scales of the launch's experts (entry i: pool buffer ents[i])
+// in the tcgen05.cp layout, entry-major: phase 1 first (blocks q of the 64
+// gate rows 64 q .. over the same 64 up rows, K = d), then phase 2 (blocks of
+// 128 down rows, K = f).  Thread = one 16-byte row of a 512-byte group.
+__global__ void interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size_t off_g,
+                                          size_t off_u, size_t off_d, const int* __restrict__ ents,
+                                          const int* __restrict__ n_tiles, int d, int f, int blk,
+                                          uint8_t* __restrict__ wsf) {
+  const int ent = blockIdx.y;
+  if (ent >= n_tiles[1]) return;
+  const int slot = ents[ent];
+  if (slot < 0) return;
+  const int ng1 = d / blk / 4, ng2 = f / blk / 4;
+  const size_t n1 = (size_t)(f / 64) * ng1 * 32, n2 = (size_t)(d / kTileRows) * ng2 * 32;
+  const size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= n1 + n2) return;
+  const uint8_t* w = slots + (size_t)slot * ebytes;
+  uint8_t* out = wsf + (size_t)ent * (3 * (size_t)d * f / blk);
+  uint32_t word[4];
+  if (v < n1) {
+    const int i = (int)(v & 31), g = (int)((v >> 5) % ng1), q = (int)((v >> 5) / ng1);
+    const int srow = d / blk;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int rho = 32 * j + i;   // block row: gate rows first, then up
+      const uint8_t* src = w + (rho < 64 ? off_g : off_u) + (size_t)(64 * q + (rho & 63)) * srow + 4 * g;
+      word[j] = *reinterpret_cast<const uint32_t*>(src);
+    }
+    *reinterpret_cast<uint4*>(out + sf_off(q, ng1, g, i, 0)) = make_uint4(word[0], word[1], word[2], word[3]);
+  } else {
+    const size_t u = v - n1;
+    const int i = (int)(u & 31), g = (int)((u >> 5) % ng2), rb = (int)((u >> 5) / ng2);
+    const int srow = f / blk;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint8_t* src = w + off_d + (size_t)(kTileRows * rb + 32 * j + i) * srow + 4 * g;
+      word[j] = *reinterpret_cast<const uint32_t*>(src);
+    }
+    *reinterpret_cast<uint4*>(out + 2 * (size_t)d * f / blk + sf_off(rb, ng2, g, i, 0)) =
+        make_uint4(word[0], word[1], word[2], word[3]);
+  }
+}
+
+// Block scales of h back to rows [rows][f / blk] (test hook): row r of
+// expert e (offsets) sits in block pbase[e] + (r - offsets[e]) / 128.
+__global__ void untile_scales_kernel(const uint8_t* __restrict__ tiled, const int* __restrict__ offsets,
+                                     const int* __restrict__ pbase, int E, int Nk, int rows, int K, int blk,
+                                     uint8_t* __restrict__ out) {
+  const int nq = K / blk, ng = nq / 4;
+  const size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= (size_t)rows * nq) return;
+  const int r = (int)(v / nq), q = (int)(v % nq);
+  int b0, local;
+  if (r < Nk) {
+    int lo = 0, hi = E - 1;   // the expert whose rows hold r: largest e with offsets[e] <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (offsets[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    b0 = pbase[lo];
+    local = r - offsets[lo];
+  } else {
+    b0 = pbase[E];
+    local = r - Nk;
+  }
+  out[v] = tiled[sf_off((size_t)b0 + local / kTileRows, ng, q >> 2, local % kTileRows, q & 3)];
 }
 
 // ---------------------------------------------------------------- GEMM pieces
 struct GemmArgs {
   const Tile* tiles;
   const int* n_tiles;
-  const uint8_t* a_scales;     // [rows, K/blk] of the A operand (activations)
+  const uint8_t* a_scales;     // block scales of the A operand (activations), tcgen05.cp layout by padded block
+  const uint8_t* w_scales;     // the launch's weight scales, tcgen05.cp layout (this phase's part of entry 0)
+  size_t ent_bytes;            // bytes of one entry's weight scales (both phases)
   const uint8_t* slots;        // slot pool (n_slots + 1 experts; the last is shared)
   size_t ebytes;
   size_t w_scales_off[3];
@@ -217,22 +379,25 @@ struct GemmArgs {
 };
 
 // ---------------------------------------------------------------- persistent warp-specialised GEMM
-// One CTA per SM walks the launch's (M tile, N tile) pairs.  Ten warps, each
+// One CTA per SM walks the launch's (M tile, N tile) pairs.  Six warps, each
 // with one job, meeting only at mbarriers:
-//   warp 0     TMA: A (128 token rows x 256 K) and B (128 weight rows x 256 K,
-//              phase 1: 64 gate rows over the same 64 up rows) per stage;
-//   warp 1     one thread issues the block-scaled MMAs (M = 128, N = 128,
-//              K = 64 each) into one of two TMEM accumulators;
-//   warps 2-5  block scales: each loads the stage's A and B scale bytes from
-//              global memory (each 32-byte sector covers several stages, so
-//              most loads hit L1; the next sectors are prefetched) and writes
-//              them into a TMEM ring slot in the layout the MMA reads (every
-//              lane quarter holds all 128 rows), one warp per lane quarter;
-//   warps 6-9  epilogue, one per lane quarter (32 rows): drain an accumulator
-//              into registers, release it, then SiLU * mul + FP4 quantisation
-//              of h (phase 1) or the fp32 O rows (phase 2), while the MMAs of
-//              the next tile run into the other accumulator.
-constexpr int kWsThreads = 320;
+//   warp 0     TMA: A (128 token rows x one 128-byte K stage) and B (128
+//              weight rows, phase 1: 64 gate rows over the same 64 up rows)
+//              per stage, and with them the stage's block scales of A and B
+//              (G groups of 512 bytes each, already in the layout
+//              tcgen05.cp reads: activations quantised into it, weight
+//              scales interleaved per launch), all on one barrier;
+//   warp 1     one thread copies the stage's scales into its TMEM ring slot
+//              (tcgen05.cp, every lane quarter gets all 128 rows) and issues
+//              the block-scaled MMAs (M = 128, N = 128, four per stage) into
+//              one of two TMEM accumulators; copies and MMAs run in issue
+//              order, so no other warp touches the scales;
+//   warps 2-5  epilogue, one per lane quarter (32 rows): drain an accumulator
+//              into registers, release it, then SiLU * mul + quantisation
+//              of h (phase 1) or the scaled f16 O rows (phase 2), while the
+//              MMAs of the next tile run into the other accumulator.
+constexpr int kWsThreads = 192;
+constexpr int kEpiWarp0 = 2;
 constexpr int kSfBase = 256;            // TMEM columns 0..255: two 128-column accumulators
 
 // Ring stages: phase 1 takes 6; phase 2 takes 5 and keeps room to stage O
@@ -243,8 +408,18 @@ template <int PH> constexpr int ws_stages() { return PH == 1 ? 6 : 5; }
 constexpr int kOStrideB = 72;   // f16 elements per staged O row (144 bytes: conflict-free 16-byte stores)
 constexpr size_t kOStage = 4 * 32 * kOStrideB * 2;
 
-template <int PH>
-size_t ws_smem() { return 1024 + (size_t)ws_stages<PH>() * 2 * kOpBytes + (PH == 2 ? kOStage : 0); }
+// Scale groups of 4 bytes per row per stage: MXFP4 2 (8 blocks of 32 over
+// 256 K), NVFP4 4 (16 blocks of 16), MXFP8 / W4A8 1 (4 blocks of 32 over 128
+// K), bf16 0.
+__host__ __device__ constexpr int stage_groups(int FMT) {
+  return FMT == MOE_MXFP4 ? 2 : FMT == MOE_NVFP4 ? 4 : (FMT == MOE_MXFP8 || FMT == kW4A8) ? 1 : 0;
+}
+// Shared memory: the operand ring (1024-byte aligned stages), then each
+// stage's scales (A groups, then B groups), then (phase 2) the O staging.
+template <int FMT, int PH>
+size_t ws_smem() {
+  return 1024 + (size_t)ws_stages<PH>() * (2 * kOpBytes + 2 * 512 * stage_groups(FMT)) + (PH == 2 ? kOStage : 0);
+}
 
 __device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
   if (*abort_flag) return false;
@@ -258,10 +433,6 @@ __device__ __forceinline__ void ws_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::su32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" :: "l"(p));
-}
-
 template <int FMT, int PH>
 __global__ void __launch_bounds__(kWsThreads, 1)
 gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
@@ -270,8 +441,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   // MXFP4 256 / 2, NVFP4 256 / 4, MXFP8 128 / 1, bf16 64 / 0 (no scales)
   constexpr int AF = act_op_fmt(FMT);
   constexpr int KST = 1024 / fmt_code_bits(AF);
-  constexpr int G = FMT == MOE_MXFP4 ? 2 : FMT == MOE_NVFP4 ? 4 : AF == MOE_MXFP8 ? 1 : 0;
-  constexpr int SB = 4 * G;                       // scale bytes per row per stage
+  constexpr int G = stage_groups(FMT);
+  constexpr uint32_t kSfStage = 2 * 512 * G;      // scale bytes of a stage in shared memory (A, then B)
   constexpr int SFC = 2 * 4 * (G > 0 ? G : 1);    // TMEM columns of one scale slot (A, then B)
   constexpr int NCOL = PH == 1 ? 64 : 128;        // output columns of one tile
   constexpr int kWsStages = ws_stages<PH>();
@@ -281,7 +452,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   constexpr uint32_t kBTxBytes = FMT == kW4A8 ? kOpBytes / 2 : kOpBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kWsStages], empty[kWsStages], sfull[kWsStages], accf[2], acce[2], fin;
+  __shared__ __align__(8) uint64_t full[kWsStages], empty[kWsStages], accf[2], acce[2], fin;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -290,7 +461,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     for (int s = 0; s < kWsStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
-      tc::mbar_init(&sfull[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accf[b], 1);
@@ -308,7 +478,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int NT = p.rows_out / NCOL;
   const long long T = (long long)n_m * NT;
   const int nkt = p.K / KST;
-  const int srow = fmt_scale_row(AF, p.K);    // scale bytes per row (A and B alike)
+  const int ng = G > 0 ? nkt * G : 0;          // scale groups per row (A and B alike)
+  uint8_t* sf_smem = smem + (size_t)kWsStages * 2 * kOpBytes;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -323,7 +494,14 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
           const uint32_t k = it / kWsStages;
           if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) { stop = true; break; }
           uint8_t* st = smem + (size_t)s * 2 * kOpBytes;
-          tc::mbar_expect_tx(&full[s], kOpBytes + kBTxBytes);
+          tc::mbar_expect_tx(&full[s], kOpBytes + kBTxBytes + kSfStage);
+          if (G > 0) {
+            uint8_t* ss = sf_smem + (size_t)s * kSfStage;
+            tc::bulk_load(ss, p.a_scales + ((size_t)tile.pb * ng + (size_t)kt * G) * 512, 512 * G, &full[s]);
+            tc::bulk_load(ss + 512 * G,
+                          p.w_scales + (size_t)tile.ent * p.ent_bytes + ((size_t)(n0 / NCOL) * ng + (size_t)kt * G) * 512,
+                          512 * G, &full[s]);
+          }
           tc::tma_load_2d(st, &ta, &full[s], kt * kKTileBytes, tile.row_start);
           if (PH == 1) {
             tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
@@ -351,13 +529,21 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         for (int kt = 0; kt < nkt; ++kt, ++it) {
           const int s = it % kWsStages;
           const uint32_t ph = (it / kWsStages) & 1;
-          if (!ws_wait(&full[s], ph, &s_abort, p.err) || (G > 0 && !ws_wait(&sfull[s], ph, &s_abort, p.err))) {
+          if (!ws_wait(&full[s], ph, &s_abort, p.err)) {
             stop = true;
             break;
           }
           tc::fence_after();
           const uint32_t a_s = tc::su32(smem + (size_t)s * 2 * kOpBytes), b_s = a_s + kOpBytes;
           const uint32_t sfa = tb + kSfBase + (uint32_t)(s * SFC), sfb = sfa + 4 * G;
+          if (G > 0) {
+            const uint32_t ss = tc::su32(sf_smem + (size_t)s * kSfStage);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              tc::cp_sf(sfa + 4 * g, tc::sdesc_rows16(ss + 512 * g));
+              tc::cp_sf(sfb + 4 * g, tc::sdesc_rows16(ss + 512 * (G + g)));
+            }
+          }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = tc::sdesc_sw128(a_s + 32 * kk), bd = tc::sdesc_sw128(b_s + 32 * kk);
@@ -385,71 +571,6 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       tc::mma_commit(&fin);
       if (!tc::mbar_wait(&fin, 0)) atomicExch(p.err, 1);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ block scales -> TMEM
-    if (G == 0) {
-      // bf16 operands carry no scales
-    } else {
-    const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's lane quarter
-    uint32_t it = 0;
-    for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-      const Tile tile = p.tiles[t / NT];
-      const int n0 = (int)(t % NT) * NCOL;
-      const uint8_t* wb = p.slots + (size_t)tile.slot * p.ebytes;
-      const uint8_t* pa[4];
-      const uint8_t* pb[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        pa[j] = p.a_scales + (size_t)(tile.row_start + 32 * j + lane) * srow;
-        if (PH == 1) pb[j] = wb + p.w_scales_off[j < 2 ? 0 : 1] + (size_t)(n0 + 32 * (j & 1) + lane) * srow;
-        else pb[j] = wb + p.w_scales_off[0] + (size_t)(n0 + 32 * j + lane) * srow;
-      }
-      for (int kt = 0; kt < nkt; ++kt, ++it) {
-        const int s = it % kWsStages;
-        const uint32_t k = it / kWsStages;
-        if (s_abort) continue;
-        // the stage's scale loads go out before the wait for its TMEM slot,
-        // so their latency overlaps the MMAs still reading the slot
-        uint32_t wa[4][G > 0 ? G : 1], wv[4][G > 0 ? G : 1];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (AF == MOE_MXFP8) {
-            wa[j][0] = *reinterpret_cast<const uint32_t*>(pa[j] + kt * SB);
-            wv[j][0] = *reinterpret_cast<const uint32_t*>(pb[j] + kt * SB);
-          } else if (FMT == MOE_MXFP4) {
-            const uint2 va = *reinterpret_cast<const uint2*>(pa[j] + kt * SB);
-            const uint2 vb = *reinterpret_cast<const uint2*>(pb[j] + kt * SB);
-            wa[j][0] = va.x; wa[j][G - 1] = va.y;
-            wv[j][0] = vb.x; wv[j][G - 1] = vb.y;
-          } else {
-            const uint4 va = *reinterpret_cast<const uint4*>(pa[j] + kt * SB);
-            const uint4 vb = *reinterpret_cast<const uint4*>(pb[j] + kt * SB);
-            const uint32_t ta4[4] = {va.x, va.y, va.z, va.w}, tb4[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-            for (int g = 0; g < G; ++g) { wa[j][g] = ta4[g & 3]; wv[j][g] = tb4[g & 3]; }
-          }
-        }
-        if (kt + 4 < nkt) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            prefetch_l1(pa[j] + (kt + 4) * SB);
-            prefetch_l1(pb[j] + (kt + 4) * SB);
-          }
-        }
-        if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) continue;
-        const uint32_t col = tb + lq + kSfBase + (uint32_t)(s * SFC);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          tc::tmem_st4(col + 4 * g, wa[0][g], wa[1][g], wa[2][g], wa[3][g]);
-          tc::tmem_st4(col + 4 * G + 4 * g, wv[0][g], wv[1][g], wv[2][g], wv[3][g]);
-        }
-        tc::tmem_st_wait();
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) ws_arrive(&sfull[s]);
-      }
-    }
-    }
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
@@ -474,11 +595,16 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       tc::fence_before();
       __syncwarp();
       if (lane == 0) ws_arrive(&acce[b]);   // the accumulator is free for the tile after next
-      if (PH == 1) {
+      // Rows past the expert's last (the tail of its last tile) carry another
+      // expert's codes under stale scale bytes, which may decode to NaN: they
+      // are never stored, so phase 1 skips their SiLU and quantisation (whose
+      // special-value paths would cost more than the live rows)
+      if (PH == 1 && live) {
         // columns 0..63: W_g rows n0.., 64..127: W_u rows n0..
         const float sg = FMT == MOE_NVFP4 ? ts[0] * p.act_scale : 1.0f;
         const float su = FMT == MOE_NVFP4 ? ts[1] * p.act_scale : 1.0f;
         const int f = p.rows_out;
+        const int ngh = sf_groups(AF, f);   // scale groups per row of h
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const uint32_t* gv = c == 0 ? v0 : v1;
@@ -493,7 +619,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             const int col = n0 + 32 * c;
             if (AF == MOE_MXFP8) {
               uint32_t w8[8];
-              p.h_scales[(size_t)r * (f / 32) + col / 32] = (uint8_t)quant_mx8_32(hv, w8);
+              const int q = col / 32;
+              p.h_scales[sf_off(tile.pb, ngh, q >> 2, rl, q & 3)] = (uint8_t)quant_mx8_32(hv, w8);
               uint4* dst = reinterpret_cast<uint4*>(p.h_codes + (size_t)r * f + col);
               dst[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
               dst[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
@@ -512,11 +639,13 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             const int col = n0 + 32 * c;
             uint32_t words[4];
             if (FMT == MOE_MXFP4) {
-              p.h_scales[(size_t)r * (f / 32) + col / 32] = (uint8_t)quant_mx32(hv, words);
+              const int q = col / 32;
+              p.h_scales[sf_off(tile.pb, ngh, q >> 2, rl, q & 3)] = (uint8_t)quant_mx32(hv, words);
             } else {
               uint32_t w2[2];
-              p.h_scales[(size_t)r * (f / 16) + col / 16] = (uint8_t)quant_nv16(hv, p.act_scale_h, words);
-              p.h_scales[(size_t)r * (f / 16) + col / 16 + 1] = (uint8_t)quant_nv16(hv + 16, p.act_scale_h, w2);
+              const int q = col / 16;   // K-blocks q and q + 1 (q even)
+              p.h_scales[sf_off(tile.pb, ngh, q >> 2, rl, q & 3)] = (uint8_t)quant_nv16(hv, p.act_scale_h, words);
+              p.h_scales[sf_off(tile.pb, ngh, q >> 2, rl, (q & 3) + 1)] = (uint8_t)quant_nv16(hv + 16, p.act_scale_h, w2);
               words[2] = w2[0];
               words[3] = w2[1];
             }
@@ -524,7 +653,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
                 make_uint4(words[0], words[1], words[2], words[3]);
           }
         }
-      } else {
+      } else if (PH == 2) {
         // lane = row in TMEM; O is written as f16 scaled by 2^-s, s per row
         // and 128-column block (max |O| * 2^-s in [2^14, 2^15), so nothing
         // overflows and the rounding is relative to the block's largest
@@ -547,8 +676,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         }
         const float sc = sd * __int_as_float((127 - se) << 23);   // sd * 2^-se
         if (live) p.O_exp[(size_t)r * (p.O_ld / 128) + n0 / 128] = (int8_t)se;
-        __half* ost = reinterpret_cast<__half*>(smem + (size_t)kWsStages * 2 * kOpBytes) +
-                      (size_t)(warp - 6) * 32 * kOStrideB;
+        __half* ost = reinterpret_cast<__half*>(sf_smem + (size_t)kWsStages * kSfStage) +
+                      (size_t)(warp - kEpiWarp0) * 32 * kOStrideB;
         uint4* myrow = reinterpret_cast<uint4*>(ost + lane * kOStrideB);
         const int row0 = tile.row_start + 32 * (warp & 3);
 #pragma unroll
@@ -688,12 +817,17 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
 void prefill_plan_destroy(PrefillPlan* pl) { delete pl; }
 bool prefill_plan_ready(const PrefillPlan* pl) { return pl && pl->ready; }
 
-cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* row_of, int N, float gx,
+cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* idx, const int* row_of,
+                                const int* counts, const int* offsets, int N, float gx, int* pbase,
                                 uint8_t* codes, uint8_t* scales, cudaStream_t st) {
   const size_t total = (size_t)N * (g.d / 32);
   if (total == 0) return cudaSuccess;
-  gather_quant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(x, row_of, N, g.k, g.d, g.afmt, gx,
-                                                                      g.has_shared, codes, scales);
+  pad_base_kernel<<<1, 1024, 0, st>>>(counts, g.E, N, g.has_shared, pbase);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gather_quant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(x, idx, row_of, offsets, pbase, N, g.k,
+                                                                      g.E, g.d, g.afmt, gx, g.has_shared,
+                                                                      codes, scales);
   return cudaGetLastError();
 }
 
@@ -702,30 +836,60 @@ int prefill_max_tiles(const Geo& g, int N) {
   return (int)((rows + kTileRows - 1) / kTileRows + g.E + 1);
 }
 
+// Block scales of the activations (x or h, K = d or f) by padded 128-row block.
+size_t prefill_act_scale_bytes(const Geo& g, int N, int K) {
+  return std::max<size_t>(16, (size_t)prefill_max_tiles(g, N) * kTileRows * fmt_scale_row(g.afmt, K));
+}
+// The interleaved weight scales of one launch: up to E + 1 entries.
+size_t prefill_wscale_bytes(const Geo& g) {
+  return std::max<size_t>(16, (size_t)(g.E + 1) * 3 * fmt_scale_row(g.afmt, g.d) * (size_t)g.f);
+}
+
+cudaError_t launch_untile_hscales(const Geo& g, const uint8_t* tiled, const int* offsets, const int* pbase, int N,
+                                  uint8_t* out, cudaStream_t st) {
+  const int blk = fmt_block(g.afmt);
+  const int rows = N * g.k + (g.has_shared ? N : 0);
+  const size_t total = (size_t)rows * (blk ? g.f / blk : 0);
+  if (total == 0) return cudaSuccess;
+  untile_scales_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(tiled, offsets, pbase, g.E, N * g.k, rows,
+                                                                       g.f, blk, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const StepRecord* rec,
-                                 const int* offsets, int N, int mode, int with_shared,
+                                 const int* offsets, const int* pbase, int N, int mode, int with_shared,
                                  void* tiles, int* n_tiles, const uint8_t* slots,
-                                 const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales,
+                                 const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales, uint8_t* wsf,
                                  float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
                                  const cudaEvent_t* ev) {
+  const int max_tiles = prefill_max_tiles(g, N);
   Tile* tl = static_cast<Tile*>(tiles);
-  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, g.E, g.S, g.X, g.shb, N, g.k, mode, with_shared, tl,
-                                         n_tiles);
+  int* ents = reinterpret_cast<int*>(tl + max_tiles);
+  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, pbase, g.E, g.S, g.X, g.shb, N, g.k, mode, with_shared, tl,
+                                         ents, n_tiles);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int max_tiles = prefill_max_tiles(g, N);
+  const int blk = fmt_block(g.afmt);   // scale block of both operands (W4A8: 32 on either side)
+  const size_t ent_bytes = blk ? 3 * (size_t)g.d * g.f / blk : 0;
+  if (blk) {
+    const size_t items = (size_t)(g.f / 64) * (g.d / blk / 4) * 32 + (size_t)(g.d / kTileRows) * (g.f / blk / 4) * 32;
+    const dim3 grid((unsigned)((items + 255) / 256), (unsigned)(g.E + 1));
+    interleave_wscales_kernel<<<grid, 256, 0, st>>>(slots, g.ebytes, g.off_scales[0], g.off_scales[1],
+                                                     g.off_scales[2], ents, n_tiles, g.d, g.f, blk, wsf);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   {
-    const int s1 = (int)ws_smem<1>(), s2 = (int)ws_smem<2>();
-    e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 1>, s1);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 1>, s1);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 1>, s1);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_BF16, 1>, s1);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<kW4A8, 1>, s1);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<kW4A8, 2>, s2);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 2>, s2);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 2>, s2);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 2>, s2);
-    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_BF16, 2>, s2);
+    e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 1>, (int)ws_smem<MOE_MXFP4, 1>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 1>, (int)ws_smem<MOE_NVFP4, 1>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 1>, (int)ws_smem<MOE_MXFP8, 1>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_BF16, 1>, (int)ws_smem<MOE_BF16, 1>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<kW4A8, 1>, (int)ws_smem<kW4A8, 1>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<kW4A8, 2>, (int)ws_smem<kW4A8, 2>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP4, 2>, (int)ws_smem<MOE_MXFP4, 2>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_NVFP4, 2>, (int)ws_smem<MOE_NVFP4, 2>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_MXFP8, 2>, (int)ws_smem<MOE_MXFP8, 2>());
+    if (e == cudaSuccess) e = ensure_smem_limit((const void*)gemm_ws_kernel<MOE_BF16, 2>, (int)ws_smem<MOE_BF16, 2>());
     if (e != cudaSuccess) return e;
   }
   GemmArgs p{};
@@ -735,8 +899,10 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.ebytes = g.ebytes;
   p.fmt = g.fmt;
   p.err = err;
+  p.ent_bytes = ent_bytes;
   // phase 1
   p.a_scales = xq_scales;
+  p.w_scales = wsf;
   p.w_scales_off[0] = g.off_scales[0];
   p.w_scales_off[1] = g.off_scales[1];
   p.w_scales_off[2] = g.off_tscale;
@@ -749,20 +915,21 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   const int grid1 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.f / 64));
   if (ev) cudaEventRecord(ev[0], st);
   if (g.afmt != g.fmt)
-    gemm_ws_kernel<kW4A8, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<kW4A8, 1><<<grid1, kWsThreads, ws_smem<kW4A8, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   else if (g.fmt == MOE_MXFP4)
-    gemm_ws_kernel<MOE_MXFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_MXFP4, 1><<<grid1, kWsThreads, ws_smem<MOE_MXFP4, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   else if (g.fmt == MOE_NVFP4)
-    gemm_ws_kernel<MOE_NVFP4, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_NVFP4, 1><<<grid1, kWsThreads, ws_smem<MOE_NVFP4, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   else if (g.fmt == MOE_MXFP8)
-    gemm_ws_kernel<MOE_MXFP8, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_MXFP8, 1><<<grid1, kWsThreads, ws_smem<MOE_MXFP8, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   else
-    gemm_ws_kernel<MOE_BF16, 1><<<grid1, kWsThreads, ws_smem<1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_BF16, 1><<<grid1, kWsThreads, ws_smem<MOE_BF16, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[1], st);
   if (e != cudaSuccess) return e;
   // phase 2
   p.a_scales = hq_scales;
+  p.w_scales = wsf + (blk ? 2 * (size_t)g.d * g.f / blk : 0);
   p.w_scales_off[0] = g.off_scales[2];
   p.w_scales_off[2] = g.off_tscale;
   p.K = g.f;
@@ -774,20 +941,22 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   const int grid2 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.d / kTileRows));
   if (ev) cudaEventRecord(ev[2], st);
   if (g.afmt != g.fmt)
-    gemm_ws_kernel<kW4A8, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<kW4A8, 2><<<grid2, kWsThreads, ws_smem<kW4A8, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else if (g.fmt == MOE_MXFP4)
-    gemm_ws_kernel<MOE_MXFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_MXFP4, 2><<<grid2, kWsThreads, ws_smem<MOE_MXFP4, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else if (g.fmt == MOE_NVFP4)
-    gemm_ws_kernel<MOE_NVFP4, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_NVFP4, 2><<<grid2, kWsThreads, ws_smem<MOE_NVFP4, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else if (g.fmt == MOE_MXFP8)
-    gemm_ws_kernel<MOE_MXFP8, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_MXFP8, 2><<<grid2, kWsThreads, ws_smem<MOE_MXFP8, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else
-    gemm_ws_kernel<MOE_BF16, 2><<<grid2, kWsThreads, ws_smem<2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_BF16, 2><<<grid2, kWsThreads, ws_smem<MOE_BF16, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[3], st);
   return e;
 }
 
-size_t prefill_tile_bytes(const Geo& g, int N) { return (size_t)prefill_max_tiles(g, N) * sizeof(Tile); }
+size_t prefill_tile_bytes(const Geo& g, int N) {
+  return (size_t)prefill_max_tiles(g, N) * sizeof(Tile) + (size_t)(g.E + 2) * sizeof(int);   // tiles, then entries
+}
 
 }  // namespace moe

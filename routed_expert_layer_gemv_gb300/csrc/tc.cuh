@@ -89,6 +89,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
                :: "r"(su32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(su32(bar)) : "memory");
 }
 
+// Non-tensor bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing on `bar` like a tensor load.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(su32(dst)), "l"(src), "r"(bytes), "r"(su32(bar)) : "memory");
+}
+
 // whole warp
 // Fetch a tensor map (a __grid_constant__ parameter) into the descriptor cache.
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -117,6 +124,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   d |= (uint64_t)1 << 46;                 // descriptor version
   d |= (uint64_t)2 << 61;                 // 128B swizzle
   return d;
+}
+
+// Descriptor of a plain (unswizzled) shared-memory matrix of 16-byte rows
+// stored back to back: core matrices of 8 rows x 16 bytes, 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(128 >> 4) << 16;        // leading offset (one core matrix wide: unused)
+  d |= (uint64_t)(128 >> 4) << 32;        // stride offset: the next 8 rows
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  return d;                               // no swizzle
+}
+
+// Block scales into TMEM: 32 rows of 16 bytes from shared memory (sdesc_rows16)
+// to columns taddr .. taddr + 3, row i into lane i of every lane quarter
+// (lanes i, 32 + i, 64 + i, 96 + i).  Asynchronous; ordered before the MMAs
+// the same thread issues after it, and tracked by its later commits.
+__device__ __forceinline__ void cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc));
 }
 
 // Instruction descriptor of a block-scaled FP4 MMA (M = 128, dense, K-major).
