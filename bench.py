@@ -181,6 +181,22 @@ def traffic_ratio(kernel, workload):
     return None
 
 
+def gemm_traffic(workload):
+    """DRAM bytes of one chunk's two GEMM launches (phase 1 + phase 2) from
+    the ncu capture listed in profiles/traffic.txt, or None without one."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    got = {}
+    try:
+        for line in open(path):
+            f = line.split()
+            if len(f) >= 5 and not line.startswith("#") and f[0] in ("gemm_ws_phase1", "gemm_ws_phase2") \
+                    and f[1] == workload + "_n8192":
+                got[f[0]] = float(f[2])
+    except OSError:
+        pass
+    return sum(got.values()) if len(got) == 2 else None
+
+
 class Ctx:
     """What every run needs: torch, the binding, the generator, a flush
     buffer, the stream, and one packed host pool per workload."""
@@ -338,6 +354,9 @@ def prefill_summary(r, fp4_peak):
         "gemm_tflops": {"gateup": t1, "down": t2, "both": tboth},
         "frac_fp4_peak": (tboth / fp4_peak) if tboth else None,
         "kernel_ms_per_step": {k: v[0] / r["steps"] for k, v in p.items() if v[1]},
+        # DRAM bytes of the two GEMM launches per chunk (ncu capture of this workload)
+        "gemm_dram_bytes_ncu": gemm_traffic("prefill35b") if r["workload"].startswith("prefill_35b") and
+        r["workload"].endswith("_mxfp4") else None,
     }
 
 
@@ -681,7 +700,8 @@ def main():
                            "detail": sm},
                 "roofline": {"bound": "tensor", "kernel": "prefill grouped GEMM (gate/up + down)",
                              "achieved": tboth, "peak": fp4, "unit": "TFLOP/s",
-                             "frac": (tboth / fp4) if tboth else None, "traffic": None, "peak_kind": fp4_kind},
+                             "frac": (tboth / fp4) if tboth else None, "traffic": gemm_traffic(args.workload),
+                             "peak_kind": fp4_kind},
                 "gpu_launches": r["launches"], "clocks": clk}
         if rank == 0:
             print(json.dumps(line))
