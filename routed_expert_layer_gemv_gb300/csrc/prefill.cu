@@ -285,9 +285,10 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
 }
 
 // Weight block scales of the launch's experts (entry i: pool buffer ents[i])
-// in the tcgen05.cp layout, entry-major: phase 1 first (blocks q of the 64
-// gate rows 64 q .. over the same 64 up rows, K = d), then phase 2 (blocks of
-// 128 down rows, K = f).  Thread = one 16-byte row of a 512-byte group.
+// in the tcgen05.cp layout, entry-major: phase 1 first (per block q of 128
+// gate rows and the same 128 up rows, per group g: the gate block's 512
+// bytes, then the up block's, K = d), then phase 2 (blocks of 128 down rows,
+// K = f).  Thread = one 16-byte row of a 512-byte group.
 __global__ void interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size_t off_g,
                                           size_t off_u, size_t off_d, const int* __restrict__ ents,
                                           const int* __restrict__ n_tiles, int d, int f, int blk,
@@ -297,22 +298,23 @@ __global__ void interleave_wscales_kernel(const uint8_t* __restrict__ slots, siz
   const int slot = ents[ent];
   if (slot < 0) return;
   const int ng1 = d / blk / 4, ng2 = f / blk / 4;
-  const size_t n1 = (size_t)(f / 64) * ng1 * 32, n2 = (size_t)(d / kTileRows) * ng2 * 32;
+  const size_t n1 = (size_t)(f / kTileRows) * ng1 * 2 * 32, n2 = (size_t)(d / kTileRows) * ng2 * 32;
   const size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= n1 + n2) return;
   const uint8_t* w = slots + (size_t)slot * ebytes;
   uint8_t* out = wsf + (size_t)ent * (3 * (size_t)d * f / blk);
   uint32_t word[4];
   if (v < n1) {
-    const int i = (int)(v & 31), g = (int)((v >> 5) % ng1), q = (int)((v >> 5) / ng1);
+    const int i = (int)(v & 31), h = (int)((v >> 5) & 1);
+    const int g = (int)((v >> 6) % ng1), q = (int)((v >> 6) / ng1);
     const int srow = d / blk;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int rho = 32 * j + i;   // block row: gate rows first, then up
-      const uint8_t* src = w + (rho < 64 ? off_g : off_u) + (size_t)(64 * q + (rho & 63)) * srow + 4 * g;
+      const uint8_t* src = w + (h ? off_u : off_g) + (size_t)(kTileRows * q + 32 * j + i) * srow + 4 * g;
       word[j] = *reinterpret_cast<const uint32_t*>(src);
     }
-    *reinterpret_cast<uint4*>(out + sf_off(q, ng1, g, i, 0)) = make_uint4(word[0], word[1], word[2], word[3]);
+    *reinterpret_cast<uint4*>(out + (((size_t)q * ng1 + g) * 2 + h) * 512 + 16 * i) =
+        make_uint4(word[0], word[1], word[2], word[3]);
   } else {
     const size_t u = v - n1;
     const int i = (int)(u & 31), g = (int)((u >> 5) % ng2), rb = (int)((u >> 5) / ng2);
@@ -379,32 +381,41 @@ struct GemmArgs {
 };
 
 // ---------------------------------------------------------------- persistent warp-specialised GEMM
-// One CTA per SM walks the launch's (M tile, N tile) pairs.  Six warps, each
-// with one job, meeting only at mbarriers:
-//   warp 0     TMA: A (128 token rows x one 128-byte K stage) and B (128
-//              weight rows, phase 1: 64 gate rows over the same 64 up rows)
-//              per stage, and with them the stage's block scales of A and B
-//              (G groups of 512 bytes each, already in the layout
-//              tcgen05.cp reads: activations quantised into it, weight
-//              scales interleaved per launch), all on one barrier;
+// One CTA per SM walks the launch's (M tile, N tile) pairs.  Warps with one
+// job each, meeting only at mbarriers:
+//   warp 0     TMA: A (128 token rows x one 128-byte K stage) and B (phase 1:
+//              128 gate rows over the same 128 up rows; phase 2: 128 down
+//              rows) per stage, and with them the stage's block scales of A
+//              and B (512-byte groups already in the layout tcgen05.cp reads:
+//              activations quantised into it, weight scales interleaved per
+//              launch), all on one barrier;
 //   warp 1     one thread copies the stage's scales into its TMEM ring slot
 //              (tcgen05.cp, every lane quarter gets all 128 rows) and issues
-//              the block-scaled MMAs (M = 128, N = 128, four per stage) into
-//              one of two TMEM accumulators; copies and MMAs run in issue
-//              order, so no other warp touches the scales;
-//   warps 2-5  epilogue, one per lane quarter (32 rows): drain an accumulator
-//              into registers, release it, then SiLU * mul + quantisation
-//              of h (phase 1) or the scaled f16 O rows (phase 2), while the
-//              MMAs of the next tile run into the other accumulator.
-constexpr int kWsThreads = 192;
+//              four block-scaled MMAs per stage (M = 128, N = 256 in phase 1
+//              into its one accumulator, N = 128 in phase 2 into one of two);
+//              copies and MMAs run in issue order, so no other warp touches
+//              the scales;
+//   warps 2-9  epilogue (phase 2: warps 2-5), by lane quarter (32 rows; in
+//              phase 1 two warps per quarter, one per half of the columns):
+//              drain the accumulator into registers, release it, then SiLU *
+//              mul + quantisation of h (phase 1) or the scaled f16 O rows
+//              (phase 2), while the MMAs of the next tile proceed.
 constexpr int kEpiWarp0 = 2;
-constexpr int kSfBase = 256;            // TMEM columns 0..255: two 128-column accumulators
+constexpr int kSfBase = 256;            // TMEM columns 0..255: the accumulator(s); then the scale ring
 
-// Ring stages: phase 1 takes 6; phase 2 takes 5 and keeps room to stage O
+// Ring stages: phase 1 takes 4 (48 KB of operands each); phase 2 takes 5 and keeps room to stage O
 // for its epilogue: per epilogue warp 32 rows x 64 fp32 (half a tile at a
 // time), rows padded by 4 floats so the row writes and reads spread over the
 // banks.
-template <int PH> constexpr int ws_stages() { return PH == 1 ? 6 : 5; }
+template <int PH> constexpr int ws_stages() { return PH == 1 ? 4 : 5; }
+// Phase 1 multiplies each A tile by 256 weight rows (128 gate over the same
+// 128 up rows) in one N = 256 MMA, twice the MMA work per staged byte of a
+// 128-row B tile; its single accumulator takes 256 TMEM columns (two would
+// leave none for the scales; the epilogue hides behind the operand ring
+// either way, measured), drained by eight epilogue warps.
+template <int PH> constexpr int ws_nb() { return PH == 1 ? 256 : 128; }        // B rows = MMA N
+template <int PH> constexpr int ws_epi_warps() { return PH == 1 ? 8 : 4; }
+template <int PH> constexpr int ws_threads() { return 32 * (2 + ws_epi_warps<PH>()); }
 constexpr int kOStrideB = 72;   // f16 elements per staged O row (144 bytes: conflict-free 16-byte stores)
 constexpr size_t kOStage = 4 * 32 * kOStrideB * 2;
 
@@ -418,7 +429,9 @@ __host__ __device__ constexpr int stage_groups(int FMT) {
 // stage's scales (A groups, then B groups), then (phase 2) the O staging.
 template <int FMT, int PH>
 size_t ws_smem() {
-  return 1024 + (size_t)ws_stages<PH>() * (2 * kOpBytes + 2 * 512 * stage_groups(FMT)) + (PH == 2 ? kOStage : 0);
+  constexpr int BA = ws_nb<PH>() / 128;   // 128-row blocks of B
+  return 1024 + (size_t)ws_stages<PH>() * ((1 + BA) * kOpBytes + (1 + BA) * 512 * stage_groups(FMT)) +
+         (PH == 2 ? kOStage : 0);
 }
 
 __device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
@@ -434,7 +447,7 @@ __device__ __forceinline__ void ws_arrive(uint64_t* bar) {
 }
 
 template <int FMT, int PH>
-__global__ void __launch_bounds__(kWsThreads, 1)
+__global__ void __launch_bounds__(ws_threads<PH>(), 1)
 gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
                const __grid_constant__ CUtensorMap tb1, GemmArgs p) {
   // K elements per 128-byte stage row and 4-byte scale groups per row per stage:
@@ -442,14 +455,19 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   constexpr int AF = act_op_fmt(FMT);
   constexpr int KST = 1024 / fmt_code_bits(AF);
   constexpr int G = stage_groups(FMT);
-  constexpr uint32_t kSfStage = 2 * 512 * G;      // scale bytes of a stage in shared memory (A, then B)
-  constexpr int SFC = 2 * 4 * (G > 0 ? G : 1);    // TMEM columns of one scale slot (A, then B)
-  constexpr int NCOL = PH == 1 ? 64 : 128;        // output columns of one tile
+  constexpr int NB = ws_nb<PH>(), BA = NB / 128;  // B rows (MMA N), their 128-row blocks
+  constexpr int EW = ws_epi_warps<PH>();
+  constexpr int NACC = PH == 1 ? 1 : 2;          // accumulators (NB TMEM columns each)
+  constexpr uint32_t kStageOp = (1 + BA) * kOpBytes;            // A, then B, of a stage
+  constexpr uint32_t kSfStage = (1 + BA) * 512 * G;             // its scales: A groups, then B (group, block)
+  constexpr int SFC = 4 * (1 + BA) * (G > 0 ? G : 1);           // TMEM columns of one scale slot
+  constexpr int NCOL = 128;                       // output columns of one tile (phase 1: h columns)
   constexpr int kWsStages = ws_stages<PH>();
+  static_assert(kSfBase + kWsStages * SFC <= 512, "TMEM columns");
   // bytes the B loads of a stage count on its barrier: the 16 x U4 loads of
-  // W4A8 count the packed bytes they read (8 KB of codes for the 16 KB they
+  // W4A8 count the packed bytes they read (8 KB of codes for each 16 KB they
   // fill with their padding)
-  constexpr uint32_t kBTxBytes = FMT == kW4A8 ? kOpBytes / 2 : kOpBytes;
+  constexpr uint32_t kBTxBytes = BA * (FMT == kW4A8 ? kOpBytes / 2 : kOpBytes);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kWsStages], empty[kWsStages], accf[2], acce[2], fin;
@@ -464,7 +482,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accf[b], 1);
-      tc::mbar_init(&acce[b], 4);
+      tc::mbar_init(&acce[b], EW);
     }
     tc::mbar_init(&fin, 1);
     s_abort = 0;
@@ -479,7 +497,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const long long T = (long long)n_m * NT;
   const int nkt = p.K / KST;
   const int ng = G > 0 ? nkt * G : 0;          // scale groups per row (A and B alike)
-  uint8_t* sf_smem = smem + (size_t)kWsStages * 2 * kOpBytes;
+  uint8_t* sf_smem = smem + (size_t)kWsStages * kStageOp;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -493,19 +511,20 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
           const int s = it % kWsStages;
           const uint32_t k = it / kWsStages;
           if (k > 0 && !ws_wait(&empty[s], (k - 1) & 1, &s_abort, p.err)) { stop = true; break; }
-          uint8_t* st = smem + (size_t)s * 2 * kOpBytes;
+          uint8_t* st = smem + (size_t)s * kStageOp;
           tc::mbar_expect_tx(&full[s], kOpBytes + kBTxBytes + kSfStage);
           if (G > 0) {
             uint8_t* ss = sf_smem + (size_t)s * kSfStage;
             tc::bulk_load(ss, p.a_scales + ((size_t)tile.pb * ng + (size_t)kt * G) * 512, 512 * G, &full[s]);
             tc::bulk_load(ss + 512 * G,
-                          p.w_scales + (size_t)tile.ent * p.ent_bytes + ((size_t)(n0 / NCOL) * ng + (size_t)kt * G) * 512,
-                          512 * G, &full[s]);
+                          p.w_scales + (size_t)tile.ent * p.ent_bytes +
+                              ((size_t)(n0 / 128) * ng + (size_t)kt * G) * 512 * BA,
+                          512 * G * BA, &full[s]);
           }
           tc::tma_load_2d(st, &ta, &full[s], kt * kKTileBytes, tile.row_start);
-          if (PH == 1) {
+          if (PH == 1) {   // 128 gate rows over the same 128 up rows
             tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
-            tc::tma_load_3d(st + kOpBytes + kOpBytes / 2, &tb1, &full[s], kt * kKTileBytes, n0, tile.slot);
+            tc::tma_load_3d(st + 2 * kOpBytes, &tb1, &full[s], kt * kKTileBytes, n0, tile.slot);
           } else {
             tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
           }
@@ -522,8 +541,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       uint32_t it = 0, nt_done = 0;
       bool stop = false;
       for (long long t = blockIdx.x; t < T && !stop; t += gridDim.x, ++nt_done) {
-        const int b = nt_done & 1;
-        const uint32_t u = nt_done >> 1;
+        const int b = NACC == 2 ? (int)(nt_done & 1) : 0;
+        const uint32_t u = NACC == 2 ? nt_done >> 1 : nt_done;
         if (u > 0 && !ws_wait(&acce[b], (u - 1) & 1, &s_abort, p.err)) { stop = true; break; }
         tc::fence_after();
         for (int kt = 0; kt < nkt; ++kt, ++it) {
@@ -534,31 +553,36 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             break;
           }
           tc::fence_after();
-          const uint32_t a_s = tc::su32(smem + (size_t)s * 2 * kOpBytes), b_s = a_s + kOpBytes;
+          const uint32_t a_s = tc::su32(smem + (size_t)s * kStageOp), b_s = a_s + kOpBytes;
+          // scale slot: A groups (4 columns each), then B groups of BA
+          // 128-row blocks (4 columns per block, the blocks of a group side by side)
           const uint32_t sfa = tb + kSfBase + (uint32_t)(s * SFC), sfb = sfa + 4 * G;
           if (G > 0) {
             const uint32_t ss = tc::su32(sf_smem + (size_t)s * kSfStage);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
               tc::cp_sf(sfa + 4 * g, tc::sdesc_rows16(ss + 512 * g));
-              tc::cp_sf(sfb + 4 * g, tc::sdesc_rows16(ss + 512 * (G + g)));
+#pragma unroll
+              for (int h = 0; h < BA; ++h)
+                tc::cp_sf(sfb + 4 * (BA * g + h), tc::sdesc_rows16(ss + 512 * (G + BA * g + h)));
             }
           }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = tc::sdesc_sw128(a_s + 32 * kk), bd = tc::sdesc_sw128(b_s + 32 * kk);
             const bool acc = kt > 0 || kk > 0;
+            const uint32_t dacc = tb + NB * b;
             if (FMT == MOE_MXFP4) {
               const uint32_t id = 2 * (kk & 1), g = kk >> 1;
-              tc::mma_mxf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, true, id, id), sfa + 4 * g, sfb + 4 * g, acc);
+              tc::mma_mxf4(dacc, ad, bd, tc::idesc_fp4(NB, true, id, id), sfa + 4 * g, sfb + 4 * BA * g, acc);
             } else if (FMT == MOE_NVFP4) {
-              tc::mma_nvf4(tb + 128 * b, ad, bd, tc::idesc_fp4(128, false, 0, 0), sfa + 4 * kk, sfb + 4 * kk, acc);
+              tc::mma_nvf4(dacc, ad, bd, tc::idesc_fp4(NB, false, 0, 0), sfa + 4 * kk, sfb + 4 * BA * kk, acc);
             } else if (AF == MOE_MXFP8) {
               // one E8M0 scale per 32-K MMA: byte kk of the stage's group;
               // B E4M3 (W8A8) or E2M1 (W4A8)
-              tc::mma_mxf8(tb + 128 * b, ad, bd, tc::idesc_mxf8(128, kk, kk, FMT == kW4A8), sfa, sfb, acc);
+              tc::mma_mxf8(dacc, ad, bd, tc::idesc_mxf8(NB, kk, kk, FMT == kW4A8), sfa, sfb, acc);
             } else {
-              tc::mma_bf16(tb + 128 * b, ad, bd, tc::idesc_bf16(128), acc);
+              tc::mma_bf16(dacc, ad, bd, tc::idesc_bf16(NB), acc);
             }
           }
           tc::mma_commit(&empty[s]);   // the stage's smem and scale slot are free once these MMAs finish
@@ -573,34 +597,40 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // warp 2 + e: lane quarter warp & 3 (the TMEM lanes a warp may read);
+    // phase 1's eight warps split the 128 h columns in two halves (hh)
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
     const int rl = 32 * (warp & 3) + lane;   // tile row of this thread
+    const int hh = (warp - kEpiWarp0) >> 2;  // 0 (phase 2: always)
     uint32_t nt_done = 0;
     for (long long t = blockIdx.x; t < T; t += gridDim.x, ++nt_done) {
       const Tile tile = p.tiles[t / NT];
       const int n0 = (int)(t % NT) * NCOL;
-      const int b = nt_done & 1;
-      if (!ws_wait(&accf[b], (nt_done >> 1) & 1, &s_abort, p.err)) continue;
+      const int b = NACC == 2 ? (int)(nt_done & 1) : 0;
+      if (!ws_wait(&accf[b], (NACC == 2 ? nt_done >> 1 : nt_done) & 1, &s_abort, p.err)) continue;
       tc::fence_after();
       const int r = tile.row_start + rl;
       const bool live = r < tile.row_end;
       const float* ts = reinterpret_cast<const float*>(p.slots + (size_t)tile.slot * p.ebytes + p.w_scales_off[2]);
       uint32_t v0[32], v1[32], v2[32], v3[32];
-      const uint32_t acc = tb + lq + 128 * b;
-      tc::tmem_ld32(acc, v0);
-      tc::tmem_ld32(acc + 32, v1);
-      tc::tmem_ld32(acc + 64, v2);
-      tc::tmem_ld32(acc + 96, v3);
+      const uint32_t acc = tb + lq + NB * b;
+      // phase 1: gate columns 64 hh .. + 63 (v0, v1) and the same up columns
+      // (128 + 64 hh .., v2, v3); phase 2: the tile's 128 O columns
+      const uint32_t c0 = PH == 1 ? 64 * hh : 0, c2 = PH == 1 ? 128 + 64 * hh : 64;
+      tc::tmem_ld32(acc + c0, v0);
+      tc::tmem_ld32(acc + c0 + 32, v1);
+      tc::tmem_ld32(acc + c2, v2);
+      tc::tmem_ld32(acc + c2 + 32, v3);
       tc::tmem_ld_wait();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ws_arrive(&acce[b]);   // the accumulator is free for the tile after next
+      if (lane == 0) ws_arrive(&acce[b]);   // the accumulator is free for a later tile
       // Rows past the expert's last (the tail of its last tile) carry another
       // expert's codes under stale scale bytes, which may decode to NaN: they
       // are never stored, so phase 1 skips their SiLU and quantisation (whose
       // special-value paths would cost more than the live rows)
       if (PH == 1 && live) {
-        // columns 0..63: W_g rows n0.., 64..127: W_u rows n0..
+        // h columns n0 + 64 hh .. + 63 of this thread's row
         const float sg = FMT == MOE_NVFP4 ? ts[0] * p.act_scale : 1.0f;
         const float su = FMT == MOE_NVFP4 ? ts[1] * p.act_scale : 1.0f;
         const int f = p.rows_out;
@@ -616,7 +646,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             hv[i2] = a / (1.0f + __expf(-a)) * u;
           }
           if (live && (AF == MOE_MXFP8 || AF == MOE_BF16)) {
-            const int col = n0 + 32 * c;
+            const int col = n0 + 64 * hh + 32 * c;
             if (AF == MOE_MXFP8) {
               uint32_t w8[8];
               const int q = col / 32;
@@ -636,7 +666,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
               for (int q = 0; q < 4; ++q) dst[q] = make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2], wb[4 * q + 3]);
             }
           } else if (live) {
-            const int col = n0 + 32 * c;
+            const int col = n0 + 64 * hh + 32 * c;
             uint32_t words[4];
             if (FMT == MOE_MXFP4) {
               const int q = col / 32;
@@ -784,7 +814,7 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
 // ---------------------------------------------------------------- host side
 struct PrefillPlan {
   CUtensorMap xq, hq, wd;
-  CUtensorMap wg64, wu64;   // gate / up in 64-row boxes (stacked into one 128-row B tile)
+  CUtensorMap wg, wu;       // gate / up in 128-row boxes (stacked into one 256-row B tile)
   bool ready;
 };
 
@@ -802,15 +832,15 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
   if (g.afmt != g.fmt) {
     pl->ready = pl->ready && g.fmt == MOE_MXFP4 && g.afmt == MOE_MXFP8 &&
                 make_map_3d_u4(&pl->wd, slots + g.off_codes[2], g.f, g.d, g.nbuf, g.ebytes, kTileRows) &&
-                make_map_3d_u4(&pl->wg64, slots + g.off_codes[0], g.d, g.f, g.nbuf, g.ebytes, 64) &&
-                make_map_3d_u4(&pl->wu64, slots + g.off_codes[1], g.d, g.f, g.nbuf, g.ebytes, 64);
+                make_map_3d_u4(&pl->wg, slots + g.off_codes[0], g.d, g.f, g.nbuf, g.ebytes, kTileRows) &&
+                make_map_3d_u4(&pl->wu, slots + g.off_codes[1], g.d, g.f, g.nbuf, g.ebytes, kTileRows);
     return pl;
   }
   const uint64_t db = (uint64_t)g.d * fmt_code_bits(g.fmt) / 8, fb = (uint64_t)g.f * fmt_code_bits(g.fmt) / 8;
   pl->ready = pl->ready &&
               make_map_3d(&pl->wd, slots + g.off_codes[2], fb, g.d, g.nbuf, g.ebytes) &&
-              make_map_3d(&pl->wg64, slots + g.off_codes[0], db, g.f, g.nbuf, g.ebytes, 64) &&
-              make_map_3d(&pl->wu64, slots + g.off_codes[1], db, g.f, g.nbuf, g.ebytes, 64);
+              make_map_3d(&pl->wg, slots + g.off_codes[0], db, g.f, g.nbuf, g.ebytes) &&
+              make_map_3d(&pl->wu, slots + g.off_codes[1], db, g.f, g.nbuf, g.ebytes);
   return pl;
 }
 
@@ -872,7 +902,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   const int blk = fmt_block(g.afmt);   // scale block of both operands (W4A8: 32 on either side)
   const size_t ent_bytes = blk ? 3 * (size_t)g.d * g.f / blk : 0;
   if (blk) {
-    const size_t items = (size_t)(g.f / 64) * (g.d / blk / 4) * 32 + (size_t)(g.d / kTileRows) * (g.f / blk / 4) * 32;
+    const size_t items = (size_t)(g.f / kTileRows) * (g.d / blk / 4) * 64 + (size_t)(g.d / kTileRows) * (g.f / blk / 4) * 32;
     const dim3 grid((unsigned)((items + 255) / 256), (unsigned)(g.E + 1));
     interleave_wscales_kernel<<<grid, 256, 0, st>>>(slots, g.ebytes, g.off_scales[0], g.off_scales[1],
                                                      g.off_scales[2], ents, n_tiles, g.d, g.f, blk, wsf);
@@ -912,18 +942,18 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.h_codes = hq_codes;
   p.h_scales = hq_scales;
   p.act_scale_h = gh;
-  const int grid1 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.f / 64));
+  const int grid1 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.f / kTileRows));
   if (ev) cudaEventRecord(ev[0], st);
   if (g.afmt != g.fmt)
-    gemm_ws_kernel<kW4A8, 1><<<grid1, kWsThreads, ws_smem<kW4A8, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<kW4A8, 1><<<grid1, ws_threads<1>(), ws_smem<kW4A8, 1>(), st>>>(pl->xq, pl->wg, pl->wu, p);
   else if (g.fmt == MOE_MXFP4)
-    gemm_ws_kernel<MOE_MXFP4, 1><<<grid1, kWsThreads, ws_smem<MOE_MXFP4, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_MXFP4, 1><<<grid1, ws_threads<1>(), ws_smem<MOE_MXFP4, 1>(), st>>>(pl->xq, pl->wg, pl->wu, p);
   else if (g.fmt == MOE_NVFP4)
-    gemm_ws_kernel<MOE_NVFP4, 1><<<grid1, kWsThreads, ws_smem<MOE_NVFP4, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_NVFP4, 1><<<grid1, ws_threads<1>(), ws_smem<MOE_NVFP4, 1>(), st>>>(pl->xq, pl->wg, pl->wu, p);
   else if (g.fmt == MOE_MXFP8)
-    gemm_ws_kernel<MOE_MXFP8, 1><<<grid1, kWsThreads, ws_smem<MOE_MXFP8, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_MXFP8, 1><<<grid1, ws_threads<1>(), ws_smem<MOE_MXFP8, 1>(), st>>>(pl->xq, pl->wg, pl->wu, p);
   else
-    gemm_ws_kernel<MOE_BF16, 1><<<grid1, kWsThreads, ws_smem<MOE_BF16, 1>(), st>>>(pl->xq, pl->wg64, pl->wu64, p);
+    gemm_ws_kernel<MOE_BF16, 1><<<grid1, ws_threads<1>(), ws_smem<MOE_BF16, 1>(), st>>>(pl->xq, pl->wg, pl->wu, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[1], st);
   if (e != cudaSuccess) return e;
@@ -941,15 +971,15 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   const int grid2 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.d / kTileRows));
   if (ev) cudaEventRecord(ev[2], st);
   if (g.afmt != g.fmt)
-    gemm_ws_kernel<kW4A8, 2><<<grid2, kWsThreads, ws_smem<kW4A8, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<kW4A8, 2><<<grid2, ws_threads<2>(), ws_smem<kW4A8, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else if (g.fmt == MOE_MXFP4)
-    gemm_ws_kernel<MOE_MXFP4, 2><<<grid2, kWsThreads, ws_smem<MOE_MXFP4, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_MXFP4, 2><<<grid2, ws_threads<2>(), ws_smem<MOE_MXFP4, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else if (g.fmt == MOE_NVFP4)
-    gemm_ws_kernel<MOE_NVFP4, 2><<<grid2, kWsThreads, ws_smem<MOE_NVFP4, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_NVFP4, 2><<<grid2, ws_threads<2>(), ws_smem<MOE_NVFP4, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else if (g.fmt == MOE_MXFP8)
-    gemm_ws_kernel<MOE_MXFP8, 2><<<grid2, kWsThreads, ws_smem<MOE_MXFP8, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_MXFP8, 2><<<grid2, ws_threads<2>(), ws_smem<MOE_MXFP8, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   else
-    gemm_ws_kernel<MOE_BF16, 2><<<grid2, kWsThreads, ws_smem<MOE_BF16, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
+    gemm_ws_kernel<MOE_BF16, 2><<<grid2, ws_threads<2>(), ws_smem<MOE_BF16, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
   e = cudaGetLastError();
   if (ev) cudaEventRecord(ev[3], st);
   return e;
