@@ -287,8 +287,9 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
 // Weight block scales of the launch's experts (entry i: pool buffer ents[i])
 // in the tcgen05.cp layout, entry-major: phase 1 first (per block q of 128
 // gate rows and the same 128 up rows, per group g: the gate block's 512
-// bytes, then the up block's, K = d), then phase 2 (blocks of 128 down rows,
-// K = f).  Thread = one 16-byte row of a 512-byte group.
+// bytes, then the up block's, K = d), then phase 2 (per block of 256 down
+// rows, per group: its two 128-row halves' 512 bytes, K = f).  Thread = one
+// 16-byte row of a 512-byte group.
 __global__ void interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size_t off_g,
                                           size_t off_u, size_t off_d, const int* __restrict__ ents,
                                           const int* __restrict__ n_tiles, int d, int f, int blk,
@@ -298,7 +299,7 @@ __global__ void interleave_wscales_kernel(const uint8_t* __restrict__ slots, siz
   const int slot = ents[ent];
   if (slot < 0) return;
   const int ng1 = d / blk / 4, ng2 = f / blk / 4;
-  const size_t n1 = (size_t)(f / kTileRows) * ng1 * 2 * 32, n2 = (size_t)(d / kTileRows) * ng2 * 32;
+  const size_t n1 = (size_t)(f / kTileRows) * ng1 * 2 * 32, n2 = (size_t)(d / 256) * ng2 * 2 * 32;
   const size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= n1 + n2) return;
   const uint8_t* w = slots + (size_t)slot * ebytes;
@@ -317,14 +318,15 @@ __global__ void interleave_wscales_kernel(const uint8_t* __restrict__ slots, siz
         make_uint4(word[0], word[1], word[2], word[3]);
   } else {
     const size_t u = v - n1;
-    const int i = (int)(u & 31), g = (int)((u >> 5) % ng2), rb = (int)((u >> 5) / ng2);
+    const int i = (int)(u & 31), h = (int)((u >> 5) & 1);
+    const int g = (int)((u >> 6) % ng2), rb = (int)((u >> 6) / ng2);
     const int srow = f / blk;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint8_t* src = w + off_d + (size_t)(kTileRows * rb + 32 * j + i) * srow + 4 * g;
+      const uint8_t* src = w + off_d + (size_t)(256 * rb + kTileRows * h + 32 * j + i) * srow + 4 * g;
       word[j] = *reinterpret_cast<const uint32_t*>(src);
     }
-    *reinterpret_cast<uint4*>(out + 2 * (size_t)d * f / blk + sf_off(rb, ng2, g, i, 0)) =
+    *reinterpret_cast<uint4*>(out + 2 * (size_t)d * f / blk + (((size_t)rb * ng2 + g) * 2 + h) * 512 + 16 * i) =
         make_uint4(word[0], word[1], word[2], word[3]);
   }
 }
@@ -403,21 +405,22 @@ struct GemmArgs {
 constexpr int kEpiWarp0 = 2;
 constexpr int kSfBase = 256;            // TMEM columns 0..255: the accumulator(s); then the scale ring
 
-// Ring stages: phase 1 takes 4 (48 KB of operands each); phase 2 takes 5 and keeps room to stage O
-// for its epilogue: per epilogue warp 32 rows x 64 fp32 (half a tile at a
-// time), rows padded by 4 floats so the row writes and reads spread over the
-// banks.
-template <int PH> constexpr int ws_stages() { return PH == 1 ? 4 : 5; }
-// Phase 1 multiplies each A tile by 256 weight rows (128 gate over the same
-// 128 up rows) in one N = 256 MMA, twice the MMA work per staged byte of a
-// 128-row B tile; its single accumulator takes 256 TMEM columns (two would
-// leave none for the scales; the epilogue hides behind the operand ring
-// either way, measured), drained by eight epilogue warps.
-template <int PH> constexpr int ws_nb() { return PH == 1 ? 256 : 128; }        // B rows = MMA N
-template <int PH> constexpr int ws_epi_warps() { return PH == 1 ? 8 : 4; }
+// Phase 2 keeps room to stage O for its epilogue: per epilogue warp 32 rows
+// x 32 f16 columns at a time, rows padded by 8 so the row writes and reads
+// spread over the banks.
+// Both phases multiply each A tile by 256 weight rows in one N = 256 MMA
+// (phase 1: 128 gate over the same 128 up rows; phase 2: 256 down rows),
+// twice the MMA work per staged byte of a 128-row B tile; the single
+// accumulator takes 256 TMEM columns (two would leave none for the scales;
+// the epilogue hides behind the operand ring either way, measured), drained
+// by eight epilogue warps.  Ring stages: 4 of 48 KB of operands, 3 for
+// NVFP4's phase 2 (its larger scales and the O staging fill the rest).
+template <int FMT, int PH> constexpr int ws_stages() { return PH == 2 && FMT == MOE_NVFP4 ? 3 : 4; }
+template <int PH> constexpr int ws_nb() { return 256; }        // B rows = MMA N
+template <int PH> constexpr int ws_epi_warps() { return 8; }
 template <int PH> constexpr int ws_threads() { return 32 * (2 + ws_epi_warps<PH>()); }
-constexpr int kOStrideB = 72;   // f16 elements per staged O row (144 bytes: conflict-free 16-byte stores)
-constexpr size_t kOStage = 4 * 32 * kOStrideB * 2;
+constexpr int kOStrideB = 40;   // f16 elements per staged O row piece (32 columns + 8 of padding)
+constexpr size_t kOStage = 8 * 32 * kOStrideB * 2;
 
 // Scale groups of 4 bytes per row per stage: MXFP4 2 (8 blocks of 32 over
 // 256 K), NVFP4 4 (16 blocks of 16), MXFP8 / W4A8 1 (4 blocks of 32 over 128
@@ -430,7 +433,7 @@ __host__ __device__ constexpr int stage_groups(int FMT) {
 template <int FMT, int PH>
 size_t ws_smem() {
   constexpr int BA = ws_nb<PH>() / 128;   // 128-row blocks of B
-  return 1024 + (size_t)ws_stages<PH>() * ((1 + BA) * kOpBytes + (1 + BA) * 512 * stage_groups(FMT)) +
+  return 1024 + (size_t)ws_stages<FMT, PH>() * ((1 + BA) * kOpBytes + (1 + BA) * 512 * stage_groups(FMT)) +
          (PH == 2 ? kOStage : 0);
 }
 
@@ -457,12 +460,12 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   constexpr int G = stage_groups(FMT);
   constexpr int NB = ws_nb<PH>(), BA = NB / 128;  // B rows (MMA N), their 128-row blocks
   constexpr int EW = ws_epi_warps<PH>();
-  constexpr int NACC = PH == 1 ? 1 : 2;          // accumulators (NB TMEM columns each)
+  constexpr int NACC = 1;                         // accumulators (NB TMEM columns each)
   constexpr uint32_t kStageOp = (1 + BA) * kOpBytes;            // A, then B, of a stage
   constexpr uint32_t kSfStage = (1 + BA) * 512 * G;             // its scales: A groups, then B (group, block)
   constexpr int SFC = 4 * (1 + BA) * (G > 0 ? G : 1);           // TMEM columns of one scale slot
-  constexpr int NCOL = 128;                       // output columns of one tile (phase 1: h columns)
-  constexpr int kWsStages = ws_stages<PH>();
+  constexpr int NCOL = PH == 1 ? 128 : 256;       // output columns of one tile (phase 1: h columns)
+  constexpr int kWsStages = ws_stages<FMT, PH>();
   static_assert(kSfBase + kWsStages * SFC <= 512, "TMEM columns");
   // bytes the B loads of a stage count on its barrier: the 16 x U4 loads of
   // W4A8 count the packed bytes they read (8 KB of codes for each 16 KB they
@@ -518,15 +521,16 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             tc::bulk_load(ss, p.a_scales + ((size_t)tile.pb * ng + (size_t)kt * G) * 512, 512 * G, &full[s]);
             tc::bulk_load(ss + 512 * G,
                           p.w_scales + (size_t)tile.ent * p.ent_bytes +
-                              ((size_t)(n0 / 128) * ng + (size_t)kt * G) * 512 * BA,
+                              ((size_t)(n0 / NCOL) * ng + (size_t)kt * G) * 512 * BA,
                           512 * G * BA, &full[s]);
           }
           tc::tma_load_2d(st, &ta, &full[s], kt * kKTileBytes, tile.row_start);
           if (PH == 1) {   // 128 gate rows over the same 128 up rows
             tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
             tc::tma_load_3d(st + 2 * kOpBytes, &tb1, &full[s], kt * kKTileBytes, n0, tile.slot);
-          } else {
+          } else {         // 256 down rows as two 128-row boxes
             tc::tma_load_3d(st + kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0, tile.slot);
+            tc::tma_load_3d(st + 2 * kOpBytes, &tb0, &full[s], kt * kKTileBytes, n0 + 128, tile.slot);
           }
         }
       }
@@ -598,10 +602,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   } else {
     // ------------------------------------------------------------ epilogue
     // warp 2 + e: lane quarter warp & 3 (the TMEM lanes a warp may read);
-    // phase 1's eight warps split the 128 h columns in two halves (hh)
+    // two warps per quarter split the tile's columns in halves (hh)
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
     const int rl = 32 * (warp & 3) + lane;   // tile row of this thread
-    const int hh = (warp - kEpiWarp0) >> 2;  // 0 (phase 2: always)
+    const int hh = (warp - kEpiWarp0) >> 2;
     uint32_t nt_done = 0;
     for (long long t = blockIdx.x; t < T; t += gridDim.x, ++nt_done) {
       const Tile tile = p.tiles[t / NT];
@@ -615,8 +619,8 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       uint32_t v0[32], v1[32], v2[32], v3[32];
       const uint32_t acc = tb + lq + NB * b;
       // phase 1: gate columns 64 hh .. + 63 (v0, v1) and the same up columns
-      // (128 + 64 hh .., v2, v3); phase 2: the tile's 128 O columns
-      const uint32_t c0 = PH == 1 ? 64 * hh : 0, c2 = PH == 1 ? 128 + 64 * hh : 64;
+      // (128 + 64 hh .., v2, v3); phase 2: O columns 128 hh .. + 127 (v0 .. v3)
+      const uint32_t c0 = PH == 1 ? 64 * hh : 128 * hh, c2 = PH == 1 ? 128 + 64 * hh : 128 * hh + 64;
       tc::tmem_ld32(acc + c0, v0);
       tc::tmem_ld32(acc + c0 + 32, v1);
       tc::tmem_ld32(acc + c2, v2);
@@ -688,8 +692,10 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         // and 128-column block (max |O| * 2^-s in [2^14, 2^15), so nothing
         // overflows and the rounding is relative to the block's largest
         // value); the combine multiplies by 2^s and accumulates in fp32.
-        // Rows go through shared memory, half a tile at a time, so that each
-        // store instruction writes four whole 128-byte row pieces
+        // This warp's block is columns nb0 .. nb0 + 127.  Rows go through
+        // shared memory 32 columns at a time, so that each store instruction
+        // writes eight whole 64-byte row pieces
+        const int nb0 = n0 + 128 * hh;
         const float sd = FMT == MOE_NVFP4 ? ts[2] * p.act_scale : 1.0f;
         __half* Oh = reinterpret_cast<__half*>(p.O);
         float mx = 0.f;
@@ -705,35 +711,32 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
           se = max(-100, min(100, ex - 15));
         }
         const float sc = sd * __int_as_float((127 - se) << 23);   // sd * 2^-se
-        if (live) p.O_exp[(size_t)r * (p.O_ld / 128) + n0 / 128] = (int8_t)se;
+        if (live) p.O_exp[(size_t)r * (p.O_ld / 128) + nb0 / 128] = (int8_t)se;
         __half* ost = reinterpret_cast<__half*>(sf_smem + (size_t)kWsStages * kSfStage) +
                       (size_t)(warp - kEpiWarp0) * 32 * kOStrideB;
         uint4* myrow = reinterpret_cast<uint4*>(ost + lane * kOStrideB);
         const int row0 = tile.row_start + 32 * (warp & 3);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t* vv = q4 == 0 ? v0 : q4 == 1 ? v1 : q4 == 2 ? v2 : v3;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t* vv = hf == 0 ? (c == 0 ? v0 : v1) : (c == 0 ? v2 : v3);
+          for (int i2 = 0; i2 < 4; ++i2) {
+            uint32_t w[4];
 #pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) {
-              uint32_t w[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const __half2 h2 = __floats2half2_rn(__uint_as_float(vv[8 * i2 + 2 * j]) * sc,
-                                                     __uint_as_float(vv[8 * i2 + 2 * j + 1]) * sc);
-                w[j] = *reinterpret_cast<const uint32_t*>(&h2);
-              }
-              myrow[4 * c + i2] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int j = 0; j < 4; ++j) {
+              const __half2 h2 = __floats2half2_rn(__uint_as_float(vv[8 * i2 + 2 * j]) * sc,
+                                                   __uint_as_float(vv[8 * i2 + 2 * j + 1]) * sc);
+              w[j] = *reinterpret_cast<const uint32_t*>(&h2);
             }
+            myrow[i2] = make_uint4(w[0], w[1], w[2], w[3]);
           }
           __syncwarp();
-          // four rows per instruction: lanes 8j .. 8j + 7 take row rr + j
-          for (int rr = 0; rr < 32; rr += 4) {
-            const int rw = rr + (lane >> 3), rg = row0 + rw;
+          // eight rows per instruction: lanes 4j .. 4j + 3 take row rr + j
+          for (int rr = 0; rr < 32; rr += 8) {
+            const int rw = rr + (lane >> 2), rg = row0 + rw;
             if (rg < tile.row_end)
-              reinterpret_cast<uint4*>(Oh + (size_t)rg * p.O_ld + n0 + 64 * hf)[lane & 7] =
-                  reinterpret_cast<const uint4*>(ost + rw * kOStrideB)[lane & 7];
+              reinterpret_cast<uint4*>(Oh + (size_t)rg * p.O_ld + nb0 + 32 * q4)[lane & 3] =
+                  reinterpret_cast<const uint4*>(ost + rw * kOStrideB)[lane & 3];
           }
           __syncwarp();
         }
@@ -902,7 +905,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   const int blk = fmt_block(g.afmt);   // scale block of both operands (W4A8: 32 on either side)
   const size_t ent_bytes = blk ? 3 * (size_t)g.d * g.f / blk : 0;
   if (blk) {
-    const size_t items = (size_t)(g.f / kTileRows) * (g.d / blk / 4) * 64 + (size_t)(g.d / kTileRows) * (g.f / blk / 4) * 32;
+    const size_t items = (size_t)(g.f / kTileRows) * (g.d / blk / 4) * 64 + (size_t)(g.d / 256) * (g.f / blk / 4) * 64;
     const dim3 grid((unsigned)((items + 255) / 256), (unsigned)(g.E + 1));
     interleave_wscales_kernel<<<grid, 256, 0, st>>>(slots, g.ebytes, g.off_scales[0], g.off_scales[1],
                                                      g.off_scales[2], ents, n_tiles, g.d, g.f, blk, wsf);
@@ -968,7 +971,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   p.O = O;
   p.O_ld = g.d;
   p.O_exp = prefill_o_exp(g, O, N);
-  const int grid2 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.d / kTileRows));
+  const int grid2 = (int)std::min<long long>(num_sms, (long long)max_tiles * (g.d / 256));
   if (ev) cudaEventRecord(ev[2], st);
   if (g.afmt != g.fmt)
     gemm_ws_kernel<kW4A8, 2><<<grid2, ws_threads<2>(), ws_smem<kW4A8, 2>(), st>>>(pl->hq, pl->wd, pl->wd, p);
