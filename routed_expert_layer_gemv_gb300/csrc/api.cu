@@ -1157,7 +1157,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   }
   cudaEvent_t* pe = prof_begin(L, MOE_PROF_ROUTER, st);
   MOE_CUDA(L, launch_router(g, xd, N, L->Wr, L->Wr_hl, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
-                            L->gates, L->xexp, L->rcounter, st));
+                            L->gates, prefill ? nullptr : L->xexp, L->rcounter, L->err_dev, st));
   prof_end(pe, st);
   L->launches += N <= 64 ? 1 : 2;
   // memcpy fills: the LRU kernel also writes the step record into mapped
@@ -1486,7 +1486,7 @@ int moe_debug_router(moe_layer_t L, const void* x, int N, int* idx, float* gates
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MOE_CUDA(L, launch_router(L->g, static_cast<const __nv_bfloat16*>(x), N, L->Wr, L->Wr_hl,
                             L->g.has_bias ? L->bias : nullptr, logits ? logits : L->logits, idx,
-                            gates, L->xexp, L->rcounter, st));
+                            gates, L->xexp, L->rcounter, L->err_dev, st));
   return MOE_OK;
 }
 

@@ -258,17 +258,21 @@ cudaError_t launch_router_split(const Geo& g, const float* Wr, __nv_bfloat16* Wp
 
 cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
                           const __nv_bfloat16* Whl, const float* bias, float* logits, int* idx,
-                          float* gates, int* xexp, unsigned int* counter, cudaStream_t st) {
+                          float* gates, int* xexp, unsigned int* counter, int* errw, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
   if (Whl == nullptr || counter == nullptr) return cudaErrorInvalidValue;
   if (N > 64) {
-    // large batches: tensor-core logits, then the top-k kernel
-    const size_t smem = (size_t)2 * kTcStage * sizeof(__nv_bfloat16);
-    cudaError_t e = ensure_smem_limit((const void*)router_tc_kernel, (int)smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((N + kTcM - 1) / kTcM, (g.E + kTcN - 1) / kTcN);
-    router_tc_kernel<<<grid, 256, smem, st>>>(x, N, g.d, g.E, Whl, bias, logits, xexp);
-    cudaError_t err = cudaGetLastError();
+    // large batches: tensor-core logits (tcgen05 where the shape allows,
+    // else mma.sync), then the top-k kernel
+    cudaError_t err = errw ? launch_router_tc5(g, x, N, Whl, bias, logits, xexp, errw, st) : cudaErrorNotSupported;
+    if (err == cudaErrorNotSupported) {
+      const size_t smem = (size_t)2 * kTcStage * sizeof(__nv_bfloat16);
+      cudaError_t e = ensure_smem_limit((const void*)router_tc_kernel, (int)smem);
+      if (e != cudaSuccess) return e;
+      const dim3 grid((N + kTcM - 1) / kTcM, (g.E + kTcN - 1) / kTcN);
+      router_tc_kernel<<<grid, 256, smem, st>>>(x, N, g.d, g.E, Whl, bias, logits, xexp);
+      err = cudaGetLastError();
+    }
     if (err != cudaSuccess) return err;
     router_topk_kernel<<<(N + 7) / 8, 256, (size_t)8 * g.E * sizeof(float), st>>>(logits, N, g.E, g.k,
                                                                                 g.norm_topk, idx, gates);
