@@ -80,6 +80,7 @@ struct moe_layer {
   unsigned long long* stamp = nullptr;
   int* buf = nullptr;                // slot -> pool buffer map, then the spare buffers (S + X)
   unsigned long long* clock = nullptr;
+  float* logits2 = nullptr;     // second K half's partial logits (large batches)
   float* logits = nullptr;
   int* idx = nullptr;
   float* gates = nullptr;
@@ -511,6 +512,7 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
     L->buf = base->buf;
     L->clock = base->clock;
     L->logits = base->logits;
+    L->logits2 = base->logits2;
     L->idx = base->idx;
     L->gates = base->gates;
     L->xexp = base->xexp;
@@ -552,6 +554,7 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
   MOE_ALLOC(buf, (size_t)(g.S + g.X) * 4);
   MOE_ALLOC(clock, 8);
   MOE_ALLOC(logits, Nm * g.E * 4);
+  MOE_ALLOC(logits2, Nm > 64 ? Nm * g.E * 4 : 16);   // the second K half of the large-batch router
   MOE_ALLOC(idx, Nm * g.k * 4);
   MOE_ALLOC(gates, Nm * g.k * 4);
   MOE_ALLOC(xexp, Nm * 4);
@@ -1157,7 +1160,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   }
   cudaEvent_t* pe = prof_begin(L, MOE_PROF_ROUTER, st);
   MOE_CUDA(L, launch_router(g, xd, N, L->Wr, L->Wr_hl, g.has_bias ? L->bias : nullptr, L->logits, L->idx,
-                            L->gates, prefill ? nullptr : L->xexp, L->rcounter, L->err_dev, st));
+                            L->gates, prefill ? nullptr : L->xexp, L->rcounter, L->err_dev, L->logits2, st));
   prof_end(pe, st);
   L->launches += N <= 64 ? 1 : 2;
   // memcpy fills: the LRU kernel also writes the step record into mapped
@@ -1486,7 +1489,7 @@ int moe_debug_router(moe_layer_t L, const void* x, int N, int* idx, float* gates
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MOE_CUDA(L, launch_router(L->g, static_cast<const __nv_bfloat16*>(x), N, L->Wr, L->Wr_hl,
                             L->g.has_bias ? L->bias : nullptr, logits ? logits : L->logits, idx,
-                            gates, L->xexp, L->rcounter, L->err_dev, st));
+                            gates, L->xexp, L->rcounter, L->err_dev, L->logits2, st));
   return MOE_OK;
 }
 

@@ -191,13 +191,17 @@ __host__ __device__ inline void miss_chunk(int m, int c, int nch, int* lo, int* 
 // error word, set when a bounded wait of the tcgen05 logits kernel runs out)
 cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
                           const __nv_bfloat16* Whl, const float* bias, float* logits, int* idx,
-                          float* gates, int* xexp, unsigned int* counter, int* err, cudaStream_t st);
+                          float* gates, int* xexp, unsigned int* counter, int* err, float* part2,
+                          cudaStream_t st);
 // router_tc.cu: logits of batches over 64 tokens on tcgen05 (E a multiple of
 // 16 up to 256, d a multiple of 64; cudaErrorNotSupported otherwise), then
-// xexp when asked
+// xexp when asked.  part2 (may be null; [N, E]): room for the second K half's
+// partial sums; *split = 2 when they were written (the logits then hold the
+// first half's, without the bias), else 1
 bool router_tc5_shape_ok(const Geo& g);
 cudaError_t launch_router_tc5(const Geo& g, const __nv_bfloat16* x, int N, const __nv_bfloat16* Whl,
-                              const float* bias, float* logits, int* xexp, int* err, cudaStream_t st);
+                              const float* bias, float* logits, float* part2, int* split, int* xexp, int* err,
+                              cudaStream_t st);
 cudaError_t launch_router_split(const Geo& g, const float* Wr, __nv_bfloat16* Whl, cudaStream_t st);
 // permute.cu
 size_t permute_scratch_bytes(const Geo& g, int max_tokens);

@@ -238,13 +238,24 @@ router_tc_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E, const
 }
 
 __global__ void __launch_bounds__(256)
-router_topk_kernel(const float* __restrict__ logits, int N, int E, int k, int norm_topk,
-                   int* __restrict__ idx, float* __restrict__ gates) {
+router_topk_kernel(float* __restrict__ logits, const float* __restrict__ part2, const float* __restrict__ bias,
+                   int N, int E, int k, int norm_topk, int* __restrict__ idx, float* __restrict__ gates) {
   extern __shared__ float Lsm[];
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= N) return;
   float* Ls = Lsm + (size_t)(threadIdx.x >> 5) * E;
-  stage_logits(logits, t, E, Ls);
+  if (part2 != nullptr) {
+    // logits from two K halves: (first + second) + bias, written back
+    for (int e = threadIdx.x & 31; e < E; e += 32) {
+      const size_t i = (size_t)t * E + e;
+      const float v = (__ldcg(logits + i) + __ldcg(part2 + i)) + (bias ? bias[e] : 0.f);
+      logits[i] = v;
+      Ls[e] = v;
+    }
+    __syncwarp();
+  } else {
+    stage_logits(logits, t, E, Ls);
+  }
   topk_row(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
@@ -258,13 +269,16 @@ cudaError_t launch_router_split(const Geo& g, const float* Wr, __nv_bfloat16* Wp
 
 cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const float* Wr,
                           const __nv_bfloat16* Whl, const float* bias, float* logits, int* idx,
-                          float* gates, int* xexp, unsigned int* counter, int* errw, cudaStream_t st) {
+                          float* gates, int* xexp, unsigned int* counter, int* errw, float* part2,
+                          cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
   if (Whl == nullptr || counter == nullptr) return cudaErrorInvalidValue;
   if (N > 64) {
     // large batches: tensor-core logits (tcgen05 where the shape allows,
     // else mma.sync), then the top-k kernel
-    cudaError_t err = errw ? launch_router_tc5(g, x, N, Whl, bias, logits, xexp, errw, st) : cudaErrorNotSupported;
+    int split = 1;
+    cudaError_t err = errw ? launch_router_tc5(g, x, N, Whl, bias, logits, part2, &split, xexp, errw, st)
+                           : cudaErrorNotSupported;
     if (err == cudaErrorNotSupported) {
       const size_t smem = (size_t)2 * kTcStage * sizeof(__nv_bfloat16);
       cudaError_t e = ensure_smem_limit((const void*)router_tc_kernel, (int)smem);
@@ -274,8 +288,8 @@ cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const flo
       err = cudaGetLastError();
     }
     if (err != cudaSuccess) return err;
-    router_topk_kernel<<<(N + 7) / 8, 256, (size_t)8 * g.E * sizeof(float), st>>>(logits, N, g.E, g.k,
-                                                                                g.norm_topk, idx, gates);
+    router_topk_kernel<<<(N + 7) / 8, 256, (size_t)8 * g.E * sizeof(float), st>>>(
+        logits, split > 1 ? part2 : nullptr, bias, N, g.E, g.k, g.norm_topk, idx, gates);
     return cudaGetLastError();
   }
   // decode sizes: one CTA per expert and token tile, top-k fused (router_dec_kernel)

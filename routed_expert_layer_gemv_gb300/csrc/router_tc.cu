@@ -9,7 +9,9 @@
 // so no long chain of tensor-core accumulations drifts.  (The pages do not
 // define the router: the standard softmax top-k router, see router.cu.)
 //
-// One CTA per 128 tokens (MMA M = 128, N = E <= 256): warp 0 streams x and
+// One CTA per 128 tokens and K half (the halves only when the token tiles
+// fill less than half of the SMs; the top-k kernel adds the two partial sums,
+// first half first, and the bias) (MMA M = 128, N = E <= 256): warp 0 streams x and
 // the three parts of W_r by TMA through a ring of K = 64 stages, warp 1 issues
 // each stage's twelve MMAs into one of several accumulator slots, the
 // epilogue warps (one or two per lane quarter) drain each stage's slot and
@@ -51,7 +53,7 @@ template <int EW>
 __global__ void __launch_bounds__(64 + 32 * EW, 1)
 router_tc5_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, int N, int d,
                   int E, int stages, const float* __restrict__ bias, float* __restrict__ logits,
-                  int* __restrict__ err) {
+                  float* __restrict__ part2, int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kRMaxStages], empty[kRMaxStages], accf[kRMaxSlots], acce[kRMaxSlots], fin;
@@ -62,7 +64,10 @@ router_tc5_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant_
   const int ncols = E <= 128 ? 128 : 256;           // TMEM columns of one accumulator slot
   const int nslot = 512 / ncols;
   const int m0 = blockIdx.x * kRM;
-  const int nk = d / kRK;
+  // this CTA's K stages [kb, kb + nk) (blockIdx.y: the K half when split)
+  const int nk_all = d / kRK, ns = gridDim.y;
+  const int kb = (int)((long long)nk_all * blockIdx.y / ns);
+  const int nk = (int)((long long)nk_all * (blockIdx.y + 1) / ns) - kb;
   if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
   if (threadIdx.x == 32) {
     for (int s = 0; s < kRMaxStages; ++s) {
@@ -92,9 +97,9 @@ router_tc5_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant_
         if (u > 0 && !rwait(&empty[s], (u - 1) & 1, &s_abort, err)) break;
         uint8_t* st = smem + (size_t)s * st_bytes;
         tc::mbar_expect_tx(&full[s], st_bytes);
-        tc::tma_load_2d(st, &tx, &full[s], kt * kRK, m0);   // rows past N read as zeros
+        tc::tma_load_2d(st, &tx, &full[s], (kb + kt) * kRK, m0);   // rows past N read as zeros
         for (int p = 0; p < kRParts; ++p)
-          tc::tma_load_2d(st + a_bytes + (size_t)p * E * 128, &tw, &full[s], kt * kRK, p * E);
+          tc::tma_load_2d(st + a_bytes + (size_t)p * E * 128, &tw, &full[s], (kb + kt) * kRK, p * E);
       }
       // copies in flight land before the CTA exits (bounded)
       const int first = kt > stages ? kt - stages : 0;
@@ -158,10 +163,12 @@ router_tc5_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant_
     }
     const int t = m0 + row;
     if (ok && t < N) {
-      float* out = logits + (size_t)t * E + c0;
+      // one K range: the logits; two: this half's partial sums (no bias)
+      float* out = (blockIdx.y == 0 ? logits : part2) + (size_t)t * E + c0;
+      const bool whole = ns == 1;
 #pragma unroll
       for (int i = 0; i < 128; ++i)
-        if (c0 + i < E) out[i] = sum[i] + (bias ? bias[c0 + i] : 0.f);
+        if (c0 + i < E) out[i] = whole ? sum[i] + (bias ? bias[c0 + i] : 0.f) : sum[i];
     }
   }
   tc::fence_before();
@@ -216,7 +223,8 @@ bool router_tc5_shape_ok(const Geo& g) {
 }
 
 cudaError_t launch_router_tc5(const Geo& g, const __nv_bfloat16* x, int N, const __nv_bfloat16* Whl,
-                              const float* bias, float* logits, int* xexp, int* err, cudaStream_t st) {
+                              const float* bias, float* logits, float* part2, int* split, int* xexp, int* err,
+                              cudaStream_t st) {
   if (!router_tc5_shape_ok(g) || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(Whl) & 15))
     return cudaErrorNotSupported;
   CUtensorMap tx, tw;
@@ -225,16 +233,22 @@ cudaError_t launch_router_tc5(const Geo& g, const __nv_bfloat16* x, int N, const
   const int stages = (int)std::min<size_t>(kRMaxStages, (226 * 1024) / st_bytes);
   if (stages < 2) return cudaErrorNotSupported;
   const int smem = (int)std::max<size_t>(kRSmemMin, 1024 + stages * st_bytes);
-  const int grid = (N + kRM - 1) / kRM;
+  const int mt = (N + kRM - 1) / kRM;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int ns = part2 != nullptr && 2 * mt <= sms && g.d / kRK >= 2 ? 2 : 1;   // K halves
+  *split = ns;
+  const dim3 grid(mt, ns);
   cudaError_t e;
   if (g.E <= 128) {
     e = ensure_smem_limit((const void*)router_tc5_kernel<4>, smem);
     if (e != cudaSuccess) return e;
-    router_tc5_kernel<4><<<grid, 64 + 32 * 4, smem, st>>>(tx, tw, N, g.d, g.E, stages, bias, logits, err);
+    router_tc5_kernel<4><<<grid, 64 + 32 * 4, smem, st>>>(tx, tw, N, g.d, g.E, stages, bias, logits, part2, err);
   } else {
     e = ensure_smem_limit((const void*)router_tc5_kernel<8>, smem);
     if (e != cudaSuccess) return e;
-    router_tc5_kernel<8><<<grid, 64 + 32 * 8, smem, st>>>(tx, tw, N, g.d, g.E, stages, bias, logits, err);
+    router_tc5_kernel<8><<<grid, 64 + 32 * 8, smem, st>>>(tx, tw, N, g.d, g.E, stages, bias, logits, part2, err);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || xexp == nullptr) return e;
