@@ -288,46 +288,47 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
 // in the tcgen05.cp layout, entry-major: phase 1 first (per block q of 128
 // gate rows and the same 128 up rows, per group g: the gate block's 512
 // bytes, then the up block's, K = d), then phase 2 (per block of 256 down
-// rows, per group: its two 128-row halves' 512 bytes, K = f).  Thread = one
-// 16-byte row of a 512-byte group.
-__global__ void interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size_t off_g,
-                                          size_t off_u, size_t off_d, const int* __restrict__ ents,
-                                          const int* __restrict__ n_tiles, int d, int f, int blk,
-                                          uint8_t* __restrict__ wsf) {
+// rows, per group: its two 128-row halves' 512 bytes, K = f).  CTA = one
+// 128-row block of one matrix (blockIdx.x: phase 1's (q, gate / up) blocks,
+// then the down matrix's), staged through shared memory (rows padded to an
+// odd word count) so that both the row reads and the 16-byte writes are
+// coalesced.
+__global__ void __launch_bounds__(256)
+interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size_t off_g, size_t off_u,
+                          size_t off_d, const int* __restrict__ ents, const int* __restrict__ n_tiles, int d,
+                          int f, int blk, uint8_t* __restrict__ wsf) {
+  extern __shared__ uint32_t smw[];
   const int ent = blockIdx.y;
   if (ent >= n_tiles[1]) return;
   const int slot = ents[ent];
   if (slot < 0) return;
-  const int ng1 = d / blk / 4, ng2 = f / blk / 4;
-  const size_t n1 = (size_t)(f / kTileRows) * ng1 * 2 * 32, n2 = (size_t)(d / 256) * ng2 * 2 * 32;
-  const size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= n1 + n2) return;
   const uint8_t* w = slots + (size_t)slot * ebytes;
   uint8_t* out = wsf + (size_t)ent * (3 * (size_t)d * f / blk);
-  uint32_t word[4];
-  if (v < n1) {
-    const int i = (int)(v & 31), h = (int)((v >> 5) & 1);
-    const int g = (int)((v >> 6) % ng1), q = (int)((v >> 6) / ng1);
-    const int srow = d / blk;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint8_t* src = w + (h ? off_u : off_g) + (size_t)(kTileRows * q + 32 * j + i) * srow + 4 * g;
-      word[j] = *reinterpret_cast<const uint32_t*>(src);
-    }
-    *reinterpret_cast<uint4*>(out + (((size_t)q * ng1 + g) * 2 + h) * 512 + 16 * i) =
-        make_uint4(word[0], word[1], word[2], word[3]);
+  const int nb1 = 2 * (f / kTileRows);
+  const int b = blockIdx.x;
+  int K, hi, hh;
+  const uint8_t* src;
+  if (b < nb1) {
+    hi = b >> 1;
+    hh = b & 1;
+    K = d;
+    src = w + (hh ? off_u : off_g) + (size_t)kTileRows * hi * (K / blk);
   } else {
-    const size_t u = v - n1;
-    const int i = (int)(u & 31), h = (int)((u >> 5) & 1);
-    const int g = (int)((u >> 6) % ng2), rb = (int)((u >> 6) / ng2);
-    const int srow = f / blk;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint8_t* src = w + off_d + (size_t)(256 * rb + kTileRows * h + 32 * j + i) * srow + 4 * g;
-      word[j] = *reinterpret_cast<const uint32_t*>(src);
-    }
-    *reinterpret_cast<uint4*>(out + 2 * (size_t)d * f / blk + (((size_t)rb * ng2 + g) * 2 + h) * 512 + 16 * i) =
-        make_uint4(word[0], word[1], word[2], word[3]);
+    const int rb = b - nb1;   // 128-row block of the down matrix
+    hi = rb >> 1;
+    hh = rb & 1;
+    K = f;
+    src = w + off_d + (size_t)kTileRows * rb * (K / blk);
+    out += 2 * (size_t)d * f / blk;
+  }
+  const int ng = K / blk / 4, ngp = ng | 1;   // words per row, padded to odd
+  const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
+  for (int v = threadIdx.x; v < kTileRows * ng; v += blockDim.x) smw[(v / ng) * ngp + v % ng] = s4[v];
+  __syncthreads();
+  for (int v = threadIdx.x; v < ng * 32; v += blockDim.x) {
+    const int i = v & 31, g = v >> 5;
+    *reinterpret_cast<uint4*>(out + (((size_t)hi * ng + g) * 2 + hh) * 512 + 16 * i) =
+        make_uint4(smw[i * ngp + g], smw[(32 + i) * ngp + g], smw[(64 + i) * ngp + g], smw[(96 + i) * ngp + g]);
   }
 }
 
@@ -905,10 +906,13 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
   const int blk = fmt_block(g.afmt);   // scale block of both operands (W4A8: 32 on either side)
   const size_t ent_bytes = blk ? 3 * (size_t)g.d * g.f / blk : 0;
   if (blk) {
-    const size_t items = (size_t)(g.f / kTileRows) * (g.d / blk / 4) * 64 + (size_t)(g.d / 256) * (g.f / blk / 4) * 64;
-    const dim3 grid((unsigned)((items + 255) / 256), (unsigned)(g.E + 1));
-    interleave_wscales_kernel<<<grid, 256, 0, st>>>(slots, g.ebytes, g.off_scales[0], g.off_scales[1],
-                                                     g.off_scales[2], ents, n_tiles, g.d, g.f, blk, wsf);
+    const int ngp_max = std::max(g.d, g.f) / blk / 4 | 1;
+    const int ismem = kTileRows * ngp_max * 4;
+    e = ensure_smem_limit((const void*)interleave_wscales_kernel, ismem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)(2 * (g.f / kTileRows) + g.d / kTileRows), (unsigned)(g.E + 1));
+    interleave_wscales_kernel<<<grid, 256, ismem, st>>>(slots, g.ebytes, g.off_scales[0], g.off_scales[1],
+                                                        g.off_scales[2], ents, n_tiles, g.d, g.f, blk, wsf);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
