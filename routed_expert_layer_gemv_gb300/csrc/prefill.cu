@@ -1,25 +1,28 @@
-// Prefill expert FFN: grouped GEMM on tcgen05 block-scaled FP4 MMAs.
+// Prefill expert FFN: grouped GEMM on tcgen05 block-scaled MMAs.
 //
 // A prefill chunk gives each expert hundreds of tokens, so the expert FFN is a
 // dense contraction (FreeToken's prefill streams whole layers of experts and
 // is bound by compute once they are resident: "FreeToken：把 284B MoE 塞进游戏
-// PC", zhichai.net, §二 "Prefill" paragraph).  FP4 x FP4 MMAs need FP4
-// activations, so x and h go through the block quantiser of the weight format
-// (actquant.cuh).  Steps:
+// PC", zhichai.net, §二 "Prefill" paragraph).  Low-precision MMAs need
+// low-precision activations, so x and h go through the block quantiser of the
+// prefill activation format (the weights' own, or MXFP8 on MXFP4 weights:
+// W4A8; actquant.cuh).  Steps:
 //  1. gather_quant: row r of the permuted activations = quant(x[tok_of[r]]);
-//     rows N*k .. N*k+N-1 hold every token for the shared expert.
+//     rows N*k .. N*k+N-1 hold every token for the shared expert; block
+//     scales by padded 128-row block in the layout tcgen05.cp reads.
 //  2. build_tiles: the launch's experts (hits, or all misses, + shared) cut
 //     into M tiles of 128 rows; the last tile of an expert is ragged (its extra
-//     rows are computed and dropped).
-//  3. phase 1 (gemm_ws_kernel<fmt, 1>): tiles of 128 rows x 64 d_ff columns;
-//     B stacks the 64 gate rows over the same 64 up rows, so one N = 128 MMA
+//     rows are computed and dropped).  interleave_wscales: the launch's
+//     weight scales into the tcgen05.cp layout.
+//  3. phase 1 (gemm_ws_kernel<fmt, 1>): tiles of 128 rows x 128 d_ff columns;
+//     B stacks the 128 gate rows over the same 128 up rows, so one N = 256 MMA
 //     yields both halves of SwiGLU; epilogue h = SiLU(a) * u, re-quantised.
-//  4. phase 2 (gemm_ws_kernel<fmt, 2>): tiles of 128 rows x 128 d_model
-//     columns, O = h W_d^T in fp32.
+//  4. phase 2 (gemm_ws_kernel<fmt, 2>): tiles of 128 rows x 256 d_model
+//     columns, O = h W_d^T, written as scaled f16.
 // Both phases run the persistent warp-specialised kernel below (TMA warp, MMA
-// warp, block-scale warps, epilogue warps).  Every wait is bounded (~2 s); on
-// a timeout the CTA records an error, skips its remaining waits, waits for its
-// own copies and MMAs (bounded again), frees its TMEM and returns.
+// warp, epilogue warps).  Every wait is bounded (~2 s); on a timeout the CTA
+// records an error, skips its remaining waits, waits for its own copies and
+// MMAs (bounded again), frees its TMEM and returns.
 #include <algorithm>
 #include <cstdio>
 
@@ -31,7 +34,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTileRows = 128;          // M and N of one MMA tile
+constexpr int kTileRows = 128;          // M of one MMA tile, rows of one TMA box
 
 // Kernel variant of W4A8: MXFP4 weights under MXFP8 activations.  The MMA is
 // kind::mxf8f6f4 with E4M3 A and E2M1 B; the FP4 weight tiles are loaded by
@@ -42,7 +45,7 @@ constexpr int kW4A8 = 100;
 // The activation (A) operand's format of a kernel variant.
 __host__ __device__ constexpr int act_op_fmt(int F) { return F == kW4A8 ? MOE_MXFP8 : F; }
 constexpr int kKTileBytes = 128;        // 256 FP4 codes per K tile
-constexpr int kOpBytes = kTileRows * kKTileBytes;   // 16 KB per operand tile
+constexpr int kOpBytes = kTileRows * kKTileBytes;   // 16 KB per 128-row operand box
 
 struct Tile {
   int slot;       // pool buffer of the expert (Geo::shb: the shared expert)
