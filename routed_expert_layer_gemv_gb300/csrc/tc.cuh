@@ -14,7 +14,11 @@
 //    4g + j holds the 4 bytes of row 32j + i (each lane quarter reads its own
 //    column), so every quarter holds all 128 rows' group g; the scale-factor id
 //    selects the first byte (MXFP4: 2 scales per MMA, id 0 or 2; NVFP4: 4 per
-//    MMA, id 0).
+//    MMA, id 0).  tcgen05.cp.32x128b.warpx4 writes exactly this from 512
+//    bytes of shared memory (byte 16 i + 4 j + b: row 32 j + i, block b);
+//  * an N = 256 MMA reads B's scales for rows 128 h + r from the 4 columns
+//    4 h further on (the two 128-row blocks of a group side by side; checked
+//    on GB300 by the layer parity tests of every block-scaled kind).
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
