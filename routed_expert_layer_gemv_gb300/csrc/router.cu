@@ -256,7 +256,7 @@ router_topk_kernel(float* __restrict__ logits, const float* __restrict__ part2, 
   } else {
     stage_logits(logits, t, E, Ls);
   }
-  topk_row(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
+  rt::topk_row_many(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
 }
 
 }  // namespace

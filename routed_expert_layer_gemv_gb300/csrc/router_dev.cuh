@@ -51,6 +51,62 @@ MOE_DEV void topk_row(const float* L, int E, int k, int norm_topk, int* idx, flo
   topk_gates(L, E, k, norm_topk, my_e, idx, gates);
 }
 
+// The same selection for E <= 32 P: each lane sorts its P entries (lane + 32 i,
+// ascending id) once by key, descending and stable, so its head is the
+// largest key it holds with the lowest id among equal ones -- what the scan of
+// topk_row finds in every round -- and the winner of a round drops its head.
+template <int P>
+MOE_DEV void topk_row_sorted(const float* L, int E, int k, int norm_topk, int* idx, float* gates) {
+  const int lane = threadIdx.x & 31;
+  uint32_t ks[P];
+  int es[P];
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int e = lane + 32 * i;
+    ks[i] = e < E ? logit_key(L[e]) : 0u;   // no entry: below every key (as the scan's start)
+    es[i] = e < E ? e : 0x7fffffff;
+  }
+#pragma unroll
+  for (int i = 1; i < P; ++i)
+#pragma unroll
+    for (int j = i; j > 0; --j)
+      if (ks[j] > ks[j - 1]) {   // strict: equal keys keep ascending ids
+        const uint32_t tk = ks[j];
+        ks[j] = ks[j - 1];
+        ks[j - 1] = tk;
+        const int te = es[j];
+        es[j] = es[j - 1];
+        es[j - 1] = te;
+      }
+  int my_e = -1;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, ks[0]);
+    const int w = (int)__reduce_min_sync(0xffffffffu, ks[0] == m ? (uint32_t)es[0] : 0xffffffffu);
+    if ((w & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i + 1 < P; ++i) {
+        ks[i] = ks[i + 1];
+        es[i] = es[i + 1];
+      }
+      ks[P - 1] = 0u;
+      es[P - 1] = 0x7fffffff;
+    }
+    if (lane == j) my_e = w;
+  }
+  topk_gates(L, E, k, norm_topk, my_e, idx, gates);
+}
+
+// topk_row with the presorted selection for E <= 256: the same ids and gates.
+// The prefill-sized top-k uses it (one warp per token, thousands of tokens);
+// inside the fused decode step the scan measured faster.
+MOE_DEV void topk_row_many(const float* L, int E, int k, int norm_topk, int* idx, float* gates) {
+  if (E <= 32) return topk_row_sorted<1>(L, E, k, norm_topk, idx, gates);
+  if (E <= 64) return topk_row_sorted<2>(L, E, k, norm_topk, idx, gates);
+  if (E <= 128) return topk_row_sorted<4>(L, E, k, norm_topk, idx, gates);
+  if (E <= 256) return topk_row_sorted<8>(L, E, k, norm_topk, idx, gates);
+  topk_row(L, E, k, norm_topk, idx, gates);
+}
+
 // The selected experts' gates (one warp): lane j < k holds my_e = the j-th
 // largest logit's expert (selection order); writes idx and gates in ascending
 // expert order.  Gates (fp32) = softmax over the selected logits, or the full

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 from helpers import bf16_tensor, need_gpu, oracle_layer, reject_near_ties, small_spec
+from oracle import layer as npl
 from oracle.native import formats, quant
 from oracle.native import layer as olayer
 from oracle.native.lru import SlotTable
@@ -119,6 +120,55 @@ def test_router_indices_bit_exact(case):
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.allclose(gates.cpu().numpy(), rg, rtol=2e-6, atol=1e-7)
     assert np.allclose(logits.cpu().numpy(), rL, rtol=1e-4, atol=2e-5)
+    L.close()
+
+
+@pytest.mark.parametrize("case", [
+    dict(spec=small_spec(E=32, k=6, d_model=512), N=7),               # one entry per lane
+    dict(spec=wl.DECODE_35B.layer, N=9),                              # decode router, E = 128
+    dict(spec=wl.DECODE_35B.layer, N=130),                            # tensor-core logits, E = 128
+    dict(spec=wl.PREFILL_753B.layer, N=40),                           # E = 256, bias
+    dict(spec=small_spec(E=512, k=8, d_model=256, n_slots=64), N=20),  # E above 256, decode router
+    dict(spec=small_spec(E=512, k=8, d_model=256, n_slots=64), N=70),  # E above 256, prefill top-k
+])
+def test_router_exact_ties_go_to_lower_id(case):
+    """Exact ties: router rows (and biases) repeat in groups of G, so the
+    logits of a group are equal bit for bit; G does not divide k, so a group
+    straddles the k-th place.  The ids must be the k largest of the library's
+    own logits with ties to the lower id (the oracle's selection run on them),
+    and the gates their softmax."""
+    spec, N = case["spec"], case["N"]
+    G = 3 if spec.k % 3 else 4
+    base = (np.arange(spec.E) // G) * G
+    W_r, b = wl.router_weights(spec, 11)
+    W_r = np.ascontiguousarray(W_r[base])
+    if b is not None:
+        b = np.ascontiguousarray(b[base])
+    from routed_expert_layer_gemv_gb300.layer import MoELayer
+    L = MoELayer(spec, N)
+    L.set_router(W_r, b)
+    x, _ = wl.iid_tokens(11, N, spec.d_model, None)
+    idx = torch.empty(N, spec.k, dtype=torch.int32, device="cuda")
+    gates = torch.empty(N, spec.k, dtype=torch.float32, device="cuda")
+    logits = torch.empty(N, spec.E, dtype=torch.float32, device="cuda")
+    capi.moe_debug_router(L.h, bf16_tensor(x), N, idx, gates, logits)
+    Lg = logits.cpu().numpy().astype(np.float64)
+    assert np.array_equal(Lg, Lg[:, base])                             # the ties are exact
+    ridx = npl.topk_select(Lg, spec.k)
+    got = idx.cpu().numpy()
+    assert np.array_equal(got, ridx)
+    # a group on the k-th place keeps its lower members
+    straddles = 0
+    for t in range(N):
+        sel = set(got[t].tolist())
+        assert all(e - 1 in sel for e in sel if e % G)
+        straddles += any(e + 1 not in sel and (e + 1) % G and e + 1 < spec.E for e in sel)
+    assert straddles >= N // 2
+    m = Lg.max(axis=1, keepdims=True)
+    p = np.exp(Lg - m)
+    sel = np.take_along_axis(p, ridx, axis=1)
+    rg = sel / sel.sum(axis=1, keepdims=True) if spec.norm_topk else sel / p.sum(axis=1, keepdims=True)
+    assert np.allclose(gates.cpu().numpy(), rg, rtol=2e-6, atol=1e-7)
     L.close()
 
 
