@@ -107,7 +107,8 @@ struct moe_layer {
   uint8_t* hq_codes = nullptr;   // FP4 h [(rows + 128), f/2]
   uint8_t* hq_scales = nullptr;
   int* pbase = nullptr;          // padded 128-row block of each expert's rows (E + 2)
-  uint8_t* wsf = nullptr;        // one launch's weight scales, interleaved for tcgen05.cp
+  uint8_t* wsf = nullptr;        // the pool buffers' weight scales, interleaved for tcgen05.cp
+  int* wtag = nullptr;           // per buffer: key of the weights wsf holds scales for (-1: none), then counts
   void* tiles = nullptr;
   int* n_tiles = nullptr;
   PrefillPlan* plan = nullptr;
@@ -412,6 +413,17 @@ void prof_end(cudaEvent_t* e, cudaStream_t st) {
 // A buffer a fill may write: an LRU slot's or a spare, never the shared expert's.
 bool buf_ok(const Geo& g, int b) { return b >= 0 && b <= g.S + g.X && b != g.S; }
 
+// Forget every buffer's laid-out weight scales (the next prefill call lays
+// them out again): after any call that writes weights into the pool, moves
+// them between buffers or registers another host pool.  Ordered on `st`.
+cudaError_t forget_wscales(moe_layer* L, cudaStream_t st) {
+  if (!L->wtag) return cudaSuccess;
+  const size_t n = prefill_wtag_ints(L->g) / 2;
+  cudaError_t e = cudaMemsetAsync(L->wtag, 0xff, n * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(L->wtag + n, 0, n * 4, st);
+  return e;
+}
+
 // The pool buffer LRU slot `slot` lives in, read once the device is idle (a
 // step's LRU kernel may remap slots).
 int slot_buffer(moe_layer* L, int slot, int* b) {
@@ -536,6 +548,7 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
     L->hq_scales = base->hq_scales;
     L->pbase = base->pbase;
     L->wsf = base->wsf;
+    L->wtag = base->wtag;
     L->tiles = base->tiles;
     L->n_tiles = base->n_tiles;
     L->gplan = base->gplan;
@@ -581,6 +594,7 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
     MOE_ALLOC(hq_scales, prefill_act_scale_bytes(g, (int)Nm, g.f));
     MOE_ALLOC(pbase, (size_t)(g.E + 2) * 4);
     MOE_ALLOC(wsf, prefill_wscale_bytes(g));
+    MOE_ALLOC(wtag, prefill_wtag_ints(g) * 4);
     MOE_ALLOC(tiles, prefill_tile_bytes(g, (int)Nm));
     MOE_ALLOC(n_tiles, 16);
   }
@@ -647,7 +661,8 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
            cudaMemset(L->expert_of, 0xff, (size_t)g.S * 4) == cudaSuccess &&
            cudaMemset(L->stamp, 0, (size_t)g.S * 8) == cudaSuccess &&
            cudaMemset(L->clock, 0, 8) == cudaSuccess &&
-           cudaMemset(L->rcounter, 0, 16) == cudaSuccess;
+           cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
+           forget_wscales(L, nullptr) == cudaSuccess;
       // slot s in buffer s; the spares after the shared expert's buffer S
       std::vector<int> b0(g.S + g.X);
       for (int s = 0; s < g.S; ++s) b0[s] = s;
@@ -714,6 +729,8 @@ int moe_register_host_experts(moe_layer_t L, const void* pool, size_t bytes) {
     cudaGetLastError();
     return fail(L, MOE_ERR_ARG, "pool must be pinned (page-locked) host memory");
   }
+  MOE_CUDA(L, forget_wscales(L, nullptr));
+  MOE_CUDA(L, cudaDeviceSynchronize());
   L->host_pool = static_cast<const uint8_t*>(pool);
   L->host_pool_bytes = bytes;
   void* dp = nullptr;
@@ -735,6 +752,8 @@ int moe_set_shared_expert(moe_layer_t L, const void* weights) {
   if (!L->g.has_shared) return fail(L, MOE_ERR_STATE, "layer has no shared expert");
   if (!weights) return fail(L, MOE_ERR_ARG, "weights is NULL");
   MOE_CUDA(L, cudaMemcpy(L->shared_w, weights, L->g.ebytes, cudaMemcpyDefault));
+  MOE_CUDA(L, forget_wscales(L, nullptr));
+  MOE_CUDA(L, cudaDeviceSynchronize());
   L->shared_set = true;
   return MOE_OK;
 }
@@ -756,6 +775,7 @@ int moe_cache_install(moe_layer_t L, int expert, int slot, void* stream) {
   MOE_CUDA(L, cudaMemcpyAsync(L->slots + (size_t)b * L->g.ebytes,
                               L->host_pool + (size_t)expert * L->g.ebytes, L->g.ebytes,
                               cudaMemcpyHostToDevice, st));
+  MOE_CUDA(L, forget_wscales(L, st));
   MOE_CUDA(L, launch_lru_install(L->g, expert, slot, L->slot_of, L->expert_of, L->stamp, L->clock, st));
   const int key = L->g.key0 + expert;
   for (int s = 0; s < L->g.S; ++s)
@@ -890,6 +910,8 @@ int moe_cache_resize(moe_layer_t L, int n_slots, void* stream) {
     }
   }
   *L->mir = eo1;
+  MOE_CUDA(L, forget_wscales(L, nullptr));
+  MOE_CUDA(L, cudaDeviceSynchronize());
   return MOE_OK;
 }
 
@@ -912,6 +934,8 @@ int moe_lru_set_state(moe_layer_t L, const int* expert_of_slot, const uint64_t* 
   MOE_CUDA(L, cudaMemcpy(L->slot_of, slot_of.data(), (size_t)E * 4, cudaMemcpyHostToDevice));
   MOE_CUDA(L, cudaMemcpy(L->stamp, stamp, (size_t)S * 8, cudaMemcpyHostToDevice));
   MOE_CUDA(L, cudaMemcpy(L->clock, &clock, 8, cudaMemcpyHostToDevice));
+  MOE_CUDA(L, forget_wscales(L, nullptr));
+  MOE_CUDA(L, cudaDeviceSynchronize());
   L->mir->assign(expert_of_slot, expert_of_slot + S);
   return MOE_OK;
 }
@@ -1248,7 +1272,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     if (prefill) {
       ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, L->pbase, N, a.mode, a.with_shared,
                                 L->tiles, L->n_tiles, L->slots, L->xq_scales, L->hq_codes,
-                                L->hq_scales, L->wsf, L->O, gx, gh, L->err_dev,
+                                L->hq_scales, L->wsf, L->wtag, L->O, gx, gh, L->err_dev,
                                 L->gemm_sms > 0 ? L->gemm_sms : L->num_sms, st, evp);
       L->launches += fmt_block(g.afmt) ? 4 : 3;
     } else {

@@ -271,7 +271,8 @@ void prefill_plan_destroy(PrefillPlan* pl);
 bool prefill_plan_ready(const PrefillPlan* pl);
 size_t prefill_tile_bytes(const Geo& g, int N);            // tiles, then the launch's entries
 size_t prefill_act_scale_bytes(const Geo& g, int N, int K);  // x (K = d) or h (K = f) block scales
-size_t prefill_wscale_bytes(const Geo& g);                   // one launch's interleaved weight scales
+size_t prefill_wscale_bytes(const Geo& g);                   // interleaved weight scales, per pool buffer
+size_t prefill_wtag_ints(const Geo& g);                      // their tags (ints, -1 = none) and counts (0)
 // Activations of the prefill regime: pbase (E + 2 ints) <- the padded
 // 128-row blocks of each expert's rows (from counts), then x quantised into
 // its permuted rows (row_of [N, k], ids idx [N, k]) with its block scales by
@@ -279,12 +280,14 @@ size_t prefill_wscale_bytes(const Geo& g);                   // one launch's int
 cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* idx, const int* row_of,
                                 const int* counts, const int* offsets, int N, float gx, int* pbase,
                                 uint8_t* codes, uint8_t* scales, cudaStream_t st);
-// ev (may be null): 4 events around phase 1 and phase 2; wsf: prefill_wscale_bytes
+// ev (may be null): 4 events around phase 1 and phase 2; wsf: prefill_wscale_bytes,
+// wtag: prefill_wtag_ints (a buffer whose weights are those its scales were
+// laid out for, and that this step did not refill, keeps them)
 cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const StepRecord* rec,
                                  const int* offsets, const int* pbase, int N, int mode, int with_shared,
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales, uint8_t* wsf,
-                                 float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
+                                 int* wtag, float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
                                  const cudaEvent_t* ev);
 // h's block scales of the last prefill call back to rows [rows][f / block]
 cudaError_t launch_untile_hscales(const Geo& g, const uint8_t* tiled, const int* offsets, const int* pbase, int N,

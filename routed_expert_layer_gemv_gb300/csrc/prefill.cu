@@ -211,10 +211,17 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
 }
 
 // ---------------------------------------------------------------- step 2
+constexpr int kSharedKey = -2;   // weight key of the shared expert's buffer (never an expert's)
+
 __global__ void __launch_bounds__(1024)
 build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ offsets,
-                   const int* __restrict__ pbase, int E, int S, int X, int shb, int N, int k, int mode,
+                   const int* __restrict__ pbase, int E, int S, int X, int shb, int key0, int N, int k, int mode,
                    int with_shared, Tile* __restrict__ tiles, int* __restrict__ ents, int* __restrict__ n_tiles) {
+  // entries: buffer ents[i], then the key of its weights ekey[i] (key0 +
+  // expert; kSharedKey for the shared expert) and efresh[i] = 1 where the
+  // buffer was (re)filled by this step (a miss)
+  int* ekey = ents + (E + 1);
+  int* efresh = ekey + (E + 1);
   __shared__ int sh[33];
   __shared__ int carry;
   const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
@@ -228,7 +235,7 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
   const int* abuf = ae + 3 * E;
   for (int e0 = 0; e0 < n_ent; e0 += blockDim.x) {
     const int i = e0 + threadIdx.x;
-    int slot = -1, r0 = 0, nrows = 0, pb0 = 0;
+    int slot = -1, r0 = 0, nrows = 0, pb0 = 0, key = -1, fresh = 0;
     if (i < nr) {
       const int ex = ae[b + i], ls = as[b + i], bb = abuf[b + i];
       if (ex >= 0 && ex < E && ls >= 0 && ls < S && b + i - S < X && bb >= 0 && bb <= S + X && bb != S) {
@@ -236,14 +243,21 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
         r0 = offsets[ex];
         nrows = offsets[ex + 1] - r0;
         pb0 = pbase[ex];
+        key = key0 + ex;
+        fresh = b + i >= nh;
       }
     } else if (i < n_ent) {
       slot = shb;
       r0 = N * k;
       nrows = N;
       pb0 = pbase[E];
+      key = kSharedKey;
     }
-    if (i < n_ent) ents[i] = nrows > 0 ? slot : -1;
+    if (i < n_ent) {
+      ents[i] = nrows > 0 ? slot : -1;
+      ekey[i] = key;
+      efresh[i] = fresh;
+    }
     const int nt = (nrows + kTileRows - 1) / kTileRows;
     // block exclusive scan of nt
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -287,8 +301,8 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
   }
 }
 
-// Weight block scales of the launch's experts (entry i: pool buffer ents[i])
-// in the tcgen05.cp layout, entry-major: phase 1 first (per block q of 128
+// Weight block scales of the launch's experts in the tcgen05.cp layout, by
+// pool buffer (the scales of buffer b at wsf + b ent_bytes): phase 1 first (per block q of 128
 // gate rows and the same 128 up rows, per group g: the gate block's 512
 // bytes, then the up block's, K = d), then phase 2 (per block of 256 down
 // rows, per group: its two 128-row halves' 512 bytes, K = f).  CTA = one
@@ -298,15 +312,22 @@ build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ o
 // coalesced.
 __global__ void __launch_bounds__(256)
 interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size_t off_g, size_t off_u,
-                          size_t off_d, const int* __restrict__ ents, const int* __restrict__ n_tiles, int d,
-                          int f, int blk, uint8_t* __restrict__ wsf) {
+                          size_t off_d, const int* __restrict__ ents, const int* __restrict__ n_tiles, int E, int d,
+                          int f, int blk, uint8_t* __restrict__ wsf, int* __restrict__ wtag, int nb) {
   extern __shared__ uint32_t smw[];
   const int ent = blockIdx.y;
   if (ent >= n_tiles[1]) return;
   const int slot = ents[ent];
   if (slot < 0) return;
+  // wtag[b]: key of the weights whose scales wsf holds for buffer b (-1:
+  // none); wtag[nb + b]: CTAs of buffer b done in this launch.  A buffer that
+  // holds the same weights as when its scales were last laid out is skipped;
+  // the tag changes only once every CTA of the buffer has written its block,
+  // so all CTAs of one buffer take the same decision.
+  const int key = ents[(E + 1) + ent], fresh = ents[2 * (E + 1) + ent];
+  if (!fresh && key != -1 && wtag[slot] == key) return;
   const uint8_t* w = slots + (size_t)slot * ebytes;
-  uint8_t* out = wsf + (size_t)ent * (3 * (size_t)d * f / blk);
+  uint8_t* out = wsf + (size_t)slot * (3 * (size_t)d * f / blk);
   const int nb1 = 2 * (f / kTileRows);
   const int b = blockIdx.x;
   int K, hi, hh;
@@ -332,6 +353,15 @@ interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size
     const int i = v & 31, g = v >> 5;
     *reinterpret_cast<uint4*>(out + (((size_t)hi * ng + g) * 2 + hh) * 512 + 16 * i) =
         make_uint4(smw[i * ngp + g], smw[(32 + i) * ngp + g], smw[(64 + i) * ngp + g], smw[(96 + i) * ngp + g]);
+  }
+  // the buffer's last CTA records the key (and resets the count)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&wtag[nb + slot], 1) == (int)gridDim.x - 1) {
+      wtag[nb + slot] = 0;
+      wtag[slot] = key;
+    }
   }
 }
 
@@ -524,7 +554,7 @@ gemm_ws_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
             uint8_t* ss = sf_smem + (size_t)s * kSfStage;
             tc::bulk_load(ss, p.a_scales + ((size_t)tile.pb * ng + (size_t)kt * G) * 512, 512 * G, &full[s]);
             tc::bulk_load(ss + 512 * G,
-                          p.w_scales + (size_t)tile.ent * p.ent_bytes +
+                          p.w_scales + (size_t)tile.slot * p.ent_bytes +
                               ((size_t)(n0 / NCOL) * ng + (size_t)kt * G) * 512 * BA,
                           512 * G * BA, &full[s]);
           }
@@ -873,14 +903,20 @@ int prefill_max_tiles(const Geo& g, int N) {
   return (int)((rows + kTileRows - 1) / kTileRows + g.E + 1);
 }
 
+// Pool buffers that can hold an expert's weights: the pool's own count, at
+// least E + 1 (a resized lone layer stays within E + 1).
+static int wscale_entries(const Geo& g) { return std::max(g.nbuf, g.E + 1); }
+
 // Block scales of the activations (x or h, K = d or f) by padded 128-row block.
 size_t prefill_act_scale_bytes(const Geo& g, int N, int K) {
   return std::max<size_t>(16, (size_t)prefill_max_tiles(g, N) * kTileRows * fmt_scale_row(g.afmt, K));
 }
-// The interleaved weight scales of one launch: up to E + 1 entries.
+// The interleaved weight scales, one entry per pool buffer.
 size_t prefill_wscale_bytes(const Geo& g) {
-  return std::max<size_t>(16, (size_t)(g.E + 1) * 3 * fmt_scale_row(g.afmt, g.d) * (size_t)g.f);
+  return std::max<size_t>(16, (size_t)wscale_entries(g) * 3 * fmt_scale_row(g.afmt, g.d) * (size_t)g.f);
 }
+// Their tags and per-launch counts (ints; all tags -1 = nothing laid out).
+size_t prefill_wtag_ints(const Geo& g) { return 2 * (size_t)wscale_entries(g); }
 
 cudaError_t launch_untile_hscales(const Geo& g, const uint8_t* tiled, const int* offsets, const int* pbase, int N,
                                   uint8_t* out, cudaStream_t st) {
@@ -897,13 +933,13 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  const int* offsets, const int* pbase, int N, int mode, int with_shared,
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales, uint8_t* wsf,
-                                 float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
+                                 int* wtag, float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
                                  const cudaEvent_t* ev) {
   const int max_tiles = prefill_max_tiles(g, N);
   Tile* tl = static_cast<Tile*>(tiles);
   int* ents = reinterpret_cast<int*>(tl + max_tiles);
-  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, pbase, g.E, g.S, g.X, g.shb, N, g.k, mode, with_shared, tl,
-                                         ents, n_tiles);
+  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, pbase, g.E, g.S, g.X, g.shb, g.key0, N, g.k, mode,
+                                         with_shared, tl, ents, n_tiles);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int blk = fmt_block(g.afmt);   // scale block of both operands (W4A8: 32 on either side)
@@ -915,7 +951,8 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(2 * (g.f / kTileRows) + g.d / kTileRows), (unsigned)(g.E + 1));
     interleave_wscales_kernel<<<grid, 256, ismem, st>>>(slots, g.ebytes, g.off_scales[0], g.off_scales[1],
-                                                        g.off_scales[2], ents, n_tiles, g.d, g.f, blk, wsf);
+                                                        g.off_scales[2], ents, n_tiles, g.E, g.d, g.f, blk, wsf,
+                                                        wtag, wscale_entries(g));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -996,7 +1033,8 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
 }
 
 size_t prefill_tile_bytes(const Geo& g, int N) {
-  return (size_t)prefill_max_tiles(g, N) * sizeof(Tile) + (size_t)(g.E + 2) * sizeof(int);   // tiles, then entries
+  // tiles, then the entries' buffers, keys and refill flags
+  return (size_t)prefill_max_tiles(g, N) * sizeof(Tile) + (size_t)3 * (g.E + 2) * sizeof(int);
 }
 
 }  // namespace moe

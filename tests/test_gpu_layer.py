@@ -856,6 +856,47 @@ def test_prefill_with_misses_and_waves():
     L.close()
 
 
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+def test_prefill_scales_follow_buffer_contents(fmt):
+    # The prefill GEMM keeps each pool buffer's weight scales laid out from
+    # one call to the next while the buffer holds the same weights.  Between
+    # prefill calls the buffers change through decode misses (SM-copy and
+    # copy-engine fills), a resize and an install; every prefill call must
+    # still match the oracle.
+    spec = small_spec(E=24, k=3, d_model=512, d_ff=256, n_slots=6, has_shared=True, fmt=fmt)
+    seed, N = 41, 96
+    experts = CachedExperts(spec, seed)
+    L = build_layer(spec, seed, N, experts_fn=experts)
+    O = oracle_layer(spec, seed, experts)
+
+    def prefill(step):
+        x = _tokens(spec, seed + 100 + step, N)
+        y, _ = L.forward(bf16_tensor(x), regime=PRE)
+        ref, _, _ = O.forward(wl.bf16_bits_to_f64(x), "prefill")
+        assert_close_layer(y, ref, "%s prefill %d" % (fmt, step))
+
+    def decode(step, fill):
+        capi.moe_set_fill_mode(L.h, fill)
+        x = _tokens(spec, seed + 200 + step, 4)
+        y, info = L.forward(bf16_tensor(x), regime=DEC)
+        ref, _, _ = O.forward(wl.bf16_bits_to_f64(x), "decode")
+        assert_close_layer(y, ref, "%s decode %d" % (fmt, step))
+        return info.n_misses
+
+    prefill(0)
+    prefill(1)                                   # same buffers again
+    misses = decode(0, capi.MOE_FILL_KERNEL) + decode(1, capi.MOE_FILL_MEMCPY)
+    assert misses > 0
+    prefill(2)
+    capi.moe_cache_resize(L.h, 9)
+    prefill(3)
+    eo, _, _ = capi.moe_lru_get_state(L.h, 9)
+    absent = [e for e in range(spec.E) if e not in eo]
+    L.install(absent[0], 0)                      # slot 0's buffer gets other weights
+    prefill(4)
+    L.close()
+
+
 def test_prefill_deterministic_bitwise():
     spec = small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True)
     x = _tokens(spec, 29, 200)
