@@ -113,7 +113,7 @@ struct moe_layer {
   int* n_tiles = nullptr;
   PrefillPlan* plan = nullptr;
   GemvPlan* gplan = nullptr;
-  unsigned int* rcounter = nullptr;  // CTA counter of the one-launch router
+  unsigned int* rcounter = nullptr;  // CTA counters of the one-launch router (one per token tile)
   int* err_host = nullptr;       // kernels' timeout flag (mapped pinned memory)
   int* err_dev = nullptr;
   // host state
@@ -583,7 +583,7 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
   MOE_ALLOC(y_stage, Nm * g.d * 2);
   L->list_cap = (int)std::max<size_t>(Nm * g.k, (size_t)g.E);
   MOE_ALLOC(list_dev, (size_t)L->list_cap * 4);
-  MOE_ALLOC(rcounter, 16);
+  MOE_ALLOC(rcounter, kRouterCounterBytes);
   MOE_ALLOC(step_trace, (size_t)std::max(L->num_sms, 1) * kStepMarks * 8);
   if (prefill_ok) {
     // prefill activations in their format (the weights' own, or MXFP8 for
@@ -661,7 +661,7 @@ int create_layer(const moe_layer_desc* desc, moe_layer* base, int index, int n_l
            cudaMemset(L->expert_of, 0xff, (size_t)g.S * 4) == cudaSuccess &&
            cudaMemset(L->stamp, 0, (size_t)g.S * 8) == cudaSuccess &&
            cudaMemset(L->clock, 0, 8) == cudaSuccess &&
-           cudaMemset(L->rcounter, 0, 16) == cudaSuccess &&
+           cudaMemset(L->rcounter, 0, kRouterCounterBytes) == cudaSuccess &&
            forget_wscales(L, nullptr) == cudaSuccess;
       // slot s in buffer s; the spares after the shared expert's buffer S
       std::vector<int> b0(g.S + g.X);

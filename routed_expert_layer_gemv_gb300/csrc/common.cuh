@@ -183,7 +183,9 @@ __host__ __device__ inline void miss_chunk(int m, int c, int nch, int* lo, int* 
 
 // ---------------------------------------------------------------- launchers
 // router.cu
-// counter: a zeroed device word (enables the one-launch path for N <= 64), or null
+// counter: kRouterCounterBytes of zeroed device memory (one word per token
+// tile of the one-launch path for N <= 64), left zeroed
+constexpr size_t kRouterCounterBytes = 64;
 // Whl (may be null): W_r split into three bf16 parts [3][E][d]
 // (launch_router_split); with it, batches over 64 tokens take the tensor-core
 // logits kernel

@@ -30,8 +30,9 @@ using rt::topk_row;
 // warps splitting K, so each lane issues all of its W_r loads at once (2
 // float4 per lane for d = 2048) and the expert's dot products finish after
 // about one memory round trip; x comes straight from L2.  The 8 partial sums
-// of each logit are added in a fixed order.  The last CTA to finish runs the
-// top-k of every token (one launch for the whole routing).
+// of each logit are added in a fixed order.  The last of a token tile's E
+// CTAs to finish runs the top-k of the tile's tokens, one warp per token
+// (one launch for the whole routing; counter[y] counts tile y's CTAs).
 template <int TN>
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_dec_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
@@ -65,19 +66,19 @@ router_dec_kernel(const __nv_bfloat16* __restrict__ x, int N, int d, int E,
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned int n = atomicAdd(counter, 1u);
-    last = n == gridDim.x * gridDim.y - 1;
+    const unsigned int n = atomicAdd(counter + blockIdx.y, 1u);
+    last = n == gridDim.x - 1;
   }
   __syncthreads();
   if (last) {
     __threadfence();
     float* Ls = reinterpret_cast<float*>(smem_raw) + (size_t)warp * E;
-    for (int t = warp; t < N; t += kRouterWarps) {
+    for (int t = t0 + warp; t < t0 + nt; t += kRouterWarps) {
       stage_logits(logits, t, E, Ls);
       topk_row(Ls, E, k, norm_topk, idx + (size_t)t * k, gates + (size_t)t * k);
       __syncwarp();
     }
-    if (threadIdx.x == 0) *counter = 0u;
+    if (threadIdx.x == 0) counter[blockIdx.y] = 0u;
   }
 }
 
