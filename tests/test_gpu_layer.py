@@ -48,6 +48,11 @@ def _tokens(spec, seed, N):
     # a prefill-sized chunk through the decode regime: FP4 weights x bf16-class
     # activations (W4A16), the tensor-core router, three permutation launches
     (small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True), 300),
+    # many experts: the fused step at 512 (32 pairs), the chain beyond it, and
+    # the largest E and k the descriptor takes (1024, 32; the top-k scans)
+    (small_spec(E=512, k=16, d_model=256, d_ff=256, n_slots=512), 2),
+    (small_spec(E=512, k=16, d_model=256, d_ff=256, n_slots=512), 9),
+    (small_spec(E=1024, k=32, d_model=256, d_ff=256, n_slots=1024), 5),
 ])
 def test_forward_all_resident(spec, N):
     seed = 11
@@ -630,6 +635,11 @@ PRE = capi.MOE_REGIME_PREFILL
     # FP4 weights x FP8 activations (W4A8)
     (small_spec(E=16, k=4, d_model=512, d_ff=256, n_slots=16, has_shared=True, prefill_act="mxfp8"), 300),
     (small_spec(E=128, k=8, d_model=2048, d_ff=768, n_slots=128, prefill_act="mxfp8"), 256),
+    # degenerate and largest expert counts: E = 1 (dense SwiGLU), E = 512 and
+    # E = 1024 with k = 32 (the mma.sync router and the top-k scan above 256)
+    (small_spec(E=1, k=1, d_model=256, d_ff=256, n_slots=1), 130),
+    (small_spec(E=512, k=16, d_model=256, d_ff=256, n_slots=512), 200),
+    (small_spec(E=1024, k=32, d_model=256, d_ff=256, n_slots=1024), 130),
 ])
 def test_prefill_all_resident(spec, N):
     seed = 17
