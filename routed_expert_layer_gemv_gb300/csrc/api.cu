@@ -1212,16 +1212,16 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     L->launches += 1;
     if (L->ev_after_route) MOE_CUDA(L, cudaEventRecord(L->ev_after_route, st));
   } else {
+    // permutation (histograms; scan + the prefill's padded blocks + LRU step
+    // in one CTA; scatter of the rows)
     pe = prof_begin(L, MOE_PROF_PERMUTE, st);
-    MOE_CUDA(L, launch_permute(g, L->idx, N, L->counts, L->offsets, L->row_of, L->tok_of,
-                               L->perm_scratch, st));
+    MOE_CUDA(L, launch_perm_hist(g, L->idx, N, L->perm_scratch, st));
+    MOE_CUDA(L, launch_scan_lru(g, N, L->perm_scratch, L->counts, L->offsets, prefill ? L->pbase : nullptr,
+                                L->slot_of, L->expert_of, L->stamp, L->clock, L->buf, L->rec, L->stats, hrec, seq,
+                                st));
+    MOE_CUDA(L, launch_perm_scatter(g, L->idx, N, L->offsets, L->perm_scratch, L->row_of, L->tok_of, st));
     prof_end(pe, st);
     L->launches += 3;
-    pe = prof_begin(L, MOE_PROF_LRU, st);
-    MOE_CUDA(L, launch_lru_step(g, L->counts, L->offsets, L->slot_of, L->expert_of, L->stamp, L->clock,
-                                L->buf, L->rec, L->stats, hrec, seq, st));
-    prof_end(pe, st);
-    L->launches += 1;
     if (L->ev_after_route) MOE_CUDA(L, cudaEventRecord(L->ev_after_route, st));
   }
   const bool dev_fill = !resident && fmode == MOE_FILL_DEVICE;
@@ -1247,10 +1247,11 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   const float gh = g.fmt == MOE_NVFP4 ? L->desc.act_scale_h : 1.0f;
   if (prefill) {
     pe = prof_begin(L, MOE_PROF_PREFILL, st);
-    MOE_CUDA(L, launch_gather_quant(g, xd, L->idx, L->row_of, L->counts, L->offsets, N, gx, L->pbase, L->xq_codes,
-                                    L->xq_scales, st));
+    // the padded blocks came with the LRU step when N > 128
+    MOE_CUDA(L, launch_gather_quant(g, xd, L->idx, L->row_of, L->counts, L->offsets, N, gx, L->pbase, N > 128,
+                                    L->xq_codes, L->xq_scales, st));
     prof_end(pe, st);
-    L->launches += 2;
+    L->launches += N > 128 ? 1 : 2;
   }
   // SM fills (decode): kFillSms SMs copy the misses, the expert GEMV takes
   // the others, and the hits' phase 2 is launched after the host has read the

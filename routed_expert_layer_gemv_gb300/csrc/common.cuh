@@ -49,6 +49,7 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
+constexpr int kPrefillTileRows = 128;   // rows of one prefill GEMM tile (its MMA M): the padded-block unit
 constexpr int kWarp = 32;
 
 // ---------------------------------------------------------------- formats
@@ -209,6 +210,12 @@ cudaError_t launch_router_split(const Geo& g, const float* Wr, __nv_bfloat16* Wh
 size_t permute_scratch_bytes(const Geo& g, int max_tokens);
 cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int* offsets,
                            int* row_of, int* tok_of, void* scratch, cudaStream_t st);
+// its first and last launches for N > 128 (block histograms and in-block
+// ranks into scratch; rows from them and the offsets), for a caller that
+// runs the scan itself (launch_scan_lru)
+cudaError_t launch_perm_hist(const Geo& g, const int* idx, int N, void* scratch, cudaStream_t st);
+cudaError_t launch_perm_scatter(const Geo& g, const int* idx, int N, const int* offsets, void* scratch,
+                                int* row_of, int* tok_of, cudaStream_t st);
 // lru.cu
 // stats (may be null): steps, distinct experts, hits, misses, accumulated
 // offsets (may be null: entries then get no rows) = the permutation's
@@ -218,6 +225,13 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
 // buf: the slot -> buffer map and spare list (S + X ints, updated in place)
 cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets, int* slot_of,
                             int* expert_of, unsigned long long* stamp, unsigned long long* clock,
+                            int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                            unsigned long long seq, cudaStream_t st);
+// N > 128: the permutation's scan (after launch_perm_hist), the prefill's
+// padded blocks (pbase, may be null: E + 2 ints, as launch_gather_quant
+// writes them) and the LRU step, in one launch
+cudaError_t launch_scan_lru(const Geo& g, int N, void* perm_scratch, int* counts, int* offsets, int* pbase,
+                            int* slot_of, int* expert_of, unsigned long long* stamp, unsigned long long* clock,
                             int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
                             unsigned long long seq, cudaStream_t st);
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
@@ -281,7 +295,7 @@ size_t prefill_wtag_ints(const Geo& g);                      // their tags (ints
 // padded block (the tcgen05.cp layout)
 cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* idx, const int* row_of,
                                 const int* counts, const int* offsets, int N, float gx, int* pbase,
-                                uint8_t* codes, uint8_t* scales, cudaStream_t st);
+                                bool pbase_ready, uint8_t* codes, uint8_t* scales, cudaStream_t st);
 // ev (may be null): 4 events around phase 1 and phase 2; wsf: prefill_wscale_bytes,
 // wtag: prefill_wtag_ints (a buffer whose weights are those its scales were
 // laid out for, and that this step did not refill, keeps them)

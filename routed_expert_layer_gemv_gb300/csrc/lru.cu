@@ -46,6 +46,37 @@ lru_step_kernel(const int* __restrict__ counts, const int* __restrict__ offsets,
                              rec, stats, host_rec, seq, m);
 }
 
+// Middle of the routing tail of large batches (N > 128), one CTA: the scan
+// of the permutation's block histograms (counts, offsets), the padded
+// 128-row blocks of each expert's rows for the prefill GEMM (pbase, when
+// given: expert e's first block, pbase[E] the shared expert's, pbase[E + 1]
+// the total), then the LRU step on the counts.  The scatter of the rows
+// follows in its own launch.
+__global__ void __launch_bounds__(kLruThreads)
+scan_lru_kernel(int* __restrict__ hist, int nblk, int E, int S, int X, int key0, int keys, int* __restrict__ counts,
+                int* __restrict__ offsets, int* __restrict__ pbase, int N, int with_shared,
+                int* __restrict__ slot_of, int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
+                unsigned long long* __restrict__ clock, int* __restrict__ buf, StepRecord* __restrict__ rec,
+                unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq) {
+  __shared__ LruSmem m;
+  const LruRegs lr = lru_load(E, S, X, key0, slot_of, expert_of, stamp, clock, buf);
+  const int c = perm::scan_hist(hist, nblk, E, counts, offsets, m.sh);
+  if (pbase != nullptr) {
+    const int e = threadIdx.x;
+    int total;
+    const int pre = perm::block_excl_scan(e < E ? (c + kPrefillTileRows - 1) / kPrefillTileRows : 0, &total, m.sh);
+    if (e < E) pbase[e] = pre;
+    if (e == 0) {
+      pbase[E] = total;
+      pbase[E + 1] = total + (with_shared ? (N + kPrefillTileRows - 1) / kPrefillTileRows : 0);
+    }
+  }
+  lru_park(lr, E, S, X, m);
+  __syncthreads();   // counts and offsets (global, this CTA's writes) are visible to every thread
+  lru::lru_body<kLruThreads>(counts, offsets, nullptr, E, S, X, key0, keys, slot_of, expert_of, stamp, clock, buf,
+                             rec, stats, host_rec, seq, m);
+}
+
 // Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
 // (as perm_single in permute.cu), then the LRU step on the counts it found.
 __global__ void __launch_bounds__(kLruThreads)
@@ -144,6 +175,17 @@ cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets,
                             unsigned long long seq, cudaStream_t st) {
   lru_step_kernel<<<1, kLruThreads, 0, st>>>(counts, offsets, g.E, g.S, g.X, g.key0, g.keys, slot_of, expert_of,
                                              stamp, clock, buf, rec, stats, host_rec, seq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan_lru(const Geo& g, int N, void* perm_scratch, int* counts, int* offsets, int* pbase,
+                            int* slot_of, int* expert_of, unsigned long long* stamp, unsigned long long* clock,
+                            int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
+                            unsigned long long seq, cudaStream_t st) {
+  const int nblk = (N + perm::kTokPerBlock - 1) / perm::kTokPerBlock;
+  scan_lru_kernel<<<1, kLruThreads, 0, st>>>(static_cast<int*>(perm_scratch), nblk, g.E, g.S, g.X, g.key0, g.keys,
+                                             counts, offsets, pbase, N, g.has_shared, slot_of, expert_of, stamp,
+                                             clock, buf, rec, stats, host_rec, seq);
   return cudaGetLastError();
 }
 

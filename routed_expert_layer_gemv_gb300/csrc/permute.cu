@@ -54,28 +54,7 @@ __global__ void __launch_bounds__(1024)
 perm_scan_kernel(int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
                  int* __restrict__ offsets) {
   __shared__ int sh[33];
-  const int e = threadIdx.x;
-  int tot = 0;
-  if (e < E) {
-    // exclusive prefix over blocks, 16 loads in flight at a time
-    for (int b0 = 0; b0 < nblk; b0 += 16) {
-      int c[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) c[i] = b0 + i < nblk ? hist[(size_t)(b0 + i) * E + e] : 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (b0 + i < nblk) hist[(size_t)(b0 + i) * E + e] = tot;
-        tot += c[i];
-      }
-    }
-  }
-  int all;
-  int off = block_excl_scan(e < E ? tot : 0, &all, sh);
-  if (e < E) {
-    counts[e] = tot;
-    offsets[e] = off;
-  }
-  if (e == 0) offsets[E] = all;
+  perm::scan_hist(hist, nblk, E, counts, offsets, sh);
 }
 
 // Step 3: rows.
@@ -162,18 +141,31 @@ cudaError_t launch_permute(const Geo& g, const int* idx, int N, int* counts, int
     return cudaGetLastError();
   }
   const int nblk = (N + kTokPerBlock - 1) / kTokPerBlock;
+  cudaError_t err = launch_perm_hist(g, idx, N, scratch, st);
+  if (err != cudaSuccess) return err;
+  perm_scan_kernel<<<1, 1024, 0, st>>>(static_cast<int*>(scratch), nblk, g.E, counts, offsets);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  return launch_perm_scatter(g, idx, N, offsets, scratch, row_of, tok_of, st);
+}
+
+cudaError_t launch_perm_hist(const Geo& g, const int* idx, int N, void* scratch, cudaStream_t st) {
+  const int nblk = (N + kTokPerBlock - 1) / kTokPerBlock;
   int* hist = static_cast<int*>(scratch);
   int* rank = hist + (size_t)nblk * g.E;
   perm_hist_kernel<<<nblk, kTokPerBlock, (size_t)g.E * kPermWarps * 4 + (size_t)kTokPerBlock * g.k * 4 +
                                           (size_t)kTokPerBlock * ((g.E + 31) / 32) * 4,
                      st>>>(idx, N, g.k, g.E, hist, rank);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  perm_scan_kernel<<<1, 1024, 0, st>>>(hist, nblk, g.E, counts, offsets);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  perm_scatter_kernel<<<(N * g.k + 255) / 256, 256, 0, st>>>(idx, N, g.k, g.E, hist, rank, offsets,
-                                                            row_of, tok_of);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_perm_scatter(const Geo& g, const int* idx, int N, const int* offsets, void* scratch,
+                                int* row_of, int* tok_of, cudaStream_t st) {
+  const int nblk = (N + kTokPerBlock - 1) / kTokPerBlock;
+  const int* hist = static_cast<const int*>(scratch);
+  const int* rank = hist + (size_t)nblk * g.E;
+  perm_scatter_kernel<<<(N * g.k + 255) / 256, 256, 0, st>>>(idx, N, g.k, g.E, hist, rank, offsets, row_of,
+                                                            tok_of);
   return cudaGetLastError();
 }
 

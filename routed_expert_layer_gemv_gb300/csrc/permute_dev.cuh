@@ -95,5 +95,36 @@ MOE_DEV int block_excl_scan(int v, int* total, int* sh) {
   return res;
 }
 
+// Thread e (< E) of a CTA of >= E threads: the block histograms hist[b][e]
+// (nblk blocks) become their exclusive prefixes over b, counts[e] gets the
+// expert's total and offsets the exclusive prefix over e (offsets[E]: all
+// rows).  Returns thread e's count (0 for e >= E).  sh: >= 33 ints.
+MOE_DEV int scan_hist(int* __restrict__ hist, int nblk, int E, int* __restrict__ counts, int* __restrict__ offsets,
+                      int* sh) {
+  const int e = threadIdx.x;
+  int tot = 0;
+  if (e < E) {
+    // exclusive prefix over blocks, 16 loads in flight at a time
+    for (int b0 = 0; b0 < nblk; b0 += 16) {
+      int c[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c[i] = b0 + i < nblk ? hist[(size_t)(b0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (b0 + i < nblk) hist[(size_t)(b0 + i) * E + e] = tot;
+        tot += c[i];
+      }
+    }
+  }
+  int all;
+  const int off = block_excl_scan(e < E ? tot : 0, &all, sh);
+  if (e < E) {
+    counts[e] = tot;
+    offsets[e] = off;
+  }
+  if (e == 0) offsets[E] = all;
+  return tot;
+}
+
 }  // namespace perm
 }  // namespace moe

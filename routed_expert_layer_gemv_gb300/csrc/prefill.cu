@@ -34,7 +34,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTileRows = 128;          // M of one MMA tile, rows of one TMA box
+constexpr int kTileRows = kPrefillTileRows;   // M of one MMA tile, rows of one TMA box
 
 // Kernel variant of W4A8: MXFP4 weights under MXFP8 activations.  The MMA is
 // kind::mxf8f6f4 with E4M3 A and E2M1 B; the FP4 weight tiles are loaded by
@@ -886,12 +886,14 @@ bool prefill_plan_ready(const PrefillPlan* pl) { return pl && pl->ready; }
 
 cudaError_t launch_gather_quant(const Geo& g, const __nv_bfloat16* x, const int* idx, const int* row_of,
                                 const int* counts, const int* offsets, int N, float gx, int* pbase,
-                                uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+                                bool pbase_ready, uint8_t* codes, uint8_t* scales, cudaStream_t st) {
   const size_t total = (size_t)N * (g.d / 32);
   if (total == 0) return cudaSuccess;
-  pad_base_kernel<<<1, 1024, 0, st>>>(counts, g.E, N, g.has_shared, pbase);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (!pbase_ready) {
+    pad_base_kernel<<<1, 1024, 0, st>>>(counts, g.E, N, g.has_shared, pbase);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   gather_quant_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(x, idx, row_of, offsets, pbase, N, g.k,
                                                                       g.E, g.d, g.afmt, gx, g.has_shared,
                                                                       codes, scales);
