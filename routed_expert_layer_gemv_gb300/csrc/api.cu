@@ -1201,6 +1201,7 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
   const bool fused = !resident && !prefill && fmode == MOE_FILL_FUSED;
   const bool host_poll = !resident && fmode != MOE_FILL_DEVICE && !fused;
   StepRecord* hrec = host_poll ? L->rec_host_dev : nullptr;
+  bool tiles_built = false;   // the prefill tiles of the hits came with the routing (N > 128)
   const unsigned long long seq = host_poll ? ++L->step_seq : 0ull;
   if (N <= 128) {
     // permutation and LRU step in one CTA
@@ -1218,7 +1219,8 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     MOE_CUDA(L, launch_perm_hist(g, L->idx, N, L->perm_scratch, st));
     MOE_CUDA(L, launch_scan_lru(g, N, L->perm_scratch, L->counts, L->offsets, prefill ? L->pbase : nullptr,
                                 L->slot_of, L->expert_of, L->stamp, L->clock, L->buf, L->rec, L->stats, hrec, seq,
-                                st));
+                                prefill ? L->tiles : nullptr, L->n_tiles, st));
+    tiles_built = prefill;
     MOE_CUDA(L, launch_perm_scatter(g, L->idx, N, L->offsets, L->perm_scratch, L->row_of, L->tok_of, st));
     prof_end(pe, st);
     L->launches += 3;
@@ -1271,11 +1273,15 @@ int moe_forward(moe_layer_t L, const void* x, int N, void* y, void* stream, int 
     }
     cudaError_t ce;
     if (prefill) {
+      // the first range (the hits and the shared expert) may come with its
+      // tiles already built by the routing CTA
+      const bool ready = tiles_built && a.mode == kRangeHits && a.with_shared == g.has_shared;
+      tiles_built = false;
       ce = launch_prefill_gemms(g, L->plan, L->rec, L->offsets, L->pbase, N, a.mode, a.with_shared,
                                 L->tiles, L->n_tiles, L->slots, L->xq_scales, L->hq_codes,
                                 L->hq_scales, L->wsf, L->wtag, L->O, gx, gh, L->err_dev,
-                                L->gemm_sms > 0 ? L->gemm_sms : L->num_sms, st, evp);
-      L->launches += fmt_block(g.afmt) ? 4 : 3;
+                                L->gemm_sms > 0 ? L->gemm_sms : L->num_sms, st, evp, ready);
+      L->launches += (fmt_block(g.afmt) ? 4 : 3) - (ready ? 1 : 0);
     } else {
       ce = launch_gemv_decode(g, L->gplan, a, xd, L->xexp, L->h, L->O, n_ent, gemv_sms, st, evp, phases);
       L->launches += (phases & 1) + (phases >> 1 & 1);

@@ -229,11 +229,14 @@ cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets,
                             unsigned long long seq, cudaStream_t st);
 // N > 128: the permutation's scan (after launch_perm_hist), the prefill's
 // padded blocks (pbase, may be null: E + 2 ints, as launch_gather_quant
-// writes them) and the LRU step, in one launch
+// writes them) and the LRU step, in one launch; with pbase and tiles (the
+// prefill tile workspace, prefill_tile_bytes; n_tiles its counts) also the
+// tile list of the step's hits and shared expert, as launch_prefill_gemms
+// builds it for its first range
 cudaError_t launch_scan_lru(const Geo& g, int N, void* perm_scratch, int* counts, int* offsets, int* pbase,
                             int* slot_of, int* expert_of, unsigned long long* stamp, unsigned long long* clock,
                             int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
-                            unsigned long long seq, cudaStream_t st);
+                            unsigned long long seq, void* tiles, int* n_tiles, cudaStream_t st);
 cudaError_t launch_lru_install(const Geo& g, int expert, int slot, int* slot_of, int* expert_of,
                                unsigned long long* stamp, unsigned long long* clock,
                                cudaStream_t st);
@@ -286,6 +289,7 @@ PrefillPlan* prefill_plan_create(const Geo& g, const uint8_t* slots, const uint8
 void prefill_plan_destroy(PrefillPlan* pl);
 bool prefill_plan_ready(const PrefillPlan* pl);
 size_t prefill_tile_bytes(const Geo& g, int N);            // tiles, then the launch's entries
+int prefill_max_tiles(const Geo& g, int N);                // tiles of one launch at most (its entries follow)
 size_t prefill_act_scale_bytes(const Geo& g, int N, int K);  // x (K = d) or h (K = f) block scales
 size_t prefill_wscale_bytes(const Geo& g);                   // interleaved weight scales, per pool buffer
 size_t prefill_wtag_ints(const Geo& g);                      // their tags (ints, -1 = none) and counts (0)
@@ -304,7 +308,7 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales, uint8_t* wsf,
                                  int* wtag, float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
-                                 const cudaEvent_t* ev);
+                                 const cudaEvent_t* ev, bool tiles_ready = false);
 // h's block scales of the last prefill call back to rows [rows][f / block]
 cudaError_t launch_untile_hscales(const Geo& g, const uint8_t* tiled, const int* offsets, const int* pbase, int N,
                                   uint8_t* out, cudaStream_t st);

@@ -23,6 +23,7 @@
 #include "common.cuh"
 #include "lru_dev.cuh"
 #include "permute_dev.cuh"
+#include "tiles_dev.cuh"
 
 namespace moe {
 
@@ -50,15 +51,18 @@ lru_step_kernel(const int* __restrict__ counts, const int* __restrict__ offsets,
 // of the permutation's block histograms (counts, offsets), the padded
 // 128-row blocks of each expert's rows for the prefill GEMM (pbase, when
 // given: expert e's first block, pbase[E] the shared expert's, pbase[E + 1]
-// the total), then the LRU step on the counts.  The scatter of the rows
-// follows in its own launch.
+// the total), then the LRU step on the counts, then (tiles given) the
+// prefill GEMM's tile list of the step's hits and the shared expert.  The
+// scatter of the rows follows in its own launch.
 __global__ void __launch_bounds__(kLruThreads)
 scan_lru_kernel(int* __restrict__ hist, int nblk, int E, int S, int X, int key0, int keys, int* __restrict__ counts,
-                int* __restrict__ offsets, int* __restrict__ pbase, int N, int with_shared,
+                int* __restrict__ offsets, int* __restrict__ pbase, int N, int k, int with_shared, int shb,
                 int* __restrict__ slot_of, int* __restrict__ expert_of, unsigned long long* __restrict__ stamp,
                 unsigned long long* __restrict__ clock, int* __restrict__ buf, StepRecord* __restrict__ rec,
-                unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq) {
+                unsigned long long* __restrict__ stats, StepRecord* host_rec, unsigned long long seq,
+                tl::Tile* __restrict__ tiles, int* __restrict__ ents, int* __restrict__ n_tiles) {
   __shared__ LruSmem m;
+  __shared__ int carry;
   const LruRegs lr = lru_load(E, S, X, key0, slot_of, expert_of, stamp, clock, buf);
   const int c = perm::scan_hist(hist, nblk, E, counts, offsets, m.sh);
   if (pbase != nullptr) {
@@ -75,6 +79,11 @@ scan_lru_kernel(int* __restrict__ hist, int nblk, int E, int S, int X, int key0,
   __syncthreads();   // counts and offsets (global, this CTA's writes) are visible to every thread
   lru::lru_body<kLruThreads>(counts, offsets, nullptr, E, S, X, key0, keys, slot_of, expert_of, stamp, clock, buf,
                              rec, stats, host_rec, seq, m);
+  if (tiles != nullptr && pbase != nullptr) {
+    __syncthreads();   // the record (global, this CTA's writes) is visible to every thread
+    tl::build_tiles(rec, offsets, pbase, E, S, X, shb, key0, N, k, kRangeHits, with_shared, tiles, ents, n_tiles,
+                    m.sh, &carry);
+  }
 }
 
 // Decode routing tail in one CTA (N <= 128): the permutation of the top-k ids
@@ -181,11 +190,13 @@ cudaError_t launch_lru_step(const Geo& g, const int* counts, const int* offsets,
 cudaError_t launch_scan_lru(const Geo& g, int N, void* perm_scratch, int* counts, int* offsets, int* pbase,
                             int* slot_of, int* expert_of, unsigned long long* stamp, unsigned long long* clock,
                             int* buf, StepRecord* rec, unsigned long long* stats, StepRecord* host_rec,
-                            unsigned long long seq, cudaStream_t st) {
+                            unsigned long long seq, void* tiles, int* n_tiles, cudaStream_t st) {
   const int nblk = (N + perm::kTokPerBlock - 1) / perm::kTokPerBlock;
+  tl::Tile* tp = static_cast<tl::Tile*>(tiles);
+  int* ents = tp ? reinterpret_cast<int*>(tp + prefill_max_tiles(g, N)) : nullptr;
   scan_lru_kernel<<<1, kLruThreads, 0, st>>>(static_cast<int*>(perm_scratch), nblk, g.E, g.S, g.X, g.key0, g.keys,
-                                             counts, offsets, pbase, N, g.has_shared, slot_of, expert_of, stamp,
-                                             clock, buf, rec, stats, host_rec, seq);
+                                             counts, offsets, pbase, N, g.k, g.has_shared, g.shb, slot_of, expert_of,
+                                             stamp, clock, buf, rec, stats, host_rec, seq, tp, ents, n_tiles);
   return cudaGetLastError();
 }
 

@@ -29,12 +29,15 @@
 #include "actquant.cuh"
 #include "common.cuh"
 #include "tc.cuh"
+#include "tiles_dev.cuh"
 
 namespace moe {
 
 namespace {
 
 constexpr int kTileRows = kPrefillTileRows;   // M of one MMA tile, rows of one TMA box
+using tl::Tile;
+using tl::kSharedKey;
 
 // Kernel variant of W4A8: MXFP4 weights under MXFP8 activations.  The MMA is
 // kind::mxf8f6f4 with E4M3 A and E2M1 B; the FP4 weight tiles are loaded by
@@ -46,15 +49,6 @@ constexpr int kW4A8 = 100;
 __host__ __device__ constexpr int act_op_fmt(int F) { return F == kW4A8 ? MOE_MXFP8 : F; }
 constexpr int kKTileBytes = 128;        // 256 FP4 codes per K tile
 constexpr int kOpBytes = kTileRows * kKTileBytes;   // 16 KB per 128-row operand box
-
-struct Tile {
-  int slot;       // pool buffer of the expert (Geo::shb: the shared expert)
-  int row_start;  // first permuted row of the tile
-  int row_end;    // one past the expert's last row
-  int pb;         // padded 128-row block of the tile's activation scales
-  int ent;        // the expert's entry in the launch (its interleaved weight scales)
-  int pad[3];
-};
 
 // Block scales in the layout tcgen05.cp copies into TMEM (32x128b, one copy
 // per lane quarter): per 128-row block and per group of 4 scale bytes along
@@ -211,105 +205,28 @@ __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, const i
 }
 
 // ---------------------------------------------------------------- step 2
-constexpr int kSharedKey = -2;   // weight key of the shared expert's buffer (never an expert's)
-
 __global__ void __launch_bounds__(1024)
 build_tiles_kernel(const StepRecord* __restrict__ rec, const int* __restrict__ offsets,
                    const int* __restrict__ pbase, int E, int S, int X, int shb, int key0, int N, int k, int mode,
                    int with_shared, Tile* __restrict__ tiles, int* __restrict__ ents, int* __restrict__ n_tiles) {
-  // entries: buffer ents[i], then the key of its weights ekey[i] (key0 +
-  // expert; kSharedKey for the shared expert) and efresh[i] = 1 where the
-  // buffer was (re)filled by this step (a miss)
-  int* ekey = ents + (E + 1);
-  int* efresh = ekey + (E + 1);
   __shared__ int sh[33];
   __shared__ int carry;
-  const int U = min(max(rec->U, 0), E), nh = min(max(rec->n_hit, 0), U);
-  const int b = mode == kRangeHits ? 0 : nh, e = mode == kRangeHits ? nh : U;
-  const int nr = max(0, e - b);
-  const int n_ent = nr + (with_shared ? 1 : 0);
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  const int* ae = reinterpret_cast<const int*>(rec + 1);
-  const int* as = ae + E;
-  const int* abuf = ae + 3 * E;
-  for (int e0 = 0; e0 < n_ent; e0 += blockDim.x) {
-    const int i = e0 + threadIdx.x;
-    int slot = -1, r0 = 0, nrows = 0, pb0 = 0, key = -1, fresh = 0;
-    if (i < nr) {
-      const int ex = ae[b + i], ls = as[b + i], bb = abuf[b + i];
-      if (ex >= 0 && ex < E && ls >= 0 && ls < S && b + i - S < X && bb >= 0 && bb <= S + X && bb != S) {
-        slot = bb;
-        r0 = offsets[ex];
-        nrows = offsets[ex + 1] - r0;
-        pb0 = pbase[ex];
-        key = key0 + ex;
-        fresh = b + i >= nh;
-      }
-    } else if (i < n_ent) {
-      slot = shb;
-      r0 = N * k;
-      nrows = N;
-      pb0 = pbase[E];
-      key = kSharedKey;
-    }
-    if (i < n_ent) {
-      ents[i] = nrows > 0 ? slot : -1;
-      ekey[i] = key;
-      efresh[i] = fresh;
-    }
-    const int nt = (nrows + kTileRows - 1) / kTileRows;
-    // block exclusive scan of nt
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int inc = nt;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += u;
-    }
-    if (lane == 31) sh[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-      const int nw = blockDim.x >> 5;
-      const int s = lane < nw ? sh[lane] : 0;
-      int si = s;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, si, o);
-        if (lane >= o) si += u;
-      }
-      if (lane < nw) sh[lane] = si - s;
-      if (lane == 31) sh[32] = si;
-    }
-    __syncthreads();
-    const int base = carry + sh[warp] + inc - nt;
-    for (int t = 0; t < nt; ++t) {
-      Tile tl;
-      tl.slot = slot;
-      tl.row_start = r0 + t * kTileRows;
-      tl.row_end = r0 + nrows;
-      tl.pb = pb0 + t;
-      tl.ent = i;
-      tl.pad[0] = tl.pad[1] = tl.pad[2] = 0;
-      tiles[base + t] = tl;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) carry += sh[32];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    n_tiles[0] = carry;
-    n_tiles[1] = n_ent;
-  }
+  tl::build_tiles(rec, offsets, pbase, E, S, X, shb, key0, N, k, mode, with_shared, tiles, ents, n_tiles, sh,
+                  &carry);
 }
 
 // Weight block scales of the launch's experts in the tcgen05.cp layout, by
-// pool buffer (the scales of buffer b at wsf + b ent_bytes): phase 1 first (per block q of 128
-// gate rows and the same 128 up rows, per group g: the gate block's 512
-// bytes, then the up block's, K = d), then phase 2 (per block of 256 down
-// rows, per group: its two 128-row halves' 512 bytes, K = f).  CTA = one
-// 128-row block of one matrix (blockIdx.x: phase 1's (q, gate / up) blocks,
-// then the down matrix's), staged through shared memory (rows padded to an
-// odd word count) so that both the row reads and the 16-byte writes are
-// coalesced.
+// pool buffer (the scales of buffer b at wsf + b ent_bytes): phase 1 first
+// (per block q of 128 gate rows and the same 128 up rows, per group g: the
+// gate block's 512 bytes, then the up block's, K = d), then phase 2 (per
+// block of 256 down rows, per group: its two 128-row halves' 512 bytes,
+// K = f).  A block is 128 rows of one matrix (phase 1's (q, gate / up)
+// blocks, then the down matrix's), staged through shared memory (rows padded
+// to an odd word count) so that both the row reads and the 16-byte writes are
+// coalesced; a CTA takes kIlvBlocks consecutive blocks of one buffer
+// (blockIdx.y: the launch entry).
+constexpr int kIlvBlocks = 4;
+
 __global__ void __launch_bounds__(256)
 interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size_t off_g, size_t off_u,
                           size_t off_d, const int* __restrict__ ents, const int* __restrict__ n_tiles, int E, int d,
@@ -322,37 +239,39 @@ interleave_wscales_kernel(const uint8_t* __restrict__ slots, size_t ebytes, size
   // wtag[b]: key of the weights whose scales wsf holds for buffer b (-1:
   // none); wtag[nb + b]: CTAs of buffer b done in this launch.  A buffer that
   // holds the same weights as when its scales were last laid out is skipped;
-  // the tag changes only once every CTA of the buffer has written its block,
+  // the tag changes only once every CTA of the buffer has written its blocks,
   // so all CTAs of one buffer take the same decision.
   const int key = ents[(E + 1) + ent], fresh = ents[2 * (E + 1) + ent];
   if (!fresh && key != -1 && wtag[slot] == key) return;
   const uint8_t* w = slots + (size_t)slot * ebytes;
-  uint8_t* out = wsf + (size_t)slot * (3 * (size_t)d * f / blk);
-  const int nb1 = 2 * (f / kTileRows);
-  const int b = blockIdx.x;
-  int K, hi, hh;
-  const uint8_t* src;
-  if (b < nb1) {
-    hi = b >> 1;
-    hh = b & 1;
-    K = d;
-    src = w + (hh ? off_u : off_g) + (size_t)kTileRows * hi * (K / blk);
-  } else {
-    const int rb = b - nb1;   // 128-row block of the down matrix
-    hi = rb >> 1;
-    hh = rb & 1;
-    K = f;
-    src = w + off_d + (size_t)kTileRows * rb * (K / blk);
-    out += 2 * (size_t)d * f / blk;
-  }
-  const int ng = K / blk / 4, ngp = ng | 1;   // words per row, padded to odd
-  const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
-  for (int v = threadIdx.x; v < kTileRows * ng; v += blockDim.x) smw[(v / ng) * ngp + v % ng] = s4[v];
-  __syncthreads();
-  for (int v = threadIdx.x; v < ng * 32; v += blockDim.x) {
-    const int i = v & 31, g = v >> 5;
-    *reinterpret_cast<uint4*>(out + (((size_t)hi * ng + g) * 2 + hh) * 512 + 16 * i) =
-        make_uint4(smw[i * ngp + g], smw[(32 + i) * ngp + g], smw[(64 + i) * ngp + g], smw[(96 + i) * ngp + g]);
+  const int nb1 = 2 * (f / kTileRows), nblk = nb1 + d / kTileRows;
+  for (int b = blockIdx.x * kIlvBlocks; b < min(nblk, (int)(blockIdx.x + 1) * kIlvBlocks); ++b) {
+    uint8_t* out = wsf + (size_t)slot * (3 * (size_t)d * f / blk);
+    int K, hi, hh;
+    const uint8_t* src;
+    if (b < nb1) {
+      hi = b >> 1;
+      hh = b & 1;
+      K = d;
+      src = w + (hh ? off_u : off_g) + (size_t)kTileRows * hi * (K / blk);
+    } else {
+      const int rb = b - nb1;   // 128-row block of the down matrix
+      hi = rb >> 1;
+      hh = rb & 1;
+      K = f;
+      src = w + off_d + (size_t)kTileRows * rb * (K / blk);
+      out += 2 * (size_t)d * f / blk;
+    }
+    const int ng = K / blk / 4, ngp = ng | 1;   // words per row, padded to odd
+    const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
+    __syncthreads();   // the previous block's reads of smw are done
+    for (int v = threadIdx.x; v < kTileRows * ng; v += blockDim.x) smw[(v / ng) * ngp + v % ng] = s4[v];
+    __syncthreads();
+    for (int v = threadIdx.x; v < ng * 32; v += blockDim.x) {
+      const int i = v & 31, g = v >> 5;
+      *reinterpret_cast<uint4*>(out + (((size_t)hi * ng + g) * 2 + hh) * 512 + 16 * i) =
+          make_uint4(smw[i * ngp + g], smw[(32 + i) * ngp + g], smw[(64 + i) * ngp + g], smw[(96 + i) * ngp + g]);
+    }
   }
   // the buffer's last CTA records the key (and resets the count)
   __syncthreads();
@@ -936,14 +855,17 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
                                  void* tiles, int* n_tiles, const uint8_t* slots,
                                  const uint8_t* xq_scales, uint8_t* hq_codes, uint8_t* hq_scales, uint8_t* wsf,
                                  int* wtag, float* O, float gx, float gh, int* err, int num_sms, cudaStream_t st,
-                                 const cudaEvent_t* ev) {
+                                 const cudaEvent_t* ev, bool tiles_ready) {
   const int max_tiles = prefill_max_tiles(g, N);
   Tile* tl = static_cast<Tile*>(tiles);
   int* ents = reinterpret_cast<int*>(tl + max_tiles);
-  build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, pbase, g.E, g.S, g.X, g.shb, g.key0, N, g.k, mode,
-                                         with_shared, tl, ents, n_tiles);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!tiles_ready) {   // (else built by the routing CTA: launch_scan_lru)
+    build_tiles_kernel<<<1, 1024, 0, st>>>(rec, offsets, pbase, g.E, g.S, g.X, g.shb, g.key0, N, g.k, mode,
+                                           with_shared, tl, ents, n_tiles);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const int blk = fmt_block(g.afmt);   // scale block of both operands (W4A8: 32 on either side)
   const size_t ent_bytes = blk ? 3 * (size_t)g.d * g.f / blk : 0;
   if (blk) {
@@ -951,7 +873,8 @@ cudaError_t launch_prefill_gemms(const Geo& g, const PrefillPlan* pl, const Step
     const int ismem = kTileRows * ngp_max * 4;
     e = ensure_smem_limit((const void*)interleave_wscales_kernel, ismem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(2 * (g.f / kTileRows) + g.d / kTileRows), (unsigned)(g.E + 1));
+    const int nblk = 2 * (g.f / kTileRows) + g.d / kTileRows;
+    const dim3 grid((unsigned)((nblk + kIlvBlocks - 1) / kIlvBlocks), (unsigned)(g.E + 1));
     interleave_wscales_kernel<<<grid, 256, ismem, st>>>(slots, g.ebytes, g.off_scales[0], g.off_scales[1],
                                                         g.off_scales[2], ents, n_tiles, g.E, g.d, g.f, blk, wsf,
                                                         wtag, wscale_entries(g));
