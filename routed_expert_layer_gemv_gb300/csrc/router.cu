@@ -294,7 +294,8 @@ cudaError_t launch_router(const Geo& g, const __nv_bfloat16* x, int N, const flo
     return cudaGetLastError();
   }
   // decode sizes: one CTA per expert and token tile, top-k fused (router_dec_kernel)
-  const int TN = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : 8;
+  // token tiles of at most 4 up to 16 tokens: more, shorter CTAs (batch 16: 102.5 -> 101.5 us)
+  const int TN = N <= 1 ? 1 : N <= 2 ? 2 : N <= 16 ? 4 : 8;
   const dim3 gd(g.E, (N + TN - 1) / TN);
   const size_t sm = (size_t)kRouterWarps * g.E * sizeof(float);
   switch (TN) {
